@@ -1,0 +1,363 @@
+"""Pins of the CPU oracle against facts outside itself.
+
+Each check ties an oracle function to something it does not compute: numpy's
+binary16 conversion, hand-worked fixtures under tests/golden, brute-force
+dequantise-then-dense products in f64 (numpy matmul), exact rational sums,
+closed-form special cases and invariants of the encodings.  A dropped term,
+a wrong sign or index, or a transposed operand in the oracle fails at least
+one of them.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import read_golden
+from q8_quantized_projection_gb300 import synth
+
+QK = 32
+
+
+# ----------------------------------------------------------------- binary16
+
+def test_f16_to_f32_all_patterns(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([orc.f16_to_f32(int(b)) for b in bits], dtype=np.float32)
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite].view(np.uint32), ref[finite].view(np.uint32))
+    assert np.all(np.isnan(got[np.isnan(ref)]))
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+
+
+def test_f32_to_f16_matches_numpy(orc):
+    rng = np.random.default_rng(1)
+    mags = np.exp2(rng.uniform(-30, 17, size=4000)).astype(np.float32)
+    vals = np.concatenate([mags, -mags])
+    # exact midpoints between neighbouring binary16 values (ties to even)
+    h = rng.integers(1, 0x7bff, size=1000, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    mids = ((lo + hi) / 2).astype(np.float32)
+    special = np.array([0.0, -0.0, 65504.0, 65519.996, 65520.0, 65536.0, 1e9,
+                        2.0**-24, 2.0**-25, 2.0**-25 * 3, 2.0**-26, 2.0**-14,
+                        2.0**-14 - 2.0**-25, 6.1e-5, 5.96e-8], dtype=np.float32)
+    vals = np.concatenate([vals, mids[np.isfinite(mids)], special, -special])
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    got = orc.f32_to_f16_array(vals)
+    assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------------------ pack
+
+def test_pack_hand_block(orc):
+    rows = read_golden("pack_block.txt")
+    scale_bits = int(rows[0][0], 16)
+    w = np.array([int(r[0]) * 2.0**-8 for r in rows[1:]], dtype=np.float32)
+    qexp = np.array([int(r[1]) for r in rows[1:]], dtype=np.int8)
+    assert w.size == QK
+    q, s, ov = orc.q8_pack(w.reshape(1, QK))
+    assert ov == 0
+    assert int(s[0, 0]) == scale_bits
+    assert np.array_equal(q[0], qexp)
+
+
+def test_pack_roundtrip_bound_and_idempotence(orc):
+    rng = np.random.default_rng(2)
+    w = synth.f32_weights(rng, 37, 96 * 2)
+    w[3, :QK] = 0.0                       # an all-zero block
+    w[5, QK:2 * QK] *= 1e-6               # scale rounds to binary16 zero
+    w[6, QK:2 * QK] *= 1e-3               # subnormal binary16 scale
+    q, s, ov = orc.q8_pack(w)
+    assert ov == 0
+    sf = s.view(np.float16).astype(np.float32)
+    sfe = np.repeat(sf, QK, axis=1)
+    err = np.abs(w.astype(np.float64) - sfe.astype(np.float64) * q)
+    # normal scales (relative rounding <= 2^-11): |w - s q| <= s/2
+    normal = sfe >= 2.0**-14
+    assert np.all((err <= sfe * 0.5 * (1 + 2.0**-20))[normal])
+    # subnormal scales may clamp: the error is then amax - 127 s at most
+    amax_e = np.repeat(np.abs(w.reshape(37, -1, QK)).max(axis=2), QK, axis=1)
+    sub = (sfe > 0) & ~normal
+    assert sub.any()
+    assert np.all((err <= np.maximum(sfe * 0.5 * (1 + 2.0**-20), amax_e - 127.0 * sfe))[sub])
+    assert s[5, 1] == 0 and np.all(q[5, QK:2 * QK] == 0)
+    assert np.all(q[3, :QK] == 0) and s[3, 0] == 0
+    assert np.all(np.abs(q.astype(np.int32)) <= 127)
+    # the largest |w| of every non-zero block maps to +-127
+    blocks = np.abs(q.reshape(37, -1, QK).astype(np.int32)).max(axis=2)
+    normal_blk = s.view(np.float16).astype(np.float32) >= 2.0**-14
+    assert np.all((blocks == 127)[normal_blk])
+    # pack(dequant(pack(w))) == pack(w)
+    w2 = (sfe * q).astype(np.float32)
+    q2, s2, _ = orc.q8_pack(w2)
+    nb = np.repeat(normal_blk, QK, axis=1)
+    assert np.array_equal(q2[nb], q[nb]) and np.array_equal(s2[normal_blk], s[normal_blk])
+    # the stored scale is the binary16 rounding of amax/127 (numpy's rounding)
+    amax = np.abs(w.reshape(37, -1, QK)).max(axis=2)
+    assert np.array_equal(s, (amax / np.float32(127)).astype(np.float16).view(np.uint16))
+
+
+def test_pack_overflow_counted(orc):
+    w = np.zeros((1, 64), np.float32)
+    w[0, 0] = 65504.0 * 127 * 2     # scale overflows binary16
+    w[0, 40] = 1.0
+    q, s, ov = orc.q8_pack(w)
+    assert ov == 1
+    assert s[0, 0] == 0x7C00 and np.all(q[0, :QK] == 0)
+    assert q[0, 40] == 127
+
+
+# --------------------------------------------------------- activation codes
+
+def test_act_i8_hand_block(orc):
+    rows = read_golden("act_i8_block.txt")
+    d = float(rows[0][0])
+    x = np.array([float(r[0]) for r in rows[1:]], dtype=np.float32)
+    qexp = np.array([int(r[1]) for r in rows[1:]], dtype=np.int8)
+    xq, xd = orc.act_quant_i8(x.reshape(1, QK))
+    assert xd[0, 0] == np.float32(d)
+    assert np.array_equal(xq[0], qexp)
+
+
+def test_act_i8_bound_and_monotone(orc):
+    rng = np.random.default_rng(3)
+    x = synth.activations(rng, 5, 4 * QK)
+    x[1, :QK] = 0.0
+    xq, xd = orc.act_quant_i8(x)
+    de = np.repeat(xd, QK, axis=1).astype(np.float64)
+    err = np.abs(x - de * xq)
+    assert np.all(err <= de * (0.5 + 1e-5))
+    assert np.all(xq[1, :QK] == 0) and xd[1, 0] == 0
+    for m in range(5):
+        for b in range(4):
+            xb, qb = x[m, b * QK:(b + 1) * QK], xq[m, b * QK:(b + 1) * QK]
+            order = np.argsort(xb, kind="stable")
+            assert np.all(np.diff(qb[order].astype(np.int32)) >= 0)
+            if xd[m, b] > 0:
+                assert np.abs(qb.astype(np.int32)).max() == 127
+
+
+def test_i8x2_split_table(orc):
+    table = [(int(a), int(b), int(c)) for a, b, c in read_golden("i8x2_split.txt")]
+    # d = 8191 / 8191 = 1 when the block holds 8191, so each code is its own x.
+    codes = [t[0] for t in table]
+    x = np.zeros(((len(codes) + QK - 2) // (QK - 1)) * QK, np.float32)
+    blocks = x.reshape(-1, QK)
+    where = {}
+    for i, c in enumerate(codes):
+        b, j = divmod(i, QK - 1)
+        blocks[b, 0] = 8191.0
+        blocks[b, j + 1] = c
+        where[c] = (b, j + 1)
+    xh, xl, xd = orc.act_quant_i8x2(x.reshape(1, -1))
+    assert np.all(xd == 1.0)
+    hb, lb = xh.reshape(-1, QK), xl.reshape(-1, QK)
+    for q, hi, lo in table:
+        b, j = where[q]
+        assert (int(hb[b, j]), int(lb[b, j])) == (hi, lo), q
+
+
+def test_i8x2_identity_ranges_bound(orc):
+    rng = np.random.default_rng(4)
+    x = synth.activations(rng, 7, 6 * QK) * np.float32(3.0)
+    x[2, QK:2 * QK] = 0.0
+    xh, xl, xd = orc.act_quant_i8x2(x)
+    Q = 128 * xh.astype(np.int32) + xl.astype(np.int32)
+    assert xh.min() >= -64 and xh.max() <= 64
+    assert xl.min() >= -64 and xl.max() <= 63
+    assert np.abs(Q).max() <= 8191
+    de = np.repeat(xd, QK, axis=1).astype(np.float64)
+    assert np.all(np.abs(x - de * Q) <= de * (0.5 + 1e-3))
+    assert np.all(xl[Q % 128 == 0] == 0)
+    for m in range(7):
+        for b in range(6):
+            xb, qb = x[m, b * QK:(b + 1) * QK], Q[m, b * QK:(b + 1) * QK]
+            order = np.argsort(xb, kind="stable")
+            assert np.all(np.diff(qb[order]) >= 0)
+            if xd[m, b] > 0:
+                assert np.abs(qb).max() == 8191
+
+
+# ----------------------------------------------------------- block dots
+
+@pytest.mark.parametrize("two_word", [False, True])
+def test_block_dots_order_invariance(orc, two_word):
+    rng = np.random.default_rng(5)
+    n, k, rows = 11, 5 * QK, 3
+    q, _ = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, rows, k)
+    if two_word:
+        xh, xl, _ = orc.act_quant_i8x2(x)
+        a = 128 * xh.astype(np.int64) + xl.astype(np.int64)
+        isum = orc.block_dots(q, xh, xl)
+    else:
+        xh, _ = orc.act_quant_i8(x)
+        a = xh.astype(np.int64)
+        isum = orc.block_dots(q, xh)
+    # independent contraction: numpy int64 einsum over (m, n, b, i)
+    ref = np.einsum("nbi,mbi->mnb", q.astype(np.int64).reshape(n, -1, QK), a.reshape(rows, -1, QK))
+    assert np.array_equal(isum.astype(np.int64), ref)
+    # reversed element order within each block gives the same integers
+    rev = np.einsum("nbi,mbi->mnb", q.astype(np.int64).reshape(n, -1, QK)[:, :, ::-1],
+                    a.reshape(rows, -1, QK)[:, :, ::-1])
+    assert np.array_equal(isum.astype(np.int64), rev)
+
+
+# --------------------------------------------------- projections vs brute force
+
+def _dense(q, s):
+    sf = s.view(np.float16).astype(np.float64)
+    return q.astype(np.float64) * np.repeat(sf, QK, axis=1)
+
+
+@pytest.mark.parametrize("n,k,rows", [(1, 32, 1), (3, 64, 2), (5, 96, 3), (4, 160, 1)])
+@pytest.mark.parametrize("mode", ["i8", "i8x2"])
+def test_proj_q_brute_force(orc, n, k, rows, mode):
+    rng = np.random.default_rng(100 + n * 7 + k + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, rows, k)
+    act = orc.quantize(mode, x)
+    y, norm = orc.project(mode, q, s, act)
+    if mode == "i8":
+        xq, xd = act
+        a = xq.astype(np.float64)
+    else:
+        xh, xl, xd = act
+        a = 128.0 * xh.astype(np.float64) + xl.astype(np.float64)
+    xdq = a * np.repeat(xd.astype(np.float64), QK, axis=1)      # dequantised activation
+    ref = xdq @ _dense(q, s).T                                   # [rows, n]
+    assert y.shape == (rows, n)
+    assert np.all(np.abs(y - ref) <= 1e-6 * norm + 1e-30)
+    # the tolerance scale is the sum over blocks of |block dot * scales|
+    wd = _dense(q, s)
+    nref = sum(np.abs(xdq[:, b * QK:(b + 1) * QK] @ wd[:, b * QK:(b + 1) * QK].T)
+               for b in range(k // QK))
+    assert np.allclose(norm, nref, rtol=1e-12, atol=0)
+
+
+@pytest.mark.parametrize("n,k,rows", [(1, 32, 1), (3, 64, 2), (2, 96, 3)])
+def test_proj_f64_exact_rational(orc, n, k, rows):
+    rng = np.random.default_rng(200 + n + k + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, rows, k)
+    y, norm = orc.proj_f64(q, s, x)
+    w = _dense(q, s)
+    for m in range(rows):
+        for j in range(n):
+            exact = sum(Fraction(float(w[j, kk])) * Fraction(float(x[m, kk])) for kk in range(k))
+            nexact = sum(abs(Fraction(float(w[j, kk])) * Fraction(float(x[m, kk]))) for kk in range(k))
+            assert abs(Fraction(float(y[m, j])) - exact) <= Fraction(k) * Fraction(2) ** -53 * nexact
+            assert math.isclose(float(norm[m, j]), float(nexact), rel_tol=1e-12)
+            fs = math.fsum(float(w[j, kk]) * float(x[m, kk]) for kk in range(k))
+            assert abs(y[m, j] - fs) <= k * 2.0**-53 * norm[m, j]
+
+
+def test_one_hot_activation(orc):
+    rng = np.random.default_rng(6)
+    n, k = 9, 4 * QK
+    q, s = synth.q8_weights(rng, n, k)
+    kk, v = 77, np.float32(-1.75)
+    x = np.zeros((1, k), np.float32)
+    x[0, kk] = v
+    sw = s.view(np.float16).astype(np.float32)[:, kk // QK]
+    # f32 activations: exactly S * Q * v
+    y64, _ = orc.proj_f64(q, s, x)
+    assert np.array_equal(y64[0], sw.astype(np.float64) * q[:, kk] * np.float64(v))
+    # one word: code -127, d = 1.75 / 127 (the sign of v is in the code)
+    xq, xd = orc.act_quant_i8(x)
+    assert xq[0, kk] == -127 and np.count_nonzero(xq) == 1
+    yb, _ = orc.proj_q(q, s, xq, None, xd)
+    ref = sw.astype(np.float64) * q[:, kk] * np.float64(v)
+    assert np.all(np.abs(yb[0] - ref) <= 2 * 2.0**-24 * np.abs(ref) + 1e-30)
+    # two words: code -8191
+    xh, xl, xd2 = orc.act_quant_i8x2(x)
+    assert 128 * int(xh[0, kk]) + int(xl[0, kk]) == -8191
+    yc, _ = orc.proj_q(q, s, xh, xl, xd2)
+    assert np.all(np.abs(yc[0] - ref) <= 3 * 2.0**-24 * np.abs(ref) + 1e-30)
+
+
+def test_zero_blocks_and_identity(orc):
+    # identity-like weights: row j has a single 127 at column 32*j with scale 1/127
+    n, k = 4, 4 * QK
+    q = np.zeros((n, k), np.int8)
+    s = np.zeros((n, k // QK), np.uint16)
+    one = np.float16(1.0 / 127).view(np.uint16)
+    for j in range(n):
+        q[j, QK * j] = 127
+        s[j, j] = one
+    x = np.zeros((1, k), np.float32)
+    x[0, ::QK] = np.array([1.0, -2.0, 0.5, 4.0], np.float32)
+    y64, _ = orc.proj_f64(q, s, x)
+    sf = np.float64(np.float32(np.float16(1.0 / 127)))
+    assert np.array_equal(y64[0], sf * 127 * x[0, ::QK].astype(np.float64))
+    xq, xd = orc.act_quant_i8(x)
+    yb, _ = orc.proj_q(q, s, xq, None, xd)
+    assert np.allclose(yb[0], x[0, ::QK], rtol=2e-3)
+    # all-zero activation gives exact zeros in every mode
+    z = np.zeros((2, k), np.float32)
+    for mode in ("f32", "i8", "i8x2"):
+        y, nrm = orc.project(mode, q, s, orc.quantize(mode, z))
+        assert np.all(y == 0) and np.all(nrm == 0)
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_power_of_two_constant(orc):
+    g = synth.gain(np.random.default_rng(7), 96)
+    for c in (0.25, -4.0, 1.0, 2.0**-10):
+        h = np.full((1, 96), c, np.float32)
+        x, r = orc.rmsnorm(h, g, eps=0.0)
+        assert r[0] == 1.0 / abs(c)
+        assert np.array_equal(x[0], np.sign(c).astype(np.float32) * g)
+
+
+def test_rmsnorm_matches_f64_formula(orc):
+    rng = np.random.default_rng(8)
+    h = synth.activations(rng, 6, 4096)
+    g = synth.gain(rng, 4096)
+    x, r = orc.rmsnorm(h, g, eps=1e-5)
+    hd = h.astype(np.float64)
+    ref_r = 1.0 / np.sqrt(np.mean(hd * hd, axis=1) + np.float64(np.float32(1e-5)))
+    assert np.allclose(r, ref_r, rtol=1e-14, atol=0)
+    ref = hd * ref_r[:, None] * g.astype(np.float64)
+    assert np.all(np.abs(x - ref) <= 3 * 2.0**-24 * np.abs(ref))
+    x1, _ = orc.rmsnorm(h, None, eps=1e-5)
+    assert np.all(np.abs(x1 - hd * ref_r[:, None]) <= 2 * 2.0**-24 * np.abs(hd * ref_r[:, None]))
+
+
+# ---------------------------------------------------------------- arg-max
+
+def test_argmax_hand_vectors(orc):
+    cases = [
+        ([1.0, 3.0, 3.0, 2.0], 1),
+        ([-0.0, 0.0], 0),
+        ([0.0, -0.0, 0.0], 0),
+        ([5.0], 0),
+        ([-1.0, -1.0, -1.0], 0),
+        ([-3.0, -2.0, -2.5], 1),
+        ([1.0, 2.0, 4.0, 4.0, 8.0], 4),
+        ([np.float32(1.0) + np.float32(2**-23), 1.0], 0),
+    ]
+    for vals, want in cases:
+        for dt in (np.float32, np.float64):
+            tok, best = orc.argmax(np.array([vals], dt))
+            assert tok[0] == want, (vals, dt)
+            assert best[0] == max(vals)
+
+
+def test_planted_head_margin(orc):
+    rng = np.random.default_rng(9)
+    n, k, rows = 3000, 256, 16
+    q, s = synth.q8_weights(rng, n, k)
+    h = synth.head_activations(rng, rows, k)
+    pos = synth.planted_positions(rng, n)
+    synth.plant_head_rows(q, s, h, pos)
+    x, _ = orc.rmsnorm(h)
+    for mode in ("f32", "i8"):
+        tok, best, y = orc.head_argmax(mode, q, s, orc.quantize(mode, x))
+        assert np.array_equal(tok, pos[np.arange(rows) % 8])
+        top2 = np.sort(y, axis=1)[:, -2]
+        assert np.all(best - top2 > 0.5 * best)
