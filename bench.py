@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q8_0 quantized projection on GB300.
+
+Default workload: the decode-step projections of a d = 4096 Llama-shaped
+layer at rows = 1 -- Wqkv 6144x4096, Wo 4096x4096, fused gate+up 28672x4096,
+down 4096x14336, all Q8_0 -- each fed by its producer (RMSNorm of an N(0,1)
+hidden vector, quantized in the producer's epilogue), in all three activation
+modes (two-word ~14-bit, one int8 word, f32 with f64 sums).  One step runs the
+12 fused producer+projection calls.  Two rotating copies of the weights
+(463 MB) keep every step's reads larger than the 129 MB L2.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Prints one JSON line on rank 0.  Under torchrun (N > 1) every rank runs its own
+replica (the projection has no exchange step on one node here), the time is
+the maximum over ranks and `value` sums the ranks' bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from q8_quantized_projection_gb300 import synth  # noqa: E402
+
+METRIC = "Q8_0 proj weight GB/s (% of GB300 HBM peak) at rows 1–256; rows/s"
+MODES = ("i8x2", "i8", "f32")
+WORKLOAD = "decode_layer_d4096_rows1"
+COPIES = 2
+QK = 32
+
+
+def weight_bytes(n, k):
+    return n * k + n * (k // QK) * 2     # 34 bytes per 32 weights
+
+
+LAYER_BYTES = sum(weight_bytes(n, k) for _, n, k in synth.LAYER_D4096)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- distributed
+
+def dist_init():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- inputs
+
+def make_host_inputs(seed=0):
+    rng = synth.rng_for(seed)
+    mats, hs = [], []
+    for name, n, k in synth.LAYER_D4096:
+        q, s = synth.q8_weights(rng, n, k)
+        mats.append((name, q, s))
+        hs.append(synth.activations(rng, 1, k))
+    return mats, hs
+
+
+# ------------------------------------------------------------- oracle arm
+
+def oracle_step(mats, hs, modes=MODES):
+    """One step of the workload on the CPU oracle: producer then projection."""
+    from oracle import oracle as orc
+    for mode in modes:
+        for (_, q, s), h in zip(mats, hs):
+            x, _ = orc.rmsnorm(h)
+            orc.project(mode, q, s, orc.quantize(mode, x))
+
+
+def cpu_baseline(mats, hs, budget_s=10.0):
+    from oracle import oracle as orc
+    orc.build()
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        oracle_step(mats, hs)
+        steps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(steps * len(MODES) * LAYER_BYTES / dt / 1e9, 4), "unit": "GB/s",
+            "cores": orc.threads(), "kind": "oracle",
+            "sample": f"{steps} full step(s) of {WORKLOAD} (3 modes x 4 projections, RMSNorm + "
+                      f"quantize + projection) in {dt:.1f} s; plain C oracle, OpenMP over "
+                      f"output rows"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+    orc.build()
+    mats, hs = make_host_inputs()
+    for _ in range(args.warmup):
+        oracle_step(mats, hs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(mats, hs)
+    dt = time.perf_counter() - t0
+    ms = dt / args.steps * 1e3
+    value = len(MODES) * LAYER_BYTES / (ms * 1e-3) / 1e9
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "int8/f32/f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "rows": 1, "modes": list(MODES),
+                      "matrices": [f"{n}x{k}" for _, n, k in synth.LAYER_D4096]},
+           "rows_per_s": round(len(MODES) * 4 / (ms * 1e-3), 2),
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": orc.threads(),
+                            "kind": "oracle",
+                            "sample": f"the whole step, {args.steps} timed steps"},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# --------------------------------------------------------------- our arm
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "q8_quantized_projection_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it is current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e.get("bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from q8_quantized_projection_gb300 import build, native
+    if rank == 0:
+        build.build()
+    barrier(world)
+    native.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    mats, hs = make_host_inputs()
+    Q = [[], []]
+    S = [[], []]
+    for _, q, s in mats:
+        qd = torch.from_numpy(q).to(dev)
+        sd = torch.from_numpy(s.view(np.int16)).to(dev)
+        Q[0].append(qd)
+        S[0].append(sd)
+        for c in range(1, COPIES):
+            Q[c].append(qd.clone())
+            S[c].append(sd.clone())
+    H = [torch.from_numpy(h).to(dev) for h in hs]
+    Y = {m: [torch.empty((1, n), dtype=torch.float32, device=dev) for _, n, _ in synth.LAYER_D4096]
+         for m in MODES}
+    WS = {m: [torch.empty(native.q8_proj_fused_workspace(m, 1, k), dtype=torch.uint8, device=dev)
+              for _, _, k in synth.LAYER_D4096] for m in MODES}
+    launches_per_fused = 2
+
+    def step(i, modes=MODES):
+        c = i % COPIES
+        for m in modes:
+            for p in range(4):
+                native.q8_proj_fused(m, Q[c][p], S[c][p], H[p], Y[m][p], WS[m][p])
+
+    def timed(nsteps, modes=MODES):
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(nsteps):
+            step(i, modes)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return e0.elapsed_time(e1) / nsteps
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ms = timed(args.steps)
+    # keep the same load running so the clock samples cover it
+    t_hold = time.perf_counter()
+    while time.perf_counter() - t_hold < 1.0:
+        for i in range(50):
+            step(i)
+        torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(world, ms)
+    step_bytes = len(MODES) * LAYER_BYTES
+    value = world * step_bytes / (ms * 1e-3) / 1e9
+
+    # per-mode breakdown (same protocol)
+    per_mode = {}
+    for m in MODES:
+        for i in range(args.warmup):
+            step(i, (m,))
+        mms = max_over_ranks(world, timed(args.steps, (m,)))
+        per_mode[m] = {"ms_per_step": round(mms, 5),
+                       "GB/s": round(LAYER_BYTES / (mms * 1e-3) / 1e9, 2)}
+
+    # dominant kernel: the GEMV, timed alone per mode (back-to-back launches, rotating copies)
+    gemv = {}
+    peak, peak_kind = load_peaks()
+    for m in MODES:
+        xq, xd = {}, {}
+        for p, (_, n, k) in enumerate(synth.LAYER_D4096):
+            xq[p], xd[p] = native.activation_buffers(m, 1, k, device=dev)
+            native.act_quant(m, H[p], xq[p], xd[p], norm=True)
+        reps = max(args.steps, 20)
+        for i in range(3):
+            for p in range(4):
+                native.q8_proj(m, Q[i % COPIES][p], S[i % COPIES][p], xq[p], xd[p], 1, Y[m][p])
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            for p in range(4):
+                native.q8_proj(m, Q[i % COPIES][p], S[i % COPIES][p], xq[p], xd[p], 1, Y[m][p])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per_launch_ms = e0.elapsed_time(e1) / (reps * 4)
+        act_b = {"f32": 4, "i8": 1 + 4 / QK, "i8x2": 2 + 4 / QK}[m]
+        alg = sum(weight_bytes(n, k) + k * act_b + n * 4 for _, n, k in synth.LAYER_D4096) / 4
+        gemv[m] = {"per_launch_ms": per_launch_ms, "alg_bytes_per_launch": alg,
+                   "GB/s": alg / (per_launch_ms * 1e-3) / 1e9}
+    dom = max(MODES, key=lambda m: gemv[m]["per_launch_ms"])
+    achieved = gemv[dom]["GB/s"]
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": committed_traffic(f"gemv_{dom}"),
+                "kernel": f"gemv_kernel<{dom}>", "peak_source": peak_kind,
+                "per_mode_GBps": {m: round(gemv[m]["GB/s"], 2) for m in MODES},
+                "note": "GEMV timed alone: 4 projections back to back, rotating weight copies; "
+                        "algorithmic bytes = 34/32 B per weight + activation + output"}
+
+    # end to end through the C ABI: pinned host inputs in, outputs back, every step
+    h_host = [torch.from_numpy(h).pin_memory() for h in hs]
+    y_host = {m: [torch.empty((1, n), dtype=torch.float32).pin_memory()
+                  for _, n, _ in synth.LAYER_D4096] for m in MODES}
+    h2d = sum(h.numel() * 4 for h in h_host)
+    d2h = sum(y.numel() * 4 for m in MODES for y in y_host[m])
+
+    def e2e_step(i):
+        for p in range(4):
+            H[p].copy_(h_host[p], non_blocking=True)
+        step(i)
+        for m in MODES:
+            for p in range(4):
+                y_host[m][p].copy_(Y[m][p], non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    e2e_ms = max_over_ranks(world, (time.perf_counter() - t0) / args.steps * 1e3)
+    e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(mats, hs, budget_s=args.cpu_budget)
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "int8/f32", "data": "synthetic",
+               "config": {"workload": WORKLOAD, "rows": 1, "modes": list(MODES),
+                          "matrices": [f"{nm} {n}x{k}" for nm, n, k in synth.LAYER_D4096],
+                          "producer": "RMSNorm(N(0,1)) quantized in the producer (fused call)",
+                          "l2": f"inputs larger than L2: {COPIES} rotating weight copies, "
+                                f"{COPIES * LAYER_BYTES / 1e6:.0f} MB",
+                          "parallelism": "replicas" if world > 1 else "single GPU"},
+               "pct_hbm_peak": round(100 * value / world / peak, 2),
+               "rows_per_s": round(world * len(MODES) * 4 / (ms * 1e-3), 1),
+               "modes": per_mode, "roofline": roofline, "cpu_baseline": base, "e2e": e2e,
+               "gpu_launches": args.steps * len(MODES) * 4 * launches_per_fused,
+               "clocks": clocks}
+        print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

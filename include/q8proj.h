@@ -1,0 +1,195 @@
+/*
+ * q8proj.h -- C ABI of the Q8_0 quantized-projection library (libq8proj.so),
+ * written for one NVIDIA GB300 (sm_103a).
+ *
+ * What it computes.  The compiled generation lane of logicaffeine_compile
+ * (codegen_cuda::lane, module description) reads every quantized projection
+ * "as rows read in place from the checkpoint", stored as a Q8_0 pair of files
+ * <var>.q / <var>.s (model::author, module description: "Q8_0 quants and
+ * block scales").  Its CudaKnobs pick the projection numerics: f32
+ * activations with f64 sums, a two-word ~14-bit int8 activation (the
+ * default), or llama.cpp's one int8 word; fuse_quant quantizes the
+ * activation in its producer.  A step has rows = 1 (decode), rows = B (a
+ * batch, every weight read once for all sequences) or T rows (a prefill
+ * chunk, every projection reading its weights once for the block), and ends
+ * with the arg-max of the logits (model::author, decode_step / decode_head).
+ *
+ * Layouts (all row-major, planar, dense pitch):
+ *   Q   int8   [N][K]      weight quants, the ".q" file
+ *   S   uint16 [N][K/32]   binary16 bit patterns of the block scales, ".s"
+ *   activations, by mode:
+ *     Q8_ACT_F32   float  [rows][K]                    (xd unused, may be NULL)
+ *     Q8_ACT_I8    int8   [rows][K]  + xd float [rows][K/32]
+ *     Q8_ACT_I8X2  int8   [2][rows][K] (hi plane, then lo plane)
+ *                                     + xd float [rows][K/32]
+ *   outputs: float [rows][N], or double [rows][N] for Q8_ACT_F32 with out_f64.
+ *
+ * Numerics (the pages name these modes but give no formulas; the readings):
+ *   block of 32 values along K; weight scale s = binary16(amax/127) and
+ *   q = round_half_away(w / s) in [-127, 127];
+ *   one-word activation: d = amax/127 (f32), q = round_half_away(x/d);
+ *   two-word activation: d = amax/8191 (f32), Q = round_half_away(x/d) in
+ *   [-8191, 8191], lo = ((Q + 64) mod 128) - 64, hi = (Q - lo) / 128;
+ *   projection (one/two-word): y = sum_b float(isum_b) * (s_b * d_b), where
+ *   isum_b is the exact int32 dot of block b (two-word: 128*dot(hi)+dot(lo));
+ *   projection (f32): y = sum_k (s_b * q_k) * x_k, summed to f64 accuracy;
+ *   RMSNorm producer: r = 1/sqrt(sum h^2 / K + eps) with the sum in f64,
+ *   x = (h * float(r)) * g.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers owned by the caller unless stated.  The
+ *     library allocates no device memory; scratch comes from caller-sized
+ *     workspaces.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Argument errors are found on the host and returned
+ *     before anything is launched.
+ *   - Every pointer must be 16-byte aligned; K must be a multiple of 32;
+ *     N, rows >= 1.  Violations return Q8_ERR_ALIGN / Q8_ERR_SHAPE.
+ *   - A failed launch returns Q8_ERR_CUDA; q8_last_cuda_error() gives the
+ *     CUDA error number.  The library never exits, aborts or traps.
+ *   - Device-side waits are bounded.  A wait that runs out records a code
+ *     that q8_device_error() reports; the kernel then returns early and its
+ *     outputs are undefined.
+ *   - By default consecutive launches use programmatic dependent launch: a
+ *     projection may start streaming its WEIGHTS before the preceding kernel
+ *     on the stream has finished (activations, outputs and workspaces are
+ *     only touched after it has).  So the kernel launched just before a
+ *     projection must not write that projection's Q or S; synchronise the
+ *     stream (or q8_set_pdl(0)) after writing weights.
+ */
+#ifndef Q8PROJ_H
+#define Q8PROJ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    Q8_OK = 0,
+    Q8_ERR_ARG = 1,          /* null pointer, bad flag or bad value */
+    Q8_ERR_SHAPE = 2,        /* K % 32 != 0, N or rows out of range */
+    Q8_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned */
+    Q8_ERR_MODE = 4,         /* activation mode not valid for this call */
+    Q8_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+    Q8_ERR_UNSUPPORTED = 6,  /* valid request this build does not serve */
+    Q8_ERR_WORKSPACE = 7     /* workspace missing or too small */
+} q8_status;
+
+typedef enum {
+    Q8_ACT_F32 = 0,   /* f32 activations, f64 sums */
+    Q8_ACT_I8 = 1,    /* one int8 word per value (llama.cpp style) */
+    Q8_ACT_I8X2 = 2   /* two-word ~14-bit int8 code (the lane's default) */
+} q8_act_mode;
+
+/* Largest activation row count one call accepts (decode batch or prefill chunk). */
+#define Q8_MAX_ROWS 256
+
+/* Name of a status code; never NULL. */
+const char* q8_status_str(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int q8_version(void);
+
+/* The CUDA error number behind the last Q8_ERR_CUDA returned on this thread. */
+int q8_last_cuda_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device: 0 = none, 1 = a bounded wait ran out.  *code receives it.
+ */
+q8_status q8_device_error(int32_t* code /* host */, void* stream);
+
+/* Programmatic dependent launch on (1, default) or off (0) for this process. */
+void q8_set_pdl(int enable);
+
+/*
+ * Q8_0 pack (model::author, module description: <var>.q / <var>.s).
+ *   w  float [N][K] -> q int8 [N][K], s uint16 [N][K/32] (binary16 bits).
+ * Per 32-value block: s = binary16(amax/127), q = round_half_away(w/s)
+ * clamped to [-127, 127] (q = 0 where s == 0).  overflow (device int32,
+ * nullable) is incremented by the number of blocks whose scale overflowed
+ * binary16 (their q are 0); the caller zeroes it.
+ */
+q8_status q8_pack(const float* w, int64_t N, int64_t K, int8_t* q, uint16_t* s,
+                  int32_t* overflow, void* stream);
+
+/*
+ * Activation producer (codegen_cuda::lane, CudaKnobs fuse_quant; "Modules:
+ * kernels", an activation quantized in a producer's epilogue, a norm).
+ *   h     float [rows][K] hidden state
+ *   norm  0: quantize h as given; 1: RMSNorm first, x = (h * r) * gain
+ *   gain  float [K] or NULL (gain of one); eps the RMSNorm epsilon
+ *   xq    output in the mode's activation layout (see top of file)
+ *   xd    float [rows][K/32] block scales (ignored for Q8_ACT_F32)
+ * rows <= Q8_MAX_ROWS.
+ */
+q8_status act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
+                    const float* gain, float eps, void* xq, float* xd, void* stream);
+
+/*
+ * Quantized projection of a stacked activation (codegen_cuda::lane: the
+ * decode step, rows = 1, and a batch's step, rows = B, as one launch with
+ * every weight read once for all rows).
+ *   y[m][n] for m < rows, n < N; y is float, or double when mode is
+ *   Q8_ACT_F32 and out_f64 != 0.  1 <= rows <= Q8_MAX_ROWS.
+ */
+q8_status q8_proj(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                  const void* xq, const float* xd, int64_t rows, void* y, int out_f64,
+                  void* stream);
+
+/*
+ * Prefill-chunk projection (codegen_cuda::lane: author::prefill's chunks of
+ * 2, 4, ... rows, every projection reading its weights once for the block).
+ * Same contract as q8_proj with rows = T (1 <= T <= Q8_MAX_ROWS) and a float
+ * output; large chunks run on the tensor cores.
+ */
+q8_status q8_proj_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                        const void* xq, const float* xd, int64_t T, float* y, void* stream);
+
+/*
+ * Producer fused with the projection (CudaKnobs fuse_quant): RMSNorm of h
+ * (gain nullable) quantized in the producer's epilogue, then the projection.
+ * workspace holds the quantized activation; its size is
+ * q8_proj_fused_workspace(mode, rows, K) bytes, 16-byte aligned.
+ */
+q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                        const float* h, int64_t rows, const float* gain, float eps, void* y,
+                        int out_f64, void* workspace, size_t ws_bytes, void* stream);
+size_t q8_proj_fused_workspace(int mode, int64_t rows, int64_t K);
+
+/*
+ * LM head fused with its arg-max (model::author, decode_head: "the final
+ * norm, the LM head and the arg-max"; decode_batch_head: one token per
+ * sequence).  Modes Q8_ACT_F32 (logits to f64 accuracy) and Q8_ACT_I8 /
+ * Q8_ACT_I8X2 (f32 logits).
+ *   tok     int32 [rows]: the smallest n holding the row's maximum logit
+ *   maxval  double [rows] or NULL: that maximum
+ *   logits  float [rows][N] (double for Q8_ACT_F32) or NULL
+ *   workspace: head_argmax_workspace(rows) bytes.  Its first 16 bytes must
+ *   be zero before the first call on it; every completed call leaves them
+ *   zero again.  Calls sharing a workspace must not overlap.
+ */
+q8_status head_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                      const void* xq, const float* xd, int64_t rows, int32_t* tok,
+                      double* maxval, void* logits, void* workspace, size_t ws_bytes,
+                      void* stream);
+size_t head_argmax_workspace(int64_t rows);
+
+/*
+ * Debug: the per-block int32 dot products the projections fold with their
+ * scales (modes Q8_ACT_I8 / Q8_ACT_I8X2), isum int32 [rows][N][K/32].
+ * path 0 runs the CUDA-core inner product the GEMV kernels use, path 1 the
+ * tensor-core chunk kernel's per-block accumulators.  Small shapes only:
+ * rows * N * K/32 <= 2^26.
+ */
+q8_status q8_debug_block_dots(int mode, const int8_t* q, const void* xq, int64_t N, int64_t K,
+                              int64_t rows, int32_t* isum, int path, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q8PROJ_H */

@@ -1,0 +1,289 @@
+// api.cu -- the C ABI of libq8proj (declared in include/q8proj.h): argument
+// validation on the host, then launches of the kernels on the caller's stream.
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+#include "q8proj.h"
+
+namespace q8 {
+cudaError_t launch_gemv_mode0(const GemvArgs& a, const LaunchCtx& ctx);
+cudaError_t launch_gemv_mode1(const GemvArgs& a, const LaunchCtx& ctx);
+cudaError_t launch_gemv_mode2(const GemvArgs& a, const LaunchCtx& ctx);
+}  // namespace q8
+
+using namespace q8;
+
+// Device error word: bounded waits that run out record a code here.
+__device__ int g_q8_dev_err;
+
+namespace {
+
+thread_local int t_last_cuda = 0;
+int g_pdl = 1;
+
+struct DevInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int* dev_err = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+q8_status cuda_fail(cudaError_t e) {
+    t_last_cuda = int(e);
+    return Q8_ERR_CUDA;
+}
+
+q8_status make_ctx(void* stream, LaunchCtx& ctx) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return Q8_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_q8_dev_err);
+        if (e != cudaSuccess) return cuda_fail(e);
+        d.dev_err = static_cast<int*>(p);
+        d.ready = true;
+    }
+    ctx.stream = static_cast<cudaStream_t>(stream);
+    ctx.pdl = g_pdl != 0;
+    ctx.num_sms = d.num_sms;
+    ctx.dev_err = d.dev_err;
+    return Q8_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+q8_status launched(cudaError_t e) { return e == cudaSuccess ? Q8_OK : cuda_fail(e); }
+
+bool valid_mode(int mode) { return mode >= Q8_ACT_F32 && mode <= Q8_ACT_I8X2; }
+
+q8_status check_shape(int64_t N, int64_t K) {
+    if (N < 1 || K < Q8_QK || K % Q8_QK != 0) return Q8_ERR_SHAPE;
+    if (N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 24)) return Q8_ERR_SHAPE;
+    return Q8_OK;
+}
+
+size_t act_bytes(int mode, int64_t rows, int64_t K) {
+    if (mode == Q8_ACT_F32) return size_t(rows) * K * 4;
+    if (mode == Q8_ACT_I8) return size_t(rows) * K;
+    return size_t(2) * rows * K;
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+cudaError_t gemv_dispatch(const GemvArgs& a, const LaunchCtx& ctx) {
+    if (a.mode == Q8_ACT_F32) return launch_gemv_mode0(a, ctx);
+    if (a.mode == Q8_ACT_I8) return launch_gemv_mode1(a, ctx);
+    return launch_gemv_mode2(a, ctx);
+}
+
+// Runs the CUDA-core projection over groups of at most 16 activation rows.
+q8_status run_projection(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                         const void* xq, const float* xd, int64_t rows, void* y, int out_f64,
+                         int32_t* tok, double* maxval, void* ws, const LaunchCtx& ctx) {
+    const int64_t nb = K / Q8_QK;
+    const int group = gemv_max_rows(mode);
+    const size_t elem = (mode == Q8_ACT_F32) ? 4 : 1;
+    const size_t ysz = (mode == Q8_ACT_F32 && out_f64) ? 8 : 4;
+    for (int64_t g0 = 0; g0 < rows; g0 += group) {
+        GemvArgs a{};
+        a.mode = mode;
+        a.q = q;
+        a.s = s;
+        a.N = N;
+        a.K = K;
+        a.act = static_cast<const unsigned char*>(xq) + size_t(g0) * K * elem;
+        a.xd = xd ? xd + g0 * nb : nullptr;
+        a.plane = rows * K;
+        a.rows = int(rows - g0 < group ? rows - g0 : group);
+        a.y = y ? static_cast<unsigned char*>(y) + size_t(g0) * N * ysz : nullptr;
+        a.out_f64 = out_f64;
+        a.tok = tok ? tok + g0 : nullptr;
+        a.maxval = maxval ? maxval + g0 : nullptr;
+        a.ws = ws;
+        cudaError_t e = gemv_dispatch(a, ctx);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return Q8_OK;
+}
+
+q8_status check_proj_args(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                          const void* xq, const float* xd, int64_t rows, const void* y) {
+    if (!valid_mode(mode)) return Q8_ERR_MODE;
+    if (!q || !s || !xq || !y || (mode != Q8_ACT_F32 && !xd)) return Q8_ERR_ARG;
+    q8_status st = check_shape(N, K);
+    if (st != Q8_OK) return st;
+    if (rows < 1 || rows > Q8_MAX_ROWS) return Q8_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(s) || !aligned16(xq) || !aligned16(y) ||
+        (xd && !aligned16(xd)))
+        return Q8_ERR_ALIGN;
+    return Q8_OK;
+}
+
+}  // namespace
+
+namespace q8 {
+int gemv_max_rows(int) { return 16; }
+}  // namespace q8
+
+extern "C" {
+
+const char* q8_status_str(int status) {
+    switch (status) {
+        case Q8_OK: return "Q8_OK";
+        case Q8_ERR_ARG: return "Q8_ERR_ARG";
+        case Q8_ERR_SHAPE: return "Q8_ERR_SHAPE";
+        case Q8_ERR_ALIGN: return "Q8_ERR_ALIGN";
+        case Q8_ERR_MODE: return "Q8_ERR_MODE";
+        case Q8_ERR_CUDA: return "Q8_ERR_CUDA";
+        case Q8_ERR_UNSUPPORTED: return "Q8_ERR_UNSUPPORTED";
+        case Q8_ERR_WORKSPACE: return "Q8_ERR_WORKSPACE";
+        default: return "Q8_ERR_UNKNOWN";
+    }
+}
+
+int q8_version(void) { return 100; }
+
+int q8_last_cuda_error(void) { return t_last_cuda; }
+
+void q8_set_pdl(int enable) { g_pdl = enable ? 1 : 0; }
+
+q8_status q8_device_error(int32_t* code, void* stream) {
+    if (!code) return Q8_ERR_ARG;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_q8_dev_err, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_q8_dev_err, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    *code = v;
+    return Q8_OK;
+}
+
+q8_status q8_pack(const float* w, int64_t N, int64_t K, int8_t* q, uint16_t* s,
+                  int32_t* overflow, void* stream) {
+    if (!w || !q || !s) return Q8_ERR_ARG;
+    q8_status st = check_shape(N, K);
+    if (st != Q8_OK) return st;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(s) || (overflow && !aligned16(overflow)))
+        return Q8_ERR_ALIGN;
+    LaunchCtx ctx;
+    if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
+    return launched(launch_pack(w, N, K, q, s, overflow, ctx));
+}
+
+q8_status act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
+                    const float* gain, float eps, void* xq, float* xd, void* stream) {
+    if (!valid_mode(mode)) return Q8_ERR_MODE;
+    if (!h || !xq || (mode != Q8_ACT_F32 && !xd)) return Q8_ERR_ARG;
+    if (norm != 0 && norm != 1) return Q8_ERR_ARG;
+    if (!(eps >= 0.0f)) return Q8_ERR_ARG;
+    q8_status st = check_shape(1, K);
+    if (st != Q8_OK) return st;
+    if (rows < 1 || rows > Q8_MAX_ROWS) return Q8_ERR_SHAPE;
+    if (!aligned16(h) || !aligned16(xq) || (xd && !aligned16(xd)) || (gain && !aligned16(gain)))
+        return Q8_ERR_ALIGN;
+    LaunchCtx ctx;
+    if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
+    return launched(launch_act_quant(mode, h, rows, K, norm, gain, eps, xq, xd, ctx));
+}
+
+q8_status q8_proj(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                  const void* xq, const float* xd, int64_t rows, void* y, int out_f64,
+                  void* stream) {
+    q8_status st = check_proj_args(mode, q, s, N, K, xq, xd, rows, y);
+    if (st != Q8_OK) return st;
+    if (out_f64 && mode != Q8_ACT_F32) return Q8_ERR_MODE;
+    LaunchCtx ctx;
+    if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
+    return run_projection(mode, q, s, N, K, xq, xd, rows, y, out_f64 ? 1 : 0, nullptr, nullptr,
+                          nullptr, ctx);
+}
+
+q8_status q8_proj_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                        const void* xq, const float* xd, int64_t T, float* y, void* stream) {
+    q8_status st = check_proj_args(mode, q, s, N, K, xq, xd, T, y);
+    if (st != Q8_OK) return st;
+    LaunchCtx ctx;
+    if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
+    return run_projection(mode, q, s, N, K, xq, xd, T, y, 0, nullptr, nullptr, nullptr, ctx);
+}
+
+size_t q8_proj_fused_workspace(int mode, int64_t rows, int64_t K) {
+    if (!valid_mode(mode) || rows < 1 || K < Q8_QK) return 0;
+    return round_up(act_bytes(mode, rows, K), 256) + round_up(size_t(rows) * (K / Q8_QK) * 4, 256);
+}
+
+q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                        const float* h, int64_t rows, const float* gain, float eps, void* y,
+                        int out_f64, void* workspace, size_t ws_bytes, void* stream) {
+    if (!workspace) return Q8_ERR_WORKSPACE;
+    q8_status st = check_proj_args(mode, q, s, N, K, h, reinterpret_cast<const float*>(h), rows, y);
+    if (st != Q8_OK) return st;
+    if (out_f64 && mode != Q8_ACT_F32) return Q8_ERR_MODE;
+    if (gain && !aligned16(gain)) return Q8_ERR_ALIGN;
+    if (!(eps >= 0.0f)) return Q8_ERR_ARG;
+    if (!aligned16(workspace)) return Q8_ERR_ALIGN;
+    if (ws_bytes < q8_proj_fused_workspace(mode, rows, K)) return Q8_ERR_WORKSPACE;
+    LaunchCtx ctx;
+    if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
+    unsigned char* act = static_cast<unsigned char*>(workspace);
+    float* xd = reinterpret_cast<float*>(act + round_up(act_bytes(mode, rows, K), 256));
+    cudaError_t e = launch_act_quant(mode, h, rows, K, 1, gain, eps, act, xd, ctx);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return run_projection(mode, q, s, N, K, act, mode == Q8_ACT_F32 ? nullptr : xd, rows, y,
+                          out_f64 ? 1 : 0, nullptr, nullptr, nullptr, ctx);
+}
+
+size_t head_argmax_workspace(int64_t rows) {
+    if (rows < 1) return 0;
+    const int64_t g = rows < 16 ? rows : 16;
+    return kArgmaxHeader + size_t(kMaxGrid) * size_t(g) * sizeof(ArgmaxCand);
+}
+
+q8_status head_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                      const void* xq, const float* xd, int64_t rows, int32_t* tok,
+                      double* maxval, void* logits, void* workspace, size_t ws_bytes,
+                      void* stream) {
+    if (!valid_mode(mode)) return Q8_ERR_MODE;
+    if (!q || !s || !xq || !tok || (mode != Q8_ACT_F32 && !xd)) return Q8_ERR_ARG;
+    q8_status st = check_shape(N, K);
+    if (st != Q8_OK) return st;
+    if (rows < 1 || rows > Q8_MAX_ROWS) return Q8_ERR_SHAPE;
+    if (!workspace || ws_bytes < head_argmax_workspace(rows)) return Q8_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(s) || !aligned16(xq) || (xd && !aligned16(xd)) ||
+        !aligned16(workspace) || (logits && !aligned16(logits)) ||
+        (reinterpret_cast<uintptr_t>(tok) & 3u) || (reinterpret_cast<uintptr_t>(maxval) & 7u))
+        return Q8_ERR_ALIGN;
+    LaunchCtx ctx;
+    if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
+    return run_projection(mode, q, s, N, K, xq, xd, rows, logits, mode == Q8_ACT_F32 ? 1 : 0, tok,
+                          maxval, workspace, ctx);
+}
+
+q8_status q8_debug_block_dots(int mode, const int8_t* q, const void* xq, int64_t N, int64_t K,
+                              int64_t rows, int32_t* isum, int path, void* stream) {
+    if (mode != Q8_ACT_I8 && mode != Q8_ACT_I8X2) return Q8_ERR_MODE;
+    if (!q || !xq || !isum) return Q8_ERR_ARG;
+    q8_status st = check_shape(N, K);
+    if (st != Q8_OK) return st;
+    if (rows < 1 || rows > Q8_MAX_ROWS) return Q8_ERR_SHAPE;
+    if (rows * N * (K / Q8_QK) > (int64_t(1) << 26)) return Q8_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(xq) || !aligned16(isum)) return Q8_ERR_ALIGN;
+    if (path != 0) return Q8_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
+    return launched(launch_debug_dots(mode, q, xq, N, K, rows, isum, ctx));
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// launch.h -- host-side launch interface between the C ABI (api.cu) and the
+// kernel translation units.  Internal to libq8proj.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace q8 {
+
+struct LaunchCtx {
+    cudaStream_t stream;
+    bool pdl;        // programmatic dependent launch
+    int num_sms;     // SMs of the current device
+    int* dev_err;    // device error word of the current device
+};
+
+// Fills `attrs` with the PDL attribute when enabled; returns the count.
+int pdl_attrs(const LaunchCtx& ctx, cudaLaunchAttribute* attrs);
+
+cudaError_t launch_pack(const float* w, int64_t N, int64_t K, int8_t* q, uint16_t* s,
+                        int32_t* overflow, const LaunchCtx& ctx);
+
+cudaError_t launch_act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
+                             const float* gain, float eps, void* xq, float* xd,
+                             const LaunchCtx& ctx);
+
+// One CUDA-core GEMV launch over a group of at most `gemv_max_rows(mode)`
+// activation rows.
+struct GemvArgs {
+    int mode;
+    const int8_t* q;
+    const uint16_t* s;
+    int64_t N, K;
+    const void* act;    // activation of the group's first row (mode layout)
+    const float* xd;    // block scales of the group's first row
+    int64_t plane;      // elements between the hi and lo planes (two-word mode)
+    int rows;           // rows in the group
+    void* y;            // output of the group's first row (row stride N), may be NULL
+    int out_f64;
+    // arg-max epilogue (head): all NULL for a plain projection
+    int32_t* tok;
+    double* maxval;
+    void* ws;
+};
+
+int gemv_max_rows(int mode);
+cudaError_t launch_gemv(const GemvArgs& a, const LaunchCtx& ctx);
+
+cudaError_t launch_debug_dots(int mode, const int8_t* q, const void* xq, int64_t N, int64_t K,
+                              int64_t rows, int32_t* isum, const LaunchCtx& ctx);
+
+// Workspace layout of the arg-max epilogue: a ticket counter, then one
+// (value, index) candidate per CTA and row.
+constexpr size_t kArgmaxHeader = 256;
+constexpr int kMaxGrid = 1024;
+struct ArgmaxCand {
+    double v;
+    long long i;
+};
+
+}  // namespace q8

@@ -1,0 +1,264 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.  Integers (codes, block dots, tokens) must match exactly;
+floats within the norm-relative tolerances of gpu_util."""
+import numpy as np
+import pytest
+
+from oracle import oracle as orc
+from q8_quantized_projection_gb300 import build, native, synth
+from gpu_util import (QK, act_to_numpy, check_close, dev, host, no_device_error, torch,
+                      upload_act, upload_weights)
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["f32", "i8", "i8x2"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    t = torch()
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    orc.build()
+    native.load()
+    yield
+    no_device_error()
+
+
+# ------------------------------------------------------------------- pack
+
+@pytest.mark.parametrize("n,k", [(1, 32), (37, 96), (300, 4096), (5, 14336)])
+def test_pack_bit_exact(n, k):
+    rng = np.random.default_rng(10 + n + k)
+    w = synth.f32_weights(rng, n, k)
+    w[0, :QK] = 0.0
+    if n > 3:
+        w[1, QK:2 * QK] *= 1e-6
+        w[2, :QK] *= 1e-3
+        w[3, 0] = 65504.0 * 127 * 4      # overflowing scale
+    q_o, s_o, ov_o = orc.q8_pack(w)
+    t = torch()
+    q = t.empty((n, k), dtype=t.int8, device="cuda")
+    s = t.empty((n, k // QK), dtype=t.int16, device="cuda")
+    ov = t.zeros(1, dtype=t.int32, device="cuda")
+    native.q8_pack(dev(w), q, s, ov)
+    assert np.array_equal(host(q), q_o)
+    assert np.array_equal(host(s).view(np.uint16), s_o)
+    assert int(host(ov)[0]) == ov_o
+
+
+# ------------------------------------------------------------- producer
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("rows,k", [(1, 32), (3, 96), (1, 4096), (17, 4096), (2, 14336),
+                                    (5, 4128), (256, 1024)])
+@pytest.mark.parametrize("norm,with_gain", [(False, False), (True, False), (True, True)])
+def test_act_quant_bit_exact(mode, rows, k, norm, with_gain):
+    rng = np.random.default_rng(rows * 7 + k + (3 if norm else 0) + (5 if with_gain else 0))
+    h = synth.activations(rng, rows, k)
+    h[0, :QK] = 0.0
+    g = synth.gain(rng, k) if with_gain else None
+    x = orc.rmsnorm(h, g, 1e-5)[0] if norm else h
+    act_o = orc.quantize(mode, x)
+    xq, xd = native.activation_buffers(mode, rows, k)
+    native.act_quant(mode, dev(h), xq, xd, norm=norm, gain=dev(g) if g is not None else None,
+                     eps=1e-5)
+    act = act_to_numpy(mode, xq, xd)
+    for a, b in zip(act, act_o):
+        assert np.array_equal(a.view(np.uint8) if a.dtype != np.float32 else a.view(np.uint32),
+                              b.view(np.uint8) if b.dtype != np.float32 else b.view(np.uint32))
+
+
+# ------------------------------------------------------------- block dots
+
+@pytest.mark.parametrize("mode", ["i8", "i8x2"])
+@pytest.mark.parametrize("n,k,rows", [(1, 32, 1), (37, 96, 3), (129, 4096, 2)])
+def test_block_dots_bit_exact(mode, n, k, rows):
+    rng = np.random.default_rng(n + k + rows)
+    q, _ = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, rows, k)
+    act = orc.quantize(mode, x)
+    isum_o = orc.block_dots(q, act[0], act[1] if mode == "i8x2" else None)
+    t = torch()
+    xq, _ = upload_act(mode, act, rows, k)
+    isum = t.empty((rows, n, k // QK), dtype=t.int32, device="cuda")
+    native.q8_debug_block_dots(mode, dev(q), xq, rows, isum, path=0)
+    assert np.array_equal(host(isum), isum_o)
+
+
+# ------------------------------------------------------------- projection
+
+SHAPES = [(1, 32), (3, 64), (37, 96), (1000, 1024), (301, 4096), (77, 4128), (64, 14336),
+          (5, 3104)]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n,k", SHAPES)
+@pytest.mark.parametrize("rows", [1, 2, 3, 8, 13, 16, 17])
+def test_proj_parity(mode, n, k, rows):
+    if rows > 3 and n * k > 1000 * 1024:
+        rows = 3  # keep the oracle within seconds on the largest shapes
+    rng = np.random.default_rng(1000 + n + k + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, rows, k)
+    act = orc.quantize(mode, x)
+    y_o, norm = orc.project(mode, q, s, act)
+    qd, sd = upload_weights(q, s)
+    xq, xd = upload_act(mode, act, rows, k)
+    t = torch()
+    y = t.empty((rows, n), dtype=t.float32, device="cuda")
+    native.q8_proj(mode, qd, sd, xq, xd, rows, y)
+    check_close(mode, host(y), y_o, norm, out_f64=False, what=f"{mode} {n}x{k} rows={rows}")
+    if mode == "f32":
+        y64 = t.empty((rows, n), dtype=t.float64, device="cuda")
+        native.q8_proj(mode, qd, sd, xq, xd, rows, y64, out_f64=True)
+        check_close(mode, host(y64), y_o, norm, out_f64=True, what=f"f64 {n}x{k} rows={rows}")
+    y2 = t.empty((rows, n), dtype=t.float32, device="cuda")
+    native.q8_proj_chunk(mode, qd, sd, xq, xd, rows, y2)
+    check_close(mode, host(y2), y_o, norm, what=f"chunk {mode} {n}x{k} rows={rows}")
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_proj_deterministic_and_zero(mode):
+    rng = np.random.default_rng(77)
+    n, k, rows = 500, 4096, 4
+    q, s = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, rows, k)
+    x[1] = 0.0
+    act = orc.quantize(mode, x)
+    qd, sd = upload_weights(q, s)
+    xq, xd = upload_act(mode, act, rows, k)
+    t = torch()
+    y1 = t.empty((rows, n), dtype=t.float32, device="cuda")
+    y2 = t.empty_like(y1)
+    native.q8_proj(mode, qd, sd, xq, xd, rows, y1)
+    native.q8_proj(mode, qd, sd, xq, xd, rows, y2)
+    a, b = host(y1), host(y2)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert np.all(a[1] == 0)
+
+
+# ----------------------------------------------------------- fused producer
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n,k,rows", [(300, 4096, 1), (100, 14336, 2), (64, 1024, 16)])
+def test_fused_matches_oracle_and_composition(mode, n, k, rows):
+    rng = np.random.default_rng(5 + n + k + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    h = synth.activations(rng, rows, k)
+    g = synth.gain(rng, k)
+    x, _ = orc.rmsnorm(h, g, 1e-5)
+    y_o, norm = orc.project(mode, q, s, orc.quantize(mode, x))
+    qd, sd = upload_weights(q, s)
+    t = torch()
+    hd, gd = dev(h), dev(g)
+    ws = t.empty(native.q8_proj_fused_workspace(mode, rows, k), dtype=t.uint8, device="cuda")
+    y = t.empty((rows, n), dtype=t.float32, device="cuda")
+    native.q8_proj_fused(mode, qd, sd, hd, y, ws, gain=gd, eps=1e-5)
+    check_close(mode, host(y), y_o, norm, what=f"fused {mode}")
+    # the fused call computes exactly what its two unfused parts compute
+    xq, xd = native.activation_buffers(mode, rows, k)
+    native.act_quant(mode, hd, xq, xd, norm=True, gain=gd, eps=1e-5)
+    y2 = t.empty_like(y)
+    native.q8_proj(mode, qd, sd, xq, xd, rows, y2)
+    assert np.array_equal(host(y).view(np.uint32), host(y2).view(np.uint32))
+
+
+# ------------------------------------------------------------- LM head
+
+def _planted_head(n, k, rows, seed):
+    rng = np.random.default_rng(seed)
+    q, s = synth.q8_weights(rng, n, k)
+    h = synth.head_activations(rng, rows, k)
+    pos = synth.planted_positions(rng, n)
+    synth.plant_head_rows(q, s, h, pos)
+    return q, s, h, pos
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n,k,rows", [(20000, 1024, 1), (20000, 1024, 16), (5000, 4096, 20),
+                                      (8, 256, 1)])
+def test_head_argmax_planted(mode, n, k, rows):
+    q, s, h, pos = _planted_head(n, k, rows, seed=n + k + rows)
+    x, _ = orc.rmsnorm(h)
+    act = orc.quantize(mode, x)
+    tok_o, best_o, y_o = orc.head_argmax(mode, q, s, act)
+    assert np.array_equal(tok_o, pos[np.arange(rows) % 8])
+    t = torch()
+    qd, sd = upload_weights(q, s)
+    xq, xd = upload_act(mode, act, rows, k)
+    ws = native.argmax_workspace(rows)
+    tok = t.empty(rows, dtype=t.int32, device="cuda")
+    mx = t.empty(rows, dtype=t.float64, device="cuda")
+    logits = t.empty((rows, n), dtype=t.float64 if mode == "f32" else t.float32, device="cuda")
+    for _ in range(2):  # the workspace counter must come back to zero
+        native.head_argmax(mode, qd, sd, xq, xd, rows, tok, ws, maxval=mx, logits=logits)
+        assert np.array_equal(host(tok), tok_o)
+    _, norm = orc.project(mode, q, s, act)
+    check_close(mode, host(logits), y_o, norm, out_f64=True, what="head logits")
+    rowsel = np.arange(rows)
+    check_close(mode, host(mx), best_o, norm[rowsel, tok_o], out_f64=True, what="head max")
+    assert int(host(ws[:4].view(t.int32))[0]) == 0
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_head_argmax_equals_argmax_of_projection(mode):
+    # unplanted random head: the fused arg-max picks the same index as the
+    # arg-max of the library's own projection output
+    rng = np.random.default_rng(31)
+    n, k, rows = 30011, 1024, 5
+    q, s = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, rows, k)
+    act = orc.quantize(mode, x)
+    t = torch()
+    qd, sd = upload_weights(q, s)
+    xq, xd = upload_act(mode, act, rows, k)
+    y = t.empty((rows, n), dtype=t.float64 if mode == "f32" else t.float32, device="cuda")
+    native.q8_proj(mode, qd, sd, xq, xd, rows, y, out_f64=(mode == "f32"))
+    tok = t.empty(rows, dtype=t.int32, device="cuda")
+    native.head_argmax(mode, qd, sd, xq, xd, rows, tok, native.argmax_workspace(rows))
+    tok_ref, _ = orc.argmax(host(y))
+    assert np.array_equal(host(tok), tok_ref)
+
+
+# --------------------------------------------------- full-size workloads
+
+@pytest.mark.parametrize("mode", MODES)
+def test_decode_layer_full_size_sampled(mode):
+    """The d=4096 layer's four projections at full size, rows = 1, activation
+    RMSNorm(N(0,1)) quantized in the producer; sampled output rows are checked
+    against the oracle one by one."""
+    t = torch()
+    rng = np.random.default_rng(0)
+    for name, n, k in synth.LAYER_D4096:
+        q, s = synth.q8_weights(rng, n, k)
+        h = synth.activations(rng, 1, k)
+        qd, sd = upload_weights(q, s)
+        ws = t.empty(native.q8_proj_fused_workspace(mode, 1, k), dtype=t.uint8, device="cuda")
+        y = t.empty((1, n), dtype=t.float32, device="cuda")
+        native.q8_proj_fused(mode, qd, sd, dev(h), y, ws)
+        idx = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 200)]))
+        x, _ = orc.rmsnorm(h)
+        y_o, norm = orc.project(mode, q[idx], s[idx], orc.quantize(mode, x))
+        check_close(mode, host(y)[:, idx], y_o, norm, what=f"{name} {mode}")
+
+
+@pytest.mark.parametrize("mode,rows", [("i8", 1), ("i8", 16), ("f32", 1)])
+def test_head_full_size(mode, rows):
+    n, k = synth.HEAD_SHAPE
+    q, s, h, pos = _planted_head(n, k, rows, seed=4)
+    x, _ = orc.rmsnorm(h)
+    act = orc.quantize(mode, x)
+    t = torch()
+    qd, sd = upload_weights(q, s)
+    xq, xd = upload_act(mode, act, rows, k)
+    tok = t.empty(rows, dtype=t.int32, device="cuda")
+    mx = t.empty(rows, dtype=t.float64, device="cuda")
+    native.head_argmax(mode, qd, sd, xq, xd, rows, tok, native.argmax_workspace(rows), maxval=mx)
+    want = pos[np.arange(rows) % 8]
+    assert np.array_equal(host(tok), want)
+    y_o, norm = orc.project(mode, q[want], s[want], act)
+    rowsel = np.arange(rows)
+    check_close(mode, host(mx), y_o[rowsel, rowsel], norm[rowsel, rowsel], out_f64=True,
+                what="head max value")
