@@ -279,7 +279,23 @@ def run_ours(args, world, rank, local):
             for p in range(4):
                 native.q8_proj_fused(m, Q[c][p], S[c][p], H[p], Y[m][p], WS[m][p])
 
-    def timed(nsteps, modes=MODES):
+    # The lane replays each step as one captured CUDA graph; so does the bench:
+    # one graph per rotating weight copy, so host launch cost is not measured.
+    def capture(fn):
+        graphs = []
+        for c in range(COPIES):
+            fn(c)                      # eager run first: attributes, first-call set-up
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap_stream):
+                fn(c)
+            graphs.append(g)
+        torch.cuda.synchronize(dev)
+        return graphs
+
+    cap_stream = torch.cuda.Stream(dev)
+
+    def timed(graphs, nsteps):
         torch.cuda.synchronize(dev)
         barrier(world)
         torch.cuda.synchronize(dev)
@@ -287,26 +303,54 @@ def run_ours(args, world, rank, local):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(nsteps):
-            step(i, modes)
+            graphs[i % COPIES].replay()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
         return e0.elapsed_time(e1) / nsteps
 
+    if args.case:
+        # one projection's kernel, warmup+steps eager launches (a profiler case)
+        parts = args.case.split(":")
+        mode, proj = parts[0], parts[1]
+        fused = len(parts) > 2 and parts[2] == "fused"
+        p = [nm for nm, _, _ in synth.LAYER_D4096].index(proj)
+        k = synth.LAYER_D4096[p][2]
+        xq, xd = native.activation_buffers(mode, 1, k, device=dev)
+        native.act_quant(mode, H[p], xq, xd, norm=True)
+        for i in range(args.warmup + args.steps):
+            if fused:
+                native.q8_proj_fused(mode, Q[i % COPIES][p], S[i % COPIES][p], H[p], Y[mode][p],
+                                     WS[mode][p])
+            else:
+                native.q8_proj(mode, Q[i % COPIES][p], S[i % COPIES][p], xq, xd, 1, Y[mode][p])
+        torch.cuda.synchronize(dev)
+        if rank == 0:
+            print(json.dumps({"case": args.case, "launches": args.warmup + args.steps}))
+        return
+
+    step_graphs = capture(lambda c: step(c))
     for i in range(args.warmup):
-        step(i)
+        step_graphs[i % COPIES].replay()
     torch.cuda.synchronize(dev)
+
+    if args.quick:
+        ms = max_over_ranks(world, timed(step_graphs, args.steps))
+        if rank == 0:
+            print(json.dumps({"quick": True, "ms_per_step": ms,
+                              "GB/s": len(MODES) * LAYER_BYTES / (ms * 1e-3) / 1e9}))
+        return
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    ms = timed(args.steps)
+    ms = timed(step_graphs, args.steps)
     # keep the same load running so the clock samples cover it
     t_hold = time.perf_counter()
     while time.perf_counter() - t_hold < 1.0:
         for i in range(50):
-            step(i)
+            step_graphs[i % COPIES].replay()
         torch.cuda.synchronize(dev)
     clocks = sampler.stop() if sampler else None
     ms = max_over_ranks(world, ms)
@@ -316,47 +360,52 @@ def run_ours(args, world, rank, local):
     # per-mode breakdown (same protocol)
     per_mode = {}
     for m in MODES:
+        gm = capture(lambda c, m=m: step(c, (m,)))
         for i in range(args.warmup):
-            step(i, (m,))
-        mms = max_over_ranks(world, timed(args.steps, (m,)))
+            gm[i % COPIES].replay()
+        mms = max_over_ranks(world, timed(gm, args.steps))
         per_mode[m] = {"ms_per_step": round(mms, 5),
                        "GB/s": round(LAYER_BYTES / (mms * 1e-3) / 1e9, 2)}
+        del gm
 
-    # dominant kernel: the GEMV, timed alone per mode (back-to-back launches, rotating copies)
+    # dominant kernel: the projection alone (producer outputs ready), each
+    # projection replayed from a graph of REPS back-to-back launches
     gemv = {}
     peak, peak_kind = load_peaks()
+    reps = 20
     for m in MODES:
         xq, xd = {}, {}
         for p, (_, n, k) in enumerate(synth.LAYER_D4096):
             xq[p], xd[p] = native.activation_buffers(m, 1, k, device=dev)
             native.act_quant(m, H[p], xq[p], xd[p], norm=True)
-        reps = max(args.steps, 20)
-        for i in range(3):
-            for p in range(4):
-                native.q8_proj(m, Q[i % COPIES][p], S[i % COPIES][p], xq[p], xd[p], 1, Y[m][p])
-        torch.cuda.synchronize(dev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(reps):
-            for p in range(4):
-                native.q8_proj(m, Q[i % COPIES][p], S[i % COPIES][p], xq[p], xd[p], 1, Y[m][p])
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        per_launch_ms = e0.elapsed_time(e1) / (reps * 4)
         act_b = {"f32": 4, "i8": 1 + 4 / QK, "i8x2": 2 + 4 / QK}[m]
-        alg = sum(weight_bytes(n, k) + k * act_b + n * 4 for _, n, k in synth.LAYER_D4096) / 4
-        gemv[m] = {"per_launch_ms": per_launch_ms, "alg_bytes_per_launch": alg,
-                   "GB/s": alg / (per_launch_ms * 1e-3) / 1e9}
+        per_proj, tot_us, tot_bytes = {}, 0.0, 0.0
+        for p, (nm, n, k) in enumerate(synth.LAYER_D4096):
+            def launches(c, p=p, m=m):
+                for i in range(reps):
+                    cc = (c + i) % COPIES
+                    native.q8_proj(m, Q[cc][p], S[cc][p], xq[p], xd[p], 1, Y[m][p])
+            gp = capture(launches)
+            for i in range(3):
+                gp[i % COPIES].replay()
+            us = timed(gp, max(args.steps // 5, 4)) / reps * 1e3
+            alg = weight_bytes(n, k) + k * act_b + n * 4
+            per_proj[nm] = {"us": round(us, 2), "GB/s": round(alg / (us * 1e-6) / 1e9, 1)}
+            tot_us += us
+            tot_bytes += alg
+            del gp
+        gemv[m] = {"per_launch_ms": tot_us / 4 * 1e-3, "alg_bytes_per_launch": tot_bytes / 4,
+                   "GB/s": tot_bytes / (tot_us * 1e-6) / 1e9, "per_projection": per_proj}
     dom = max(MODES, key=lambda m: gemv[m]["per_launch_ms"])
     achieved = gemv[dom]["GB/s"]
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": committed_traffic(f"gemv_{dom}"),
-                "kernel": f"gemv_kernel<{dom}>", "peak_source": peak_kind,
+                "kernel": f"gemv_row_kernel<{dom}>", "peak_source": peak_kind,
                 "per_mode_GBps": {m: round(gemv[m]["GB/s"], 2) for m in MODES},
-                "note": "GEMV timed alone: 4 projections back to back, rotating weight copies; "
-                        "algorithmic bytes = 34/32 B per weight + activation + output"}
+                "per_projection": {m: gemv[m]["per_projection"] for m in MODES},
+                "note": "projection kernel alone, graph-replayed launches with rotating weight "
+                        "copies; algorithmic bytes = 34/32 B per weight + activation + output"}
 
     # end to end through the C ABI: pinned host inputs in, outputs back, every step
     h_host = [torch.from_numpy(h).pin_memory() for h in hs]
@@ -365,24 +414,29 @@ def run_ours(args, world, rank, local):
     h2d = sum(h.numel() * 4 for h in h_host)
     d2h = sum(y.numel() * 4 for m in MODES for y in y_host[m])
 
-    def e2e_step(i):
+    def e2e_body(c):
         for p in range(4):
             H[p].copy_(h_host[p], non_blocking=True)
-        step(i)
+        step(c)
         for m in MODES:
             for p in range(4):
                 y_host[m][p].copy_(Y[m][p], non_blocking=True)
-        torch.cuda.synchronize(dev)
 
+    e2e_graphs = capture(e2e_body)
     for i in range(args.warmup):
-        e2e_step(i)
+        e2e_graphs[i % COPIES].replay()
+        torch.cuda.synchronize(dev)
     barrier(world)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        e2e_step(i)
+        e2e_graphs[i % COPIES].replay()
+        torch.cuda.synchronize(dev)      # the host reads every step's outputs
     e2e_ms = max_over_ranks(world, (time.perf_counter() - t0) / args.steps * 1e3)
     e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+           "note": "host wall clock per step: graph replay of H2D copy + 12 C-ABI calls + D2H "
+                   "copy, then stream sync"}
+    launches_per_fused = 2
 
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -415,6 +469,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="warm-up and timed steps only (for launch lists under a profiler)")
+    ap.add_argument("--case", default=None,
+                    help="MODE:PROJ -- run only that projection's GEMV, warmup+steps launches "
+                         "(a small case for a full profiler capture)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

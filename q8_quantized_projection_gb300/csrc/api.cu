@@ -10,6 +10,8 @@ namespace q8 {
 cudaError_t launch_gemv_mode0(const GemvArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_gemv_mode1(const GemvArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_gemv_mode2(const GemvArgs& a, const LaunchCtx& ctx);
+cudaError_t launch_gemv_fused_mode1(const GemvArgs& a, const LaunchCtx& ctx);
+cudaError_t launch_gemv_fused_mode2(const GemvArgs& a, const LaunchCtx& ctx);
 }  // namespace q8
 
 using namespace q8;
@@ -131,7 +133,7 @@ q8_status check_proj_args(int mode, const int8_t* q, const uint16_t* s, int64_t 
 }  // namespace
 
 namespace q8 {
-int gemv_max_rows(int) { return 16; }
+int gemv_max_rows(int mode) { return mode == 0 ? 4 : 16; }
 }  // namespace q8
 
 extern "C" {
@@ -228,7 +230,8 @@ q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N,
                         const float* h, int64_t rows, const float* gain, float eps, void* y,
                         int out_f64, void* workspace, size_t ws_bytes, void* stream) {
     if (!workspace) return Q8_ERR_WORKSPACE;
-    q8_status st = check_proj_args(mode, q, s, N, K, h, reinterpret_cast<const float*>(h), rows, y);
+    // (h stands in for the scales argument: the fused call has none)
+    q8_status st = check_proj_args(mode, q, s, N, K, h, h, rows, y);
     if (st != Q8_OK) return st;
     if (out_f64 && mode != Q8_ACT_F32) return Q8_ERR_MODE;
     if (gain && !aligned16(gain)) return Q8_ERR_ALIGN;
@@ -237,6 +240,23 @@ q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N,
     if (ws_bytes < q8_proj_fused_workspace(mode, rows, K)) return Q8_ERR_WORKSPACE;
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
+    if (mode != Q8_ACT_F32 && rows == 1 && K <= kFusedMaxK) {
+        // decode step: one launch, the producer runs inside the projection
+        GemvArgs a{};
+        a.mode = mode;
+        a.q = q;
+        a.s = s;
+        a.N = N;
+        a.K = K;
+        a.rows = 1;
+        a.plane = K;
+        a.y = y;
+        a.h = h;
+        a.gain = gain;
+        a.eps = eps;
+        return launched(mode == Q8_ACT_I8 ? launch_gemv_fused_mode1(a, ctx)
+                                          : launch_gemv_fused_mode2(a, ctx));
+    }
     unsigned char* act = static_cast<unsigned char*>(workspace);
     float* xd = reinterpret_cast<float*>(act + round_up(act_bytes(mode, rows, K), 256));
     cudaError_t e = launch_act_quant(mode, h, rows, K, 1, gain, eps, act, xd, ctx);

@@ -106,6 +106,11 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// Named barrier `id` (1..15) over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------- programmatic dependent launch
 
 // Blocks until every grid this one depends on has completed and its memory
@@ -130,6 +135,22 @@ __device__ __forceinline__ int4 ldg_nc_v4(const void* p) {
 
 __device__ __forceinline__ int4 lds_v4(const void* p) {
     return *reinterpret_cast<const int4*>(p);
+}
+
+// Explicit shared-space loads on 32-bit shared addresses (data written by the
+// bulk-copy engine and published through an mbarrier wait).
+__device__ __forceinline__ int4 lds128(uint32_t addr) {
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t lds16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
 }
 
 __device__ __forceinline__ float half_bits_to_float(uint16_t bits) {

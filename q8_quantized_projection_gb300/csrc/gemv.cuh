@@ -1,29 +1,31 @@
 // gemv.cuh -- CUDA-core Q8_0 projection for few activation rows (decode step,
 // small batches, the LM head), sm_103a.
 //
-// The projection at rows = 1..16 is bound by HBM: every weight byte is read
+// At rows = 1..16 the projection is bound by HBM: every weight byte is read
 // once per step (34 bytes per 32 weights) and the arithmetic per byte is a
 // fraction of a dp4a.  Design:
 //
 //  * Persistent grid, one CTA per SM.  CTA c owns the contiguous weight rows
 //    [N*c/G, N*(c+1)/G), so the imbalance between CTAs is at most one row.
-//  * A producer warp streams the CTA's rows through a 4-stage shared-memory
-//    ring with the bulk-copy (TMA) engine: a stage is 8*rpw rows by a K-slice
-//    of at most 4096 bytes, one contiguous copy when whole rows fit, one copy
-//    per row otherwise, plus the matching binary16 scales.  Up to 128 KB per
-//    SM are in flight, which covers HBM latency without register pressure.
-//  * The weights do not depend on the previous kernel on the stream, so the
-//    producer starts before griddepcontrol.wait (programmatic dependent
-//    launch); only the consumers wait before reading activations.
-//  * Eight consumer warps each own whole weight rows of a stage; lanes walk
-//    the row in 16-byte chunks (half a Q8_0 block), read the activation chunk
-//    through the read-only path (it is shared by every warp of the SM and
-//    stays in L1), and fold each half-block's exact int32 dot with the two
-//    scales.  A row ends with one warp-shuffle reduction.
-//  * Modes: one-word (4 dp4a per 16 weights), two-word (8 dp4a: hi and lo
-//    planes, combined as 128*hi + lo exactly in int32), f32 (exact
-//    TwoProduct/TwoSum double-float accumulation in f32 arithmetic, since
-//    the GB300's FP64 rate is far below one add per weight at HBM speed).
+//  * K is cut into slices of SLB = 512*CPL bytes (the last one shorter).  Work
+//    runs slice-major: for a slice, all of the CTA's rows stream through a
+//    shared-memory ring fed by the bulk-copy (TMA) engine, NW*RPW rows a stage
+//    (NW = 8 or 16 consumer warps), 128 KB in flight per SM.  Weights never depend on the previous kernel,
+//    so the producer warp starts before griddepcontrol.wait (programmatic
+//    dependent launch); consumers wait before touching activations.
+//  * Consumer warp w owns rows w, w+NW, ... of every stage; lane l owns the
+//    16-byte chunks l + 32c (c < CPL) of the slice, so its activation chunks
+//    stay in registers for the whole slice.  A row costs each lane CPL shared
+//    loads, the dots, and one warp-shuffle reduction; a row's running sum
+//    across slices lives in shared memory and is touched only by its warp, so
+//    consumer warps never synchronise with each other.
+//  * One-word mode: 4 dp4a per 16 weights; two-word: 8 dp4a (hi and lo
+//    planes) combined as 128*hi + lo exactly in int32.  f32 mode: each lane
+//    writes its 16 activations of a chunk as 31-bit fixed point relative to
+//    their own binade (4 int8 planes), so a chunk's dot with the int8 weights
+//    is an exact int64 from 16 dp4a; chunk values are scaled and summed as f32
+//    pairs (error-free transforms, ~48 bits), because the GB300's FP64 rate
+//    and f32<->f64 conversions are far below one operation per weight.
 //  * Optional arg-max epilogue for the LM head: per-CTA best (value, lowest
 //    index), then the last CTA to take a ticket reduces all candidates.
 #pragma once
@@ -33,11 +35,11 @@
 
 namespace q8 {
 
-constexpr int kGemvConsumerWarps = 8;
-constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 1);
-constexpr int kGemvStage = 32768;   // weight bytes per ring stage
-constexpr int kGemvStages = 4;
-constexpr int kGemvMaxRows = 16;
+constexpr int kGemvMaxConsumerWarps = 16;
+constexpr int kGemvRing = 131072;       // weight bytes in flight per CTA
+constexpr int kGemvStageMax = 32768;    // weight bytes of one stage, upper bound
+constexpr int kGemvMaxStages = 16;
+constexpr int kGemvYaccBytes = 32768;   // row accumulators of one super-block
 
 struct GemvParams {
     const int8_t* q;
@@ -49,83 +51,273 @@ struct GemvParams {
     int rows;
     void* y;
     int out_f64;
-    int KS;          // K-slice bytes of a stage (multiple of 32)
-    int nks;         // slices per row
-    int rpw;         // rows per consumer warp per stage
-    int scale_bulk;  // scales staged by bulk copy (K % 256 == 0)
     int32_t* tok;
     double* maxval;
     unsigned char* ws;
     int* err;
+    const float* h;      // fused producer input (decode kernel only)
+    const float* gain;
+    float eps;
 };
 
-__host__ __device__ constexpr size_t gemv_smem_bytes() {
-    return size_t(kGemvStages) * kGemvStage + size_t(kGemvStages) * (kGemvStage / 16) +
-           2 * kGemvStages * sizeof(uint64_t) +
-           size_t(kGemvConsumerWarps) * kGemvMaxRows * sizeof(ArgmaxCand) + 16;
+// Chunks (16 bytes of K) each lane owns per slice, and consumer warps per
+// CTA, for the slice-major kernel (4 to 16 activation rows).
+template <int MODE, int R>
+__host__ __device__ constexpr int gemv_cpl() {
+    return MODE == 0 ? (R == 1 ? 4 : (R == 2 ? 2 : 1)) : (R <= 8 ? 8 / R : 1);
+}
+template <int MODE, int R>
+__host__ __device__ constexpr int gemv_warps() {
+    return 8;
 }
 
-__device__ __forceinline__ void consumer_bar() {
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kGemvConsumerWarps) : "memory");
-}
+// ------------------------------------------------------------ f32 pairs
 
-__device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
-__device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+// Unevaluated f32 pair hi + lo (about 48 significant bits), added with
+// error-free transforms.
+struct DF {
+    float hi, lo;
+};
 
-template <typename T>
-__device__ __forceinline__ T warp_sum(T v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// Error-free transforms in f32 (no contraction: explicit _rn intrinsics).
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     s = __fadd_rn(a, b);
     const float bb = __fsub_rn(s, a);
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-// Accumulates the 16 exact products sw*q_e*x_e of one chunk into (hi, lo).
-__device__ __forceinline__ void f32_chunk(const int4 w, float sw, const float4* xv, float& hi,
-                                          float& lo) {
-    const int words[4] = {w.x, w.y, w.z, w.w};
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+    float s, e;
+    two_sum(a.hi, b.hi, s, e);
+    return DF{s, __fadd_rn(__fadd_rn(a.lo, b.lo), e)};
+}
+
+template <int MODE>
+struct AccT {
+    using T = float;
+};
+template <>
+struct AccT<0> {
+    using T = DF;
+};
+
+__device__ __forceinline__ float acc_zero(float) { return 0.0f; }
+__device__ __forceinline__ DF acc_zero(DF) { return DF{0.0f, 0.0f}; }
+__device__ __forceinline__ float acc_add(float a, float b) { return a + b; }
+__device__ __forceinline__ DF acc_add(DF a, DF b) { return df_add(a, b); }
+__device__ __forceinline__ double acc_value(float a) { return double(a); }
+__device__ __forceinline__ double acc_value(DF a) { return double(a.hi) + double(a.lo); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ DF warp_sum(DF v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const DF r{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+        v = df_add(v, r);
+    }
+    return v;
+}
+
+// ------------------------------------------------------------ f32-mode math
+
+__device__ __forceinline__ int dp4a_su(int a_signed, unsigned b_unsigned, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a_signed), "r"(b_unsigned), "r"(c));
+    return d;
+}
+
+// Binade bound: |x| < 2^e (subnormals and zero give -126).
+__device__ __forceinline__ int binade(float a) {
+    const int eb = (__float_as_int(a) >> 23) & 0xff;
+    return eb == 0 ? -126 : eb - 126;
+}
+
+// 16 f32 activations -> 4 byte planes of X = rint(x * 2^(30-E)), |X| <= 2^30,
+// X = p3*2^24 + p2*2^16 + p1*2^8 + p0 (p3 signed, p2..p0 unsigned), and the
+// chunk's binade E.  Plane j word u packs elements 4u..4u+3.
+struct FixChunk {
+    int p[4][4];
+    int e;
+};
+
+__device__ __forceinline__ FixChunk fix_chunk(const float (&x)[16]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    FixChunk f;
+    f.e = binade(amax);
+    int X[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) X[i] = __float2int_rn(ldexpf(x[i], 30 - f.e));
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        const float xs[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float wv = __fmul_rn(sw, byte_as_float(words[u], j));  // exact: 11 x 7 bits
-            const float p = __fmul_rn(wv, xs[j]);
-            const float pe = __fmaf_rn(wv, xs[j], -p);                   // exact product error
-            float s, e;
-            two_sum(hi, p, s, e);
-            hi = s;
-            lo = __fadd_rn(lo, __fadd_rn(e, pe));
+            const unsigned b0 = (unsigned(X[4 * u + 0]) >> (8 * j)) & 0xffu;
+            const unsigned b1 = (unsigned(X[4 * u + 1]) >> (8 * j)) & 0xffu;
+            const unsigned b2 = (unsigned(X[4 * u + 2]) >> (8 * j)) & 0xffu;
+            const unsigned b3 = (unsigned(X[4 * u + 3]) >> (8 * j)) & 0xffu;
+            f.p[j][u] = int(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
         }
+    }
+    return f;
+}
+
+// Exact chunk dot sum_e q_e * X_e as int64 (|.| < 2^42).
+__device__ __forceinline__ long long fix_dot(const int4 w, const FixChunk& f) {
+    const int wv[4] = {w.x, w.y, w.z, w.w};
+    int P[4];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        int a = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a = dp4a_su(wv[u], unsigned(f.p[j][u]), a);
+        P[j] = a;
+    }
+    int a = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) a = __dp4a(wv[u], f.p[3][u], a);
+    P[3] = a;
+    const long long lo = (long long)P[1] * 256 + P[0];
+    return ((long long)P[3] << 24) + ((long long)P[2] << 16) + lo;
+}
+
+// f * V exactly as an f32 pair (hi, lo), |lo| <~ 2^-23 |hi|.
+__device__ __forceinline__ DF scaled_pair(float f, long long V) {
+    const int vh = int(V >> 21);
+    const int vl = int(V & 0x1fffff);
+    const float fh = __int2float_rn(vh) * 2097152.0f;   // exact
+    const float fl = __int2float_rn(vl);                // exact
+    const float p1 = __fmul_rn(f, fh);
+    const float e1 = __fmaf_rn(f, fh, -p1);
+    const float p2 = __fmul_rn(f, fl);
+    const float e2 = __fmaf_rn(f, fl, -p2);
+    float s, e3;
+    two_sum(p1, p2, s, e3);
+    return DF{s, __fadd_rn(__fadd_rn(e1, e2), e3)};
+}
+
+// --------------------------------------------------------------- geometry
+
+__device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+struct Geo {
+    int64_t K;
+    int slb;        // slice bytes (the last slice may be shorter)
+    int nks;        // slices
+    int RS;         // rows per stage (8 * rows per warp)
+    int rpw;        // rows per consumer warp per stage
+    int stage_bytes;
+    int nstages;
+    int64_t r0, r1; // CTA rows
+    int64_t sbrows; // rows per super-block (multiple of RS)
+};
+
+// Walks the stages in the order producer and consumers share: super-block,
+// then slice, then row block.  Advancing never divides.
+struct StageIter {
+    int64_t sb0, sb_end, rb, ks;
+    int sl, kl, slot;
+    uint32_t phase;
+    bool done;
+};
+
+__device__ __forceinline__ void stage_init(const Geo& g, StageIter& it) {
+    it.sb0 = g.r0;
+    it.sb_end = min64(g.r1, g.r0 + g.sbrows);
+    it.rb = g.r0;
+    it.ks = 0;
+    it.sl = 0;
+    it.kl = int(min64(g.slb, g.K));
+    it.slot = 0;
+    it.phase = 0;
+    it.done = g.r0 >= g.r1;
+}
+
+__device__ __forceinline__ void stage_next(const Geo& g, StageIter& it) {
+    it.rb += g.RS;
+    if (it.rb >= it.sb_end) {
+        it.ks += it.kl;
+        ++it.sl;
+        if (it.sl == g.nks) {
+            it.sb0 += g.sbrows;
+            it.done = it.sb0 >= g.r1;
+            it.sb_end = min64(g.r1, it.sb0 + g.sbrows);
+            it.sl = 0;
+            it.ks = 0;
+        }
+        it.kl = int(min64(g.slb, g.K - it.ks));
+        it.rb = it.sb0;
+    }
+    if (++it.slot == g.nstages) {
+        it.slot = 0;
+        it.phase ^= 1u;
     }
 }
 
-template <int MODE, int R, int RPWMAX, bool ARGMAX>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams p) {
+template <int MODE, int R>
+__host__ __device__ constexpr size_t gemv_smem_bytes() {
+    return size_t(kGemvRing) + size_t(kGemvRing) / 16 + 2 * kGemvMaxStages * sizeof(uint64_t) +
+           kGemvYaccBytes + size_t(kGemvMaxConsumerWarps) * R * sizeof(ArgmaxCand) + 64;
+}
+
+template <int NT>
+__device__ __forceinline__ void consumer_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+
+// --------------------------------------------------------------- the kernel
+
+template <int MODE, int R, bool ARGMAX>
+__global__ void __launch_bounds__(32 * (gemv_warps<MODE, R>() + 1), 1)
+    gemv_kernel(const GemvParams p) {
+    using A = typename AccT<MODE>::T;
+    constexpr int CPL = gemv_cpl<MODE, R>();
+    constexpr int kGemvConsumerWarps = gemv_warps<MODE, R>();
+    constexpr int kGemvConsumers = 32 * kGemvConsumerWarps;
+
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* wring = smem;
-    unsigned char* sring = smem + size_t(kGemvStages) * kGemvStage;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sring + size_t(kGemvStages) * (kGemvStage / 16));
-    uint64_t* empty = full + kGemvStages;
-    ArgmaxCand* cand = reinterpret_cast<ArgmaxCand*>(empty + kGemvStages);
+    unsigned char* sring = wring + kGemvRing;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sring + kGemvRing / 16);
+    uint64_t* empty = full + kGemvMaxStages;
+    A* yacc = reinterpret_cast<A*>(empty + kGemvMaxStages);              // [sbrows][R]
+    ArgmaxCand* cand = reinterpret_cast<ArgmaxCand*>(reinterpret_cast<unsigned char*>(yacc) +
+                                                     kGemvYaccBytes);   // [8][R]
+    __shared__ float s_amax[kGemvConsumerWarps][R];
+    __shared__ int s_emax[R];
     __shared__ unsigned int s_ticket;
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
-    const int64_t N = p.N, K = p.K, nb = K / Q8_QK;
-    const int64_t r0 = N * c / G, r1 = N * (c + 1) / G;
-    const int RS = 8 * p.rpw, KS = p.KS, nks = p.nks;
-    const int64_t nrb = (r1 - r0 + RS - 1) / RS;
-    const int64_t total = nrb * nks;
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kGemvStages; ++i) {
+    Geo g;
+    g.K = p.K;
+    g.slb = 512 * CPL;
+    g.nks = int((p.K + g.slb - 1) / g.slb);
+    {
+        const int kmax = int(min64(p.K, g.slb));
+        int rpw = (kGemvStageMax / kGemvConsumerWarps) / kmax;
+        if (rpw * kGemvConsumerWarps * kmax > kGemvStageMax) rpw = 1;
+        g.rpw = rpw < 1 ? 1 : (rpw > 16 ? 16 : rpw);
+        g.RS = kGemvConsumerWarps * g.rpw;
+        g.stage_bytes = (g.RS * kmax + 1023) & ~1023;
+        const int ns = kGemvRing / g.stage_bytes;
+        g.nstages = ns > kGemvMaxStages ? kGemvMaxStages : ns;
+        g.r0 = p.N * c / G;
+        g.r1 = p.N * (c + 1) / G;
+        const int64_t yrows = kGemvYaccBytes / int64_t(R * sizeof(A));
+        g.sbrows = (yrows / g.RS) * g.RS;
+    }
+
+    if (tid == 0) {
+        for (int i = 0; i < g.nstages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kGemvConsumerWarps);
         }
@@ -134,65 +326,99 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     __syncthreads();
     pdl_launch_dependents();
 
+    const bool scale_bulk = (p.K % 256) == 0;
+
     if (warp == kGemvConsumerWarps) {
-        // ------------------------------------------------------------ producer
+        // -------------------------------------------------------------- producer
         if (lane == 0) {
             const uint64_t policy = policy_evict_first();
+            const unsigned char* qsrc = reinterpret_cast<const unsigned char*>(p.q);
+            const unsigned char* ssrc = reinterpret_cast<const unsigned char*>(p.s);
             int64_t issued = 0;
-            for (int64_t i = 0; i < total; ++i) {
-                const int slot = int(i % kGemvStages);
-                if (i >= kGemvStages) {
-                    if (!mbar_wait(&empty[slot], uint32_t(((i / kGemvStages) - 1) & 1), p.err))
-                        break;
-                }
-                const int64_t rb = r0 + (i / nks) * RS;
-                const int nrows = int(min64(RS, r1 - rb));
-                const int64_t ks = int64_t(i % nks) * KS;
-                const int kl = int(min64(KS, K - ks));
+            StageIter it;
+            stage_init(g, it);
+            while (!it.done) {
+                if (issued >= g.nstages && !mbar_wait(&empty[it.slot], it.phase ^ 1u, p.err)) break;
+                const int nrows = int(min64(g.RS, it.sb_end - it.rb));
+                const int kl = it.kl;
                 uint32_t bytes = uint32_t(nrows) * kl;
-                if (p.scale_bulk) bytes += uint32_t(nrows) * (kl / 16);
-                mbar_arrive_expect_tx(&full[slot], bytes);
-                unsigned char* wdst = wring + size_t(slot) * kGemvStage;
-                unsigned char* sdst = sring + size_t(slot) * (kGemvStage / 16);
-                const unsigned char* qsrc = reinterpret_cast<const unsigned char*>(p.q);
-                const unsigned char* ssrc = reinterpret_cast<const unsigned char*>(p.s);
-                if (kl == K) {
-                    bulk_g2s_hint(wdst, qsrc + rb * K, uint32_t(nrows) * kl, &full[slot], policy);
-                    if (p.scale_bulk)
-                        bulk_g2s_hint(sdst, ssrc + rb * (K / 16), uint32_t(nrows) * (kl / 16),
-                                      &full[slot], policy);
+                if (scale_bulk) bytes += uint32_t(nrows) * (kl / 16);
+                mbar_arrive_expect_tx(&full[it.slot], bytes);
+                unsigned char* wdst = wring + size_t(it.slot) * g.stage_bytes;
+                unsigned char* sdst = sring + size_t(it.slot) * (g.stage_bytes / 16);
+                if (kl == p.K) {
+                    bulk_g2s_hint(wdst, qsrc + it.rb * p.K, uint32_t(nrows) * kl, &full[it.slot],
+                                  policy);
+                    if (scale_bulk)
+                        bulk_g2s_hint(sdst, ssrc + it.rb * (p.K / 16), uint32_t(nrows) * (kl / 16),
+                                      &full[it.slot], policy);
                 } else {
+                    const unsigned char* qrow = qsrc + it.rb * p.K + it.ks;
+                    const unsigned char* srow = ssrc + it.rb * (p.K / 16) + it.ks / 16;
                     for (int j = 0; j < nrows; ++j) {
-                        bulk_g2s_hint(wdst + size_t(j) * KS, qsrc + (rb + j) * K + ks, uint32_t(kl),
-                                      &full[slot], policy);
-                        if (p.scale_bulk)
-                            bulk_g2s_hint(sdst + size_t(j) * (KS / 16),
-                                          ssrc + (rb + j) * (K / 16) + ks / 16, uint32_t(kl / 16),
-                                          &full[slot], policy);
+                        bulk_g2s_hint(wdst + size_t(j) * kl, qrow, uint32_t(kl), &full[it.slot],
+                                      policy);
+                        if (scale_bulk)
+                            bulk_g2s_hint(sdst + size_t(j) * (kl / 16), srow, uint32_t(kl / 16),
+                                          &full[it.slot], policy);
+                        qrow += p.K;
+                        srow += p.K / 16;
                     }
                 }
                 ++issued;
+                stage_next(g, it);
             }
             // Never leave with copies in flight into this CTA's shared memory.
-            for (int64_t i = max64(0, issued - kGemvStages); i < issued; ++i)
-                mbar_wait(&full[i % kGemvStages], uint32_t((i / kGemvStages) & 1), p.err);
+            for (int64_t i = max64(0, issued - g.nstages); i < issued; ++i)
+                mbar_wait(&full[i % g.nstages], uint32_t((i / g.nstages) & 1), p.err);
         }
         return;
     }
 
-    // ------------------------------------------------------------- consumers
-    pdl_wait();  // activations and outputs belong to the previous kernel until here
+    // ---------------------------------------------------------------- consumers
+    pdl_wait();   // activations and outputs belong to the previous kernel until here
 
     const int rows = p.rows;
+    const int64_t K = p.K, N = p.N, nb = K / Q8_QK;
     const signed char* act8 = reinterpret_cast<const signed char*>(p.act);
     const float* actf = reinterpret_cast<const float*>(p.act);
 
-    float acc[RPWMAX][R];
-    float acc_lo[RPWMAX][R];  // f32 mode: low word of the double-float sum
+    if constexpr (MODE == 0) {
+        // Per activation row, the binade of its largest |x|: the common scale
+        // of all chunk values (each chunk is relative to its own binade).
+        float amax[R];
 #pragma unroll
-    for (int jj = 0; jj < RPWMAX; ++jj)
+        for (int m = 0; m < R; ++m) amax[m] = 0.0f;
+        for (int64_t k = int64_t(tid) * 4; k < K; k += 4 * kGemvConsumers) {
 #pragma unroll
-        for (int m = 0; m < R; ++m) acc[jj][m] = acc_lo[jj][m] = 0.0f;
+            for (int m = 0; m < R; ++m) {
+                if (m < rows) {
+                    const int4 t4 = ldg_nc_v4(actf + m * K + k);
+                    amax[m] = fmaxf(amax[m], fmaxf(fmaxf(fabsf(__int_as_float(t4.x)),
+                                                         fabsf(__int_as_float(t4.y))),
+                                                   fmaxf(fabsf(__int_as_float(t4.z)),
+                                                         fabsf(__int_as_float(t4.w)))));
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            float a = amax[m];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            if (lane == 0) s_amax[warp][m] = a;
+        }
+        consumer_bar<kGemvConsumers>();
+        if (tid < R) {
+            float a = 0.0f;
+            for (int w = 0; w < kGemvConsumerWarps; ++w) a = fmaxf(a, s_amax[w][tid]);
+            s_emax[tid] = binade(a);
+        }
+    }
+
+    // zero the row accumulators (a row's entry is only touched by its warp afterwards)
+    for (int i = tid; i < g.sbrows * R; i += kGemvConsumers) yacc[i] = acc_zero(A{});
+    consumer_bar<kGemvConsumers>();
 
     double best_v[ARGMAX ? R : 1];
     long long best_i[ARGMAX ? R : 1];
@@ -202,55 +428,164 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
         best_i[m] = 0x7fffffffffffffffll;
     }
 
+    // activation chunk registers for the current slice
+    int4 a1[CPL][R];
+    int4 a2[CPL][R];
+    float xdv[CPL][R];
+    FixChunk fx[MODE == 0 ? CPL : 1][MODE == 0 ? R : 1];
+    float p2s[CPL][R];
+    int cur_sl = -1;
+
     bool ok = true;
-    for (int64_t i = 0; i < total; ++i) {
-        const int slot = int(i % kGemvStages);
-        const int64_t rb = r0 + (i / nks) * RS;
-        const int nrows = int(min64(RS, r1 - rb));
-        const int sl = int(i % nks);
-        const int64_t ks = int64_t(sl) * KS;
-        const int kl = int(min64(KS, K - ks));
-        if (ok) ok = mbar_wait(&full[slot], uint32_t((i / kGemvStages) & 1), p.err);
-        if (ok) {
-            const unsigned char* W = wring + size_t(slot) * kGemvStage;
-            const uint16_t* SC = reinterpret_cast<const uint16_t*>(sring + size_t(slot) * (kGemvStage / 16));
-            const int nch = kl / 16;
+    StageIter it;
+    stage_init(g, it);
+    for (; !it.done; stage_next(g, it)) {
+        const int slot = it.slot;
+        const int64_t rb = it.rb, ks = it.ks, sb0 = it.sb0;
+        const int kl = it.kl, sl = it.sl;
+        const int cpr = kl >> 4;
+        const int nrows = int(min64(g.RS, it.sb_end - rb));
+
+        if (sl != cur_sl) {
+            // new slice: this lane's activation chunks
+            cur_sl = sl;
 #pragma unroll
-            for (int jj = 0; jj < RPWMAX; ++jj) {
-                const int j = warp + 8 * jj;
-                if (jj < p.rpw && j < nrows) {
-                    const unsigned char* wrow = W + size_t(j) * KS;
-                    for (int ch = lane; ch < nch; ch += 32) {
-                        const int4 w = lds_v4(wrow + ch * 16);
-                        const int64_t k = ks + ch * 16;
-                        const int64_t blk = k >> 5;
-                        const float sw =
-                            p.scale_bulk ? half_bits_to_float(SC[j * (KS / 32) + (ch >> 1)])
-                                         : half_bits_to_float(__ldg(p.s + (rb + j) * nb + blk));
+            for (int cc = 0; cc < CPL; ++cc) {
+                const int ch = lane + 32 * cc;
+                if (ch < cpr) {
+                    const int64_t k = ks + int64_t(ch) * 16;
 #pragma unroll
-                        for (int m = 0; m < R; ++m) {
-                            if (m < rows) {
-                                if constexpr (MODE == 0) {
-                                    float4 xv[4];
-                                    const float* xp = actf + m * K + k;
+                    for (int m = 0; m < R; ++m) {
+                        if (m < rows) {
+                            if constexpr (MODE == 0) {
+                                float xs[16];
 #pragma unroll
-                                    for (int u = 0; u < 4; ++u) {
-                                        const int4 t = ldg_nc_v4(xp + 4 * u);
-                                        xv[u] = make_float4(__int_as_float(t.x), __int_as_float(t.y),
-                                                            __int_as_float(t.z), __int_as_float(t.w));
-                                    }
-                                    f32_chunk(w, sw, xv, acc[jj][m], acc_lo[jj][m]);
-                                } else {
-                                    int isum;
-                                    if constexpr (MODE == 1) {
-                                        isum = dot16_i8(w, ldg_nc_v4(act8 + m * K + k));
-                                    } else {
-                                        isum = dot16_i8x2(w, ldg_nc_v4(act8 + m * K + k),
-                                                          ldg_nc_v4(act8 + p.plane + m * K + k));
-                                    }
-                                    const float sc = sw * __ldg(p.xd + m * nb + blk);
-                                    acc[jj][m] = fmaf(float(isum), sc, acc[jj][m]);
+                                for (int u = 0; u < 4; ++u) {
+                                    const int4 t4 = ldg_nc_v4(actf + m * K + k + 4 * u);
+                                    xs[4 * u + 0] = __int_as_float(t4.x);
+                                    xs[4 * u + 1] = __int_as_float(t4.y);
+                                    xs[4 * u + 2] = __int_as_float(t4.z);
+                                    xs[4 * u + 3] = __int_as_float(t4.w);
                                 }
+                                fx[cc][m] = fix_chunk(xs);
+                                p2s[cc][m] = ldexpf(1.0f, fx[cc][m].e - s_emax[m]);
+                            } else {
+                                a1[cc][m] = ldg_nc_v4(act8 + m * K + k);
+                                if constexpr (MODE == 2)
+                                    a2[cc][m] = ldg_nc_v4(act8 + p.plane + m * K + k);
+                                xdv[cc][m] = __ldg(p.xd + m * nb + (k >> 5));
+                            }
+                        }
+                    }
+                }
+            }
+        }
+
+        if (ok) ok = mbar_wait(&full[slot], it.phase, p.err);
+        if (ok) {
+            const uint32_t W = smem_u32(wring) + uint32_t(slot * g.stage_bytes);
+            const uint32_t SC = smem_u32(sring) + uint32_t(slot * (g.stage_bytes / 16));
+            const bool last = (sl == g.nks - 1);
+            for (int jj = 0; jj < g.rpw; ++jj) {
+                const int r = warp + kGemvConsumerWarps * jj;
+                if (r >= nrows) break;
+                A part[R];
+#pragma unroll
+                for (int m = 0; m < R; ++m) part[m] = acc_zero(A{});
+                const uint32_t wrow = W + uint32_t(r * kl) + uint32_t(lane * 16);
+                if (cpr == 32 * CPL) {
+                    // full slice: every chunk valid, no predicates, so the
+                    // CPL independent dots interleave
+                    int4 w[CPL];
+                    float sw[CPL];
+#pragma unroll
+                    for (int cc = 0; cc < CPL; ++cc) w[cc] = lds128(wrow + 512 * cc);
+                    if (scale_bulk) {
+                        const uint32_t srow = SC + uint32_t(r * (kl >> 4)) + uint32_t((lane >> 1) * 2);
+#pragma unroll
+                        for (int cc = 0; cc < CPL; ++cc) sw[cc] = half_bits_to_float(lds16(srow + 32 * cc));
+                    } else {
+                        const uint16_t* srow = p.s + (rb + r) * nb + (ks >> 5) + (lane >> 1);
+#pragma unroll
+                        for (int cc = 0; cc < CPL; ++cc) sw[cc] = half_bits_to_float(__ldg(srow + 16 * cc));
+                    }
+#pragma unroll
+                    for (int m = 0; m < R; ++m) {
+                        if (m < rows) {
+                            if constexpr (MODE == 0) {
+                                DF d[CPL];
+#pragma unroll
+                                for (int cc = 0; cc < CPL; ++cc)
+                                    d[cc] = scaled_pair(__fmul_rn(sw[cc], p2s[cc][m]),
+                                                        fix_dot(w[cc], fx[cc][m]));
+#pragma unroll
+                                for (int cc = 0; cc < CPL; ++cc) part[m] = df_add(part[m], d[cc]);
+                            } else {
+                                float f[CPL];
+#pragma unroll
+                                for (int cc = 0; cc < CPL; ++cc) {
+                                    const int isum = (MODE == 1) ? dot16_i8(w[cc], a1[cc][m])
+                                                                 : dot16_i8x2(w[cc], a1[cc][m], a2[cc][m]);
+                                    f[cc] = float(isum) * (sw[cc] * xdv[cc][m]);
+                                }
+#pragma unroll
+                                for (int cc = 0; cc < CPL; ++cc) part[m] += f[cc];
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < CPL; ++cc) {
+                        const int ch = lane + 32 * cc;
+                        if (ch < cpr) {
+                            const int4 w = lds128(wrow + 512 * cc);
+                            const float sw =
+                                scale_bulk
+                                    ? half_bits_to_float(lds16(SC + uint32_t(r * (kl >> 4)) + uint32_t((ch >> 1) * 2)))
+                                    : half_bits_to_float(__ldg(p.s + (rb + r) * nb + (ks >> 5) + (ch >> 1)));
+#pragma unroll
+                            for (int m = 0; m < R; ++m) {
+                                if (m < rows) {
+                                    if constexpr (MODE == 0) {
+                                        part[m] = df_add(part[m], scaled_pair(__fmul_rn(sw, p2s[cc][m]),
+                                                                              fix_dot(w, fx[cc][m])));
+                                    } else {
+                                        const int isum = (MODE == 1) ? dot16_i8(w, a1[cc][m])
+                                                                     : dot16_i8x2(w, a1[cc][m], a2[cc][m]);
+                                        part[m] = fmaf(float(isum), sw * xdv[cc][m], part[m]);
+                                    }
+                                }
+                            }
+                        }
+                    }
+                }
+                // one warp reduction per row, then the row's running sum
+                const int64_t n = rb + r;
+                A* yrow = yacc + int(n - sb0) * R;
+#pragma unroll
+                for (int m = 0; m < R; ++m) {
+                    if (m < rows) {
+                        const A tot = warp_sum(part[m]);
+                        if (lane == 0) {
+                            const A acc = acc_add(yrow[m], tot);
+                            if (last) {
+                                double val = acc_value(acc);
+                                if constexpr (MODE == 0) val = ldexp(val, s_emax[m] - 30);
+                                if (p.y) {
+                                    if (MODE == 0 && p.out_f64)
+                                        reinterpret_cast<double*>(p.y)[m * N + n] = val;
+                                    else
+                                        reinterpret_cast<float*>(p.y)[m * N + n] = float(val);
+                                }
+                                if constexpr (ARGMAX) {
+                                    if (val > best_v[m] || (val == best_v[m] && n < best_i[m])) {
+                                        best_v[m] = val;
+                                        best_i[m] = n;
+                                    }
+                                }
+                                yrow[m] = acc_zero(A{});
+                            } else {
+                                yrow[m] = acc;
                             }
                         }
                     }
@@ -259,105 +594,55 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
         }
-
-        if (sl == nks - 1) {
-            // Row block complete: reduce each owned row across the warp and emit.
-#pragma unroll
-            for (int jj = 0; jj < RPWMAX; ++jj) {
-                const int j = warp + 8 * jj;
-                if (jj < p.rpw && j < nrows) {
-                    const int64_t n = rb + j;
-#pragma unroll
-                    for (int m = 0; m < R; ++m) {
-                        if (m < rows) {
-                            double v;
-                            if constexpr (MODE == 0) {
-                                v = warp_sum(double(acc[jj][m]) + double(acc_lo[jj][m]));
-                            } else {
-                                v = double(warp_sum(acc[jj][m]));
-                            }
-                            if (lane == 0) {
-                                if (p.y) {
-                                    if (MODE == 0 && p.out_f64)
-                                        reinterpret_cast<double*>(p.y)[m * N + n] = v;
-                                    else
-                                        reinterpret_cast<float*>(p.y)[m * N + n] = float(v);
-                                }
-                                if constexpr (ARGMAX) {
-                                    if (v > best_v[m] || (v == best_v[m] && n < best_i[m])) {
-                                        best_v[m] = v;
-                                        best_i[m] = n;
-                                    }
-                                }
-                            }
-                        }
-                        acc[jj][m] = 0.0f;
-                        acc_lo[jj][m] = 0.0f;
-                    }
-                }
-            }
-        }
     }
 
     if constexpr (ARGMAX) {
-        // Per-CTA candidates, then the last CTA to finish reduces them all.
+        // Per-CTA candidates, then the last CTA to take a ticket reduces the
+        // whole grid's candidates.
         if (lane == 0) {
 #pragma unroll
-            for (int m = 0; m < R; ++m) cand[warp * kGemvMaxRows + m] = {best_v[m], best_i[m]};
+            for (int m = 0; m < R; ++m) cand[warp * R + m] = {best_v[m], best_i[m]};
         }
-        consumer_bar();
+        consumer_bar<kGemvConsumers>();
         ArgmaxCand* gc = reinterpret_cast<ArgmaxCand*>(p.ws + kArgmaxHeader);
         unsigned int* counter = reinterpret_cast<unsigned int*>(p.ws);
-        if (threadIdx.x < rows) {
-            const int m = threadIdx.x;
-            ArgmaxCand b = cand[m];
+        if (tid < rows) {
+            ArgmaxCand b = cand[tid];
             for (int w2 = 1; w2 < kGemvConsumerWarps; ++w2) {
-                const ArgmaxCand o = cand[w2 * kGemvMaxRows + m];
+                const ArgmaxCand o = cand[w2 * R + tid];
                 if (o.v > b.v || (o.v == b.v && o.i < b.i)) b = o;
             }
-            gc[size_t(c) * rows + m] = b;
+            gc[size_t(c) * rows + tid] = b;
             __threadfence();
         }
-        consumer_bar();
-        if (threadIdx.x == 0) s_ticket = atomicAdd(counter, 1u);
-        consumer_bar();
+        consumer_bar<kGemvConsumers>();
+        if (tid == 0) s_ticket = atomicAdd(counter, 1u);
+        consumer_bar<kGemvConsumers>();
         if (s_ticket == unsigned(G - 1)) {
             __threadfence();
-            if (threadIdx.x < rows) {
-                const int m = threadIdx.x;
+            if (tid < rows) {
                 ArgmaxCand b = {-INFINITY, 0x7fffffffffffffffll};
                 for (int c2 = 0; c2 < G; ++c2) {
-                    const volatile ArgmaxCand* src = gc + size_t(c2) * rows + m;
+                    const volatile ArgmaxCand* src = gc + size_t(c2) * rows + tid;
                     const ArgmaxCand o = {src->v, src->i};
                     if (o.v > b.v || (o.v == b.v && o.i < b.i)) b = o;
                 }
-                p.tok[m] = int32_t(b.i);
-                if (p.maxval) p.maxval[m] = b.v;
+                p.tok[tid] = int32_t(b.i);
+                if (p.maxval) p.maxval[tid] = b.v;
             }
-            if (threadIdx.x == 0) *counter = 0u;
+            if (tid == 0) *counter = 0u;
         }
     }
 }
 
-// Stage geometry for a (mode, R) kernel and a given K.
-inline void gemv_geometry(int64_t K, int rpwmax, GemvParams& p) {
-    int rpw = 1;
-    const int64_t per_warp_rows = kGemvStage / (8 * K);
-    if (per_warp_rows >= 2) rpw = int(per_warp_rows >= rpwmax ? rpwmax : per_warp_rows);
-    const int64_t ks_max = kGemvStage / (8 * rpw);
-    p.rpw = rpw;
-    p.KS = int(K <= ks_max ? K : ks_max);
-    p.nks = int((K + p.KS - 1) / p.KS);
-    p.scale_bulk = (K % 256 == 0) ? 1 : 0;
-}
-
-template <int MODE, int R, int RPWMAX, bool ARGMAX>
+template <int MODE, int R, bool ARGMAX>
 cudaError_t launch_gemv_t(const GemvArgs& a, const LaunchCtx& ctx) {
-    auto kern = gemv_kernel<MODE, R, RPWMAX, ARGMAX>;
-    static bool configured = false;  // per process; the attribute is per function
+    auto kern = gemv_kernel<MODE, R, ARGMAX>;
+    constexpr size_t smem = gemv_smem_bytes<MODE, R>();
+    static bool configured = false;  // per process; one device per process
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(gemv_smem_bytes()));
+                                             int(smem));
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -376,7 +661,6 @@ cudaError_t launch_gemv_t(const GemvArgs& a, const LaunchCtx& ctx) {
     p.maxval = a.maxval;
     p.ws = reinterpret_cast<unsigned char*>(a.ws);
     p.err = ctx.dev_err;
-    gemv_geometry(a.K, RPWMAX, p);
 
     int grid = ctx.num_sms;
     if (grid > kMaxGrid) grid = kMaxGrid;
@@ -385,8 +669,8 @@ cudaError_t launch_gemv_t(const GemvArgs& a, const LaunchCtx& ctx) {
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attrs[2];
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kGemvThreads);
-    cfg.dynamicSmemBytes = gemv_smem_bytes();
+    cfg.blockDim = dim3(32 * (gemv_warps<MODE, R>() + 1));
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = ctx.stream;
     cfg.numAttrs = pdl_attrs(ctx, attrs);
     cfg.attrs = attrs;

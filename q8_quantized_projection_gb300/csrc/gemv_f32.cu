@@ -1,16 +1,15 @@
 // gemv_f32.cu -- instantiations of the CUDA-core projection for activation
-// mode 0 (see gemv.cuh), split per mode so the build compiles in parallel.
-#include "gemv.cuh"
+// mode 0: the decode kernel (gemv_row.cuh) for 1-2 rows, the slice-major
+// kernel (gemv.cuh) for more.  One file per mode so the build runs in parallel.
+#include "gemv_row.cuh"
 
 namespace q8 {
 
 template <bool ARGMAX>
 static cudaError_t dispatch_rows(const GemvArgs& a, const LaunchCtx& ctx) {
-    if (a.rows <= 1) return launch_gemv_t<0, 1, 4, ARGMAX>(a, ctx);
-    if (a.rows <= 2) return launch_gemv_t<0, 2, 4, ARGMAX>(a, ctx);
-    if (a.rows <= 4) return launch_gemv_t<0, 4, 2, ARGMAX>(a, ctx);
-    if (a.rows <= 8) return launch_gemv_t<0, 8, 1, ARGMAX>(a, ctx);
-    return launch_gemv_t<0, 16, 1, ARGMAX>(a, ctx);
+    if (a.rows <= 1) return launch_gemv_row_t<0, 1, ARGMAX>(a, ctx);
+    if (a.rows <= 2) return launch_gemv_row_t<0, 2, ARGMAX>(a, ctx);
+    return launch_gemv_t<0, 4, ARGMAX>(a, ctx);
 }
 
 cudaError_t launch_gemv_mode0(const GemvArgs& a, const LaunchCtx& ctx) {

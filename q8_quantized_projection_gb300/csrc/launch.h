@@ -42,10 +42,17 @@ struct GemvArgs {
     int32_t* tok;
     double* maxval;
     void* ws;
+    // producer fused into the projection (decode step, one row): when h is
+    // set, act/xd are ignored and the kernel runs RMSNorm -> quant itself
+    const float* h;
+    const float* gain;
+    float eps;
 };
 
+// Largest K the decode kernel quantises in its own shared memory.
+constexpr int64_t kFusedMaxK = 16384;
+
 int gemv_max_rows(int mode);
-cudaError_t launch_gemv(const GemvArgs& a, const LaunchCtx& ctx);
 
 cudaError_t launch_debug_dots(int mode, const int8_t* q, const void* xq, int64_t N, int64_t K,
                               int64_t rows, int32_t* isum, const LaunchCtx& ctx);

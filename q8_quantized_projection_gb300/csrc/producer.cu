@@ -1,18 +1,8 @@
-// producer.cu -- weight pack, the activation producer (RMSNorm -> quant) and
-// the debug block-dot kernel.
-//
-// The producer is tiny in bytes but sits on the decode step's critical path,
-// so it is spread wide: a row's K is split over a thread-block cluster (up to
-// 16 CTAs), each CTA folds its slice's sum of squares in f64, the partial sums
-// are exchanged through distributed shared memory and every CTA adds them in
-// rank order (so all agree bit for bit), then each CTA normalises and
-// quantises its own blocks, one warp per 32-value block.
-#include <cooperative_groups.h>
-
+// producer.cu -- weight pack, the stand-alone activation producer (RMSNorm ->
+// quant, one CTA per row) and the debug block-dot kernel.
 #include "common.cuh"
 #include "launch.h"
-
-namespace cg = cooperative_groups;
+#include "rmsnorm.cuh"
 
 namespace q8 {
 
@@ -86,128 +76,55 @@ struct AqParams {
     float* xd;
 };
 
+// One CTA of kProdThreads threads per activation row (rmsnorm.cuh holds the
+// arithmetic, shared with the decode projection's fused producer).
 template <int MODE, bool NORM>
-__global__ void __launch_bounds__(256) act_quant_kernel(const AqParams p) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int C = gridDim.x, c = blockIdx.x;
-    const int64_t m = blockIdx.y;
+__global__ void __launch_bounds__(kProdThreads) act_quant_kernel(const AqParams p) {
+    __shared__ double s_warp[kProdWarps];
+    __shared__ float s_rf;
+    const int tid = threadIdx.x;
+    const int64_t m = blockIdx.x;
     const int64_t K = p.K, nb = K / Q8_QK;
-    const int64_t bpc = (nb + C - 1) / C;
-    const int64_t b0 = int64_t(c) * bpc, b1 = min(nb, b0 + bpc);
     const float* h = p.h + m * K;
 
     pdl_wait();
     pdl_launch_dependents();
 
     float rf = 1.0f;
-    if constexpr (NORM) {
-        __shared__ double warp_ss[8];
-        __shared__ double cta_ss;
-        __shared__ float s_rf;
-        double ss = 0.0;
-        for (int64_t b = b0 + warp; b < b1; b += 8) {
-            const double v = double(h[b * Q8_QK + lane]);
-            ss = fma(v, v, ss);  // v*v is exact in f64
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) warp_ss[warp] = ss;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            double t = 0.0;
-            for (int w2 = 0; w2 < 8; ++w2) t += warp_ss[w2];
-            cta_ss = t;
-        }
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        if (threadIdx.x == 0) {
-            double tot = 0.0;
-            for (int r = 0; r < C; ++r) tot += *cluster.map_shared_rank(&cta_ss, r);
-            const double mean = __ddiv_rn(tot, double(K));
-            const double r = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(mean, double(p.eps))));
-            s_rf = __double2float_rn(r);
-        }
-        cluster.sync();  // no CTA leaves while a peer still reads its partial
-        rf = s_rf;
-    }
-
-    for (int64_t b = b0 + warp; b < b1; b += 8) {
-        const int64_t k = b * Q8_QK + lane;
-        float x = h[k];
-        if constexpr (NORM) {
-            x = __fmul_rn(x, rf);
-            if (p.gain) x = __fmul_rn(x, p.gain[k]);
-        }
-        if constexpr (MODE == 0) {
-            reinterpret_cast<float*>(p.out)[m * K + k] = x;
-        } else {
-            float a = fabsf(x);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-            const float lim = (MODE == 1) ? 127.0f : 8191.0f;
-            const float d = __fdiv_rn(a, lim);
-            const int code = quantize_code(x, d, lim);
-            int8_t* out = reinterpret_cast<int8_t*>(p.out);
-            if constexpr (MODE == 1) {
-                out[m * K + k] = static_cast<int8_t>(code);
-            } else {
-                const int lo = ((code + 64) & 127) - 64;  // Euclidean residue, centred
-                const int hi = (code - lo) >> 7;          // exact: code - lo is a multiple of 128
-                out[m * K + k] = static_cast<int8_t>(hi);
-                out[p.rows * K + m * K + k] = static_cast<int8_t>(lo);
-            }
-            if (lane == 0) p.xd[m * nb + b] = d;
-        }
-    }
+    if constexpr (NORM) rf = row_rms_scale(h, K, p.eps, tid, 1, s_warp, &s_rf);
+    void* out;
+    if constexpr (MODE == 0)
+        out = reinterpret_cast<float*>(p.out) + m * K;
+    else
+        out = reinterpret_cast<int8_t*>(p.out) + m * K;
+    row_quantize<MODE, NORM>(h, p.gain, rf, K, tid, out, p.rows * K,
+                             MODE == 0 ? nullptr : p.xd + m * nb);
 }
 
 template <int MODE, bool NORM>
-static cudaError_t launch_aq_t(const AqParams& p, int C, const LaunchCtx& ctx) {
-    auto kern = act_quant_kernel<MODE, NORM>;
+static cudaError_t launch_aq_t(const AqParams& p, const LaunchCtx& ctx) {
     cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attrs[2];
-    int na = pdl_attrs(ctx, attrs);
-    if (NORM) {
-        static bool configured = false;
-        if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
-            configured = true;
-        }
-        attrs[na].id = cudaLaunchAttributeClusterDimension;
-        attrs[na].val.clusterDim.x = unsigned(C);
-        attrs[na].val.clusterDim.y = 1;
-        attrs[na].val.clusterDim.z = 1;
-        ++na;
-    }
-    cfg.gridDim = dim3(unsigned(C), unsigned(p.rows));
-    cfg.blockDim = dim3(256);
+    cudaLaunchAttribute attrs[1];
+    cfg.gridDim = dim3(unsigned(p.rows));
+    cfg.blockDim = dim3(kProdThreads);
     cfg.stream = ctx.stream;
-    cfg.numAttrs = unsigned(na);
+    cfg.numAttrs = pdl_attrs(ctx, attrs);
     cfg.attrs = attrs;
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    return cudaLaunchKernelEx(&cfg, act_quant_kernel<MODE, NORM>, p);
 }
 
 cudaError_t launch_act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
                              const float* gain, float eps, void* xq, float* xd,
                              const LaunchCtx& ctx) {
     AqParams p{h, gain, eps, rows, K, xq, xd};
-    const int64_t nb = K / Q8_QK;
-    int C;
     if (norm) {
-        C = int(nb < 16 ? nb : 16);  // cluster over the row (16 = non-portable maximum)
-    } else {
-        const int64_t c = (nb + 15) / 16;
-        C = int(c > 64 ? 64 : c);
+        if (mode == 0) return launch_aq_t<0, true>(p, ctx);
+        if (mode == 1) return launch_aq_t<1, true>(p, ctx);
+        return launch_aq_t<2, true>(p, ctx);
     }
-    if (norm) {
-        if (mode == 0) return launch_aq_t<0, true>(p, C, ctx);
-        if (mode == 1) return launch_aq_t<1, true>(p, C, ctx);
-        return launch_aq_t<2, true>(p, C, ctx);
-    }
-    if (mode == 0) return launch_aq_t<0, false>(p, C, ctx);
-    if (mode == 1) return launch_aq_t<1, false>(p, C, ctx);
-    return launch_aq_t<2, false>(p, C, ctx);
+    if (mode == 0) return launch_aq_t<0, false>(p, ctx);
+    if (mode == 1) return launch_aq_t<1, false>(p, ctx);
+    return launch_aq_t<2, false>(p, ctx);
 }
 
 // ----------------------------------------------------------- debug block dots

@@ -61,15 +61,17 @@ def gain(rng: np.random.Generator, k: int):
 
 
 def head_activations(rng: np.random.Generator, rows: int, k: int):
-    """Rows 0..7 are N(0,1); row m >= 8 is row m-8 plus 0.1 N(0,1) noise."""
-    base = rng.standard_normal(size=(min(rows, 8), k), dtype=np.float32)
+    """Activation rows for the LM head: rows 0..7 are N(0,1); row m >= 8 is
+    row m-8 plus 0.1 N(0,1) noise.  Always draws the eight base rows, so the
+    planted head rows exist whatever `rows` is; returns (h [rows, k], base [8, k])."""
+    base = rng.standard_normal(size=(8, k), dtype=np.float32)
     out = np.empty((rows, k), dtype=np.float32)
     for m in range(rows):
         if m < 8:
             out[m] = base[m]
         else:
             out[m] = out[m - 8] + np.float32(0.1) * rng.standard_normal(size=(k,), dtype=np.float32)
-    return out
+    return out, base
 
 
 def planted_positions(rng: np.random.Generator, n: int, count: int = 8):
@@ -84,11 +86,21 @@ def planted_positions(rng: np.random.Generator, n: int, count: int = 8):
     return np.array(pos, dtype=np.int64)
 
 
-def plant_head_rows(q: np.ndarray, s: np.ndarray, h: np.ndarray, positions: np.ndarray):
-    """Write the planted rows in place: quants 127*sign(h_j), scales fp16(0.02/127)."""
+def plant_head_rows(q: np.ndarray, s: np.ndarray, base: np.ndarray, positions: np.ndarray):
+    """Write the planted rows in place: quants 127*sign(base_j), scales fp16(0.02/127)."""
     s_planted = np.float16(0.02 / 127.0).view(np.uint16)
     for j, p in enumerate(positions):
-        sign = np.where(h[j] >= 0, 127, -127).astype(np.int8)
-        q[p] = sign
+        q[p] = np.where(base[j] >= 0, 127, -127).astype(np.int8)
         s[p] = s_planted
     return q, s
+
+
+def planted_head(seed: int, n: int, k: int, rows: int):
+    """A Q8_0 head with 8 planted rows and its activation rows.
+    Returns (q, s, h, positions); the winner of row m is positions[m % 8]."""
+    rng = rng_for(seed)
+    q, s = q8_weights(rng, n, k)
+    h, base = head_activations(rng, rows, k)
+    pos = planted_positions(rng, n)
+    plant_head_rows(q, s, base, pos)
+    return q, s, h, pos

@@ -349,14 +349,10 @@ def test_argmax_hand_vectors(orc):
 
 
 def test_planted_head_margin(orc):
-    rng = np.random.default_rng(9)
     n, k, rows = 3000, 256, 16
-    q, s = synth.q8_weights(rng, n, k)
-    h = synth.head_activations(rng, rows, k)
-    pos = synth.planted_positions(rng, n)
-    synth.plant_head_rows(q, s, h, pos)
+    q, s, h, pos = synth.planted_head(9, n, k, rows)
     x, _ = orc.rmsnorm(h)
-    for mode in ("f32", "i8"):
+    for mode in ("f32", "i8", "i8x2"):
         tok, best, y = orc.head_argmax(mode, q, s, orc.quantize(mode, x))
         assert np.array_equal(tok, pos[np.arange(rows) % 8])
         top2 = np.sort(y, axis=1)[:, -2]

@@ -142,7 +142,8 @@ def test_proj_deterministic_and_zero(mode):
 # ----------------------------------------------------------- fused producer
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("n,k,rows", [(300, 4096, 1), (100, 14336, 2), (64, 1024, 16)])
+@pytest.mark.parametrize("n,k,rows", [(300, 4096, 1), (100, 14336, 2), (64, 1024, 16),
+                                      (50, 16384, 1), (40, 16416, 1), (37, 96, 1), (7, 14336, 1)])
 def test_fused_matches_oracle_and_composition(mode, n, k, rows):
     rng = np.random.default_rng(5 + n + k + rows)
     q, s = synth.q8_weights(rng, n, k)
@@ -168,12 +169,7 @@ def test_fused_matches_oracle_and_composition(mode, n, k, rows):
 # ------------------------------------------------------------- LM head
 
 def _planted_head(n, k, rows, seed):
-    rng = np.random.default_rng(seed)
-    q, s = synth.q8_weights(rng, n, k)
-    h = synth.head_activations(rng, rows, k)
-    pos = synth.planted_positions(rng, n)
-    synth.plant_head_rows(q, s, h, pos)
-    return q, s, h, pos
+    return synth.planted_head(seed, n, k, rows)
 
 
 @pytest.mark.parametrize("mode", MODES)
