@@ -179,6 +179,28 @@ q8_status head_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, i
 size_t head_argmax_workspace(int64_t rows);
 
 /*
+ * head_argmax without a workspace, for callers that cannot allocate device
+ * memory: code that runs where a framework's allocator owns all device memory
+ * (raw cudaMalloc is forbidden or would fragment its pool), or a serving loop
+ * that must not allocate once it is running.  The pages describing the method
+ * have no counterpart to this call; it exists only for those callers.
+ *   Same arguments and results as head_argmax, minus the workspace.  The
+ *   scratch is a fixed device array inside the library,
+ *   head_argmax_noalloc_scratch_bytes() bytes (about 256 KB), which every GPU
+ *   that loads the library keeps until the process exits; it covers every
+ *   rows <= Q8_MAX_ROWS, and larger rows return Q8_ERR_SHAPE.
+ *   The first call on a device (with that device current) looks up the
+ *   array's device address, so make that first call before any stream
+ *   capture.  Each call clears the array's counter on `stream` first.  All
+ *   calls share the one array: calls that overlap on the GPU race and give
+ *   undefined results.  No allocation happens in any call.
+ */
+q8_status head_argmax_noalloc(int mode, const int8_t* q, const uint16_t* s, int64_t N,
+                              int64_t K, const void* xq, const float* xd, int64_t rows,
+                              int32_t* tok, double* maxval, void* logits, void* stream);
+size_t head_argmax_noalloc_scratch_bytes(void);
+
+/*
  * Debug: the per-block int32 dot products the projections fold with their
  * scales (modes Q8_ACT_I8 / Q8_ACT_I8X2), isum int32 [rows][N][K/32].
  * path 0 runs the CUDA-core inner product the GEMV kernels use, path 1 the

@@ -41,6 +41,9 @@ SIGNATURES = {
                            _vp]),
     "head_argmax_workspace": (_sz, [_i64]),
     "q8_debug_block_dots": (_int, [_int, _vp, _vp, _i64, _i64, _i64, _vp, _int, _vp]),
+    "head_argmax_noalloc": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp,
+                                   _vp]),
+    "head_argmax_noalloc_scratch_bytes": (_sz, []),
 }
 
 
@@ -156,6 +159,14 @@ def head_argmax(mode, q, s, xq, xd, rows, tok, workspace, maxval=None, logits=No
                               _ptr(tok), _ptr(maxval), _ptr(logits), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream)),
            "head_argmax")
+
+
+def head_argmax_noalloc(mode, q, s, xq, xd, rows, tok, maxval=None, logits=None, stream=None):
+    """head_argmax with the library's own fixed scratch (no workspace, no allocation)."""
+    n, k = q.shape
+    _check(load().head_argmax_noalloc(_mode(mode), _ptr(q), _ptr(s), n, k, _ptr(xq), _ptr(xd),
+                                      rows, _ptr(tok), _ptr(maxval), _ptr(logits),
+                                      _stream(stream)), "head_argmax_noalloc")
 
 
 def q8_debug_block_dots(mode, q, xq, rows, isum, path=0, stream=None):
