@@ -117,6 +117,17 @@ q8_status run_projection(int mode, const int8_t* q, const uint16_t* s, int64_t N
     return Q8_OK;
 }
 
+// Plain projection of a quantised activation: the tensor-core chunk kernel from
+// kChunkMinRows rows on (int8 modes, K % 256 == 0), the CUDA-core kernels else.
+q8_status project_dispatch(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                           const void* xq, const float* xd, int64_t rows, void* y, int out_f64,
+                           const LaunchCtx& ctx) {
+    if (!out_f64 && rows >= kChunkMinRows && chunk_supported(mode, N, K, rows))
+        return launched(launch_chunk(mode, q, s, N, K, xq, xd, rows, static_cast<float*>(y), ctx));
+    return run_projection(mode, q, s, N, K, xq, xd, rows, y, out_f64, nullptr, nullptr, nullptr,
+                          ctx);
+}
+
 q8_status check_proj_args(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                           const void* xq, const float* xd, int64_t rows, const void* y) {
     if (!valid_mode(mode)) return Q8_ERR_MODE;
@@ -208,8 +219,7 @@ q8_status q8_proj(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64
     if (out_f64 && mode != Q8_ACT_F32) return Q8_ERR_MODE;
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
-    return run_projection(mode, q, s, N, K, xq, xd, rows, y, out_f64 ? 1 : 0, nullptr, nullptr,
-                          nullptr, ctx);
+    return project_dispatch(mode, q, s, N, K, xq, xd, rows, y, out_f64 ? 1 : 0, ctx);
 }
 
 q8_status q8_proj_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
@@ -218,7 +228,7 @@ q8_status q8_proj_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N,
     if (st != Q8_OK) return st;
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
-    return run_projection(mode, q, s, N, K, xq, xd, T, y, 0, nullptr, nullptr, nullptr, ctx);
+    return project_dispatch(mode, q, s, N, K, xq, xd, T, y, 0, ctx);
 }
 
 size_t q8_proj_fused_workspace(int mode, int64_t rows, int64_t K) {
@@ -261,8 +271,8 @@ q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N,
     float* xd = reinterpret_cast<float*>(act + round_up(act_bytes(mode, rows, K), 256));
     cudaError_t e = launch_act_quant(mode, h, rows, K, 1, gain, eps, act, xd, ctx);
     if (e != cudaSuccess) return cuda_fail(e);
-    return run_projection(mode, q, s, N, K, act, mode == Q8_ACT_F32 ? nullptr : xd, rows, y,
-                          out_f64 ? 1 : 0, nullptr, nullptr, nullptr, ctx);
+    return project_dispatch(mode, q, s, N, K, act, mode == Q8_ACT_F32 ? nullptr : xd, rows, y,
+                            out_f64 ? 1 : 0, ctx);
 }
 
 size_t head_argmax_workspace(int64_t rows) {
@@ -300,9 +310,13 @@ q8_status q8_debug_block_dots(int mode, const int8_t* q, const void* xq, int64_t
     if (rows < 1 || rows > Q8_MAX_ROWS) return Q8_ERR_SHAPE;
     if (rows * N * (K / Q8_QK) > (int64_t(1) << 26)) return Q8_ERR_SHAPE;
     if (!aligned16(q) || !aligned16(xq) || !aligned16(isum)) return Q8_ERR_ALIGN;
-    if (path != 0) return Q8_ERR_UNSUPPORTED;
+    if (path != 0 && path != 1) return Q8_ERR_ARG;
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
+    if (path == 1) {
+        if (!chunk_supported(mode, N, K, rows)) return Q8_ERR_UNSUPPORTED;
+        return launched(launch_chunk_debug(mode, q, N, K, xq, rows, isum, ctx));
+    }
     return launched(launch_debug_dots(mode, q, xq, N, K, rows, isum, ctx));
 }
 

@@ -54,6 +54,15 @@ constexpr int64_t kFusedMaxK = 16384;
 
 int gemv_max_rows(int mode);
 
+// tensor-core chunk path (chunk.cu): modes 1 and 2, K % 256 == 0
+bool chunk_supported(int mode, int64_t N, int64_t K, int64_t T);
+cudaError_t launch_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                         const void* xq, const float* xd, int64_t T, float* y, const LaunchCtx& ctx);
+cudaError_t launch_chunk_debug(int mode, const int8_t* q, int64_t N, int64_t K, const void* xq,
+                               int64_t T, int32_t* isum, const LaunchCtx& ctx);
+// activation rows from which projections run on the tensor cores
+constexpr int64_t kChunkMinRows = 16;
+
 cudaError_t launch_debug_dots(int mode, const int8_t* q, const void* xq, int64_t N, int64_t K,
                               int64_t rows, int32_t* isum, const LaunchCtx& ctx);
 

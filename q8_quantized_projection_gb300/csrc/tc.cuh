@@ -1,0 +1,141 @@
+// tc.cuh -- 5th-generation tensor-core (tcgen05) helpers for sm_103a, inline PTX.
+//
+// Operand tiles live in shared memory in the K-major, no-swizzle canonical
+// layout: "core matrices" of 8 rows x 16 bytes (8 f16 along K), each stored as
+// 128 contiguous bytes.  For a tile of R rows by 32 f16 along K (one Q8_0
+// block) the core matrix (row group g = r/8, K chunk c = k/8) sits at byte
+// g*512 + c*128, and inside it row r%8 at (r%8)*16, element k%8 at 2*(k%8).
+// So the leading (K) byte offset between core matrices is 128 and the stride
+// (row-group) byte offset is 512.  One MMA consumes K = 16, i.e. two core
+// matrices along K; the second half of a block starts 256 bytes later.
+//
+// Accumulators live in tensor memory (TMEM): 128 lanes x up to 512 columns of
+// 32 bits per SM; lane i of an M = 128 accumulator is row i, column j is N
+// index j.  A warp may only touch the 32 lanes of its quadrant (warp id % 4).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace q8 {
+
+// ------------------------------------------------------- descriptors (host+device)
+
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets (all >> 4), version 1 (sm_100 family), no swizzle.
+__host__ __device__ constexpr uint64_t smem_desc_kmajor(uint32_t saddr, uint32_t lbo,
+                                                        uint32_t sbo) {
+    return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+           (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D f32, A and B f16, both
+// K-major, M rows by N columns.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4)                       // D format: f32
+           | (0u << 7) | (0u << 10)        // A, B format: f16
+           | (0u << 15) | (0u << 16)       // A, B K-major
+           | (uint32_t(N >> 3) << 17)      // N / 8
+           | (uint32_t(M >> 4) << 24);     // M / 16
+}
+
+// Byte offset of element (r, k) in a [rows][32 f16] K-major no-swizzle tile.
+__host__ __device__ constexpr uint32_t tile_offset(int r, int k) {
+    return uint32_t((r >> 3) * 512 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// ------------------------------------------------------------ TMEM management
+
+// One whole warp allocates `ncols` TMEM columns (a power of two >= 32); the
+// base address is written to shared memory at `dst`.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Generic-proxy shared-memory writes become visible to the tensor core.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- the MMA
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by a single thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// Arrives once on the mbarrier when all MMAs this thread issued so far finish.
+__device__ __forceinline__ void mma_commit(uint32_t mbar_smem) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            mbar_smem)
+        : "memory");
+}
+
+// ------------------------------------------------------------- TMEM -> registers
+
+// 32 lanes x 32 consecutive columns: thread i of the warp gets lane (base+i),
+// columns col..col+31.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// --------------------------------------------------------- int8 -> f16 pairs
+
+// Four signed bytes of w -> two f16x2 words (bytes 0,1 and bytes 2,3), exact:
+// each byte b maps to the f16 1024 + (b + 128), then 1152 is subtracted.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;           // b + 128 as unsigned bytes
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x7170;" : "=r"(a) : "r"(u), "r"(0x64646464u));  // bytes 0,1
+    asm("prmt.b32 %0, %1, %2, 0x7372;" : "=r"(b) : "r"(u), "r"(0x64646464u));  // bytes 2,3
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&ha);
+    hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+}  // namespace q8

@@ -258,3 +258,66 @@ def test_head_full_size(mode, rows):
     rowsel = np.arange(rows)
     check_close(mode, host(mx), y_o[rowsel, rowsel], norm[rowsel, rowsel], out_f64=True,
                 what="head max value")
+
+
+# ------------------------------------------------------- tensor-core chunk path
+
+@pytest.mark.parametrize("mode", ["i8", "i8x2"])
+@pytest.mark.parametrize("n,k,t", [(300, 1024, 16), (129, 4096, 33), (257, 1024, 128),
+                                   (130, 4096, 129), (64, 14336, 48), (1000, 1024, 256)])
+def test_chunk_tensor_core_parity(mode, n, k, t):
+    rng = np.random.default_rng(3000 + n + k + t)
+    q, s = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, t, k)
+    act = orc.quantize(mode, x)
+    y_o, norm = orc.project(mode, q, s, act)
+    qd, sd = upload_weights(q, s)
+    xq, xd = upload_act(mode, act, t, k)
+    tt = torch()
+    y = tt.empty((t, n), dtype=tt.float32, device="cuda")
+    native.q8_proj_chunk(mode, qd, sd, xq, xd, t, y)
+    check_close(mode, host(y), y_o, norm, what=f"chunk {mode} {n}x{k} T={t}")
+    y2 = tt.empty_like(y)
+    native.q8_proj_chunk(mode, qd, sd, xq, xd, t, y2)
+    assert np.array_equal(host(y).view(np.uint32), host(y2).view(np.uint32))
+
+
+@pytest.mark.parametrize("mode", ["i8", "i8x2"])
+@pytest.mark.parametrize("n,k,t", [(129, 1024, 16), (64, 4096, 130)])
+def test_chunk_block_dots_exact(mode, n, k, t):
+    """The tensor-core per-block accumulators are the exact integer block dots."""
+    rng = np.random.default_rng(4000 + n + k + t)
+    q, _ = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, t, k)
+    act = orc.quantize(mode, x)
+    isum_o = orc.block_dots(q, act[0], act[1] if mode == "i8x2" else None)
+    tt = torch()
+    xq, _ = upload_act(mode, act, t, k)
+    isum = tt.empty((t, n, k // QK), dtype=tt.int32, device="cuda")
+    native.q8_debug_block_dots(mode, dev(q), xq, t, isum, path=1)
+    assert np.array_equal(host(isum), isum_o)
+
+
+@pytest.mark.parametrize("mode", ["i8", "i8x2"])
+def test_prefill_chunk_full_size_sampled(mode):
+    """A 256-row prefill chunk through the d=4096 layer's matrices at full size,
+    each row RMSNorm(N(0,1)) quantized in the producer; sampled output columns
+    are checked against the oracle."""
+    tt = torch()
+    rng = np.random.default_rng(5)
+    T = 256
+    for name, n, k in synth.LAYER_D4096:
+        q, s = synth.q8_weights(rng, n, k)
+        h = synth.activations(rng, T, k)
+        qd, sd = upload_weights(q, s)
+        xq, xd = native.activation_buffers(mode, T, k)
+        native.act_quant(mode, dev(h), xq, xd, norm=True)
+        y = tt.empty((T, n), dtype=tt.float32, device="cuda")
+        native.q8_proj_chunk(mode, qd, sd, xq, xd, T, y)
+        idx = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 64)]))
+        x, _ = orc.rmsnorm(h)
+        act = orc.quantize(mode, x)
+        for a, b in zip(act_to_numpy(mode, xq, xd), act):
+            assert np.array_equal(a, b)
+        y_o, norm = orc.project(mode, q[idx], s[idx], act)
+        check_close(mode, host(y)[:, idx], y_o, norm, what=f"{name} {mode} T={T}")
