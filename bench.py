@@ -312,6 +312,21 @@ def run_ours(args, world, rank, local):
     if args.case:
         # one projection's kernel, warmup+steps eager launches (a profiler case)
         parts = args.case.split(":")
+        if parts[0] == "chunk":
+            # a prefill chunk: chunk:MODE:PROJ:T
+            mode, proj, T = parts[1], parts[2], int(parts[3])
+            p = [nm for nm, _, _ in synth.LAYER_D4096].index(proj)
+            n, k = synth.LAYER_D4096[p][1], synth.LAYER_D4096[p][2]
+            h = torch.from_numpy(synth.activations(synth.rng_for(3), T, k)).to(dev)
+            xq, xd = native.activation_buffers(mode, T, k, device=dev)
+            native.act_quant(mode, h, xq, xd, norm=True)
+            y = torch.empty((T, n), dtype=torch.float32, device=dev)
+            for i in range(args.warmup + args.steps):
+                native.q8_proj_chunk(mode, Q[i % COPIES][p], S[i % COPIES][p], xq, xd, T, y)
+            torch.cuda.synchronize(dev)
+            if rank == 0:
+                print(json.dumps({"case": args.case, "launches": args.warmup + args.steps}))
+            return
         mode, proj = parts[0], parts[1]
         fused = len(parts) > 2 and parts[2] == "fused"
         p = [nm for nm, _, _ in synth.LAYER_D4096].index(proj)
@@ -438,6 +453,8 @@ def run_ours(args, world, rank, local):
                    "copy, then stream sync"}
     launches_per_fused = 2
 
+    sweeps = {} if args.no_sweeps else run_sweeps(native, torch, dev, capture, timed, Q, S)
+
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base = cpu_baseline(mats, hs, budget_s=args.cpu_budget)
@@ -457,8 +474,120 @@ def run_ours(args, world, rank, local):
                "rows_per_s": round(world * len(MODES) * 4 / (ms * 1e-3), 1),
                "modes": per_mode, "roofline": roofline, "cpu_baseline": base, "e2e": e2e,
                "gpu_launches": args.steps * len(MODES) * 4 * launches_per_fused,
-               "clocks": clocks}
+               "clocks": clocks, "sweeps": sweeps}
         print(json.dumps(out), flush=True)
+
+
+def run_sweeps(native, torch, dev, capture, timed, Q, S):
+    """The other workload configurations, each graph-replayed with rotating
+    inputs larger than L2: the 1024x1024 GEMV, batched decode, prefill chunks
+    and the LM head with its arg-max."""
+    out = {}
+    rng = synth.rng_for(7)
+
+    def per_call_us(body, calls, nrep=10):
+        graphs = capture(body)
+        for i in range(3):
+            graphs[i % COPIES].replay()
+        ms = timed(graphs, nrep)
+        del graphs
+        return ms * 1e3 / calls
+
+    # 1024 x 1024, rows = 1: launch-latency bound; 128 rotating copies (142 MB)
+    q0, s0 = synth.q8_weights(rng, 1024, 1024)
+    nrot = 128
+    Q0 = [torch.from_numpy(q0).to(dev) for _ in range(nrot)]
+    S0 = [torch.from_numpy(s0.view(np.int16)).to(dev) for _ in range(nrot)]
+    h0 = torch.from_numpy(synth.activations(rng, 1, 1024)).to(dev)
+    y0 = torch.empty((1, 1024), dtype=torch.float32, device=dev)
+    cfg0 = {}
+    for m in MODES:
+        ws = torch.empty(native.q8_proj_fused_workspace(m, 1, 1024), dtype=torch.uint8, device=dev)
+
+        def body(c, m=m, ws=ws):
+            for i in range(nrot // COPIES):
+                j = c * (nrot // COPIES) + i
+                native.q8_proj_fused(m, Q0[j], S0[j], h0, y0, ws)
+        us = per_call_us(body, nrot // COPIES)
+        cfg0[m] = {"us_per_call": round(us, 2),
+                   "GB/s": round(weight_bytes(1024, 1024) / (us * 1e-6) / 1e9, 1)}
+    out["gemv_1024x1024_rows1"] = cfg0
+    del Q0, S0
+
+    # batched decode: B stacked rows, each weight read once per batch
+    batch = {}
+    for m in ("i8", "i8x2"):
+        batch[m] = {}
+        for B in (1, 2, 4, 8, 16, 32, 64):
+            acts = []
+            for p, (_, n, k) in enumerate(synth.LAYER_D4096):
+                h = torch.from_numpy(synth.activations(rng, B, k)).to(dev)
+                xq, xd = native.activation_buffers(m, B, k, device=dev)
+                native.act_quant(m, h, xq, xd, norm=True)
+                acts.append((xq, xd, torch.empty((B, n), dtype=torch.float32, device=dev)))
+
+            def body(c, m=m, B=B, acts=acts):
+                for p in range(4):
+                    xq, xd, y = acts[p]
+                    native.q8_proj(m, Q[c][p], S[c][p], xq, xd, B, y)
+            us = per_call_us(body, 1)
+            batch[m][str(B)] = {"us_per_layer": round(us, 2),
+                                "GB/s": round(LAYER_BYTES / (us * 1e-6) / 1e9, 1),
+                                "rows_per_s": round(B * 4 / (us * 1e-6), 1)}
+    out["batched_decode_d4096"] = batch
+
+    # prefill chunks: T rows, producer (RMSNorm -> quant) then the chunk projection
+    chunk = {}
+    flops_row = 2.0 * sum(n * k for _, n, k in synth.LAYER_D4096)
+    for m in ("i8", "i8x2"):
+        chunk[m] = {}
+        for T in (2, 4, 8, 16, 32, 64, 128, 256):
+            bufs = []
+            for p, (_, n, k) in enumerate(synth.LAYER_D4096):
+                h = torch.from_numpy(synth.activations(rng, T, k)).to(dev)
+                xq, xd = native.activation_buffers(m, T, k, device=dev)
+                bufs.append((h, xq, xd, torch.empty((T, n), dtype=torch.float32, device=dev)))
+
+            def body(c, m=m, T=T, bufs=bufs):
+                for p in range(4):
+                    h, xq, xd, y = bufs[p]
+                    native.act_quant(m, h, xq, xd, norm=True)
+                    native.q8_proj_chunk(m, Q[c][p], S[c][p], xq, xd, T, y)
+            us = per_call_us(body, 1)
+            chunk[m][str(T)] = {"us_per_layer": round(us, 2),
+                                "GB/s": round(LAYER_BYTES / (us * 1e-6) / 1e9, 1),
+                                "tokens_per_s": round(T / (us * 1e-6), 1),
+                                "TFLOP/s": round(flops_row * T / (us * 1e-6) / 1e12, 1)}
+    out["prefill_chunk_d4096"] = chunk
+
+    # LM head 128256 x 4096 with planted rows, fused arg-max
+    nh, kh = synth.HEAD_SHAPE
+    qh, sh, hh16, pos = synth.planted_head(4, nh, kh, 16)
+    QH = [torch.from_numpy(qh).to(dev)]
+    SH = [torch.from_numpy(sh.view(np.int16)).to(dev)]
+    QH.append(QH[0].clone())
+    SH.append(SH[0].clone())
+    head = {}
+    for m in ("i8", "f32"):
+        head[m] = {}
+        for rows in (1, 16):
+            h = torch.from_numpy(np.ascontiguousarray(hh16[:rows])).to(dev)
+            xq, xd = native.activation_buffers(m, rows, kh, device=dev)
+            native.act_quant(m, h, xq, xd, norm=True)
+            tok = torch.empty(rows, dtype=torch.int32, device=dev)
+            ws = native.argmax_workspace(rows, device=dev)
+
+            def body(c, m=m, rows=rows, xq=xq, xd=xd, tok=tok, ws=ws):
+                native.head_argmax(m, QH[c], SH[c], xq, xd, rows, tok, ws)
+            us = per_call_us(body, 1)
+            ok = bool(np.array_equal(tok.cpu().numpy(), pos[np.arange(rows) % 8]))
+            head[m][str(rows)] = {"us": round(us, 2),
+                                  "GB/s": round(weight_bytes(nh, kh) / (us * 1e-6) / 1e9, 1),
+                                  "tokens_per_s": round(rows / (us * 1e-6), 1),
+                                  "argmax_matches_planted": ok}
+    out["lm_head_128256x4096"] = head
+    del QH, SH
+    return out
 
 
 def main():
@@ -469,6 +598,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweeps", action="store_true",
+                    help="skip the other workload configurations")
     ap.add_argument("--quick", action="store_true",
                     help="warm-up and timed steps only (for launch lists under a profiler)")
     ap.add_argument("--case", default=None,
