@@ -482,6 +482,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps<MODE, R>() + 1), 1)
         }
 
         if (ok) ok = mbar_wait(&full[slot], it.phase, p.err);
+        ok = __all_sync(0xffffffffu, ok);   // a timeout ends the whole warp's work together
         if (ok) {
             const uint32_t W = smem_u32(wring) + uint32_t(slot * g.stage_bytes);
             const uint32_t SC = smem_u32(sring) + uint32_t(slot * (g.stage_bytes / 16));

@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         }
 
         if (ok) ok = mbar_wait(&full[slot], it.phase, p.err);
+        ok = __all_sync(0xffffffffu, ok);   // a timeout ends the whole warp's work together
         // rows this warp serves in this stage (it releases the slot after the
         // last of them is in registers, before any arithmetic)
         int nj = 0;

@@ -264,7 +264,9 @@ def test_head_full_size(mode, rows):
 
 @pytest.mark.parametrize("mode", ["i8", "i8x2"])
 @pytest.mark.parametrize("n,k,t", [(300, 1024, 16), (129, 4096, 33), (257, 1024, 128),
-                                   (130, 4096, 129), (64, 14336, 48), (1000, 1024, 256)])
+                                   (130, 4096, 129), (64, 14336, 48), (1000, 1024, 256),
+                                   (77, 2048, 5), (128, 3328, 20), (2000, 4096, 64),
+                                   (96, 1280, 97)])
 def test_chunk_tensor_core_parity(mode, n, k, t):
     rng = np.random.default_rng(3000 + n + k + t)
     q, s = synth.q8_weights(rng, n, k)
@@ -283,7 +285,7 @@ def test_chunk_tensor_core_parity(mode, n, k, t):
 
 
 @pytest.mark.parametrize("mode", ["i8", "i8x2"])
-@pytest.mark.parametrize("n,k,t", [(129, 1024, 16), (64, 4096, 130)])
+@pytest.mark.parametrize("n,k,t", [(129, 1024, 16), (64, 4096, 130), (40, 512, 3), (130, 768, 64)])
 def test_chunk_block_dots_exact(mode, n, k, t):
     """The tensor-core per-block accumulators are the exact integer block dots."""
     rng = np.random.default_rng(4000 + n + k + t)
