@@ -327,21 +327,29 @@ def run_ours(args, world, rank, local):
             if rank == 0:
                 print(json.dumps({"case": args.case, "launches": args.warmup + args.steps}))
             return
+        # MODE:PROJ[:fused], PROJ one of the layer's matrices or "all" (the four
+        # in layer order each iteration)
         mode, proj = parts[0], parts[1]
         fused = len(parts) > 2 and parts[2] == "fused"
-        p = [nm for nm, _, _ in synth.LAYER_D4096].index(proj)
-        k = synth.LAYER_D4096[p][2]
-        xq, xd = native.activation_buffers(mode, 1, k, device=dev)
-        native.act_quant(mode, H[p], xq, xd, norm=True)
+        names = [nm for nm, _, _ in synth.LAYER_D4096]
+        projs = list(range(len(names))) if proj == "all" else [names.index(proj)]
+        acts = {}
+        for p in projs:
+            k = synth.LAYER_D4096[p][2]
+            acts[p] = native.activation_buffers(mode, 1, k, device=dev)
+            native.act_quant(mode, H[p], acts[p][0], acts[p][1], norm=True)
         for i in range(args.warmup + args.steps):
-            if fused:
-                native.q8_proj_fused(mode, Q[i % COPIES][p], S[i % COPIES][p], H[p], Y[mode][p],
-                                     WS[mode][p])
-            else:
-                native.q8_proj(mode, Q[i % COPIES][p], S[i % COPIES][p], xq, xd, 1, Y[mode][p])
+            for p in projs:
+                if fused:
+                    native.q8_proj_fused(mode, Q[i % COPIES][p], S[i % COPIES][p], H[p],
+                                         Y[mode][p], WS[mode][p])
+                else:
+                    native.q8_proj(mode, Q[i % COPIES][p], S[i % COPIES][p], acts[p][0],
+                                   acts[p][1], 1, Y[mode][p])
         torch.cuda.synchronize(dev)
         if rank == 0:
-            print(json.dumps({"case": args.case, "launches": args.warmup + args.steps}))
+            print(json.dumps({"case": args.case,
+                              "launches": (args.warmup + args.steps) * len(projs)}))
         return
 
     step_graphs = capture(lambda c: step(c))
@@ -603,8 +611,9 @@ def main():
     ap.add_argument("--quick", action="store_true",
                     help="warm-up and timed steps only (for launch lists under a profiler)")
     ap.add_argument("--case", default=None,
-                    help="MODE:PROJ -- run only that projection's GEMV, warmup+steps launches "
-                         "(a small case for a full profiler capture)")
+                    help="MODE:PROJ[:fused] (PROJ a matrix of the layer or 'all') or "
+                         "chunk:MODE:PROJ:T -- only those projections, warmup+steps eager "
+                         "launches each (a case for a profiler capture)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -7,8 +7,8 @@ namespace q8 {
 
 template <bool ARGMAX>
 static cudaError_t dispatch_rows(const GemvArgs& a, const LaunchCtx& ctx) {
-    if (a.rows <= 1) return launch_gemv_row_t<2, 1, ARGMAX>(a, ctx);
-    if (a.rows <= 2) return launch_gemv_row_t<2, 2, ARGMAX>(a, ctx);
+    if (a.rows <= 1 && row_kernel_fits<2, 1>(a.K)) return launch_gemv_row_t<2, 1, ARGMAX>(a, ctx);
+    if (a.rows <= 2 && row_kernel_fits<2, 2>(a.K)) return launch_gemv_row_t<2, 2, ARGMAX>(a, ctx);
     if (a.rows <= 4) return launch_gemv_t<2, 4, ARGMAX>(a, ctx);
     if (a.rows <= 8) return launch_gemv_t<2, 8, ARGMAX>(a, ctx);
     return launch_gemv_t<2, 16, ARGMAX>(a, ctx);

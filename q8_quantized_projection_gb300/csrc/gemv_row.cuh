@@ -1,27 +1,29 @@
 // gemv_row.cuh -- the decode-step projection (1 or 2 activation rows), sm_103a.
 //
 // The decode step is pure HBM streaming: 34 bytes per 32 weights, read once.
-// This kernel keeps the memory side as simple as the bulk-copy engine likes
-// it and the compute side free of synchronisation:
+// The kernel keeps the memory side as simple as the bulk-copy engine likes it
+// and the compute side free of synchronisation:
 //
 //  * Persistent grid, one CTA per SM; CTA c owns the contiguous weight rows
 //    [N*c/G, N*(c+1)/G).
-//  * A stage is RS whole rows of the weight matrix (RS*K <= 32 KB), so the
-//    producer warp moves it with ONE contiguous bulk copy (plus one for its
-//    binary16 scales).  Rows longer than 32 KB are cut into 32 KB slices, one
-//    row-slice a stage.  Up to 128 KB per SM are in flight; the producer runs
-//    ahead of griddepcontrol.wait because weights never depend on the
-//    previous kernel on the stream.
-//  * The 16 consumer warps split each stage's rows into parts of PB = 512*CPL
-//    bytes of K: warp w always serves part w % NWR of row w / NWR, so its
-//    lanes hold that part's activation chunks in registers for the whole
-//    kernel (for K <= 32 KB), and every stage costs a lane CPL 16-byte
-//    shared loads plus the dots.
-//  * A row's parts meet through shared memory: each part's warp publishes its
-//    sum, the row's warps meet on a named barrier of their own (2 warps for
-//    K = 4096), and the part-0 warp adds the parts in part order (so the
-//    result is bitwise reproducible) and emits the row.  No CTA-wide barrier
-//    is needed while streaming.
+//  * A stage is RS whole rows of the weight matrix (RS*K <= 32 KB), moved by
+//    ONE contiguous bulk copy (plus one for its binary16 scales); rows longer
+//    than the stage are cut into slices, one row-slice a stage.  128 KB per SM
+//    are in flight; the producer warp runs ahead of griddepcontrol.wait, since
+//    weights never depend on the previous kernel on the stream.
+//  * A row-slice is cut into npr parts of PB = 512*CPL bytes (npr a power of
+//    two; trailing parts may be short or empty), so a stage holds
+//    items = RS*npr (row, part) pairs with items | 16.  Consumer warp w always
+//    serves item w % items, in every (16/items)-th stage: its part never
+//    changes, so its lanes hold that part's activation chunks in registers
+//    for the whole kernel (one slice) and a stage costs a lane CPL 16-byte
+//    shared loads plus the dots.  The slot is released as soon as the weights
+//    are in registers.
+//  * Each item's warp-reduced sum goes to a shared-memory slot of its own
+//    (row, slice, part); at the end of a super-block of rows the consumers
+//    meet once and add every row's parts in slice and part order, so the
+//    result is bitwise reproducible.  Nothing synchronises consumer warps
+//    while weights stream.
 //  * Numerics per mode are those of gemv.cuh (exact int32 block dots for the
 //    int8 modes; exact fixed-point chunk dots and f32 pairs for f32).
 #pragma once
@@ -33,12 +35,12 @@ namespace q8 {
 
 constexpr int kRowWarps = 16;
 constexpr int kRowThreads = 32 * (kRowWarps + 1);
-constexpr int kRowStage = 32768;
-constexpr int kRowMaxRS = 64;
+constexpr int kRowStage = 32768;       // weight bytes of one stage at most
+constexpr int kRowPsumBytes = 32768;   // part sums of one super-block of rows
 
 template <int MODE, int R>
 __host__ __device__ constexpr int row_cpl() {
-    return MODE == 0 ? (R == 1 ? 2 : 1) : (R == 1 ? 4 : 2);
+    return MODE == 1 ? (R == 1 ? 8 : 4) : MODE == 2 ? (R == 1 ? 4 : 2) : (R == 1 ? 2 : 1);
 }
 
 // Shared bytes of the fused producer's activation: codes (two planes at most)
@@ -47,26 +49,67 @@ constexpr size_t kFusedActBytes = 2 * 16384 + (16384 / 32) * 4;
 
 template <int MODE, int R, bool FUSE>
 __host__ __device__ constexpr size_t row_smem_bytes() {
-    using A = typename AccT<MODE>::T;
     return size_t(kGemvRing) + size_t(kGemvRing) / 16 + 2 * kGemvMaxStages * sizeof(uint64_t) +
-           size_t(kGemvMaxStages) * kRowWarps * R * sizeof(A) +      // part sums
-           kGemvYaccBytes + size_t(kRowWarps) * R * sizeof(ArgmaxCand) + 64 +
+           kRowPsumBytes + size_t(kRowWarps) * R * sizeof(ArgmaxCand) + 64 +
            (FUSE ? kFusedActBytes : 0);
 }
 
 struct RowGeo {
-    int64_t K;
-    int KS;          // bytes of K per stage (whole rows when KS == K)
+    int KS;          // bytes of K per slice (whole rows when KS == K)
     int nks;         // slices per row
-    int RS;          // rows per stage
-    int RPW;         // rows per warp per stage when a row has one part
-    int NWR;         // warps (parts) per row
     int PB;          // part bytes
+    int npr;         // parts per slice: a power of two <= 16
+    int nprr;        // parts that hold data (the rest are empty)
+    int RS;          // rows per stage: a power of two
+    int items;       // RS * npr, a divisor of kRowWarps
+    int stride;      // kRowWarps / items: stages between a warp's stages
     int stage_bytes;
     int nstages;
     int64_t r0, r1;
-    int64_t sbrows;  // rows per super-block of running sums (multiple of RS)
+    int64_t sbrows;  // rows per super-block (a multiple of RS, >= RS when usable)
 };
+
+__host__ __device__ inline RowGeo row_geo(int64_t N, int64_t K, int G, int c, int cpl,
+                                          int psum_row_unit) {
+    RowGeo g;
+    g.PB = 512 * cpl;
+    int64_t ks = K;
+    if (ks > kRowStage) ks = kRowStage;
+    if (ks > int64_t(kRowWarps) * g.PB) ks = int64_t(kRowWarps) * g.PB;
+    g.KS = int(ks);
+    g.nks = int((K + g.KS - 1) / g.KS);
+    g.nprr = (g.KS + g.PB - 1) / g.PB;
+    g.npr = 1;
+    while (g.npr < g.nprr) g.npr <<= 1;
+    const int rsmax = kRowStage / g.KS;
+    g.RS = 1;
+    while (g.RS * 2 <= rsmax && g.RS * 2 * g.npr <= kRowWarps) g.RS <<= 1;
+    g.items = g.RS * g.npr;
+    g.stride = kRowWarps / g.items;
+    g.stage_bytes = (g.RS * g.KS + 1023) & ~1023;
+    const int ns = kGemvRing / g.stage_bytes;
+    g.nstages = ns > kGemvMaxStages ? kGemvMaxStages : ns;
+    g.r0 = N * c / G;
+    g.r1 = N * (c + 1) / G;
+    const int64_t per_row = int64_t(g.nks) * g.nprr * psum_row_unit;
+    g.sbrows = ((kRowPsumBytes / per_row) / g.RS) * g.RS;
+    return g;
+}
+
+// Whether the decode kernel handles this K (the part sums of RS rows fit).
+template <int MODE, int R>
+inline bool row_kernel_fits(int64_t K) {
+    using A = typename AccT<MODE>::T;
+    const RowGeo g = row_geo(1, K, 1, 0, row_cpl<MODE, R>(), int(R * sizeof(A)));
+    return g.sbrows >= g.RS;
+}
+
+__device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v, long long i) {
+    if (v > bv || (v == bv && i < bi)) {
+        bv = v;
+        bi = i;
+    }
+}
 
 template <int MODE, int R, bool ARGMAX, bool FUSE>
 __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvParams p) {
@@ -74,16 +117,16 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     using A = typename AccT<MODE>::T;
     constexpr int CPL = row_cpl<MODE, R>();
     constexpr int NW = kRowWarps;
+    constexpr int NT = 32 * NW;
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* wring = smem;
     unsigned char* sring = wring + kGemvRing;
     uint64_t* full = reinterpret_cast<uint64_t*>(sring + kGemvRing / 16);
     uint64_t* empty = full + kGemvMaxStages;
-    A* psum = reinterpret_cast<A*>(empty + kGemvMaxStages);                 // [slot][warp][R]
-    A* yacc = reinterpret_cast<A*>(psum + kGemvMaxStages * NW * R);         // [sbrows][R]
-    ArgmaxCand* cand = reinterpret_cast<ArgmaxCand*>(reinterpret_cast<unsigned char*>(yacc) +
-                                                     kGemvYaccBytes);       // [NW][R]
+    A* psum = reinterpret_cast<A*>(empty + kGemvMaxStages);   // [sbrows][nks][nprr][R]
+    ArgmaxCand* cand = reinterpret_cast<ArgmaxCand*>(reinterpret_cast<unsigned char*>(psum) +
+                                                     kRowPsumBytes);   // [NW][R]
     __shared__ float s_amax[NW][R];
     __shared__ int s_emax[R];
     __shared__ unsigned int s_ticket;
@@ -93,56 +136,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
-
-    RowGeo g;
-    g.K = p.K;
-    g.PB = 512 * CPL;
-    {
-        int64_t ks = p.K;
-        if (ks > kRowStage) ks = kRowStage;
-        if (ks > int64_t(NW) * g.PB) ks = int64_t(NW) * g.PB;
-        g.KS = int(ks);
-        g.nks = int((p.K + g.KS - 1) / g.KS);
-        const int npr = (g.KS + g.PB - 1) / g.PB;
-        if (npr == 1) {
-            int rs = kRowStage / g.KS;
-            if (rs > kRowMaxRS) rs = kRowMaxRS;
-            rs = (rs / NW) * NW;
-            g.RS = rs;
-            g.RPW = rs / NW;
-            g.NWR = 1;
-        } else {
-            int rs = kRowStage / g.KS;
-            if (rs > NW / npr) rs = NW / npr;
-            g.RS = rs < 1 ? 1 : rs;
-            g.RPW = 1;
-            g.NWR = npr;
-        }
-        g.stage_bytes = (g.RS * g.KS + 1023) & ~1023;
-        const int ns = kGemvRing / g.stage_bytes;
-        g.nstages = ns > kGemvMaxStages ? kGemvMaxStages : ns;
-        g.r0 = p.N * c / G;
-        g.r1 = p.N * (c + 1) / G;
-        const int64_t yrows = kGemvYaccBytes / int64_t(R * sizeof(A));
-        g.sbrows = (yrows / g.RS) * g.RS;
-    }
-    // Stage walk shared with gemv.cuh's iterator (RS rows x KS-byte slices).
-    Geo sg;
-    sg.K = g.K;
-    sg.slb = g.KS;
-    sg.nks = g.nks;
-    sg.RS = g.RS;
-    sg.rpw = g.RPW;
-    sg.stage_bytes = g.stage_bytes;
-    sg.nstages = g.nstages;
-    sg.r0 = g.r0;
-    sg.r1 = g.r1;
-    sg.sbrows = g.sbrows;
+    const RowGeo g = row_geo(p.N, p.K, G, c, CPL, int(R * sizeof(A)));
 
     if (tid == 0) {
         for (int i = 0; i < g.nstages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NW);
+            mbar_init(&empty[i], g.items);
         }
         fence_barrier_init();
     }
@@ -154,6 +153,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     if (warp == NW) {
         // -------------------------------------------------------------- producer
         if (lane == 0) {
+            Geo sg;
+            sg.K = p.K;
+            sg.slb = g.KS;
+            sg.nks = g.nks;
+            sg.RS = g.RS;
+            sg.rpw = 1;
+            sg.stage_bytes = g.stage_bytes;
+            sg.nstages = g.nstages;
+            sg.r0 = g.r0;
+            sg.r1 = g.r1;
+            sg.sbrows = g.sbrows;
             const uint64_t policy = policy_evict_first();
             const unsigned char* qsrc = reinterpret_cast<const unsigned char*>(p.q);
             const unsigned char* ssrc = reinterpret_cast<const unsigned char*>(p.s);
@@ -211,26 +221,23 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         // The producer, fused: RMSNorm -> quant of the one activation row into
         // shared memory, by the same code and thread layout as act_quant, while
         // the producer warp already streams weights.
-        static_assert(32 * NW == kProdThreads, "fused producer needs kProdThreads consumers");
+        static_assert(NT == kProdThreads, "fused producer needs kProdThreads consumers");
         unsigned char* sact = reinterpret_cast<unsigned char*>(cand + NW * R) + 64;
         float* sxd = reinterpret_cast<float*>(sact + 2 * kFusedMaxK);
         const float rf = row_rms_scale(p.h, K, p.eps, tid, 1, s_warp, &s_rf);
         row_quantize<MODE, true>(p.h, p.gain, rf, K, tid, sact, K, sxd);
-        consumer_bar<32 * NW>();
+        consumer_bar<NT>();
         act8 = reinterpret_cast<const signed char*>(sact);
         xdp = sxd;
         plane = K;
     }
-    // this warp's place in a stage
-    const int rw = (g.NWR == 1) ? warp : warp / g.NWR;   // first row (NWR == 1: rows rw + NW*j)
-    const int pw = (g.NWR == 1) ? 0 : warp % g.NWR;      // part
-    const bool active = (g.NWR == 1) || (rw < g.RS);
 
     if constexpr (MODE == 0) {
+        // the row's largest binade: the fixed-point grids are relative to it
         float amax[R];
 #pragma unroll
         for (int m = 0; m < R; ++m) amax[m] = 0.0f;
-        for (int64_t k = int64_t(tid) * 4; k < K; k += 4 * 32 * NW) {
+        for (int64_t k = int64_t(tid) * 4; k < K; k += 4 * NT) {
 #pragma unroll
             for (int m = 0; m < R; ++m) {
                 if (m < rows) {
@@ -249,15 +256,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
             for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
             if (lane == 0) s_amax[warp][m] = a;
         }
-        consumer_bar<32 * NW>();
+        consumer_bar<NT>();
         if (tid < R) {
             float a = 0.0f;
             for (int w = 0; w < NW; ++w) a = fmaxf(a, s_amax[w][tid]);
             s_emax[tid] = binade(a);
         }
+        consumer_bar<NT>();
     }
-    for (int i = tid; i < g.sbrows * R; i += 32 * NW) yacc[i] = acc_zero(A{});
-    consumer_bar<32 * NW>();
 
     double best_v[ARGMAX ? R : 1];
     long long best_i[ARGMAX ? R : 1];
@@ -267,217 +273,217 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         best_i[m] = 0x7fffffffffffffffll;
     }
 
+    // this warp's place in every stage it serves
+    const int q = warp % g.items;
+    const int jrow = q / g.npr;   // row within the stage
+    const int pw = q % g.npr;     // part within the row-slice
+    const int s_first = warp / g.items;
+
     int4 a1[CPL][R];
     int4 a2[CPL][R];
     float xdv[CPL][R];
     FixChunk fx[MODE == 0 ? CPL : 1][MODE == 0 ? R : 1];
     float p2s[CPL][R];
     int cur_sl = -1;
-    int cpp = 0;   // chunks in this warp's part of the current slice
+    int ncc = 0, rag = 0;   // full 512-byte chunk columns of this part, lanes of the ragged one
 
+    const uint32_t wring_a = smem_u32(wring), sring_a = smem_u32(sring);
     bool ok = true;
-    StageIter it;
-    stage_init(sg, it);
-    for (; !it.done; stage_next(sg, it)) {
-        const int slot = it.slot;
-        const int64_t rb = it.rb, ks = it.ks, sb0 = it.sb0;
-        const int kl = it.kl, sl = it.sl;
-        const int nrows = int(min64(g.RS, it.sb_end - rb));
-        const int pbyte0 = pw * g.PB;   // this warp's part within the slice
-
-        if (sl != cur_sl) {
-            cur_sl = sl;
-            const int pbytes = kl - pbyte0 < g.PB ? (kl - pbyte0 > 0 ? kl - pbyte0 : 0) : g.PB;
-            cpp = pbytes >> 4;
+    int64_t gbase = 0;   // global index of the super-block's first stage
+    for (int64_t sb0 = g.r0; sb0 < g.r1; sb0 += g.sbrows) {
+        const int sbn = int(min64(g.sbrows, g.r1 - sb0));
+        const int nrb = (sbn + g.RS - 1) / g.RS;
+        const int nst_sb = g.nks * nrb;
+        int t = int((int64_t(s_first) - gbase) & int64_t(g.stride - 1));
+        int sl = t / nrb, rbi = t % nrb;
+        int slot = int((gbase + t) % g.nstages);
+        uint32_t phase = uint32_t(((gbase + t) / g.nstages) & 1);
+        for (; t < nst_sb && ok; t += g.stride) {
+            const int64_t ks = int64_t(sl) * g.KS;
+            const int kl = int(min64(g.KS, K - ks));
+            if (sl != cur_sl) {
+                // this part's activation chunks into registers
+                cur_sl = sl;
+                int pbytes = kl - pw * g.PB;
+                pbytes = pbytes < 0 ? 0 : (pbytes > g.PB ? g.PB : pbytes);
+                ncc = pbytes >> 9;
+                rag = (pbytes & 511) >> 4;
 #pragma unroll
-            for (int cc = 0; cc < CPL; ++cc) {
-                const int ch = lane + 32 * cc;
+                for (int cc = 0; cc < CPL; ++cc) {
 #pragma unroll
-                for (int m = 0; m < R; ++m) {
-                    a1[cc][m] = a2[cc][m] = make_int4(0, 0, 0, 0);
-                    xdv[cc][m] = 0.0f;
-                    p2s[cc][m] = 0.0f;
-                    if constexpr (MODE == 0) fx[cc][m] = FixChunk{};
+                    for (int m = 0; m < R; ++m) {
+                        a1[cc][m] = a2[cc][m] = make_int4(0, 0, 0, 0);
+                        xdv[cc][m] = 0.0f;
+                        p2s[cc][m] = 0.0f;
+                        if constexpr (MODE == 0) fx[cc][m] = FixChunk{};
+                    }
+                    if (cc < ncc || (cc == ncc && lane < rag)) {
+                        const int64_t k = ks + pw * g.PB + int64_t(lane) * 16 + 512 * cc;
+#pragma unroll
+                        for (int m = 0; m < R; ++m) {
+                            if (m < rows) {
+                                if constexpr (MODE == 0) {
+                                    float xs[16];
+#pragma unroll
+                                    for (int u = 0; u < 4; ++u) {
+                                        const int4 t4 = ldg_nc_v4(actf + m * K + k + 4 * u);
+                                        xs[4 * u + 0] = __int_as_float(t4.x);
+                                        xs[4 * u + 1] = __int_as_float(t4.y);
+                                        xs[4 * u + 2] = __int_as_float(t4.z);
+                                        xs[4 * u + 3] = __int_as_float(t4.w);
+                                    }
+                                    fx[cc][m] = fix_chunk(xs);
+                                    p2s[cc][m] = ldexpf(1.0f, fx[cc][m].e - s_emax[m]);
+                                } else if constexpr (FUSE) {
+                                    a1[cc][m] = lds_v4(act8 + m * K + k);
+                                    if constexpr (MODE == 2) a2[cc][m] = lds_v4(act8 + plane + m * K + k);
+                                    xdv[cc][m] = xdp[m * nb + (k >> 5)];
+                                } else {
+                                    a1[cc][m] = ldg_nc_v4(act8 + m * K + k);
+                                    if constexpr (MODE == 2)
+                                        a2[cc][m] = ldg_nc_v4(act8 + plane + m * K + k);
+                                    xdv[cc][m] = __ldg(xdp + m * nb + (k >> 5));
+                                }
+                            }
+                        }
+                    }
                 }
-                if (active && ch < cpp) {
-                    const int64_t k = ks + pbyte0 + int64_t(ch) * 16;
+            }
+
+            if (ok) ok = mbar_wait(&full[slot], phase, p.err);
+            ok = __all_sync(0xffffffffu, ok);   // a timeout ends the whole warp's work together
+            const int row_sb = rbi * g.RS + jrow;   // row within the super-block
+            const bool have = ok && row_sb < sbn && pw < g.nprr;
+            // weights and scales of this item, at most 4 chunks (64 registers
+            // worth) at a time; the slot goes back once the last group is loaded
+            constexpr int GC = CPL < 4 ? CPL : 4;
+            A part[R];
+#pragma unroll
+            for (int m = 0; m < R; ++m) part[m] = acc_zero(A{});
+            const uint32_t wrow = wring_a + uint32_t(slot * g.stage_bytes + jrow * kl + pw * g.PB) +
+                                  uint32_t(lane * 16);
+            const int blk0 = (pw * g.PB) >> 5;   // first block of the part within the slice
+            const uint32_t sbase = sring_a + uint32_t(slot * (g.stage_bytes / 16) + jrow * (kl >> 4));
+#pragma unroll
+            for (int c0 = 0; c0 < CPL; c0 += GC) {
+                int4 w[GC];
+                float sw[GC];
+                if (have) {
+                    if (ncc == CPL && scale_bulk) {
+                        // common case: every chunk valid, scales staged with the weights
+                        const uint32_t srow = sbase + uint32_t((blk0 + (lane >> 1)) * 2);
+#pragma unroll
+                        for (int cc = 0; cc < GC; ++cc) w[cc] = lds128(wrow + 512 * (c0 + cc));
+#pragma unroll
+                        for (int cc = 0; cc < GC; ++cc)
+                            sw[cc] = half_bits_to_float(lds16(srow + 32 * (c0 + cc)));
+                    } else {
+                        const int64_t nrow = sb0 + row_sb;
+#pragma unroll
+                        for (int cc = 0; cc < GC; ++cc) {
+                            const int ch = c0 + cc;
+                            w[cc] = make_int4(0, 0, 0, 0);
+                            sw[cc] = 0.0f;
+                            if (ch < ncc || (ch == ncc && lane < rag)) {
+                                const int blk = blk0 + (lane >> 1) + 16 * ch;
+                                w[cc] = lds128(wrow + 512 * ch);
+                                sw[cc] = scale_bulk ? half_bits_to_float(lds16(sbase + uint32_t(blk * 2)))
+                                                    : half_bits_to_float(__ldg(p.s + nrow * nb + (ks >> 5) + blk));
+                            }
+                        }
+                    }
+                }
+                if (c0 + GC >= CPL) {
+                    // the weights are in registers: give the slot back
+                    __syncwarp();
+                    if (lane == 0 && ok) mbar_arrive(&empty[slot]);
+                }
+                if (have) {
 #pragma unroll
                     for (int m = 0; m < R; ++m) {
                         if (m < rows) {
                             if constexpr (MODE == 0) {
-                                float xs[16];
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const int4 t4 = ldg_nc_v4(actf + m * K + k + 4 * u);
-                                    xs[4 * u + 0] = __int_as_float(t4.x);
-                                    xs[4 * u + 1] = __int_as_float(t4.y);
-                                    xs[4 * u + 2] = __int_as_float(t4.z);
-                                    xs[4 * u + 3] = __int_as_float(t4.w);
-                                }
-                                fx[cc][m] = fix_chunk(xs);
-                                p2s[cc][m] = ldexpf(1.0f, fx[cc][m].e - s_emax[m]);
-                            } else if constexpr (FUSE) {
-                                a1[cc][m] = lds_v4(act8 + m * K + k);
-                                if constexpr (MODE == 2) a2[cc][m] = lds_v4(act8 + plane + m * K + k);
-                                xdv[cc][m] = xdp[m * nb + (k >> 5)];
+                                for (int cc = 0; cc < GC; ++cc)
+                                    part[m] = df_add(part[m], scaled_pair(__fmul_rn(sw[cc], p2s[c0 + cc][m]),
+                                                                          fix_dot(w[cc], fx[c0 + cc][m])));
                             } else {
-                                a1[cc][m] = ldg_nc_v4(act8 + m * K + k);
-                                if constexpr (MODE == 2)
-                                    a2[cc][m] = ldg_nc_v4(act8 + plane + m * K + k);
-                                xdv[cc][m] = __ldg(xdp + m * nb + (k >> 5));
+#pragma unroll
+                                for (int cc = 0; cc < GC; ++cc) {
+                                    const int isum = (MODE == 1) ? dot16_i8(w[cc], a1[c0 + cc][m])
+                                                                 : dot16_i8x2(w[cc], a1[c0 + cc][m], a2[c0 + cc][m]);
+                                    part[m] = fmaf(float(isum), sw[cc] * xdv[c0 + cc][m], part[m]);
+                                }
                             }
                         }
                     }
                 }
             }
+            if (have) {
+#pragma unroll
+                for (int m = 0; m < R; ++m) part[m] = warp_sum(part[m]);
+                if (lane == 0) {
+                    A* ps = psum + ((size_t(row_sb) * g.nks + sl) * g.nprr + pw) * R;
+#pragma unroll
+                    for (int m = 0; m < R; ++m) ps[m] = part[m];
+                }
+            }
+            // the next stage this warp serves
+            rbi += g.stride;
+            while (rbi >= nrb) {
+                rbi -= nrb;
+                ++sl;
+            }
+            slot += g.stride;
+            while (slot >= g.nstages) {
+                slot -= g.nstages;
+                phase ^= 1u;
+            }
         }
+        gbase += nst_sb;
 
-        if (ok) ok = mbar_wait(&full[slot], it.phase, p.err);
-        ok = __all_sync(0xffffffffu, ok);   // a timeout ends the whole warp's work together
-        // rows this warp serves in this stage (it releases the slot after the
-        // last of them is in registers, before any arithmetic)
-        int nj = 0;
-        if (active) {
-            if (g.NWR == 1) {
-                nj = (nrows - rw + NW - 1) / NW;
-                if (nj > g.RPW) nj = g.RPW;
-                if (nj < 0) nj = 0;
-            } else {
-                nj = rw < nrows ? 1 : 0;
+        // every row of the super-block: its parts in slice and part order
+        consumer_bar<NT>();
+        if (ok) {
+            const int nparts = g.nks * g.nprr;
+            for (int i = tid; i < sbn * R; i += NT) {
+                const int row_sb = i / R, m = i % R;
+                if (m >= rows) continue;
+                const A* ps = psum + size_t(row_sb) * nparts * R + m;
+                A s = ps[0];
+                for (int u = 1; u < nparts; ++u) s = acc_add(s, ps[size_t(u) * R]);
+                const int64_t n = sb0 + row_sb;
+                double val = acc_value(s);
+                if constexpr (MODE == 0) val = ldexp(val, s_emax[m] - 30);
+                if (p.y) {
+                    if (MODE == 0 && p.out_f64)
+                        reinterpret_cast<double*>(p.y)[m * N + n] = val;
+                    else
+                        reinterpret_cast<float*>(p.y)[m * N + n] = float(val);
+                }
+                if constexpr (ARGMAX) argmax_keep(best_v[m], best_i[m], val, n);
             }
         }
-        bool released = false;
-        if (active) {
-            const uint32_t W = smem_u32(wring) + uint32_t(slot * g.stage_bytes);
-            const uint32_t SC = smem_u32(sring) + uint32_t(slot * (g.stage_bytes / 16));
-            const bool last_slice = (sl == g.nks - 1);
-            const bool full_part = (cpp == 32 * CPL);
-            for (int j = 0; j < nj; ++j) {
-                const int r = (g.NWR == 1) ? rw + NW * j : rw;
-                A part[R];
-#pragma unroll
-                for (int m = 0; m < R; ++m) part[m] = acc_zero(A{});
-                const uint32_t wrow = W + uint32_t(r * kl + pbyte0) + uint32_t(lane * 16);
-                const int blk0 = pbyte0 >> 5;   // first block of the part within the slice
-                // ---- loads: this row's weights and scales into registers
-                int4 w[CPL];
-                float sw[CPL];
-                if (ok && full_part && scale_bulk) {
-                    // common case: every chunk valid, scales staged with the weights
-                    const uint32_t srow = SC + uint32_t(r * (kl >> 4)) + uint32_t((blk0 + (lane >> 1)) * 2);
-#pragma unroll
-                    for (int cc = 0; cc < CPL; ++cc) w[cc] = lds128(wrow + 512 * cc);
-#pragma unroll
-                    for (int cc = 0; cc < CPL; ++cc) sw[cc] = half_bits_to_float(lds16(srow + 32 * cc));
-                } else {
-#pragma unroll
-                    for (int cc = 0; cc < CPL; ++cc) {
-                        const bool v = ok && (full_part || lane + 32 * cc < cpp);
-                        const int blk = blk0 + (lane >> 1) + 16 * cc;
-                        w[cc] = make_int4(0, 0, 0, 0);
-                        sw[cc] = 0.0f;
-                        if (v) {
-                            w[cc] = lds128(wrow + 512 * cc);
-                            sw[cc] = scale_bulk
-                                         ? half_bits_to_float(lds16(SC + uint32_t(r * (kl >> 4)) + uint32_t(blk * 2)))
-                                         : half_bits_to_float(__ldg(p.s + (rb + r) * nb + (ks >> 5) + blk));
-                        }
-                    }
-                }
-                if (j == nj - 1 && ok) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[slot]);
-                    released = true;
-                }
-                // ---- arithmetic (invalid chunks hold zero weights and scales)
-#pragma unroll
-                for (int m = 0; m < R; ++m) {
-                    if (m < rows) {
-                        if constexpr (MODE == 0) {
-                            DF d[CPL];
-#pragma unroll
-                            for (int cc = 0; cc < CPL; ++cc)
-                                d[cc] = scaled_pair(__fmul_rn(sw[cc], p2s[cc][m]), fix_dot(w[cc], fx[cc][m]));
-#pragma unroll
-                            for (int cc = 0; cc < CPL; ++cc) part[m] = df_add(part[m], d[cc]);
-                        } else {
-#pragma unroll
-                            for (int cc = 0; cc < CPL; ++cc) {
-                                const int isum = (MODE == 1) ? dot16_i8(w[cc], a1[cc][m])
-                                                             : dot16_i8x2(w[cc], a1[cc][m], a2[cc][m]);
-                                part[m] = fmaf(float(isum), sw[cc] * xdv[cc][m], part[m]);
-                            }
-                        }
-                    }
-                }
-                A tot[R];
-#pragma unroll
-                for (int m = 0; m < R; ++m) tot[m] = warp_sum(part[m]);
-                // A row's parts meet through shared memory: every part's warp
-                // publishes its sum, the row group syncs on its own named
-                // barrier, and the part-0 warp adds the parts in order.
-                bool finisher = true;
-                if (g.NWR > 1) {
-                    if (lane == 0) {
-                        A* ps = psum + (slot * NW + warp) * R;
-#pragma unroll
-                        for (int m = 0; m < R; ++m) ps[m] = tot[m];
-                    }
-                    named_bar(2 + rw, 32 * g.NWR);
-                    finisher = (pw == 0);
-                    if (finisher && lane == 0) {
-#pragma unroll
-                        for (int m = 0; m < R; ++m) {
-                            A s = psum[(slot * NW + rw * g.NWR) * R + m];
-                            for (int q2 = 1; q2 < g.NWR; ++q2)
-                                s = acc_add(s, psum[(slot * NW + rw * g.NWR + q2) * R + m]);
-                            tot[m] = s;
-                        }
-                    }
-                }
-                if (finisher && lane == 0) {
-                    const int64_t n = rb + r;
-                    A* yrow = yacc + int(n - sb0) * R;
-#pragma unroll
-                    for (int m = 0; m < R; ++m) {
-                        if (m < rows) {
-                            const A acc = (g.nks > 1) ? acc_add(yrow[m], tot[m]) : tot[m];
-                            if (last_slice) {
-                                double val = acc_value(acc);
-                                if constexpr (MODE == 0) val = ldexp(val, s_emax[m] - 30);
-                                if (p.y) {
-                                    if (MODE == 0 && p.out_f64)
-                                        reinterpret_cast<double*>(p.y)[m * N + n] = val;
-                                    else
-                                        reinterpret_cast<float*>(p.y)[m * N + n] = float(val);
-                                }
-                                if constexpr (ARGMAX) {
-                                    if (val > best_v[m] || (val == best_v[m] && n < best_i[m])) {
-                                        best_v[m] = val;
-                                        best_i[m] = n;
-                                    }
-                                }
-                                if (g.nks > 1) yrow[m] = acc_zero(A{});
-                            } else {
-                                yrow[m] = acc;
-                            }
-                        }
-                    }
-                }
-            }
-        }
-        if (ok && !released) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-        }
+        consumer_bar<NT>();
     }
 
     if constexpr (ARGMAX) {
+        // per warp, then per CTA, then the last CTA to take a ticket reduces
+        // every CTA's candidate (lowest index on ties)
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const double ov = __shfl_xor_sync(0xffffffffu, best_v[m], o);
+                const long long oi = __shfl_xor_sync(0xffffffffu, best_i[m], o);
+                argmax_keep(best_v[m], best_i[m], ov, oi);
+            }
+        }
         if (lane == 0) {
 #pragma unroll
             for (int m = 0; m < R; ++m) cand[warp * R + m] = {best_v[m], best_i[m]};
         }
-        consumer_bar<32 * NW>();
+        consumer_bar<NT>();
         ArgmaxCand* gc = reinterpret_cast<ArgmaxCand*>(p.ws + kArgmaxHeader);
         unsigned int* counter = reinterpret_cast<unsigned int*>(p.ws);
         if (tid < rows) {
@@ -489,9 +495,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
             gc[size_t(c) * rows + tid] = b;
             __threadfence();
         }
-        consumer_bar<32 * NW>();
+        consumer_bar<NT>();
         if (tid == 0) s_ticket = atomicAdd(counter, 1u);
-        consumer_bar<32 * NW>();
+        consumer_bar<NT>();
         if (s_ticket == unsigned(G - 1)) {
             __threadfence();
             if (tid < rows) {
