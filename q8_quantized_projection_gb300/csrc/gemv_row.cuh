@@ -8,17 +8,18 @@
 //    [N*c/G, N*(c+1)/G).
 //  * A stage is RS whole rows of the weight matrix (RS*K <= 32 KB), moved by
 //    ONE contiguous bulk copy (plus one for its binary16 scales); rows longer
-//    than the stage are cut into slices, one row-slice a stage.  128 KB per SM
+//    than the stage are cut into slices, one row-slice a stage.  160 KB per SM
 //    are in flight; the producer warp runs ahead of griddepcontrol.wait, since
 //    weights never depend on the previous kernel on the stream.
 //  * A row-slice is cut into npr parts of PB = 512*CPL bytes (npr a power of
 //    two; trailing parts may be short or empty), so a stage holds
 //    items = RS*npr (row, part) pairs with items | 16.  Consumer warp w always
-//    serves item w % items, in every (16/items)-th stage: its part never
-//    changes, so its lanes hold that part's activation chunks in registers
-//    for the whole kernel (one slice) and a stage costs a lane CPL 16-byte
-//    shared loads plus the dots.  The slot is released as soon as the weights
-//    are in registers.
+//    serves item w % items, in the stages whose ring slot is congruent to
+//    w / items modulo 16/items (so every phase of a slot's barriers is seen by
+//    the same warps): its part never changes, so its lanes hold that part's
+//    activation chunks in registers for the whole kernel (one slice) and a
+//    stage costs a lane CPL 16-byte shared loads plus the dots.  The slot is
+//    released as soon as the weights are in registers.
 //  * Each item's warp-reduced sum goes to a shared-memory slot of its own
 //    (row, slice, part); at the end of a super-block of rows the consumers
 //    meet once and add every row's parts in slice and part order, so the
@@ -36,7 +37,8 @@ namespace q8 {
 constexpr int kRowWarps = 16;
 constexpr int kRowThreads = 32 * (kRowWarps + 1);
 constexpr int kRowStage = 32768;       // weight bytes of one stage at most
-constexpr int kRowPsumBytes = 32768;   // part sums of one super-block of rows
+constexpr int kRowRing = 163840;       // weight bytes in flight per CTA
+constexpr int kRowPsumBytes = 16384;   // part sums of one super-block of rows
 
 template <int MODE, int R>
 __host__ __device__ constexpr int row_cpl() {
@@ -49,7 +51,7 @@ constexpr size_t kFusedActBytes = 2 * 16384 + (16384 / 32) * 4;
 
 template <int MODE, int R, bool FUSE>
 __host__ __device__ constexpr size_t row_smem_bytes() {
-    return size_t(kGemvRing) + size_t(kGemvRing) / 16 + 2 * kGemvMaxStages * sizeof(uint64_t) +
+    return size_t(kRowRing) + size_t(kRowRing) / 16 + 2 * kGemvMaxStages * sizeof(uint64_t) +
            kRowPsumBytes + size_t(kRowWarps) * R * sizeof(ArgmaxCand) + 64 +
            (FUSE ? kFusedActBytes : 0);
 }
@@ -62,7 +64,7 @@ struct RowGeo {
     int nprr;        // parts that hold data (the rest are empty)
     int RS;          // rows per stage: a power of two
     int items;       // RS * npr, a divisor of kRowWarps
-    int stride;      // kRowWarps / items: stages between a warp's stages
+    int stride;      // kRowWarps / items: warp groups, one per slot residue
     int stage_bytes;
     int nstages;
     int64_t r0, r1;
@@ -87,7 +89,7 @@ __host__ __device__ inline RowGeo row_geo(int64_t N, int64_t K, int G, int c, in
     g.items = g.RS * g.npr;
     g.stride = kRowWarps / g.items;
     g.stage_bytes = (g.RS * g.KS + 1023) & ~1023;
-    const int ns = kGemvRing / g.stage_bytes;
+    const int ns = kRowRing / g.stage_bytes;
     g.nstages = ns > kGemvMaxStages ? kGemvMaxStages : ns;
     g.r0 = N * c / G;
     g.r1 = N * (c + 1) / G;
@@ -121,8 +123,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* wring = smem;
-    unsigned char* sring = wring + kGemvRing;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sring + kGemvRing / 16);
+    unsigned char* sring = wring + kRowRing;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sring + kRowRing / 16);
     uint64_t* empty = full + kGemvMaxStages;
     A* psum = reinterpret_cast<A*>(empty + kGemvMaxStages);   // [sbrows][nks][nprr][R]
     ArgmaxCand* cand = reinterpret_cast<ArgmaxCand*>(reinterpret_cast<unsigned char*>(psum) +
@@ -130,7 +132,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     __shared__ float s_amax[NW][R];
     __shared__ int s_emax[R];
     __shared__ unsigned int s_ticket;
-    __shared__ double s_warp[kProdWarps];
+    __shared__ float2 s_pair[kProdWarps];
     __shared__ float s_rf;
 
     const int tid = threadIdx.x;
@@ -224,8 +226,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         static_assert(NT == kProdThreads, "fused producer needs kProdThreads consumers");
         unsigned char* sact = reinterpret_cast<unsigned char*>(cand + NW * R) + 64;
         float* sxd = reinterpret_cast<float*>(sact + 2 * kFusedMaxK);
-        const float rf = row_rms_scale(p.h, K, p.eps, tid, 1, s_warp, &s_rf);
-        row_quantize<MODE, true>(p.h, p.gain, rf, K, tid, sact, K, sxd);
+        row_produce<MODE, true>(p.h, p.gain, p.eps, K, tid, 1, s_pair, &s_rf, sact, K, sxd);
         consumer_bar<NT>();
         act8 = reinterpret_cast<const signed char*>(sact);
         xdp = sxd;
@@ -294,11 +295,23 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         const int sbn = int(min64(g.sbrows, g.r1 - sb0));
         const int nrb = (sbn + g.RS - 1) / g.RS;
         const int nst_sb = g.nks * nrb;
-        int t = int((int64_t(s_first) - gbase) & int64_t(g.stride - 1));
-        int sl = t / nrb, rbi = t % nrb;
-        int slot = int((gbase + t) % g.nstages);
-        uint32_t phase = uint32_t(((gbase + t) / g.nstages) & 1);
-        for (; t < nst_sb && ok; t += g.stride) {
+        int sl = 0, rbi = 0;
+        int slot = int(gbase % g.nstages);
+        uint32_t phase = uint32_t((gbase / g.nstages) & 1);
+        for (int t = 0; t < nst_sb && ok; ++t) {
+            // a ring slot is always served by the same warps, so each of them
+            // sees every phase of the slot's barriers
+            if ((slot & (g.stride - 1)) != s_first) {
+                if (++rbi == nrb) {
+                    rbi = 0;
+                    ++sl;
+                }
+                if (++slot == g.nstages) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+                continue;
+            }
             const int64_t ks = int64_t(sl) * g.KS;
             const int kl = int(min64(g.KS, K - ks));
             if (sl != cur_sl) {
@@ -428,15 +441,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     for (int m = 0; m < R; ++m) ps[m] = part[m];
                 }
             }
-            // the next stage this warp serves
-            rbi += g.stride;
-            while (rbi >= nrb) {
-                rbi -= nrb;
+            if (++rbi == nrb) {
+                rbi = 0;
                 ++sl;
             }
-            slot += g.stride;
-            while (slot >= g.nstages) {
-                slot -= g.nstages;
+            if (++slot == g.nstages) {
+                slot = 0;
                 phase ^= 1u;
             }
         }

@@ -80,7 +80,7 @@ struct AqParams {
 // arithmetic, shared with the decode projection's fused producer).
 template <int MODE, bool NORM>
 __global__ void __launch_bounds__(kProdThreads) act_quant_kernel(const AqParams p) {
-    __shared__ double s_warp[kProdWarps];
+    __shared__ float2 s_pair[kProdWarps];
     __shared__ float s_rf;
     const int tid = threadIdx.x;
     const int64_t m = blockIdx.x;
@@ -90,15 +90,13 @@ __global__ void __launch_bounds__(kProdThreads) act_quant_kernel(const AqParams 
     pdl_wait();
     pdl_launch_dependents();
 
-    float rf = 1.0f;
-    if constexpr (NORM) rf = row_rms_scale(h, K, p.eps, tid, 1, s_warp, &s_rf);
     void* out;
     if constexpr (MODE == 0)
         out = reinterpret_cast<float*>(p.out) + m * K;
     else
         out = reinterpret_cast<int8_t*>(p.out) + m * K;
-    row_quantize<MODE, NORM>(h, p.gain, rf, K, tid, out, p.rows * K,
-                             MODE == 0 ? nullptr : p.xd + m * nb);
+    row_produce<MODE, NORM>(h, p.gain, p.eps, K, tid, 1, s_pair, &s_rf, out, p.rows * K,
+                            MODE == 0 ? nullptr : p.xd + m * nb);
 }
 
 template <int MODE, bool NORM>

@@ -6,10 +6,9 @@
 // thread t owns the float4 groups t, t + kProdThreads, ... of the row.
 //  * Sum of squares: each square is split exactly by an FMA and accumulated
 //    as an f32 pair (error-free transforms, ~48 bits), reduced over the warp
-//    in a fixed xor order, then the warp sums are added in warp order in f64
-//    (f64 arithmetic and f32<->f64 conversions are slow on this part, so only
-//    one value per warp goes to f64).  r = 1/sqrt(ss/K + eps) in f64 with
-//    IEEE division and square root; rf = float(r).
+//    and then over the warps in fixed orders.  rf = float(1/sqrt(ss/K + eps))
+//    is evaluated in f32 pairs to ~2^-44 relative before its final rounding
+//    (the part's FP64 latency would dominate the producer).
 //  * Quantisation: a 32-value block is 8 consecutive float4 groups, held by 8
 //    consecutive lanes; amax is an exact max over 3 shuffles, the scale is
 //    d = amax / lim (IEEE division) and every code is round_half_away(x / d).
@@ -37,107 +36,238 @@ __device__ __forceinline__ void pair_add_sq(float& sh, float& sl, float v) {
     sl = __fadd_rn(sl, pe);
 }
 
-// rf = float(1 / sqrt(sum(h^2)/K + eps)) for one row.  All kProdThreads
-// threads call it; `bar` is a named-barrier id over exactly those threads.
-// s_warp: kProdWarps doubles of shared scratch; s_rf: one float.
-__device__ __forceinline__ float row_rms_scale(const float* h, int64_t K, float eps, int tid,
-                                               int bar, double* s_warp, float* s_rf) {
-    float sh = 0.0f, sl = 0.0f;
-    const int64_t groups = K >> 2;
-    for (int64_t gi = tid; gi < groups; gi += kProdThreads) {
-        const int4 v = ldg_nc_v4(h + 4 * gi);
-        pair_add_sq(sh, sl, __int_as_float(v.x));
-        pair_add_sq(sh, sl, __int_as_float(v.y));
-        pair_add_sq(sh, sl, __int_as_float(v.z));
-        pair_add_sq(sh, sl, __int_as_float(v.w));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float rh = __shfl_xor_sync(0xffffffffu, sh, o);
-        const float rl = __shfl_xor_sync(0xffffffffu, sl, o);
-        pair_add(sh, sl, rh);
-        sl = __fadd_rn(sl, rl);
-    }
-    if ((tid & 31) == 0) s_warp[tid >> 5] = double(sh) + double(sl);
-    named_bar(bar, kProdThreads);
-    if (tid == 0) {
-        double t = 0.0;
-        for (int w = 0; w < kProdWarps; ++w) t += s_warp[w];
-        const double mean = __ddiv_rn(t, double(K));
-        const double r = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(mean, double(eps))));
-        *s_rf = __double2float_rn(r);
-    }
-    named_bar(bar, kProdThreads);
-    return *s_rf;
+// Float4 groups of the row a thread keeps in registers between the two
+// passes (K <= kProdThreads * 4 * kProdCache = 16384); longer rows reload
+// the groups beyond from global memory.
+constexpr int kProdCache = 8;
+
+// f32 pair arithmetic for the one scalar chain of the row (the part's FP64
+// rate and f32<->f64 conversions are far too slow for a latency path).
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    e = __fsub_rn(b, __fsub_rn(s, a));
 }
 
-// Normalises (when rf is given) and quantises one row in the mode's layout.
-// MODE 0 writes f32 x; MODE 1 one int8 code plane; MODE 2 the hi plane at
-// out and the lo plane at out + plane.  xd receives one scale per block.
-// Every thread of the kProdThreads calls it (block lanes meet in shuffles).
+// rf = float(1 / sqrt(S/K + eps)) for S = sh + sl, to about 2^-44 relative
+// before the final rounding: the quotient S/K with its exact FMA remainder,
+// then one Newton step on the hardware reciprocal square root evaluated in
+// f32 pairs.
+__device__ __forceinline__ float rms_scale_from_sum(float sh, float sl, int64_t K, float eps) {
+    const float kf = float(K);   // exact for K < 2^24
+    const float q1 = __fdiv_rn(sh, kf);
+    const float rem = __fmaf_rn(-q1, kf, sh);   // sh - q1*K exactly
+    const float q2 = __fdiv_rn(__fadd_rn(rem, sl), kf);
+    float mh, ml;
+    fast_two_sum(q1, q2, mh, ml);
+    float vh, vl;   // v = mean + eps
+    {
+        float s, e;
+        const float bb = __fadd_rn(mh, eps);
+        s = bb;
+        const float z = __fsub_rn(s, mh);
+        e = __fadd_rn(__fsub_rn(mh, __fsub_rn(s, z)), __fsub_rn(eps, z));
+        fast_two_sum(s, __fadd_rn(e, ml), vh, vl);
+    }
+    if (!(vh > 0.0f)) return vh == 0.0f ? INFINITY : __int_as_float(0x7fc00000);
+    if (isinf(vh)) return 0.0f;
+    const float y0 = rsqrtf(vh);
+    // t = v*y0^2 - 1, with y0^2 and v*y0^2 split exactly by FMAs
+    const float ph = __fmul_rn(y0, y0);
+    const float pl = __fmaf_rn(y0, y0, -ph);
+    const float ah = __fmul_rn(vh, ph);
+    float al = __fmaf_rn(vh, ph, -ah);
+    al = __fmaf_rn(vh, pl, al);
+    al = __fmaf_rn(vl, ph, al);
+    const float tt = __fadd_rn(__fsub_rn(ah, 1.0f), al);   // ah - 1 is exact (ah ~ 1)
+    const float corr = __fmul_rn(__fmul_rn(-0.5f, y0), tt);
+    float rh, rl;
+    fast_two_sum(y0, corr, rh, rl);
+    return __fadd_rn(rh, rl);
+}
+
+// round_half_away(x / d) clamped to [-lim, lim] (d > 0), with rcp the
+// correctly rounded 1/d.  qa = x*rcp is within 1.5*2^-23 (relative) of the
+// IEEE quotient x/d, so the two round alike unless |qa| lies within
+// 2^-21*|qa| of a half-integer; such codes (about 2^-20*|q| of them) take the
+// IEEE division itself, in a branch of their own.
+__device__ __forceinline__ int quantize_code_rcp(float x, float d, float rcp, float lim) {
+    const float qa = __fmul_rn(x, rcp);
+    const float aq = fabsf(qa);
+    const float u = __fadd_rn(aq, 0.5f);
+    float v = floorf(u);
+    const float fr = __fsub_rn(u, v);   // exact: u and floor(u) share an exponent range
+    const float thr = __fmaf_rn(-aq, 0x1p-21f, 0.5f);
+    if (fabsf(__fsub_rn(fr, 0.5f)) > thr) {
+        // too close to a tie: the IEEE quotient decides (rare, divergent)
+        v = fabsf(roundf(__fdiv_rn(x, d)));
+    }
+    v = fminf(v, lim);
+    const int c = static_cast<int>(v);
+    return x < 0.0f ? -c : c;
+}
+
+// One float4 group of the row: normalise, then store (MODE 0) or quantise
+// with its block (MODE 1, 2).  All lanes of the warp call it together.
 template <int MODE, bool NORM>
-__device__ __forceinline__ void row_quantize(const float* h, const float* gain, float rf,
-                                             int64_t K, int tid, void* out, int64_t plane,
-                                             float* xd) {
+__device__ __forceinline__ void produce_group(float (&x)[4], const float (&gg)[4], bool has_gain,
+                                              float rf, int64_t gi, bool live, void* out,
+                                              int64_t plane, float* xd) {
+    if constexpr (NORM) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[e] = __fmul_rn(x[e], rf);
+            if (has_gain) x[e] = __fmul_rn(x[e], gg[e]);
+        }
+    }
+    if constexpr (MODE == 0) {
+        if (live)
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + 4 * gi) =
+                make_float4(x[0], x[1], x[2], x[3]);
+    } else {
+        float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        if (live) {
+            const float lim = (MODE == 1) ? 127.0f : 8191.0f;
+            const float d = __fdiv_rn(a, lim);
+            int code[4] = {0, 0, 0, 0};
+            if (d != 0.0f) {
+                const float rcp = __frcp_rn(d);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) code[e] = quantize_code_rcp(x[e], d, rcp, lim);
+            }
+            int8_t* o = reinterpret_cast<int8_t*>(out);
+            if constexpr (MODE == 1) {
+                const unsigned w = (unsigned(code[0]) & 0xffu) | ((unsigned(code[1]) & 0xffu) << 8) |
+                                   ((unsigned(code[2]) & 0xffu) << 16) | (unsigned(code[3]) << 24);
+                *reinterpret_cast<unsigned*>(o + 4 * gi) = w;
+            } else {
+                unsigned wh = 0, wl = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int lo = ((code[e] + 64) & 127) - 64;   // Euclidean residue, centred
+                    const int hi = (code[e] - lo) >> 7;           // exact
+                    wh |= (unsigned(hi) & 0xffu) << (8 * e);
+                    wl |= (unsigned(lo) & 0xffu) << (8 * e);
+                }
+                *reinterpret_cast<unsigned*>(o + 4 * gi) = wh;
+                *reinterpret_cast<unsigned*>(o + plane + 4 * gi) = wl;
+            }
+            if ((gi & 7) == 0) xd[gi >> 3] = d;
+        }
+    }
+}
+
+// The producer of one row: optional RMSNorm (x = (h * rf) * g), then the
+// mode's quantisation (MODE 0 writes f32 x; MODE 1 one int8 code plane;
+// MODE 2 the hi plane at out and the lo plane at out + plane; xd receives one
+// scale per block).  Every one of the kProdThreads threads calls it; `bar` is
+// a named-barrier id over exactly those threads.  s_pair: kProdWarps float2
+// of shared scratch; s_rf: one float.
+//  * Sum of squares: each square is split exactly by an FMA and accumulated
+//    as an f32 pair (error-free transforms, ~48 bits), reduced over the warp
+//    in a fixed xor order, then over the warps in a fixed tree.
+//  * Quantisation: a 32-value block is 8 consecutive float4 groups, held by 8
+//    consecutive lanes; amax is an exact max over 3 shuffles, the scale is
+//    d = amax / lim (IEEE division) and every code is round_half_away(x / d).
+template <int MODE, bool NORM>
+__device__ __forceinline__ void row_produce(const float* h, const float* gain, float eps,
+                                            int64_t K, int tid, int bar, float2* s_pair,
+                                            float* s_rf, void* out, int64_t plane, float* xd) {
     const int64_t groups = K >> 2;
-    // Every lane of a warp runs the same number of iterations (groups is a
-    // multiple of 8 and the stride a multiple of 32), so shuffles stay full.
-    for (int64_t gi = tid; gi < ((groups + 31) & ~int64_t(31)); gi += kProdThreads) {
+    // every lane of a warp runs the same iterations (groups is a multiple of 8
+    // and the stride a multiple of 32), so the block shuffles stay full
+    const int iters = int((groups + kProdThreads - 1) / kProdThreads);
+    float4 hv[kProdCache], gv[kProdCache];
+#pragma unroll
+    for (int j = 0; j < kProdCache; ++j) {
+        const int64_t gi = tid + int64_t(j) * kProdThreads;
+        hv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        gv[j] = make_float4(1.f, 1.f, 1.f, 1.f);
+        if (j < iters && gi < groups) {
+            const int4 v = ldg_nc_v4(h + 4 * gi);
+            hv[j] = make_float4(__int_as_float(v.x), __int_as_float(v.y), __int_as_float(v.z),
+                                __int_as_float(v.w));
+            if (NORM && gain) {
+                const int4 g4 = ldg_nc_v4(gain + 4 * gi);
+                gv[j] = make_float4(__int_as_float(g4.x), __int_as_float(g4.y),
+                                    __int_as_float(g4.z), __int_as_float(g4.w));
+            }
+        }
+    }
+    float rf = 1.0f;
+    if constexpr (NORM) {
+        float sh = 0.0f, sl = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kProdCache; ++j) {
+            pair_add_sq(sh, sl, hv[j].x);
+            pair_add_sq(sh, sl, hv[j].y);
+            pair_add_sq(sh, sl, hv[j].z);
+            pair_add_sq(sh, sl, hv[j].w);
+        }
+        for (int64_t gi = tid + int64_t(kProdCache) * kProdThreads; gi < groups; gi += kProdThreads) {
+            const int4 v = ldg_nc_v4(h + 4 * gi);
+            pair_add_sq(sh, sl, __int_as_float(v.x));
+            pair_add_sq(sh, sl, __int_as_float(v.y));
+            pair_add_sq(sh, sl, __int_as_float(v.z));
+            pair_add_sq(sh, sl, __int_as_float(v.w));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float rh = __shfl_xor_sync(0xffffffffu, sh, o);
+            const float rl = __shfl_xor_sync(0xffffffffu, sl, o);
+            pair_add(sh, sl, rh);
+            sl = __fadd_rn(sl, rl);
+        }
+        if ((tid & 31) == 0) s_pair[tid >> 5] = make_float2(sh, sl);
+        named_bar(bar, kProdThreads);
+        if (tid < 32) {
+            float2 v = tid < kProdWarps ? s_pair[tid] : make_float2(0.0f, 0.0f);
+            sh = v.x;
+            sl = v.y;
+#pragma unroll
+            for (int o = kProdWarps / 2; o > 0; o >>= 1) {
+                const float rh = __shfl_xor_sync(0xffffffffu, sh, o);
+                const float rl = __shfl_xor_sync(0xffffffffu, sl, o);
+                pair_add(sh, sl, rh);
+                sl = __fadd_rn(sl, rl);
+            }
+            if (tid == 0) *s_rf = rms_scale_from_sum(sh, sl, K, eps);
+        }
+        named_bar(bar, kProdThreads);
+        rf = *s_rf;
+    }
+    // cached groups: unrolled, so independent groups overlap their latencies
+#pragma unroll
+    for (int j = 0; j < kProdCache; ++j) {
+        if (j < iters) {
+            const int64_t gi = tid + int64_t(j) * kProdThreads;
+            float x[4] = {hv[j].x, hv[j].y, hv[j].z, hv[j].w};
+            const float gg[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+            produce_group<MODE, NORM>(x, gg, gain != nullptr, rf, gi, gi < groups, out, plane, xd);
+        }
+    }
+    for (int j = kProdCache; j < iters; ++j) {
+        const int64_t gi = tid + int64_t(j) * kProdThreads;
         const bool live = gi < groups;
         float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float gg[4] = {1.0f, 1.0f, 1.0f, 1.0f};
         if (live) {
             const int4 v = ldg_nc_v4(h + 4 * gi);
             x[0] = __int_as_float(v.x);
             x[1] = __int_as_float(v.y);
             x[2] = __int_as_float(v.z);
             x[3] = __int_as_float(v.w);
-            if constexpr (NORM) {
-                int4 g4 = make_int4(0x3f800000, 0x3f800000, 0x3f800000, 0x3f800000);
-                if (gain) g4 = ldg_nc_v4(gain + 4 * gi);
-                const float gv[4] = {__int_as_float(g4.x), __int_as_float(g4.y),
-                                     __int_as_float(g4.z), __int_as_float(g4.w)};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    x[e] = __fmul_rn(x[e], rf);
-                    if (gain) x[e] = __fmul_rn(x[e], gv[e]);
-                }
+            if (NORM && gain) {
+                const int4 g4 = ldg_nc_v4(gain + 4 * gi);
+                gg[0] = __int_as_float(g4.x);
+                gg[1] = __int_as_float(g4.y);
+                gg[2] = __int_as_float(g4.z);
+                gg[3] = __int_as_float(g4.w);
             }
         }
-        if constexpr (MODE == 0) {
-            if (live)
-                *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + 4 * gi) =
-                    make_float4(x[0], x[1], x[2], x[3]);
-        } else {
-            float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-            if (live) {
-                const float lim = (MODE == 1) ? 127.0f : 8191.0f;
-                const float d = __fdiv_rn(a, lim);
-                int code[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) code[e] = quantize_code(x[e], d, lim);
-                int8_t* o = reinterpret_cast<int8_t*>(out);
-                if constexpr (MODE == 1) {
-                    const unsigned w = (unsigned(code[0]) & 0xffu) | ((unsigned(code[1]) & 0xffu) << 8) |
-                                       ((unsigned(code[2]) & 0xffu) << 16) | (unsigned(code[3]) << 24);
-                    *reinterpret_cast<unsigned*>(o + 4 * gi) = w;
-                } else {
-                    unsigned wh = 0, wl = 0;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int lo = ((code[e] + 64) & 127) - 64;   // Euclidean residue, centred
-                        const int hi = (code[e] - lo) >> 7;           // exact
-                        wh |= (unsigned(hi) & 0xffu) << (8 * e);
-                        wl |= (unsigned(lo) & 0xffu) << (8 * e);
-                    }
-                    *reinterpret_cast<unsigned*>(o + 4 * gi) = wh;
-                    *reinterpret_cast<unsigned*>(o + plane + 4 * gi) = wl;
-                }
-                if ((gi & 7) == 0) xd[gi >> 3] = d;
-            }
-        }
+        produce_group<MODE, NORM>(x, gg, gain != nullptr, rf, gi, live, out, plane, xd);
     }
 }
 
