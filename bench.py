@@ -117,14 +117,17 @@ class ClockSampler:
 # ---------------------------------------------------------- distributed
 
 def dist_init():
+    """One process per GPU (replicas: no data-path collective).  Q8_BENCH_BACKEND
+    overrides the process-group backend (the CPU tests use gloo)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if torch.cuda.is_available():
+        backend = os.environ.get("Q8_BENCH_BACKEND") or (
+            "nccl" if torch.cuda.is_available() else "gloo")
+        if backend == "nccl":
             torch.cuda.set_device(local)
         dist.init_process_group(backend=backend)
     elif torch.cuda.is_available():
@@ -136,6 +139,12 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def aggregate_gbps(world, bytes_per_rank_step, ms_per_step_max):
+    """Whole-job rate: the bytes every rank streamed per step over the slowest
+    rank's step time (replicas, weak scaling)."""
+    return world * bytes_per_rank_step / (ms_per_step_max * 1e-3) / 1e9
 
 
 def max_over_ranks(world, v):
@@ -378,7 +387,7 @@ def run_ours(args, world, rank, local):
     clocks = sampler.stop() if sampler else None
     ms = max_over_ranks(world, ms)
     step_bytes = len(MODES) * LAYER_BYTES
-    value = world * step_bytes / (ms * 1e-3) / 1e9
+    value = aggregate_gbps(world, step_bytes, ms)
 
     # per-mode breakdown (same protocol)
     per_mode = {}
@@ -455,7 +464,7 @@ def run_ours(args, world, rank, local):
         e2e_graphs[i % COPIES].replay()
         torch.cuda.synchronize(dev)      # the host reads every step's outputs
     e2e_ms = max_over_ranks(world, (time.perf_counter() - t0) / args.steps * 1e3)
-    e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+    e2e = {"value": round(aggregate_gbps(world, step_bytes, e2e_ms), 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
            "note": "host wall clock per step: graph replay of H2D copy + 12 C-ABI calls + D2H "
                    "copy, then stream sync"}
