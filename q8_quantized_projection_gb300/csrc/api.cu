@@ -144,7 +144,9 @@ q8_status check_proj_args(int mode, const int8_t* q, const uint16_t* s, int64_t 
 }  // namespace
 
 namespace q8 {
-int gemv_max_rows(int mode) { return mode == 0 ? 4 : 16; }
+// rows per CUDA-core launch: the decode kernel's widest row count per mode
+// (more rows are split into groups, each reading the weights once)
+int gemv_max_rows(int mode) { return mode == 0 ? 2 : mode == 1 ? 8 : 4; }
 }  // namespace q8
 
 extern "C" {

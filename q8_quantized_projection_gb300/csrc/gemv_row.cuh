@@ -1,4 +1,4 @@
-// gemv_row.cuh -- the decode-step projection (1 or 2 activation rows), sm_103a.
+// gemv_row.cuh -- the decode-step projection (1 to 8 activation rows), sm_103a.
 //
 // The decode step is pure HBM streaming: 34 bytes per 32 weights, read once.
 // The kernel keeps the memory side as simple as the bulk-copy engine likes it
@@ -40,9 +40,11 @@ constexpr int kRowStage = 32768;       // weight bytes of one stage at most
 constexpr int kRowRing = 163840;       // weight bytes in flight per CTA
 constexpr int kRowPsumBytes = 16384;   // part sums of one super-block of rows
 
+// 16-byte chunks a lane owns per part: the activation registers (R rows, one
+// or two planes, or 17 words of fixed point in f32 mode) stay within ~32.
 template <int MODE, int R>
 __host__ __device__ constexpr int row_cpl() {
-    return MODE == 1 ? (R == 1 ? 8 : 4) : MODE == 2 ? (R == 1 ? 4 : 2) : (R == 1 ? 2 : 1);
+    return MODE == 1 ? 8 / R : MODE == 2 ? 4 / R : (R == 1 ? 2 : 1);
 }
 
 // Shared bytes of the fused producer's activation: codes (two planes at most)
@@ -104,6 +106,31 @@ inline bool row_kernel_fits(int64_t K) {
     using A = typename AccT<MODE>::T;
     const RowGeo g = row_geo(1, K, 1, 0, row_cpl<MODE, R>(), int(R * sizeof(A)));
     return g.sbrows >= g.RS;
+}
+
+// Sums each of R per-lane values over the warp with a butterfly that halves
+// the rows at every exchange (log2(R) exchanges of R/2, R/4, ... values, then
+// a plain reduction over the 32/R lanes left): lanes [r*32/R, (r+1)*32/R)
+// end with row r's total.  Fixed order, so bitwise reproducible.
+template <int R>
+__device__ __forceinline__ float warp_sum_rows(const float (&v)[R], int lane) {
+    float cur[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) cur[i] = v[i];
+#pragma unroll
+    for (int step = 16, h = R / 2; h >= 1; step >>= 1, h >>= 1) {
+        const bool upper = (lane & step) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? cur[i] : cur[i + h];
+            const float keep = upper ? cur[i + h] : cur[i];
+            cur[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
+        }
+    }
+    float s = cur[0];
+#pragma unroll
+    for (int o = 16 / R; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
 }
 
 __device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v, long long i) {
@@ -433,12 +460,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 }
             }
             if (have) {
+                A* ps = psum + ((size_t(row_sb) * g.nks + sl) * g.nprr + pw) * R;
+                if constexpr (MODE == 0) {
 #pragma unroll
-                for (int m = 0; m < R; ++m) part[m] = warp_sum(part[m]);
-                if (lane == 0) {
-                    A* ps = psum + ((size_t(row_sb) * g.nks + sl) * g.nprr + pw) * R;
+                    for (int m = 0; m < R; ++m) part[m] = warp_sum(part[m]);
+                    if (lane == 0) {
 #pragma unroll
-                    for (int m = 0; m < R; ++m) ps[m] = part[m];
+                        for (int m = 0; m < R; ++m) ps[m] = part[m];
+                    }
+                } else {
+                    const float tot = warp_sum_rows<R>(part, lane);
+                    if ((lane & (32 / R - 1)) == 0) ps[lane / (32 / R)] = tot;
                 }
             }
             if (++rbi == nrb) {

@@ -95,7 +95,7 @@ SHAPES = [(1, 32), (3, 64), (37, 96), (1000, 1024), (301, 4096), (77, 4128), (64
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("n,k", SHAPES)
-@pytest.mark.parametrize("rows", [1, 2, 3, 8, 13, 16, 17])
+@pytest.mark.parametrize("rows", [1, 2, 3, 4, 5, 7, 8, 13, 16, 17])
 def test_proj_parity(mode, n, k, rows):
     if rows > 3 and n * k > 1000 * 1024:
         rows = 3  # keep the oracle within seconds on the largest shapes
