@@ -472,6 +472,11 @@ def run_ours(args, world, rank, local):
 
     sweeps = {} if args.no_sweeps else run_sweeps(native, torch, dev, capture, timed, Q, S)
 
+    # a kernel whose bounded wait ran out reports it here; its timings are void
+    dev_err = native.q8_device_error()
+    if dev_err:
+        print(f"bench: device error word {dev_err}: a kernel wait timed out", file=sys.stderr)
+
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base = cpu_baseline(mats, hs, budget_s=args.cpu_budget)
@@ -491,8 +496,10 @@ def run_ours(args, world, rank, local):
                "rows_per_s": round(world * len(MODES) * 4 / (ms * 1e-3), 1),
                "modes": per_mode, "roofline": roofline, "cpu_baseline": base, "e2e": e2e,
                "gpu_launches": args.steps * len(MODES) * 4 * launches_per_fused,
-               "clocks": clocks, "sweeps": sweeps}
+               "clocks": clocks, "sweeps": sweeps, "device_error": dev_err}
         print(json.dumps(out), flush=True)
+    if dev_err:
+        sys.exit(3)
 
 
 def run_sweeps(native, torch, dev, capture, timed, Q, S):

@@ -18,12 +18,13 @@
 //   warp 1      owns TMEM; one thread issues the MMAs (kind::f16, K = 16, two
 //               per block and activation plane) into one of NSLOT accumulator
 //               slots, and commits them;
-//   warps 2-5   converters, two blocks at a time: weights int8 -> f16 straight
+//   warps 2-5   converters (2-9: two groups of four taking alternate block
+//               pairs), two blocks at a time: weights int8 -> f16 straight
 //               into TMEM (the MMA's A operand, lane = weight row), activation
 //               codes int8 -> f16 operand tiles in shared memory (K-major, no
 //               swizzle), and both blocks' scales into the scale ring entries
 //               of their accumulator slots;
-//   warps 6-13  epilogue: TMEM -> registers, rescale with packed f32x2 FMAs,
+//   next 8      epilogue: TMEM -> registers, rescale with packed f32x2 FMAs,
 //               accumulate.
 // A converted pair is freed by its MMAs' own completion (commit); an
 // accumulator slot and its scale-ring entry by the epilogue.  TMEM columns
@@ -48,7 +49,6 @@ constexpr int kCkGroup = 8;        // blocks per weight-scale group (16 bytes of
 constexpr int kCkPairs = 4;        // converted block pairs in flight
 constexpr int kCkAccCols = 384;    // TMEM columns for accumulator slots
 constexpr int kCkEpiWarps = 8;
-constexpr int kCkThreads = (6 + kCkEpiWarps) * 32;
 constexpr int kCkMaxSplit = 8;
 constexpr int kCkSmemBudget = 227 * 1024;
 
@@ -70,6 +70,12 @@ struct CkCfg {
     static constexpr int kOpPair = 2 * kBBlock;
     static constexpr int kScl = kCkM * 2 + TT * 4;                    // sw[128] f16, xd[TT] f32
     static constexpr int kCW = TT / 2;                                // columns per epilogue warp
+    // Two converter groups take alternate block pairs when there are at
+    // least 4 accumulator slots: a group then never waits on a slot barrier
+    // more than one phase ahead of what it has seen (the parity would alias).
+    static constexpr int kConvGroups = kSlots >= 4 ? 2 : 1;
+    static constexpr int kEpiWarp0 = 2 + 4 * kConvGroups;
+    static constexpr int kThreads = (kEpiWarp0 + kCkEpiWarps) * 32;
     static constexpr int kFixed = kSGroups * kSGroup + kCkPairs * kOpPair + kSlots * kScl +
                                   512 /*barriers*/ + 1024 /*alignment*/;
     static constexpr int kStages = (kCkSmemBudget - kFixed) / kStage < 8
@@ -176,7 +182,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 template <int MODE, int TT, bool DEBUG>
-__global__ void __launch_bounds__(kCkThreads, 1)
+__global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
                  const __grid_constant__ CUtensorMap tm_xl, const __grid_constant__ CUtensorMap tm_s,
                  const __grid_constant__ CUtensorMap tm_xd, const CkParams p) {
@@ -218,11 +224,11 @@ __global__ void __launch_bounds__(kCkThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&st_full[i], 1);
-            mbar_init(&st_empty[i], 4);
+            mbar_init(&st_empty[i], 8);    // each converter warp, once per pair (2 a stage)
         }
         for (int i = 0; i < C::kSGroups; ++i) {
             mbar_init(&sg_full[i], 1);
-            mbar_init(&sg_empty[i], 4);
+            mbar_init(&sg_empty[i], 16);   // each converter warp, once per pair (4 a group)
         }
         for (int i = 0; i < kCkPairs; ++i) {
             mbar_init(&op_full[i], 4);
@@ -246,11 +252,6 @@ __global__ void __launch_bounds__(kCkThreads, 1)
     pdl_launch_dependents();
     const uint32_t stages_a = smem_u32(stages), sgroups_a = smem_u32(sgroups);
     const uint32_t ops_a = smem_u32(ops), scl_a = smem_u32(scl);
-
-    // epilogue accumulators: pairs of activation rows for one weight row
-    uint64_t acc[C::kCW / 2];
-#pragma unroll
-    for (int i = 0; i < C::kCW / 2; ++i) acc[i] = 0;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -327,19 +328,20 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                 mbar_wait(&tm_full[(issued - 1) % C::kSlots], uint32_t((issued - 1) / C::kSlots) & 1u,
                           p.err);
         }
-    } else if (warp < 6) {
+    } else if (warp < C::kEpiWarp0) {
         // ------------------------------------------------------------ converters
+        // group cg converts the pairs pr = cg (mod kConvGroups)
+        const int cg = (warp - 2) >> 2;
         const int rw = (warp & 3) * 32 + lane;        // weight row = TMEM lane; activation row
         const uint32_t a_lane = uint32_t((warp & 3) * 32) << 16;
         const bool act = rw < np;                     // the MMA reads activation rows < np only
         bool ok = true;
-        for (int pr = 0; pr < npairs; ++pr) {
+        for (int pr = cg; pr < npairs; pr += C::kConvGroups) {
             const int s = pr >> 1, half = pr & 1, slot = s % C::kStages;
             const int g = pr >> 2, gs = g % C::kSGroups, ps = pr % kCkPairs;
             const int b0 = 2 * pr, j0 = 2 * half;
-            if (ok && half == 0) ok = mbar_wait(&st_full[slot], uint32_t(s / C::kStages) & 1u, p.err);
-            if (!DEBUG && ok && (pr & 3) == 0)
-                ok = mbar_wait(&sg_full[gs], uint32_t(g / C::kSGroups) & 1u, p.err);
+            if (ok) ok = mbar_wait(&st_full[slot], uint32_t(s / C::kStages) & 1u, p.err);
+            if (!DEBUG && ok) ok = mbar_wait(&sg_full[gs], uint32_t(g / C::kSGroups) & 1u, p.err);
             if (ok && pr >= kCkPairs)
                 ok = mbar_wait(&op_empty[ps], uint32_t(pr / kCkPairs - 1) & 1u, p.err);
             // the scale-ring entries of both blocks are free once the epilogue
@@ -412,13 +414,17 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                     mbar_arrive(&sc_full[b0 % C::kSlots]);
                     mbar_arrive(&sc_full[(b0 + 1) % C::kSlots]);
                 }
-                if (half == 1) mbar_arrive(&st_empty[slot]);
-                if (!DEBUG && (pr & 3) == 3) mbar_arrive(&sg_empty[gs]);
+                mbar_arrive(&st_empty[slot]);
+                if constexpr (!DEBUG) mbar_arrive(&sg_empty[gs]);
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 6;          // 0..7
+        // accumulators: pairs of activation rows for one weight row
+        uint64_t acc[C::kCW / 2];
+#pragma unroll
+        for (int i = 0; i < C::kCW / 2; ++i) acc[i] = 0;
+        const int ew = warp - C::kEpiWarp0;   // 0..7
         const int q = warp & 3;           // TMEM lane quadrant of this warp
         const int h = ew >> 2;            // column half
         const int n = q * 32 + lane;      // weight row within the tile
@@ -459,7 +465,9 @@ __global__ void __launch_bounds__(kCkThreads, 1)
                 const uint64_t sw2 = f2_pack(sw, sw);
                 const uint32_t xdv = e + uint32_t(kCkM * 2 + c0 * 4);
                 // waves of up to 32 columns: all TMEM loads of a wave, one wait
-                constexpr int kWave = C::kCW < 32 ? C::kCW : 32;
+                // registers: two planes or 64 accumulated columns take half-width waves
+                constexpr int kWaveMax = (MODE == 2 || C::kCW > 32) ? 16 : 32;
+                constexpr int kWave = C::kCW < kWaveMax ? C::kCW : kWaveMax;
 #pragma unroll
                 for (int w = 0; w < C::kCW / kWave; ++w) {
                     if (c0 + kWave * w >= np) break;   // warp-uniform
@@ -499,7 +507,28 @@ __global__ void __launch_bounds__(kCkThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tm_empty[ts]);
         }
+        if constexpr (!DEBUG) {
+            if (gridDim.z == 1) {
+                const int64_t row = m0 + n;
+                if (row < p.N) {
+#pragma unroll
+                    for (int i = 0; i < C::kCW; ++i) {
+                        const int64_t t = t0 + c0 + i;
+                        const float v = (i & 1) ? f2_hi(acc[i >> 1]) : f2_lo(acc[i >> 1]);
+                        if (t < p.T) p.y[t * p.N + row] = v;
+                    }
+                }
+            } else {
+                // partial tile [TT][128] f32 in the stage buffers: every stage has
+                // been consumed once this warp has rescaled the last block
+#pragma unroll
+                for (int i = 0; i < C::kCW; ++i)
+                    sts32(stages_a + uint32_t(((c0 + i) * kCkM + n) * 4),
+                          (i & 1) ? uint32_t(acc[i >> 1] >> 32) : uint32_t(acc[i >> 1]));
+            }
+        }
     }
+
 
     tc_fence_before();
     __syncthreads();
@@ -507,55 +536,33 @@ __global__ void __launch_bounds__(kCkThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
-    if constexpr (!DEBUG) {
-        const bool epi = warp >= 6;
-        const int q = warp & 3, h = (warp - 6) >> 2;
-        const int n = q * 32 + lane, c0 = C::kCW * h;
-        if (gridDim.z == 1) {
-            const int64_t row = m0 + n;
-            if (epi && row < p.N) {
-#pragma unroll
-                for (int i = 0; i < C::kCW; ++i) {
-                    const int64_t t = t0 + c0 + i;
-                    const float v = (i & 1) ? f2_hi(acc[i >> 1]) : f2_lo(acc[i >> 1]);
-                    if (t < p.T) p.y[t * p.N + row] = v;
-                }
+    if (!DEBUG && gridDim.z > 1) {
+        cluster_sync();
+        const uint32_t ks = gridDim.z, rank = blockIdx.z;
+        const int n4 = TT * kCkM / 4;
+        const int per = (n4 + int(ks) - 1) / int(ks);
+        const int i_end = min(n4, int(rank + 1) * per);
+        const uint32_t base = stages_a;
+        for (int i = int(rank) * per + tid; i < i_end; i += C::kThreads) {
+            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (uint32_t r = 0; r < ks; ++r) {
+                const float4 v = ld_cluster_v4(cluster_map(base + uint32_t(i) * 16u, r));
+                s.x += v.x;
+                s.y += v.y;
+                s.z += v.z;
+                s.w += v.w;
             }
-        } else {
-            // partial tile [TT][128] f32 in the (now idle) stage buffers
-            if (epi) {
+            const int e = 4 * i, t = e / kCkM, nn = e % kCkM;
+            if (t0 + t < p.T) {
+                float* yr = p.y + (t0 + t) * p.N + m0 + nn;
+                const float sv[4] = {s.x, s.y, s.z, s.w};
 #pragma unroll
-                for (int i = 0; i < C::kCW; ++i)
-                    sts32(stages_a + uint32_t(((c0 + i) * kCkM + n) * 4),
-                          (i & 1) ? uint32_t(acc[i >> 1] >> 32) : uint32_t(acc[i >> 1]));
+                for (int u = 0; u < 4; ++u)
+                    if (m0 + nn + u < p.N) yr[u] = sv[u];
             }
-            cluster_sync();
-            const uint32_t ks = gridDim.z, rank = blockIdx.z;
-            const int n4 = TT * kCkM / 4;
-            const int per = (n4 + int(ks) - 1) / int(ks);
-            const int i_end = min(n4, int(rank + 1) * per);
-            const uint32_t base = stages_a;
-            for (int i = int(rank) * per + tid; i < i_end; i += kCkThreads) {
-                float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (uint32_t r = 0; r < ks; ++r) {
-                    const float4 v = ld_cluster_v4(cluster_map(base + uint32_t(i) * 16u, r));
-                    s.x += v.x;
-                    s.y += v.y;
-                    s.z += v.z;
-                    s.w += v.w;
-                }
-                const int e = 4 * i, t = e / kCkM, nn = e % kCkM;
-                if (t0 + t < p.T) {
-                    float* yr = p.y + (t0 + t) * p.N + m0 + nn;
-                    const float sv[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (m0 + nn + u < p.N) yr[u] = sv[u];
-                }
-            }
-            // no CTA may leave while another still reads its shared memory
-            cluster_sync();
         }
+        // no CTA may leave while another still reads its shared memory
+        cluster_sync();
     }
 }
 
@@ -611,7 +618,7 @@ static int active_clusters(int ks, const LaunchCtx& ctx) {
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = unsigned(ks);
         cfg.gridDim = dim3(1, 1, unsigned(ks));
-        cfg.blockDim = dim3(kCkThreads);
+        cfg.blockDim = dim3(C::kThreads);
         cfg.dynamicSmemBytes = C::kSmem;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -680,7 +687,7 @@ static cudaError_t launch_chunk_t(const int8_t* q, const uint16_t* s, int64_t N,
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attrs[2];
     cfg.gridDim = dim3(unsigned(t_tiles), unsigned(n_tiles), unsigned((groups + per - 1) / per));
-    cfg.blockDim = dim3(kCkThreads);
+    cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = ctx.stream;
     int na = pdl_attrs(ctx, attrs);
