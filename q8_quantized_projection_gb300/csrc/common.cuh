@@ -180,6 +180,12 @@ __device__ __forceinline__ float half_bits_to_float(uint16_t bits) {
 
 // ------------------------------------------------------------ block dots
 
+// float(v) for |v| < 2^22 without a conversion instruction: v added to the
+// bit pattern of 1.5*2^23 is that float plus v, exactly.
+__device__ __forceinline__ float small_int_to_float(int v) {
+    return __fsub_rn(__int_as_float(0x4B400000 + v), 12582912.0f);
+}
+
 // Exact int32 dot of 16 int8 weights with 16 int8 activation codes.
 __device__ __forceinline__ int dot16_i8(const int4 w, const int4 a) {
     int acc = __dp4a(w.x, a.x, 0);

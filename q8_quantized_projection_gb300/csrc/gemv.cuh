@@ -190,8 +190,8 @@ __device__ __forceinline__ long long fix_dot(const int4 w, const FixChunk& f) {
 __device__ __forceinline__ DF scaled_pair(float f, long long V) {
     const int vh = int(V >> 21);
     const int vl = int(V & 0x1fffff);
-    const float fh = __int2float_rn(vh) * 2097152.0f;   // exact
-    const float fl = __int2float_rn(vl);                // exact
+    const float fh = small_int_to_float(vh) * 2097152.0f;   // exact: |vh| < 2^21
+    const float fl = small_int_to_float(vl);                // exact: 0 <= vl < 2^21
     const float p1 = __fmul_rn(f, fh);
     const float e1 = __fmaf_rn(f, fh, -p1);
     const float p2 = __fmul_rn(f, fl);

@@ -452,7 +452,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                                 for (int cc = 0; cc < GC; ++cc) {
                                     const int isum = (MODE == 1) ? dot16_i8(w[cc], a1[c0 + cc][m])
                                                                  : dot16_i8x2(w[cc], a1[c0 + cc][m], a2[c0 + cc][m]);
-                                    part[m] = fmaf(float(isum), sw[cc] * xdv[c0 + cc][m], part[m]);
+                                    // |isum| < 2^18 (one word) / 2^24 (two words)
+                                    const float fi = MODE == 1 ? small_int_to_float(isum) : float(isum);
+                                    part[m] = fmaf(fi, sw[cc] * xdv[c0 + cc][m], part[m]);
                                 }
                             }
                         }

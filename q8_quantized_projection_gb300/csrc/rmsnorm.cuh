@@ -85,25 +85,38 @@ __device__ __forceinline__ float rms_scale_from_sum(float sh, float sl, int64_t 
     return __fadd_rn(rh, rl);
 }
 
-// round_half_away(x / d) clamped to [-lim, lim] (d > 0), with rcp the
-// correctly rounded 1/d.  qa = x*rcp is within 1.5*2^-23 (relative) of the
-// IEEE quotient x/d, so the two round alike unless |qa| lies within
-// 2^-21*|qa| of a half-integer; such codes (about 2^-20*|q| of them) take the
-// IEEE division itself, in a branch of their own.
-__device__ __forceinline__ int quantize_code_rcp(float x, float d, float rcp, float lim) {
-    const float qa = __fmul_rn(x, rcp);
-    const float aq = fabsf(qa);
-    const float u = __fadd_rn(aq, 0.5f);
-    float v = floorf(u);
-    const float fr = __fsub_rn(u, v);   // exact: u and floor(u) share an exponent range
-    const float thr = __fmaf_rn(-aq, 0x1p-21f, 0.5f);
-    if (fabsf(__fsub_rn(fr, 0.5f)) > thr) {
-        // too close to a tie: the IEEE quotient decides (rare, divergent)
-        v = fabsf(roundf(__fdiv_rn(x, d)));
+// 1/d to within one ulp: the hardware reciprocal estimate refined by one
+// Newton step, r1 = r0 + r0*(1 - d*r0), evaluated with FMAs.
+__device__ __forceinline__ float recip_refined(float d) {
+    float r0;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r0) : "f"(d));
+    const float e = __fmaf_rn(-d, r0, 1.0f);
+    return __fmaf_rn(r0, e, r0);
+}
+
+// The 4 codes round_half_away(x / d), clamped to [-lim, lim] (d > 0), of one
+// float4 group.  qa = x*(1/d) with 1/d within one ulp is within 2^-22
+// (relative) of the IEEE quotient x/d, so qa and x/d round alike unless |qa|
+// lies within 2^-21*|qa| of a half-integer; only those values take the IEEE
+// division (a divergent branch, about 2^-20*|q| of the codes).  Away from
+// ties, rounding |qa| < 2^22 to the nearest integer is exact by adding and
+// subtracting 1.5*2^23, whose low bits then hold the integer: no conversion
+// instruction (a narrow pipe on this part) on the common path.
+__device__ __forceinline__ void quantize4(const float (&x)[4], float d, float lim, int (&code)[4]) {
+    constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
+    const float rcp = recip_refined(d);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float aq = fabsf(__fmul_rn(x[e], rcp));
+        const float t = __fadd_rn(fminf(aq, lim + 1.0f), kMagic);
+        const float vf = __fsub_rn(t, kMagic);                     // nearest integer, exact
+        int c = __float_as_int(t) - __float_as_int(kMagic);
+        const float dist = fabsf(__fsub_rn(aq, vf));              // to the nearest integer
+        if (dist > __fmaf_rn(-aq, 0x1p-21f, 0.5f))
+            c = static_cast<int>(fabsf(roundf(__fdiv_rn(x[e], d))));   // near a tie: IEEE decides
+        c = min(c, static_cast<int>(lim));
+        code[e] = x[e] < 0.0f ? -c : c;
     }
-    v = fminf(v, lim);
-    const int c = static_cast<int>(v);
-    return x < 0.0f ? -c : c;
 }
 
 // One float4 group of the row: normalise, then store (MODE 0) or quantise
@@ -132,11 +145,8 @@ __device__ __forceinline__ void produce_group(float (&x)[4], const float (&gg)[4
             const float lim = (MODE == 1) ? 127.0f : 8191.0f;
             const float d = __fdiv_rn(a, lim);
             int code[4] = {0, 0, 0, 0};
-            if (d != 0.0f) {
-                const float rcp = __frcp_rn(d);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) code[e] = quantize_code_rcp(x[e], d, rcp, lim);
-            }
+            quantize4(x, d == 0.0f ? 1.0f : d, lim, code);   // d == 0: every x is 0
+            if (d == 0.0f) code[0] = code[1] = code[2] = code[3] = 0;
             int8_t* o = reinterpret_cast<int8_t*>(out);
             if constexpr (MODE == 1) {
                 const unsigned w = (unsigned(code[0]) & 0xffu) | ((unsigned(code[1]) & 0xffu) << 8) |
