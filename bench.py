@@ -280,7 +280,7 @@ def run_ours(args, world, rank, local):
          for m in MODES}
     WS = {m: [torch.empty(native.q8_proj_fused_workspace(m, 1, k), dtype=torch.uint8, device=dev)
               for _, _, k in synth.LAYER_D4096] for m in MODES}
-    launches_per_fused = 2
+    launches_per_fused = 1   # every mode runs its producer inside the decode kernel
 
     def step(i, modes=MODES):
         c = i % COPIES
@@ -468,7 +468,7 @@ def run_ours(args, world, rank, local):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
            "note": "host wall clock per step: graph replay of H2D copy + 12 C-ABI calls + D2H "
                    "copy, then stream sync"}
-    launches_per_fused = 2
+    launches_per_fused = 1   # every mode runs its producer inside the decode kernel
 
     sweeps = {} if args.no_sweeps else run_sweeps(native, torch, dev, capture, timed, Q, S)
 

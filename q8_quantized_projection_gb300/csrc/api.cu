@@ -10,6 +10,7 @@ namespace q8 {
 cudaError_t launch_gemv_mode0(const GemvArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_gemv_mode1(const GemvArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_gemv_mode2(const GemvArgs& a, const LaunchCtx& ctx);
+cudaError_t launch_gemv_fused_mode0(const GemvArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_gemv_fused_mode1(const GemvArgs& a, const LaunchCtx& ctx);
 cudaError_t launch_gemv_fused_mode2(const GemvArgs& a, const LaunchCtx& ctx);
 }  // namespace q8
@@ -252,7 +253,7 @@ q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N,
     if (ws_bytes < q8_proj_fused_workspace(mode, rows, K)) return Q8_ERR_WORKSPACE;
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
-    if (mode != Q8_ACT_F32 && rows == 1 && K <= kFusedMaxK) {
+    if (rows == 1 && K <= kFusedMaxK) {
         // decode step: one launch, the producer runs inside the projection
         GemvArgs a{};
         a.mode = mode;
@@ -263,11 +264,13 @@ q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N,
         a.rows = 1;
         a.plane = K;
         a.y = y;
+        a.out_f64 = out_f64 ? 1 : 0;
         a.h = h;
         a.gain = gain;
         a.eps = eps;
-        return launched(mode == Q8_ACT_I8 ? launch_gemv_fused_mode1(a, ctx)
-                                          : launch_gemv_fused_mode2(a, ctx));
+        return launched(mode == Q8_ACT_F32 ? launch_gemv_fused_mode0(a, ctx)
+                        : mode == Q8_ACT_I8 ? launch_gemv_fused_mode1(a, ctx)
+                                            : launch_gemv_fused_mode2(a, ctx));
     }
     unsigned char* act = static_cast<unsigned char*>(workspace);
     float* xd = reinterpret_cast<float*>(act + round_up(act_bytes(mode, rows, K), 256));

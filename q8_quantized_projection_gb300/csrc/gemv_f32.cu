@@ -16,4 +16,8 @@ cudaError_t launch_gemv_mode0(const GemvArgs& a, const LaunchCtx& ctx) {
     return a.tok ? dispatch_rows<true>(a, ctx) : dispatch_rows<false>(a, ctx);
 }
 
+cudaError_t launch_gemv_fused_mode0(const GemvArgs& a, const LaunchCtx& ctx) {
+    return launch_gemv_row_t<0, 1, false, true>(a, ctx);
+}
+
 }  // namespace q8

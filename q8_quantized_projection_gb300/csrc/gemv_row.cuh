@@ -55,7 +55,7 @@ template <int MODE, int R, bool FUSE>
 __host__ __device__ constexpr size_t row_smem_bytes() {
     return size_t(kRowRing) + size_t(kRowRing) / 16 + 2 * kGemvMaxStages * sizeof(uint64_t) +
            kRowPsumBytes + size_t(kRowWarps) * R * sizeof(ArgmaxCand) + 64 +
-           (FUSE ? kFusedActBytes : 0);
+           (FUSE && MODE != 0 ? kFusedActBytes : 0);
 }
 
 struct RowGeo {
@@ -133,6 +133,33 @@ __device__ __forceinline__ float warp_sum_rows(const float (&v)[R], int lane) {
     return s;
 }
 
+// Four f32 activation values: read as they are, or (f32 mode with the
+// producer fused) formed as x = (h*rf)*g with the producer's two roundings.
+template <bool FUSE>
+__device__ __forceinline__ void load_x4(const float* x, const float* h, const float* g, float rf,
+                                        float (&v)[4]) {
+    const int4 t4 = ldg_nc_v4(FUSE ? h : x);
+    v[0] = __int_as_float(t4.x);
+    v[1] = __int_as_float(t4.y);
+    v[2] = __int_as_float(t4.z);
+    v[3] = __int_as_float(t4.w);
+    if constexpr (FUSE) {
+        float gg[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+        if (g) {
+            const int4 g4 = ldg_nc_v4(g);
+            gg[0] = __int_as_float(g4.x);
+            gg[1] = __int_as_float(g4.y);
+            gg[2] = __int_as_float(g4.z);
+            gg[3] = __int_as_float(g4.w);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            v[e] = __fmul_rn(v[e], rf);
+            if (g) v[e] = __fmul_rn(v[e], gg[e]);
+        }
+    }
+}
+
 __device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v, long long i) {
     if (v > bv || (v == bv && i < bi)) {
         bv = v;
@@ -142,7 +169,7 @@ __device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v,
 
 template <int MODE, int R, bool ARGMAX, bool FUSE>
 __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvParams p) {
-    static_assert(!FUSE || (MODE != 0 && R == 1), "fused producer: int8 modes, one row");
+    static_assert(!FUSE || R == 1, "fused producer: one row");
     using A = typename AccT<MODE>::T;
     constexpr int CPL = row_cpl<MODE, R>();
     constexpr int NW = kRowWarps;
@@ -246,7 +273,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     const float* actf = reinterpret_cast<const float*>(p.act);
     const float* xdp = p.xd;
     int64_t plane = p.plane;
-    if constexpr (FUSE) {
+    float rf = 1.0f;   // f32 mode, fused: x = (h*rf)*g is formed where it is used
+    if constexpr (FUSE && MODE == 0) {
+        rf = row_rms_scale(p.h, K, p.eps, tid, 1, s_pair, &s_rf);
+    } else if constexpr (FUSE) {
         // The producer, fused: RMSNorm -> quant of the one activation row into
         // shared memory, by the same code and thread layout as act_quant, while
         // the producer warp already streams weights.
@@ -269,11 +299,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
 #pragma unroll
             for (int m = 0; m < R; ++m) {
                 if (m < rows) {
-                    const int4 t4 = ldg_nc_v4(actf + m * K + k);
-                    amax[m] = fmaxf(amax[m], fmaxf(fmaxf(fabsf(__int_as_float(t4.x)),
-                                                         fabsf(__int_as_float(t4.y))),
-                                                   fmaxf(fabsf(__int_as_float(t4.z)),
-                                                         fabsf(__int_as_float(t4.w)))));
+                    float xv[4];
+                    load_x4<FUSE>(actf + m * K + k, p.h + k, p.gain ? p.gain + k : nullptr, rf, xv);
+                    amax[m] = fmaxf(amax[m], fmaxf(fmaxf(fabsf(xv[0]), fabsf(xv[1])),
+                                                   fmaxf(fabsf(xv[2]), fabsf(xv[3]))));
                 }
             }
         }
@@ -366,11 +395,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                                     float xs[16];
 #pragma unroll
                                     for (int u = 0; u < 4; ++u) {
-                                        const int4 t4 = ldg_nc_v4(actf + m * K + k + 4 * u);
-                                        xs[4 * u + 0] = __int_as_float(t4.x);
-                                        xs[4 * u + 1] = __int_as_float(t4.y);
-                                        xs[4 * u + 2] = __int_as_float(t4.z);
-                                        xs[4 * u + 3] = __int_as_float(t4.w);
+                                        float xv[4];
+                                        load_x4<FUSE>(actf + m * K + k + 4 * u, p.h + k + 4 * u,
+                                                      p.gain ? p.gain + k + 4 * u : nullptr, rf, xv);
+                                        xs[4 * u + 0] = xv[0];
+                                        xs[4 * u + 1] = xv[1];
+                                        xs[4 * u + 2] = xv[2];
+                                        xs[4 * u + 3] = xv[3];
                                     }
                                     fx[cc][m] = fix_chunk(xs);
                                     p2s[cc][m] = ldexpf(1.0f, fx[cc][m].e - s_emax[m]);

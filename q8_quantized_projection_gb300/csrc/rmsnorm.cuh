@@ -169,6 +169,54 @@ __device__ __forceinline__ void produce_group(float (&x)[4], const float (&gg)[4
     }
 }
 
+// The thread partials (sh, sl) of the sum of squares -> rf, shared by every
+// producer: the warp reduction in a fixed xor order, then the warps' pairs in
+// a fixed tree, then the scale (rms_scale_from_sum).  All kProdThreads threads
+// call it; `bar` is a named-barrier id over exactly those threads.
+__device__ __forceinline__ float rms_scale_reduce(float sh, float sl, int64_t K, float eps, int tid,
+                                                  int bar, float2* s_pair, float* s_rf) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float rh = __shfl_xor_sync(0xffffffffu, sh, o);
+        const float rl = __shfl_xor_sync(0xffffffffu, sl, o);
+        pair_add(sh, sl, rh);
+        sl = __fadd_rn(sl, rl);
+    }
+    if ((tid & 31) == 0) s_pair[tid >> 5] = make_float2(sh, sl);
+    named_bar(bar, kProdThreads);
+    if (tid < 32) {
+        float2 v = tid < kProdWarps ? s_pair[tid] : make_float2(0.0f, 0.0f);
+        sh = v.x;
+        sl = v.y;
+#pragma unroll
+        for (int o = kProdWarps / 2; o > 0; o >>= 1) {
+            const float rh = __shfl_xor_sync(0xffffffffu, sh, o);
+            const float rl = __shfl_xor_sync(0xffffffffu, sl, o);
+            pair_add(sh, sl, rh);
+            sl = __fadd_rn(sl, rl);
+        }
+        if (tid == 0) *s_rf = rms_scale_from_sum(sh, sl, K, eps);
+    }
+    named_bar(bar, kProdThreads);
+    return *s_rf;
+}
+
+// rf alone (the f32 mode's fused producer, whose consumers form x = (h*rf)*g
+// themselves): the same per-thread order of squares as row_produce, so the
+// same rf.
+__device__ __forceinline__ float row_rms_scale(const float* h, int64_t K, float eps, int tid, int bar,
+                                               float2* s_pair, float* s_rf) {
+    float sh = 0.0f, sl = 0.0f;
+    for (int64_t gi = tid; gi < (K >> 2); gi += kProdThreads) {
+        const int4 v = ldg_nc_v4(h + 4 * gi);
+        pair_add_sq(sh, sl, __int_as_float(v.x));
+        pair_add_sq(sh, sl, __int_as_float(v.y));
+        pair_add_sq(sh, sl, __int_as_float(v.z));
+        pair_add_sq(sh, sl, __int_as_float(v.w));
+    }
+    return rms_scale_reduce(sh, sl, K, eps, tid, bar, s_pair, s_rf);
+}
+
 // The producer of one row: optional RMSNorm (x = (h * rf) * g), then the
 // mode's quantisation (MODE 0 writes f32 x; MODE 1 one int8 code plane;
 // MODE 2 the hi plane at out and the lo plane at out + plane; xd receives one
@@ -223,30 +271,7 @@ __device__ __forceinline__ void row_produce(const float* h, const float* gain, f
             pair_add_sq(sh, sl, __int_as_float(v.z));
             pair_add_sq(sh, sl, __int_as_float(v.w));
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float rh = __shfl_xor_sync(0xffffffffu, sh, o);
-            const float rl = __shfl_xor_sync(0xffffffffu, sl, o);
-            pair_add(sh, sl, rh);
-            sl = __fadd_rn(sl, rl);
-        }
-        if ((tid & 31) == 0) s_pair[tid >> 5] = make_float2(sh, sl);
-        named_bar(bar, kProdThreads);
-        if (tid < 32) {
-            float2 v = tid < kProdWarps ? s_pair[tid] : make_float2(0.0f, 0.0f);
-            sh = v.x;
-            sl = v.y;
-#pragma unroll
-            for (int o = kProdWarps / 2; o > 0; o >>= 1) {
-                const float rh = __shfl_xor_sync(0xffffffffu, sh, o);
-                const float rl = __shfl_xor_sync(0xffffffffu, sl, o);
-                pair_add(sh, sl, rh);
-                sl = __fadd_rn(sl, rl);
-            }
-            if (tid == 0) *s_rf = rms_scale_from_sum(sh, sl, K, eps);
-        }
-        named_bar(bar, kProdThreads);
-        rf = *s_rf;
+        rf = rms_scale_reduce(sh, sl, K, eps, tid, bar, s_pair, s_rf);
     }
     // cached groups: unrolled, so independent groups overlap their latencies
 #pragma unroll
