@@ -468,7 +468,6 @@ def run_ours(args, world, rank, local):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
            "note": "host wall clock per step: graph replay of H2D copy + 12 C-ABI calls + D2H "
                    "copy, then stream sync"}
-    launches_per_fused = 1   # every mode runs its producer inside the decode kernel
 
     sweeps = {} if args.no_sweeps else run_sweeps(native, torch, dev, capture, timed, Q, S)
 
