@@ -186,6 +186,56 @@ __device__ __forceinline__ long long fix_dot(const int4 w, const FixChunk& f) {
     return ((long long)P[3] << 24) + ((long long)P[2] << 16) + lo;
 }
 
+// The same for a whole 32-value block (one binade for the block): plane j
+// word u packs elements 4u..4u+3, u < 8.
+struct FixChunk32 {
+    int p[4][8];
+    int e;
+};
+
+__device__ __forceinline__ FixChunk32 fix_chunk32(const float (&x)[32]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    FixChunk32 f;
+    f.e = binade(amax);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        int X[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) X[i] = __float2int_rn(ldexpf(x[4 * u + i], 30 - f.e));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const unsigned b0 = (unsigned(X[0]) >> (8 * j)) & 0xffu;
+            const unsigned b1 = (unsigned(X[1]) >> (8 * j)) & 0xffu;
+            const unsigned b2 = (unsigned(X[2]) >> (8 * j)) & 0xffu;
+            const unsigned b3 = (unsigned(X[3]) >> (8 * j)) & 0xffu;
+            f.p[j][u] = int(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
+        }
+    }
+    return f;
+}
+
+// Exact block dot sum_e q_e * X_e as int64 (|.| < 2^42): 32 weights as two
+// 16-byte chunks.
+__device__ __forceinline__ long long fix_dot32(const int4 w0, const int4 w1, const FixChunk32& f) {
+    const int wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    int P[4];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        int a = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a = dp4a_su(wv[u], unsigned(f.p[j][u]), a);
+        P[j] = a;
+    }
+    int a = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) a = __dp4a(wv[u], f.p[3][u], a);
+    P[3] = a;
+    const long long lo = (long long)P[1] * 256 + P[0];
+    return ((long long)P[3] << 24) + ((long long)P[2] << 16) + lo;
+}
+
 // f * V exactly as an f32 pair (hi, lo), |lo| <~ 2^-23 |hi|.
 __device__ __forceinline__ DF scaled_pair(float f, long long V) {
     const int vh = int(V >> 21);

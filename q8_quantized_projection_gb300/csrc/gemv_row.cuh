@@ -47,6 +47,14 @@ __host__ __device__ constexpr int row_cpl() {
     return MODE == 1 ? 8 / R : MODE == 2 ? 4 / R : (R == 1 ? 2 : 1);
 }
 
+// Rows a warp serves per stage: the f32 mode's items are short (1 KB), so a
+// warp takes two rows of its part (sharing its activation block), which gives
+// it two independent dot chains.
+template <int MODE, int R>
+__host__ __device__ constexpr int row_rpw() {
+    return (MODE == 0 && R == 1) ? 2 : 1;
+}
+
 // Shared bytes of the fused producer's activation: codes (two planes at most)
 // and block scales of one row of up to kFusedMaxK values.
 constexpr size_t kFusedActBytes = 2 * 16384 + (16384 / 32) * 4;
@@ -65,7 +73,8 @@ struct RowGeo {
     int npr;         // parts per slice: a power of two <= 16
     int nprr;        // parts that hold data (the rest are empty)
     int RS;          // rows per stage: a power of two
-    int items;       // RS * npr, a divisor of kRowWarps
+    int rpw;         // rows a warp serves per stage (its part of each)
+    int items;       // RS * npr / rpw, a divisor of kRowWarps
     int stride;      // kRowWarps / items: warp groups, one per slot residue
     int stage_bytes;
     int nstages;
@@ -74,7 +83,7 @@ struct RowGeo {
 };
 
 __host__ __device__ inline RowGeo row_geo(int64_t N, int64_t K, int G, int c, int cpl,
-                                          int psum_row_unit) {
+                                          int psum_row_unit, int rpw_max = 1) {
     RowGeo g;
     g.PB = 512 * cpl;
     int64_t ks = K;
@@ -87,8 +96,10 @@ __host__ __device__ inline RowGeo row_geo(int64_t N, int64_t K, int G, int c, in
     while (g.npr < g.nprr) g.npr <<= 1;
     const int rsmax = kRowStage / g.KS;
     g.RS = 1;
-    while (g.RS * 2 <= rsmax && g.RS * 2 * g.npr <= kRowWarps) g.RS <<= 1;
-    g.items = g.RS * g.npr;
+    while (g.RS * 2 <= rsmax && g.RS * 2 * g.npr <= kRowWarps * rpw_max) g.RS <<= 1;
+    g.rpw = g.RS >= rpw_max ? rpw_max : 1;
+    while (g.RS * g.npr > kRowWarps * g.rpw) g.RS >>= 1;   // (only when rpw fell back to 1)
+    g.items = g.RS * g.npr / g.rpw;
     g.stride = kRowWarps / g.items;
     g.stage_bytes = (g.RS * g.KS + 1023) & ~1023;
     const int ns = kRowRing / g.stage_bytes;
@@ -104,7 +115,7 @@ __host__ __device__ inline RowGeo row_geo(int64_t N, int64_t K, int G, int c, in
 template <int MODE, int R>
 inline bool row_kernel_fits(int64_t K) {
     using A = typename AccT<MODE>::T;
-    const RowGeo g = row_geo(1, K, 1, 0, row_cpl<MODE, R>(), int(R * sizeof(A)));
+    const RowGeo g = row_geo(1, K, 1, 0, row_cpl<MODE, R>(), int(R * sizeof(A)), row_rpw<MODE, R>());
     return g.sbrows >= g.RS;
 }
 
@@ -192,7 +203,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
-    const RowGeo g = row_geo(p.N, p.K, G, c, CPL, int(R * sizeof(A)));
+    const RowGeo g = row_geo(p.N, p.K, G, c, CPL, int(R * sizeof(A)), row_rpw<MODE, R>());
 
     if (tid == 0) {
         for (int i = 0; i < g.nstages; ++i) {
@@ -332,7 +343,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
 
     // this warp's place in every stage it serves
     const int q = warp % g.items;
-    const int jrow = q / g.npr;   // row within the stage
+    const int jrow = q / g.npr;   // (first) row within the stage; the others RS/rpw apart
     const int pw = q % g.npr;     // part within the row-slice
     const int s_first = warp / g.items;
 
@@ -341,6 +352,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     float xdv[CPL][R];
     FixChunk fx[MODE == 0 ? CPL : 1][MODE == 0 ? R : 1];
     float p2s[CPL][R];
+    // f32 mode, one row: a lane owns a whole 32-value block of its part (one
+    // binade, one weight scale, one exact dot and one f32-pair scaling)
+    constexpr bool kBL = (MODE == 0 && R == 1 && CPL == 2);
+    FixChunk32 fxb;
+    float p2sb = 0.0f;
+    bool validb = false;
     int cur_sl = -1;
     int ncc = 0, rag = 0;   // full 512-byte chunk columns of this part, lanes of the ragged one
 
@@ -377,8 +394,29 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 pbytes = pbytes < 0 ? 0 : (pbytes > g.PB ? g.PB : pbytes);
                 ncc = pbytes >> 9;
                 rag = (pbytes & 511) >> 4;
+                if constexpr (kBL) {
+                    validb = lane < (pbytes >> 5);
+                    fxb = FixChunk32{};
+                    p2sb = 0.0f;
+                    if (validb) {
+                        const int64_t k = ks + pw * g.PB + int64_t(lane) * 32;
+                        float xs[32];
 #pragma unroll
-                for (int cc = 0; cc < CPL; ++cc) {
+                        for (int u = 0; u < 8; ++u) {
+                            float xv[4];
+                            load_x4<FUSE>(actf + k + 4 * u, p.h + k + 4 * u, p.gain ? p.gain + k + 4 * u : nullptr,
+                                          rf, xv);
+                            xs[4 * u + 0] = xv[0];
+                            xs[4 * u + 1] = xv[1];
+                            xs[4 * u + 2] = xv[2];
+                            xs[4 * u + 3] = xv[3];
+                        }
+                        fxb = fix_chunk32(xs);
+                        p2sb = ldexpf(1.0f, fxb.e - s_emax[0]);
+                    }
+                }
+#pragma unroll
+                for (int cc = 0; cc < (kBL ? 0 : CPL); ++cc) {
 #pragma unroll
                     for (int m = 0; m < R; ++m) {
                         a1[cc][m] = a2[cc][m] = make_int4(0, 0, 0, 0);
@@ -435,8 +473,42 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                                   uint32_t(lane * 16);
             const int blk0 = (pw * g.PB) >> 5;   // first block of the part within the slice
             const uint32_t sbase = sring_a + uint32_t(slot * (g.stage_bytes / 16) + jrow * (kl >> 4));
+            constexpr int RPW = row_rpw<MODE, R>();
+            DF part2[RPW];   // f32 mode: this warp's rows of the stage
+            bool have2[RPW];
+            if constexpr (kBL) {
+                // every row's weights first, then the independent dot chains
+                const int rstep = g.RS / g.rpw;
+                int4 w0[RPW], w1[RPW];
+                float swb[RPW];
 #pragma unroll
-            for (int c0 = 0; c0 < CPL; c0 += GC) {
+                for (int i = 0; i < RPW; ++i) {
+                    const int rr = jrow + i * rstep;   // row within the stage
+                    have2[i] = have && i < g.rpw && rbi * g.RS + rr < sbn;
+                    w0[i] = w1[i] = make_int4(0, 0, 0, 0);
+                    swb[i] = 0.0f;
+                    if (have2[i] && validb) {
+                        const uint32_t wb = wring_a + uint32_t(slot * g.stage_bytes + rr * kl + pw * g.PB) +
+                                            uint32_t(lane * 32);
+                        w0[i] = lds128(wb);
+                        w1[i] = lds128(wb + 16);
+                        const uint32_t sb = sring_a + uint32_t(slot * (g.stage_bytes / 16) + rr * (kl >> 4));
+                        swb[i] = scale_bulk
+                                     ? half_bits_to_float(lds16(sb + uint32_t((blk0 + lane) * 2)))
+                                     : half_bits_to_float(__ldg(p.s + (sb0 + rbi * g.RS + rr) * nb + (ks >> 5) + blk0 + lane));
+                    }
+                }
+                __syncwarp();
+                if (lane == 0 && ok) mbar_arrive(&empty[slot]);
+#pragma unroll
+                for (int i = 0; i < RPW; ++i) {
+                    part2[i] = DF{0.0f, 0.0f};
+                    if (have2[i] && validb)
+                        part2[i] = scaled_pair(__fmul_rn(swb[i], p2sb), fix_dot32(w0[i], w1[i], fxb));
+                }
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < (kBL ? 0 : CPL); c0 += GC) {
                 int4 w[GC];
                 float sw[GC];
                 if (have) {
@@ -492,7 +564,16 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     }
                 }
             }
-            if (have) {
+            if constexpr (kBL) {
+#pragma unroll
+                for (int i = 0; i < RPW; ++i) {
+                    if (have2[i]) {
+                        const DF tot = warp_sum(part2[i]);
+                        const int rsb = rbi * g.RS + jrow + i * (g.RS / g.rpw);
+                        if (lane == 0) psum[(size_t(rsb) * g.nks + sl) * g.nprr + pw] = reinterpret_cast<const A&>(tot);
+                    }
+                }
+            } else if (have) {
                 A* ps = psum + ((size_t(row_sb) * g.nks + sl) * g.nprr + pw) * R;
                 if constexpr (MODE == 0) {
 #pragma unroll
