@@ -193,25 +193,42 @@ struct FixChunk32 {
     int e;
 };
 
+// 2^n as a float for -126 <= n <= 127, from its bit pattern.
+__device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }
+
+// The four byte planes of four int32 values: plane j holds byte j of v0..v3
+// (v0 in the low byte), by two rounds of byte permutes.
+__device__ __forceinline__ void byte_planes4(int v0, int v1, int v2, int v3, int& p0, int& p1,
+                                             int& p2, int& p3) {
+    unsigned t0, t1, t2, t3;
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(t0) : "r"(v0), "r"(v1));   // v0.b0 v1.b0 v0.b1 v1.b1
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(t1) : "r"(v2), "r"(v3));
+    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(t2) : "r"(v0), "r"(v1));   // v0.b2 v1.b2 v0.b3 v1.b3
+    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(t3) : "r"(v2), "r"(v3));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(p0) : "r"(t0), "r"(t1));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(p1) : "r"(t0), "r"(t1));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(p2) : "r"(t2), "r"(t3));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(p3) : "r"(t2), "r"(t3));
+}
+
+// 32 values -> X = rint(x * 2^(30-E)) in four byte planes, E the block's
+// binade.  The scaling by 2^(30-E) (30-E in [-98, 156]) is two multiplies by
+// normal powers of two: exact, except that an intermediate below 2^-126 can
+// only arise when the product itself is below 2^-126, where X = 0 either way.
 __device__ __forceinline__ FixChunk32 fix_chunk32(const float (&x)[32]) {
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
     FixChunk32 f;
     f.e = binade(amax);
+    const int sh = 30 - f.e;
+    const float s1 = pow2i(sh >> 1), s2 = pow2i(sh - (sh >> 1));
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
         int X[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) X[i] = __float2int_rn(ldexpf(x[4 * u + i], 30 - f.e));
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const unsigned b0 = (unsigned(X[0]) >> (8 * j)) & 0xffu;
-            const unsigned b1 = (unsigned(X[1]) >> (8 * j)) & 0xffu;
-            const unsigned b2 = (unsigned(X[2]) >> (8 * j)) & 0xffu;
-            const unsigned b3 = (unsigned(X[3]) >> (8 * j)) & 0xffu;
-            f.p[j][u] = int(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
-        }
+        for (int i = 0; i < 4; ++i) X[i] = __float2int_rn(__fmul_rn(__fmul_rn(x[4 * u + i], s1), s2));
+        byte_planes4(X[0], X[1], X[2], X[3], f.p[0][u], f.p[1][u], f.p[2][u], f.p[3][u]);
     }
     return f;
 }
@@ -234,6 +251,45 @@ __device__ __forceinline__ long long fix_dot32(const int4 w0, const int4 w1, con
     P[3] = a;
     const long long lo = (long long)P[1] * 256 + P[0];
     return ((long long)P[3] << 24) + ((long long)P[2] << 16) + lo;
+}
+
+// The same block dot as fix_dot32, returned split for an exact conversion to
+// f32 without 64-bit arithmetic: V = vh * 2^21 + vl with |vh| <= 2^22 and
+// -2^21 <= vl < 2^21.  With L = P1*2^8 + P0 and H = P3*2^8 + P2 (so
+// V = H*2^16 + L): L = (L >> 21)*2^21 + (L & (2^21-1)) and
+// H*2^16 = (H >> 5)*2^21 + (H & 31)*2^16; one 2^21 moves from vl to vh to
+// centre vl.  |V| <= 32*128*(2^31 - 2^7) < 2^43 - 2^18 keeps vh in range
+// even for -128 weights.
+__device__ __forceinline__ int2 fix_dot32_split(const int4 w0, const int4 w1, const FixChunk32& f) {
+    const int wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    int P[4];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        int a = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a = dp4a_su(wv[u], unsigned(f.p[j][u]), a);
+        P[j] = a;
+    }
+    int a = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) a = __dp4a(wv[u], f.p[3][u], a);
+    P[3] = a;
+    const int L = P[1] * 256 + P[0];   // |P1| < 2^20, |P0| < 2^20
+    const int H = P[3] * 256 + P[2];   // |P3| < 2^19, |P2| < 2^20
+    return make_int2((H >> 5) + (L >> 21) + 1, (H & 31) * 65536 + (L & 0x1fffff) - 2097152);
+}
+
+// f * (vh * 2^21 + vl) exactly as an f32 pair, for fix_dot32_split's parts.
+__device__ __forceinline__ DF scaled_pair_split(float f, int2 v) {
+    const float fh = small_int_to_float(v.x) * 2097152.0f;   // exact: |vh| <= 2^22
+    const float fl = small_int_to_float(v.y);                // exact: |vl| <= 2^21
+    const float p1 = __fmul_rn(f, fh);
+    const float e1 = __fmaf_rn(f, fh, -p1);
+    const float p2 = __fmul_rn(f, fl);
+    const float e2 = __fmaf_rn(f, fl, -p2);
+    float s, e3;
+    two_sum(p1, p2, s, e3);
+    return DF{s, __fadd_rn(__fadd_rn(e1, e2), e3)};
 }
 
 // f * V exactly as an f32 pair (hi, lo), |lo| <~ 2^-23 |hi|.

@@ -9,11 +9,13 @@
 //  * A stage is RS whole rows of the weight matrix (RS*K <= 32 KB), moved by
 //    ONE contiguous bulk copy (plus one for its binary16 scales); rows longer
 //    than the stage are cut into slices, one row-slice a stage.  160 KB per SM
-//    are in flight; the producer warp runs ahead of griddepcontrol.wait, since
-//    weights never depend on the previous kernel on the stream.
+//    are in flight (192 KB in f32 mode); the producer warp runs ahead of
+//    griddepcontrol.wait, since weights never depend on the previous kernel
+//    on the stream.
 //  * A row-slice is cut into npr parts of PB = 512*CPL bytes (npr a power of
-//    two; trailing parts may be short or empty), so a stage holds
-//    items = RS*npr (row, part) pairs with items | 16.  Consumer warp w always
+//    two; trailing parts may be short or empty), so a stage holds RS*npr
+//    (row, part) pairs, served as items = RS*npr/rpw items of rpw rows of one
+//    part (rpw = 4 in f32 mode, else 1), items | 16.  Consumer warp w always
 //    serves item w % items, in the stages whose ring slot is congruent to
 //    w / items modulo 16/items (so every phase of a slot's barriers is seen by
 //    the same warps): its part never changes, so its lanes hold that part's
@@ -37,7 +39,14 @@ namespace q8 {
 constexpr int kRowWarps = 16;
 constexpr int kRowThreads = 32 * (kRowWarps + 1);
 constexpr int kRowStage = 32768;       // weight bytes of one stage at most
-constexpr int kRowRing = 163840;       // weight bytes in flight per CTA
+constexpr int kRowRing = 163840;       // weight bytes in flight per CTA (int8 modes)
+constexpr int kRowRingF32 = 196608;    // f32 mode: six 32 KB stages, so the two warp
+                                       // groups of K = 4096 rows own three slots each
+
+template <int MODE>
+__host__ __device__ constexpr int row_ring() {
+    return MODE == 0 ? kRowRingF32 : kRowRing;
+}
 constexpr int kRowPsumBytes = 16384;   // part sums of one super-block of rows
 
 // 16-byte chunks a lane owns per part: the activation registers (R rows, one
@@ -48,11 +57,18 @@ __host__ __device__ constexpr int row_cpl() {
 }
 
 // Rows a warp serves per stage: the f32 mode's items are short (1 KB), so a
-// warp takes two rows of its part (sharing its activation block), which gives
-// it two independent dot chains.
+// warp takes up to four rows of its part (sharing its activation block): four
+// independent dot chains, and one butterfly reduction for all of them.
 template <int MODE, int R>
 __host__ __device__ constexpr int row_rpw() {
-    return (MODE == 0 && R == 1) ? 2 : 1;
+    return (MODE == 0 && R == 1) ? 4 : 1;
+}
+
+// Bytes per (slice, part) kept beside the part sums: the f32 one-row path
+// stores each part's activation binade there (its sums are relative to it).
+template <int MODE, int R>
+__host__ __device__ constexpr int row_part_extra() {
+    return (MODE == 0 && R == 1) ? 2 : 0;
 }
 
 // Shared bytes of the fused producer's activation: codes (two planes at most)
@@ -61,7 +77,7 @@ constexpr size_t kFusedActBytes = 2 * 16384 + (16384 / 32) * 4;
 
 template <int MODE, int R, bool FUSE>
 __host__ __device__ constexpr size_t row_smem_bytes() {
-    return size_t(kRowRing) + size_t(kRowRing) / 16 + 2 * kGemvMaxStages * sizeof(uint64_t) +
+    return size_t(row_ring<MODE>()) + size_t(row_ring<MODE>()) / 16 + 2 * kGemvMaxStages * sizeof(uint64_t) +
            kRowPsumBytes + size_t(kRowWarps) * R * sizeof(ArgmaxCand) + 64 +
            (FUSE && MODE != 0 ? kFusedActBytes : 0);
 }
@@ -80,15 +96,19 @@ struct RowGeo {
     int nstages;
     int64_t r0, r1;
     int64_t sbrows;  // rows per super-block (a multiple of RS, >= RS when usable)
+    int ep_off;      // byte offset of the per-(slice, part) binades in the part-sum area
 };
 
 __host__ __device__ inline RowGeo row_geo(int64_t N, int64_t K, int G, int c, int cpl,
-                                          int psum_row_unit, int rpw_max = 1) {
+                                          int psum_row_unit, int rpw_max, int ring,
+                                          int part_extra) {
     RowGeo g;
     g.PB = 512 * cpl;
     int64_t ks = K;
     if (ks > kRowStage) ks = kRowStage;
     if (ks > int64_t(kRowWarps) * g.PB) ks = int64_t(kRowWarps) * g.PB;
+    // rows of rpw_max within one stage: long rows are cut into slices
+    if (rpw_max > 1 && ks > kRowStage / rpw_max) ks = kRowStage / rpw_max;
     g.KS = int(ks);
     g.nks = int((K + g.KS - 1) / g.KS);
     g.nprr = (g.KS + g.PB - 1) / g.PB;
@@ -97,17 +117,19 @@ __host__ __device__ inline RowGeo row_geo(int64_t N, int64_t K, int G, int c, in
     const int rsmax = kRowStage / g.KS;
     g.RS = 1;
     while (g.RS * 2 <= rsmax && g.RS * 2 * g.npr <= kRowWarps * rpw_max) g.RS <<= 1;
-    g.rpw = g.RS >= rpw_max ? rpw_max : 1;
-    while (g.RS * g.npr > kRowWarps * g.rpw) g.RS >>= 1;   // (only when rpw fell back to 1)
+    g.rpw = g.RS < rpw_max ? g.RS : rpw_max;
+    while (g.RS * g.npr > kRowWarps * g.rpw) g.RS >>= 1;   // (never: kept as a guard)
     g.items = g.RS * g.npr / g.rpw;
     g.stride = kRowWarps / g.items;
     g.stage_bytes = (g.RS * g.KS + 1023) & ~1023;
-    const int ns = kRowRing / g.stage_bytes;
+    const int ns = ring / g.stage_bytes;
     g.nstages = ns > kGemvMaxStages ? kGemvMaxStages : ns;
     g.r0 = N * c / G;
     g.r1 = N * (c + 1) / G;
     const int64_t per_row = int64_t(g.nks) * g.nprr * psum_row_unit;
-    g.sbrows = ((kRowPsumBytes / per_row) / g.RS) * g.RS;
+    const int64_t ep_bytes = (int64_t(g.nks) * g.nprr * part_extra + 15) & ~int64_t(15);
+    g.ep_off = int(kRowPsumBytes - ep_bytes);
+    g.sbrows = ep_bytes >= kRowPsumBytes ? 0 : (((kRowPsumBytes - ep_bytes) / per_row) / g.RS) * g.RS;
     return g;
 }
 
@@ -115,7 +137,8 @@ __host__ __device__ inline RowGeo row_geo(int64_t N, int64_t K, int G, int c, in
 template <int MODE, int R>
 inline bool row_kernel_fits(int64_t K) {
     using A = typename AccT<MODE>::T;
-    const RowGeo g = row_geo(1, K, 1, 0, row_cpl<MODE, R>(), int(R * sizeof(A)), row_rpw<MODE, R>());
+    const RowGeo g = row_geo(1, K, 1, 0, row_cpl<MODE, R>(), int(R * sizeof(A)), row_rpw<MODE, R>(),
+                             row_ring<MODE>(), row_part_extra<MODE, R>());
     return g.sbrows >= g.RS;
 }
 
@@ -141,6 +164,34 @@ __device__ __forceinline__ float warp_sum_rows(const float (&v)[R], int lane) {
     float s = cur[0];
 #pragma unroll
     for (int o = 16 / R; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+}
+
+// The same butterfly for f32 pairs: lanes [r*32/R, (r+1)*32/R) end with row
+// r's total, each exchange an error-free f32-pair addition.
+template <int R>
+__device__ __forceinline__ DF warp_sum_rows(const DF (&v)[R], int lane) {
+    DF cur[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) cur[i] = v[i];
+#pragma unroll
+    for (int step = 16, h = R / 2; h >= 1; step >>= 1, h >>= 1) {
+        const bool upper = (lane & step) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const DF send = upper ? cur[i] : cur[i + h];
+            const DF keep = upper ? cur[i + h] : cur[i];
+            const DF got{__shfl_xor_sync(0xffffffffu, send.hi, step),
+                         __shfl_xor_sync(0xffffffffu, send.lo, step)};
+            cur[i] = df_add(keep, got);
+        }
+    }
+    DF s = cur[0];
+#pragma unroll
+    for (int o = 16 / R; o > 0; o >>= 1) {
+        const DF got{__shfl_xor_sync(0xffffffffu, s.hi, o), __shfl_xor_sync(0xffffffffu, s.lo, o)};
+        s = df_add(s, got);
+    }
     return s;
 }
 
@@ -188,8 +239,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* wring = smem;
-    unsigned char* sring = wring + kRowRing;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sring + kRowRing / 16);
+    constexpr int kRing = row_ring<MODE>();
+    unsigned char* sring = wring + kRing;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sring + kRing / 16);
     uint64_t* empty = full + kGemvMaxStages;
     A* psum = reinterpret_cast<A*>(empty + kGemvMaxStages);   // [sbrows][nks][nprr][R]
     ArgmaxCand* cand = reinterpret_cast<ArgmaxCand*>(reinterpret_cast<unsigned char*>(psum) +
@@ -203,7 +255,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
-    const RowGeo g = row_geo(p.N, p.K, G, c, CPL, int(R * sizeof(A)), row_rpw<MODE, R>());
+    const RowGeo g = row_geo(p.N, p.K, G, c, CPL, int(R * sizeof(A)), row_rpw<MODE, R>(), kRing,
+                             row_part_extra<MODE, R>());
+    // f32 mode, one row: a lane owns a whole 32-value block of its part (one
+    // binade, one weight scale, one exact dot and one f32-pair scaling), and
+    // each part's sums are relative to the part's own largest binade
+    constexpr bool kBL = (MODE == 0 && R == 1 && CPL == 2);
+    short* s_ep = reinterpret_cast<short*>(reinterpret_cast<unsigned char*>(psum) + g.ep_off);
 
     if (tid == 0) {
         for (int i = 0; i < g.nstages; ++i) {
@@ -301,7 +359,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         plane = K;
     }
 
-    if constexpr (MODE == 0) {
+    if constexpr (MODE == 0 && !kBL) {
         // the row's largest binade: the fixed-point grids are relative to it
         float amax[R];
 #pragma unroll
@@ -352,9 +410,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     float xdv[CPL][R];
     FixChunk fx[MODE == 0 ? CPL : 1][MODE == 0 ? R : 1];
     float p2s[CPL][R];
-    // f32 mode, one row: a lane owns a whole 32-value block of its part (one
-    // binade, one weight scale, one exact dot and one f32-pair scaling)
-    constexpr bool kBL = (MODE == 0 && R == 1 && CPL == 2);
     FixChunk32 fxb;
     float p2sb = 0.0f;
     bool validb = false;
@@ -397,7 +452,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 if constexpr (kBL) {
                     validb = lane < (pbytes >> 5);
                     fxb = FixChunk32{};
-                    p2sb = 0.0f;
+                    fxb.e = -126;   // the binade of zero: below every other
                     if (validb) {
                         const int64_t k = ks + pw * g.PB + int64_t(lane) * 32;
                         float xs[32];
@@ -412,8 +467,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                             xs[4 * u + 3] = xv[3];
                         }
                         fxb = fix_chunk32(xs);
-                        p2sb = ldexpf(1.0f, fxb.e - s_emax[0]);
                     }
+                    // the part's largest binade; its sums are in units of 2^(ep-30)
+                    const int ep = __reduce_max_sync(0xffffffffu, fxb.e);
+                    p2sb = validb ? ldexpf(1.0f, fxb.e - ep) : 0.0f;
+                    if (lane == 0 && pw < g.nprr) s_ep[sl * g.nprr + pw] = short(ep);
                 }
 #pragma unroll
                 for (int cc = 0; cc < (kBL ? 0 : CPL); ++cc) {
@@ -477,25 +535,28 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
             DF part2[RPW];   // f32 mode: this warp's rows of the stage
             bool have2[RPW];
             if constexpr (kBL) {
-                // every row's weights first, then the independent dot chains
+                // each row's exact dot right after its weights are in
+                // registers (one row's weights live at a time); the slot goes
+                // back after the last row, then the f32-pair scalings
                 const int rstep = g.RS / g.rpw;
-                int4 w0[RPW], w1[RPW];
+                int2 vb[RPW];
                 float swb[RPW];
 #pragma unroll
                 for (int i = 0; i < RPW; ++i) {
                     const int rr = jrow + i * rstep;   // row within the stage
                     have2[i] = have && i < g.rpw && rbi * g.RS + rr < sbn;
-                    w0[i] = w1[i] = make_int4(0, 0, 0, 0);
+                    vb[i] = make_int2(0, 0);
                     swb[i] = 0.0f;
                     if (have2[i] && validb) {
                         const uint32_t wb = wring_a + uint32_t(slot * g.stage_bytes + rr * kl + pw * g.PB) +
                                             uint32_t(lane * 32);
-                        w0[i] = lds128(wb);
-                        w1[i] = lds128(wb + 16);
+                        const int4 w0 = lds128(wb);
+                        const int4 w1 = lds128(wb + 16);
                         const uint32_t sb = sring_a + uint32_t(slot * (g.stage_bytes / 16) + rr * (kl >> 4));
                         swb[i] = scale_bulk
                                      ? half_bits_to_float(lds16(sb + uint32_t((blk0 + lane) * 2)))
                                      : half_bits_to_float(__ldg(p.s + (sb0 + rbi * g.RS + rr) * nb + (ks >> 5) + blk0 + lane));
+                        vb[i] = fix_dot32_split(w0, w1, fxb);
                     }
                 }
                 __syncwarp();
@@ -503,8 +564,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
 #pragma unroll
                 for (int i = 0; i < RPW; ++i) {
                     part2[i] = DF{0.0f, 0.0f};
-                    if (have2[i] && validb)
-                        part2[i] = scaled_pair(__fmul_rn(swb[i], p2sb), fix_dot32(w0[i], w1[i], fxb));
+                    if (have2[i] && validb) part2[i] = scaled_pair_split(__fmul_rn(swb[i], p2sb), vb[i]);
                 }
             }
 #pragma unroll
@@ -565,13 +625,16 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 }
             }
             if constexpr (kBL) {
+                // one butterfly for the warp's rows: lanes [i*32/RPW, ...) end with row i
+                const DF tot = warp_sum_rows<RPW>(part2, lane);
+                const int i = lane / (32 / RPW);
+                bool hv = false;
 #pragma unroll
-                for (int i = 0; i < RPW; ++i) {
-                    if (have2[i]) {
-                        const DF tot = warp_sum(part2[i]);
-                        const int rsb = rbi * g.RS + jrow + i * (g.RS / g.rpw);
-                        if (lane == 0) psum[(size_t(rsb) * g.nks + sl) * g.nprr + pw] = reinterpret_cast<const A&>(tot);
-                    }
+                for (int k = 0; k < RPW; ++k)
+                    if (k == i) hv = have2[k];
+                if ((lane & (32 / RPW - 1)) == 0 && hv) {
+                    const int rsb = rbi * g.RS + jrow + i * (g.RS / g.rpw);
+                    psum[(size_t(rsb) * g.nks + sl) * g.nprr + pw] = reinterpret_cast<const A&>(tot);
                 }
             } else if (have) {
                 A* ps = psum + ((size_t(row_sb) * g.nks + sl) * g.nprr + pw) * R;
@@ -602,15 +665,34 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         consumer_bar<NT>();
         if (ok) {
             const int nparts = g.nks * g.nprr;
+            int E = -126;   // one row: the largest part binade is the row's
+            if constexpr (kBL) {
+                for (int u = 0; u < nparts; ++u) E = max(E, int(s_ep[u]));
+            }
             for (int i = tid; i < sbn * R; i += NT) {
                 const int row_sb = i / R, m = i % R;
                 if (m >= rows) continue;
                 const A* ps = psum + size_t(row_sb) * nparts * R + m;
                 A s = ps[0];
-                for (int u = 1; u < nparts; ++u) s = acc_add(s, ps[size_t(u) * R]);
+                if constexpr (kBL) {
+                    // each part rescaled to the row's binade (powers of two: exact
+                    // but for parts 2^-126 below the largest), then added in order
+                    s = DF{ldexpf(s.hi, s_ep[0] - E), ldexpf(s.lo, s_ep[0] - E)};
+                    for (int u = 1; u < nparts; ++u) {
+                        const A v = ps[size_t(u) * R];
+                        const int d = s_ep[u] - E;
+                        s = acc_add(s, DF{ldexpf(v.hi, d), ldexpf(v.lo, d)});
+                    }
+                } else {
+                    for (int u = 1; u < nparts; ++u) s = acc_add(s, ps[size_t(u) * R]);
+                }
                 const int64_t n = sb0 + row_sb;
                 double val = acc_value(s);
-                if constexpr (MODE == 0) val = ldexp(val, s_emax[m] - 30);
+                if constexpr (kBL) {
+                    val = ldexp(val, E - 30);
+                } else if constexpr (MODE == 0) {
+                    val = ldexp(val, s_emax[m] - 30);
+                }
                 if (p.y) {
                     if (MODE == 0 && p.out_f64)
                         reinterpret_cast<double*>(p.y)[m * N + n] = val;
