@@ -139,6 +139,40 @@ __device__ __forceinline__ int binade(float a) {
 // 16 f32 activations -> 4 byte planes of X = rint(x * 2^(30-E)), |X| <= 2^30,
 // X = p3*2^24 + p2*2^16 + p1*2^8 + p0 (p3 signed, p2..p0 unsigned), and the
 // chunk's binade E.  Plane j word u packs elements 4u..4u+3.
+// 2^n as a float for -126 <= n <= 127, from its bit pattern.
+__device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }
+
+// The four byte planes of four int32 values: plane j holds byte j of v0..v3
+// (v0 in the low byte), by two rounds of byte permutes.
+__device__ __forceinline__ void byte_planes4(int v0, int v1, int v2, int v3, int& p0, int& p1,
+                                             int& p2, int& p3) {
+    unsigned t0, t1, t2, t3;
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(t0) : "r"(v0), "r"(v1));   // v0.b0 v1.b0 v0.b1 v1.b1
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(t1) : "r"(v2), "r"(v3));
+    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(t2) : "r"(v0), "r"(v1));   // v0.b2 v1.b2 v0.b3 v1.b3
+    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(t3) : "r"(v2), "r"(v3));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(p0) : "r"(t0), "r"(t1));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(p1) : "r"(t0), "r"(t1));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(p2) : "r"(t2), "r"(t3));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(p3) : "r"(t2), "r"(t3));
+}
+
+// rint(t * s2) for |t * s2| <= 2^30, exactly and without a conversion
+// instruction (those run on a narrow pipe): u = (3*2^30 + v) rounded, where
+// floats are 2^8 apart, so vh = u - 3*2^30 is v rounded to a multiple of 2^8
+// and its bits count those multiples; vl = v - vh (|vl| <= 2^7) is exact by
+// a fused multiply-add, and rint(vl) is read from the bits of 1.5*2^23 + vl.
+// rint(v) = vh + rint(vl), ties to even as vh is even.
+__device__ __forceinline__ int rint_scaled30(float t, float s2) {
+    const float C = 3221225472.0f;   // 3*2^30
+    const float M = 12582912.0f;     // 1.5*2^23
+    const float u = __fmaf_rn(t, s2, C);
+    const float vh = __fsub_rn(u, C);
+    const float vl = __fmaf_rn(t, s2, -vh);
+    const float w = __fadd_rn(vl, M);
+    return int((__float_as_uint(u) << 8) + __float_as_uint(w) - (0x4F400000u << 8) - 0x4B400000u);
+}
+
 struct FixChunk {
     int p[4][4];
     int e;
@@ -150,19 +184,15 @@ __device__ __forceinline__ FixChunk fix_chunk(const float (&x)[16]) {
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
     FixChunk f;
     f.e = binade(amax);
-    int X[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) X[i] = __float2int_rn(ldexpf(x[i], 30 - f.e));
+    // x * 2^(30-E) as two multiplies by normal powers of two (see fix_chunk32)
+    const int sh = 30 - f.e;
+    const float s1 = pow2i(sh >> 1), s2 = pow2i(sh - (sh >> 1));
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
+        int X[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const unsigned b0 = (unsigned(X[4 * u + 0]) >> (8 * j)) & 0xffu;
-            const unsigned b1 = (unsigned(X[4 * u + 1]) >> (8 * j)) & 0xffu;
-            const unsigned b2 = (unsigned(X[4 * u + 2]) >> (8 * j)) & 0xffu;
-            const unsigned b3 = (unsigned(X[4 * u + 3]) >> (8 * j)) & 0xffu;
-            f.p[j][u] = int(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
-        }
+        for (int i = 0; i < 4; ++i) X[i] = rint_scaled30(__fmul_rn(x[4 * u + i], s1), s2);
+        byte_planes4(X[0], X[1], X[2], X[3], f.p[0][u], f.p[1][u], f.p[2][u], f.p[3][u]);
     }
     return f;
 }
@@ -193,24 +223,6 @@ struct FixChunk32 {
     int e;
 };
 
-// 2^n as a float for -126 <= n <= 127, from its bit pattern.
-__device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }
-
-// The four byte planes of four int32 values: plane j holds byte j of v0..v3
-// (v0 in the low byte), by two rounds of byte permutes.
-__device__ __forceinline__ void byte_planes4(int v0, int v1, int v2, int v3, int& p0, int& p1,
-                                             int& p2, int& p3) {
-    unsigned t0, t1, t2, t3;
-    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(t0) : "r"(v0), "r"(v1));   // v0.b0 v1.b0 v0.b1 v1.b1
-    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(t1) : "r"(v2), "r"(v3));
-    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(t2) : "r"(v0), "r"(v1));   // v0.b2 v1.b2 v0.b3 v1.b3
-    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(t3) : "r"(v2), "r"(v3));
-    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(p0) : "r"(t0), "r"(t1));
-    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(p1) : "r"(t0), "r"(t1));
-    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(p2) : "r"(t2), "r"(t3));
-    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(p3) : "r"(t2), "r"(t3));
-}
-
 // 32 values -> X = rint(x * 2^(30-E)) in four byte planes, E the block's
 // binade.  The scaling by 2^(30-E) (30-E in [-98, 156]) is two multiplies by
 // normal powers of two: exact, except that an intermediate below 2^-126 can
@@ -227,7 +239,7 @@ __device__ __forceinline__ FixChunk32 fix_chunk32(const float (&x)[32]) {
     for (int u = 0; u < 8; ++u) {
         int X[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) X[i] = __float2int_rn(__fmul_rn(__fmul_rn(x[4 * u + i], s1), s2));
+        for (int i = 0; i < 4; ++i) X[i] = rint_scaled30(__fmul_rn(x[4 * u + i], s1), s2);
         byte_planes4(X[0], X[1], X[2], X[3], f.p[0][u], f.p[1][u], f.p[2][u], f.p[3][u]);
     }
     return f;

@@ -195,6 +195,14 @@ __device__ __forceinline__ DF warp_sum_rows(const DF (&v)[R], int lane) {
     return s;
 }
 
+// v * 2^d for d <= 0 by two multiplies by normal powers of two (exact but in
+// the subnormal range); a part more than 2^252 below the row's largest is
+// dropped.
+__device__ __forceinline__ float mul_pow2_neg(float v, int d) {
+    if (d < -252) return 0.0f;
+    return __fmul_rn(__fmul_rn(v, pow2i(d >> 1)), pow2i(d - (d >> 1)));
+}
+
 // Four f32 activation values: read as they are, or (f32 mode with the
 // producer fused) formed as x = (h*rf)*g with the producer's two roundings.
 template <bool FUSE>
@@ -674,19 +682,27 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 if (m >= rows) continue;
                 const A* ps = psum + size_t(row_sb) * nparts * R + m;
                 A s = ps[0];
+                const int64_t n = sb0 + row_sb;
                 if constexpr (kBL) {
                     // each part rescaled to the row's binade (powers of two: exact
-                    // but for parts 2^-126 below the largest), then added in order
-                    s = DF{ldexpf(s.hi, s_ep[0] - E), ldexpf(s.lo, s_ep[0] - E)};
+                    // but in the subnormal range), then added in order
+                    s = DF{mul_pow2_neg(s.hi, s_ep[0] - E), mul_pow2_neg(s.lo, s_ep[0] - E)};
                     for (int u = 1; u < nparts; ++u) {
                         const A v = ps[size_t(u) * R];
                         const int d = s_ep[u] - E;
-                        s = acc_add(s, DF{ldexpf(v.hi, d), ldexpf(v.lo, d)});
+                        s = acc_add(s, DF{mul_pow2_neg(v.hi, d), mul_pow2_neg(v.lo, d)});
+                    }
+                    if (!ARGMAX && !p.out_f64) {
+                        // f32 output: the pair rounded once, then scaled by 2^(E-30)
+                        const int sc = E - 30;   // in [-156, 98]
+                        if (p.y)
+                            reinterpret_cast<float*>(p.y)[n] =
+                                __fmul_rn(__fmul_rn(__fadd_rn(s.hi, s.lo), pow2i(sc >> 1)), pow2i(sc - (sc >> 1)));
+                        continue;
                     }
                 } else {
                     for (int u = 1; u < nparts; ++u) s = acc_add(s, ps[size_t(u) * R]);
                 }
-                const int64_t n = sb0 + row_sb;
                 double val = acc_value(s);
                 if constexpr (kBL) {
                     val = ldexp(val, E - 30);
