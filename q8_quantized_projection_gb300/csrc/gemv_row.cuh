@@ -58,10 +58,15 @@ __host__ __device__ constexpr int row_cpl() {
 
 // Rows a warp serves per stage: the f32 mode's items are short (1 KB), so a
 // warp takes up to four rows of its part (sharing its activation block): four
-// independent dot chains, and one butterfly reduction for all of them.
+// independent dot chains, and one butterfly reduction for all of them.  The
+// int8 modes with one or two chunks a lane (one-word 4 and 8 rows, two-word 2
+// and 4) take two rows, so one butterfly over 2R values serves twice the
+// weights.
 template <int MODE, int R>
 __host__ __device__ constexpr int row_rpw() {
-    return (MODE == 0 && R == 1) ? 4 : 1;
+    return (MODE == 0 && R == 1) ? 4
+           : ((MODE == 1 && R >= 4) || (MODE == 2 && R >= 2)) ? 2
+                                                              : 1;
 }
 
 // Bytes per (slice, part) kept beside the part sums: the f32 one-row path
@@ -542,6 +547,51 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
             constexpr int RPW = row_rpw<MODE, R>();
             DF part2[RPW];   // f32 mode: this warp's rows of the stage
             bool have2[RPW];
+            // int8 modes, two rows of the part per stage (kMR)
+            constexpr bool kMR = (MODE != 0 && RPW > 1);
+            float pm[kMR ? RPW : 1][kMR ? R : 1];
+            bool hvm[kMR ? RPW : 1];
+            if constexpr (kMR) {
+                const int rstep = g.RS / g.rpw;
+                int4 wm[RPW][CPL];
+                float swm[RPW][CPL];
+#pragma unroll
+                for (int i = 0; i < RPW; ++i) {
+                    const int rr = jrow + i * rstep;   // row within the stage
+                    hvm[i] = have && i < g.rpw && rbi * g.RS + rr < sbn;
+                    const uint32_t wr = wring_a + uint32_t(slot * g.stage_bytes + rr * kl + pw * g.PB) +
+                                        uint32_t(lane * 16);
+                    const uint32_t sr = sring_a + uint32_t(slot * (g.stage_bytes / 16) + rr * (kl >> 4));
+                    const int64_t nrow = sb0 + rbi * g.RS + rr;
+#pragma unroll
+                    for (int cc = 0; cc < CPL; ++cc) {
+                        wm[i][cc] = make_int4(0, 0, 0, 0);
+                        swm[i][cc] = 0.0f;
+                        if (hvm[i] && (cc < ncc || (cc == ncc && lane < rag))) {
+                            const int blk = blk0 + (lane >> 1) + 16 * cc;
+                            wm[i][cc] = lds128(wr + 512 * cc);
+                            swm[i][cc] = scale_bulk ? half_bits_to_float(lds16(sr + uint32_t(blk * 2)))
+                                                    : half_bits_to_float(__ldg(p.s + nrow * nb + (ks >> 5) + blk));
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0 && ok) mbar_arrive(&empty[slot]);
+#pragma unroll
+                for (int i = 0; i < RPW; ++i) {
+#pragma unroll
+                    for (int m = 0; m < R; ++m) {
+                        pm[i][m] = 0.0f;
+#pragma unroll
+                        for (int cc = 0; cc < CPL; ++cc) {
+                            const int isum = (MODE == 1) ? dot16_i8(wm[i][cc], a1[cc][m])
+                                                         : dot16_i8x2(wm[i][cc], a1[cc][m], a2[cc][m]);
+                            const float fi = MODE == 1 ? small_int_to_float(isum) : float(isum);
+                            pm[i][m] = fmaf(fi, swm[i][cc] * xdv[cc][m], pm[i][m]);
+                        }
+                    }
+                }
+            }
             if constexpr (kBL) {
                 // each row's exact dot right after its weights are in
                 // registers (one row's weights live at a time); the slot goes
@@ -576,7 +626,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 }
             }
 #pragma unroll
-            for (int c0 = 0; c0 < (kBL ? 0 : CPL); c0 += GC) {
+            for (int c0 = 0; c0 < ((kBL || kMR) ? 0 : CPL); c0 += GC) {
                 int4 w[GC];
                 float sw[GC];
                 if (have) {
@@ -643,6 +693,25 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 if ((lane & (32 / RPW - 1)) == 0 && hv) {
                     const int rsb = rbi * g.RS + jrow + i * (g.RS / g.rpw);
                     psum[(size_t(rsb) * g.nks + sl) * g.nprr + pw] = reinterpret_cast<const A&>(tot);
+                }
+            } else if constexpr (kMR) {
+                // one butterfly over the warp's RPW x R sums: lanes [v*32/V, ...)
+                // end with sum v = i*R + m
+                constexpr int V = RPW * R;
+                float flat[V];
+#pragma unroll
+                for (int i = 0; i < RPW; ++i)
+#pragma unroll
+                    for (int m = 0; m < R; ++m) flat[i * R + m] = pm[i][m];
+                const float tot = warp_sum_rows<V>(flat, lane);
+                const int v = lane / (32 / V), i = v / R, m = v % R;
+                bool hv = false;
+#pragma unroll
+                for (int k = 0; k < RPW; ++k)
+                    if (k == i) hv = hvm[k];
+                if ((lane & (32 / V - 1)) == 0 && hv) {
+                    const int rsb = rbi * g.RS + jrow + i * (g.RS / g.rpw);
+                    psum[((size_t(rsb) * g.nks + sl) * g.nprr + pw) * R + m] = tot;
                 }
             } else if (have) {
                 A* ps = psum + ((size_t(row_sb) * g.nks + sl) * g.nprr + pw) * R;
