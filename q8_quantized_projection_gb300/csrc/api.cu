@@ -119,11 +119,12 @@ q8_status run_projection(int mode, const int8_t* q, const uint16_t* s, int64_t N
 }
 
 // Plain projection of a quantised activation: the tensor-core chunk kernel from
-// kChunkMinRows rows on (int8 modes, K % 256 == 0), the CUDA-core kernels else.
+// chunk_min_rows(mode) rows on (int8 modes, K % 256 == 0), the CUDA-core
+// kernels else.
 q8_status project_dispatch(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                            const void* xq, const float* xd, int64_t rows, void* y, int out_f64,
                            const LaunchCtx& ctx) {
-    if (!out_f64 && rows >= kChunkMinRows && chunk_supported(mode, N, K, rows))
+    if (!out_f64 && rows >= chunk_min_rows(mode) && chunk_supported(mode, N, K, rows))
         return launched(launch_chunk(mode, q, s, N, K, xq, xd, rows, static_cast<float*>(y), ctx));
     return run_projection(mode, q, s, N, K, xq, xd, rows, y, out_f64, nullptr, nullptr, nullptr,
                           ctx);
@@ -146,8 +147,10 @@ q8_status check_proj_args(int mode, const int8_t* q, const uint16_t* s, int64_t 
 
 namespace q8 {
 // rows per CUDA-core launch: the decode kernel's widest row count per mode
-// (more rows are split into groups, each reading the weights once)
-int gemv_max_rows(int mode) { return mode == 0 ? 2 : mode == 1 ? 8 : 4; }
+// (more rows are split into groups, each reading the weights once); f32 runs
+// a row per launch: it is issue-bound, and a two-row pass cost 1.5x two
+// one-row passes (LM head, 16 rows: 3.19 ms in pairs, 2.07 ms row by row)
+int gemv_max_rows(int mode) { return mode == 0 ? 1 : mode == 1 ? 8 : 4; }
 }  // namespace q8
 
 extern "C" {

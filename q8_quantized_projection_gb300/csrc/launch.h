@@ -60,8 +60,10 @@ cudaError_t launch_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N
                          const void* xq, const float* xd, int64_t T, float* y, const LaunchCtx& ctx);
 cudaError_t launch_chunk_debug(int mode, const int8_t* q, int64_t N, int64_t K, const void* xq,
                                int64_t T, int32_t* isum, const LaunchCtx& ctx);
-// activation rows from which projections run on the tensor cores
-constexpr int64_t kChunkMinRows = 16;
+// Activation rows from which projections run on the tensor cores: where one
+// chunk launch beats the decode kernel's groups of rows (one-word: groups of
+// 8, so 9 rows and more; two-word: groups of 4, so 5 and more).
+inline int64_t chunk_min_rows(int mode) { return mode == 2 ? 5 : 9; }
 
 cudaError_t launch_debug_dots(int mode, const int8_t* q, const void* xq, int64_t N, int64_t K,
                               int64_t rows, int32_t* isum, const LaunchCtx& ctx);
