@@ -245,6 +245,7 @@ __device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v,
 template <int MODE, int R, bool ARGMAX, bool FUSE>
 __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvParams p) {
     static_assert(!FUSE || R == 1, "fused producer: one row");
+    static_assert(MODE != 0 || R == 1, "f32 mode: one row per launch");
     using A = typename AccT<MODE>::T;
     constexpr int CPL = row_cpl<MODE, R>();
     constexpr int NW = kRowWarps;
@@ -259,8 +260,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     A* psum = reinterpret_cast<A*>(empty + kGemvMaxStages);   // [sbrows][nks][nprr][R]
     ArgmaxCand* cand = reinterpret_cast<ArgmaxCand*>(reinterpret_cast<unsigned char*>(psum) +
                                                      kRowPsumBytes);   // [NW][R]
-    __shared__ float s_amax[NW][R];
-    __shared__ int s_emax[R];
     __shared__ unsigned int s_ticket;
     __shared__ float2 s_pair[kProdWarps];
     __shared__ float s_rf;
@@ -372,38 +371,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         plane = K;
     }
 
-    if constexpr (MODE == 0 && !kBL) {
-        // the row's largest binade: the fixed-point grids are relative to it
-        float amax[R];
-#pragma unroll
-        for (int m = 0; m < R; ++m) amax[m] = 0.0f;
-        for (int64_t k = int64_t(tid) * 4; k < K; k += 4 * NT) {
-#pragma unroll
-            for (int m = 0; m < R; ++m) {
-                if (m < rows) {
-                    float xv[4];
-                    load_x4<FUSE>(actf + m * K + k, p.h + k, p.gain ? p.gain + k : nullptr, rf, xv);
-                    amax[m] = fmaxf(amax[m], fmaxf(fmaxf(fabsf(xv[0]), fabsf(xv[1])),
-                                                   fmaxf(fabsf(xv[2]), fabsf(xv[3]))));
-                }
-            }
-        }
-#pragma unroll
-        for (int m = 0; m < R; ++m) {
-            float a = amax[m];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-            if (lane == 0) s_amax[warp][m] = a;
-        }
-        consumer_bar<NT>();
-        if (tid < R) {
-            float a = 0.0f;
-            for (int w = 0; w < NW; ++w) a = fmaxf(a, s_amax[w][tid]);
-            s_emax[tid] = binade(a);
-        }
-        consumer_bar<NT>();
-    }
-
     double best_v[ARGMAX ? R : 1];
     long long best_i[ARGMAX ? R : 1];
 #pragma unroll
@@ -421,8 +388,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     int4 a1[CPL][R];
     int4 a2[CPL][R];
     float xdv[CPL][R];
-    FixChunk fx[MODE == 0 ? CPL : 1][MODE == 0 ? R : 1];
-    float p2s[CPL][R];
     FixChunk32 fxb;
     float p2sb = 0.0f;
     bool validb = false;
@@ -492,29 +457,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     for (int m = 0; m < R; ++m) {
                         a1[cc][m] = a2[cc][m] = make_int4(0, 0, 0, 0);
                         xdv[cc][m] = 0.0f;
-                        p2s[cc][m] = 0.0f;
-                        if constexpr (MODE == 0) fx[cc][m] = FixChunk{};
                     }
                     if (cc < ncc || (cc == ncc && lane < rag)) {
                         const int64_t k = ks + pw * g.PB + int64_t(lane) * 16 + 512 * cc;
 #pragma unroll
                         for (int m = 0; m < R; ++m) {
                             if (m < rows) {
-                                if constexpr (MODE == 0) {
-                                    float xs[16];
-#pragma unroll
-                                    for (int u = 0; u < 4; ++u) {
-                                        float xv[4];
-                                        load_x4<FUSE>(actf + m * K + k + 4 * u, p.h + k + 4 * u,
-                                                      p.gain ? p.gain + k + 4 * u : nullptr, rf, xv);
-                                        xs[4 * u + 0] = xv[0];
-                                        xs[4 * u + 1] = xv[1];
-                                        xs[4 * u + 2] = xv[2];
-                                        xs[4 * u + 3] = xv[3];
-                                    }
-                                    fx[cc][m] = fix_chunk(xs);
-                                    p2s[cc][m] = ldexpf(1.0f, fx[cc][m].e - s_emax[m]);
-                                } else if constexpr (FUSE) {
+                                if constexpr (FUSE) {
                                     a1[cc][m] = lds_v4(act8 + m * K + k);
                                     if constexpr (MODE == 2) a2[cc][m] = lds_v4(act8 + plane + m * K + k);
                                     xdv[cc][m] = xdp[m * nb + (k >> 5)];
@@ -659,16 +608,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     __syncwarp();
                     if (lane == 0 && ok) mbar_arrive(&empty[slot]);
                 }
-                if (have) {
+                if constexpr (MODE != 0) if (have) {
 #pragma unroll
                     for (int m = 0; m < R; ++m) {
                         if (m < rows) {
-                            if constexpr (MODE == 0) {
-#pragma unroll
-                                for (int cc = 0; cc < GC; ++cc)
-                                    part[m] = df_add(part[m], scaled_pair(__fmul_rn(sw[cc], p2s[c0 + cc][m]),
-                                                                          fix_dot(w[cc], fx[c0 + cc][m])));
-                            } else {
+                            {
 #pragma unroll
                                 for (int cc = 0; cc < GC; ++cc) {
                                     const int isum = (MODE == 1) ? dot16_i8(w[cc], a1[c0 + cc][m])
@@ -713,16 +657,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     const int rsb = rbi * g.RS + jrow + i * (g.RS / g.rpw);
                     psum[((size_t(rsb) * g.nks + sl) * g.nprr + pw) * R + m] = tot;
                 }
-            } else if (have) {
-                A* ps = psum + ((size_t(row_sb) * g.nks + sl) * g.nprr + pw) * R;
-                if constexpr (MODE == 0) {
-#pragma unroll
-                    for (int m = 0; m < R; ++m) part[m] = warp_sum(part[m]);
-                    if (lane == 0) {
-#pragma unroll
-                        for (int m = 0; m < R; ++m) ps[m] = part[m];
-                    }
-                } else {
+            } else if constexpr (MODE != 0) {
+                if (have) {
+                    A* ps = psum + ((size_t(row_sb) * g.nks + sl) * g.nprr + pw) * R;
                     const float tot = warp_sum_rows<R>(part, lane);
                     if ((lane & (32 / R - 1)) == 0) ps[lane / (32 / R)] = tot;
                 }
@@ -775,8 +712,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 double val = acc_value(s);
                 if constexpr (kBL) {
                     val = ldexp(val, E - 30);
-                } else if constexpr (MODE == 0) {
-                    val = ldexp(val, s_emax[m] - 30);
                 }
                 if (p.y) {
                     if (MODE == 0 && p.out_f64)
