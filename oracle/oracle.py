@@ -59,6 +59,7 @@ def _load():
                 "orc_f32_to_f16": (C.c_uint16, [C.c_float]),
                 "orc_q8_pack": (i64, [vp, i64, i64, vp, vp]),
                 "orc_rmsnorm": (None, [vp, vp, i64, i64, C.c_float, vp, vp]),
+                "orc_residual_add": (None, [vp, vp, i64, i64, vp]),
                 "orc_act_quant_i8": (None, [vp, i64, i64, vp, vp]),
                 "orc_act_quant_i8x2": (None, [vp, i64, i64, vp, vp, vp]),
                 "orc_block_dots": (None, [vp, vp, vp, i64, i64, i64, vp]),
@@ -132,6 +133,18 @@ def rmsnorm(h: np.ndarray, g: np.ndarray | None = None, eps: float = 1e-5):
     r = np.empty(rows, np.float64)
     _load().orc_rmsnorm(_p(h), _p(g), rows, k, float(eps), _p(x), _p(r))
     return x, r
+
+
+def residual_add(h: np.ndarray, r: np.ndarray):
+    """The residual added before the norm: s = h + r (f32, one rounding)."""
+    h = _c(h, np.float32)
+    r = _c(r, np.float32)
+    if h.shape != r.shape:
+        raise ValueError("h and r must have the same shape")
+    rows, k = h.shape
+    s = np.empty_like(h)
+    _load().orc_residual_add(_p(h), _p(r), rows, k, _p(s))
+    return s
 
 
 def act_quant_i8(x: np.ndarray):

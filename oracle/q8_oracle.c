@@ -176,6 +176,16 @@ void orc_rmsnorm(const float* h, const float* g, int64_t rows, int64_t K, float 
 }
 
 /*
+ * Residual added before the norm [lane: "Modules: kernels", a residual added
+ * before a norm].  s = h + r per value, one f32 addition (the sum of two f32
+ * values rounded once to f32); s is the RMSNorm's input and the updated
+ * residual stream.
+ */
+void orc_residual_add(const float* h, const float* r, int64_t rows, int64_t K, float* s) {
+    for (int64_t i = 0; i < rows * K; ++i) s[i] = h[i] + r[i];
+}
+
+/*
  * Mode "one int8 word" [lane: CudaKnobs, llama.cpp's one int8 word].  Per row m
  * and block b: amax = max |x|, d = amax / 127 (f32, kept as f32),
  * q = round_half_away(x / d) clamped to [-127, 127]; q = 0 when d == 0.

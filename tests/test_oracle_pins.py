@@ -328,6 +328,66 @@ def test_rmsnorm_matches_f64_formula(orc):
     assert np.all(np.abs(x1 - hd * ref_r[:, None]) <= 2 * 2.0**-24 * np.abs(hd * ref_r[:, None]))
 
 
+# ---------------------------------------------------------------- residual
+
+def _round_f32(v: Fraction) -> float:
+    """An exact rational rounded to the nearest binary32, ties to even (an
+    independent restatement of IEEE rounding: scale to a 24-bit integer
+    significand, round, rescale)."""
+    if v == 0:
+        return 0.0
+    sign = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)                      # subnormal range: fixed quantum 2^-149
+    q = Fraction(2) ** (e - 23)           # the quantum at this binade
+    m = a / q
+    n = m.numerator // m.denominator
+    rem = m - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    r = n * q
+    if r >= Fraction(2) ** 128:
+        return sign * float("inf")
+    return sign * float(r)
+
+
+def test_residual_add_exact_rational(orc):
+    # s = h + r rounded once: against exact rationals, over wide exponent gaps
+    rng = np.random.default_rng(21)
+    rows, k = 3, 256
+    h = (rng.standard_normal((rows, k)) * np.exp2(rng.integers(-30, 30, (rows, k)))).astype(np.float32)
+    r = (rng.standard_normal((rows, k)) * np.exp2(rng.integers(-30, 30, (rows, k)))).astype(np.float32)
+    s = orc.residual_add(h, r)
+    for i in range(rows):
+        for j in range(k):
+            want = _round_f32(Fraction(float(h[i, j])) + Fraction(float(r[i, j])))
+            assert float(s[i, j]) == want, (h[i, j], r[i, j], s[i, j], want)
+
+
+def test_residual_add_hand_cases(orc):
+    # hand-worked binary32 sums: ties to even at 2^24 and at 1, cancellation,
+    # overflow, and the identities r = 0 and r = -h
+    two24 = float(2 ** 24)
+    cases = [
+        (two24, 1.0, two24),                      # 2^24 + 1: a tie, stays even
+        (two24, 3.0, two24 + 4.0),                # 2^24 + 3: a tie, rounds up to even
+        (1.0, 2.0 ** -24, 1.0),                   # 1 + half an ulp: tie to even
+        (1.0, 3 * 2.0 ** -25, 1.0 + 2.0 ** -23),  # just above the tie
+        (1e30, -1e30, 0.0),
+        (3.0e38, 3.0e38, float("inf")),
+    ]
+    h = np.array([[c[0] for c in cases]], np.float32)
+    r = np.array([[c[1] for c in cases]], np.float32)
+    s = orc.residual_add(h, r)
+    assert [float(v) for v in s[0]] == [c[2] for c in cases]
+    x = synth.activations(np.random.default_rng(22), 2, 64)
+    assert np.array_equal(orc.residual_add(x, np.zeros_like(x)), x)
+    assert not np.any(orc.residual_add(x, -x))
+
+
 # ---------------------------------------------------------------- arg-max
 
 def test_argmax_hand_vectors(orc):
