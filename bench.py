@@ -554,6 +554,31 @@ def run_sweeps(native, torch, dev, capture, timed, Q, S):
     out["gemv_1024x1024_rows1"] = cfg0
     del Q0, S0
 
+    # the decode layer with the residual added before the norm in every
+    # producer (s = h + r written back), against the plain fused layer
+    resid = {}
+    Hs = [torch.from_numpy(synth.activations(rng, 1, k)).to(dev) for _, _, k in synth.LAYER_D4096]
+    R_in = [torch.from_numpy(synth.activations(rng, 1, k)).to(dev) for _, _, k in synth.LAYER_D4096]
+    S_out = [torch.empty((1, k), dtype=torch.float32, device=dev) for _, _, k in synth.LAYER_D4096]
+    for m in MODES:
+        ws = [torch.empty(native.q8_proj_fused_workspace(m, 1, k), dtype=torch.uint8, device=dev)
+              for _, _, k in synth.LAYER_D4096]
+        ys = [torch.empty((1, n), dtype=torch.float32, device=dev) for _, n, _ in synth.LAYER_D4096]
+
+        def body_r(c, m=m, ws=ws, ys=ys):
+            for p in range(4):
+                native.q8_proj_fused_residual(m, Q[c][p], S[c][p], Hs[p], R_in[p], ys[p], ws[p],
+                                              s_out=S_out[p])
+
+        def body_p(c, m=m, ws=ws, ys=ys):
+            for p in range(4):
+                native.q8_proj_fused(m, Q[c][p], S[c][p], Hs[p], ys[p], ws[p])
+        us_r = per_call_us(body_r, 1)
+        us_p = per_call_us(body_p, 1)
+        resid[m] = {"us_per_layer": round(us_r, 2), "plain_fused_us_per_layer": round(us_p, 2),
+                    "GB/s": round(LAYER_BYTES / (us_r * 1e-6) / 1e9, 1)}
+    out["decode_layer_residual_d4096"] = resid
+
     # batched decode: B stacked rows, each weight read once per batch
     batch = {}
     for m in ("i8", "i8x2", "f32"):

@@ -130,6 +130,20 @@ q8_status act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
                     const float* gain, float eps, void* xq, float* xd, void* stream);
 
 /*
+ * The producer with a residual added before the norm (codegen_cuda::lane,
+ * "Modules: kernels": a residual added before a norm).
+ *   s = h + r per value (one f32 rounding) is the producer's input: RMSNorm
+ *   of s, x = (s * rs) * gain, then the mode's quantisation, exactly as
+ *   act_quant with norm = 1 applied to s.
+ *   r      float [rows][K], required
+ *   s_out  float [rows][K] or NULL: receives s (the updated residual stream);
+ *          it must not overlap h or r (Q8_ERR_ARG)
+ */
+q8_status act_quant_residual(int mode, const float* h, const float* r, float* s_out, int64_t rows,
+                             int64_t K, const float* gain, float eps, void* xq, float* xd,
+                             void* stream);
+
+/*
  * Quantized projection of a stacked activation (codegen_cuda::lane: the
  * decode step, rows = 1, and a batch's step, rows = B, as one launch with
  * every weight read once for all rows).
@@ -159,6 +173,17 @@ q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N,
                         const float* h, int64_t rows, const float* gain, float eps, void* y,
                         int out_f64, void* workspace, size_t ws_bytes, void* stream);
 size_t q8_proj_fused_workspace(int mode, int64_t rows, int64_t K);
+
+/*
+ * q8_proj_fused with the residual added before the norm: the producer's
+ * input is s = h + r (see act_quant_residual), written to s_out when it is
+ * not NULL (s_out must not overlap h or r: every block of the decode launch
+ * reads all of h and r).  Same workspace as q8_proj_fused.
+ */
+q8_status q8_proj_fused_residual(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                                 const float* h, const float* r, float* s_out, int64_t rows,
+                                 const float* gain, float eps, void* y, int out_f64,
+                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * LM head fused with its arg-max (model::author, decode_head: "the final

@@ -169,7 +169,7 @@ const char* q8_status_str(int status) {
     }
 }
 
-int q8_version(void) { return 100; }
+int q8_version(void) { return 101; }
 
 int q8_last_cuda_error(void) { return t_last_cuda; }
 
@@ -201,8 +201,27 @@ q8_status q8_pack(const float* w, int64_t N, int64_t K, int8_t* q, uint16_t* s,
     return launched(launch_pack(w, N, K, q, s, overflow, ctx));
 }
 
-q8_status act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
-                    const float* gain, float eps, void* xq, float* xd, void* stream) {
+// [a, a + n) and [b, b + n) overlap (either NULL: no)
+static bool overlaps(const void* a, const void* b, size_t n) {
+    if (!a || !b) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + n && y < x + n;
+}
+
+// The residual's arguments: r required; s_out optional, 16-byte aligned and
+// disjoint from h and r (every CTA of a fused call reads all of h and r).
+static q8_status check_residual(const float* h, const float* r, const float* s_out, int64_t rows,
+                                int64_t K) {
+    if (!r) return Q8_ERR_ARG;
+    if (!aligned16(r) || (s_out && !aligned16(s_out))) return Q8_ERR_ALIGN;
+    const size_t n = size_t(rows) * size_t(K) * sizeof(float);
+    if (overlaps(s_out, h, n) || overlaps(s_out, r, n)) return Q8_ERR_ARG;
+    return Q8_OK;
+}
+
+static q8_status act_quant_impl(int mode, const float* h, const float* res, float* s_out, int64_t rows,
+                                int64_t K, int norm, const float* gain, float eps, void* xq, float* xd,
+                                void* stream) {
     if (!valid_mode(mode)) return Q8_ERR_MODE;
     if (!h || !xq || (mode != Q8_ACT_F32 && !xd)) return Q8_ERR_ARG;
     if (norm != 0 && norm != 1) return Q8_ERR_ARG;
@@ -214,7 +233,21 @@ q8_status act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
         return Q8_ERR_ALIGN;
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
-    return launched(launch_act_quant(mode, h, rows, K, norm, gain, eps, xq, xd, ctx));
+    return launched(launch_act_quant(mode, h, res, s_out, rows, K, norm, gain, eps, xq, xd, ctx));
+}
+
+q8_status act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
+                    const float* gain, float eps, void* xq, float* xd, void* stream) {
+    return act_quant_impl(mode, h, nullptr, nullptr, rows, K, norm, gain, eps, xq, xd, stream);
+}
+
+q8_status act_quant_residual(int mode, const float* h, const float* r, float* s_out, int64_t rows,
+                             int64_t K, const float* gain, float eps, void* xq, float* xd,
+                             void* stream) {
+    if (!h) return Q8_ERR_ARG;
+    const q8_status st = check_residual(h, r, s_out, rows, K);
+    if (st != Q8_OK) return st;
+    return act_quant_impl(mode, h, r, s_out, rows, K, 1, gain, eps, xq, xd, stream);
 }
 
 q8_status q8_proj(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
@@ -242,9 +275,10 @@ size_t q8_proj_fused_workspace(int mode, int64_t rows, int64_t K) {
     return round_up(act_bytes(mode, rows, K), 256) + round_up(size_t(rows) * (K / Q8_QK) * 4, 256);
 }
 
-q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
-                        const float* h, int64_t rows, const float* gain, float eps, void* y,
-                        int out_f64, void* workspace, size_t ws_bytes, void* stream) {
+static q8_status proj_fused_impl(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                                 const float* h, const float* res, float* s_out, int64_t rows,
+                                 const float* gain, float eps, void* y, int out_f64, void* workspace,
+                                 size_t ws_bytes, void* stream) {
     if (!workspace) return Q8_ERR_WORKSPACE;
     // (h stands in for the scales argument: the fused call has none)
     q8_status st = check_proj_args(mode, q, s, N, K, h, h, rows, y);
@@ -269,6 +303,8 @@ q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N,
         a.y = y;
         a.out_f64 = out_f64 ? 1 : 0;
         a.h = h;
+        a.res = res;
+        a.s_out = s_out;
         a.gain = gain;
         a.eps = eps;
         return launched(mode == Q8_ACT_F32 ? launch_gemv_fused_mode0(a, ctx)
@@ -277,10 +313,29 @@ q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N,
     }
     unsigned char* act = static_cast<unsigned char*>(workspace);
     float* xd = reinterpret_cast<float*>(act + round_up(act_bytes(mode, rows, K), 256));
-    cudaError_t e = launch_act_quant(mode, h, rows, K, 1, gain, eps, act, xd, ctx);
+    cudaError_t e = launch_act_quant(mode, h, res, s_out, rows, K, 1, gain, eps, act, xd, ctx);
     if (e != cudaSuccess) return cuda_fail(e);
     return project_dispatch(mode, q, s, N, K, act, mode == Q8_ACT_F32 ? nullptr : xd, rows, y,
                             out_f64 ? 1 : 0, ctx);
+}
+
+q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                        const float* h, int64_t rows, const float* gain, float eps, void* y,
+                        int out_f64, void* workspace, size_t ws_bytes, void* stream) {
+    return proj_fused_impl(mode, q, s, N, K, h, nullptr, nullptr, rows, gain, eps, y, out_f64,
+                           workspace, ws_bytes, stream);
+}
+
+q8_status q8_proj_fused_residual(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                                 const float* h, const float* r, float* s_out, int64_t rows,
+                                 const float* gain, float eps, void* y, int out_f64,
+                                 void* workspace, size_t ws_bytes, void* stream) {
+    if (!h) return Q8_ERR_ARG;
+    if (rows < 1 || rows > Q8_MAX_ROWS) return Q8_ERR_SHAPE;
+    const q8_status st = check_residual(h, r, s_out, rows, K);
+    if (st != Q8_OK) return st;
+    return proj_fused_impl(mode, q, s, N, K, h, r, s_out, rows, gain, eps, y, out_f64, workspace,
+                           ws_bytes, stream);
 }
 
 size_t head_argmax_workspace(int64_t rows) {

@@ -56,6 +56,8 @@ struct GemvParams {
     unsigned char* ws;
     int* err;
     const float* h;      // fused producer input (decode kernel only)
+    const float* res;    // residual added before the norm, or NULL
+    float* s_out;        // h + res written back (by CTA 0), or NULL
     const float* gain;
     float eps;
 };
@@ -136,9 +138,6 @@ __device__ __forceinline__ int binade(float a) {
     return eb == 0 ? -126 : eb - 126;
 }
 
-// 16 f32 activations -> 4 byte planes of X = rint(x * 2^(30-E)), |X| <= 2^30,
-// X = p3*2^24 + p2*2^16 + p1*2^8 + p0 (p3 signed, p2..p0 unsigned), and the
-// chunk's binade E.  Plane j word u packs elements 4u..4u+3.
 // 2^n as a float for -126 <= n <= 127, from its bit pattern.
 __device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }
 
@@ -173,6 +172,9 @@ __device__ __forceinline__ int rint_scaled30(float t, float s2) {
     return int((__float_as_uint(u) << 8) + __float_as_uint(w) - (0x4F400000u << 8) - 0x4B400000u);
 }
 
+// 16 f32 activations -> 4 byte planes of X = rint(x * 2^(30-E)), |X| <= 2^30,
+// X = p3*2^24 + p2*2^16 + p1*2^8 + p0 (p3 signed, p2..p0 unsigned), and the
+// chunk's binade E.  Plane j word u packs elements 4u..4u+3.
 struct FixChunk {
     int p[4][4];
     int e;

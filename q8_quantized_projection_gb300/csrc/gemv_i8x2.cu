@@ -20,7 +20,8 @@ cudaError_t launch_gemv_mode2(const GemvArgs& a, const LaunchCtx& ctx) {
 }
 
 cudaError_t launch_gemv_fused_mode2(const GemvArgs& a, const LaunchCtx& ctx) {
-    return launch_gemv_row_t<2, 1, false, true>(a, ctx);
+    return a.res ? launch_gemv_row_t<2, 1, false, true, true>(a, ctx)
+                 : launch_gemv_row_t<2, 1, false, true>(a, ctx);
 }
 
 }  // namespace q8

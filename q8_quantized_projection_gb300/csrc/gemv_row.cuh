@@ -209,16 +209,24 @@ __device__ __forceinline__ float mul_pow2_neg(float v, int d) {
 }
 
 // Four f32 activation values: read as they are, or (f32 mode with the
-// producer fused) formed as x = (h*rf)*g with the producer's two roundings.
+// producer fused) formed as x = (s*rf)*g with the producer's two roundings,
+// s = h or, with a residual r, h + r rounded once.
 template <bool FUSE>
-__device__ __forceinline__ void load_x4(const float* x, const float* h, const float* g, float rf,
-                                        float (&v)[4]) {
+__device__ __forceinline__ void load_x4(const float* x, const float* h, const float* r, const float* g,
+                                        float rf, float (&v)[4]) {
     const int4 t4 = ldg_nc_v4(FUSE ? h : x);
     v[0] = __int_as_float(t4.x);
     v[1] = __int_as_float(t4.y);
     v[2] = __int_as_float(t4.z);
     v[3] = __int_as_float(t4.w);
     if constexpr (FUSE) {
+        if (r) {
+            const int4 r4 = ldg_nc_v4(r);
+            v[0] = __fadd_rn(v[0], __int_as_float(r4.x));
+            v[1] = __fadd_rn(v[1], __int_as_float(r4.y));
+            v[2] = __fadd_rn(v[2], __int_as_float(r4.z));
+            v[3] = __fadd_rn(v[3], __int_as_float(r4.w));
+        }
         float gg[4] = {1.0f, 1.0f, 1.0f, 1.0f};
         if (g) {
             const int4 g4 = ldg_nc_v4(g);
@@ -242,10 +250,16 @@ __device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v,
     }
 }
 
-template <int MODE, int R, bool ARGMAX, bool FUSE>
+// RES (fused producer only): the residual is added before the norm; a
+// separate instantiation, so the plain fused kernel carries none of it.
+template <int MODE, int R, bool ARGMAX, bool FUSE, bool RES = false>
 __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvParams p) {
     static_assert(!FUSE || R == 1, "fused producer: one row");
     static_assert(MODE != 0 || R == 1, "f32 mode: one row per launch");
+    static_assert(!RES || FUSE, "the residual belongs to the fused producer");
+    // residual input and the updated residual stream (written by CTA 0 only)
+    const float* const res = RES ? p.res : nullptr;
+    float* const s_out = RES && blockIdx.x == 0 ? p.s_out : nullptr;
     using A = typename AccT<MODE>::T;
     constexpr int CPL = row_cpl<MODE, R>();
     constexpr int NW = kRowWarps;
@@ -356,7 +370,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     int64_t plane = p.plane;
     float rf = 1.0f;   // f32 mode, fused: x = (h*rf)*g is formed where it is used
     if constexpr (FUSE && MODE == 0) {
-        rf = row_rms_scale(p.h, K, p.eps, tid, 1, s_pair, &s_rf);
+        rf = row_rms_scale(p.h, res, s_out, K, p.eps, tid, 1, s_pair, &s_rf);
     } else if constexpr (FUSE) {
         // The producer, fused: RMSNorm -> quant of the one activation row into
         // shared memory, by the same code and thread layout as act_quant, while
@@ -364,7 +378,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         static_assert(NT == kProdThreads, "fused producer needs kProdThreads consumers");
         unsigned char* sact = reinterpret_cast<unsigned char*>(cand + NW * R) + 64;
         float* sxd = reinterpret_cast<float*>(sact + 2 * kFusedMaxK);
-        row_produce<MODE, true>(p.h, p.gain, p.eps, K, tid, 1, s_pair, &s_rf, sact, K, sxd);
+        // CTA 0 writes the updated residual stream, when asked
+        row_produce<MODE, true>(p.h, res, s_out, p.gain, p.eps, K, tid, 1, s_pair, &s_rf, sact, K,
+                                sxd);
         consumer_bar<NT>();
         act8 = reinterpret_cast<const signed char*>(sact);
         xdp = sxd;
@@ -437,8 +453,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             float xv[4];
-                            load_x4<FUSE>(actf + k + 4 * u, p.h + k + 4 * u, p.gain ? p.gain + k + 4 * u : nullptr,
-                                          rf, xv);
+                            load_x4<FUSE>(actf + k + 4 * u, p.h + k + 4 * u, RES ? res + k + 4 * u : nullptr,
+                                          p.gain ? p.gain + k + 4 * u : nullptr, rf, xv);
                             xs[4 * u + 0] = xv[0];
                             xs[4 * u + 1] = xv[1];
                             xs[4 * u + 2] = xv[2];
@@ -773,9 +789,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     }
 }
 
-template <int MODE, int R, bool ARGMAX, bool FUSE = false>
+template <int MODE, int R, bool ARGMAX, bool FUSE = false, bool RES = false>
 cudaError_t launch_gemv_row_t(const GemvArgs& a, const LaunchCtx& ctx) {
-    auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE>;
+    auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, RES>;
     constexpr size_t smem = row_smem_bytes<MODE, R, FUSE>();
     static bool configured = false;  // per process; one device per process
     if (!configured) {
@@ -800,6 +816,8 @@ cudaError_t launch_gemv_row_t(const GemvArgs& a, const LaunchCtx& ctx) {
     p.ws = reinterpret_cast<unsigned char*>(a.ws);
     p.err = ctx.dev_err;
     p.h = a.h;
+    p.res = a.res;
+    p.s_out = a.s_out;
     p.gain = a.gain;
     p.eps = a.eps;
 

@@ -21,8 +21,8 @@ int pdl_attrs(const LaunchCtx& ctx, cudaLaunchAttribute* attrs);
 cudaError_t launch_pack(const float* w, int64_t N, int64_t K, int8_t* q, uint16_t* s,
                         int32_t* overflow, const LaunchCtx& ctx);
 
-cudaError_t launch_act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
-                             const float* gain, float eps, void* xq, float* xd,
+cudaError_t launch_act_quant(int mode, const float* h, const float* res, float* s_out, int64_t rows,
+                             int64_t K, int norm, const float* gain, float eps, void* xq, float* xd,
                              const LaunchCtx& ctx);
 
 // One CUDA-core GEMV launch over a group of at most `gemv_max_rows(mode)`
@@ -45,6 +45,8 @@ struct GemvArgs {
     // producer fused into the projection (decode step, one row): when h is
     // set, act/xd are ignored and the kernel runs RMSNorm -> quant itself
     const float* h;
+    const float* res;    // residual added before the norm, or NULL
+    float* s_out;        // h + res written back, or NULL
     const float* gain;
     float eps;
 };

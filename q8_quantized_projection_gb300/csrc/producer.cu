@@ -69,6 +69,8 @@ cudaError_t launch_pack(const float* w, int64_t N, int64_t K, int8_t* q, uint16_
 
 struct AqParams {
     const float* h;
+    const float* res;   // residual added before the norm, or NULL
+    float* s_out;       // h + res written back, or NULL
     const float* gain;
     float eps;
     int64_t rows, K;
@@ -78,7 +80,7 @@ struct AqParams {
 
 // One CTA of kProdThreads threads per activation row (rmsnorm.cuh holds the
 // arithmetic, shared with the decode projection's fused producer).
-template <int MODE, bool NORM>
+template <int MODE, bool NORM, bool RES>
 __global__ void __launch_bounds__(kProdThreads) act_quant_kernel(const AqParams p) {
     __shared__ float2 s_pair[kProdWarps];
     __shared__ float s_rf;
@@ -95,11 +97,13 @@ __global__ void __launch_bounds__(kProdThreads) act_quant_kernel(const AqParams 
         out = reinterpret_cast<float*>(p.out) + m * K;
     else
         out = reinterpret_cast<int8_t*>(p.out) + m * K;
-    row_produce<MODE, NORM>(h, p.gain, p.eps, K, tid, 1, s_pair, &s_rf, out, p.rows * K,
+    row_produce<MODE, NORM>(h, RES ? p.res + m * K : nullptr,
+                            RES && p.s_out ? p.s_out + m * K : nullptr, p.gain, p.eps, K, tid, 1,
+                            s_pair, &s_rf, out, p.rows * K,
                             MODE == 0 ? nullptr : p.xd + m * nb);
 }
 
-template <int MODE, bool NORM>
+template <int MODE, bool NORM, bool RES = false>
 static cudaError_t launch_aq_t(const AqParams& p, const LaunchCtx& ctx) {
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attrs[1];
@@ -108,13 +112,18 @@ static cudaError_t launch_aq_t(const AqParams& p, const LaunchCtx& ctx) {
     cfg.stream = ctx.stream;
     cfg.numAttrs = pdl_attrs(ctx, attrs);
     cfg.attrs = attrs;
-    return cudaLaunchKernelEx(&cfg, act_quant_kernel<MODE, NORM>, p);
+    return cudaLaunchKernelEx(&cfg, act_quant_kernel<MODE, NORM, RES>, p);
 }
 
-cudaError_t launch_act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
-                             const float* gain, float eps, void* xq, float* xd,
+cudaError_t launch_act_quant(int mode, const float* h, const float* res, float* s_out, int64_t rows,
+                             int64_t K, int norm, const float* gain, float eps, void* xq, float* xd,
                              const LaunchCtx& ctx) {
-    AqParams p{h, gain, eps, rows, K, xq, xd};
+    AqParams p{h, res, s_out, gain, eps, rows, K, xq, xd};
+    if (res) {   // the residual comes with the norm (act_quant_residual)
+        if (mode == 0) return launch_aq_t<0, true, true>(p, ctx);
+        if (mode == 1) return launch_aq_t<1, true, true>(p, ctx);
+        return launch_aq_t<2, true, true>(p, ctx);
+    }
     if (norm) {
         if (mode == 0) return launch_aq_t<0, true>(p, ctx);
         if (mode == 1) return launch_aq_t<1, true>(p, ctx);

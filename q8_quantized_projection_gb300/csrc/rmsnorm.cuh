@@ -201,18 +201,38 @@ __device__ __forceinline__ float rms_scale_reduce(float sh, float sl, int64_t K,
     return *s_rf;
 }
 
+// Float4 group gi of the producer's input: h, or with a residual r the sum
+// s = h + r (one f32 rounding, the residual added before the norm), stored to
+// s_out when it is set (the updated residual stream).
+__device__ __forceinline__ float4 load_input4(const float* h, const float* r, float* s_out, int64_t gi) {
+    const int4 v = ldg_nc_v4(h + 4 * gi);
+    float4 s = make_float4(__int_as_float(v.x), __int_as_float(v.y), __int_as_float(v.z),
+                           __int_as_float(v.w));
+    if (r) {
+        const int4 w = ldg_nc_v4(r + 4 * gi);
+        s.x = __fadd_rn(s.x, __int_as_float(w.x));
+        s.y = __fadd_rn(s.y, __int_as_float(w.y));
+        s.z = __fadd_rn(s.z, __int_as_float(w.z));
+        s.w = __fadd_rn(s.w, __int_as_float(w.w));
+    }
+    if (s_out) *reinterpret_cast<float4*>(s_out + 4 * gi) = s;
+    return s;
+}
+
 // rf alone (the f32 mode's fused producer, whose consumers form x = (h*rf)*g
 // themselves): the same per-thread order of squares as row_produce, so the
 // same rf.
-__device__ __forceinline__ float row_rms_scale(const float* h, int64_t K, float eps, int tid, int bar,
-                                               float2* s_pair, float* s_rf) {
+// With a residual r the input is s = h + r, stored to s_out when it is set.
+__device__ __forceinline__ float row_rms_scale(const float* h, const float* r, float* s_out, int64_t K,
+                                               float eps, int tid, int bar, float2* s_pair,
+                                               float* s_rf) {
     float sh = 0.0f, sl = 0.0f;
     for (int64_t gi = tid; gi < (K >> 2); gi += kProdThreads) {
-        const int4 v = ldg_nc_v4(h + 4 * gi);
-        pair_add_sq(sh, sl, __int_as_float(v.x));
-        pair_add_sq(sh, sl, __int_as_float(v.y));
-        pair_add_sq(sh, sl, __int_as_float(v.z));
-        pair_add_sq(sh, sl, __int_as_float(v.w));
+        const float4 v = load_input4(h, r, s_out, gi);
+        pair_add_sq(sh, sl, v.x);
+        pair_add_sq(sh, sl, v.y);
+        pair_add_sq(sh, sl, v.z);
+        pair_add_sq(sh, sl, v.w);
     }
     return rms_scale_reduce(sh, sl, K, eps, tid, bar, s_pair, s_rf);
 }
@@ -229,10 +249,13 @@ __device__ __forceinline__ float row_rms_scale(const float* h, int64_t K, float 
 //  * Quantisation: a 32-value block is 8 consecutive float4 groups, held by 8
 //    consecutive lanes; amax is an exact max over 3 shuffles, the scale is
 //    d = amax / lim (IEEE division) and every code is round_half_away(x / d).
+// With a residual r (the residual added before the norm) the input is
+// s = h + r, one rounding, stored to s_out when it is set.
 template <int MODE, bool NORM>
-__device__ __forceinline__ void row_produce(const float* h, const float* gain, float eps,
-                                            int64_t K, int tid, int bar, float2* s_pair,
-                                            float* s_rf, void* out, int64_t plane, float* xd) {
+__device__ __forceinline__ void row_produce(const float* h, const float* r, float* s_out,
+                                            const float* gain, float eps, int64_t K, int tid,
+                                            int bar, float2* s_pair, float* s_rf, void* out,
+                                            int64_t plane, float* xd) {
     const int64_t groups = K >> 2;
     // every lane of a warp runs the same iterations (groups is a multiple of 8
     // and the stride a multiple of 32), so the block shuffles stay full
@@ -244,9 +267,7 @@ __device__ __forceinline__ void row_produce(const float* h, const float* gain, f
         hv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         gv[j] = make_float4(1.f, 1.f, 1.f, 1.f);
         if (j < iters && gi < groups) {
-            const int4 v = ldg_nc_v4(h + 4 * gi);
-            hv[j] = make_float4(__int_as_float(v.x), __int_as_float(v.y), __int_as_float(v.z),
-                                __int_as_float(v.w));
+            hv[j] = load_input4(h, r, s_out, gi);
             if (NORM && gain) {
                 const int4 g4 = ldg_nc_v4(gain + 4 * gi);
                 gv[j] = make_float4(__int_as_float(g4.x), __int_as_float(g4.y),
@@ -265,11 +286,11 @@ __device__ __forceinline__ void row_produce(const float* h, const float* gain, f
             pair_add_sq(sh, sl, hv[j].w);
         }
         for (int64_t gi = tid + int64_t(kProdCache) * kProdThreads; gi < groups; gi += kProdThreads) {
-            const int4 v = ldg_nc_v4(h + 4 * gi);
-            pair_add_sq(sh, sl, __int_as_float(v.x));
-            pair_add_sq(sh, sl, __int_as_float(v.y));
-            pair_add_sq(sh, sl, __int_as_float(v.z));
-            pair_add_sq(sh, sl, __int_as_float(v.w));
+            const float4 v = load_input4(h, r, nullptr, gi);   // stored in the pass below
+            pair_add_sq(sh, sl, v.x);
+            pair_add_sq(sh, sl, v.y);
+            pair_add_sq(sh, sl, v.z);
+            pair_add_sq(sh, sl, v.w);
         }
         rf = rms_scale_reduce(sh, sl, K, eps, tid, bar, s_pair, s_rf);
     }
@@ -289,11 +310,11 @@ __device__ __forceinline__ void row_produce(const float* h, const float* gain, f
         float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         float gg[4] = {1.0f, 1.0f, 1.0f, 1.0f};
         if (live) {
-            const int4 v = ldg_nc_v4(h + 4 * gi);
-            x[0] = __int_as_float(v.x);
-            x[1] = __int_as_float(v.y);
-            x[2] = __int_as_float(v.z);
-            x[3] = __int_as_float(v.w);
+            const float4 v = load_input4(h, r, s_out, gi);
+            x[0] = v.x;
+            x[1] = v.y;
+            x[2] = v.z;
+            x[3] = v.w;
             if (NORM && gain) {
                 const int4 g4 = ldg_nc_v4(gain + 4 * gi);
                 gg[0] = __int_as_float(g4.x);

@@ -32,11 +32,14 @@ SIGNATURES = {
     "q8_set_pdl": (None, [_int]),
     "q8_pack": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp]),
     "act_quant": (_int, [_int, _vp, _i64, _i64, _int, _vp, C.c_float, _vp, _vp, _vp]),
+    "act_quant_residual": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _vp, C.c_float, _vp, _vp, _vp]),
     "q8_proj": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _int, _vp]),
     "q8_proj_chunk": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp]),
     "q8_proj_fused": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _i64, _vp, C.c_float, _vp, _int,
                              _vp, _sz, _vp]),
     "q8_proj_fused_workspace": (_sz, [_int, _i64, _i64]),
+    "q8_proj_fused_residual": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, C.c_float,
+                                      _vp, _int, _vp, _sz, _vp]),
     "head_argmax": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _sz,
                            _vp]),
     "head_argmax_workspace": (_sz, [_i64]),
@@ -124,6 +127,13 @@ def act_quant(mode, h, xq, xd, norm=False, gain=None, eps=1e-5, stream=None):
                             float(eps), _ptr(xq), _ptr(xd), _stream(stream)), "act_quant")
 
 
+def act_quant_residual(mode, h, r, xq, xd, s_out=None, gain=None, eps=1e-5, stream=None):
+    rows, k = h.shape
+    _check(load().act_quant_residual(_mode(mode), _ptr(h), _ptr(r), _ptr(s_out), rows, k, _ptr(gain),
+                                     float(eps), _ptr(xq), _ptr(xd), _stream(stream)),
+           "act_quant_residual")
+
+
 def q8_proj(mode, q, s, xq, xd, rows, y, out_f64=False, stream=None):
     n, k = q.shape
     _check(load().q8_proj(_mode(mode), _ptr(q), _ptr(s), n, k, _ptr(xq), _ptr(xd), rows, _ptr(y),
@@ -147,6 +157,18 @@ def q8_proj_fused(mode, q, s, h, y, workspace, gain=None, eps=1e-5, out_f64=Fals
                                 float(eps), _ptr(y), 1 if out_f64 else 0, _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream)),
            "q8_proj_fused")
+
+
+def q8_proj_fused_residual(mode, q, s, h, r, y, workspace, s_out=None, gain=None, eps=1e-5,
+                           out_f64=False, stream=None):
+    n, k = q.shape
+    rows = h.shape[0]
+    _check(load().q8_proj_fused_residual(_mode(mode), _ptr(q), _ptr(s), n, k, _ptr(h), _ptr(r),
+                                         _ptr(s_out), rows, _ptr(gain), float(eps), _ptr(y),
+                                         1 if out_f64 else 0, _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream(stream)),
+           "q8_proj_fused_residual")
 
 
 def head_argmax_workspace(rows) -> int:

@@ -166,6 +166,84 @@ def test_fused_matches_oracle_and_composition(mode, n, k, rows):
     assert np.array_equal(host(y).view(np.uint32), host(y2).view(np.uint32))
 
 
+# ------------------------------------------- residual added before the norm
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("rows,k", [(1, 96), (1, 4096), (3, 4128), (2, 14336), (17, 1024)])
+@pytest.mark.parametrize("with_gain", [False, True])
+def test_act_quant_residual_bit_exact(mode, rows, k, with_gain):
+    # s = h + r (one f32 rounding) written back, then the producer on s
+    rng = np.random.default_rng(40 + rows * 3 + k + (1 if with_gain else 0))
+    h = synth.activations(rng, rows, k)
+    r = synth.activations(rng, rows, k)
+    r[0, :QK] = -h[0, :QK]                      # a block that cancels to zero
+    g = synth.gain(rng, k) if with_gain else None
+    s_o = orc.residual_add(h, r)
+    act_o = orc.quantize(mode, orc.rmsnorm(s_o, g, 1e-5)[0])
+    t = torch()
+    xq, xd = native.activation_buffers(mode, rows, k)
+    s_out = t.empty((rows, k), dtype=t.float32, device="cuda")
+    native.act_quant_residual(mode, dev(h), dev(r), xq, xd, s_out=s_out,
+                              gain=dev(g) if g is not None else None, eps=1e-5)
+    assert np.array_equal(host(s_out).view(np.uint32), s_o.view(np.uint32))
+    for a, b in zip(act_to_numpy(mode, xq, xd), act_o):
+        assert np.array_equal(a.view(np.uint8) if a.dtype != np.float32 else a.view(np.uint32),
+                              b.view(np.uint8) if b.dtype != np.float32 else b.view(np.uint32))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n,k,rows", [(300, 4096, 1), (7, 14336, 1), (37, 96, 1), (100, 4096, 3)])
+def test_fused_residual_matches_oracle_and_composition(mode, n, k, rows):
+    rng = np.random.default_rng(60 + n + k + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    h = synth.activations(rng, rows, k)
+    r = synth.activations(rng, rows, k)
+    g = synth.gain(rng, k)
+    s_o = orc.residual_add(h, r)
+    y_o, norm = orc.project(mode, q, s, orc.quantize(mode, orc.rmsnorm(s_o, g, 1e-5)[0]))
+    qd, sd = upload_weights(q, s)
+    t = torch()
+    hd, rd, gd = dev(h), dev(r), dev(g)
+    ws = t.empty(native.q8_proj_fused_workspace(mode, rows, k), dtype=t.uint8, device="cuda")
+    y = t.empty((rows, n), dtype=t.float32, device="cuda")
+    s_out = t.full((rows, k), float("nan"), dtype=t.float32, device="cuda")
+    native.q8_proj_fused_residual(mode, qd, sd, hd, rd, y, ws, s_out=s_out, gain=gd, eps=1e-5)
+    check_close(mode, host(y), y_o, norm, what=f"fused residual {mode}")
+    assert np.array_equal(host(s_out).view(np.uint32), s_o.view(np.uint32))
+    # bitwise what the residual producer followed by the projection computes,
+    # and what the plain fused call computes on s
+    xq, xd = native.activation_buffers(mode, rows, k)
+    native.act_quant_residual(mode, hd, rd, xq, xd, gain=gd, eps=1e-5)
+    y2 = t.empty_like(y)
+    native.q8_proj(mode, qd, sd, xq, xd, rows, y2)
+    assert np.array_equal(host(y).view(np.uint32), host(y2).view(np.uint32))
+    y3 = t.empty_like(y)
+    native.q8_proj_fused(mode, qd, sd, dev(s_o), y3, ws, gain=gd, eps=1e-5)
+    assert np.array_equal(host(y).view(np.uint32), host(y3).view(np.uint32))
+    # without s_out nothing else changes
+    y4 = t.empty_like(y)
+    native.q8_proj_fused_residual(mode, qd, sd, hd, rd, y4, ws, gain=gd, eps=1e-5)
+    assert np.array_equal(host(y).view(np.uint32), host(y4).view(np.uint32))
+
+
+def test_residual_argument_errors():
+    t = torch()
+    k, n = 64, 8
+    q = t.zeros((n, k), dtype=t.int8, device="cuda")
+    s = t.zeros((n, k // QK), dtype=t.int16, device="cuda")
+    h = t.zeros((1, k), dtype=t.float32, device="cuda")
+    r = t.zeros((1, k), dtype=t.float32, device="cuda")
+    y = t.empty((1, n), dtype=t.float32, device="cuda")
+    ws = t.empty(native.q8_proj_fused_workspace("i8", 1, k), dtype=t.uint8, device="cuda")
+    xq, xd = native.activation_buffers("i8", 1, k)
+    with pytest.raises(native.Q8Error, match="Q8_ERR_ARG"):   # no residual
+        native.act_quant_residual("i8", h, None, xq, xd)
+    with pytest.raises(native.Q8Error, match="Q8_ERR_ARG"):   # s_out overlaps h
+        native.q8_proj_fused_residual("i8", q, s, h, r, y, ws, s_out=h)
+    with pytest.raises(native.Q8Error, match="Q8_ERR_ARG"):   # s_out overlaps r
+        native.act_quant_residual("i8", h, r, xq, xd, s_out=r)
+
+
 # ------------------------------------------------------------- LM head
 
 def _planted_head(n, k, rows, seed):
