@@ -60,6 +60,8 @@ def _load():
                 "orc_q8_pack": (i64, [vp, i64, i64, vp, vp]),
                 "orc_rmsnorm": (None, [vp, vp, i64, i64, C.c_float, vp, vp]),
                 "orc_residual_add": (None, [vp, vp, i64, i64, vp]),
+                "orc_exp_f32": (C.c_float, [C.c_float]),
+                "orc_swiglu": (None, [vp, i64, i64, vp]),
                 "orc_act_quant_i8": (None, [vp, i64, i64, vp, vp]),
                 "orc_act_quant_i8x2": (None, [vp, i64, i64, vp, vp, vp]),
                 "orc_block_dots": (None, [vp, vp, vp, i64, i64, i64, vp]),
@@ -145,6 +147,22 @@ def residual_add(h: np.ndarray, r: np.ndarray):
     s = np.empty_like(h)
     _load().orc_residual_add(_p(h), _p(r), rows, k, _p(s))
     return s
+
+
+def exp_f32(x: float) -> float:
+    """e^x in binary32 by the oracle's one definition (Cody-Waite + Taylor)."""
+    return float(_load().orc_exp_f32(float(x)))
+
+
+def swiglu(gu: np.ndarray):
+    """SwiGLU producer input: gu [rows, 2F] (gate | up) -> x f32 [rows, F]."""
+    gu = _c(gu, np.float32)
+    rows, f2 = gu.shape
+    if f2 % 2:
+        raise ValueError("gate+up row must have an even length")
+    x = np.empty((rows, f2 // 2), np.float32)
+    _load().orc_swiglu(_p(gu), rows, f2 // 2, _p(x))
+    return x
 
 
 def act_quant_i8(x: np.ndarray):

@@ -186,6 +186,59 @@ void orc_residual_add(const float* h, const float* r, int64_t rows, int64_t K, f
 }
 
 /*
+ * e^x in binary32, the one definition both sides of a SwiGLU parity check
+ * compute (a decision of a quantised code rests on it).  Method: Cody and
+ * Waite's argument reduction, x = k*ln2 + r with k = rint(x/ln2) and
+ * |r| <= ln2/2, where ln2 is carried as a 16-bit head (so k*head is exact for
+ * |k| <= 2^8) plus its binary32 remainder; then e^r by its Taylor series to
+ * degree 7, 1 + r + r^2/2! + ... + r^7/7! (coefficients 1/i! rounded to
+ * binary32), in Horner form with fused multiply-adds; then times 2^k in two
+ * exact power-of-two steps.  Truncation error below r^8/8! < 6e-9 relative.
+ *   1/ln2 -> 0x1.715476p+0, ln2 head 0x1.62e4p-1, remainder 0x1.7f7d1cp-20.
+ */
+float orc_exp_f32(float x) {
+    if (x != x) return x;
+    if (x > 88.75f) return INFINITY;
+    if (x < -104.0f) return 0.0f;
+    const float magic = 12582912.0f;   /* 1.5 * 2^23: rint by addition */
+    const float t = fmaf(x, 0x1.715476p+0f, magic);
+    const float kf = t - magic;
+    const int k = (int)kf;
+    float r = fmaf(-kf, 0x1.62e4p-1f, x);
+    r = fmaf(-kf, 0x1.7f7d1cp-20f, r);
+    float p = 0x1.a01a02p-13f;           /* 1/7! */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);      /* 1/6! */
+    p = fmaf(p, r, 0x1.111112p-7f);       /* 1/5! */
+    p = fmaf(p, r, 0x1.555556p-5f);       /* 1/4! */
+    p = fmaf(p, r, 0x1.555556p-3f);       /* 1/3! */
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    const int k1 = k >> 1, k2 = k - k1;   /* each in [-76, 64]: exact powers */
+    return (p * ldexpf(1.0f, k1)) * ldexpf(1.0f, k2);
+}
+
+/*
+ * The SwiGLU producer of the down projection [lane: "Modules: kernels", an
+ * activation quantized in a producer's epilogue; the FFN whose gate and up
+ * projections run as one fused matrix].  gu[m] holds the fused gate+up output
+ * row: gate = gu[m][0..F), up = gu[m][F..2F).  x = silu(gate) * up with
+ * silu(g) = g / (1 + e^-g), every step one binary32 rounding (e^-g by
+ * orc_exp_f32, the division IEEE).
+ */
+void orc_swiglu(const float* gu, int64_t rows, int64_t F, float* x) {
+    for (int64_t m = 0; m < rows; ++m) {
+        const float* g = gu + m * 2 * F;
+        const float* u = g + F;
+        for (int64_t k = 0; k < F; ++k) {
+            const float e = orc_exp_f32(-g[k]);
+            const float silu = g[k] / (1.0f + e);
+            x[m * F + k] = silu * u[k];
+        }
+    }
+}
+
+/*
  * Mode "one int8 word" [lane: CudaKnobs, llama.cpp's one int8 word].  Per row m
  * and block b: amax = max |x|, d = amax / 127 (f32, kept as f32),
  * q = round_half_away(x / d) clamped to [-127, 127]; q = 0 when d == 0.

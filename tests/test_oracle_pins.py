@@ -388,6 +388,55 @@ def test_residual_add_hand_cases(orc):
     assert not np.any(orc.residual_add(x, -x))
 
 
+# ---------------------------------------------------------------- SwiGLU
+
+def _ulps(a: float, b: float) -> int:
+    ia = int(np.float32(a).view(np.int32))
+    ib = int(np.float32(b).view(np.int32))
+    return abs(ia - ib)
+
+
+def test_exp_f32_within_one_ulp(orc):
+    # against the double-precision exponential rounded to binary32, over the
+    # whole finite range and its edges
+    xs = np.concatenate([np.linspace(-103.9, 88.7, 40001, dtype=np.float64),
+                         [1e-30, -1e-30, 0.5, -0.5, 1.0, -1.0, 10.0, -10.0]])
+    for x in xs.astype(np.float32):
+        want = math.exp(float(x))
+        assert _ulps(orc.exp_f32(float(x)), want) <= 1, x
+    assert orc.exp_f32(0.0) == 1.0
+    assert orc.exp_f32(89.0) == math.inf and orc.exp_f32(-105.0) == 0.0
+    assert orc.exp_f32(-math.inf) == 0.0 and orc.exp_f32(math.inf) == math.inf
+    assert math.isnan(orc.exp_f32(math.nan))
+    assert 0.0 < orc.exp_f32(-100.0) < 2.0 ** -126       # subnormal results exist
+
+
+def test_swiglu_special_values_and_layout(orc):
+    f = 4
+    gu = np.array([[0.0, 1.0, 20.0, -100.0,   # gate
+                    5.0, 2.0, 3.0, 7.0]],      # up
+                  np.float32)
+    x = orc.swiglu(gu)[0]
+    assert x[0] == 0.0                                  # silu(0) = 0
+    assert _ulps(x[1], 2.0 / (1.0 + math.exp(-1.0))) <= 2
+    assert x[2] == np.float32(60.0)                     # 1 + e^-20 rounds to 1
+    assert x[3] == 0.0                                  # e^100 overflows: silu -> -0
+    swapped = orc.swiglu(np.concatenate([gu[:, f:], gu[:, :f]], axis=1))[0]
+    assert not np.array_equal(swapped, x)               # gate first, then up
+
+
+def test_swiglu_matches_f64_formula(orc):
+    rng = np.random.default_rng(31)
+    f = 512
+    gu = (rng.standard_normal((3, 2 * f)) * 3.0).astype(np.float32)
+    x = orc.swiglu(gu)
+    g = gu[:, :f].astype(np.float64)
+    u = gu[:, f:].astype(np.float64)
+    ref = g / (1.0 + np.exp(-g)) * u
+    # four roundings of binary32 (exp, 1 + e, the division, the product)
+    assert np.all(np.abs(x - ref) <= 6 * 2.0 ** -24 * np.abs(ref) + 1e-38)
+
+
 # ---------------------------------------------------------------- arg-max
 
 def test_argmax_hand_vectors(orc):
