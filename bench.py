@@ -579,6 +579,26 @@ def run_sweeps(native, torch, dev, capture, timed, Q, S):
                     "GB/s": round(LAYER_BYTES / (us_r * 1e-6) / 1e9, 1)}
     out["decode_layer_residual_d4096"] = resid
 
+    # the down projection (4096 x 14336) fed by its SwiGLU producer from the
+    # gate+up output (2 x 14336 values), against the RMSNorm producer
+    swi = {}
+    _, n_dn, k_dn = synth.LAYER_D4096[3]
+    GU = torch.from_numpy((synth.activations(rng, 1, 2 * k_dn) * 3.0).astype(np.float32)).to(dev)
+    for m in MODES:
+        ws = torch.empty(native.q8_proj_fused_workspace(m, 1, k_dn), dtype=torch.uint8, device=dev)
+        yd = torch.empty((1, n_dn), dtype=torch.float32, device=dev)
+
+        def body_s(c, m=m, ws=ws, yd=yd):
+            native.q8_proj_fused_swiglu(m, Q[c][3], S[c][3], GU, yd, ws)
+
+        def body_n(c, m=m, ws=ws, yd=yd):
+            native.q8_proj_fused(m, Q[c][3], S[c][3], Hs[3], yd, ws)
+        us_s = per_call_us(body_s, 1, nrep=20)
+        us_n = per_call_us(body_n, 1, nrep=20)
+        swi[m] = {"us_per_call": round(us_s, 2), "rmsnorm_producer_us_per_call": round(us_n, 2),
+                  "GB/s": round(weight_bytes(n_dn, k_dn) / (us_s * 1e-6) / 1e9, 1)}
+    out["down_swiglu_4096x14336"] = swi
+
     # batched decode: B stacked rows, each weight read once per batch
     batch = {}
     for m in ("i8", "i8x2", "f32"):

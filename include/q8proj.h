@@ -144,6 +144,20 @@ q8_status act_quant_residual(int mode, const float* h, const float* r, float* s_
                              void* stream);
 
 /*
+ * The SwiGLU producer of the down projection (codegen_cuda::lane, "Modules:
+ * kernels": an activation quantized in its producer's epilogue; the FFN's gate
+ * and up projections run as one fused matrix).
+ *   gu  float [rows][2K]: each row the fused gate+up output, gate first
+ *       (gu[m][0..K)), then up (gu[m][K..2K))
+ *   x = silu(gate) * up, silu(g) = g / (1 + e^-g), every step one binary32
+ *   rounding with e^x computed by a fixed method (Cody-Waite reduction, the
+ *   degree-7 Taylor series), then the mode's quantisation (no norm); the
+ *   rest as act_quant.
+ */
+q8_status act_quant_swiglu(int mode, const float* gu, int64_t rows, int64_t K, void* xq, float* xd,
+                           void* stream);
+
+/*
  * Quantized projection of a stacked activation (codegen_cuda::lane: the
  * decode step, rows = 1, and a batch's step, rows = B, as one launch with
  * every weight read once for all rows).
@@ -184,6 +198,15 @@ q8_status q8_proj_fused_residual(int mode, const int8_t* q, const uint16_t* s, i
                                  const float* h, const float* r, float* s_out, int64_t rows,
                                  const float* gain, float eps, void* y, int out_f64,
                                  void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * The down projection with its SwiGLU producer fused (act_quant_swiglu, then
+ * the projection; one launch at rows = 1): q [N][K], gu [rows][2K].  Same
+ * workspace as q8_proj_fused.
+ */
+q8_status q8_proj_fused_swiglu(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                               const float* gu, int64_t rows, void* y, int out_f64, void* workspace,
+                               size_t ws_bytes, void* stream);
 
 /*
  * LM head fused with its arg-max (model::author, decode_head: "the final

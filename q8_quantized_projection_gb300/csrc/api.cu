@@ -169,7 +169,7 @@ const char* q8_status_str(int status) {
     }
 }
 
-int q8_version(void) { return 101; }
+int q8_version(void) { return 102; }
 
 int q8_last_cuda_error(void) { return t_last_cuda; }
 
@@ -219,9 +219,10 @@ static q8_status check_residual(const float* h, const float* r, const float* s_o
     return Q8_OK;
 }
 
-static q8_status act_quant_impl(int mode, const float* h, const float* res, float* s_out, int64_t rows,
-                                int64_t K, int norm, const float* gain, float eps, void* xq, float* xd,
-                                void* stream) {
+// prod: 0 plain, 1 residual, 2 SwiGLU (h: the gate+up output, rows of 2K)
+static q8_status act_quant_impl(int mode, int prod, const float* h, const float* res, float* s_out,
+                                int64_t rows, int64_t K, int norm, const float* gain, float eps,
+                                void* xq, float* xd, void* stream) {
     if (!valid_mode(mode)) return Q8_ERR_MODE;
     if (!h || !xq || (mode != Q8_ACT_F32 && !xd)) return Q8_ERR_ARG;
     if (norm != 0 && norm != 1) return Q8_ERR_ARG;
@@ -233,12 +234,12 @@ static q8_status act_quant_impl(int mode, const float* h, const float* res, floa
         return Q8_ERR_ALIGN;
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
-    return launched(launch_act_quant(mode, h, res, s_out, rows, K, norm, gain, eps, xq, xd, ctx));
+    return launched(launch_act_quant(mode, prod, h, res, s_out, rows, K, norm, gain, eps, xq, xd, ctx));
 }
 
 q8_status act_quant(int mode, const float* h, int64_t rows, int64_t K, int norm,
                     const float* gain, float eps, void* xq, float* xd, void* stream) {
-    return act_quant_impl(mode, h, nullptr, nullptr, rows, K, norm, gain, eps, xq, xd, stream);
+    return act_quant_impl(mode, 0, h, nullptr, nullptr, rows, K, norm, gain, eps, xq, xd, stream);
 }
 
 q8_status act_quant_residual(int mode, const float* h, const float* r, float* s_out, int64_t rows,
@@ -247,7 +248,12 @@ q8_status act_quant_residual(int mode, const float* h, const float* r, float* s_
     if (!h) return Q8_ERR_ARG;
     const q8_status st = check_residual(h, r, s_out, rows, K);
     if (st != Q8_OK) return st;
-    return act_quant_impl(mode, h, r, s_out, rows, K, 1, gain, eps, xq, xd, stream);
+    return act_quant_impl(mode, 1, h, r, s_out, rows, K, 1, gain, eps, xq, xd, stream);
+}
+
+q8_status act_quant_swiglu(int mode, const float* gu, int64_t rows, int64_t K, void* xq, float* xd,
+                           void* stream) {
+    return act_quant_impl(mode, 2, gu, nullptr, nullptr, rows, K, 0, nullptr, 0.0f, xq, xd, stream);
 }
 
 q8_status q8_proj(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
@@ -275,8 +281,8 @@ size_t q8_proj_fused_workspace(int mode, int64_t rows, int64_t K) {
     return round_up(act_bytes(mode, rows, K), 256) + round_up(size_t(rows) * (K / Q8_QK) * 4, 256);
 }
 
-static q8_status proj_fused_impl(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
-                                 const float* h, const float* res, float* s_out, int64_t rows,
+static q8_status proj_fused_impl(int mode, int prod, const int8_t* q, const uint16_t* s, int64_t N,
+                                 int64_t K, const float* h, const float* res, float* s_out, int64_t rows,
                                  const float* gain, float eps, void* y, int out_f64, void* workspace,
                                  size_t ws_bytes, void* stream) {
     if (!workspace) return Q8_ERR_WORKSPACE;
@@ -303,6 +309,7 @@ static q8_status proj_fused_impl(int mode, const int8_t* q, const uint16_t* s, i
         a.y = y;
         a.out_f64 = out_f64 ? 1 : 0;
         a.h = h;
+        a.prod = prod;
         a.res = res;
         a.s_out = s_out;
         a.gain = gain;
@@ -313,7 +320,8 @@ static q8_status proj_fused_impl(int mode, const int8_t* q, const uint16_t* s, i
     }
     unsigned char* act = static_cast<unsigned char*>(workspace);
     float* xd = reinterpret_cast<float*>(act + round_up(act_bytes(mode, rows, K), 256));
-    cudaError_t e = launch_act_quant(mode, h, res, s_out, rows, K, 1, gain, eps, act, xd, ctx);
+    cudaError_t e = launch_act_quant(mode, prod, h, res, s_out, rows, K, prod == 2 ? 0 : 1, gain, eps,
+                                     act, xd, ctx);
     if (e != cudaSuccess) return cuda_fail(e);
     return project_dispatch(mode, q, s, N, K, act, mode == Q8_ACT_F32 ? nullptr : xd, rows, y,
                             out_f64 ? 1 : 0, ctx);
@@ -322,7 +330,7 @@ static q8_status proj_fused_impl(int mode, const int8_t* q, const uint16_t* s, i
 q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                         const float* h, int64_t rows, const float* gain, float eps, void* y,
                         int out_f64, void* workspace, size_t ws_bytes, void* stream) {
-    return proj_fused_impl(mode, q, s, N, K, h, nullptr, nullptr, rows, gain, eps, y, out_f64,
+    return proj_fused_impl(mode, 0, q, s, N, K, h, nullptr, nullptr, rows, gain, eps, y, out_f64,
                            workspace, ws_bytes, stream);
 }
 
@@ -334,8 +342,15 @@ q8_status q8_proj_fused_residual(int mode, const int8_t* q, const uint16_t* s, i
     if (rows < 1 || rows > Q8_MAX_ROWS) return Q8_ERR_SHAPE;
     const q8_status st = check_residual(h, r, s_out, rows, K);
     if (st != Q8_OK) return st;
-    return proj_fused_impl(mode, q, s, N, K, h, r, s_out, rows, gain, eps, y, out_f64, workspace,
+    return proj_fused_impl(mode, 1, q, s, N, K, h, r, s_out, rows, gain, eps, y, out_f64, workspace,
                            ws_bytes, stream);
+}
+
+q8_status q8_proj_fused_swiglu(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                               const float* gu, int64_t rows, void* y, int out_f64, void* workspace,
+                               size_t ws_bytes, void* stream) {
+    return proj_fused_impl(mode, 2, q, s, N, K, gu, nullptr, nullptr, rows, nullptr, 0.0f, y, out_f64,
+                           workspace, ws_bytes, stream);
 }
 
 size_t head_argmax_workspace(int64_t rows) {

@@ -211,9 +211,19 @@ __device__ __forceinline__ float mul_pow2_neg(float v, int d) {
 // Four f32 activation values: read as they are, or (f32 mode with the
 // producer fused) formed as x = (s*rf)*g with the producer's two roundings,
 // s = h or, with a residual r, h + r rounded once.
-template <bool FUSE>
+// PROD == kProdSwiglu: h points into the fused gate+up row, whose up half
+// starts K values later, and x is the SwiGLU of the two (no norm).
+template <bool FUSE, int PROD = kProdPlain>
 __device__ __forceinline__ void load_x4(const float* x, const float* h, const float* r, const float* g,
-                                        float rf, float (&v)[4]) {
+                                        float rf, float (&v)[4], int64_t K = 0) {
+    if constexpr (FUSE && PROD == kProdSwiglu) {
+        const float4 s = load_swiglu4(h, K, 0);
+        v[0] = s.x;
+        v[1] = s.y;
+        v[2] = s.z;
+        v[3] = s.w;
+        return;
+    }
     const int4 t4 = ldg_nc_v4(FUSE ? h : x);
     v[0] = __int_as_float(t4.x);
     v[1] = __int_as_float(t4.y);
@@ -250,13 +260,17 @@ __device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v,
     }
 }
 
-// RES (fused producer only): the residual is added before the norm; a
-// separate instantiation, so the plain fused kernel carries none of it.
-template <int MODE, int R, bool ARGMAX, bool FUSE, bool RES = false>
+// PROD (fused producer only): kProdPlain (RMSNorm of h), kProdResidual (the
+// residual added before the norm) or kProdSwiglu (the SwiGLU of the fused
+// gate+up row h); each a separate instantiation, so the plain fused kernel
+// carries none of the others.
+template <int MODE, int R, bool ARGMAX, bool FUSE, int PROD = kProdPlain>
 __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvParams p) {
     static_assert(!FUSE || R == 1, "fused producer: one row");
     static_assert(MODE != 0 || R == 1, "f32 mode: one row per launch");
-    static_assert(!RES || FUSE, "the residual belongs to the fused producer");
+    static_assert(PROD == kProdPlain || FUSE, "producer kinds belong to the fused producer");
+    constexpr bool RES = PROD == kProdResidual;
+    constexpr bool NORM = PROD != kProdSwiglu;
     // residual input and the updated residual stream (written by CTA 0 only)
     const float* const res = RES ? p.res : nullptr;
     float* const s_out = RES && blockIdx.x == 0 ? p.s_out : nullptr;
@@ -370,8 +384,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     int64_t plane = p.plane;
     float rf = 1.0f;   // f32 mode, fused: x = (h*rf)*g is formed where it is used
     if constexpr (FUSE && MODE == 0) {
-        rf = row_rms_scale(p.h, res, s_out, K, p.eps, tid, 1, s_pair, &s_rf);
+        // f32: the consumers form x themselves (no shared-memory activation:
+        // the f32 kernel allocates none); with the norm only rf is computed here
+        if constexpr (NORM) rf = row_rms_scale(p.h, res, s_out, K, p.eps, tid, 1, s_pair, &s_rf);
     } else if constexpr (FUSE) {
+        static_assert(MODE != 0, "the shared-memory activation exists for the int8 modes only");
         // The producer, fused: RMSNorm -> quant of the one activation row into
         // shared memory, by the same code and thread layout as act_quant, while
         // the producer warp already streams weights.
@@ -379,8 +396,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         unsigned char* sact = reinterpret_cast<unsigned char*>(cand + NW * R) + 64;
         float* sxd = reinterpret_cast<float*>(sact + 2 * kFusedMaxK);
         // CTA 0 writes the updated residual stream, when asked
-        row_produce<MODE, true>(p.h, res, s_out, p.gain, p.eps, K, tid, 1, s_pair, &s_rf, sact, K,
-                                sxd);
+        row_produce<MODE, NORM, PROD>(p.h, res, s_out, p.gain, p.eps, K, tid, 1, s_pair, &s_rf, sact,
+                                      K, sxd);
         consumer_bar<NT>();
         act8 = reinterpret_cast<const signed char*>(sact);
         xdp = sxd;
@@ -453,8 +470,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             float xv[4];
-                            load_x4<FUSE>(actf + k + 4 * u, p.h + k + 4 * u, RES ? res + k + 4 * u : nullptr,
-                                          p.gain ? p.gain + k + 4 * u : nullptr, rf, xv);
+                            load_x4<FUSE, PROD>(actf + k + 4 * u, p.h + k + 4 * u,
+                                                RES ? res + k + 4 * u : nullptr,
+                                                p.gain ? p.gain + k + 4 * u : nullptr, rf, xv, K);
                             xs[4 * u + 0] = xv[0];
                             xs[4 * u + 1] = xv[1];
                             xs[4 * u + 2] = xv[2];
@@ -789,9 +807,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     }
 }
 
-template <int MODE, int R, bool ARGMAX, bool FUSE = false, bool RES = false>
+template <int MODE, int R, bool ARGMAX, bool FUSE = false, int PROD = kProdPlain>
 cudaError_t launch_gemv_row_t(const GemvArgs& a, const LaunchCtx& ctx) {
-    auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, RES>;
+    auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD>;
     constexpr size_t smem = row_smem_bytes<MODE, R, FUSE>();
     static bool configured = false;  // per process; one device per process
     if (!configured) {

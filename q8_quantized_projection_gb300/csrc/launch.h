@@ -21,9 +21,11 @@ int pdl_attrs(const LaunchCtx& ctx, cudaLaunchAttribute* attrs);
 cudaError_t launch_pack(const float* w, int64_t N, int64_t K, int8_t* q, uint16_t* s,
                         int32_t* overflow, const LaunchCtx& ctx);
 
-cudaError_t launch_act_quant(int mode, const float* h, const float* res, float* s_out, int64_t rows,
-                             int64_t K, int norm, const float* gain, float eps, void* xq, float* xd,
-                             const LaunchCtx& ctx);
+// prod: 0 plain (h, norm as given), 1 residual (h + res, normalised), 2 SwiGLU
+// (h the fused gate+up output, rows of 2K values; no norm)
+cudaError_t launch_act_quant(int mode, int prod, const float* h, const float* res, float* s_out,
+                             int64_t rows, int64_t K, int norm, const float* gain, float eps, void* xq,
+                             float* xd, const LaunchCtx& ctx);
 
 // One CUDA-core GEMV launch over a group of at most `gemv_max_rows(mode)`
 // activation rows.
@@ -45,6 +47,7 @@ struct GemvArgs {
     // producer fused into the projection (decode step, one row): when h is
     // set, act/xd are ignored and the kernel runs RMSNorm -> quant itself
     const float* h;
+    int prod;            // producer input: 0 h, 1 h + res, 2 SwiGLU of h (gate+up row)
     const float* res;    // residual added before the norm, or NULL
     float* s_out;        // h + res written back, or NULL
     const float* gain;

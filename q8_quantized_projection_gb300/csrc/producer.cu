@@ -80,14 +80,16 @@ struct AqParams {
 
 // One CTA of kProdThreads threads per activation row (rmsnorm.cuh holds the
 // arithmetic, shared with the decode projection's fused producer).
-template <int MODE, bool NORM, bool RES>
+// PROD: kProdPlain, kProdResidual (h + r before the norm) or kProdSwiglu (h is
+// the fused gate+up output, rows of 2K values).
+template <int MODE, bool NORM, int PROD>
 __global__ void __launch_bounds__(kProdThreads) act_quant_kernel(const AqParams p) {
     __shared__ float2 s_pair[kProdWarps];
     __shared__ float s_rf;
     const int tid = threadIdx.x;
     const int64_t m = blockIdx.x;
     const int64_t K = p.K, nb = K / Q8_QK;
-    const float* h = p.h + m * K;
+    const float* h = p.h + m * K * (PROD == kProdSwiglu ? 2 : 1);
 
     pdl_wait();
     pdl_launch_dependents();
@@ -97,13 +99,14 @@ __global__ void __launch_bounds__(kProdThreads) act_quant_kernel(const AqParams 
         out = reinterpret_cast<float*>(p.out) + m * K;
     else
         out = reinterpret_cast<int8_t*>(p.out) + m * K;
-    row_produce<MODE, NORM>(h, RES ? p.res + m * K : nullptr,
-                            RES && p.s_out ? p.s_out + m * K : nullptr, p.gain, p.eps, K, tid, 1,
-                            s_pair, &s_rf, out, p.rows * K,
+    constexpr bool RES = PROD == kProdResidual;
+    row_produce<MODE, NORM, PROD>(h, RES ? p.res + m * K : nullptr,
+                                  RES && p.s_out ? p.s_out + m * K : nullptr, p.gain, p.eps, K, tid,
+                                  1, s_pair, &s_rf, out, p.rows * K,
                             MODE == 0 ? nullptr : p.xd + m * nb);
 }
 
-template <int MODE, bool NORM, bool RES = false>
+template <int MODE, bool NORM, int PROD = kProdPlain>
 static cudaError_t launch_aq_t(const AqParams& p, const LaunchCtx& ctx) {
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attrs[1];
@@ -112,17 +115,22 @@ static cudaError_t launch_aq_t(const AqParams& p, const LaunchCtx& ctx) {
     cfg.stream = ctx.stream;
     cfg.numAttrs = pdl_attrs(ctx, attrs);
     cfg.attrs = attrs;
-    return cudaLaunchKernelEx(&cfg, act_quant_kernel<MODE, NORM, RES>, p);
+    return cudaLaunchKernelEx(&cfg, act_quant_kernel<MODE, NORM, PROD>, p);
 }
 
-cudaError_t launch_act_quant(int mode, const float* h, const float* res, float* s_out, int64_t rows,
-                             int64_t K, int norm, const float* gain, float eps, void* xq, float* xd,
-                             const LaunchCtx& ctx) {
+cudaError_t launch_act_quant(int mode, int prod, const float* h, const float* res, float* s_out,
+                             int64_t rows, int64_t K, int norm, const float* gain, float eps, void* xq,
+                             float* xd, const LaunchCtx& ctx) {
     AqParams p{h, res, s_out, gain, eps, rows, K, xq, xd};
-    if (res) {   // the residual comes with the norm (act_quant_residual)
-        if (mode == 0) return launch_aq_t<0, true, true>(p, ctx);
-        if (mode == 1) return launch_aq_t<1, true, true>(p, ctx);
-        return launch_aq_t<2, true, true>(p, ctx);
+    if (prod == kProdResidual) {   // the residual comes with the norm
+        if (mode == 0) return launch_aq_t<0, true, kProdResidual>(p, ctx);
+        if (mode == 1) return launch_aq_t<1, true, kProdResidual>(p, ctx);
+        return launch_aq_t<2, true, kProdResidual>(p, ctx);
+    }
+    if (prod == kProdSwiglu) {     // no norm
+        if (mode == 0) return launch_aq_t<0, false, kProdSwiglu>(p, ctx);
+        if (mode == 1) return launch_aq_t<1, false, kProdSwiglu>(p, ctx);
+        return launch_aq_t<2, false, kProdSwiglu>(p, ctx);
     }
     if (norm) {
         if (mode == 0) return launch_aq_t<0, true>(p, ctx);

@@ -201,6 +201,58 @@ __device__ __forceinline__ float rms_scale_reduce(float sh, float sl, int64_t K,
     return *s_rf;
 }
 
+// Kinds of producer input: h as given (optionally normalised), the residual
+// sum h + r (normalised), or the SwiGLU of a fused gate+up row (not
+// normalised).
+constexpr int kProdPlain = 0;
+constexpr int kProdResidual = 1;
+constexpr int kProdSwiglu = 2;
+
+// e^x in binary32 by one fixed method, so that a producer's codes are
+// reproducible from its definition: Cody and Waite's reduction x = k*ln2 + r,
+// k = rint(x/ln2), |r| <= ln2/2, with ln2 as a 16-bit head (k*head exact for
+// |k| <= 2^8) plus its binary32 remainder; e^r by its Taylor series to degree
+// 7 (coefficients 1/i! rounded to binary32) in Horner form with fused
+// multiply-adds; then 2^k in two exact power-of-two steps.  Within one ulp of
+// the correctly rounded e^x on [-104, 88.7].
+__device__ __forceinline__ float exp_cw(float x) {
+    if (x != x) return x;
+    if (x > 88.75f) return __int_as_float(0x7f800000);
+    if (x < -104.0f) return 0.0f;
+    const float magic = 12582912.0f;   // 1.5*2^23: rint by addition
+    const float t = __fmaf_rn(x, 0x1.715476p+0f, magic);
+    const float kf = __fsub_rn(t, magic);
+    const int k = __float_as_int(t) - 0x4B400000;
+    float r = __fmaf_rn(-kf, 0x1.62e4p-1f, x);
+    r = __fmaf_rn(-kf, 0x1.7f7d1cp-20f, r);
+    float q = 0x1.a01a02p-13f;              // 1/7!
+    q = __fmaf_rn(q, r, 0x1.6c16c2p-10f);   // 1/6!
+    q = __fmaf_rn(q, r, 0x1.111112p-7f);    // 1/5!
+    q = __fmaf_rn(q, r, 0x1.555556p-5f);    // 1/4!
+    q = __fmaf_rn(q, r, 0x1.555556p-3f);    // 1/3!
+    q = __fmaf_rn(q, r, 0.5f);
+    q = __fmaf_rn(q, r, 1.0f);
+    q = __fmaf_rn(q, r, 1.0f);
+    const int k1 = k >> 1, k2 = k - k1;     // each in [-76, 64]
+    return __fmul_rn(__fmul_rn(q, __int_as_float((k1 + 127) << 23)), __int_as_float((k2 + 127) << 23));
+}
+
+// silu(g) * u = g / (1 + e^-g) * u, each step one binary32 rounding.
+__device__ __forceinline__ float swiglu1(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, exp_cw(-g))), u);
+}
+
+// Float4 group gi of a SwiGLU producer's input: gate = gu[0..F), up =
+// gu[F..2F) of the fused gate+up row.
+__device__ __forceinline__ float4 load_swiglu4(const float* gu, int64_t F, int64_t gi) {
+    const int4 g = ldg_nc_v4(gu + 4 * gi);
+    const int4 u = ldg_nc_v4(gu + F + 4 * gi);
+    return make_float4(swiglu1(__int_as_float(g.x), __int_as_float(u.x)),
+                       swiglu1(__int_as_float(g.y), __int_as_float(u.y)),
+                       swiglu1(__int_as_float(g.z), __int_as_float(u.z)),
+                       swiglu1(__int_as_float(g.w), __int_as_float(u.w)));
+}
+
 // Float4 group gi of the producer's input: h, or with a residual r the sum
 // s = h + r (one f32 rounding, the residual added before the norm), stored to
 // s_out when it is set (the updated residual stream).
@@ -250,8 +302,10 @@ __device__ __forceinline__ float row_rms_scale(const float* h, const float* r, f
 //    consecutive lanes; amax is an exact max over 3 shuffles, the scale is
 //    d = amax / lim (IEEE division) and every code is round_half_away(x / d).
 // With a residual r (the residual added before the norm) the input is
-// s = h + r, one rounding, stored to s_out when it is set.
-template <int MODE, bool NORM>
+// s = h + r, one rounding, stored to s_out when it is set.  PROD ==
+// kProdSwiglu: h is the fused gate+up row (2K values) and the input is its
+// SwiGLU (NORM is then false).
+template <int MODE, bool NORM, int PROD = kProdPlain>
 __device__ __forceinline__ void row_produce(const float* h, const float* r, float* s_out,
                                             const float* gain, float eps, int64_t K, int tid,
                                             int bar, float2* s_pair, float* s_rf, void* out,
@@ -267,7 +321,7 @@ __device__ __forceinline__ void row_produce(const float* h, const float* r, floa
         hv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         gv[j] = make_float4(1.f, 1.f, 1.f, 1.f);
         if (j < iters && gi < groups) {
-            hv[j] = load_input4(h, r, s_out, gi);
+            hv[j] = PROD == kProdSwiglu ? load_swiglu4(h, K, gi) : load_input4(h, r, s_out, gi);
             if (NORM && gain) {
                 const int4 g4 = ldg_nc_v4(gain + 4 * gi);
                 gv[j] = make_float4(__int_as_float(g4.x), __int_as_float(g4.y),
@@ -310,7 +364,7 @@ __device__ __forceinline__ void row_produce(const float* h, const float* r, floa
         float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         float gg[4] = {1.0f, 1.0f, 1.0f, 1.0f};
         if (live) {
-            const float4 v = load_input4(h, r, s_out, gi);
+            const float4 v = PROD == kProdSwiglu ? load_swiglu4(h, K, gi) : load_input4(h, r, s_out, gi);
             x[0] = v.x;
             x[1] = v.y;
             x[2] = v.z;

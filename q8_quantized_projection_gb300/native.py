@@ -33,6 +33,7 @@ SIGNATURES = {
     "q8_pack": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp]),
     "act_quant": (_int, [_int, _vp, _i64, _i64, _int, _vp, C.c_float, _vp, _vp, _vp]),
     "act_quant_residual": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _vp, C.c_float, _vp, _vp, _vp]),
+    "act_quant_swiglu": (_int, [_int, _vp, _i64, _i64, _vp, _vp, _vp]),
     "q8_proj": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _int, _vp]),
     "q8_proj_chunk": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp]),
     "q8_proj_fused": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _i64, _vp, C.c_float, _vp, _int,
@@ -40,6 +41,7 @@ SIGNATURES = {
     "q8_proj_fused_workspace": (_sz, [_int, _i64, _i64]),
     "q8_proj_fused_residual": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, C.c_float,
                                       _vp, _int, _vp, _sz, _vp]),
+    "q8_proj_fused_swiglu": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _i64, _vp, _int, _vp, _sz, _vp]),
     "head_argmax": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _sz,
                            _vp]),
     "head_argmax_workspace": (_sz, [_i64]),
@@ -134,6 +136,12 @@ def act_quant_residual(mode, h, r, xq, xd, s_out=None, gain=None, eps=1e-5, stre
            "act_quant_residual")
 
 
+def act_quant_swiglu(mode, gu, xq, xd, stream=None):
+    rows, k2 = gu.shape
+    _check(load().act_quant_swiglu(_mode(mode), _ptr(gu), rows, k2 // 2, _ptr(xq), _ptr(xd),
+                                   _stream(stream)), "act_quant_swiglu")
+
+
 def q8_proj(mode, q, s, xq, xd, rows, y, out_f64=False, stream=None):
     n, k = q.shape
     _check(load().q8_proj(_mode(mode), _ptr(q), _ptr(s), n, k, _ptr(xq), _ptr(xd), rows, _ptr(y),
@@ -169,6 +177,17 @@ def q8_proj_fused_residual(mode, q, s, h, r, y, workspace, s_out=None, gain=None
                                          workspace.numel() * workspace.element_size(),
                                          _stream(stream)),
            "q8_proj_fused_residual")
+
+
+def q8_proj_fused_swiglu(mode, q, s, gu, y, workspace, out_f64=False, stream=None):
+    n, k = q.shape
+    rows = gu.shape[0]
+    if gu.shape[1] != 2 * k:
+        raise ValueError("gate+up rows must hold 2K values")
+    _check(load().q8_proj_fused_swiglu(_mode(mode), _ptr(q), _ptr(s), n, k, _ptr(gu), rows, _ptr(y),
+                                       1 if out_f64 else 0, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)),
+           "q8_proj_fused_swiglu")
 
 
 def head_argmax_workspace(rows) -> int:

@@ -226,6 +226,45 @@ def test_fused_residual_matches_oracle_and_composition(mode, n, k, rows):
     assert np.array_equal(host(y).view(np.uint32), host(y4).view(np.uint32))
 
 
+# ------------------------------------------------ SwiGLU producer of down
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("rows,k", [(1, 96), (1, 14336), (3, 4128), (2, 1024), (17, 512)])
+def test_act_quant_swiglu_bit_exact(mode, rows, k):
+    rng = np.random.default_rng(80 + rows + k)
+    gu = (synth.activations(rng, rows, 2 * k) * 3.0).astype(np.float32)
+    gu[0, :QK] = 0.0                            # a gate block of zeros: x = 0
+    gu[-1, 1] = -120.0                          # e^120 overflows: silu -> -0
+    act_o = orc.quantize(mode, orc.swiglu(gu))
+    xq, xd = native.activation_buffers(mode, rows, k)
+    native.act_quant_swiglu(mode, dev(gu), xq, xd)
+    for a, b in zip(act_to_numpy(mode, xq, xd), act_o):
+        assert np.array_equal(a.view(np.uint8) if a.dtype != np.float32 else a.view(np.uint32),
+                              b.view(np.uint8) if b.dtype != np.float32 else b.view(np.uint32))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n,k,rows", [(300, 14336, 1), (64, 4096, 1), (37, 96, 1), (100, 1024, 3)])
+def test_fused_swiglu_matches_oracle_and_composition(mode, n, k, rows):
+    rng = np.random.default_rng(90 + n + k + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    gu = (synth.activations(rng, rows, 2 * k) * 3.0).astype(np.float32)
+    y_o, norm = orc.project(mode, q, s, orc.quantize(mode, orc.swiglu(gu)))
+    qd, sd = upload_weights(q, s)
+    t = torch()
+    gud = dev(gu)
+    ws = t.empty(native.q8_proj_fused_workspace(mode, rows, k), dtype=t.uint8, device="cuda")
+    y = t.empty((rows, n), dtype=t.float32, device="cuda")
+    native.q8_proj_fused_swiglu(mode, qd, sd, gud, y, ws)
+    check_close(mode, host(y), y_o, norm, what=f"fused swiglu {mode}")
+    # bitwise what the SwiGLU producer followed by the projection computes
+    xq, xd = native.activation_buffers(mode, rows, k)
+    native.act_quant_swiglu(mode, gud, xq, xd)
+    y2 = t.empty_like(y)
+    native.q8_proj(mode, qd, sd, xq, xd, rows, y2)
+    assert np.array_equal(host(y).view(np.uint32), host(y2).view(np.uint32))
+
+
 def test_residual_argument_errors():
     t = torch()
     k, n = 64, 8
