@@ -62,6 +62,7 @@ def _load():
                 "orc_residual_add": (None, [vp, vp, i64, i64, vp]),
                 "orc_exp_f32": (C.c_float, [C.c_float]),
                 "orc_swiglu": (None, [vp, i64, i64, vp]),
+                "orc_kv_write": (i64, [vp, i64, i64, vp, i64, i64, i64, vp, vp]),
                 "orc_act_quant_i8": (None, [vp, i64, i64, vp, vp]),
                 "orc_act_quant_i8x2": (None, [vp, i64, i64, vp, vp, vp]),
                 "orc_block_dots": (None, [vp, vp, vp, i64, i64, i64, vp]),
@@ -163,6 +164,24 @@ def swiglu(gu: np.ndarray):
     x = np.empty((rows, f2 // 2), np.float32)
     _load().orc_swiglu(_p(gu), rows, f2 // 2, _p(x))
     return x
+
+
+def kv_write(y: np.ndarray, pos, kv_col: int, d: int, k_cache: np.ndarray, v_cache: np.ndarray):
+    """Row m's K/V slices of y into cache row pos[m] (caches [rows, n_pos, d],
+    updated in place); returns the number of positions out of range."""
+    y = _c(y, np.float32)
+    rows, n = y.shape
+    pos = _c(np.asarray(pos), np.int32)
+    if k_cache.dtype != np.float32 or v_cache.dtype != np.float32:
+        raise ValueError("caches must be float32")
+    if not (k_cache.flags.c_contiguous and v_cache.flags.c_contiguous):
+        raise ValueError("caches must be contiguous")
+    if k_cache.shape != v_cache.shape or k_cache.shape[0] != rows or k_cache.shape[2] != d:
+        raise ValueError("caches must be [rows, n_pos, d]")
+    if kv_col < 0 or kv_col + 2 * d > n:
+        raise ValueError("K/V columns out of the row")
+    return int(_load().orc_kv_write(_p(y), rows, n, _p(pos), kv_col, d, k_cache.shape[1],
+                                    _p(k_cache), _p(v_cache)))
 
 
 def act_quant_i8(x: np.ndarray):

@@ -239,6 +239,31 @@ void orc_swiglu(const float* gu, int64_t rows, int64_t F, float* x) {
 }
 
 /*
+ * The K/V slice of a fused QKV projection written into the row of a cache a
+ * position names [lane: "Modules: kernels", a result written into the row of
+ * a cache a position names].  y [rows][N] is the projection output; row m's
+ * columns [kv_col, kv_col + D) are its K, [kv_col + D, kv_col + 2D) its V; the
+ * caches are [rows][n_pos][D] (one per sequence) and row m's entries go to
+ * cache row pos[m].  A position outside [0, n_pos) writes nothing and is
+ * counted in the return value.
+ */
+int64_t orc_kv_write(const float* y, int64_t rows, int64_t N, const int32_t* pos, int64_t kv_col,
+                     int64_t D, int64_t n_pos, float* k_cache, float* v_cache) {
+    int64_t bad = 0;
+    for (int64_t m = 0; m < rows; ++m) {
+        if (pos[m] < 0 || pos[m] >= n_pos) {
+            ++bad;
+            continue;
+        }
+        for (int64_t d = 0; d < D; ++d) {
+            k_cache[(m * n_pos + pos[m]) * D + d] = y[m * N + kv_col + d];
+            v_cache[(m * n_pos + pos[m]) * D + d] = y[m * N + kv_col + D + d];
+        }
+    }
+    return bad;
+}
+
+/*
  * Mode "one int8 word" [lane: CudaKnobs, llama.cpp's one int8 word].  Per row m
  * and block b: amax = max |x|, d = amax / 127 (f32, kept as f32),
  * q = round_half_away(x / d) clamped to [-127, 127]; q = 0 when d == 0.

@@ -437,6 +437,26 @@ def test_swiglu_matches_f64_formula(orc):
     assert np.all(np.abs(x - ref) <= 6 * 2.0 ** -24 * np.abs(ref) + 1e-38)
 
 
+# ---------------------------------------------------------------- KV rows
+
+def test_kv_write_hand_example(orc):
+    # two sequences, N = 10 outputs: q = columns 0..3, K = 4..6, V = 7..9
+    y = np.arange(20, dtype=np.float32).reshape(2, 10) + 0.5
+    kc = np.full((2, 4, 3), -1.0, np.float32)
+    vc = np.full((2, 4, 3), -1.0, np.float32)
+    bad = orc.kv_write(y, [2, 0], 4, 3, kc, vc)
+    assert bad == 0
+    assert kc[0, 2].tolist() == [4.5, 5.5, 6.5] and vc[0, 2].tolist() == [7.5, 8.5, 9.5]
+    assert kc[1, 0].tolist() == [14.5, 15.5, 16.5] and vc[1, 0].tolist() == [17.5, 18.5, 19.5]
+    untouched = np.ones((2, 4), bool)
+    untouched[0, 2] = untouched[1, 0] = False
+    assert np.all(kc[untouched] == -1.0) and np.all(vc[untouched] == -1.0)
+    # a position out of range writes nothing and is counted
+    kc2, vc2 = kc.copy(), vc.copy()
+    assert orc.kv_write(y, [4, -1], 4, 3, kc2, vc2) == 2
+    assert np.array_equal(kc2, kc) and np.array_equal(vc2, vc)
+
+
 # ---------------------------------------------------------------- arg-max
 
 def test_argmax_hand_vectors(orc):
