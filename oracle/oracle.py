@@ -171,7 +171,7 @@ def kv_write(y: np.ndarray, pos, kv_col: int, d: int, k_cache: np.ndarray, v_cac
     updated in place); returns the number of positions out of range."""
     y = _c(y, np.float32)
     rows, n = y.shape
-    pos = _c(np.asarray(pos), np.int32)
+    pos = _c(np.asarray(pos, dtype=np.int32), np.int32)
     if k_cache.dtype != np.float32 or v_cache.dtype != np.float32:
         raise ValueError("caches must be float32")
     if not (k_cache.flags.c_contiguous and v_cache.flags.c_contiguous):
