@@ -599,6 +599,27 @@ def run_sweeps(native, torch, dev, capture, timed, Q, S):
                   "GB/s": round(weight_bytes(n_dn, k_dn) / (us_s * 1e-6) / 1e9, 1)}
     out["down_swiglu_4096x14336"] = swi
 
+    # Wqkv (q 4096 | K 1024 | V 1024) with the K/V slices written into the
+    # cache rows a device position names (4096-row caches), against plain
+    kvl = {}
+    _, n_qkv, k_qkv = synth.LAYER_D4096[0]
+    KC = torch.zeros((1, 4096, 1024), dtype=torch.float32, device=dev)
+    VC = torch.zeros((1, 4096, 1024), dtype=torch.float32, device=dev)
+    POS = torch.tensor([1234], dtype=torch.int32, device=dev)
+    for m in MODES:
+        ws = torch.empty(native.q8_proj_fused_workspace(m, 1, k_qkv), dtype=torch.uint8, device=dev)
+        yq = torch.empty((1, n_qkv), dtype=torch.float32, device=dev)
+
+        def body_kv(c, m=m, ws=ws, yq=yq):
+            native.q8_proj_fused_kv(m, Q[c][0], S[c][0], Hs[0], yq, ws, POS, 4096, KC, VC)
+
+        def body_q(c, m=m, ws=ws, yq=yq):
+            native.q8_proj_fused(m, Q[c][0], S[c][0], Hs[0], yq, ws)
+        us_kv = per_call_us(body_kv, 1, nrep=20)
+        us_q = per_call_us(body_q, 1, nrep=20)
+        kvl[m] = {"us_per_call": round(us_kv, 2), "plain_fused_us_per_call": round(us_q, 2)}
+    out["wqkv_kv_rows_6144x4096"] = kvl
+
     # batched decode: B stacked rows, each weight read once per batch
     batch = {}
     for m in ("i8", "i8x2", "f32"):

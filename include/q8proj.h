@@ -98,7 +98,8 @@ int q8_last_cuda_error(void);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word of the
- * current device: 0 = none, 1 = a bounded wait ran out.  *code receives it.
+ * current device: 0 = none, 1 = a bounded wait ran out, 2 = a KV-cache
+ * position outside its cache (q8_proj_fused_kv).  *code receives it.
  */
 q8_status q8_device_error(int32_t* code /* host */, void* stream);
 
@@ -187,6 +188,26 @@ q8_status q8_proj_fused(int mode, const int8_t* q, const uint16_t* s, int64_t N,
                         const float* h, int64_t rows, const float* gain, float eps, void* y,
                         int out_f64, void* workspace, size_t ws_bytes, void* stream);
 size_t q8_proj_fused_workspace(int mode, int64_t rows, int64_t K);
+
+/*
+ * q8_proj_fused with the K/V slices of a fused QKV projection also written
+ * into the row of a cache that a position names (codegen_cuda::lane, "Modules:
+ * kernels": a result written into the row of a cache a position names).
+ *   y        float [rows][N]: the whole projection output, as q8_proj_fused
+ *   pos      int32 [rows], device memory: row m's position (read by the
+ *            launch, so one captured graph serves every step)
+ *   kv_col   first column of the K slice: K = columns [kv_col, kv_col + kv_dim),
+ *            V = [kv_col + kv_dim, kv_col + 2 kv_dim); kv_col + 2 kv_dim <= N
+ *   k_cache, v_cache  float [rows][n_pos][kv_dim], one cache per row's
+ *            sequence, disjoint; row m's slices go to cache row pos[m]
+ * K <= 16384.  A position outside [0, n_pos) writes no cache entry of its row
+ * and sets device error 2 (q8_device_error); y is written either way.
+ */
+q8_status q8_proj_fused_kv(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                           const float* h, int64_t rows, const float* gain, float eps, void* y,
+                           const int32_t* pos, int64_t kv_col, int64_t kv_dim, float* k_cache,
+                           float* v_cache, int64_t n_pos, void* workspace, size_t ws_bytes,
+                           void* stream);
 
 /*
  * q8_proj_fused with the residual added before the norm: the producer's

@@ -88,6 +88,14 @@ cudaError_t gemv_dispatch(const GemvArgs& a, const LaunchCtx& ctx) {
     return launch_gemv_mode2(a, ctx);
 }
 
+// The KV-row epilogue's arguments (k_cache NULL: none).
+struct KvArgs {
+    const int32_t* pos = nullptr;
+    int64_t kv_col = 0, kv_dim = 0, n_pos = 0;
+    float* k_cache = nullptr;
+    float* v_cache = nullptr;
+};
+
 // Runs the CUDA-core projection over groups of at most 16 activation rows.
 q8_status run_projection(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                          const void* xq, const float* xd, int64_t rows, void* y, int out_f64,
@@ -169,7 +177,7 @@ const char* q8_status_str(int status) {
     }
 }
 
-int q8_version(void) { return 102; }
+int q8_version(void) { return 103; }
 
 int q8_last_cuda_error(void) { return t_last_cuda; }
 
@@ -284,7 +292,7 @@ size_t q8_proj_fused_workspace(int mode, int64_t rows, int64_t K) {
 static q8_status proj_fused_impl(int mode, int prod, const int8_t* q, const uint16_t* s, int64_t N,
                                  int64_t K, const float* h, const float* res, float* s_out, int64_t rows,
                                  const float* gain, float eps, void* y, int out_f64, void* workspace,
-                                 size_t ws_bytes, void* stream) {
+                                 size_t ws_bytes, void* stream, const KvArgs& kv = KvArgs{}) {
     if (!workspace) return Q8_ERR_WORKSPACE;
     // (h stands in for the scales argument: the fused call has none)
     q8_status st = check_proj_args(mode, q, s, N, K, h, h, rows, y);
@@ -314,6 +322,12 @@ static q8_status proj_fused_impl(int mode, int prod, const int8_t* q, const uint
         a.s_out = s_out;
         a.gain = gain;
         a.eps = eps;
+        a.pos = kv.pos;
+        a.kv_col = kv.kv_col;
+        a.kv_dim = kv.kv_dim;
+        a.n_pos = kv.n_pos;
+        a.k_cache = kv.k_cache;
+        a.v_cache = kv.v_cache;
         return launched(mode == Q8_ACT_F32 ? launch_gemv_fused_mode0(a, ctx)
                         : mode == Q8_ACT_I8 ? launch_gemv_fused_mode1(a, ctx)
                                             : launch_gemv_fused_mode2(a, ctx));
@@ -323,6 +337,14 @@ static q8_status proj_fused_impl(int mode, int prod, const int8_t* q, const uint
     cudaError_t e = launch_act_quant(mode, prod, h, res, s_out, rows, K, prod == 2 ? 0 : 1, gain, eps,
                                      act, xd, ctx);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (kv.k_cache) {
+        // batches: the projection, then the K/V slices copied into the caches
+        const q8_status st2 = project_dispatch(mode, q, s, N, K, act, mode == Q8_ACT_F32 ? nullptr : xd,
+                                               rows, y, 0, ctx);
+        if (st2 != Q8_OK) return st2;
+        return launched(launch_kv_scatter(static_cast<const float*>(y), rows, N, kv.pos, kv.kv_col,
+                                          kv.kv_dim, kv.n_pos, kv.k_cache, kv.v_cache, ctx));
+    }
     return project_dispatch(mode, q, s, N, K, act, mode == Q8_ACT_F32 ? nullptr : xd, rows, y,
                             out_f64 ? 1 : 0, ctx);
 }
@@ -344,6 +366,29 @@ q8_status q8_proj_fused_residual(int mode, const int8_t* q, const uint16_t* s, i
     if (st != Q8_OK) return st;
     return proj_fused_impl(mode, 1, q, s, N, K, h, r, s_out, rows, gain, eps, y, out_f64, workspace,
                            ws_bytes, stream);
+}
+
+q8_status q8_proj_fused_kv(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                           const float* h, int64_t rows, const float* gain, float eps, void* y,
+                           const int32_t* pos, int64_t kv_col, int64_t kv_dim, float* k_cache,
+                           float* v_cache, int64_t n_pos, void* workspace, size_t ws_bytes,
+                           void* stream) {
+    if (!pos || !k_cache || !v_cache) return Q8_ERR_ARG;
+    if (rows < 1 || rows > Q8_MAX_ROWS) return Q8_ERR_SHAPE;
+    if (kv_dim < 1 || kv_col < 0 || kv_col + 2 * kv_dim > N || n_pos < 1) return Q8_ERR_SHAPE;
+    if (K > kFusedMaxK) return Q8_ERR_UNSUPPORTED;   // the decode kernel's K
+    if (!aligned16(pos) || !aligned16(k_cache) || !aligned16(v_cache)) return Q8_ERR_ALIGN;
+    const size_t cache = size_t(rows) * size_t(n_pos) * size_t(kv_dim) * sizeof(float);
+    if (overlaps(k_cache, v_cache, cache)) return Q8_ERR_ARG;
+    KvArgs kv;
+    kv.pos = pos;
+    kv.kv_col = kv_col;
+    kv.kv_dim = kv_dim;
+    kv.n_pos = n_pos;
+    kv.k_cache = k_cache;
+    kv.v_cache = v_cache;
+    return proj_fused_impl(mode, 0, q, s, N, K, h, nullptr, nullptr, rows, gain, eps, y, 0, workspace,
+                           ws_bytes, stream, kv);
 }
 
 q8_status q8_proj_fused_swiglu(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,

@@ -13,6 +13,7 @@
 
 // Device error codes written to the library's error word.
 #define Q8_DEVERR_TIMEOUT 1
+#define Q8_DEVERR_POSITION 2   // a KV-cache position outside the cache
 
 // A bounded wait gives up after this many nanoseconds of global time.
 #define Q8_WAIT_LIMIT_NS 2000000000ull

@@ -60,6 +60,13 @@ struct GemvParams {
     float* s_out;        // h + res written back (by CTA 0), or NULL
     const float* gain;
     float eps;
+    // KV-row epilogue (decode kernel only): columns [kv_col, kv_col + kv_dim)
+    // of row m also go to k_cache row pos[m], the next kv_dim to v_cache;
+    // caches [rows][n_pos][kv_dim].  k_cache NULL: none.
+    const int32_t* pos;
+    int64_t kv_col, kv_dim, n_pos;
+    float* k_cache;
+    float* v_cache;
 };
 
 // Chunks (16 bytes of K) each lane owns per slice, and consumer warps per

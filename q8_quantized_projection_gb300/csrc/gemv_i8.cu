@@ -21,6 +21,7 @@ cudaError_t launch_gemv_mode1(const GemvArgs& a, const LaunchCtx& ctx) {
 }
 
 cudaError_t launch_gemv_fused_mode1(const GemvArgs& a, const LaunchCtx& ctx) {
+    if (a.k_cache) return launch_gemv_row_t<1, 1, false, true, kProdPlain, true>(a, ctx);
     if (a.prod == kProdResidual) return launch_gemv_row_t<1, 1, false, true, kProdResidual>(a, ctx);
     if (a.prod == kProdSwiglu) return launch_gemv_row_t<1, 1, false, true, kProdSwiglu>(a, ctx);
     return launch_gemv_row_t<1, 1, false, true>(a, ctx);

@@ -253,6 +253,19 @@ __device__ __forceinline__ void load_x4(const float* x, const float* h, const fl
     }
 }
 
+// The KV-row epilogue: output column n of row m, when it falls in the K or V
+// slice, also goes to cache row s_pos[m] of that row's sequence (-1: none).
+__device__ __forceinline__ void kv_store(const GemvParams& p, const int* s_pos, int m, int64_t n,
+                                         float v) {
+    const int ps = s_pos[m];
+    if (ps < 0) return;
+    const int64_t d = n - p.kv_col;
+    if (d < 0 || d >= 2 * p.kv_dim) return;
+    float* cache = d < p.kv_dim ? p.k_cache : p.v_cache;
+    const int64_t dd = d < p.kv_dim ? d : d - p.kv_dim;
+    cache[(int64_t(m) * p.n_pos + ps) * p.kv_dim + dd] = v;
+}
+
 __device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v, long long i) {
     if (v > bv || (v == bv && i < bi)) {
         bv = v;
@@ -264,7 +277,8 @@ __device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v,
 // residual added before the norm) or kProdSwiglu (the SwiGLU of the fused
 // gate+up row h); each a separate instantiation, so the plain fused kernel
 // carries none of the others.
-template <int MODE, int R, bool ARGMAX, bool FUSE, int PROD = kProdPlain>
+// KV: the KV-row epilogue (the one-row fused decode launch only).
+template <int MODE, int R, bool ARGMAX, bool FUSE, int PROD = kProdPlain, bool KV = false>
 __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvParams p) {
     static_assert(!FUSE || R == 1, "fused producer: one row");
     static_assert(MODE != 0 || R == 1, "f32 mode: one row per launch");
@@ -289,6 +303,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     ArgmaxCand* cand = reinterpret_cast<ArgmaxCand*>(reinterpret_cast<unsigned char*>(psum) +
                                                      kRowPsumBytes);   // [NW][R]
     __shared__ unsigned int s_ticket;
+    __shared__ int s_pos[R];   // KV-row epilogue: each row's cache position
     __shared__ float2 s_pair[kProdWarps];
     __shared__ float s_rf;
 
@@ -378,6 +393,16 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
 
     const int rows = p.rows;
     const int64_t K = p.K, N = p.N, nb = K / Q8_QK;
+    if (KV && tid < rows) {
+        // positions belong to the previous kernel until griddepcontrol.wait;
+        // one outside the cache writes nothing and is reported
+        int ps = p.pos[tid];
+        if (ps < 0 || ps >= p.n_pos) {
+            atomicExch(p.err, Q8_DEVERR_POSITION);
+            ps = -1;
+        }
+        s_pos[tid] = ps;
+    }
     const signed char* act8 = reinterpret_cast<const signed char*>(p.act);
     const float* actf = reinterpret_cast<const float*>(p.act);
     const float* xdp = p.xd;
@@ -735,9 +760,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     if (!ARGMAX && !p.out_f64) {
                         // f32 output: the pair rounded once, then scaled by 2^(E-30)
                         const int sc = E - 30;   // in [-156, 98]
-                        if (p.y)
-                            reinterpret_cast<float*>(p.y)[n] =
-                                __fmul_rn(__fmul_rn(__fadd_rn(s.hi, s.lo), pow2i(sc >> 1)), pow2i(sc - (sc >> 1)));
+                        const float yv =
+                            __fmul_rn(__fmul_rn(__fadd_rn(s.hi, s.lo), pow2i(sc >> 1)), pow2i(sc - (sc >> 1)));
+                        if (p.y) reinterpret_cast<float*>(p.y)[n] = yv;
+                        if constexpr (KV) kv_store(p, s_pos, 0, n, yv);
                         continue;
                     }
                 } else {
@@ -753,6 +779,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     else
                         reinterpret_cast<float*>(p.y)[m * N + n] = float(val);
                 }
+                if constexpr (KV) kv_store(p, s_pos, m, n, float(val));
                 if constexpr (ARGMAX) argmax_keep(best_v[m], best_i[m], val, n);
             }
         }
@@ -807,9 +834,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     }
 }
 
-template <int MODE, int R, bool ARGMAX, bool FUSE = false, int PROD = kProdPlain>
+template <int MODE, int R, bool ARGMAX, bool FUSE = false, int PROD = kProdPlain, bool KV = false>
 cudaError_t launch_gemv_row_t(const GemvArgs& a, const LaunchCtx& ctx) {
-    auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD>;
+    auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD, KV>;
     constexpr size_t smem = row_smem_bytes<MODE, R, FUSE>();
     static bool configured = false;  // per process; one device per process
     if (!configured) {
@@ -838,6 +865,12 @@ cudaError_t launch_gemv_row_t(const GemvArgs& a, const LaunchCtx& ctx) {
     p.s_out = a.s_out;
     p.gain = a.gain;
     p.eps = a.eps;
+    p.pos = a.pos;
+    p.kv_col = a.kv_col;
+    p.kv_dim = a.kv_dim;
+    p.n_pos = a.n_pos;
+    p.k_cache = a.k_cache;
+    p.v_cache = a.v_cache;
 
     int grid = ctx.num_sms;
     if (grid > kMaxGrid) grid = kMaxGrid;

@@ -52,6 +52,11 @@ struct GemvArgs {
     float* s_out;        // h + res written back, or NULL
     const float* gain;
     float eps;
+    // KV-row epilogue (see GemvParams); k_cache NULL: none
+    const int32_t* pos;
+    int64_t kv_col, kv_dim, n_pos;
+    float* k_cache;
+    float* v_cache;
 };
 
 // Largest K the decode kernel quantises in its own shared memory.
@@ -69,6 +74,11 @@ cudaError_t launch_chunk_debug(int mode, const int8_t* q, int64_t N, int64_t K, 
 // chunk launch beats the decode kernel's groups of rows (one-word: groups of
 // 8, so 9 rows and more; two-word: groups of 4, so 5 and more).
 inline int64_t chunk_min_rows(int mode) { return mode == 2 ? 5 : 9; }
+
+// K/V slices of y [rows][N] into cache row pos[m] of each row's cache
+cudaError_t launch_kv_scatter(const float* y, int64_t rows, int64_t N, const int32_t* pos, int64_t kv_col,
+                              int64_t kv_dim, int64_t n_pos, float* k_cache, float* v_cache,
+                              const LaunchCtx& ctx);
 
 cudaError_t launch_debug_dots(int mode, const int8_t* q, const void* xq, int64_t N, int64_t K,
                               int64_t rows, int32_t* isum, const LaunchCtx& ctx);

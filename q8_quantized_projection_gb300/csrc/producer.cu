@@ -142,6 +142,44 @@ cudaError_t launch_act_quant(int mode, int prod, const float* h, const float* re
     return launch_aq_t<2, false>(p, ctx);
 }
 
+// -------------------------------------------------------- KV-row scatter
+
+// The KV-row epilogue for batches: row m's K/V slices of y [rows][N] into
+// cache row pos[m] of its sequence (caches [rows][n_pos][kv_dim]).  One CTA
+// per (row, 256 cache entries of K then V); a position outside the cache
+// writes nothing and sets the device error word.
+__global__ void kv_scatter_kernel(const float* y, int64_t N, const int32_t* pos, int64_t kv_col,
+                                  int64_t kv_dim, int64_t n_pos, float* k_cache, float* v_cache,
+                                  int* err) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t m = blockIdx.y;
+    const int ps = pos[m];
+    if (ps < 0 || ps >= n_pos) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicExch(err, Q8_DEVERR_POSITION);
+        return;
+    }
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;   // [0, 2*kv_dim)
+    if (i >= 2 * kv_dim) return;
+    const float v = y[m * N + kv_col + i];
+    float* cache = i < kv_dim ? k_cache : v_cache;
+    cache[(m * n_pos + ps) * kv_dim + (i < kv_dim ? i : i - kv_dim)] = v;
+}
+
+cudaError_t launch_kv_scatter(const float* y, int64_t rows, int64_t N, const int32_t* pos, int64_t kv_col,
+                              int64_t kv_dim, int64_t n_pos, float* k_cache, float* v_cache,
+                              const LaunchCtx& ctx) {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attrs[1];
+    cfg.gridDim = dim3(unsigned((2 * kv_dim + 255) / 256), unsigned(rows));
+    cfg.blockDim = dim3(256);
+    cfg.stream = ctx.stream;
+    cfg.numAttrs = pdl_attrs(ctx, attrs);
+    cfg.attrs = attrs;
+    return cudaLaunchKernelEx(&cfg, kv_scatter_kernel, y, N, pos, kv_col, kv_dim, n_pos, k_cache,
+                              v_cache, ctx.dev_err);
+}
+
 // ----------------------------------------------------------- debug block dots
 
 // isum[m][n][b] from the same 16-value dot helpers the GEMV kernels use.

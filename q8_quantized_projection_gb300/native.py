@@ -42,6 +42,8 @@ SIGNATURES = {
     "q8_proj_fused_residual": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, C.c_float,
                                       _vp, _int, _vp, _sz, _vp]),
     "q8_proj_fused_swiglu": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _i64, _vp, _int, _vp, _sz, _vp]),
+    "q8_proj_fused_kv": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _i64, _vp, C.c_float, _vp, _vp, _i64,
+                                _i64, _vp, _vp, _i64, _vp, _sz, _vp]),
     "head_argmax": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _sz,
                            _vp]),
     "head_argmax_workspace": (_sz, [_i64]),
@@ -188,6 +190,19 @@ def q8_proj_fused_swiglu(mode, q, s, gu, y, workspace, out_f64=False, stream=Non
                                        1 if out_f64 else 0, _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream)),
            "q8_proj_fused_swiglu")
+
+
+def q8_proj_fused_kv(mode, q, s, h, y, workspace, pos, kv_col, k_cache, v_cache, gain=None,
+                     eps=1e-5, stream=None):
+    """k_cache, v_cache: [rows, n_pos, kv_dim] float32; pos: int32 [rows] on the device."""
+    n, k = q.shape
+    rows = h.shape[0]
+    _, n_pos, kv_dim = k_cache.shape
+    _check(load().q8_proj_fused_kv(_mode(mode), _ptr(q), _ptr(s), n, k, _ptr(h), rows, _ptr(gain),
+                                   float(eps), _ptr(y), _ptr(pos), kv_col, kv_dim, _ptr(k_cache),
+                                   _ptr(v_cache), n_pos, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "q8_proj_fused_kv")
 
 
 def head_argmax_workspace(rows) -> int:

@@ -265,6 +265,58 @@ def test_fused_swiglu_matches_oracle_and_composition(mode, n, k, rows):
     assert np.array_equal(host(y).view(np.uint32), host(y2).view(np.uint32))
 
 
+# ------------------------------------------------------- KV-row epilogue
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("rows,pos", [(1, [3]), (1, [0]), (3, [0, 4, 2]), (9, [4, 0, 1, 2, 3, 4, 0, 1, 2])])
+def test_fused_kv_rows(mode, rows, pos):
+    # a QKV projection of N = 384 (q 256, K 64, V 64) into caches of 5 rows
+    n, k, kv_col, d, n_pos = 384, 1024, 256, 64, 5
+    rng = np.random.default_rng(100 + rows + pos[0])
+    q, s = synth.q8_weights(rng, n, k)
+    h = synth.activations(rng, rows, k)
+    g = synth.gain(rng, k)
+    y_o, norm = orc.project(mode, q, s, orc.quantize(mode, orc.rmsnorm(h, g, 1e-5)[0]))
+    qd, sd = upload_weights(q, s)
+    t = torch()
+    ws = t.empty(native.q8_proj_fused_workspace(mode, rows, k), dtype=t.uint8, device="cuda")
+    y = t.empty((rows, n), dtype=t.float32, device="cuda")
+    kc = t.full((rows, n_pos, d), float("nan"), dtype=t.float32, device="cuda")
+    vc = t.full((rows, n_pos, d), float("nan"), dtype=t.float32, device="cuda")
+    posd = t.tensor(pos, dtype=t.int32, device="cuda")
+    native.q8_proj_fused_kv(mode, qd, sd, dev(h), y, ws, posd, kv_col, kc, vc, gain=dev(g), eps=1e-5)
+    yh = host(y)
+    check_close(mode, yh, y_o, norm, what=f"fused kv {mode}")
+    kc_o = np.full((rows, n_pos, d), np.nan, np.float32)
+    vc_o = np.full((rows, n_pos, d), np.nan, np.float32)
+    assert orc.kv_write(yh, pos, kv_col, d, kc_o, vc_o) == 0
+    assert np.array_equal(host(kc).view(np.uint32), kc_o.view(np.uint32))
+    assert np.array_equal(host(vc).view(np.uint32), vc_o.view(np.uint32))
+    # y is what the plain fused call computes
+    y2 = t.empty_like(y)
+    native.q8_proj_fused(mode, qd, sd, dev(h), y2, ws, gain=dev(g), eps=1e-5)
+    assert np.array_equal(yh.view(np.uint32), host(y2).view(np.uint32))
+
+
+@pytest.mark.parametrize("rows", [1, 3])
+def test_fused_kv_position_out_of_range(rows):
+    n, k, kv_col, d, n_pos = 256, 512, 128, 32, 4
+    rng = np.random.default_rng(7 + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    h = synth.activations(rng, rows, k)
+    qd, sd = upload_weights(q, s)
+    t = torch()
+    ws = t.empty(native.q8_proj_fused_workspace("i8", rows, k), dtype=t.uint8, device="cuda")
+    y = t.empty((rows, n), dtype=t.float32, device="cuda")
+    kc = t.full((rows, n_pos, d), 7.0, dtype=t.float32, device="cuda")
+    vc = t.full((rows, n_pos, d), 7.0, dtype=t.float32, device="cuda")
+    bad = [n_pos] + [-1] * (rows - 1)
+    native.q8_proj_fused_kv("i8", qd, sd, dev(h), y, ws, t.tensor(bad, dtype=t.int32, device="cuda"),
+                            kv_col, kc, vc)
+    assert native.q8_device_error() == 2          # reported, and cleared by the read
+    assert np.all(host(kc) == 7.0) and np.all(host(vc) == 7.0)
+
+
 def test_residual_argument_errors():
     t = torch()
     k, n = 64, 8
