@@ -48,6 +48,7 @@ __host__ __device__ constexpr int row_ring() {
     return MODE == 0 ? kRowRingF32 : kRowRing;
 }
 constexpr int kRowPsumBytes = 16384;   // part sums of one super-block of rows
+constexpr int kRowEpBytes = 1024;      // f32 mode: the parts' binades, beside the part sums
 
 // 16-byte chunks a lane owns per part: the activation registers (R rows, one
 // or two planes, or 17 words of fixed point in f32 mode) stay within ~32.
@@ -83,7 +84,7 @@ constexpr size_t kFusedActBytes = 2 * 16384 + (16384 / 32) * 4;
 template <int MODE, int R, bool FUSE>
 __host__ __device__ constexpr size_t row_smem_bytes() {
     return size_t(row_ring<MODE>()) + size_t(row_ring<MODE>()) / 16 + 2 * kGemvMaxStages * sizeof(uint64_t) +
-           kRowPsumBytes + size_t(kRowWarps) * R * sizeof(ArgmaxCand) + 64 +
+           kRowPsumBytes + (MODE == 0 ? kRowEpBytes : 0) + size_t(kRowWarps) * R * sizeof(ArgmaxCand) + 64 +
            (FUSE && MODE != 0 ? kFusedActBytes : 0);
 }
 
@@ -133,8 +134,8 @@ __host__ __device__ inline RowGeo row_geo(int64_t N, int64_t K, int G, int c, in
     g.r1 = N * (c + 1) / G;
     const int64_t per_row = int64_t(g.nks) * g.nprr * psum_row_unit;
     const int64_t ep_bytes = (int64_t(g.nks) * g.nprr * part_extra + 15) & ~int64_t(15);
-    g.ep_off = int(kRowPsumBytes - ep_bytes);
-    g.sbrows = ep_bytes >= kRowPsumBytes ? 0 : (((kRowPsumBytes - ep_bytes) / per_row) / g.RS) * g.RS;
+    g.ep_off = kRowPsumBytes;   // in an area of kRowEpBytes after the part sums
+    g.sbrows = ep_bytes > kRowEpBytes ? 0 : ((kRowPsumBytes / per_row) / g.RS) * g.RS;
     return g;
 }
 
@@ -301,7 +302,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     uint64_t* empty = full + kGemvMaxStages;
     A* psum = reinterpret_cast<A*>(empty + kGemvMaxStages);   // [sbrows][nks][nprr][R]
     ArgmaxCand* cand = reinterpret_cast<ArgmaxCand*>(reinterpret_cast<unsigned char*>(psum) +
-                                                     kRowPsumBytes);   // [NW][R]
+                                                     kRowPsumBytes +
+                                                     (MODE == 0 ? kRowEpBytes : 0));   // [NW][R]
     __shared__ unsigned int s_ticket;
     __shared__ int s_pos[R];   // KV-row epilogue: each row's cache position
     __shared__ float2 s_pair[kProdWarps];
@@ -451,6 +453,75 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     bool validb = false;
     int cur_sl = -1;
     int ncc = 0, rag = 0;   // full 512-byte chunk columns of this part, lanes of the ragged one
+    if constexpr (kBL) {
+        if (g.nks == 1 && K <= 4096) {
+            // Rows of one slice and up to 4096 values: each 32-value block is
+            // converted once, by the first warp of its part (one warp a part),
+            // into the part-sum area (not in use yet), and every warp reads its
+            // block from there: a quarter of the conversions and of the
+            // activation's L2 traffic.  Block b's 32 words sit at b*128 bytes,
+            // 16-byte word group i in slot i ^ (b & 7) (no bank conflicts).
+            unsigned char* planes = reinterpret_cast<unsigned char*>(psum);
+            short* pe = reinterpret_cast<short*>(reinterpret_cast<unsigned char*>(psum) + kRowPsumBytes +
+                                                 kRowEpBytes / 2);   // block binades [K/32]
+            const int bpp = g.PB >> 5;                              // blocks a part
+            if (warp < g.npr) {
+                // warp w < npr is the first warp of part w (item w: row 0, part w)
+                const int pbytes = int(min64(max64(K - int64_t(warp) * g.PB, 0), g.PB));
+                const bool valid = lane < (pbytes >> 5);
+                FixChunk32 f = FixChunk32{};
+                f.e = -126;
+                if (valid) {
+                    const int64_t k = int64_t(warp) * g.PB + int64_t(lane) * 32;
+                    float xs[32];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        float xv[4];
+                        load_x4<FUSE, PROD>(actf + k + 4 * u, p.h + k + 4 * u, RES ? res + k + 4 * u : nullptr,
+                                            p.gain ? p.gain + k + 4 * u : nullptr, rf, xv, K);
+                        xs[4 * u + 0] = xv[0];
+                        xs[4 * u + 1] = xv[1];
+                        xs[4 * u + 2] = xv[2];
+                        xs[4 * u + 3] = xv[3];
+                    }
+                    f = fix_chunk32(xs);
+                }
+                const int ep = __reduce_max_sync(0xffffffffu, f.e);
+                if (lane == 0 && warp < g.nprr) s_ep[warp] = short(ep);
+                if (valid) {
+                    const int blk = warp * bpp + lane;
+                    const uint32_t base = smem_u32(planes) + uint32_t(blk) * 128u;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        sts128(base + uint32_t(((i ^ (blk & 7)) << 4)), uint32_t(f.p[i >> 1][4 * (i & 1) + 0]),
+                               uint32_t(f.p[i >> 1][4 * (i & 1) + 1]), uint32_t(f.p[i >> 1][4 * (i & 1) + 2]),
+                               uint32_t(f.p[i >> 1][4 * (i & 1) + 3]));
+                    pe[blk] = short(f.e);
+                }
+            }
+            consumer_bar<NT>();
+            cur_sl = 0;
+            const int pbytes = int(min64(max64(K - int64_t(pw) * g.PB, 0), g.PB));
+            validb = lane < (pbytes >> 5);
+            fxb = FixChunk32{};
+            fxb.e = -126;
+            if (validb) {
+                const int blk = pw * bpp + lane;
+                const uint32_t base = smem_u32(planes) + uint32_t(blk) * 128u;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int4 v = lds128(base + uint32_t(((i ^ (blk & 7)) << 4)));
+                    fxb.p[i >> 1][4 * (i & 1) + 0] = v.x;
+                    fxb.p[i >> 1][4 * (i & 1) + 1] = v.y;
+                    fxb.p[i >> 1][4 * (i & 1) + 2] = v.z;
+                    fxb.p[i >> 1][4 * (i & 1) + 3] = v.w;
+                }
+                fxb.e = pe[blk];
+            }
+            p2sb = validb ? ldexpf(1.0f, fxb.e - s_ep[pw]) : 0.0f;
+            consumer_bar<NT>();   // the area holds part sums from here on
+        }
+    }
 
     const uint32_t wring_a = smem_u32(wring), sring_a = smem_u32(sring);
     bool ok = true;
