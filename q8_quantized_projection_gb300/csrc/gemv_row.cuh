@@ -413,7 +413,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     if constexpr (FUSE && MODE == 0) {
         // f32: the consumers form x themselves (no shared-memory activation:
         // the f32 kernel allocates none); with the norm only rf is computed here
-        if constexpr (NORM) rf = row_rms_scale(p.h, res, s_out, K, p.eps, tid, 1, s_pair, &s_rf);
+        // rows of one slice and K <= 4096 keep the input in the part-sum area
+        // (not in use yet) for the block conversion below
+        float* const stage = (g.nks == 1 && K <= 4096) ? reinterpret_cast<float*>(psum) : nullptr;
+        if constexpr (NORM) rf = row_rms_scale(p.h, res, s_out, K, p.eps, tid, 1, s_pair, &s_rf, stage);
     } else if constexpr (FUSE) {
         static_assert(MODE != 0, "the shared-memory activation exists for the int8 modes only");
         // The producer, fused: RMSNorm -> quant of the one activation row into
@@ -474,15 +477,41 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 if (valid) {
                     const int64_t k = int64_t(warp) * g.PB + int64_t(lane) * 32;
                     float xs[32];
+                    if constexpr (FUSE && NORM) {
+                        // the RMS pass kept the input (h, or h + r) in this very
+                        // block of the area: x = (s*rf)*g, then the planes in place
+                        const float* sp = reinterpret_cast<const float*>(planes) + k;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        float xv[4];
-                        load_x4<FUSE, PROD>(actf + k + 4 * u, p.h + k + 4 * u, RES ? res + k + 4 * u : nullptr,
-                                            p.gain ? p.gain + k + 4 * u : nullptr, rf, xv, K);
-                        xs[4 * u + 0] = xv[0];
-                        xs[4 * u + 1] = xv[1];
-                        xs[4 * u + 2] = xv[2];
-                        xs[4 * u + 3] = xv[3];
+                        for (int u = 0; u < 8; ++u) {
+                            const float4 s4 = *reinterpret_cast<const float4*>(sp + 4 * u);
+                            float gg[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+                            if (p.gain) {
+                                const int4 g4 = ldg_nc_v4(p.gain + k + 4 * u);
+                                gg[0] = __int_as_float(g4.x);
+                                gg[1] = __int_as_float(g4.y);
+                                gg[2] = __int_as_float(g4.z);
+                                gg[3] = __int_as_float(g4.w);
+                            }
+                            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float v = __fmul_rn(sv[e], rf);
+                                if (p.gain) v = __fmul_rn(v, gg[e]);
+                                xs[4 * u + e] = v;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            float xv[4];
+                            load_x4<FUSE, PROD>(actf + k + 4 * u, p.h + k + 4 * u,
+                                                RES ? res + k + 4 * u : nullptr,
+                                                p.gain ? p.gain + k + 4 * u : nullptr, rf, xv, K);
+                            xs[4 * u + 0] = xv[0];
+                            xs[4 * u + 1] = xv[1];
+                            xs[4 * u + 2] = xv[2];
+                            xs[4 * u + 3] = xv[3];
+                        }
                     }
                     f = fix_chunk32(xs);
                 }

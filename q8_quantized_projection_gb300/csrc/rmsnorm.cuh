@@ -274,13 +274,15 @@ __device__ __forceinline__ float4 load_input4(const float* h, const float* r, fl
 // rf alone (the f32 mode's fused producer, whose consumers form x = (h*rf)*g
 // themselves): the same per-thread order of squares as row_produce, so the
 // same rf.
-// With a residual r the input is s = h + r, stored to s_out when it is set.
+// With a residual r the input is s = h + r, stored to s_out when it is set;
+// with `stage` (shared memory, K floats) the input is also kept there.
 __device__ __forceinline__ float row_rms_scale(const float* h, const float* r, float* s_out, int64_t K,
                                                float eps, int tid, int bar, float2* s_pair,
-                                               float* s_rf) {
+                                               float* s_rf, float* stage = nullptr) {
     float sh = 0.0f, sl = 0.0f;
     for (int64_t gi = tid; gi < (K >> 2); gi += kProdThreads) {
         const float4 v = load_input4(h, r, s_out, gi);
+        if (stage) *reinterpret_cast<float4*>(stage + 4 * gi) = v;
         pair_add_sq(sh, sl, v.x);
         pair_add_sq(sh, sl, v.y);
         pair_add_sq(sh, sl, v.z);
