@@ -15,7 +15,8 @@
 //  * A row-slice is cut into npr parts of PB = 512*CPL bytes (npr a power of
 //    two; trailing parts may be short or empty), so a stage holds RS*npr
 //    (row, part) pairs, served as items = RS*npr/rpw items of rpw rows of one
-//    part (rpw = 4 in f32 mode, else 1), items | 16.  Consumer warp w always
+//    part (rpw = 4 in f32 mode; 2 for one-word 4 and 8 rows and two-word 2
+//    and 4 rows; else 1), items | 16.  Consumer warp w always
 //    serves item w % items, in the stages whose ring slot is congruent to
 //    w / items modulo 16/items (so every phase of a slot's barriers is seen by
 //    the same warps): its part never changes, so its lanes hold that part's
@@ -27,8 +28,15 @@
 //    meet once and add every row's parts in slice and part order, so the
 //    result is bitwise reproducible.  Nothing synchronises consumer warps
 //    while weights stream.
-//  * Numerics per mode are those of gemv.cuh (exact int32 block dots for the
-//    int8 modes; exact fixed-point chunk dots and f32 pairs for f32).
+//  * Numerics: exact int32 block dots for the int8 modes; for f32 (one row a
+//    launch) a lane owns a whole 32-value block: its 31-bit fixed-point copy
+//    relative to the block's binade, an exact block dot, one f32-pair scaling,
+//    each part's sums relative to the part's largest binade (rescaled to the
+//    row's in the combine).
+//  * Fused producer (FUSE): the consumers run RMSNorm -> quant (or, by PROD,
+//    the residual added before the norm, or the SwiGLU of a gate+up row) in
+//    the prologue while the producer warp streams weights; KV adds the
+//    KV-cache-row epilogue to the combine.
 #pragma once
 
 #include "gemv.cuh"
