@@ -90,7 +90,7 @@ def test_block_dots_bit_exact(mode, n, k, rows):
 # ------------------------------------------------------------- projection
 
 SHAPES = [(1, 32), (3, 64), (37, 96), (1000, 1024), (301, 4096), (77, 4128), (64, 14336),
-          (5, 3104)]
+          (5, 3104), (33, 11008), (19, 5120)]
 
 
 @pytest.mark.parametrize("mode", MODES)
