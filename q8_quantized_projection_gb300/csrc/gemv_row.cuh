@@ -662,7 +662,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
             const uint32_t sbase = sring_a + uint32_t(slot * (g.stage_bytes / 16) + jrow * (kl >> 4));
             constexpr int RPW = row_rpw<MODE, R>();
             DF part2[RPW];   // f32 mode: this warp's rows of the stage
-            bool have2[RPW];
+            unsigned have_rows = 0;   // f32 mode: bit i, row i of the item holds data
             // int8 modes, two rows of the part per stage (kMR)
             constexpr bool kMR = (MODE != 0 && RPW > 1);
             float pm[kMR ? RPW : 1][kMR ? R : 1];
@@ -711,35 +711,46 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
             if constexpr (kBL) {
                 // each row's exact dot right after its weights are in
                 // registers (one row's weights live at a time); the slot goes
-                // back after the last row, then the f32-pair scalings
-                const int rstep = g.RS / g.rpw;
+                // back after the last row, then the f32-pair scalings.  Every
+                // f32 one-row geometry serves four rows a warp (RS >= 4), rows
+                // RS/4 apart.
+                const int rstep = g.RS >> 2;
                 int2 vb[RPW];
-                float swb[RPW];
+                uint16_t swh[RPW];
+                unsigned rows_in = 0;   // bit i: the item's row i holds data
 #pragma unroll
                 for (int i = 0; i < RPW; ++i) {
                     const int rr = jrow + i * rstep;   // row within the stage
-                    have2[i] = have && i < g.rpw && rbi * g.RS + rr < sbn;
+                    const bool hr = have && rbi * g.RS + rr < sbn;
+                    rows_in |= unsigned(hr) << i;
                     vb[i] = make_int2(0, 0);
-                    swb[i] = 0.0f;
-                    if (have2[i] && validb) {
-                        const uint32_t wb = wring_a + uint32_t(slot * g.stage_bytes + rr * kl + pw * g.PB) +
-                                            uint32_t(lane * 32);
-                        const int4 w0 = lds128(wb);
-                        const int4 w1 = lds128(wb + 16);
-                        const uint32_t sb = sring_a + uint32_t(slot * (g.stage_bytes / 16) + rr * (kl >> 4));
-                        swb[i] = scale_bulk
-                                     ? half_bits_to_float(lds16(sb + uint32_t((blk0 + lane) * 2)))
-                                     : half_bits_to_float(__ldg(p.s + (sb0 + rbi * g.RS + rr) * nb + (ks >> 5) + blk0 + lane));
+                    swh[i] = 0;
+                    if (hr && validb) {
+                        // the lane's block; its scale sits at a sixteenth of the
+                        // offset within the scale ring
+                        const uint32_t o = uint32_t(slot * g.stage_bytes + rr * kl + pw * g.PB + lane * 32);
+                        const int4 w0 = lds128(wring_a + o);
+                        const int4 w1 = lds128(wring_a + o + 16u);
+                        if (scale_bulk) swh[i] = lds16(sring_a + (o >> 4));
                         vb[i] = fix_dot32_split(w0, w1, fxb);
                     }
                 }
                 __syncwarp();
                 if (lane == 0 && ok) mbar_arrive(&empty[slot]);
+                if (!scale_bulk && validb) {
+                    // scales not staged with the weights (K not a multiple of 256)
+#pragma unroll
+                    for (int i = 0; i < RPW; ++i)
+                        if ((rows_in >> i) & 1u)
+                            swh[i] = __ldg(p.s + (sb0 + rbi * g.RS + jrow + i * rstep) * nb + (ks >> 5) + blk0 + lane);
+                }
 #pragma unroll
                 for (int i = 0; i < RPW; ++i) {
                     part2[i] = DF{0.0f, 0.0f};
-                    if (have2[i] && validb) part2[i] = scaled_pair_split(__fmul_rn(swb[i], p2sb), vb[i]);
+                    if (((rows_in >> i) & 1u) && validb)
+                        part2[i] = scaled_pair_split(__fmul_rn(half_bits_to_float(swh[i]), p2sb), vb[i]);
                 }
+                have_rows = rows_in;
             }
 #pragma unroll
             for (int c0 = 0; c0 < ((kBL || kMR) ? 0 : CPL); c0 += GC) {
@@ -797,12 +808,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 // one butterfly for the warp's rows: lanes [i*32/RPW, ...) end with row i
                 const DF tot = warp_sum_rows<RPW>(part2, lane);
                 const int i = lane / (32 / RPW);
-                bool hv = false;
-#pragma unroll
-                for (int k = 0; k < RPW; ++k)
-                    if (k == i) hv = have2[k];
-                if ((lane & (32 / RPW - 1)) == 0 && hv) {
-                    const int rsb = rbi * g.RS + jrow + i * (g.RS / g.rpw);
+                if ((lane & (32 / RPW - 1)) == 0 && ((have_rows >> i) & 1u)) {
+                    const int rsb = rbi * g.RS + jrow + i * (g.RS >> 2);
                     psum[(size_t(rsb) * g.nks + sl) * g.nprr + pw] = reinterpret_cast<const A&>(tot);
                 }
             } else if constexpr (kMR) {
