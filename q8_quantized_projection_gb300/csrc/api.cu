@@ -30,7 +30,6 @@ struct DevInfo {
     int num_sms = 0;
     int* dev_err = nullptr;
 };
-constexpr int kMaxDevices = 64;
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
@@ -55,6 +54,7 @@ q8_status make_ctx(void* stream, LaunchCtx& ctx) {
         d.dev_err = static_cast<int*>(p);
         d.ready = true;
     }
+    ctx.dev = dev;
     ctx.stream = static_cast<cudaStream_t>(stream);
     ctx.pdl = g_pdl != 0;
     ctx.num_sms = d.num_sms;

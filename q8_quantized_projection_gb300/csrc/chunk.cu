@@ -657,13 +657,9 @@ static cudaError_t launch_chunk_t(const int8_t* q, const uint16_t* s, int64_t N,
                                   int32_t* isum, const LaunchCtx& ctx) {
     using C = CkCfg<MODE, TT>;
     auto kern = chunk_kernel<MODE, TT, DEBUG>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(C::kSmem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<bool> configured[kMaxDevices];
+    if (const cudaError_t e = set_smem_once(kern, size_t(C::kSmem), ctx.dev, configured); e != cudaSuccess)
+        return e;
     alignas(64) CUtensorMap tw, txh, txl, ts, txd;
     const int64_t nb = K / Q8_QK;
     const int8_t* xh = reinterpret_cast<const int8_t*>(xq);

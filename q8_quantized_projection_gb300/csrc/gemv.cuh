@@ -767,13 +767,9 @@ template <int MODE, int R, bool ARGMAX>
 cudaError_t launch_gemv_t(const GemvArgs& a, const LaunchCtx& ctx) {
     auto kern = gemv_kernel<MODE, R, ARGMAX>;
     constexpr size_t smem = gemv_smem_bytes<MODE, R>();
-    static bool configured = false;  // per process; one device per process
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(smem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<bool> configured[kMaxDevices];
+    if (const cudaError_t e = set_smem_once(kern, size_t(smem), ctx.dev, configured); e != cudaSuccess)
+        return e;
     GemvParams p{};
     p.q = a.q;
     p.s = a.s;

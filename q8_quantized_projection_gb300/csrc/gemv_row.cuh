@@ -153,6 +153,9 @@ inline bool row_kernel_fits(int64_t K) {
     using A = typename AccT<MODE>::T;
     const RowGeo g = row_geo(1, K, 1, 0, row_cpl<MODE, R>(), int(R * sizeof(A)), row_rpw<MODE, R>(),
                              row_ring<MODE>(), row_part_extra<MODE, R>());
+    // the f32 one-row items take four rows RS/4 apart (rows a stage >= 4, which
+    // every K up to 2^20 gives: slices of at most 8192 values leave room for 4)
+    if (MODE == 0 && R == 1 && (g.rpw != 4 || g.RS % 4 != 0)) return false;
     return g.sbrows >= g.RS;
 }
 
@@ -953,13 +956,10 @@ template <int MODE, int R, bool ARGMAX, bool FUSE = false, int PROD = kProdPlain
 cudaError_t launch_gemv_row_t(const GemvArgs& a, const LaunchCtx& ctx) {
     auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD, KV>;
     constexpr size_t smem = row_smem_bytes<MODE, R, FUSE>();
-    static bool configured = false;  // per process; one device per process
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(smem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<bool> configured[kMaxDevices];
+    if (const cudaError_t e = set_smem_once(kern, size_t(smem), ctx.dev, configured); e != cudaSuccess)
+        return e;
+    if (!row_kernel_fits<MODE, R>(a.K)) return cudaErrorInvalidValue;   // callers check first
     GemvParams p{};
     p.q = a.q;
     p.s = a.s;

@@ -6,9 +6,26 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace q8 {
 
+constexpr int kMaxDevices = 64;   // devices one process may use
+
+// Raises a kernel's dynamic shared-memory limit once per device: the attribute
+// belongs to that device's context.  `done` is the kernel's own flag array;
+// two threads that race here both set the same value.
+template <typename F>
+inline cudaError_t set_smem_once(F kern, size_t smem, int dev, std::atomic<bool>* done) {
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+    return e;
+}
+
 struct LaunchCtx {
+    int dev;         // current device, 0 <= dev < kMaxDevices
     cudaStream_t stream;
     bool pdl;        // programmatic dependent launch
     int num_sms;     // SMs of the current device
