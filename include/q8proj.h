@@ -47,6 +47,10 @@
  *     N, rows >= 1.  Violations return Q8_ERR_ALIGN / Q8_ERR_SHAPE.
  *   - A failed launch returns Q8_ERR_CUDA; q8_last_cuda_error() gives the
  *     CUDA error number.  The library never exits, aborts or traps.
+ *   - Each call runs on the calling thread's current device (cudaSetDevice).
+ *     One process may use several devices (up to 64) and call from several
+ *     threads: the per-device state (SM count, device error word, kernel
+ *     attributes) is set up once per device under a lock or atomically.
  *   - Device-side waits are bounded.  A wait that runs out records a code
  *     that q8_device_error() reports; the kernel then returns early and its
  *     outputs are undefined.
