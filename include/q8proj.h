@@ -285,6 +285,22 @@ size_t head_argmax_noalloc_scratch_bytes(void);
 q8_status q8_debug_block_dots(int mode, const int8_t* q, const void* xq, int64_t N, int64_t K,
                               int64_t rows, int32_t* isum, int path, void* stream);
 
+/*
+ * Debug, host only (no device work, no CUDA call): the stage geometry the
+ * decode kernel (rows <= 8 one-word, <= 4 two-word, 1 f32) uses for CTA `cta`
+ * of a grid of `grid` CTAs (the library launches min(SM count, N) of them).
+ * out (host, 21 int64) receives: R (activation rows the kernel is built for),
+ * KS (bytes of K a slice), nks (slices a row), PB (bytes a part), npr (parts a
+ * slice, a power of two), nprr (parts holding data), RS (rows a stage), rpw
+ * (rows a warp serves per stage), items (RS*npr/rpw), stride (warp groups,
+ * 16/items), stage_bytes, nstages, r0, r1 (the CTA's rows [r0, r1)), sbrows
+ * (rows a super-block), ep_off, ring bytes, part-sum bytes, part-sum bytes a
+ * row-part, CPL (16-byte chunks a lane), consumer warps.  Returns
+ * Q8_ERR_UNSUPPORTED when the projection would use its slice-major kernel.
+ */
+q8_status q8_debug_row_geometry(int mode, int64_t rows, int64_t N, int64_t K, int grid, int cta,
+                                int64_t* out);
+
 #ifdef __cplusplus
 }
 #endif

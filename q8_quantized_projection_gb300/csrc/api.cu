@@ -177,7 +177,7 @@ const char* q8_status_str(int status) {
     }
 }
 
-int q8_version(void) { return 103; }
+int q8_version(void) { return 104; }
 
 int q8_last_cuda_error(void) { return t_last_cuda; }
 

@@ -48,6 +48,7 @@ SIGNATURES = {
                            _vp]),
     "head_argmax_workspace": (_sz, [_i64]),
     "q8_debug_block_dots": (_int, [_int, _vp, _vp, _i64, _i64, _i64, _vp, _int, _vp]),
+    "q8_debug_row_geometry": (_int, [_int, _i64, _i64, _i64, _int, _int, _vp]),
     "head_argmax_noalloc": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp,
                                    _vp]),
     "head_argmax_noalloc_scratch_bytes": (_sz, []),
@@ -229,6 +230,23 @@ def q8_debug_block_dots(mode, q, xq, rows, isum, path=0, stream=None):
     n, k = q.shape
     _check(load().q8_debug_block_dots(_mode(mode), _ptr(q), _ptr(xq), n, k, rows, _ptr(isum),
                                       int(path), _stream(stream)), "q8_debug_block_dots")
+
+
+ROW_GEOMETRY_FIELDS = ("R", "KS", "nks", "PB", "npr", "nprr", "RS", "rpw", "items", "stride",
+                       "stage_bytes", "nstages", "r0", "r1", "sbrows", "ep_off", "ring_bytes",
+                       "psum_bytes", "psum_row_unit", "cpl", "warps")
+
+
+def q8_debug_row_geometry(mode, rows, n, k, grid, cta):
+    """The decode kernel's stage geometry for one CTA (host only), as a dict;
+    None when the projection would run its slice-major kernel instead."""
+    out = (C.c_int64 * len(ROW_GEOMETRY_FIELDS))()
+    st = load().q8_debug_row_geometry(_mode(mode), int(rows), int(n), int(k), int(grid), int(cta),
+                                      C.cast(out, C.c_void_p))
+    if st == 6:   # Q8_ERR_UNSUPPORTED
+        return None
+    _check(st, "q8_debug_row_geometry")
+    return dict(zip(ROW_GEOMETRY_FIELDS, list(out)))
 
 
 # ------------------------------------------------------------ buffer helpers
