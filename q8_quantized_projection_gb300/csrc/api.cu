@@ -1,5 +1,6 @@
 // api.cu -- the C ABI of libq8proj (declared in include/q8proj.h): argument
 // validation on the host, then launches of the kernels on the caller's stream.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -23,7 +24,7 @@ __device__ int g_q8_dev_err;
 namespace {
 
 thread_local int t_last_cuda = 0;
-int g_pdl = 1;
+std::atomic<int> g_pdl{1};   // q8_set_pdl may race with launches on other threads
 
 struct DevInfo {
     bool ready = false;
@@ -56,7 +57,7 @@ q8_status make_ctx(void* stream, LaunchCtx& ctx) {
     }
     ctx.dev = dev;
     ctx.stream = static_cast<cudaStream_t>(stream);
-    ctx.pdl = g_pdl != 0;
+    ctx.pdl = g_pdl.load(std::memory_order_relaxed) != 0;
     ctx.num_sms = d.num_sms;
     ctx.dev_err = d.dev_err;
     return Q8_OK;
@@ -181,7 +182,7 @@ int q8_version(void) { return 104; }
 
 int q8_last_cuda_error(void) { return t_last_cuda; }
 
-void q8_set_pdl(int enable) { g_pdl = enable ? 1 : 0; }
+void q8_set_pdl(int enable) { g_pdl.store(enable ? 1 : 0, std::memory_order_relaxed); }
 
 q8_status q8_device_error(int32_t* code, void* stream) {
     if (!code) return Q8_ERR_ARG;
