@@ -343,10 +343,12 @@ struct Geo {
     int nstages;
     int64_t r0, r1; // CTA rows
     int64_t sbrows; // rows per super-block (multiple of RS)
+    bool sl_inner = false;   // row block, then slice (the slices of a row block back to back)
 };
 
 // Walks the stages in the order producer and consumers share: super-block,
-// then slice, then row block.  Advancing never divides.
+// then slice, then row block (or with sl_inner row block, then slice).
+// Advancing never divides.
 struct StageIter {
     int64_t sb0, sb_end, rb, ks;
     int sl, kl, slot;
@@ -367,8 +369,21 @@ __device__ __forceinline__ void stage_init(const Geo& g, StageIter& it) {
 }
 
 __device__ __forceinline__ void stage_next(const Geo& g, StageIter& it) {
-    it.rb += g.RS;
-    if (it.rb >= it.sb_end) {
+    if (g.sl_inner) {
+        it.ks += it.kl;
+        if (++it.sl == g.nks) {
+            it.sl = 0;
+            it.ks = 0;
+            it.rb += g.RS;
+            if (it.rb >= it.sb_end) {
+                it.sb0 += g.sbrows;
+                it.done = it.sb0 >= g.r1;
+                it.sb_end = min64(g.r1, it.sb0 + g.sbrows);
+                it.rb = it.sb0;
+            }
+        }
+        it.kl = int(min64(g.slb, g.K - it.ks));
+    } else if ((it.rb += g.RS) >= it.sb_end) {
         it.ks += it.kl;
         ++it.sl;
         if (it.sl == g.nks) {

@@ -159,6 +159,16 @@ inline bool row_kernel_fits(int64_t K) {
     return g.sbrows >= g.RS;
 }
 
+// Whether the f32 one-row kernel runs K's stages row block, then slice: rows
+// cut into slices whose count divides the warp groups, which divide the ring,
+// so that each warp group's ring slots always carry the same slice and a warp
+// converts its activation block once instead of at every slice change.
+inline bool row_slices_inner(int64_t K) {
+    const RowGeo g = row_geo(1, K, 1, 0, row_cpl<0, 1>(), int(sizeof(DF)), row_rpw<0, 1>(),
+                             row_ring<0>(), row_part_extra<0, 1>());
+    return g.nks > 1 && g.stride % g.nks == 0 && g.nstages % g.stride == 0;
+}
+
 // Sums each of R per-lane values over the warp with a butterfly that halves
 // the rows at every exchange (log2(R) exchanges of R/2, R/4, ... values, then
 // a plain reduction over the 32/R lanes left): lanes [r*32/R, (r+1)*32/R)
@@ -290,7 +300,11 @@ __device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v,
 // gate+up row h); each a separate instantiation, so the plain fused kernel
 // carries none of the others.
 // KV: the KV-row epilogue (the one-row fused decode launch only).
-template <int MODE, int R, bool ARGMAX, bool FUSE, int PROD = kProdPlain, bool KV = false>
+// SLI: stages run row block, then slice (the unfused f32 one-row kernel, rows
+// cut into slices whose count divides the warp groups, which divide the ring:
+// row_slices_inner).
+template <int MODE, int R, bool ARGMAX, bool FUSE, int PROD = kProdPlain, bool KV = false,
+          bool SLI = false>
 __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvParams p) {
     static_assert(!FUSE || R == 1, "fused producer: one row");
     static_assert(MODE != 0 || R == 1, "f32 mode: one row per launch");
@@ -329,6 +343,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     // binade, one weight scale, one exact dot and one f32-pair scaling), and
     // each part's sums are relative to the part's own largest binade
     constexpr bool kBL = (MODE == 0 && R == 1 && CPL == 2);
+    static_assert(!SLI || kBL, "the slice-inner order serves the f32 one-row kernel");
     short* s_ep = reinterpret_cast<short*>(reinterpret_cast<unsigned char*>(psum) + g.ep_off);
 
     if (tid == 0) {
@@ -357,6 +372,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
             sg.r0 = g.r0;
             sg.r1 = g.r1;
             sg.sbrows = g.sbrows;
+            sg.sl_inner = SLI;
             const uint64_t policy = policy_evict_first();
             const unsigned char* qsrc = reinterpret_cast<const unsigned char*>(p.q);
             const unsigned char* ssrc = reinterpret_cast<const unsigned char*>(p.s);
@@ -577,7 +593,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
             // a ring slot is always served by the same warps, so each of them
             // sees every phase of the slot's barriers
             if ((slot & (g.stride - 1)) != s_first) {
-                if (++rbi == nrb) {
+                if constexpr (SLI) {
+                    if (++sl == g.nks) {
+                        sl = 0;
+                        ++rbi;
+                    }
+                } else if (++rbi == nrb) {
                     rbi = 0;
                     ++sl;
                 }
@@ -841,7 +862,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     if ((lane & (32 / R - 1)) == 0) ps[lane / (32 / R)] = tot;
                 }
             }
-            if (++rbi == nrb) {
+            if constexpr (SLI) {
+                if (++sl == g.nks) {
+                    sl = 0;
+                    ++rbi;
+                }
+            } else if (++rbi == nrb) {
                 rbi = 0;
                 ++sl;
             }
@@ -954,10 +980,18 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
 
 template <int MODE, int R, bool ARGMAX, bool FUSE = false, int PROD = kProdPlain, bool KV = false>
 cudaError_t launch_gemv_row_t(const GemvArgs& a, const LaunchCtx& ctx) {
-    auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD, KV>;
+    auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD, KV, false>;
+    bool sli = false;
+    if constexpr (MODE == 0 && R == 1 && !FUSE) {
+        // (measured: the fused launches run slower in this order, so they keep
+        // the slice-outer one)
+        sli = row_slices_inner(a.K);
+        if (sli) kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD, KV, true>;
+    }
     constexpr size_t smem = row_smem_bytes<MODE, R, FUSE>();
-    static std::atomic<bool> configured[kMaxDevices];
-    if (const cudaError_t e = set_smem_once(kern, size_t(smem), ctx.dev, configured); e != cudaSuccess)
+    static std::atomic<bool> configured[2][kMaxDevices];   // per kernel (order), per device
+    if (const cudaError_t e = set_smem_once(kern, size_t(smem), ctx.dev, configured[sli ? 1 : 0]);
+        e != cudaSuccess)
         return e;
     if (!row_kernel_fits<MODE, R>(a.K)) return cudaErrorInvalidValue;   // callers check first
     GemvParams p{};
