@@ -114,3 +114,13 @@ def test_geometry_argument_errors(lib):
     assert f(1, 1, 5, 4096, 10, 0, out) == 1             # more CTAs than rows
     assert f(0, 2, 100, 4096, 10, 0, out) == 6           # f32 decodes one row a launch
     assert f(1, 9, 100, 4096, 10, 0, out) == 6           # one-word: 8 rows a pass at most
+
+
+def test_f32_two_slice_rows_take_the_slice_inner_order(lib):
+    # rows of 8,192 < K <= 16,384 values run in two slices; with two warp groups
+    # and an even ring each group's slots then always carry one slice (the
+    # kernel's slice-inner stage order, taken by the unfused f32 launches)
+    for k in (8224, 11008, 14336, 16384):
+        g = geometry("f32", 1, 4096, k, 152, 0)
+        assert g["nks"] == 2 and g["stride"] % g["nks"] == 0, g
+        assert g["nstages"] % g["stride"] == 0, g
