@@ -181,9 +181,7 @@ def oracle_step(mats, hs, modes=MODES):
             orc.project(mode, q, s, orc.quantize(mode, x))
 
 
-def cpu_baseline(mats, hs, budget_s=10.0):
-    from oracle import oracle as orc
-    orc.build()
+def _timed_oracle_steps(mats, hs, budget_s):
     t0 = time.perf_counter()
     steps = 0
     while True:
@@ -191,12 +189,30 @@ def cpu_baseline(mats, hs, budget_s=10.0):
         steps += 1
         if time.perf_counter() - t0 >= budget_s:
             break
-    dt = time.perf_counter() - t0
+    return steps, time.perf_counter() - t0
+
+
+def cpu_baseline(mats, hs, budget_s=10.0):
+    """The oracle on the host cores (OpenMP over output rows), then the same
+    code on one thread for a shorter sample (results are identical: each
+    output's order of operations does not depend on the thread count)."""
+    from oracle import oracle as orc
+    orc.build()
+    steps, dt = _timed_oracle_steps(mats, hs, budget_s)
+    cores = orc.threads()
+    orc.set_threads(1)
+    try:
+        steps1, dt1 = _timed_oracle_steps(mats, hs, budget_s * 0.3)
+    finally:
+        orc.set_threads(cores)
     return {"value": round(steps * len(MODES) * LAYER_BYTES / dt / 1e9, 4), "unit": "GB/s",
-            "cores": orc.threads(), "kind": "oracle",
+            "cores": cores, "kind": "oracle",
             "sample": f"{steps} full step(s) of {WORKLOAD} (3 modes x 4 projections, RMSNorm + "
                       f"quantize + projection) in {dt:.1f} s; plain C oracle, OpenMP over "
-                      f"output rows"}
+                      f"output rows",
+            "single_thread": {"value": round(steps1 * len(MODES) * LAYER_BYTES / dt1 / 1e9, 4),
+                              "unit": "GB/s", "cores": 1,
+                              "sample": f"{steps1} full step(s) in {dt1:.1f} s, one thread"}}
 
 
 def run_reference(args, world, rank):
