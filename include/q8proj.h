@@ -205,7 +205,9 @@ size_t q8_proj_fused_workspace(int mode, int64_t rows, int64_t K);
  *   kv_col   first column of the K slice: K = columns [kv_col, kv_col + kv_dim),
  *            V = [kv_col + kv_dim, kv_col + 2 kv_dim); kv_col + 2 kv_dim <= N
  *   k_cache, v_cache  float [rows][n_pos][kv_dim], one cache per row's
- *            sequence, disjoint; row m's slices go to cache row pos[m]
+ *            sequence, disjoint; row m's slices go to cache row pos[m];
+ *            1 <= n_pos <= 2^31 - 1 and each cache at most 2^40 bytes
+ *            (Q8_ERR_SHAPE otherwise)
  * K <= 16384.  A position outside [0, n_pos) writes no cache entry of its row
  * and sets device error 2 (q8_device_error); y is written either way.
  */

@@ -376,7 +376,10 @@ q8_status q8_proj_fused_kv(int mode, const int8_t* q, const uint16_t* s, int64_t
                            void* stream) {
     if (!pos || !k_cache || !v_cache) return Q8_ERR_ARG;
     if (rows < 1 || rows > Q8_MAX_ROWS) return Q8_ERR_SHAPE;
-    if (kv_dim < 1 || kv_col < 0 || kv_col + 2 * kv_dim > N || n_pos < 1) return Q8_ERR_SHAPE;
+    if (kv_dim < 1 || kv_col < 0 || kv_dim > N / 2 || kv_col > N - 2 * kv_dim) return Q8_ERR_SHAPE;
+    // positions are int32; a cache of more than 2^40 bytes exceeds any device
+    if (n_pos < 1 || n_pos > INT32_MAX || kv_dim > (int64_t(1) << 38) / (rows * n_pos))
+        return Q8_ERR_SHAPE;
     if (K > kFusedMaxK) return Q8_ERR_UNSUPPORTED;   // the decode kernel's K
     if (!aligned16(pos) || !aligned16(k_cache) || !aligned16(v_cache)) return Q8_ERR_ALIGN;
     const size_t cache = size_t(rows) * size_t(n_pos) * size_t(kv_dim) * sizeof(float);

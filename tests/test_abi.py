@@ -89,3 +89,42 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert lib.head_argmax(1, A, A, 8, 64, A, A, 1, None, None, None, A, 1 << 20, None) == 1
     assert lib.q8_debug_block_dots(0, A, A, 8, 64, 1, A, 0, None) == 4
     assert lib.q8_debug_block_dots(1, A, A, 1 << 20, 4096, 256, A, 0, None) == 2
+
+
+def test_widened_entry_points_reject_bad_arguments(lib):
+    # residual before the norm: r required, s_out aligned and disjoint from h and r
+    f = lib.act_quant_residual
+    assert f(1, A, None, None, 1, 64, None, 1e-5, A, A, None) == 1
+    assert f(1, A, U, None, 1, 64, None, 1e-5, A, A, None) == 3
+    assert f(1, A, C.c_void_p(8192), A, 1, 64, None, 1e-5, A, A, None) == 1   # s_out == h
+    assert f(5, A, C.c_void_p(8192), None, 1, 64, None, 1e-5, A, A, None) == 4
+    g = lib.q8_proj_fused_residual
+    assert g(1, A, A, 8, 64, None, A, None, 1, None, 1e-5, A, 0, A, 1 << 20, None) == 1
+    assert g(1, A, A, 8, 64, A, A, None, 0, None, 1e-5, A, 0, A, 1 << 20, None) == 2
+    assert g(1, A, A, 8, 64, A, None, None, 1, None, 1e-5, A, 0, A, 1 << 20, None) == 1
+    # SwiGLU producer
+    assert lib.act_quant_swiglu(5, A, 1, 64, A, A, None) == 4
+    assert lib.act_quant_swiglu(1, U, 1, 64, A, A, None) == 3
+    assert lib.q8_proj_fused_swiglu(1, A, A, 8, 64, A, 1, A, 0, None, 0, None) == 7
+    # KV-cache-row epilogue
+    kv = lib.q8_proj_fused_kv
+    ok = dict(pos=A, col=0, dim=2, kc=C.c_void_p(1 << 20), vc=C.c_void_p(1 << 21), npos=16)
+
+    def call(N=8, K=64, rows=1, **over):
+        a = dict(ok, **over)
+        return kv(1, A, A, N, K, A, rows, None, 1e-5, A, a["pos"], a["col"], a["dim"], a["kc"],
+                  a["vc"], a["npos"], A, 1 << 20, None)
+
+    assert call(pos=None) == 1
+    assert call(kc=None) == 1
+    assert call(rows=0) == 2
+    assert call(dim=0) == 2
+    assert call(col=5, dim=2) == 2                 # V slice past N
+    assert call(col=-1) == 2
+    assert call(dim=1 << 62) == 2                  # no overflow in the range check
+    assert call(npos=0) == 2
+    assert call(npos=1 << 31) == 2                 # positions are int32
+    assert call(N=1 << 20, dim=1 << 18, npos=(1 << 31) - 1) == 2   # a cache beyond 2^40 bytes
+    assert call(K=16416) == 6                      # the decode kernel's K
+    assert call(pos=U) == 3
+    assert call(vc=C.c_void_p((1 << 20) + 16)) == 1   # K and V caches overlap
