@@ -70,6 +70,7 @@ def _load():
                 "orc_proj_f64": (None, [vp, vp, vp, i64, i64, i64, vp, vp]),
                 "orc_argmax_f32": (None, [vp, i64, i64, vp, vp]),
                 "orc_argmax_f64": (None, [vp, i64, i64, vp, vp]),
+                "orc_near_tie": (C.c_int, [C.c_double, C.c_double]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -248,7 +249,8 @@ def proj_f64(q, s, x):
 
 
 def argmax(logits: np.ndarray):
-    """Row arg-max with the lowest index on ties -> (tok int32, best value)."""
+    """Row arg-max with the lowest index on ties -> (tok int32, best value).
+    NaN logits are no candidates; a row of NaN only gives index 0, value NaN."""
     logits = np.ascontiguousarray(logits)
     rows, n = logits.shape
     tok = np.empty(rows, np.int32)
@@ -261,6 +263,21 @@ def argmax(logits: np.ndarray):
     else:
         raise TypeError("logits must be f32 or f64")
     return tok, best
+
+
+# Relative distance from an f32 rounding boundary within which the RMS scale r
+# of a row is a "near tie": the oracle's own sequential f64 sum of squares is
+# accurate to about 2^-42 relative at K <= 16384, and the library evaluates r
+# to about 2^-44, so either may round r to the other f32 neighbour there.
+NEAR_TIE_REL = 2.0 ** -40
+
+
+def near_tie(r, rel: float = NEAR_TIE_REL) -> np.ndarray:
+    """Per row: whether the f64 RMS scale r lies within rel * r of an f32
+    rounding boundary (see orc_near_tie)."""
+    lib = _load()
+    rr = np.atleast_1d(np.asarray(r, dtype=np.float64))
+    return np.array([bool(lib.orc_near_tie(float(v), float(rel))) for v in rr], dtype=bool)
 
 
 # ----------------------------------------------------------------- compositions

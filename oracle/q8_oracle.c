@@ -416,17 +416,26 @@ void orc_proj_f64(const int8_t* q, const uint16_t* s, const float* x, int64_t N,
 /*
  * Arg-max of each logit row [author: decode_head / decode_step, "the step
  * ends with the arg-max of the logits"]: the smallest n holding the maximum
- * (equal values, including -0 and +0, keep the earlier index).
+ * (equal values, including -0 and +0, keep the earlier index).  A NaN logit
+ * is no candidate (a Q8_0 block whose binary16 scale overflowed carries an
+ * infinite scale, and 0 * inf is NaN); a row of NaN only gives index 0 and the
+ * value NaN.  A row of -inf gives index 0 and -inf.
  */
 void orc_argmax_f32(const float* logits, int64_t rows, int64_t N, int32_t* tok, float* best) {
     for (int64_t m = 0; m < rows; ++m) {
-        int64_t bi = 0;
-        float bv = logits[m * N];
-        for (int64_t n = 1; n < N; ++n) {
-            if (logits[m * N + n] > bv) {
-                bv = logits[m * N + n];
+        int64_t bi = -1;
+        float bv = 0.0f;
+        for (int64_t n = 0; n < N; ++n) {
+            float v = logits[m * N + n];
+            if (isnan(v)) continue;
+            if (bi < 0 || v > bv) {
+                bv = v;
                 bi = n;
             }
+        }
+        if (bi < 0) {
+            bi = 0;
+            bv = NAN;
         }
         tok[m] = (int32_t)bi;
         if (best) best[m] = bv;
@@ -435,15 +444,41 @@ void orc_argmax_f32(const float* logits, int64_t rows, int64_t N, int32_t* tok, 
 
 void orc_argmax_f64(const double* logits, int64_t rows, int64_t N, int32_t* tok, double* best) {
     for (int64_t m = 0; m < rows; ++m) {
-        int64_t bi = 0;
-        double bv = logits[m * N];
-        for (int64_t n = 1; n < N; ++n) {
-            if (logits[m * N + n] > bv) {
-                bv = logits[m * N + n];
+        int64_t bi = -1;
+        double bv = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double v = logits[m * N + n];
+            if (isnan(v)) continue;
+            if (bi < 0 || v > bv) {
+                bv = v;
                 bi = n;
             }
+        }
+        if (bi < 0) {
+            bi = 0;
+            bv = NAN;
         }
         tok[m] = (int32_t)bi;
         if (best) best[m] = bv;
     }
+}
+
+/* ------------------------------------------------- RMSNorm near-tie report */
+
+/*
+ * Whether the f64 RMS scale r of a row lies within rel * r of an f32 rounding
+ * boundary (the midpoint of two neighbouring binary32 values), where another
+ * correct evaluation of r -- another summation order of sum h^2, or an
+ * evaluation accurate to rel -- may round to the other f32 neighbour, so
+ * rf = float(r), and with it the row's codes, may differ from the oracle's
+ * [lane: CudaKnobs fuse_quant; the producer's norm].  Used to classify a
+ * mismatch of quantised codes, never to accept one silently.
+ */
+int orc_near_tie(double r, double rel) {
+    if (!(r > 0.0) || isinf(r)) return 0;
+    float f = (float)r;
+    if ((double)f == r) return 0;
+    float other = r > (double)f ? nextafterf(f, INFINITY) : nextafterf(f, -INFINITY);
+    double mid = ((double)f + (double)other) * 0.5;   /* exact: 25 significant bits */
+    return fabs(r - mid) <= rel * r;
 }

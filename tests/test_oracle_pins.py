@@ -314,6 +314,62 @@ def test_rmsnorm_power_of_two_constant(orc):
         assert np.array_equal(x[0], np.sign(c).astype(np.float32) * g)
 
 
+def _round_bin64(v: Fraction) -> Fraction:
+    """An exact positive rational rounded to binary64 (53-bit significand),
+    ties to even."""
+    e = v.numerator.bit_length() - v.denominator.bit_length()
+    if Fraction(2) ** e > v:
+        e -= 1
+    q = Fraction(2) ** (e - 52)
+    m = v / q
+    n = m.numerator // m.denominator
+    rem = m - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return n * q
+
+
+def test_rmsnorm_rounding_order_golden(orc):
+    """The producer rounds h * rf first, then multiplies by the gain: a block
+    where h * (rf * g) rounds one ulp apart, and where that ulp moves a
+    one-word code from 64 to 63 (tests/golden/rmsnorm_order.txt).
+
+    The projection's scale product has the same kind of freedom: the oracle
+    rounds (s_w * d_x) first, then multiplies by float(isum), and no pin tells
+    that from s_w * (d_x * isum); both stay within the float tolerance, so
+    they change no verdict."""
+    fx = {r[0]: r[1] for r in read_golden("rmsnorm_order.txt")}
+    hx = lambda k: float.fromhex(fx[k])
+    g0 = np.float32(hx("g0"))
+    h = np.zeros((1, QK), np.float32)
+    h[0, :2] = 3.0
+    g = np.ones(QK, np.float32)
+    g[0], g[1] = g0, g0 / np.float32(2)
+    # the fixture against exact rationals, both orders
+    r = _round_bin64(Fraction(4, 3))
+    rf = Fraction(_round_f32(r))
+    hrf = Fraction(_round_f32(3 * rf))
+    x0 = _round_f32(hrf * Fraction(float(g0)))
+    alt = _round_f32(3 * Fraction(_round_f32(rf * Fraction(float(g0)))))
+    assert (float(r), float(rf), float(hrf)) == (hx("r"), hx("rf"), hx("hrf"))
+    assert (x0, alt) == (hx("x0"), hx("x0_alt")) and x0 != alt
+    assert _round_f32(Fraction(x0) / 127) == hx("d_i8")
+    assert _round_f32(Fraction(alt) / 127) == hx("d_alt")
+    # the oracle takes the first order
+    x, rr = orc.rmsnorm(h, g, eps=0.0)
+    assert rr[0] == hx("r")
+    assert float(x[0, 0]) == hx("x0") and float(x[0, 1]) == hx("x1")
+    assert not np.any(x[0, 2:])
+    xq, xd = orc.act_quant_i8(x)
+    assert float(xd[0, 0]) == hx("d_i8")
+    assert (int(xq[0, 0]), int(xq[0, 1])) == (int(fx["code0"]), int(fx["code1"]))
+    # the code depends on the order: the other order's x gives the other code
+    xa = x.copy()
+    xa[0, 0], xa[0, 1] = np.float32(hx("x0_alt")), np.float32(hx("x0_alt") / 2)
+    xqa, _ = orc.act_quant_i8(xa)
+    assert int(xqa[0, 1]) == int(fx["code1_alt"])
+
+
 def test_rmsnorm_matches_f64_formula(orc):
     rng = np.random.default_rng(8)
     h = synth.activations(rng, 6, 4096)
@@ -469,12 +525,29 @@ def test_argmax_hand_vectors(orc):
         ([-3.0, -2.0, -2.5], 1),
         ([1.0, 2.0, 4.0, 4.0, 8.0], 4),
         ([np.float32(1.0) + np.float32(2**-23), 1.0], 0),
+        ([-np.inf, -np.inf, -np.inf], 0),
+        ([-np.inf, -3.0e38, -np.inf], 1),
+        ([np.inf, 1.0, np.inf], 0),
     ]
     for vals, want in cases:
         for dt in (np.float32, np.float64):
             tok, best = orc.argmax(np.array([vals], dt))
             assert tok[0] == want, (vals, dt)
             assert best[0] == max(vals)
+    # NaN is no candidate; a row of NaN only gives index 0 and the value NaN
+    nan = np.nan
+    nan_cases = [
+        ([nan, 1.0, 2.0, 2.0], 2, 2.0),
+        ([1.0, nan, 0.5], 0, 1.0),
+        ([nan, -np.inf, nan], 1, -np.inf),
+        ([nan, nan, nan], 0, nan),
+        ([-1.0, nan, -1.0], 0, -1.0),
+    ]
+    for vals, want, wbest in nan_cases:
+        for dt in (np.float32, np.float64):
+            tok, best = orc.argmax(np.array([vals], dt))
+            assert tok[0] == want, (vals, dt)
+            assert (np.isnan(best[0]) and np.isnan(wbest)) or best[0] == wbest, (vals, dt)
 
 
 def test_planted_head_margin(orc):
@@ -486,3 +559,46 @@ def test_planted_head_margin(orc):
         assert np.array_equal(tok, pos[np.arange(rows) % 8])
         top2 = np.sort(y, axis=1)[:, -2]
         assert np.all(best - top2 > 0.5 * best)
+
+
+# --------------------------------------------------- RMSNorm near-tie report
+
+def test_near_tie_classifier_at_known_distances(orc):
+    # binary32 neighbours f and f + ulp; their midpoint is the rounding boundary
+    for f in (1.0, 1.5 - 2.0**-23, 0.7390851, 3.0e-5, 1234.5):
+        f = float(np.float32(f))
+        ulp = float(np.spacing(np.float32(f)))
+        mid = f + ulp / 2                           # exact in binary64
+        assert orc.near_tie([mid])[0]
+        for rel in (2.0**-45, 2.0**-41):
+            assert orc.near_tie([mid * (1 + rel)])[0] and orc.near_tie([mid * (1 - rel)])[0]
+        for rel in (2.0**-38, 2.0**-30):
+            assert not orc.near_tie([mid * (1 + rel)])[0]
+            assert not orc.near_tie([mid * (1 - rel)])[0]
+        assert not orc.near_tie([f])[0]             # an f32 value: half an ulp away
+    # across a binade boundary the midpoint below 2^k uses the smaller ulp
+    mid_below = 2.0 - 2.0**-24
+    assert orc.near_tie([mid_below])[0] and not orc.near_tie([2.0 - 2.0**-23])[0]
+    assert not orc.near_tie([0.0])[0] and not orc.near_tie([np.inf])[0]
+
+
+def test_near_tie_constructed_row(orc):
+    # K = 32, eps = 0, h = (1 - 2^-19, 1, ..., 1): sum h^2 = 32 - 2^-18 + 2^-38
+    # exactly, so r = (1 - 2^-23 + 2^-43)^(-1/2) = 1 + 2^-24 - 2^-44 + O(2^-46):
+    # 2^-44 from the boundary 1 + 2^-24 between 1 and 1 + 2^-23
+    h = np.ones((2, QK), np.float32)
+    h[0, 0] = np.float32(1 - 2.0**-19)
+    h[1, 0] = np.float32(1.25)                      # a row far from any boundary
+    _, r = orc.rmsnorm(h, None, eps=0.0)
+    ss = Fraction(float(h[0, 0])) ** 2 + 31
+    m = ss / 32
+    mid = 1 + Fraction(1, 2**24)
+    # r lies between the two bounds 1/sqrt(m) is squeezed into
+    assert abs(Fraction(float(r[0])) - mid) < Fraction(1, 2**43)
+    assert (1 / (mid * mid) - m) != 0
+    flags = orc.near_tie(r)
+    assert flags[0] and not flags[1]
+    # random RMSNorm rows are almost never near ties (about 2^-16 each)
+    hr = synth.activations(np.random.default_rng(17), 64, 4096)
+    _, rr = orc.rmsnorm(hr)
+    assert orc.near_tie(rr).sum() == 0
