@@ -97,7 +97,8 @@ struct KvArgs {
     float* v_cache = nullptr;
 };
 
-// Runs the CUDA-core projection over groups of at most 16 activation rows.
+// Runs the CUDA-core projection over groups of gemv_max_rows(mode) activation
+// rows (each group one launch reading the weights once).
 q8_status run_projection(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                          const void* xq, const float* xd, int64_t rows, void* y, int out_f64,
                          int32_t* tok, double* maxval, void* ws, const LaunchCtx& ctx) {
@@ -153,14 +154,6 @@ q8_status check_proj_args(int mode, const int8_t* q, const uint16_t* s, int64_t 
 }
 
 }  // namespace
-
-namespace q8 {
-// rows per CUDA-core launch: the decode kernel's widest row count per mode
-// (more rows are split into groups, each reading the weights once); f32 runs
-// a row per launch: it is issue-bound, and a two-row pass cost 1.5x two
-// one-row passes (LM head, 16 rows: 3.19 ms in pairs, 2.07 ms row by row)
-int gemv_max_rows(int mode) { return mode == 0 ? 1 : mode == 1 ? 8 : 4; }
-}  // namespace q8
 
 extern "C" {
 
@@ -404,7 +397,7 @@ q8_status q8_proj_fused_swiglu(int mode, const int8_t* q, const uint16_t* s, int
 
 size_t head_argmax_workspace(int64_t rows) {
     if (rows < 1) return 0;
-    const int64_t g = rows < 16 ? rows : 16;
+    const int64_t g = rows < kArgmaxGroupRows ? rows : kArgmaxGroupRows;
     return kArgmaxHeader + size_t(kMaxGrid) * size_t(g) * sizeof(ArgmaxCand);
 }
 

@@ -603,12 +603,10 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, u
 template <int MODE, int TT, bool DEBUG>
 static int active_clusters(int ks, const LaunchCtx& ctx) {
     using C = CkCfg<MODE, TT>;
-    static int cache[64][kCkMaxSplit + 1];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    int& slot = cache[dev][ks];
-    if (slot > 0) return slot;
+    // per device and split; threads that race here store the same value
+    static std::atomic<int> cache[kMaxDevices][kCkMaxSplit + 1];
+    std::atomic<int>& slot = cache[ctx.dev][ks];
+    if (const int v = slot.load(std::memory_order_relaxed); v > 0) return v;
     int n = ctx.num_sms / ks;
     if (ks > 1) {
         cudaLaunchConfig_t cfg{};
@@ -629,8 +627,9 @@ static int active_clusters(int ks, const LaunchCtx& ctx) {
         else
             cudaGetLastError();
     }
-    slot = n > 0 ? n : 1;
-    return slot;
+    n = n > 0 ? n : 1;
+    slot.store(n, std::memory_order_relaxed);
+    return n;
 }
 
 // Split of K over a cluster: the count with the fewest 8-block groups on

@@ -408,6 +408,16 @@ __host__ __device__ constexpr size_t gemv_smem_bytes() {
            kGemvYaccBytes + size_t(kGemvMaxConsumerWarps) * R * sizeof(ArgmaxCand) + 64;
 }
 
+// The arg-max result of one activation row from its best (value, index)
+// candidate: a row without any candidate (every logit NaN: NaN is never the
+// maximum) gives index 0 and the value NaN.
+__device__ __forceinline__ void argmax_store(const ArgmaxCand& b, int32_t* tok, double* maxval,
+                                             int m) {
+    const bool none = b.i == 0x7fffffffffffffffll;
+    tok[m] = none ? 0 : int32_t(b.i);
+    if (maxval) maxval[m] = none ? __longlong_as_double(0x7ff8000000000000ll) : b.v;
+}
+
 template <int NT>
 __device__ __forceinline__ void consumer_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
@@ -770,8 +780,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps<MODE, R>() + 1), 1)
                     const ArgmaxCand o = {src->v, src->i};
                     if (o.v > b.v || (o.v == b.v && o.i < b.i)) b = o;
                 }
-                p.tok[tid] = int32_t(b.i);
-                if (p.maxval) p.maxval[tid] = b.v;
+                argmax_store(b, p.tok, p.maxval, tid);
             }
             if (tid == 0) *counter = 0u;
         }

@@ -970,8 +970,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     const ArgmaxCand o = {src->v, src->i};
                     if (o.v > b.v || (o.v == b.v && o.i < b.i)) b = o;
                 }
-                p.tok[tid] = int32_t(b.i);
-                if (p.maxval) p.maxval[tid] = b.v;
+                argmax_store(b, p.tok, p.maxval, tid);
             }
             if (tid == 0) *counter = 0u;
         }

@@ -79,7 +79,11 @@ struct GemvArgs {
 // Largest K the decode kernel quantises in its own shared memory.
 constexpr int64_t kFusedMaxK = 16384;
 
-int gemv_max_rows(int mode);
+// Rows per CUDA-core launch: the decode kernel's widest row count per mode
+// (more rows run as groups, each reading the weights once); f32 runs a row
+// per launch: it is issue-bound, and a two-row pass cost 1.5x two one-row
+// passes (LM head, 16 rows: 3.19 ms in pairs, 2.07 ms row by row).
+constexpr int gemv_max_rows(int mode) { return mode == 0 ? 1 : mode == 1 ? 8 : 4; }
 
 // tensor-core chunk path (chunk.cu): modes 1 and 2, K % 256 == 0
 bool chunk_supported(int mode, int64_t N, int64_t K, int64_t T);
@@ -108,5 +112,10 @@ struct ArgmaxCand {
     double v;
     long long i;
 };
+// Rows of one arg-max launch the workspace is sized for (every mode's group).
+constexpr int kArgmaxGroupRows = 16;
+static_assert(gemv_max_rows(0) <= kArgmaxGroupRows && gemv_max_rows(1) <= kArgmaxGroupRows &&
+                  gemv_max_rows(2) <= kArgmaxGroupRows,
+              "the arg-max workspace holds one candidate per CTA and row of a group");
 
 }  // namespace q8

@@ -21,7 +21,7 @@
 namespace {
 
 constexpr size_t kNoAllocScratch = q8::kArgmaxHeader +
-                                   size_t(q8::kMaxGrid) * 16 * sizeof(q8::ArgmaxCand);
+                                   size_t(q8::kMaxGrid) * q8::kArgmaxGroupRows * sizeof(q8::ArgmaxCand);
 
 __device__ __align__(256) unsigned char g_q8_head_scratch[kNoAllocScratch];
 

@@ -6,8 +6,9 @@ import pytest
 
 from oracle import oracle as orc
 from q8_quantized_projection_gb300 import build, native, synth
-from gpu_util import (QK, act_to_numpy, check_close, dev, host, no_device_error, torch,
-                      upload_act, upload_weights)
+from conftest import read_golden
+from gpu_util import (QK, act_to_numpy, assert_codes_match, check_close, dev, host,
+                      no_device_error, torch, upload_act, upload_weights)
 
 pytestmark = pytest.mark.gpu
 
@@ -59,15 +60,48 @@ def test_act_quant_bit_exact(mode, rows, k, norm, with_gain):
     h = synth.activations(rng, rows, k)
     h[0, :QK] = 0.0
     g = synth.gain(rng, k) if with_gain else None
-    x = orc.rmsnorm(h, g, 1e-5)[0] if norm else h
+    x, r = orc.rmsnorm(h, g, 1e-5) if norm else (h, None)
     act_o = orc.quantize(mode, x)
     xq, xd = native.activation_buffers(mode, rows, k)
     native.act_quant(mode, dev(h), xq, xd, norm=norm, gain=dev(g) if g is not None else None,
                      eps=1e-5)
-    act = act_to_numpy(mode, xq, xd)
-    for a, b in zip(act, act_o):
-        assert np.array_equal(a.view(np.uint8) if a.dtype != np.float32 else a.view(np.uint32),
-                              b.view(np.uint8) if b.dtype != np.float32 else b.view(np.uint32))
+    assert_codes_match(act_to_numpy(mode, xq, xd), act_o, r, what=f"act_quant {mode} {rows}x{k}")
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_act_quant_rounding_order_golden(mode):
+    """The hand-worked block of tests/golden/rmsnorm_order.txt: x = (h*rf)*g,
+    where the other order of the two roundings moves a one-word code."""
+    fx = {r[0]: r[1] for r in read_golden("rmsnorm_order.txt")}
+    g0 = np.float32(float.fromhex(fx["g0"]))
+    h = np.zeros((1, QK), np.float32)
+    h[0, :2] = 3.0
+    g = np.ones(QK, np.float32)
+    g[0], g[1] = g0, g0 / np.float32(2)
+    x, r = orc.rmsnorm(h, g, eps=0.0)
+    assert float(x[0, 0]) == float.fromhex(fx["x0"])
+    act_o = orc.quantize(mode, x)
+    if mode == "i8":
+        assert (int(act_o[0][0, 0]), int(act_o[0][0, 1])) == (int(fx["code0"]), int(fx["code1"]))
+    xq, xd = native.activation_buffers(mode, 1, QK)
+    native.act_quant(mode, dev(h), xq, xd, norm=True, gain=dev(g), eps=0.0)
+    assert_codes_match(act_to_numpy(mode, xq, xd), act_o, None, what=f"golden order {mode}")
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_act_quant_near_tie_row(mode):
+    """A row whose RMS scale lies 2^-44 from an f32 rounding boundary (K = 32,
+    h = (1 - 2^-19, 1, ..., 1), eps = 0): the codes match the oracle's, or
+    the mismatch is reported as a near tie (an expected failure)."""
+    h = np.ones((2, QK), np.float32)
+    h[0, 0] = np.float32(1 - 2.0 ** -19)
+    h[1, 0] = np.float32(1.25)
+    x, r = orc.rmsnorm(h, None, eps=0.0)
+    assert orc.near_tie(r).tolist() == [True, False]
+    act_o = orc.quantize(mode, x)
+    xq, xd = native.activation_buffers(mode, 2, QK)
+    native.act_quant(mode, dev(h), xq, xd, norm=True, eps=0.0)
+    assert_codes_match(act_to_numpy(mode, xq, xd), act_o, r, what=f"near-tie row {mode}")
 
 
 # ------------------------------------------------------------- block dots
@@ -117,6 +151,26 @@ def test_proj_parity(mode, n, k, rows):
     y2 = t.empty((rows, n), dtype=t.float32, device="cuda")
     native.q8_proj_chunk(mode, qd, sd, xq, xd, rows, y2)
     check_close(mode, host(y2), y_o, norm, what=f"chunk {mode} {n}x{k} rows={rows}")
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n,k", [(300, 4096), (64, 14336), (129, 4128)])
+@pytest.mark.parametrize("rows", [32, 64])
+def test_proj_parity_large_batches(mode, n, k, rows):
+    """q8_proj itself (not only q8_proj_chunk) at the largest batches of the
+    batched-decode workload, K = 4096 and 14336 (tensor cores for the int8
+    modes), and K = 4128 (not a multiple of 256: the CUDA-core kernels)."""
+    rng = np.random.default_rng(2000 + n + k + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, rows, k)
+    act = orc.quantize(mode, x)
+    y_o, norm = orc.project(mode, q, s, act)
+    qd, sd = upload_weights(q, s)
+    xq, xd = upload_act(mode, act, rows, k)
+    t = torch()
+    y = t.empty((rows, n), dtype=t.float32, device="cuda")
+    native.q8_proj(mode, qd, sd, xq, xd, rows, y)
+    check_close(mode, host(y), y_o, norm, what=f"{mode} {n}x{k} rows={rows}")
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -179,16 +233,15 @@ def test_act_quant_residual_bit_exact(mode, rows, k, with_gain):
     r[0, :QK] = -h[0, :QK]                      # a block that cancels to zero
     g = synth.gain(rng, k) if with_gain else None
     s_o = orc.residual_add(h, r)
-    act_o = orc.quantize(mode, orc.rmsnorm(s_o, g, 1e-5)[0])
+    x_o, rs = orc.rmsnorm(s_o, g, 1e-5)
+    act_o = orc.quantize(mode, x_o)
     t = torch()
     xq, xd = native.activation_buffers(mode, rows, k)
     s_out = t.empty((rows, k), dtype=t.float32, device="cuda")
     native.act_quant_residual(mode, dev(h), dev(r), xq, xd, s_out=s_out,
                               gain=dev(g) if g is not None else None, eps=1e-5)
     assert np.array_equal(host(s_out).view(np.uint32), s_o.view(np.uint32))
-    for a, b in zip(act_to_numpy(mode, xq, xd), act_o):
-        assert np.array_equal(a.view(np.uint8) if a.dtype != np.float32 else a.view(np.uint32),
-                              b.view(np.uint8) if b.dtype != np.float32 else b.view(np.uint32))
+    assert_codes_match(act_to_numpy(mode, xq, xd), act_o, rs, what=f"residual {mode} {rows}x{k}")
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -387,6 +440,92 @@ def test_head_argmax_equals_argmax_of_projection(mode):
     assert np.array_equal(host(tok), tok_ref)
 
 
+def _tie_head(n, k, rows, pairs, seed):
+    """A random Q8_0 head where activation row m's winner is planted at the
+    two indices pairs[m % 8] (identical rows, so their logits are equal
+    bit for bit): the arg-max must return the lower index."""
+    rng = np.random.default_rng(seed)
+    q, s = synth.q8_weights(rng, n, k)
+    h, base = synth.head_activations(rng, rows, k)
+    for j, (a, b) in enumerate(pairs):
+        synth.plant_head_rows(q, s, base[j:j + 1], np.array([a]))
+        q[b], s[b] = q[a], s[a]
+    return q, s, h
+
+
+TIE_PAIRS = [(0, 19999), (1000, 1001), (5000, 5003), (7, 12000), (19990, 19998), (2, 3),
+             (9000, 9100), (15000, 15001)]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("rows", [1, 16])
+@pytest.mark.parametrize("noalloc", [False, True])
+def test_head_argmax_exact_ties(mode, rows, noalloc):
+    """Exact ties between identical head rows, inside one CTA's rows and in
+    different CTAs (n = 0 with n = N-1): the lowest index wins."""
+    n, k = 20000, 1024
+    q, s, h = _tie_head(n, k, rows, TIE_PAIRS, seed=rows + 3)
+    x, _ = orc.rmsnorm(h)
+    act = orc.quantize(mode, x)
+    tok_o, _, y_o = orc.head_argmax(mode, q, s, act)
+    want = np.array([min(TIE_PAIRS[m % 8]) for m in range(rows)])
+    assert np.array_equal(tok_o, want)
+    rowsel = np.arange(rows)
+    assert np.array_equal(y_o[rowsel, want], y_o[rowsel, [max(TIE_PAIRS[m % 8]) for m in range(rows)]])
+    t = torch()
+    qd, sd = upload_weights(q, s)
+    xq, xd = upload_act(mode, act, rows, k)
+    tok = t.full((rows,), -7, dtype=t.int32, device="cuda")
+    if noalloc:
+        native.head_argmax_noalloc(mode, qd, sd, xq, xd, rows, tok)
+    else:
+        native.head_argmax(mode, qd, sd, xq, xd, rows, tok, native.argmax_workspace(rows))
+    assert np.array_equal(host(tok), want)
+
+
+@pytest.mark.parametrize("mode", ["i8", "i8x2"])
+@pytest.mark.parametrize("rows", [1, 16])
+def test_head_argmax_nan_and_infinite_logits(mode, rows):
+    """NaN logits are never the maximum; a row of -inf gives index 0; a row of
+    NaN gives index 0 and the value NaN (infinite binary16 scales: 0 * inf is
+    NaN, a negative block dot times inf is -inf)."""
+    n, k = 3000, 256
+    rng = np.random.default_rng(77 + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    h, base = synth.head_activations(rng, rows, k)
+    pos = np.array([5, 2999, 1, 700, 1500, 2000, 2500, 2998])
+    synth.plant_head_rows(q, s, base, pos)
+    inf16 = np.uint16(0x7C00)
+    q[0], s[0] = 0, inf16                       # logit NaN at n = 0
+    x, _ = orc.rmsnorm(h)
+    act = orc.quantize(mode, x)
+    tok_o, _, _ = orc.head_argmax(mode, q, s, act)
+    assert np.array_equal(tok_o, pos[np.arange(rows) % 8])
+    t = torch()
+    xq, xd = upload_act(mode, act, rows, k)
+    tok = t.full((rows,), -7, dtype=t.int32, device="cuda")
+    mx = t.empty(rows, dtype=t.float64, device="cuda")
+    qd, sd = upload_weights(q, s)
+    native.head_argmax(mode, qd, sd, xq, xd, rows, tok, native.argmax_workspace(rows), maxval=mx)
+    assert np.array_equal(host(tok), tok_o)
+    # every logit -inf: weights -1 with infinite scales, activation codes > 0
+    hp = np.abs(h) + np.float32(0.5)
+    actp = orc.quantize(mode, orc.rmsnorm(hp)[0])
+    qn = np.full((n, k), -1, np.int8)
+    sn = np.full((n, k // QK), inf16, np.uint16)
+    tok_o, best_o, _ = orc.head_argmax(mode, qn, sn, actp)
+    assert np.all(tok_o == 0) and np.all(best_o == -np.inf)
+    xq, xd = upload_act(mode, actp, rows, k)
+    qd, sd = upload_weights(qn, sn)
+    native.head_argmax(mode, qd, sd, xq, xd, rows, tok, native.argmax_workspace(rows), maxval=mx)
+    assert np.all(host(tok) == 0) and np.all(host(mx) == -np.inf)
+    # every logit NaN: zero weights with infinite scales
+    qd, sd = upload_weights(np.zeros((n, k), np.int8), sn)
+    tok.fill_(-7)
+    native.head_argmax(mode, qd, sd, xq, xd, rows, tok, native.argmax_workspace(rows), maxval=mx)
+    assert np.all(host(tok) == 0) and np.all(np.isnan(host(mx)))
+
+
 # --------------------------------------------------- full-size workloads
 
 @pytest.mark.parametrize("mode", MODES)
@@ -486,9 +625,8 @@ def test_prefill_chunk_full_size_sampled(mode):
         y = tt.empty((T, n), dtype=tt.float32, device="cuda")
         native.q8_proj_chunk(mode, qd, sd, xq, xd, T, y)
         idx = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 64)]))
-        x, _ = orc.rmsnorm(h)
+        x, r = orc.rmsnorm(h)
         act = orc.quantize(mode, x)
-        for a, b in zip(act_to_numpy(mode, xq, xd), act):
-            assert np.array_equal(a, b)
+        assert_codes_match(act_to_numpy(mode, xq, xd), act, r, what=f"{name} {mode} T={T}")
         y_o, norm = orc.project(mode, q[idx], s[idx], act)
         check_close(mode, host(y)[:, idx], y_o, norm, what=f"{name} {mode} T={T}")
