@@ -241,13 +241,16 @@ q8_status q8_proj_fused_swiglu(int mode, const int8_t* q, const uint16_t* s, int
  * LM head fused with its arg-max (model::author, decode_head: "the final
  * norm, the LM head and the arg-max"; decode_batch_head: one token per
  * sequence).  Modes Q8_ACT_F32 (logits to f64 accuracy) and Q8_ACT_I8 /
- * Q8_ACT_I8X2 (f32 logits).
- *   tok     int32 [rows]: the smallest n holding the row's maximum logit
- *   maxval  double [rows] or NULL: that maximum
+ * Q8_ACT_I8X2 (f32 logits).  The int8 modes from 9 (one-word) or 5
+ * (two-word) rows on, with K % 256 == 0, read the head once for all rows on
+ * the tensor cores.
+ *   tok     int32 [rows]: the smallest n holding the row's maximum logit; NaN
+ *           logits are never the maximum, and a row of NaN gives 0
+ *   maxval  double [rows] or NULL: that maximum (NaN for a row of NaN)
  *   logits  float [rows][N] (double for Q8_ACT_F32) or NULL
- *   workspace: head_argmax_workspace(rows) bytes.  Its first 16 bytes must
- *   be zero before the first call on it; every completed call leaves them
- *   zero again.  Calls sharing a workspace must not overlap.
+ *   workspace: head_argmax_workspace(rows) bytes, zeroed whole before the
+ *   first call on it; every completed call leaves the counters and keys it
+ *   uses zero again.  Calls sharing a workspace must not overlap.
  */
 q8_status head_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                       const void* xq, const float* xd, int64_t rows, int32_t* tok,

@@ -398,7 +398,7 @@ q8_status q8_proj_fused_swiglu(int mode, const int8_t* q, const uint16_t* s, int
 size_t head_argmax_workspace(int64_t rows) {
     if (rows < 1) return 0;
     const int64_t g = rows < kArgmaxGroupRows ? rows : kArgmaxGroupRows;
-    return kArgmaxHeader + size_t(kMaxGrid) * size_t(g) * sizeof(ArgmaxCand);
+    return kArgmaxGemvOff + kArgmaxHeader + size_t(kMaxGrid) * size_t(g) * sizeof(ArgmaxCand);
 }
 
 q8_status head_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
@@ -417,8 +417,12 @@ q8_status head_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, i
         return Q8_ERR_ALIGN;
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
+    static_assert(kArgmaxKeyBytes >= 8 * Q8_MAX_ROWS, "one arg-max key per row");
+    if (mode != Q8_ACT_F32 && rows >= chunk_min_rows(mode) && chunk_supported(mode, N, K, rows))
+        return launched(launch_chunk_argmax(mode, q, s, N, K, xq, xd, rows, static_cast<float*>(logits), tok,
+                                            maxval, workspace, ctx));
     return run_projection(mode, q, s, N, K, xq, xd, rows, logits, mode == Q8_ACT_F32 ? 1 : 0, tok,
-                          maxval, workspace, ctx);
+                          maxval, static_cast<unsigned char*>(workspace) + kArgmaxGemvOff, ctx);
 }
 
 q8_status q8_debug_block_dots(int mode, const int8_t* q, const void* xq, int64_t N, int64_t K,

@@ -1,41 +1,61 @@
 // chunk.cu -- the prefill-chunk / batched projection on the 5th-generation
 // tensor cores (tcgen05, sm_103a): T activation rows at once, every weight
-// byte read from HBM once per launch.
+// byte read from HBM once per launch; optionally fused with the LM head's
+// arg-max.
 //
 // Per Q8_0 block b the block dots of a 128-weight-row by TT-activation-row
 // tile are one exact tensor-core product: int8 values are exact in f16, and
 // 32 products of |q| <= 127 codes sum to < 2^24, so an f32 accumulator holds
-// the integer isum exactly (two-word mode: one product per plane, then
-// 128*hi + lo rounds once, exactly like float(isum)).  The scales do not fold
-// into the product (they differ per block on both sides), so each block's
-// product is read back and rescaled:  y[t][n] += isum * (s[n][b] * d[t][b]).
+// the integer isum exactly (two-word mode: the hi and lo planes stacked along
+// the MMA's N, then 128*hi + lo rounds once, exactly like float(isum)).  The
+// scales do not fold into the product (they differ per block on both sides),
+// so each block's product is read back and rescaled:
+//   y[t][n] += isum * (s[n][b] * d[t][b]).
+// (tcgen05.mma kind::i8 does not exist for sm_103a; ptxas rejects it.)
 //
-// CTA tile: 128 weight rows (MMA M) x TT activation rows (MMA N), over a
-// range of K.  Warp roles, connected by mbarriers whose waits are bounded:
-//   warp 0      producer: 2-D TMA tiles of weights (int8, 128-byte swizzle),
-//               activation codes (one or two planes), activation scales and,
-//               every 8 blocks, weight scales;
-//   warp 1      owns TMEM; one thread issues the MMAs (kind::f16, K = 16, two
-//               per block and activation plane) into one of NSLOT accumulator
-//               slots, and commits them;
-//   warps 2-5   converters (2-9: two groups of four taking alternate block
-//               pairs), two blocks at a time: weights int8 -> f16 straight
-//               into TMEM (the MMA's A operand, lane = weight row), activation
-//               codes int8 -> f16 operand tiles in shared memory (K-major, no
-//               swizzle), and both blocks' scales into the scale ring entries
-//               of their accumulator slots;
-//   next 8      epilogue: TMEM -> registers, rescale with packed f32x2 FMAs,
-//               accumulate.
-// A converted pair is freed by its MMAs' own completion (commit); an
-// accumulator slot and its scale-ring entry by the epilogue.  TMEM columns
-// 0..383 hold the accumulator slots, 384..511 four A pairs.
+// One tcgen05.mma (M = 128, K = 16) costs about the same for every N up to
+// 128 on this part, so a block costs two MMAs whatever the tile's row count,
+// and the per-block work around it decides the speed: the accumulator read
+// back from tensor memory (a long-latency load) and the rescale.
+//
+// CTA tile: 128 weight rows (MMA M) x TT activation rows (MMA N = TT * planes)
+// over a range of K.  Warp roles, connected by mbarriers whose waits are
+// bounded:
+//   warp 0      producer: 2-D TMA tiles of a stage (4 blocks of K): weights
+//               (int8, 128-byte swizzle) -- issued before the wait on the
+//               previous kernel, since weights never depend on it --, then
+//               activation codes (one or two planes) and activation scales;
+//               every 8 blocks the weight scales;
+//   warp 1      owns TMEM; one thread issues two K = 16 MMAs per block into
+//               one of kSlots accumulator slots and commits each block;
+//   next 6-10   converters, a whole stage at a time: 4 or 8 warps (one or
+//               two per TMEM lane quadrant) the weights int8 -> f16 into TMEM
+//               (the MMA's A operand) and their scales; two warps the
+//               activation codes int8 -> f16 into the K-major operand tiles in
+//               shared memory (B) and their scales;
+//   last 8/16   epilogue: kEG groups take the blocks in turn (so one group's
+//               wait on its tensor-memory load overlaps the others' work),
+//               kEC warps a lane quadrant split the columns; TMEM ->
+//               registers, rescale with packed f32x2 FMAs, accumulate; the
+//               groups' partial sums are added in group order at the end.
+// A converted stage is freed by its MMAs' own completion (commit); an
+// accumulator slot, and a block's entry in the ring of 8 scale entries, by the
+// epilogue as soon as it holds them in registers.  TMEM holds the
+// accumulator slots, then two or three converted stages (64 columns each).
 //
 // Split K: when there are too few 128 x TT tiles to fill the GPU, KS CTAs (a
 // thread-block cluster along z) share a tile, each over a contiguous range
 // of 8-block groups; their partial sums meet in shared memory and each CTA
 // adds up a slice of the tile over the cluster (distributed shared memory),
 // in rank order, so results do not depend on timing.
+//
+// Arg-max (the LM head): each tile's best (value, lowest row) per activation
+// row goes into a 64-bit key, value-ordered bits above the complemented row,
+// merged by one atomicMax per row and tile; the last CTA to take a ticket
+// writes the tokens and clears the keys and the ticket.
 #include <cuda.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "launch.h"
@@ -46,56 +66,88 @@ namespace q8 {
 constexpr int kCkM = 128;          // weight rows per tile
 constexpr int kCkStageK = 128;     // bytes of K per TMA stage (4 blocks)
 constexpr int kCkGroup = 8;        // blocks per weight-scale group (16 bytes of f16)
-constexpr int kCkPairs = 4;        // converted block pairs in flight
-constexpr int kCkAccCols = 384;    // TMEM columns for accumulator slots
-constexpr int kCkEpiWarps = 8;
+constexpr int kCkSGroups = 4;      // weight-scale groups in flight
+constexpr int kCkACols = 64;       // TMEM columns of one converted stage (4 blocks x 16)
+constexpr int kCkAConvWarps = 2;   // activation converters
 constexpr int kCkMaxSplit = 8;
 constexpr int kCkSmemBudget = 227 * 1024;
+
+// what a launch writes
+constexpr int kCkPlain = 0;    // y
+constexpr int kCkDebug = 1;    // the per-block integer dots
+constexpr int kCkArgmax = 2;   // the arg-max of every row (and y when given)
 
 template <int MODE, int TT>
 struct CkCfg {
     static constexpr int kPlanes = (MODE == 2) ? 2 : 1;
-    static constexpr int kSlotCols = TT * kPlanes;                    // TMEM columns per block
-    static constexpr int kSlots = (kCkAccCols / kSlotCols) < 8 ? (kCkAccCols / kSlotCols) : 8;
-    static constexpr int kTmemCols = 512;
-    static constexpr int kW = kCkM * kCkStageK;                       // 16 KB
+    static constexpr int kN = TT * kPlanes;                            // MMA N
+    // converted stages in flight (A in TMEM, B in shared memory): three where
+    // the accumulator slots leave room, so the converters run two stages ahead
+    static constexpr int kQuads = kN <= 64 ? 3 : 2;
+    static constexpr int kAccCols = 512 - kQuads * kCkACols;           // accumulator slots
+    static constexpr int kSlotsRaw = (kAccCols / kN) < 8 ? (kAccCols / kN) : 8;
+    // epilogue: kEC warps per lane quadrant split the columns, kEG groups
+    // take the blocks in turn
+    // small tiles: light epilogue work per block, so 8 epilogue warps, and
+    // the weight conversion (the same per block whatever the tile) over 8
+    // warps, two per TMEM lane quadrant, each half of a stage's blocks;
+    // larger tiles: 16 epilogue warps and 4 weight converters
+    static constexpr int kWConv = kN <= 32 ? 8 : 4;
+    static constexpr int kConv = kWConv + kCkAConvWarps;
+    static constexpr int kEpiWarps = kN <= 32 ? 8 : 16;
+    static constexpr int kEC = kN >= 128 ? 4 : (kN >= 64 ? 2 : 1);
+    static constexpr int kEG = kEpiWarps / (4 * kEC);
+    static constexpr int kSlots = kSlotsRaw / kEG * kEG;               // a multiple of the groups
+    // accumulator slots are released in groups of kGS blocks (one barrier a
+    // group), so that the MMA issuer waits once per group, not per block
+    static constexpr int kGS = kSlots >= 8 ? 4 : (kSlots % 2 == 0 ? kSlots / 2 : 1);
+    static constexpr int kSG = kSlots / kGS;
+    static constexpr int kCW = TT / kEC;                               // columns per thread
+    static constexpr int kW = kCkM * kCkStageK;                        // 16 KB
     static constexpr int kXPlane = TT * kCkStageK;
     static constexpr int kX = kXPlane * kPlanes;
-    static constexpr int kXD = TT * 4 * 4;                            // [TT][4 blocks] f32
+    static constexpr int kXD = TT * 4 * 4;                             // [TT][4 blocks] f32
     static constexpr int kStage = (kW + kX + kXD + 1023) / 1024 * 1024;
-    static constexpr int kSGroup = kCkM * kCkGroup * 2;               // [128][8 blocks] f16
-    static constexpr int kSGroups = 4;
-    static constexpr int kBPlane = TT * 64;                           // [TT][32] f16
-    static constexpr int kBBlock = kBPlane * kPlanes;
-    static constexpr int kOpPair = 2 * kBBlock;
-    static constexpr int kScl = kCkM * 2 + TT * 4;                    // sw[128] f16, xd[TT] f32
-    static constexpr int kCW = TT / 2;                                // columns per epilogue warp
-    // Two converter groups take alternate block pairs when there are at
-    // least 4 accumulator slots: a group then never waits on a slot barrier
-    // more than one phase ahead of what it has seen (the parity would alias).
-    static constexpr int kConvGroups = kSlots >= 4 ? 2 : 1;
-    static constexpr int kEpiWarp0 = 2 + 4 * kConvGroups;
-    static constexpr int kThreads = (kEpiWarp0 + kCkEpiWarps) * 32;
-    static constexpr int kFixed = kSGroups * kSGroup + kCkPairs * kOpPair + kSlots * kScl +
-                                  512 /*barriers*/ + 1024 /*alignment*/;
+    static constexpr int kSGroup = kCkM * kCkGroup * 2;                // [128][8 blocks] f16
+    static constexpr int kBBlock = kN * 64;                            // [kN][32] f16
+    static constexpr int kBQuad = 4 * kBBlock;
+    static constexpr int kScl = kCkM * 2 + TT * 4;                     // sw[128] f16, xd[TT] f32
+    static constexpr int kSE = 8;                                      // scale entries: two stages
+    static constexpr int kEpiWarp0 = 2 + kConv;
+    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+    static constexpr int kBarBytes = 1024;
+    static constexpr int kFixed = kCkSGroups * kSGroup + kQuads * kBQuad +
+                                  (kSE * kScl + 127) / 128 * 128 + kBarBytes + 1024 /*alignment*/;
     static constexpr int kStages = (kCkSmemBudget - kFixed) / kStage < 8
                                        ? (kCkSmemBudget - kFixed) / kStage
                                        : 8;
     static constexpr size_t kSmem = size_t(kStages) * kStage + kFixed;
+    // the end-of-tile scratch in the stage area: the groups' partial sums
+    // (or the CTA's split-K partial), then the arg-max candidates
+    static constexpr int kPartial = kCkM * TT * 4;
+    static constexpr int kCandOff = (kEG > 1 ? kEG - 1 : 1) * kPartial;
     static_assert(kStages >= 3, "TMA pipeline depth");
     static_assert(kStage % 1024 == 0, "swizzled TMA tiles need 1024-byte alignment");
-    static_assert(kCkM * TT * 4 <= kStages * kStage, "split-K partial must fit the stages");
+    static_assert(kCandOff + 4 * TT * 8 <= kStages * kStage, "end-of-tile scratch must fit the stages");
     static_assert(kSmem <= size_t(kCkSmemBudget), "shared memory");
-    static_assert(kCW % 16 == 0, "epilogue columns");
-    static_assert(kSlots >= 3, "accumulator slots");
+    static_assert(kCW % 16 == 0 && kCW <= 32, "epilogue columns");
+    static_assert(kSlots >= 3 && kSlots % kEG == 0, "accumulator slots: each served by one group");
+    static_assert(kSE == 8 && kSE % kEG == 0, "scale entries: two stages, each served by one group");
+    static_assert(kSlots % kGS == 0 && kSG >= 2 && kGS % kEG == 0 || kGS == 1, "slot groups");
+    static_assert(kN <= 256 && kN % 16 == 0, "MMA N");
+    static_assert(4 * kEC * kEG == kEpiWarps, "epilogue warps");
 };
 
 struct CkParams {
     int64_t N, K, T;
     int groups_per_split;   // 8-block groups of K per CTA of a cluster
-    float* y;
+    float* y;               // [T][N], may be NULL for the arg-max
     int32_t* isum;          // debug: per-block dots [T][N][K/32] instead of y
     int* err;
+    unsigned int* ticket;   // arg-max: CTAs done
+    unsigned long long* keys;   // arg-max: one key per activation row
+    int32_t* tok;
+    double* maxval;
 };
 
 __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -112,9 +164,8 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return uint32_t(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// The 32 int8 values of one block row (two 16-byte chunks of a 128-byte-
-// swizzled TMA tile) as f16, stored as row r of a K-major no-swizzle operand
-// tile at `dst`.
+// The 32 int8 values of one block row (two 16-byte chunks) as f16, stored as
+// row r of a K-major no-swizzle operand tile at `dst`.
 __device__ __forceinline__ void store_row_f16(uint32_t dst, int r, const int4 a, const int4 b) {
     const uint32_t w[8] = {uint32_t(a.x), uint32_t(a.y), uint32_t(a.z), uint32_t(a.w),
                            uint32_t(b.x), uint32_t(b.y), uint32_t(b.z), uint32_t(b.w)};
@@ -124,6 +175,17 @@ __device__ __forceinline__ void store_row_f16(uint32_t dst, int r, const int4 a,
         i8x4_to_f16x4(w[2 * c], h[0], h[1]);
         i8x4_to_f16x4(w[2 * c + 1], h[2], h[3]);
         sts128(dst + tile_offset(r, 8 * c), h[0], h[1], h[2], h[3]);
+    }
+}
+
+// Four 16-byte chunks of int8 weights -> 32 f16x2 words (8 per chunk, the
+// lower K index in the low half).
+__device__ __forceinline__ void weights_f16(const int4 (&w)[4], uint32_t (&hw)[32]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t v[4] = {uint32_t(w[c].x), uint32_t(w[c].y), uint32_t(w[c].z), uint32_t(w[c].w)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) i8x4_to_f16x4(v[i], hw[8 * c + 2 * i], hw[8 * c + 2 * i + 1]);
     }
 }
 
@@ -140,6 +202,11 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
 __device__ __forceinline__ float f2_lo(uint64_t a) { return __uint_as_float(uint32_t(a)); }
@@ -168,7 +235,7 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
 }
 
 // 16 consecutive TMEM columns of the warp's 32 lanes.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     uint32_t r[16];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -181,31 +248,59 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int MODE, int TT, bool DEBUG>
+// ------------------------------------------------------------- arg-max keys
+
+// The 64-bit arg-max key of logit v at row n: the value's bits in an order
+// that sorts like the value (-0 taken as +0), above the complemented row, so
+// the largest key is the largest value at its lowest row.  0 is no key (every
+// real key has a non-zero upper word).
+__device__ __forceinline__ unsigned long long argmax_key(float v, unsigned n) {
+    const unsigned b = __float_as_uint(v == 0.0f ? 0.0f : v);
+    const unsigned ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return (static_cast<unsigned long long>(ord) << 32) | (0xffffffffu - n);
+}
+
+__device__ __forceinline__ void argmax_unkey(unsigned long long key, int32_t& tok, double& val) {
+    if (key == 0ull) {   // no candidate: every logit of the row was NaN
+        tok = 0;
+        val = __longlong_as_double(0x7ff8000000000000ll);
+        return;
+    }
+    const unsigned ord = unsigned(key >> 32);
+    const unsigned b = (ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord;
+    tok = int32_t(0xffffffffu - unsigned(key & 0xffffffffull));
+    val = double(__uint_as_float(b));
+}
+
+template <int MODE, int TT, int KIND>
 __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
                  const __grid_constant__ CUtensorMap tm_xl, const __grid_constant__ CUtensorMap tm_s,
                  const __grid_constant__ CUtensorMap tm_xd, const CkParams p) {
     using C = CkCfg<MODE, TT>;
+    constexpr bool DEBUG = KIND == kCkDebug;
+    constexpr bool ARGMAX = KIND == kCkArgmax;
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled TMA tiles
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* stages = smem;
     unsigned char* sgroups = stages + size_t(C::kStages) * C::kStage;
-    unsigned char* ops = sgroups + size_t(C::kSGroups) * C::kSGroup;
-    unsigned char* scl = ops + size_t(kCkPairs) * C::kOpPair;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(scl + size_t(C::kSlots) * C::kScl);
+    unsigned char* bquads = sgroups + size_t(kCkSGroups) * C::kSGroup;
+    unsigned char* scl = bquads + size_t(C::kQuads) * C::kBQuad;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(scl + (C::kSE * C::kScl + 127) / 128 * 128);
     uint64_t* st_full = bars;
     uint64_t* st_empty = st_full + C::kStages;
     uint64_t* sg_full = st_empty + C::kStages;
-    uint64_t* sg_empty = sg_full + C::kSGroups;
-    uint64_t* op_full = sg_empty + C::kSGroups;
-    uint64_t* op_empty = op_full + kCkPairs;
-    uint64_t* tm_full = op_empty + kCkPairs;
-    uint64_t* tm_empty = tm_full + C::kSlots;
-    uint64_t* sc_full = tm_empty + C::kSlots;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sc_full + C::kSlots);
+    uint64_t* sg_empty = sg_full + kCkSGroups;
+    uint64_t* a_full = sg_empty + kCkSGroups;
+    uint64_t* a_empty = a_full + C::kQuads;
+    uint64_t* tm_full = a_empty + C::kQuads;
+    uint64_t* tm_empty = tm_full + C::kSlots;          // per slot group
+    uint64_t* sc_full = tm_empty + C::kSG;             // per stage of scale entries
+    uint64_t* sc_empty = sc_full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sc_empty + 2);
+    __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t t0 = int64_t(blockIdx.x) * TT;
@@ -216,33 +311,32 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
     const int g_end = min(total_groups, g_begin + p.groups_per_split);
     const int nblk = g_end > g_begin ? (g_end - g_begin) * kCkGroup : 0;
     const int nst = nblk / 4;
-    const int npairs = nblk / 2;
     const int st0 = g_begin * (kCkGroup / 4);   // first TMA stage (global)
-    const int64_t trows = p.T - t0 < TT ? p.T - t0 : TT;
-    const int np = int((trows + 15) / 16) * 16;   // MMA N
 
     if (tid == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&st_full[i], 1);
-            mbar_init(&st_empty[i], 8);    // each converter warp, once per pair (2 a stage)
+            mbar_init(&st_empty[i], C::kConv);
         }
-        for (int i = 0; i < C::kSGroups; ++i) {
+        for (int i = 0; i < kCkSGroups; ++i) {
             mbar_init(&sg_full[i], 1);
-            mbar_init(&sg_empty[i], 16);   // each converter warp, once per pair (4 a group)
+            mbar_init(&sg_empty[i], C::kWConv);
         }
-        for (int i = 0; i < kCkPairs; ++i) {
-            mbar_init(&op_full[i], 4);
-            mbar_init(&op_empty[i], 1);
+        for (int i = 0; i < C::kQuads; ++i) {
+            mbar_init(&a_full[i], C::kConv);
+            mbar_init(&a_empty[i], 1);
         }
-        for (int i = 0; i < C::kSlots; ++i) {
-            mbar_init(&tm_full[i], 1);
-            mbar_init(&tm_empty[i], kCkEpiWarps);
-            mbar_init(&sc_full[i], 4);
+        for (int i = 0; i < C::kSlots; ++i) mbar_init(&tm_full[i], 1);
+        // each block of a group is released by the 4 * kEC warps that read it
+        for (int i = 0; i < C::kSG; ++i) mbar_init(&tm_empty[i], C::kGS * 4 * C::kEC);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sc_full[i], C::kConv);
+            mbar_init(&sc_empty[i], 4 * 4 * C::kEC);
         }
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -251,290 +345,412 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     pdl_launch_dependents();
     const uint32_t stages_a = smem_u32(stages), sgroups_a = smem_u32(sgroups);
-    const uint32_t ops_a = smem_u32(ops), scl_a = smem_u32(scl);
+    const uint32_t bquads_a = smem_u32(bquads), scl_a = smem_u32(scl);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            pdl_wait();
-            int issued = 0, sissued = 0;
-            for (int s = 0; s < nst; ++s) {
+            const uint32_t stage_tx = uint32_t(C::kW + C::kX + (DEBUG ? 0 : C::kXD));
+            const int npre = nst < C::kStages ? nst : C::kStages;
+            const int ngroups = nst / 2;
+            const int gpre = DEBUG ? 0 : (ngroups < kCkSGroups ? ngroups : kCkSGroups);
+            auto weights = [&](int s) {
                 const int slot = s % C::kStages;
-                if (s >= C::kStages &&
-                    !mbar_wait(&st_empty[slot], uint32_t(s / C::kStages - 1) & 1u, p.err))
-                    break;
-                unsigned char* st = stages + size_t(slot) * C::kStage;
+                mbar_arrive_expect_tx(&st_full[slot], stage_tx);
+                tma2d(stages + size_t(slot) * C::kStage, &tm_w, (st0 + s) * kCkStageK, int(m0), &st_full[slot]);
+            };
+            auto acts = [&](int s) {
+                unsigned char* st = stages + size_t(s % C::kStages) * C::kStage;
                 const int kx = (st0 + s) * kCkStageK;   // byte (= element) of K
-                mbar_arrive_expect_tx(&st_full[slot], uint32_t(C::kW + C::kX + (DEBUG ? 0 : C::kXD)));
-                tma2d(st, &tm_w, kx, int(m0), &st_full[slot]);
-                tma2d(st + C::kW, &tm_xh, kx, int(t0), &st_full[slot]);
-                if constexpr (MODE == 2)
-                    tma2d(st + C::kW + C::kXPlane, &tm_xl, kx, int(t0), &st_full[slot]);
-                if constexpr (!DEBUG)
-                    tma2d(st + C::kW + C::kX, &tm_xd, kx / Q8_QK, int(t0), &st_full[slot]);
+                uint64_t* bar = &st_full[s % C::kStages];
+                tma2d(st + C::kW, &tm_xh, kx, int(t0), bar);
+                if constexpr (MODE == 2) tma2d(st + C::kW + C::kXPlane, &tm_xl, kx, int(t0), bar);
+                if constexpr (!DEBUG) tma2d(st + C::kW + C::kX, &tm_xd, kx / Q8_QK, int(t0), bar);
+            };
+            auto scales = [&](int g) {
+                const int gs = g % kCkSGroups;
+                mbar_arrive_expect_tx(&sg_full[gs], uint32_t(C::kSGroup));
+                tma2d(sgroups + size_t(gs) * C::kSGroup, &tm_s, (st0 + 2 * g) * kCkStageK / Q8_QK, int(m0),
+                      &sg_full[gs]);
+            };
+            // weights and their scales first: they never depend on the
+            // previous kernel on the stream
+            for (int s = 0; s < npre; ++s) weights(s);
+            for (int g = 0; g < gpre; ++g) scales(g);
+            pdl_wait();
+            for (int s = 0; s < npre; ++s) acts(s);
+            int issued = npre, sissued = gpre;
+            for (int s = npre; s < nst; ++s) {
+                const int slot = s % C::kStages;
+                if (!mbar_wait_fast(&st_empty[slot], uint32_t(s / C::kStages - 1) & 1u, p.err)) break;
+                weights(s);
+                acts(s);
                 ++issued;
-                if (!DEBUG && (s & 1) == 0) {
-                    const int g = s >> 1, gs = g % C::kSGroups;
-                    if (g >= C::kSGroups &&
-                        !mbar_wait(&sg_empty[gs], uint32_t(g / C::kSGroups - 1) & 1u, p.err))
-                        break;
-                    mbar_arrive_expect_tx(&sg_full[gs], uint32_t(C::kSGroup));
-                    tma2d(sgroups + size_t(gs) * C::kSGroup, &tm_s, kx / Q8_QK, int(m0), &sg_full[gs]);
+                if (!DEBUG && (s & 1) == 0 && s / 2 >= gpre) {
+                    const int g = s >> 1;
+                    if (!mbar_wait_fast(&sg_empty[g % kCkSGroups], uint32_t(g / kCkSGroups - 1) & 1u, p.err)) break;
+                    scales(g);
                     ++sissued;
                 }
             }
             // never leave with copies in flight into this CTA's shared memory
             for (int s = issued > C::kStages ? issued - C::kStages : 0; s < issued; ++s)
-                mbar_wait(&st_full[s % C::kStages], uint32_t(s / C::kStages) & 1u, p.err);
-            for (int g = sissued > C::kSGroups ? sissued - C::kSGroups : 0; g < sissued; ++g)
-                mbar_wait(&sg_full[g % C::kSGroups], uint32_t(g / C::kSGroups) & 1u, p.err);
+                mbar_wait_fast(&st_full[s % C::kStages], uint32_t(s / C::kStages) & 1u, p.err);
+            for (int g = sissued > kCkSGroups ? sissued - kCkSGroups : 0; g < sissued; ++g)
+                mbar_wait_fast(&sg_full[g % kCkSGroups], uint32_t(g / kCkSGroups) & 1u, p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(kCkM, np);
+            const uint32_t idesc = idesc_f16_f32(kCkM, C::kN);
             int issued = 0;
             bool ok = true;
-            for (int pr = 0; pr < npairs && ok; ++pr) {
-                const int ps = pr % kCkPairs;
-                if (!mbar_wait(&op_full[ps], uint32_t(pr / kCkPairs) & 1u, p.err)) break;
+            for (int s = 0; s < nst && ok; ++s) {
+                const int qs = s % C::kQuads;
+                if (!mbar_wait_fast(&a_full[qs], uint32_t(s / C::kQuads) & 1u, p.err)) break;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int b = 2 * pr + h, ts = b % C::kSlots;
-                    if (b >= C::kSlots &&
-                        !mbar_wait(&tm_empty[ts], uint32_t(b / C::kSlots - 1) & 1u, p.err)) {
+                for (int j = 0; j < 4; ++j) {
+                    const int b = 4 * s + j, ts = b % C::kSlots;
+                    if (b >= C::kSlots && b % C::kGS == 0 &&
+                        !mbar_wait_fast(&tm_empty[(b / C::kGS) % C::kSG], uint32_t(b / C::kSlots - 1) & 1u, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a = tmem + uint32_t(kCkAccCols + 32 * ps + 16 * h);
-                    const uint32_t bb = ops_a + uint32_t(ps * C::kOpPair + h * C::kBBlock);
-                    const uint32_t d = tmem + uint32_t(ts * C::kSlotCols);
-#pragma unroll
-                    for (int pl = 0; pl < C::kPlanes; ++pl)
-#pragma unroll
-                        for (int s2 = 0; s2 < 2; ++s2)
-                            mma_f16_ts(d + uint32_t(pl * TT), a + uint32_t(8 * s2),
-                                       smem_desc_kmajor(bb + uint32_t(pl * C::kBPlane + 256 * s2), 128, 512),
-                                       idesc, s2 > 0);
+                    const uint32_t a = tmem + uint32_t(C::kAccCols + kCkACols * qs + 16 * j);
+                    const uint32_t bb = bquads_a + uint32_t(qs * C::kBQuad + j * C::kBBlock);
+                    const uint32_t d = tmem + uint32_t(ts * C::kN);
+                    mma_f16_ts(d, a, smem_desc_kmajor(bb, 128, 512), idesc, false);
+                    mma_f16_ts(d, a + 8u, smem_desc_kmajor(bb + 256u, 128, 512), idesc, true);
                     mma_commit(smem_u32(&tm_full[ts]));
                     ++issued;
                 }
-                mma_commit(smem_u32(&op_empty[ps]));
+                if (ok) mma_commit(smem_u32(&a_empty[qs]));
             }
             // nothing may be left in flight when TMEM is released (the epilogue
             // normally drains every block; this covers an early exit)
             if (issued > 0)
-                mbar_wait(&tm_full[(issued - 1) % C::kSlots], uint32_t((issued - 1) / C::kSlots) & 1u,
+                mbar_wait_fast(&tm_full[(issued - 1) % C::kSlots], uint32_t((issued - 1) / C::kSlots) & 1u,
                           p.err);
         }
     } else if (warp < C::kEpiWarp0) {
         // ------------------------------------------------------------ converters
-        // group cg converts the pairs pr = cg (mod kConvGroups)
-        const int cg = (warp - 2) >> 2;
-        const int rw = (warp & 3) * 32 + lane;        // weight row = TMEM lane; activation row
-        const uint32_t a_lane = uint32_t((warp & 3) * 32) << 16;
-        const bool act = rw < np;                     // the MMA reads activation rows < np only
+        // warps 2 .. 2+kWConv-1: the weights of one TMEM lane quadrant each
+        // (all four blocks of a stage, or with two warps a quadrant, half of
+        // them) and their scales; the next two warps the activation codes and
+        // their scales, one (row, block) pair a lane and pass, rows first
+        // (consecutive lanes take consecutive rows of one block, so the
+        // swizzled loads and the operand stores stay free of bank
+        // conflicts).  Both sets follow the same stages in step.
+        const bool wconv = warp < 2 + C::kWConv;
+        const int qd = warp & 3;                      // TMEM lane quadrant
+        const int rw = qd * 32 + lane;                // weight row = TMEM lane
+        const uint32_t a_lane = uint32_t(qd * 32) << 16;
+        constexpr int kHalves = C::kWConv == 8 ? 1 : 2;   // 32-column halves a weight warp converts
+        const int h0 = C::kWConv == 8 ? (warp - 2) / 4 : 0;
+        const int aw = warp - 2 - C::kWConv;               // activation warp 0 or 1
+        constexpr int kAPasses = (TT * 4 + 63) / 64;      // (row, block) pairs a lane (TT <= 32)
         bool ok = true;
-        for (int pr = cg; pr < npairs; pr += C::kConvGroups) {
-            const int s = pr >> 1, half = pr & 1, slot = s % C::kStages;
-            const int g = pr >> 2, gs = g % C::kSGroups, ps = pr % kCkPairs;
-            const int b0 = 2 * pr, j0 = 2 * half;
-            if (ok) ok = mbar_wait(&st_full[slot], uint32_t(s / C::kStages) & 1u, p.err);
-            if (!DEBUG && ok) ok = mbar_wait(&sg_full[gs], uint32_t(g / C::kSGroups) & 1u, p.err);
-            if (ok && pr >= kCkPairs)
-                ok = mbar_wait(&op_empty[ps], uint32_t(pr / kCkPairs - 1) & 1u, p.err);
-            // the scale-ring entries of both blocks are free once the epilogue
-            // has released the later one's previous user (it releases in order)
-            if (!DEBUG && ok && b0 + 1 >= C::kSlots)
-                ok = mbar_wait(&tm_empty[(b0 + 1) % C::kSlots], uint32_t((b0 + 1) / C::kSlots - 1) & 1u,
-                               p.err);
-            // leave together: the warp-wide TMEM store and __syncwarp below need every lane
+        for (int s = 0; s < nst; ++s) {
+            const int slot = s % C::kStages, qs = s % C::kQuads;
+            const int g = s >> 1, gs = g % kCkSGroups;
+            if (ok) ok = mbar_wait_fast(&st_full[slot], uint32_t(s / C::kStages) & 1u, p.err);
+            if (!DEBUG && wconv && ok && (s & 1) == 0)
+                ok = mbar_wait_fast(&sg_full[gs], uint32_t(g / kCkSGroups) & 1u, p.err);
+            if (ok && s >= C::kQuads) ok = mbar_wait_fast(&a_empty[qs], uint32_t(s / C::kQuads - 1) & 1u, p.err);
+            // the stage's scale entries are free once the epilogue has read
+            // the scales of the stage two back
+            if (!DEBUG && ok && s >= 2) ok = mbar_wait_fast(&sc_empty[s & 1], uint32_t(s / 2 - 1) & 1u, p.err);
+            // leave together: the warp-wide TMEM stores below need every lane
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            tc_fence_after();
             const uint32_t st = stages_a + uint32_t(slot * C::kStage);
-            // every shared-memory read first, then convert and store
-            int4 w[4], x[4], l[4];
+            if (wconv) {
+                tc_fence_after();
+                // weights of two blocks (32 TMEM columns) a half
 #pragma unroll
-            for (int c = 0; c < 4; ++c) w[c] = lds128(st + sw128(rw, 2 * j0 + c));
-            if (act) {
+                for (int hh = 0; hh < kHalves; ++hh) {
+                    const int h = h0 + hh;
+                    int4 w[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    x[c] = lds128(st + C::kW + sw128(rw, 2 * j0 + c));
-                    if constexpr (MODE == 2) l[c] = lds128(st + C::kW + C::kXPlane + sw128(rw, 2 * j0 + c));
+                    for (int c = 0; c < 4; ++c) w[c] = lds128(st + sw128(rw, 4 * h + c));
+                    uint32_t hw[32];
+                    weights_f16(w, hw);
+                    tmem_st32(tmem + a_lane + uint32_t(C::kAccCols + kCkACols * qs + 32 * h), hw);
                 }
-            }
-            uint32_t sw2 = 0, xd0 = 0, xd1 = 0;
-            if constexpr (!DEBUG) {
-                sw2 = lds32(sgroups_a + uint32_t(gs * C::kSGroup + rw * kCkGroup * 2 + (b0 & 7) * 2));
-                if (act) {
-                    xd0 = lds32(st + uint32_t(C::kW + C::kX + rw * 16 + j0 * 4));
-                    xd1 = lds32(st + uint32_t(C::kW + C::kX + rw * 16 + j0 * 4 + 4));
-                }
-            }
-            // weights of both blocks -> 32 TMEM columns of A pair `ps`
-            {
-                uint32_t hw[32];
+                if constexpr (!DEBUG) {
+                    // this row's weight scales of those blocks (its 16-byte group row)
+                    const uint32_t sgr = sgroups_a + uint32_t(gs * C::kSGroup + rw * kCkGroup * 2 + (s & 1) * 8);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t v[4] = {uint32_t(w[c].x), uint32_t(w[c].y), uint32_t(w[c].z),
-                                           uint32_t(w[c].w)};
+                    for (int hh = 0; hh < kHalves; ++hh) {
+                        const int h = h0 + hh;
+                        const uint32_t sw2 = lds32(sgr + uint32_t(4 * h));
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) i8x4_to_f16x4(v[i], hw[8 * c + 2 * i], hw[8 * c + 2 * i + 1]);
+                        for (int jj = 0; jj < 2; ++jj)
+                            sts16(scl_a + uint32_t(((4 * s + 2 * h + jj) % C::kSE) * C::kScl + 2 * rw),
+                                  uint16_t(jj ? (sw2 >> 16) : (sw2 & 0xFFFFu)));
+                    }
                 }
-                tmem_st32(tmem + a_lane + uint32_t(kCkAccCols + 32 * ps), hw);
-            }
-            if (act) {
-                const uint32_t bb = ops_a + uint32_t(ps * C::kOpPair);
-                store_row_f16(bb, rw, x[0], x[1]);
-                store_row_f16(bb + C::kBBlock, rw, x[2], x[3]);
-                if constexpr (MODE == 2) {
-                    store_row_f16(bb + C::kBPlane, rw, l[0], l[1]);
-                    store_row_f16(bb + C::kBBlock + C::kBPlane, rw, l[2], l[3]);
+                tmem_wait_st();
+                tc_fence_before();
+            } else {
+                if constexpr (TT <= 32) {
+                    // exactly 4 * TT (row, block) pairs: two warps of 32 lanes,
+                    // kAPasses passes, rows first within a block
+                    static_assert(TT * 4 == kAPasses * 64, "activation pairs");
+#pragma unroll
+                    for (int pass = 0; pass < kAPasses; ++pass) {
+                        const int item = (2 * pass + aw) * 32 + lane;   // j * TT + ra
+                        const int ra = item % TT, j = item / TT;
+                        const uint32_t bq = bquads_a + uint32_t(qs * C::kBQuad + j * C::kBBlock);
+#pragma unroll
+                        for (int pl = 0; pl < C::kPlanes; ++pl) {
+                            const uint32_t xs = st + uint32_t(C::kW + pl * C::kXPlane);
+                            const int4 x0 = lds128(xs + sw128(ra, 2 * j));
+                            const int4 x1 = lds128(xs + sw128(ra, 2 * j + 1));
+                            store_row_f16(bq, pl * TT + ra, x0, x1);
+                        }
+                        if constexpr (!DEBUG)
+                            sts32(scl_a + uint32_t(((4 * s + j) % C::kSE) * C::kScl + kCkM * 2 + 4 * ra),
+                                  lds32(st + uint32_t(C::kW + C::kX + ra * 16 + j * 4)));
+                    }
+                } else {
+                    // one row a lane, its four blocks (the row's 128 bytes
+                    // loaded at once), rows in groups of 8 consecutive rows,
+                    // group g to warp g % 2, 64 rows a pass
+#pragma unroll
+                    for (int pass = 0; pass < TT / 64; ++pass) {
+                        const int ra = 8 * (2 * (4 * pass + (lane >> 3)) + aw) + (lane & 7);
+                        const uint32_t bq = bquads_a + uint32_t(qs * C::kBQuad);
+#pragma unroll
+                        for (int pl = 0; pl < C::kPlanes; ++pl) {
+                            const uint32_t xs = st + uint32_t(C::kW + pl * C::kXPlane);
+                            int4 x[8];
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) x[c] = lds128(xs + sw128(ra, c));
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                store_row_f16(bq + uint32_t(j * C::kBBlock), pl * TT + ra, x[2 * j], x[2 * j + 1]);
+                        }
+                        if constexpr (!DEBUG) {
+                            const int4 xd4 = lds128(st + uint32_t(C::kW + C::kX + ra * 16));
+                            const uint32_t xdv[4] = {uint32_t(xd4.x), uint32_t(xd4.y), uint32_t(xd4.z),
+                                                     uint32_t(xd4.w)};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                sts32(scl_a + uint32_t(((4 * s + j) % C::kSE) * C::kScl + kCkM * 2 + 4 * ra),
+                                      xdv[j]);
+                        }
+                    }
                 }
+                fence_proxy_async_smem();   // the B operand is read by the tensor core
             }
-            if constexpr (!DEBUG) {
-                const uint32_t e0 = scl_a + uint32_t((b0 % C::kSlots) * C::kScl);
-                const uint32_t e1 = scl_a + uint32_t(((b0 + 1) % C::kSlots) * C::kScl);
-                sts16(e0 + uint32_t(2 * rw), uint16_t(sw2 & 0xFFFFu));
-                sts16(e1 + uint32_t(2 * rw), uint16_t(sw2 >> 16));
-                if (act) {
-                    sts32(e0 + uint32_t(kCkM * 2 + 4 * rw), xd0);
-                    sts32(e1 + uint32_t(kCkM * 2 + 4 * rw), xd1);
-                }
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&op_full[ps]);
+                mbar_arrive(&a_full[qs]);
                 if constexpr (!DEBUG) {
-                    mbar_arrive(&sc_full[b0 % C::kSlots]);
-                    mbar_arrive(&sc_full[(b0 + 1) % C::kSlots]);
+                    mbar_arrive(&sc_full[s & 1]);
+                    if (wconv && (s & 1)) mbar_arrive(&sg_empty[gs]);
                 }
                 mbar_arrive(&st_empty[slot]);
-                if constexpr (!DEBUG) mbar_arrive(&sg_empty[gs]);
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // accumulators: pairs of activation rows for one weight row
-        uint64_t acc[C::kCW / 2];
+        pdl_wait();   // outputs and arg-max keys belong to the previous kernel until here
+        constexpr int CW = C::kCW;
+        const int ew = warp - C::kEpiWarp0;           // 0..15
+        const int qd = warp & 3;                      // TMEM lane quadrant of this warp
+        const int ec = (ew >> 2) % C::kEC;            // column slice
+        const int eg = (ew >> 2) / C::kEC;            // block group
+        const int n = qd * 32 + lane;                 // weight row within the tile
+        const int c0 = ec * CW;
+        uint64_t acc[CW / 2];
 #pragma unroll
-        for (int i = 0; i < C::kCW / 2; ++i) acc[i] = 0;
-        const int ew = warp - C::kEpiWarp0;   // 0..7
-        const int q = warp & 3;           // TMEM lane quadrant of this warp
-        const int h = ew >> 2;            // column half
-        const int n = q * 32 + lane;      // weight row within the tile
-        const int c0 = C::kCW * h;
+        for (int i = 0; i < CW / 2; ++i) acc[i] = 0;
         bool ok = true;
-        for (int b = 0; b < nblk; ++b) {
-            const int ts = b % C::kSlots;
+        for (int b = eg; b < nblk; b += C::kEG) {
+            const int ts = b % C::kSlots, se = b % C::kSE;
             const uint32_t par = uint32_t(b / C::kSlots) & 1u;
-            if (!DEBUG && ok) ok = mbar_wait(&sc_full[ts], par, p.err);
-            if (ok) ok = mbar_wait(&tm_full[ts], par, p.err);
+            if (!DEBUG && ok) ok = mbar_wait_fast(&sc_full[(b >> 2) & 1], uint32_t(b >> 3) & 1u, p.err);
+            if (ok) ok = mbar_wait_fast(&tm_full[ts], par, p.err);
             ok = __all_sync(0xffffffffu, ok);   // the TMEM loads below are warp-wide
             if (!ok) break;
             tc_fence_after();
-            const uint32_t d = tmem + (uint32_t(q * 32) << 16) + uint32_t(ts * C::kSlotCols + c0);
+            const uint32_t d = tmem + (uint32_t(qd * 32) << 16) + uint32_t(ts * C::kN + c0);
+            float v[CW];
+            float vl[MODE == 2 ? CW : 1];
+#pragma unroll
+            for (int c = 0; c < CW / 16; ++c) {
+                tmem_ld16(d + uint32_t(16 * c), v + 16 * c);
+                if constexpr (MODE == 2) tmem_ld16(d + uint32_t(TT + 16 * c), vl + 16 * c);
+            }
+            // the block's weight scale while the accumulator is on its way
+            const uint32_t e = scl_a + uint32_t(se * C::kScl);
+            const float sw = DEBUG ? 0.0f : half_bits_to_float(lds16(e + uint32_t(2 * n)));
+            tmem_wait_ld();
+            // the data is in registers: the slot goes back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tm_empty[(b / C::kGS) % C::kSG]);
             if constexpr (DEBUG) {
                 // the plane sums are exact integers below 2^24
                 const int64_t row = m0 + n;
 #pragma unroll
-                for (int cc = 0; cc < C::kCW / 16; ++cc) {
-                    if (c0 + 16 * cc >= np) break;
-                    float v[16], vl[16];
-                    tmem_ld16(d + uint32_t(16 * cc), v);
-                    if constexpr (MODE == 2) tmem_ld16(d + TT + uint32_t(16 * cc), vl);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int64_t t = t0 + c0 + 16 * cc + i;
-                        if (t < p.T && row < p.N) {
-                            int iv = __float2int_rn(v[i]);
-                            if constexpr (MODE == 2) iv = 128 * iv + __float2int_rn(vl[i]);
-                            p.isum[(t * p.N + row) * (p.K / Q8_QK) + g_begin * kCkGroup + b] = iv;
-                        }
+                for (int i = 0; i < CW; ++i) {
+                    const int64_t t = t0 + c0 + i;
+                    if (t < p.T && row < p.N) {
+                        int iv = __float2int_rn(v[i]);
+                        if constexpr (MODE == 2) iv = 128 * iv + __float2int_rn(vl[i]);
+                        p.isum[(t * p.N + row) * (p.K / Q8_QK) + g_begin * kCkGroup + b] = iv;
                     }
                 }
             } else {
-                const uint32_t e = scl_a + uint32_t(ts * C::kScl);
-                const float sw = half_bits_to_float(lds16(e + uint32_t(2 * n)));
+                if constexpr (MODE == 2) {
+                    // 128*hi + lo rounds once: exactly float(isum)
+                    const uint64_t k128 = f2_pack(128.0f, 128.0f);
+#pragma unroll
+                    for (int i = 0; i < CW / 2; ++i) {
+                        const uint64_t r = f2_fma(k128, f2_pack(v[2 * i], v[2 * i + 1]),
+                                                  f2_pack(vl[2 * i], vl[2 * i + 1]));
+                        v[2 * i] = f2_lo(r);
+                        v[2 * i + 1] = f2_hi(r);
+                    }
+                }
                 const uint64_t sw2 = f2_pack(sw, sw);
-                const uint32_t xdv = e + uint32_t(kCkM * 2 + c0 * 4);
-                // waves of up to 32 columns: all TMEM loads of a wave, one wait
-                // registers: two planes or 64 accumulated columns take half-width waves
-                constexpr int kWaveMax = (MODE == 2 || C::kCW > 32) ? 16 : 32;
-                constexpr int kWave = C::kCW < kWaveMax ? C::kCW : kWaveMax;
 #pragma unroll
-                for (int w = 0; w < C::kCW / kWave; ++w) {
-                    if (c0 + kWave * w >= np) break;   // warp-uniform
-                    float v[kWave];
-                    float vl[MODE == 2 ? kWave : 1];
+                for (int i4 = 0; i4 < CW / 4; ++i4) {
+                    const int4 x4 = lds128(e + uint32_t(kCkM * 2 + c0 * 4 + 16 * i4));
+                    const uint64_t c01 = f2_mul(sw2, uint64_t(uint32_t(x4.x)) | (uint64_t(uint32_t(x4.y)) << 32));
+                    const uint64_t c23 = f2_mul(sw2, uint64_t(uint32_t(x4.z)) | (uint64_t(uint32_t(x4.w)) << 32));
+                    acc[2 * i4] = f2_fma(f2_pack(v[4 * i4], v[4 * i4 + 1]), c01, acc[2 * i4]);
+                    acc[2 * i4 + 1] = f2_fma(f2_pack(v[4 * i4 + 2], v[4 * i4 + 3]), c23, acc[2 * i4 + 1]);
+                }
+                // the block's scales are read: its scale entry goes back
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sc_empty[(b >> 2) & 1]);
+            }
+        }
+        if constexpr (!DEBUG) {
+            constexpr int kEpiThreads = 32 * C::kEpiWarps;
+            // every block is consumed once all epilogue warps get here, so the
+            // stage area is free for the end-of-tile scratch
+            named_bar(1, kEpiThreads);
+            if constexpr (C::kEG > 1) {
+                if (eg > 0) {
 #pragma unroll
-                    for (int c = 0; c < kWave / 16; ++c) {
-                        tmem_ld16(d + uint32_t(kWave * w + 16 * c), *reinterpret_cast<float(*)[16]>(v + 16 * c));
-                        if constexpr (MODE == 2)
-                            tmem_ld16(d + TT + uint32_t(kWave * w + 16 * c),
-                                      *reinterpret_cast<float(*)[16]>(vl + 16 * c));
-                    }
-                    tmem_wait_ld();
-                    if constexpr (MODE == 2) {
-                        // 128*hi + lo rounds once: exactly float(isum)
-                        const uint64_t k128 = f2_pack(128.0f, 128.0f);
+                    for (int i = 0; i < CW; ++i)
+                        sts32(stages_a + uint32_t(((eg - 1) * C::kPartial) + ((c0 + i) * kCkM + n) * 4),
+                              (i & 1) ? uint32_t(acc[i >> 1] >> 32) : uint32_t(acc[i >> 1]));
+                }
+                named_bar(1, kEpiThreads);
+                if (eg == 0) {
+                    // the groups' partial sums in group order
+                    for (int g2 = 1; g2 < C::kEG; ++g2) {
 #pragma unroll
-                        for (int i = 0; i < kWave / 2; ++i) {
-                            const uint64_t r = f2_fma(k128, f2_pack(v[2 * i], v[2 * i + 1]),
-                                                      f2_pack(vl[2 * i], vl[2 * i + 1]));
-                            v[2 * i] = f2_lo(r);
-                            v[2 * i + 1] = f2_hi(r);
+                        for (int i = 0; i < CW / 2; ++i) {
+                            const uint32_t a0 = stages_a + uint32_t((g2 - 1) * C::kPartial + ((c0 + 2 * i) * kCkM + n) * 4);
+                            const uint64_t o = uint64_t(lds32(a0)) | (uint64_t(lds32(a0 + kCkM * 4)) << 32);
+                            acc[i] = f2_add(acc[i], o);
                         }
-                    }
-#pragma unroll
-                    for (int i4 = 0; i4 < kWave / 4; ++i4) {
-                        const int4 x4 = lds128(xdv + uint32_t(4 * kWave * w + 16 * i4));
-                        const uint64_t c01 = f2_mul(sw2, uint64_t(uint32_t(x4.x)) | (uint64_t(uint32_t(x4.y)) << 32));
-                        const uint64_t c23 = f2_mul(sw2, uint64_t(uint32_t(x4.z)) | (uint64_t(uint32_t(x4.w)) << 32));
-                        const int a = (kWave * w) / 2 + 2 * i4;
-                        acc[a] = f2_fma(f2_pack(v[4 * i4], v[4 * i4 + 1]), c01, acc[a]);
-                        acc[a + 1] = f2_fma(f2_pack(v[4 * i4 + 2], v[4 * i4 + 3]), c23, acc[a + 1]);
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tm_empty[ts]);
-        }
-        if constexpr (!DEBUG) {
-            if (gridDim.z == 1) {
+            if (eg == 0) {
                 const int64_t row = m0 + n;
-                if (row < p.N) {
+                if (gridDim.z == 1) {
+                    if (p.y && row < p.N) {
 #pragma unroll
-                    for (int i = 0; i < C::kCW; ++i) {
-                        const int64_t t = t0 + c0 + i;
-                        const float v = (i & 1) ? f2_hi(acc[i >> 1]) : f2_lo(acc[i >> 1]);
-                        if (t < p.T) p.y[t * p.N + row] = v;
+                        for (int i = 0; i < CW; ++i) {
+                            const int64_t t = t0 + c0 + i;
+                            const float v = (i & 1) ? f2_hi(acc[i >> 1]) : f2_lo(acc[i >> 1]);
+                            if (t < p.T) p.y[t * p.N + row] = v;
+                        }
+                    }
+                } else {
+                    // the CTA's partial tile [TT][128] f32 for the cluster sum
+#pragma unroll
+                    for (int i = 0; i < CW; ++i)
+                        sts32(stages_a + uint32_t(((c0 + i) * kCkM + n) * 4),
+                              (i & 1) ? uint32_t(acc[i >> 1] >> 32) : uint32_t(acc[i >> 1]));
+                }
+                if constexpr (ARGMAX) {
+                    // per activation row: the best (value, lowest row) of this
+                    // warp's 32 weight rows, then of the four quadrants
+                    const uint32_t cand = stages_a + uint32_t(C::kCandOff);
+#pragma unroll
+                    for (int i = 0; i < CW; ++i) {
+                        float v = (i & 1) ? f2_hi(acc[i >> 1]) : f2_lo(acc[i >> 1]);
+                        unsigned ni = unsigned(row);
+                        const bool valid = row < p.N && !(v != v);
+                        if (!valid) {
+                            v = -INFINITY;
+                            ni = 0xffffffffu;
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+                            const unsigned on = __shfl_xor_sync(0xffffffffu, ni, o);
+                            if (ov > v || (ov == v && on < ni)) {
+                                v = ov;
+                                ni = on;
+                            }
+                        }
+                        if (lane == 0) {
+                            sts32(cand + uint32_t((qd * TT + c0 + i) * 8), __float_as_uint(v));
+                            sts32(cand + uint32_t((qd * TT + c0 + i) * 8 + 4), ni);
+                        }
                     }
                 }
-            } else {
-                // partial tile [TT][128] f32 in the stage buffers: every stage has
-                // been consumed once this warp has rescaled the last block
-#pragma unroll
-                for (int i = 0; i < C::kCW; ++i)
-                    sts32(stages_a + uint32_t(((c0 + i) * kCkM + n) * 4),
-                          (i & 1) ? uint32_t(acc[i >> 1] >> 32) : uint32_t(acc[i >> 1]));
+            }
+            if constexpr (ARGMAX) {
+                constexpr int kG0 = 32 * 4 * C::kEC;   // threads of group 0
+                if (eg == 0) {
+                    named_bar(2, kG0);
+                    const int j = (ec * 4 + ((warp - C::kEpiWarp0) & 3)) * 32 + lane;   // 0..kG0-1
+                    const uint32_t cand = stages_a + uint32_t(C::kCandOff);
+                    for (int col = j; col < TT; col += kG0) {
+                        float bv = -INFINITY;
+                        unsigned bn = 0xffffffffu;
+                        for (int q2 = 0; q2 < 4; ++q2) {   // quadrants in row order
+                            const float ov = __uint_as_float(lds32(cand + uint32_t((q2 * TT + col) * 8)));
+                            const unsigned on = lds32(cand + uint32_t((q2 * TT + col) * 8 + 4));
+                            if (ov > bv || (ov == bv && on < bn)) {
+                                bv = ov;
+                                bn = on;
+                            }
+                        }
+                        const int64_t t = t0 + col;
+                        if (t < p.T && bn != 0xffffffffu) atomicMax(p.keys + t, argmax_key(bv, bn));
+                    }
+                    __threadfence();
+                    named_bar(2, kG0);
+                    if (j == 0) s_last = atomicAdd(p.ticket, 1u) == gridDim.x * gridDim.y - 1u;
+                    named_bar(2, kG0);
+                    if (s_last) {
+                        // the last CTA: every row's token, and the keys and the
+                        // ticket cleared for the next call
+                        __threadfence();
+                        for (int64_t t = j; t < p.T; t += kG0) {
+                            const unsigned long long key = atomicExch(p.keys + t, 0ull);
+                            int32_t tk;
+                            double val;
+                            argmax_unkey(key, tk, val);
+                            p.tok[t] = tk;
+                            if (p.maxval) p.maxval[t] = val;
+                        }
+                        if (j == 0) *p.ticket = 0u;
+                    }
+                }
             }
         }
     }
-
 
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, C::kTmemCols);
+        tmem_dealloc(tmem, 512);
     }
     if (!DEBUG && gridDim.z > 1) {
         cluster_sync();
@@ -574,16 +790,19 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_acquire);
+    if (!f) {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<EncodeTiledFn>(p);
+            fn.store(f, std::memory_order_release);
+        }
     }
-    return fn;
+    return f;
 }
 
 static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
@@ -600,7 +819,7 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, u
 }
 
 // Clusters of `ks` CTAs of this kernel that fit on the device at once.
-template <int MODE, int TT, bool DEBUG>
+template <int MODE, int TT, int KIND>
 static int active_clusters(int ks, const LaunchCtx& ctx) {
     using C = CkCfg<MODE, TT>;
     // per device and split; threads that race here store the same value
@@ -621,7 +840,7 @@ static int active_clusters(int ks, const LaunchCtx& ctx) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, chunk_kernel<MODE, TT, DEBUG>, &cfg) == cudaSuccess &&
+        if (cudaOccupancyMaxActiveClusters(&c, chunk_kernel<MODE, TT, KIND>, &cfg) == cudaSuccess &&
             c > 0)
             n = c;
         else
@@ -634,13 +853,13 @@ static int active_clusters(int ks, const LaunchCtx& ctx) {
 
 // Split of K over a cluster: the count with the fewest 8-block groups on
 // the busiest SM, counting whole waves of clusters.
-template <int MODE, int TT, bool DEBUG>
+template <int MODE, int TT, int KIND>
 static int choose_split(int64_t tiles, int groups, const LaunchCtx& ctx) {
     int best = 1;
     int64_t best_cost = -1;
     for (int ks = 1; ks <= kCkMaxSplit && ks <= groups; ++ks) {
-        const int64_t waves = (tiles + active_clusters<MODE, TT, DEBUG>(ks, ctx) - 1) /
-                              active_clusters<MODE, TT, DEBUG>(ks, ctx);
+        const int ac = active_clusters<MODE, TT, KIND>(ks, ctx);
+        const int64_t waves = (tiles + ac - 1) / ac;
         const int64_t cost = waves * ((groups + ks - 1) / ks);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
@@ -650,12 +869,22 @@ static int choose_split(int64_t tiles, int groups, const LaunchCtx& ctx) {
     return best;
 }
 
-template <int MODE, int TT, bool DEBUG>
+struct ChunkOut {
+    float* y = nullptr;
+    int32_t* isum = nullptr;
+    // arg-max
+    unsigned char* ws = nullptr;
+    int32_t* tok = nullptr;
+    double* maxval = nullptr;
+};
+
+template <int MODE, int TT, int KIND>
 static cudaError_t launch_chunk_t(const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
-                                  const void* xq, const float* xd, int64_t T, float* y,
-                                  int32_t* isum, const LaunchCtx& ctx) {
+                                  const void* xq, const float* xd, int64_t T, const ChunkOut& out,
+                                  const LaunchCtx& ctx) {
     using C = CkCfg<MODE, TT>;
-    auto kern = chunk_kernel<MODE, TT, DEBUG>;
+    constexpr bool DEBUG = KIND == kCkDebug;
+    auto kern = chunk_kernel<MODE, TT, KIND>;
     static std::atomic<bool> configured[kMaxDevices];
     if (const cudaError_t e = set_smem_once(kern, size_t(C::kSmem), ctx.dev, configured); e != cudaSuccess)
         return e;
@@ -675,10 +904,24 @@ static cudaError_t launch_chunk_t(const int8_t* q, const uint16_t* s, int64_t N,
                        DEBUG ? nb / 2 : nb, DEBUG ? N : T, nb * 4, 4, TT, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return cudaErrorInvalidValue;
     const int64_t t_tiles = (T + TT - 1) / TT, n_tiles = (N + kCkM - 1) / kCkM;
+    if (t_tiles > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
     const int groups = int(K / (Q8_QK * kCkGroup));
-    const int ks = DEBUG ? 1 : choose_split<MODE, TT, DEBUG>(t_tiles * n_tiles, groups, ctx);
+    const int ks = KIND != kCkPlain ? 1 : choose_split<MODE, TT, KIND>(t_tiles * n_tiles, groups, ctx);
     const int per = (groups + ks - 1) / ks;
-    CkParams p{N, K, T, per, y, isum, ctx.dev_err};
+    CkParams p{};
+    p.N = N;
+    p.K = K;
+    p.T = T;
+    p.groups_per_split = per;
+    p.y = out.y;
+    p.isum = out.isum;
+    p.err = ctx.dev_err;
+    if (KIND == kCkArgmax) {
+        p.ticket = reinterpret_cast<unsigned int*>(out.ws);
+        p.keys = reinterpret_cast<unsigned long long*>(out.ws + kArgmaxHeader);
+        p.tok = out.tok;
+        p.maxval = out.maxval;
+    }
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attrs[2];
     cfg.gridDim = dim3(unsigned(t_tiles), unsigned(n_tiles), unsigned((groups + per - 1) / per));
@@ -703,28 +946,45 @@ bool chunk_supported(int mode, int64_t N, int64_t K, int64_t T) {
            encode_fn() != nullptr;
 }
 
-template <bool DEBUG>
+template <int KIND>
 static cudaError_t launch_chunk_any(int mode, const int8_t* q, const uint16_t* s, int64_t N,
-                                    int64_t K, const void* xq, const float* xd, int64_t T, float* y,
-                                    int32_t* isum, const LaunchCtx& ctx) {
+                                    int64_t K, const void* xq, const float* xd, int64_t T,
+                                    const ChunkOut& out, const LaunchCtx& ctx) {
     if (mode == 1) {
-        if (T <= 32) return launch_chunk_t<1, 32, DEBUG>(q, s, N, K, xq, xd, T, y, isum, ctx);
-        if (T <= 64) return launch_chunk_t<1, 64, DEBUG>(q, s, N, K, xq, xd, T, y, isum, ctx);
-        return launch_chunk_t<1, 128, DEBUG>(q, s, N, K, xq, xd, T, y, isum, ctx);
+        if (T <= 16) return launch_chunk_t<1, 16, KIND>(q, s, N, K, xq, xd, T, out, ctx);
+        if (T <= 32) return launch_chunk_t<1, 32, KIND>(q, s, N, K, xq, xd, T, out, ctx);
+        if (T <= 64) return launch_chunk_t<1, 64, KIND>(q, s, N, K, xq, xd, T, out, ctx);
+        return launch_chunk_t<1, 128, KIND>(q, s, N, K, xq, xd, T, out, ctx);
     }
-    if (T <= 32) return launch_chunk_t<2, 32, DEBUG>(q, s, N, K, xq, xd, T, y, isum, ctx);
-    return launch_chunk_t<2, 64, DEBUG>(q, s, N, K, xq, xd, T, y, isum, ctx);
+    if (T <= 16) return launch_chunk_t<2, 16, KIND>(q, s, N, K, xq, xd, T, out, ctx);
+    if (T <= 32) return launch_chunk_t<2, 32, KIND>(q, s, N, K, xq, xd, T, out, ctx);
+    return launch_chunk_t<2, 64, KIND>(q, s, N, K, xq, xd, T, out, ctx);
 }
 
 cudaError_t launch_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                          const void* xq, const float* xd, int64_t T, float* y,
                          const LaunchCtx& ctx) {
-    return launch_chunk_any<false>(mode, q, s, N, K, xq, xd, T, y, nullptr, ctx);
+    ChunkOut out;
+    out.y = y;
+    return launch_chunk_any<kCkPlain>(mode, q, s, N, K, xq, xd, T, out, ctx);
 }
 
 cudaError_t launch_chunk_debug(int mode, const int8_t* q, int64_t N, int64_t K, const void* xq,
                                int64_t T, int32_t* isum, const LaunchCtx& ctx) {
-    return launch_chunk_any<true>(mode, q, nullptr, N, K, xq, nullptr, T, nullptr, isum, ctx);
+    ChunkOut out;
+    out.isum = isum;
+    return launch_chunk_any<kCkDebug>(mode, q, nullptr, N, K, xq, nullptr, T, out, ctx);
+}
+
+cudaError_t launch_chunk_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                                const void* xq, const float* xd, int64_t T, float* logits,
+                                int32_t* tok, double* maxval, void* ws, const LaunchCtx& ctx) {
+    ChunkOut out;
+    out.y = logits;
+    out.ws = static_cast<unsigned char*>(ws);
+    out.tok = tok;
+    out.maxval = maxval;
+    return launch_chunk_any<kCkArgmax>(mode, q, s, N, K, xq, xd, T, out, ctx);
 }
 
 }  // namespace q8

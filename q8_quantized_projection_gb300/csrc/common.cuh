@@ -64,6 +64,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // Q8_WAIT_LIMIT_NS, records Q8_DEVERR_TIMEOUT in *err and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
@@ -76,6 +78,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
             return false;
         }
     }
+}
+
+// The polling loop of mbar_wait_fast, out of line.
+static __device__ __noinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, int* err) {
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > Q8_WAIT_LIMIT_NS) {
+            atomicExch(err, Q8_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// mbar_wait whose common case (a phase that has already completed) costs one
+// try_wait, without the polling loop's reconvergence around it (measured:
+// about 50 cycles against 170), for fine-grained pipelines where most waits
+// find the phase complete.  The out-of-line loop costs registers at the call
+// site, so register-bound kernels keep mbar_wait.
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity, int* err) {
+    return mbar_try_wait(bar, parity) || mbar_wait_poll(bar, parity, err);
 }
 
 // ----------------------------------------------------------- bulk copy (TMA)

@@ -91,6 +91,12 @@ cudaError_t launch_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N
                          const void* xq, const float* xd, int64_t T, float* y, const LaunchCtx& ctx);
 cudaError_t launch_chunk_debug(int mode, const int8_t* q, int64_t N, int64_t K, const void* xq,
                                int64_t T, int32_t* isum, const LaunchCtx& ctx);
+// The chunk projection fused with the arg-max of every activation row (the LM
+// head): ws is the arg-max workspace (ticket and keys, see below); logits
+// (float [T][N]) may be NULL.
+cudaError_t launch_chunk_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
+                                const void* xq, const float* xd, int64_t T, float* logits,
+                                int32_t* tok, double* maxval, void* ws, const LaunchCtx& ctx);
 // Activation rows from which projections run on the tensor cores: where one
 // chunk launch beats the decode kernel's groups of rows (one-word: groups of
 // 8, so 9 rows and more; two-word: groups of 4, so 5 and more).
@@ -104,9 +110,18 @@ cudaError_t launch_kv_scatter(const float* y, int64_t rows, int64_t N, const int
 cudaError_t launch_debug_dots(int mode, const int8_t* q, const void* xq, int64_t N, int64_t K,
                               int64_t rows, int32_t* isum, const LaunchCtx& ctx);
 
-// Workspace layout of the arg-max epilogue: a ticket counter, then one
-// (value, index) candidate per CTA and row.
+// Workspace layout of the arg-max epilogues, all at fixed offsets so that one
+// workspace serves calls of any row count:
+//   [0, 256)                      the tensor-core path's ticket counter
+//   [256, 256 + kArgmaxKeyBytes)  its 64-bit key per activation row
+//   [kArgmaxGemvOff, ...)         the CUDA-core path: a ticket counter, then
+//                                 from kArgmaxHeader on one (value, index)
+//                                 candidate per CTA and row of a group.
+// Counters and keys must be zero before the first call; every completed call
+// leaves them zero.
 constexpr size_t kArgmaxHeader = 256;
+constexpr size_t kArgmaxKeyBytes = 8 * 256;   // one key per row, up to the largest row count
+constexpr size_t kArgmaxGemvOff = kArgmaxHeader + kArgmaxKeyBytes;
 constexpr int kMaxGrid = 1024;
 struct ArgmaxCand {
     double v;

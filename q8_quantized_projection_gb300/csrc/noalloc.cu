@@ -1,7 +1,7 @@
 // noalloc.cu -- head_argmax for callers that cannot allocate device memory.
 //
-// The arg-max epilogue needs a little scratch (a ticket counter and one
-// candidate per CTA and row).  head_argmax takes it from the caller; this
+// The arg-max epilogues need a little scratch (ticket counters, one key per
+// activation row, and one candidate per CTA and row).  head_argmax takes it from the caller; this
 // entry point keeps it instead in a file-scope device array of fixed size,
 // which every GPU that loads the library holds until the process exits.
 //
@@ -10,7 +10,7 @@
 // with that device current, looks the real address up with
 // cudaGetSymbolAddress and caches it; that first call should therefore come
 // before any stream capture.  All calls share the one array and it keeps the
-// last call's contents, so each call clears the counter words it relies on
+// last call's contents, so each call clears the counters and keys it relies on
 // (an asynchronous memset on the caller's stream) and calls that overlap on
 // the GPU race on the array.  Nothing here allocates.
 #include <mutex>
@@ -20,7 +20,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratch = q8::kArgmaxHeader +
+constexpr size_t kNoAllocScratch = q8::kArgmaxGemvOff + q8::kArgmaxHeader +
                                    size_t(q8::kMaxGrid) * q8::kArgmaxGroupRows * sizeof(q8::ArgmaxCand);
 
 __device__ __align__(256) unsigned char g_q8_head_scratch[kNoAllocScratch];
@@ -54,8 +54,9 @@ q8_status head_argmax_noalloc(int mode, const int8_t* q, const uint16_t* s, int6
         }
         ptr = g_scratch_ptr[dev];
     }
-    // the ticket counter must read zero when the kernel starts
-    if (cudaMemsetAsync(ptr, 0, q8::kArgmaxHeader, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // the ticket counters and the keys must read zero when the kernel starts
+    if (cudaMemsetAsync(ptr, 0, q8::kArgmaxGemvOff + q8::kArgmaxHeader,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return Q8_ERR_CUDA;
     return head_argmax(mode, q, s, N, K, xq, xd, rows, tok, maxval, logits, ptr, kNoAllocScratch,
                        stream);

@@ -52,9 +52,12 @@ def test_workspace_sizes(lib):
     assert lib.q8_proj_fused_workspace(1, 3, 4096) == 12288 + 1536
     assert lib.q8_proj_fused_workspace(2, 3, 4096) == 24576 + 1536
     assert lib.q8_proj_fused_workspace(7, 3, 4096) == 0
-    assert lib.head_argmax_workspace(1) == 256 + 1024 * 16
-    assert lib.head_argmax_workspace(40) == 256 + 1024 * 16 * 16
+    # tensor-core ticket + one key per row (up to 256 rows) + the CUDA-core
+    # path's ticket and one candidate per CTA (up to 1024) and row of a group
+    assert lib.head_argmax_workspace(1) == 256 + 8 * 256 + 256 + 1024 * 16
+    assert lib.head_argmax_workspace(40) == 256 + 8 * 256 + 256 + 1024 * 16 * 16
     assert lib.head_argmax_workspace(0) == 0
+    assert lib.head_argmax_noalloc_scratch_bytes() == lib.head_argmax_workspace(256)
 
 
 A = C.c_void_p(4096)          # a 16-byte aligned non-null placeholder (never dereferenced)
