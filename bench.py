@@ -350,6 +350,23 @@ def run_ours(args, world, rank, local):
     if args.case:
         # one projection's kernel, warmup+steps eager launches (a profiler case)
         parts = args.case.split(":")
+        if parts[0] == "head":
+            # the LM head with its arg-max: head:MODE:ROWS
+            mode, rows = parts[1], int(parts[2])
+            nh, kh = synth.HEAD_SHAPE
+            qh, sh, hh, _ = synth.planted_head(4, nh, kh, rows)
+            qd = torch.from_numpy(qh).to(dev)
+            sd = torch.from_numpy(sh.view(np.int16)).to(dev)
+            xq, xd = native.activation_buffers(mode, rows, kh, device=dev)
+            native.act_quant(mode, torch.from_numpy(hh).to(dev), xq, xd, norm=True)
+            tok = torch.empty(rows, dtype=torch.int32, device=dev)
+            ws = native.argmax_workspace(rows, device=dev)
+            for i in range(args.warmup + args.steps):
+                native.head_argmax(mode, qd, sd, xq, xd, rows, tok, ws)
+            torch.cuda.synchronize(dev)
+            if rank == 0:
+                print(json.dumps({"case": args.case, "launches": args.warmup + args.steps}))
+            return
         if parts[0] == "chunk":
             # a prefill chunk: chunk:MODE:PROJ:T
             mode, proj, T = parts[1], parts[2], int(parts[3])
@@ -522,7 +539,9 @@ def run_ours(args, world, rank, local):
                    "12 C-ABI calls, one D2H copy of each mode's outputs (overlapping the next "
                    "mode's calls), then stream sync"}
 
-    sweeps = {} if args.no_sweeps else run_sweeps(native, torch, dev, capture, timed, Q, S)
+    sweeps = {} if args.no_sweeps else run_sweeps(native, torch, dev, capture, timed, Q, S, mats,
+                                                  oracle_slices=(rank == 0 and world == 1 and
+                                                                 not args.no_cpu_baseline))
 
     # a kernel whose bounded wait ran out reports it here; its timings are void
     dev_err = native.q8_device_error()
@@ -554,12 +573,45 @@ def run_ours(args, world, rank, local):
         sys.exit(3)
 
 
-def run_sweeps(native, torch, dev, capture, timed, Q, S):
+def oracle_slice_us(fn, reps=3):
+    """Host time of fn (the oracle on a slice of a workload), best of reps."""
+    best = None
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t0
+        best = dt if best is None else min(best, dt)
+    return best * 1e6
+
+
+def e2e_us(torch, dev, capture, body, steps=20):
+    """Host wall clock per step of a captured step that copies its inputs in
+    from pinned host memory and its results out, the host waiting for each."""
+    graphs = capture(body)
+    for i in range(3):
+        graphs[i % COPIES].replay()
+        torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        graphs[i % COPIES].replay()
+        torch.cuda.synchronize(dev)
+    dt = (time.perf_counter() - t0) / steps
+    del graphs
+    return dt * 1e6
+
+
+def run_sweeps(native, torch, dev, capture, timed, Q, S, mats, oracle_slices=True):
     """The other workload configurations, each graph-replayed with rotating
     inputs larger than L2: the 1024x1024 GEMV, batched decode, prefill chunks
-    and the LM head with its arg-max."""
+    and the LM head with its arg-max.  The prefill chunk at T = 256 and the
+    16-row head also run end to end (host buffers in and out through the C
+    ABI), and the CPU oracle is timed on a slice of each (scaled to the whole
+    workload, and labelled so)."""
     out = {}
     rng = synth.rng_for(7)
+    if oracle_slices:
+        from oracle import oracle as orc
+        orc.build()
 
     def per_call_us(body, calls, nrep=10):
         graphs = capture(body)
@@ -700,6 +752,40 @@ def run_sweeps(native, torch, dev, capture, timed, Q, S):
                                 "GB/s": round(LAYER_BYTES / (us * 1e-6) / 1e9, 1),
                                 "tokens_per_s": round(T / (us * 1e-6), 1),
                                 "TFLOP/s": round(flops_row * T / (us * 1e-6) / 1e12, 1)}
+            if T == 256:
+                # end to end: each layer step copies its T x K inputs in from
+                # pinned host memory and its T x N outputs back
+                h_host = [bufs[p][0].cpu().pin_memory() for p in range(4)]
+                y_host = [torch.empty(bufs[p][3].shape, dtype=torch.float32).pin_memory() for p in range(4)]
+
+                def body_e2e(c, m=m, T=T, bufs=bufs, h_host=h_host, y_host=y_host):
+                    for p in range(4):
+                        h, xq, xd, y = bufs[p]
+                        h.copy_(h_host[p], non_blocking=True)
+                        native.act_quant(m, h, xq, xd, norm=True)
+                        native.q8_proj_chunk(m, Q[c][p], S[c][p], xq, xd, T, y)
+                        y_host[p].copy_(y, non_blocking=True)
+                ue = e2e_us(torch, dev, capture, body_e2e)
+                chunk[m][str(T)]["e2e"] = {
+                    "us_per_layer": round(ue, 2), "tokens_per_s": round(T / (ue * 1e-6), 1),
+                    "h2d_bytes_per_step": sum(int(x.numel()) * 4 for x in h_host),
+                    "d2h_bytes_per_step": sum(int(x.numel()) * 4 for x in y_host),
+                    "note": "host wall clock: one captured layer step with the inputs copied in "
+                            "from pinned host memory and the outputs copied back, then stream sync"}
+                if oracle_slices and m == "i8":
+                    # the oracle (RMSNorm, quantisation, projection) on 32 output
+                    # rows of each matrix, scaled to the matrix's N
+                    tot = 0.0
+                    for p, (nm, n, k) in enumerate(synth.LAYER_D4096):
+                        hp = bufs[p][0].cpu().numpy()
+                        qs_, ss_ = mats[p][1][:32], mats[p][2][:32]
+                        t_us = oracle_slice_us(lambda: orc.project(m, qs_, ss_, orc.quantize(m, orc.rmsnorm(hp)[0])))
+                        tot += t_us * n / 32
+                    chunk[m][str(T)]["cpu_oracle"] = {
+                        "us_per_layer": round(tot, 1), "tokens_per_s": round(T / (tot * 1e-6), 2),
+                        "cores": orc.threads(), "arch": platform.machine(),
+                        "sample": "32 output rows of each matrix at T = 256, timed on the host "
+                                  "(best of 3) and scaled linearly to the matrix's rows"}
     out["prefill_chunk_d4096"] = chunk
 
     # LM head 128256 x 4096 with planted rows, fused arg-max
@@ -727,6 +813,32 @@ def run_sweeps(native, torch, dev, capture, timed, Q, S):
                                   "GB/s": round(weight_bytes(nh, kh) / (us * 1e-6) / 1e9, 1),
                                   "tokens_per_s": round(rows / (us * 1e-6), 1),
                                   "argmax_matches_planted": ok}
+            if rows == 16:
+                # end to end: the hidden rows in from pinned host memory, the
+                # producer, the head with its arg-max, the tokens back
+                h_host = h.cpu().pin_memory()
+                tok_host = torch.empty(rows, dtype=torch.int32).pin_memory()
+
+                def body_e2e(c, m=m, rows=rows, h=h, xq=xq, xd=xd, tok=tok, ws=ws, h_host=h_host,
+                             tok_host=tok_host):
+                    h.copy_(h_host, non_blocking=True)
+                    native.act_quant(m, h, xq, xd, norm=True)
+                    native.head_argmax(m, QH[c], SH[c], xq, xd, rows, tok, ws)
+                    tok_host.copy_(tok, non_blocking=True)
+                ue = e2e_us(torch, dev, capture, body_e2e)
+                head[m][str(rows)]["e2e"] = {
+                    "us": round(ue, 2), "tokens_per_s": round(rows / (ue * 1e-6), 1),
+                    "h2d_bytes_per_step": int(h_host.numel()) * 4, "d2h_bytes_per_step": rows * 4,
+                    "note": "host wall clock: hidden rows in, RMSNorm -> quant, head + arg-max, "
+                            "tokens out, then stream sync"}
+                if oracle_slices:
+                    act_h = orc.quantize(m, orc.rmsnorm(h.cpu().numpy())[0])
+                    t_us = oracle_slice_us(lambda: orc.project(m, qh[:512], sh[:512], act_h)) * nh / 512
+                    head[m][str(rows)]["cpu_oracle"] = {
+                        "us": round(t_us, 1), "tokens_per_s": round(rows / (t_us * 1e-6), 2),
+                        "cores": orc.threads(), "arch": platform.machine(),
+                        "sample": "512 of the 128256 head rows, 16 activation rows, timed on the "
+                                  "host (best of 3) and scaled linearly to the whole head"}
     out["lm_head_128256x4096"] = head
     del QH, SH
     return out
@@ -745,9 +857,9 @@ def main():
     ap.add_argument("--quick", action="store_true",
                     help="warm-up and timed steps only (for launch lists under a profiler)")
     ap.add_argument("--case", default=None,
-                    help="MODE:PROJ[:fused] (PROJ a matrix of the layer or 'all') or "
-                         "chunk:MODE:PROJ:T -- only those projections, warmup+steps eager "
-                         "launches each (a case for a profiler capture)")
+                    help="MODE:PROJ[:fused] (PROJ a matrix of the layer or 'all'), "
+                         "chunk:MODE:PROJ:T or head:MODE:ROWS -- only those launches, "
+                         "warmup+steps eager launches each (a case for a profiler capture)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -423,6 +423,53 @@ __device__ __forceinline__ void consumer_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
+__device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v, long long i) {
+    if (v > bv || (v == bv && i < bi)) {
+        bv = v;
+        bi = i;
+    }
+}
+
+// The last CTA's reduction of the grid's arg-max candidates (gc[c][rows],
+// G CTAs) by all NT consumer threads: a strided share of the CTAs a thread,
+// then the warp, then the warps in order (lowest index on ties).  The
+// candidates are read from L2, which the ticket's fences made current, many
+// at once (a single thread reading them one after another cost a round trip
+// to L2 each, tens of microseconds for a grid of 152).  red: NT/32 entries of
+// shared scratch.
+template <int NT>
+__device__ __forceinline__ void argmax_final(const ArgmaxCand* gc, int G, int rows, int tid,
+                                             ArgmaxCand* red, int32_t* tok, double* maxval) {
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int m = 0; m < rows; ++m) {
+        double bv = -INFINITY;
+        long long bi = 0x7fffffffffffffffll;
+        for (int c2 = tid; c2 < G; c2 += NT) {
+            const ArgmaxCand* src = gc + size_t(c2) * rows + m;
+            argmax_keep(bv, bi, __ldcg(&src->v), __ldcg(&src->i));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const long long oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            argmax_keep(bv, bi, ov, oi);
+        }
+        if (lane == 0) red[warp] = {bv, bi};
+        consumer_bar<NT>();
+        if (tid == 0) {
+            ArgmaxCand b = red[0];
+            for (int w = 1; w < NT / 32; ++w) {
+                double v = b.v;
+                long long i = b.i;
+                argmax_keep(v, i, red[w].v, red[w].i);
+                b = {v, i};
+            }
+            argmax_store(b, tok, maxval, m);
+        }
+        consumer_bar<NT>();
+    }
+}
+
 // --------------------------------------------------------------- the kernel
 
 template <int MODE, int R, bool ARGMAX>
@@ -773,15 +820,7 @@ __global__ void __launch_bounds__(32 * (gemv_warps<MODE, R>() + 1), 1)
         consumer_bar<kGemvConsumers>();
         if (s_ticket == unsigned(G - 1)) {
             __threadfence();
-            if (tid < rows) {
-                ArgmaxCand b = {-INFINITY, 0x7fffffffffffffffll};
-                for (int c2 = 0; c2 < G; ++c2) {
-                    const volatile ArgmaxCand* src = gc + size_t(c2) * rows + tid;
-                    const ArgmaxCand o = {src->v, src->i};
-                    if (o.v > b.v || (o.v == b.v && o.i < b.i)) b = o;
-                }
-                argmax_store(b, p.tok, p.maxval, tid);
-            }
+            argmax_final<kGemvConsumers>(gc, G, rows, tid, cand, p.tok, p.maxval);
             if (tid == 0) *counter = 0u;
         }
     }

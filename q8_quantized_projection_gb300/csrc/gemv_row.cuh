@@ -288,13 +288,6 @@ __device__ __forceinline__ void kv_store(const GemvParams& p, const int* s_pos, 
     cache[(int64_t(m) * p.n_pos + ps) * p.kv_dim + dd] = v;
 }
 
-__device__ __forceinline__ void argmax_keep(double& bv, long long& bi, double v, long long i) {
-    if (v > bv || (v == bv && i < bi)) {
-        bv = v;
-        bi = i;
-    }
-}
-
 // PROD (fused producer only): kProdPlain (RMSNorm of h), kProdResidual (the
 // residual added before the norm) or kProdSwiglu (the SwiGLU of the fused
 // gate+up row h); each a separate instantiation, so the plain fused kernel
@@ -461,12 +454,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         plane = K;
     }
 
-    double best_v[ARGMAX ? R : 1];
-    long long best_i[ARGMAX ? R : 1];
-#pragma unroll
-    for (int m = 0; m < (ARGMAX ? R : 1); ++m) {
-        best_v[m] = -INFINITY;
-        best_i[m] = 0x7fffffffffffffffll;
+    if constexpr (ARGMAX) {
+        // each warp's best (value, lowest index) per row, kept in shared
+        // memory between super-blocks (out of the streaming loop's registers)
+        if (tid < NW * R) cand[tid] = {-INFINITY, 0x7fffffffffffffffll};
     }
 
     // this warp's place in every stage it serves
@@ -886,6 +877,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
             if constexpr (kBL) {
                 for (int u = 0; u < nparts; ++u) E = max(E, int(s_ep[u]));
             }
+            // arg-max: this thread's rows all have activation row m = tid % R
+            // (NT is a multiple of R)
+            double bv = -INFINITY;
+            long long bi = 0x7fffffffffffffffll;
             for (int i = tid; i < sbn * R; i += NT) {
                 const int row_sb = i / R, m = i % R;
                 if (m >= rows) continue;
@@ -924,28 +919,33 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                         reinterpret_cast<float*>(p.y)[m * N + n] = float(val);
                 }
                 if constexpr (KV) kv_store(p, s_pos, m, n, float(val));
-                if constexpr (ARGMAX) argmax_keep(best_v[m], best_i[m], val, n);
+                if constexpr (ARGMAX) argmax_keep(bv, bi, val, n);
+            }
+            if constexpr (ARGMAX) {
+                // over the warp's lanes of the same row m, then into the warp's
+                // candidate of that row
+#pragma unroll
+                for (int o = 16; o >= R; o >>= 1) {
+                    const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const long long oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                    argmax_keep(bv, bi, ov, oi);
+                }
+                if (lane < R) {
+                    ArgmaxCand& c = cand[warp * R + lane];
+                    double cv = c.v;
+                    long long ci = c.i;
+                    argmax_keep(cv, ci, bv, bi);
+                    c = {cv, ci};
+                }
             }
         }
         consumer_bar<NT>();
     }
 
     if constexpr (ARGMAX) {
-        // per warp, then per CTA, then the last CTA to take a ticket reduces
-        // every CTA's candidate (lowest index on ties)
-#pragma unroll
-        for (int m = 0; m < R; ++m) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const double ov = __shfl_xor_sync(0xffffffffu, best_v[m], o);
-                const long long oi = __shfl_xor_sync(0xffffffffu, best_i[m], o);
-                argmax_keep(best_v[m], best_i[m], ov, oi);
-            }
-        }
-        if (lane == 0) {
-#pragma unroll
-            for (int m = 0; m < R; ++m) cand[warp * R + m] = {best_v[m], best_i[m]};
-        }
+        // the warps' candidates (merged per super-block above), then per CTA,
+        // then the last CTA to take a ticket reduces every CTA's candidate
+        // (lowest index on ties)
         consumer_bar<NT>();
         ArgmaxCand* gc = reinterpret_cast<ArgmaxCand*>(p.ws + kArgmaxHeader);
         unsigned int* counter = reinterpret_cast<unsigned int*>(p.ws);
@@ -963,15 +963,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
         consumer_bar<NT>();
         if (s_ticket == unsigned(G - 1)) {
             __threadfence();
-            if (tid < rows) {
-                ArgmaxCand b = {-INFINITY, 0x7fffffffffffffffll};
-                for (int c2 = 0; c2 < G; ++c2) {
-                    const volatile ArgmaxCand* src = gc + size_t(c2) * rows + tid;
-                    const ArgmaxCand o = {src->v, src->i};
-                    if (o.v > b.v || (o.v == b.v && o.i < b.i)) b = o;
-                }
-                argmax_store(b, p.tok, p.maxval, tid);
-            }
+            argmax_final<NT>(gc, G, rows, tid, cand, p.tok, p.maxval);
             if (tid == 0) *counter = 0u;
         }
     }
