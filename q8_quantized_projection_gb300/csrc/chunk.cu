@@ -295,8 +295,8 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
     uint64_t* sg_empty = sg_full + kCkSGroups;
     uint64_t* a_full = sg_empty + kCkSGroups;
     uint64_t* a_empty = a_full + C::kQuads;
-    uint64_t* tm_full = a_empty + C::kQuads;
-    uint64_t* tm_empty = tm_full + C::kSlots;          // per slot group
+    uint64_t* tm_full = a_empty + C::kQuads;           // per slot group
+    uint64_t* tm_empty = tm_full + C::kSG;             // per slot group
     uint64_t* sc_full = tm_empty + C::kSG;             // per stage of scale entries
     uint64_t* sc_empty = sc_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sc_empty + 2);
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
             mbar_init(&a_full[i], C::kConv);
             mbar_init(&a_empty[i], 1);
         }
-        for (int i = 0; i < C::kSlots; ++i) mbar_init(&tm_full[i], 1);
+        for (int i = 0; i < C::kSG; ++i) mbar_init(&tm_full[i], 1);
         // each block of a group is released by the 4 * kEC warps that read it
         for (int i = 0; i < C::kSG; ++i) mbar_init(&tm_empty[i], C::kGS * 4 * C::kEC);
         for (int i = 0; i < 2; ++i) {
@@ -422,16 +422,20 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
                     const uint32_t d = tmem + uint32_t(ts * C::kN);
                     mma_f16_ts(d, a, smem_desc_kmajor(bb, 128, 512), idesc, false);
                     mma_f16_ts(d, a + 8u, smem_desc_kmajor(bb + 256u, 128, 512), idesc, true);
-                    mma_commit(smem_u32(&tm_full[ts]));
+                    // one commit a slot group: its accumulators are ready together
+                    if ((b + 1) % C::kGS == 0) mma_commit(smem_u32(&tm_full[(b / C::kGS) % C::kSG]));
                     ++issued;
                 }
                 if (ok) mma_commit(smem_u32(&a_empty[qs]));
             }
             // nothing may be left in flight when TMEM is released (the epilogue
-            // normally drains every block; this covers an early exit)
-            if (issued > 0)
-                mbar_wait_fast(&tm_full[(issued - 1) % C::kSlots], uint32_t((issued - 1) / C::kSlots) & 1u,
-                          p.err);
+            // normally drains every block; this covers an early exit, whose
+            // last group may still want its commit)
+            if (issued > 0) {
+                const int bl = issued - 1;
+                if (issued % C::kGS != 0) mma_commit(smem_u32(&tm_full[(bl / C::kGS) % C::kSG]));
+                mbar_wait_fast(&tm_full[(bl / C::kGS) % C::kSG], uint32_t(bl / C::kSlots) & 1u, p.err);
+            }
         }
     } else if (warp < C::kEpiWarp0) {
         // ------------------------------------------------------------ converters
@@ -573,7 +577,7 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
             const int ts = b % C::kSlots, se = b % C::kSE;
             const uint32_t par = uint32_t(b / C::kSlots) & 1u;
             if (!DEBUG && ok) ok = mbar_wait_fast(&sc_full[(b >> 2) & 1], uint32_t(b >> 3) & 1u, p.err);
-            if (ok) ok = mbar_wait_fast(&tm_full[ts], par, p.err);
+            if (ok) ok = mbar_wait_fast(&tm_full[(b / C::kGS) % C::kSG], par, p.err);
             ok = __all_sync(0xffffffffu, ok);   // the TMEM loads below are warp-wide
             if (!ok) break;
             tc_fence_after();
