@@ -27,7 +27,8 @@
 //               activation codes (one or two planes) and activation scales;
 //               every 8 blocks the weight scales;
 //   warp 1      owns TMEM; one thread issues two K = 16 MMAs per block into
-//               one of kSlots accumulator slots and commits each block;
+//               one of kSlots accumulator slots, and commits once per group
+//               of kGS blocks (one barrier a group of slots);
 //   next 6-10   converters, a whole stage at a time: 4 or 8 warps (one or
 //               two per TMEM lane quadrant) the weights int8 -> f16 into TMEM
 //               (the MMA's A operand) and their scales; two warps the
