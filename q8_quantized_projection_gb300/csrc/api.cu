@@ -171,7 +171,7 @@ const char* q8_status_str(int status) {
     }
 }
 
-int q8_version(void) { return 104; }
+int q8_version(void) { return 105; }
 
 int q8_last_cuda_error(void) { return t_last_cuda; }
 
@@ -276,6 +276,18 @@ q8_status q8_proj_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N,
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
     return project_dispatch(mode, q, s, N, K, xq, xd, T, y, 0, ctx);
+}
+
+q8_status q8_debug_chunk_plan(int mode, int64_t N, int64_t K, int64_t T, int argmax, int64_t* out) {
+    if (!out) return Q8_ERR_ARG;
+    if (mode != Q8_ACT_I8 && mode != Q8_ACT_I8X2) return Q8_ERR_MODE;
+    if (N < 1 || N > (int64_t(1) << 31) || T < 1 || T > Q8_MAX_ROWS || K < 256 || K % 256 != 0 ||
+        K > (int64_t(1) << 24))
+        return Q8_ERR_SHAPE;
+    LaunchCtx ctx;
+    q8_status st = make_ctx(nullptr, ctx);
+    if (st != Q8_OK) return st;
+    return chunk_plan(mode, N, K, T, argmax != 0, ctx, out) ? Q8_OK : Q8_ERR_UNSUPPORTED;
 }
 
 size_t q8_proj_fused_workspace(int mode, int64_t rows, int64_t K) {

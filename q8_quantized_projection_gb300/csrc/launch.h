@@ -97,6 +97,12 @@ cudaError_t launch_chunk_debug(int mode, const int8_t* q, int64_t N, int64_t K, 
 cudaError_t launch_chunk_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                                 const void* xq, const float* xd, int64_t T, float* logits,
                                 int32_t* tok, double* maxval, void* ws, const LaunchCtx& ctx);
+// The launch plan the chunk path would use (host side; occupancy queries
+// only): out[6] = TT, ks (CTAs splitting K), walk (1: clusters walk several
+// tiles), clusters, tiles, pipeline stages.  False where the path does not
+// apply (mode, K).
+bool chunk_plan(int mode, int64_t N, int64_t K, int64_t T, bool argmax, const LaunchCtx& ctx,
+                int64_t* out);
 // Activation rows from which projections run on the tensor cores: where one
 // chunk launch beats the decode kernel's groups of rows (one-word: groups of
 // 8, so 9 rows and more; two-word: groups of 4, so 5 and more).

@@ -49,6 +49,7 @@ SIGNATURES = {
     "head_argmax_workspace": (_sz, [_i64]),
     "q8_debug_block_dots": (_int, [_int, _vp, _vp, _i64, _i64, _i64, _vp, _int, _vp]),
     "q8_debug_row_geometry": (_int, [_int, _i64, _i64, _i64, _int, _int, _vp]),
+    "q8_debug_chunk_plan": (_int, [_int, _i64, _i64, _i64, _int, _vp]),
     "head_argmax_noalloc": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp,
                                    _vp]),
     "head_argmax_noalloc_scratch_bytes": (_sz, []),
@@ -247,6 +248,19 @@ def q8_debug_row_geometry(mode, rows, n, k, grid, cta):
         return None
     _check(st, "q8_debug_row_geometry")
     return dict(zip(ROW_GEOMETRY_FIELDS, list(out)))
+
+
+CHUNK_PLAN_FIELDS = ("TT", "ks", "walk", "clusters", "tiles", "stages")
+
+
+def q8_debug_chunk_plan(mode, n, k, t, argmax=False):
+    """The tensor-core path's launch plan for a projection of t rows (host
+    side, the current device's occupancy), as a dict."""
+    out = (C.c_int64 * len(CHUNK_PLAN_FIELDS))()
+    st = load().q8_debug_chunk_plan(_mode(mode), int(n), int(k), int(t), int(bool(argmax)),
+                                    C.cast(out, C.c_void_p))
+    _check(st, "q8_debug_chunk_plan")
+    return dict(zip(CHUNK_PLAN_FIELDS, list(out)))
 
 
 # ------------------------------------------------------------ buffer helpers

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
 
 
 def test_status_names_and_version(lib):
-    assert lib.q8_version() == 104
+    assert lib.q8_version() == 105
     for i, name in enumerate(native._STATUS):
         assert lib.q8_status_str(i).decode() == name
     assert lib.q8_status_str(99).decode() == "Q8_ERR_UNKNOWN"
@@ -131,3 +131,13 @@ def test_widened_entry_points_reject_bad_arguments(lib):
     assert call(K=16416) == 6                      # the decode kernel's K
     assert call(pos=U) == 3
     assert call(vc=C.c_void_p((1 << 20) + 16)) == 1   # K and V caches overlap
+
+def test_chunk_plan_host_errors(lib):
+    """q8_debug_chunk_plan checks its arguments before touching a device."""
+    import ctypes as C
+    out = (C.c_int64 * 6)()
+    assert lib.q8_debug_chunk_plan(0, 128, 4096, 16, 0, C.cast(out, C.c_void_p)) == 4     # f32: MODE
+    assert lib.q8_debug_chunk_plan(1, 128, 4100, 16, 0, C.cast(out, C.c_void_p)) == 2     # K % 256
+    assert lib.q8_debug_chunk_plan(1, 128, 4096, 0, 0, C.cast(out, C.c_void_p)) == 2      # T
+    assert lib.q8_debug_chunk_plan(1, 128, 4096, 257, 0, C.cast(out, C.c_void_p)) == 2    # T > max
+    assert lib.q8_debug_chunk_plan(1, 128, 4096, 16, 0, None) == 1                         # out
