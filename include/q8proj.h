@@ -311,9 +311,9 @@ q8_status q8_debug_row_geometry(int mode, int64_t rows, int64_t N, int64_t K, in
  * launched): the plan of the tensor-core path for a projection of T rows
  * (argmax = 0: q8_proj_chunk and q8_proj from 9 one-word / 5 two-word rows;
  * argmax = 1: head_argmax).  out (host, 6 int64) receives: TT (activation rows
- * a tile), ks (CTAs of a cluster, each over 1/ks of K), walk (1: each cluster
- * walks several 128 x TT tiles, start-up paid once; 0: one tile a cluster, in
- * waves), clusters, tiles, pipeline stages.  Modes Q8_ACT_I8 / Q8_ACT_I8X2,
+ * a tile), ks (CTAs of a cluster, each over 1/ks of K), tiles (128 x TT, one
+ * cluster each), clusters that fit on the device at once, waves, pipeline
+ * stages.  Modes Q8_ACT_I8 / Q8_ACT_I8X2,
  * K % 256 == 0, 1 <= T <= Q8_MAX_ROWS; otherwise Q8_ERR_MODE / Q8_ERR_SHAPE.
  */
 q8_status q8_debug_chunk_plan(int mode, int64_t N, int64_t K, int64_t T, int argmax, int64_t* out);

@@ -78,10 +78,7 @@ constexpr int kCkPlain = 0;    // y
 constexpr int kCkDebug = 1;    // the per-block integer dots
 constexpr int kCkArgmax = 2;   // the arg-max of every row (and y when given)
 
-// WALK: the persistent layout, where a cluster walks several tiles (its
-// end-of-tile areas kept apart from the pipeline's); without it a CTA takes
-// one tile, and the end-of-tile scratch reuses the drained stage area.
-template <int MODE, int TT, bool WALK = false>
+template <int MODE, int TT>
 struct CkCfg {
     static constexpr int kPlanes = (MODE == 2) ? 2 : 1;
     static constexpr int kN = TT * kPlanes;                            // MMA N
@@ -120,50 +117,21 @@ struct CkCfg {
     static constexpr int kEpiWarp0 = 2 + kConv;
     static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
     static constexpr int kBarBytes = 1024;
-    // the epilogue's end-of-tile areas, kept apart from the pipeline's so that
-    // a CTA's next tile streams on while they are in use: the groups' partial
-    // sums, the arg-max candidates, and the split-K partials that the other
-    // CTAs of the cluster push for every tile but the last, (ks - 1) slices of
-    // ceil(128 / ks) weight rows
-    static constexpr int kPartial = kCkM * TT * 4;
-    static constexpr int kGScr = WALK ? (kEG > 1 ? kEG - 1 : 0) * kPartial : 0;
-    static constexpr int kCand = WALK ? 4 * TT * 8 : 0;
-    // without WALK: the groups' partial sums (or the split-K partial) at the
-    // start of the stage area, the arg-max candidates after them
-    static constexpr int kCandOff = (kEG > 1 ? kEG - 1 : 1) * kPartial;
-    static constexpr int recv_bytes(int ks) { return ks <= 1 ? 0 : (ks - 1) * ((kCkM + ks - 1) / ks) * TT * 4; }
-    static constexpr int recv_max(int kmax) {
-        int m = 0;
-        for (int k = 2; k <= kmax; ++k) m = recv_bytes(k) > m ? recv_bytes(k) : m;
-        return m;
-    }
-    static constexpr int kFixedBase = kCkSGroups * kSGroup + kQuads * kBQuad +
-                                      (kSE * kScl + 127) / 128 * 128 + kGScr + kCand + kBarBytes +
-                                      1024 /*alignment*/;
-    static constexpr int stages_for(int kmax) { return (kCkSmemBudget - kFixedBase - recv_max(kmax)) / kStage; }
-    // the largest split of K whose receive area leaves the pipeline at least
-    // 4 stages (or as many as it has without one): splits up to it walk
-    // several tiles per cluster (measured: a 3-stage pipeline at TT = 128
-    // streams a tile ~20% slower than 4 stages)
-    static constexpr int kMinStages = stages_for(1) < 4 ? stages_for(1) : 4;
-    static constexpr int kRecvKs = !WALK                         ? 1
-                                   : stages_for(8) >= kMinStages ? 8
-                                   : stages_for(4) >= kMinStages ? 4
-                                   : stages_for(2) >= kMinStages ? 2
-                                                                 : 1;
-    static constexpr int kRecv = WALK ? recv_max(kRecvKs) : 0;
-    static constexpr int kFixed = kFixedBase + kRecv;
+    static constexpr int kFixed = kCkSGroups * kSGroup + kQuads * kBQuad +
+                                  (kSE * kScl + 127) / 128 * 128 + kBarBytes + 1024 /*alignment*/;
     static constexpr int kStages = (kCkSmemBudget - kFixed) / kStage < 8
                                        ? (kCkSmemBudget - kFixed) / kStage
                                        : 8;
     static constexpr size_t kSmem = size_t(kStages) * kStage + kFixed;
+    // the end-of-tile scratch in the stage area: the groups' partial sums
+    // (or the CTA's split-K partial), then the arg-max candidates
+    static constexpr int kPartial = kCkM * TT * 4;
+    static constexpr int kCandOff = (kEG > 1 ? kEG - 1 : 1) * kPartial;
     static_assert(kStages >= 3, "TMA pipeline depth");
     static_assert(kStage % 1024 == 0, "swizzled TMA tiles need 1024-byte alignment");
-    static_assert(kPartial <= kStages * kStage, "the last tile's split-K partial must fit the stages");
-    static_assert(WALK || kCandOff + 4 * TT * 8 <= kStages * kStage, "end-of-tile scratch must fit the stages");
+    static_assert(kCandOff + 4 * TT * 8 <= kStages * kStage, "end-of-tile scratch must fit the stages");
     static_assert(kSmem <= size_t(kCkSmemBudget), "shared memory");
     static_assert(kCW % 16 == 0 && kCW <= 32, "epilogue columns");
-    static_assert(kEG == 1 || kEG == 2, "epilogue groups");
     static_assert(kSlots >= 3 && kSlots % kEG == 0, "accumulator slots: each served by one group");
     static_assert(kSE == 8 && kSE % kEG == 0, "scale entries: two stages, each served by one group");
     static_assert(kSlots % kGS == 0 && kSG >= 2 && kGS % kEG == 0 || kGS == 1, "slot groups");
@@ -173,16 +141,11 @@ struct CkCfg {
 
 struct CkParams {
     int64_t N, K, T;
-    int tiles;              // 128 x TT output tiles; cluster x walks tiles x, x + gridDim.x, ...
-    int t_tiles;            // tiles along T (tile = n_tile * t_tiles + t_tile)
     int groups_per_split;   // 8-block groups of K per CTA of a cluster
-    int dtx, dty;           // gridDim.x as (tiles along T, tiles along N): the step to a cluster's next tile
-    int maxr;               // split K: ceil(128 / ks), the most weight rows a CTA owns
-    int r0[kCkMaxSplit + 1];   // split K: CTA q owns weight rows [r0[q], r0[q+1]) of a tile
     float* y;               // [T][N], may be NULL for the arg-max
     int32_t* isum;          // debug: per-block dots [T][N][K/32] instead of y
     int* err;
-    unsigned int* ticket;   // arg-max: tiles done
+    unsigned int* ticket;   // arg-max: CTAs done
     unsigned long long* keys;   // arg-max: one key per activation row
     int32_t* tok;
     double* maxval;
@@ -257,18 +220,6 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// The two halves of cluster_sync, for threads that meet the rest of the
-// cluster at different points: arrive (relaxed: mbarrier initialisation is
-// released by its own fence) early, wait just before the first access to
-// another CTA's shared memory.  Not aligned: the waits need not be
-// warp-uniform.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
@@ -282,57 +233,6 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
-}
-
-// Four floats (two packed pairs) to another CTA's shared memory, counted in
-// bytes on that CTA's mbarrier `bar` (both shared::cluster addresses of the
-// same CTA); the writer does not wait for it.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint64_t a, uint64_t b, uint32_t bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-        "r"(uint32_t(a)), "r"(uint32_t(a >> 32)), "r"(uint32_t(b)), "r"(uint32_t(b >> 32)), "r"(bar)
-        : "memory");
-}
-
-// Arrives on an mbarrier of another CTA of the cluster (a shared::cluster
-// address from cluster_map) without ordering this thread's memory accesses
-// (a release at cluster scope measured ~1 us here).  For a "your data has
-// been read" signal: the loads it follows have returned, since their values
-// were consumed by instructions that issued before it.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// A wait on a barrier that the other CTAs of the cluster arrive on, acquiring
-// their writes; bounded like every wait of the library.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* err) {
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait_cluster(bar, parity)) {
-        if (globaltimer() - t0 > Q8_WAIT_LIMIT_NS) {
-            atomicExch(err, Q8_DEVERR_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
-// The arriving half of named barrier `id`: counts this warp's threads towards
-// `count` without waiting (the other side waits with named_bar).
-__device__ __forceinline__ void named_bar_arrive(int id, int count) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // 16 consecutive TMEM columns of the warp's 32 lanes.
@@ -373,12 +273,12 @@ __device__ __forceinline__ void argmax_unkey(unsigned long long key, int32_t& to
     val = double(__uint_as_float(b));
 }
 
-template <int MODE, int TT, int KIND, bool WALK>
-__global__ void __launch_bounds__(CkCfg<MODE, TT, WALK>::kThreads, 1)
+template <int MODE, int TT, int KIND>
+__global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
                  const __grid_constant__ CUtensorMap tm_xl, const __grid_constant__ CUtensorMap tm_s,
                  const __grid_constant__ CUtensorMap tm_xd, const CkParams p) {
-    using C = CkCfg<MODE, TT, WALK>;
+    using C = CkCfg<MODE, TT>;
     constexpr bool DEBUG = KIND == kCkDebug;
     constexpr bool ARGMAX = KIND == kCkArgmax;
     extern __shared__ unsigned char smem_raw[];
@@ -389,10 +289,7 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT, WALK>::kThreads, 1)
     unsigned char* sgroups = stages + size_t(C::kStages) * C::kStage;
     unsigned char* bquads = sgroups + size_t(kCkSGroups) * C::kSGroup;
     unsigned char* scl = bquads + size_t(C::kQuads) * C::kBQuad;
-    unsigned char* gscr = scl + (C::kSE * C::kScl + 127) / 128 * 128;
-    unsigned char* cand = gscr + C::kGScr;
-    unsigned char* recv = cand + C::kCand;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(recv + C::kRecv);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(scl + (C::kSE * C::kScl + 127) / 128 * 128);
     uint64_t* st_full = bars;
     uint64_t* st_empty = st_full + C::kStages;
     uint64_t* sg_full = st_empty + C::kStages;
@@ -403,54 +300,19 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT, WALK>::kThreads, 1)
     uint64_t* tm_empty = tm_full + C::kSG;             // per slot group
     uint64_t* sc_full = tm_empty + C::kSG;             // per stage of scale entries
     uint64_t* sc_empty = sc_full + 2;
-    uint64_t* red_full = sc_empty + 2;                 // the cluster's partials are here
-    uint64_t* sent_ok = red_full + 1;                  // the cluster has read what this CTA sent
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sent_ok + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sc_empty + 2);
     __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // tiles of this cluster: cl, cl + ncl, ... (all CTAs of a cluster walk the
-    // same tiles, each over its own range of K)
-    const int ncl = int(gridDim.x), cl = int(blockIdx.x);
-    const int ks = int(gridDim.z), rank = int(blockIdx.z);
-    const int ntl = !WALK ? 1 : cl < p.tiles ? (p.tiles - 1 - cl) / ncl + 1 : 0;
+    const int64_t t0 = int64_t(blockIdx.x) * TT;
+    const int64_t m0 = int64_t(blockIdx.y) * kCkM;
     // this CTA's range of K, in 8-block groups
     const int total_groups = int(p.K / (Q8_QK * kCkGroup));
-    const int g_begin = rank * p.groups_per_split;
+    const int g_begin = int(blockIdx.z) * p.groups_per_split;
     const int g_end = min(total_groups, g_begin + p.groups_per_split);
-    const int nblk = g_end > g_begin ? (g_end - g_begin) * kCkGroup : 0;   // blocks per tile
-    const int nst = nblk / 4;                                               // stages per tile
-    const int nst_all = ntl * nst;                                          // stages of this CTA
-    const int st0 = g_begin * (kCkGroup / 4);   // first TMA stage of a tile (global along K)
-    // tile i of this cluster as (tile along T, tile along N): without WALK the
-    // grid is (T tiles, N tiles, ks) and the block index is the tile; walking
-    // clusters step through tile = cl + i * ncl (one tile along T is the
-    // common case, and no division sits before the first copy)
-    auto tile_xy = [&](int i, int& tx, int& ty) {
-        if constexpr (!WALK) {
-            tx = int(blockIdx.x);
-            ty = int(blockIdx.y);
-        } else {
-            const int t = cl + i * ncl;
-            if (p.t_tiles == 1) {
-                tx = 0;
-                ty = t;
-            } else {
-                tx = t % p.t_tiles;
-                ty = t / p.t_tiles;
-            }
-        }
-    };
-    auto tile_t0 = [&](int i) {
-        int tx, ty;
-        tile_xy(i, tx, ty);
-        return int64_t(tx) * TT;
-    };
-    auto tile_m0 = [&](int i) {
-        int tx, ty;
-        tile_xy(i, tx, ty);
-        return int64_t(ty) * kCkM;
-    };
+    const int nblk = g_end > g_begin ? (g_end - g_begin) * kCkGroup : 0;
+    const int nst = nblk / 4;
+    const int st0 = g_begin * (kCkGroup / 4);   // first TMA stage (global)
 
     if (tid == 0) {
         for (int i = 0; i < C::kStages; ++i) {
@@ -472,10 +334,6 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT, WALK>::kThreads, 1)
             mbar_init(&sc_full[i], C::kConv);
             mbar_init(&sc_empty[i], 4 * 4 * C::kEC);
         }
-        // red_full: this CTA's own arrival with the bytes the others push;
-        // sent_ok: every thread of epilogue group 0 of every other CTA
-        mbar_init(red_full, 1);
-        mbar_init(sent_ok, uint32_t(ks > 1 ? ks - 1 : 1) * uint32_t(32 * 4 * C::kEC));
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -485,12 +343,6 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT, WALK>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // split K over several tiles: the other CTAs' barriers must be initialised
-    // before this CTA writes to them (it waits just before its first push)
-    // (only plain projections split K: the arg-max and the debug dots run
-    // with ks = 1)
-    const bool walk_split = WALK && KIND == kCkPlain && ks > 1 && ntl > 1;
-    if (walk_split) cluster_arrive_relaxed();
     const uint32_t tmem = *tmem_slot;
     pdl_launch_dependents();
     const uint32_t stages_a = smem_u32(stages), sgroups_a = smem_u32(sgroups);
@@ -500,49 +352,27 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT, WALK>::kThreads, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint32_t stage_tx = uint32_t(C::kW + C::kX + (DEBUG ? 0 : C::kXD));
-            const int npre = nst_all < C::kStages ? nst_all : C::kStages;
-            const int ngroups = nst_all / 2;   // a tile's stages come in pairs (one weight-scale group)
+            const int npre = nst < C::kStages ? nst : C::kStages;
+            const int ngroups = nst / 2;
             const int gpre = DEBUG ? 0 : (ngroups < kCkSGroups ? ngroups : kCkSGroups);
-            // the three streams (weights, activations, weight scales) each walk
-            // the tiles in order; a cursor keeps each one's tile and stage
-            // without a division per copy
-            struct Cursor {
-                int i, sl, t0, m0;
-            };
-            const Cursor first{0, 0, int(tile_t0(0)), int(tile_m0(0))};
-            Cursor cw = first, ca = first, cs = first;
-            auto advance = [&](Cursor& c, int by) {
-                c.sl += by;
-                if (c.sl == nst) {
-                    c.sl = 0;
-                    ++c.i;
-                    c.t0 = int(tile_t0(c.i));
-                    c.m0 = int(tile_m0(c.i));
-                }
-            };
             auto weights = [&](int s) {
                 const int slot = s % C::kStages;
                 mbar_arrive_expect_tx(&st_full[slot], stage_tx);
-                tma2d(stages + size_t(slot) * C::kStage, &tm_w, (st0 + cw.sl) * kCkStageK, cw.m0,
-                      &st_full[slot]);
-                advance(cw, 1);
+                tma2d(stages + size_t(slot) * C::kStage, &tm_w, (st0 + s) * kCkStageK, int(m0), &st_full[slot]);
             };
             auto acts = [&](int s) {
                 unsigned char* st = stages + size_t(s % C::kStages) * C::kStage;
-                const int kx = (st0 + ca.sl) * kCkStageK;   // byte (= element) of K
-                const int t0 = ca.t0;
+                const int kx = (st0 + s) * kCkStageK;   // byte (= element) of K
                 uint64_t* bar = &st_full[s % C::kStages];
-                tma2d(st + C::kW, &tm_xh, kx, t0, bar);
-                if constexpr (MODE == 2) tma2d(st + C::kW + C::kXPlane, &tm_xl, kx, t0, bar);
-                if constexpr (!DEBUG) tma2d(st + C::kW + C::kX, &tm_xd, kx / Q8_QK, t0, bar);
-                advance(ca, 1);
+                tma2d(st + C::kW, &tm_xh, kx, int(t0), bar);
+                if constexpr (MODE == 2) tma2d(st + C::kW + C::kXPlane, &tm_xl, kx, int(t0), bar);
+                if constexpr (!DEBUG) tma2d(st + C::kW + C::kX, &tm_xd, kx / Q8_QK, int(t0), bar);
             };
             auto scales = [&](int g) {
                 const int gs = g % kCkSGroups;
                 mbar_arrive_expect_tx(&sg_full[gs], uint32_t(C::kSGroup));
-                tma2d(sgroups + size_t(gs) * C::kSGroup, &tm_s, (st0 + cs.sl) * kCkStageK / Q8_QK,
-                      cs.m0, &sg_full[gs]);
-                advance(cs, 2);
+                tma2d(sgroups + size_t(gs) * C::kSGroup, &tm_s, (st0 + 2 * g) * kCkStageK / Q8_QK, int(m0),
+                      &sg_full[gs]);
             };
             // weights and their scales first: they never depend on the
             // previous kernel on the stream
@@ -551,7 +381,7 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT, WALK>::kThreads, 1)
             pdl_wait();
             for (int s = 0; s < npre; ++s) acts(s);
             int issued = npre, sissued = gpre;
-            for (int s = npre; s < nst_all; ++s) {
+            for (int s = npre; s < nst; ++s) {
                 const int slot = s % C::kStages;
                 if (!mbar_wait_fast(&st_empty[slot], uint32_t(s / C::kStages - 1) & 1u, p.err)) break;
                 weights(s);
@@ -576,7 +406,7 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT, WALK>::kThreads, 1)
             const uint32_t idesc = idesc_f16_f32(kCkM, C::kN);
             int issued = 0;
             bool ok = true;
-            for (int s = 0; s < nst_all && ok; ++s) {
+            for (int s = 0; s < nst && ok; ++s) {
                 const int qs = s % C::kQuads;
                 if (!mbar_wait_fast(&a_full[qs], uint32_t(s / C::kQuads) & 1u, p.err)) break;
 #pragma unroll
@@ -626,7 +456,7 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT, WALK>::kThreads, 1)
         const int aw = warp - 2 - C::kWConv;               // activation warp 0 or 1
         constexpr int kAPasses = (TT * 4 + 63) / 64;      // (row, block) pairs a lane (TT <= 32)
         bool ok = true;
-        for (int s = 0; s < nst_all; ++s) {
+        for (int s = 0; s < nst; ++s) {
             const int slot = s % C::kStages, qs = s % C::kQuads;
             const int g = s >> 1, gs = g % kCkSGroups;
             if (ok) ok = mbar_wait_fast(&st_full[slot], uint32_t(s / C::kStages) & 1u, p.err);
@@ -734,284 +564,210 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT, WALK>::kThreads, 1)
         // ------------------------------------------------------------ epilogue
         pdl_wait();   // outputs and arg-max keys belong to the previous kernel until here
         constexpr int CW = C::kCW;
-        constexpr int kEpiThreads = 32 * C::kEpiWarps;
-        constexpr int kG0 = 32 * 4 * C::kEC;          // threads of group 0
         const int ew = warp - C::kEpiWarp0;           // 0..15
         const int qd = warp & 3;                      // TMEM lane quadrant of this warp
         const int ec = (ew >> 2) % C::kEC;            // column slice
         const int eg = (ew >> 2) / C::kEC;            // block group
         const int n = qd * 32 + lane;                 // weight row within the tile
         const int c0 = ec * CW;
-        // the tile's place, carried from tile to tile without a division
-        int tx, ty;
-        tile_xy(0, tx, ty);
+        uint64_t acc[CW / 2];
+#pragma unroll
+        for (int i = 0; i < CW / 2; ++i) acc[i] = 0;
         bool ok = true;
-        for (int i = 0; i < ntl; ++i) {
-            uint64_t acc[CW / 2];
+        for (int b = eg; b < nblk; b += C::kEG) {
+            const int ts = b % C::kSlots, se = b % C::kSE;
+            const uint32_t par = uint32_t(b / C::kSlots) & 1u;
+            if (!DEBUG && ok) ok = mbar_wait_fast(&sc_full[(b >> 2) & 1], uint32_t(b >> 3) & 1u, p.err);
+            if (ok) ok = mbar_wait_fast(&tm_full[(b / C::kGS) % C::kSG], par, p.err);
+            ok = __all_sync(0xffffffffu, ok);   // the TMEM loads below are warp-wide
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t(qd * 32) << 16) + uint32_t(ts * C::kN + c0);
+            float v[CW];
+            float vl[MODE == 2 ? CW : 1];
 #pragma unroll
-            for (int u = 0; u < CW / 2; ++u) acc[u] = 0;
-            for (int bl = eg; bl < nblk && ok; bl += C::kEG) {
-                const int b = i * nblk + bl;   // block of this CTA's stream
-                const int ts = b % C::kSlots, se = b % C::kSE;
-                const uint32_t par = uint32_t(b / C::kSlots) & 1u;
-                if (!DEBUG && ok) ok = mbar_wait_fast(&sc_full[(b >> 2) & 1], uint32_t(b >> 3) & 1u, p.err);
-                if (ok) ok = mbar_wait_fast(&tm_full[(b / C::kGS) % C::kSG], par, p.err);
-                ok = __all_sync(0xffffffffu, ok);   // the TMEM loads below are warp-wide
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t d = tmem + (uint32_t(qd * 32) << 16) + uint32_t(ts * C::kN + c0);
-                float v[CW];
-                float vl[MODE == 2 ? CW : 1];
+            for (int c = 0; c < CW / 16; ++c) {
+                tmem_ld16(d + uint32_t(16 * c), v + 16 * c);
+                if constexpr (MODE == 2) tmem_ld16(d + uint32_t(TT + 16 * c), vl + 16 * c);
+            }
+            // the block's weight scale while the accumulator is on its way
+            const uint32_t e = scl_a + uint32_t(se * C::kScl);
+            const float sw = DEBUG ? 0.0f : half_bits_to_float(lds16(e + uint32_t(2 * n)));
+            tmem_wait_ld();
+            // the data is in registers: the slot goes back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tm_empty[(b / C::kGS) % C::kSG]);
+            if constexpr (DEBUG) {
+                // the plane sums are exact integers below 2^24
+                const int64_t row = m0 + n;
 #pragma unroll
-                for (int c = 0; c < CW / 16; ++c) {
-                    tmem_ld16(d + uint32_t(16 * c), v + 16 * c);
-                    if constexpr (MODE == 2) tmem_ld16(d + uint32_t(TT + 16 * c), vl + 16 * c);
+                for (int i = 0; i < CW; ++i) {
+                    const int64_t t = t0 + c0 + i;
+                    if (t < p.T && row < p.N) {
+                        int iv = __float2int_rn(v[i]);
+                        if constexpr (MODE == 2) iv = 128 * iv + __float2int_rn(vl[i]);
+                        p.isum[(t * p.N + row) * (p.K / Q8_QK) + g_begin * kCkGroup + b] = iv;
+                    }
                 }
-                // the block's weight scale while the accumulator is on its way
-                const uint32_t e = scl_a + uint32_t(se * C::kScl);
-                const float sw = DEBUG ? 0.0f : half_bits_to_float(lds16(e + uint32_t(2 * n)));
-                tmem_wait_ld();
-                // the data is in registers: the slot goes back
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tm_empty[(b / C::kGS) % C::kSG]);
-                if constexpr (DEBUG) {
-                    // the plane sums are exact integers below 2^24
-                    const int64_t t0 = int64_t(tx) * TT, row = int64_t(ty) * kCkM + n;
+            } else {
+                if constexpr (MODE == 2) {
+                    // 128*hi + lo rounds once: exactly float(isum)
+                    const uint64_t k128 = f2_pack(128.0f, 128.0f);
 #pragma unroll
-                    for (int u = 0; u < CW; ++u) {
-                        const int64_t t = t0 + c0 + u;
-                        if (t < p.T && row < p.N) {
-                            int iv = __float2int_rn(v[u]);
-                            if constexpr (MODE == 2) iv = 128 * iv + __float2int_rn(vl[u]);
-                            p.isum[(t * p.N + row) * (p.K / Q8_QK) + g_begin * kCkGroup + bl] = iv;
+                    for (int i = 0; i < CW / 2; ++i) {
+                        const uint64_t r = f2_fma(k128, f2_pack(v[2 * i], v[2 * i + 1]),
+                                                  f2_pack(vl[2 * i], vl[2 * i + 1]));
+                        v[2 * i] = f2_lo(r);
+                        v[2 * i + 1] = f2_hi(r);
+                    }
+                }
+                const uint64_t sw2 = f2_pack(sw, sw);
+#pragma unroll
+                for (int i4 = 0; i4 < CW / 4; ++i4) {
+                    const int4 x4 = lds128(e + uint32_t(kCkM * 2 + c0 * 4 + 16 * i4));
+                    const uint64_t c01 = f2_mul(sw2, uint64_t(uint32_t(x4.x)) | (uint64_t(uint32_t(x4.y)) << 32));
+                    const uint64_t c23 = f2_mul(sw2, uint64_t(uint32_t(x4.z)) | (uint64_t(uint32_t(x4.w)) << 32));
+                    acc[2 * i4] = f2_fma(f2_pack(v[4 * i4], v[4 * i4 + 1]), c01, acc[2 * i4]);
+                    acc[2 * i4 + 1] = f2_fma(f2_pack(v[4 * i4 + 2], v[4 * i4 + 3]), c23, acc[2 * i4 + 1]);
+                }
+                // the block's scales are read: its scale entry goes back
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sc_empty[(b >> 2) & 1]);
+            }
+        }
+        if constexpr (!DEBUG) {
+            constexpr int kEpiThreads = 32 * C::kEpiWarps;
+            // every block is consumed once all epilogue warps get here, so the
+            // stage area is free for the end-of-tile scratch
+            named_bar(1, kEpiThreads);
+            if constexpr (C::kEG > 1) {
+                if (eg > 0) {
+#pragma unroll
+                    for (int i = 0; i < CW; ++i)
+                        sts32(stages_a + uint32_t(((eg - 1) * C::kPartial) + ((c0 + i) * kCkM + n) * 4),
+                              (i & 1) ? uint32_t(acc[i >> 1] >> 32) : uint32_t(acc[i >> 1]));
+                }
+                named_bar(1, kEpiThreads);
+                if (eg == 0) {
+                    // the groups' partial sums in group order
+                    for (int g2 = 1; g2 < C::kEG; ++g2) {
+#pragma unroll
+                        for (int i = 0; i < CW / 2; ++i) {
+                            const uint32_t a0 = stages_a + uint32_t((g2 - 1) * C::kPartial + ((c0 + 2 * i) * kCkM + n) * 4);
+                            const uint64_t o = uint64_t(lds32(a0)) | (uint64_t(lds32(a0 + kCkM * 4)) << 32);
+                            acc[i] = f2_add(acc[i], o);
+                        }
+                    }
+                }
+            }
+            if (eg == 0) {
+                const int64_t row = m0 + n;
+                if (gridDim.z == 1) {
+                    if (p.y && row < p.N) {
+#pragma unroll
+                        for (int i = 0; i < CW; ++i) {
+                            const int64_t t = t0 + c0 + i;
+                            const float v = (i & 1) ? f2_hi(acc[i >> 1]) : f2_lo(acc[i >> 1]);
+                            if (t < p.T) p.y[t * p.N + row] = v;
                         }
                     }
                 } else {
-                    if constexpr (MODE == 2) {
-                        // 128*hi + lo rounds once: exactly float(isum)
-                        const uint64_t k128 = f2_pack(128.0f, 128.0f);
+                    // the CTA's partial tile [TT][128] f32 for the cluster sum
 #pragma unroll
-                        for (int u = 0; u < CW / 2; ++u) {
-                            const uint64_t r = f2_fma(k128, f2_pack(v[2 * u], v[2 * u + 1]),
-                                                      f2_pack(vl[2 * u], vl[2 * u + 1]));
-                            v[2 * u] = f2_lo(r);
-                            v[2 * u + 1] = f2_hi(r);
+                    for (int i = 0; i < CW; ++i)
+                        sts32(stages_a + uint32_t(((c0 + i) * kCkM + n) * 4),
+                              (i & 1) ? uint32_t(acc[i >> 1] >> 32) : uint32_t(acc[i >> 1]));
+                }
+                if constexpr (ARGMAX) {
+                    // per activation row: the best (value, lowest row) of this
+                    // warp's 32 weight rows, then of the four quadrants
+                    const uint32_t cand = stages_a + uint32_t(C::kCandOff);
+#pragma unroll
+                    for (int i = 0; i < CW; ++i) {
+                        float v = (i & 1) ? f2_hi(acc[i >> 1]) : f2_lo(acc[i >> 1]);
+                        unsigned ni = unsigned(row);
+                        const bool valid = row < p.N && !(v != v);
+                        if (!valid) {
+                            v = -INFINITY;
+                            ni = 0xffffffffu;
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+                            const unsigned on = __shfl_xor_sync(0xffffffffu, ni, o);
+                            if (ov > v || (ov == v && on < ni)) {
+                                v = ov;
+                                ni = on;
+                            }
+                        }
+                        if (lane == 0) {
+                            sts32(cand + uint32_t((qd * TT + c0 + i) * 8), __float_as_uint(v));
+                            sts32(cand + uint32_t((qd * TT + c0 + i) * 8 + 4), ni);
                         }
                     }
-                    const uint64_t sw2 = f2_pack(sw, sw);
-#pragma unroll
-                    for (int i4 = 0; i4 < CW / 4; ++i4) {
-                        const int4 x4 = lds128(e + uint32_t(kCkM * 2 + c0 * 4 + 16 * i4));
-                        const uint64_t c01 = f2_mul(sw2, uint64_t(uint32_t(x4.x)) | (uint64_t(uint32_t(x4.y)) << 32));
-                        const uint64_t c23 = f2_mul(sw2, uint64_t(uint32_t(x4.z)) | (uint64_t(uint32_t(x4.w)) << 32));
-                        acc[2 * i4] = f2_fma(f2_pack(v[4 * i4], v[4 * i4 + 1]), c01, acc[2 * i4]);
-                        acc[2 * i4 + 1] = f2_fma(f2_pack(v[4 * i4 + 2], v[4 * i4 + 3]), c23, acc[2 * i4 + 1]);
-                    }
-                    // the block's scales are read: its scale entry goes back
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sc_empty[(b >> 2) & 1]);
                 }
             }
-            if constexpr (!DEBUG) {
-                // ---- end of the tile.  Every thread takes part in every
-                // named barrier below whatever its `ok`, so that an early exit
-                // of one warp cannot leave another waiting at one.
-                const bool last = i == ntl - 1;
-                const uint32_t gscr_a = WALK ? smem_u32(gscr) : stages_a;
-                if constexpr (C::kEG > 1) {
-                    // the groups' partial sums, added in group order
-                    if (eg > 0) {
-                        if (i > 0) named_bar(4, kEpiThreads);   // group 0 has read the last ones
-#pragma unroll
-                        for (int u = 0; u < CW; ++u)
-                            sts32(gscr_a + uint32_t(((c0 + u) * kCkM + n) * 4),
-                                  (u & 1) ? uint32_t(acc[u >> 1] >> 32) : uint32_t(acc[u >> 1]));
-                        named_bar_arrive(3, kEpiThreads);
-                    } else {
-                        named_bar(3, kEpiThreads);
-#pragma unroll
-                        for (int u = 0; u < CW / 2; ++u) {
-                            const uint32_t a0 = gscr_a + uint32_t(((c0 + 2 * u) * kCkM + n) * 4);
-                            const uint64_t o = uint64_t(lds32(a0)) | (uint64_t(lds32(a0 + kCkM * 4)) << 32);
-                            acc[u] = f2_add(acc[u], o);
-                        }
-                        if (!last) named_bar_arrive(4, kEpiThreads);
-                    }
-                }
+            if constexpr (ARGMAX) {
+                constexpr int kG0 = 32 * 4 * C::kEC;   // threads of group 0
                 if (eg == 0) {
-                    const int64_t t0 = int64_t(tx) * TT, row = int64_t(ty) * kCkM + n;
-                    if (KIND != kCkPlain || ks == 1) {
-                        if (p.y && row < p.N) {
-#pragma unroll
-                            for (int u = 0; u < CW; ++u) {
-                                const int64_t t = t0 + c0 + u;
-                                const float v = (u & 1) ? f2_hi(acc[u >> 1]) : f2_lo(acc[u >> 1]);
-                                if (t < p.T) p.y[t * p.N + row] = v;
+                    named_bar(2, kG0);
+                    const int j = (ec * 4 + ((warp - C::kEpiWarp0) & 3)) * 32 + lane;   // 0..kG0-1
+                    const uint32_t cand = stages_a + uint32_t(C::kCandOff);
+                    for (int col = j; col < TT; col += kG0) {
+                        float bv = -INFINITY;
+                        unsigned bn = 0xffffffffu;
+                        for (int q2 = 0; q2 < 4; ++q2) {   // quadrants in row order
+                            const float ov = __uint_as_float(lds32(cand + uint32_t((q2 * TT + col) * 8)));
+                            const unsigned on = lds32(cand + uint32_t((q2 * TT + col) * 8 + 4));
+                            if (ov > bv || (ov == bv && on < bn)) {
+                                bv = ov;
+                                bn = on;
                             }
                         }
-                    } else if (WALK && KIND == kCkPlain && !last) {
-                        // split K, a tile before the last: the tile's weight
-                        // rows are shared out over the cluster (rows
-                        // [r0[q], r0[q+1]) to CTA q); each thread pushes its
-                        // row's partials to the row's owner (st.async, counted
-                        // in bytes on the owner's red_full), and the owner adds
-                        // them in rank order once all have arrived
-                        const uint32_t recv_a = smem_u32(recv);
-                        const int q = ((n + 1) * ks - 1) >> 7;   // owner of row n (128 rows)
-                        const int rq = p.r0[q], maxr = p.maxr;
-                        if (i == 0) cluster_wait();   // group 0 meets the cluster here, the rest at the end
-                        if (i > 0 && ok) ok = mbar_wait_cluster(sent_ok, uint32_t(i - 1) & 1u, p.err);
-                        if (q != rank) {
-                            const int slot = rank < q ? rank : rank - 1;
-                            const uint32_t dst = cluster_map(
-                                recv_a + uint32_t(((slot * maxr + n - rq) * TT + c0) * 4), uint32_t(q));
-                            const uint32_t bar = cluster_map(smem_u32(red_full), uint32_t(q));
-#pragma unroll
-                            for (int u = 0; u < CW / 4; ++u)
-                                st_async_v4(dst + uint32_t(16 * u), acc[2 * u], acc[2 * u + 1], bar);
-                        }
-                        if (n == 0 && ec == 0) {
-                            // this CTA's rows from each of the others
-                            const int own = p.r0[rank + 1] - p.r0[rank];
-                            mbar_arrive_expect_tx(red_full, uint32_t((ks - 1) * own * TT * 4));
-                        }
-                        if (ok) ok = mbar_wait_cluster(red_full, uint32_t(i) & 1u, p.err);
-                        if (q == rank) {   // the sums replace the partials
-#pragma unroll
-                            for (int u = 0; u < CW / 4; ++u) {
-                                uint64_t s01 = 0, s23 = 0;
-                                for (int r = 0; r < ks; ++r) {
-                                    uint64_t v01 = acc[2 * u], v23 = acc[2 * u + 1];
-                                    if (r != rank) {
-                                        const int slot = r < rank ? r : r - 1;
-                                        const int4 v = lds128(recv_a + uint32_t(((slot * maxr + n - rq) * TT + c0 + 4 * u) * 4));
-                                        v01 = uint64_t(uint32_t(v.x)) | (uint64_t(uint32_t(v.y)) << 32);
-                                        v23 = uint64_t(uint32_t(v.z)) | (uint64_t(uint32_t(v.w)) << 32);
-                                    }
-                                    s01 = f2_add(s01, v01);
-                                    s23 = f2_add(s23, v23);
-                                }
-                                acc[2 * u] = s01;
-                                acc[2 * u + 1] = s23;
-                            }
-                        }
-                        // the pushed partials are read (the sums above used
-                        // them): the others may push the next tile's
-                        for (int r = 0; r < ks; ++r)
-                            if (r != rank) mbar_arrive_remote_relaxed(cluster_map(smem_u32(sent_ok), uint32_t(r)));
-                        if (q == rank && row < p.N) {
-#pragma unroll
-                            for (int u = 0; u < CW; ++u) {
-                                const float v = (u & 1) ? f2_hi(acc[u >> 1]) : f2_lo(acc[u >> 1]);
-                                if (t0 + c0 + u < p.T) p.y[(t0 + c0 + u) * p.N + row] = v;
-                            }
-                        }
-                    } else if (KIND == kCkPlain) {
-                        // split K, the last tile: the CTA's partial tile
-                        // [TT][128] f32 for the cluster sum after the pipeline
-                        // is drained (the stage area is free by then)
-#pragma unroll
-                        for (int u = 0; u < CW; ++u)
-                            sts32(stages_a + uint32_t(((c0 + u) * kCkM + n) * 4),
-                                  (u & 1) ? uint32_t(acc[u >> 1] >> 32) : uint32_t(acc[u >> 1]));
+                        const int64_t t = t0 + col;
+                        if (t < p.T && bn != 0xffffffffu) atomicMax(p.keys + t, argmax_key(bv, bn));
                     }
-                    if constexpr (ARGMAX) {
-                        const uint32_t cand_a = WALK ? smem_u32(cand) : stages_a + uint32_t(C::kCandOff);
-                        const int j0 = (ec * 4 + (ew & 3)) * 32 + lane;   // 0..kG0-1 in group 0
-                        // per activation row: the best (value, lowest row) of
-                        // this warp's 32 weight rows, then of the four quadrants
-#pragma unroll
-                        for (int u = 0; u < CW; ++u) {
-                            float v = (u & 1) ? f2_hi(acc[u >> 1]) : f2_lo(acc[u >> 1]);
-                            unsigned ni = unsigned(row);
-                            const bool valid = row < p.N && !(v != v);
-                            if (!valid) {
-                                v = -INFINITY;
-                                ni = 0xffffffffu;
-                            }
-#pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) {
-                                const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-                                const unsigned on = __shfl_xor_sync(0xffffffffu, ni, o);
-                                if (ov > v || (ov == v && on < ni)) {
-                                    v = ov;
-                                    ni = on;
-                                }
-                            }
-                            if (lane == 0) {
-                                sts32(cand_a + uint32_t((qd * TT + c0 + u) * 8), __float_as_uint(v));
-                                sts32(cand_a + uint32_t((qd * TT + c0 + u) * 8 + 4), ni);
-                            }
-                        }
-                        named_bar(2, kG0);
-                        for (int col = j0; col < TT; col += kG0) {
-                            float bv = -INFINITY;
-                            unsigned bn = 0xffffffffu;
-                            for (int q2 = 0; q2 < 4; ++q2) {   // quadrants in row order
-                                const float ov = __uint_as_float(lds32(cand_a + uint32_t((q2 * TT + col) * 8)));
-                                const unsigned on = lds32(cand_a + uint32_t((q2 * TT + col) * 8 + 4));
-                                if (ov > bv || (ov == bv && on < bn)) {
-                                    bv = ov;
-                                    bn = on;
-                                }
-                            }
-                            const int64_t t = t0 + col;
-                            if (t < p.T && bn != 0xffffffffu) atomicMax(p.keys + t, argmax_key(bv, bn));
-                        }
+                    __threadfence();
+                    named_bar(2, kG0);
+                    if (j == 0) s_last = atomicAdd(p.ticket, 1u) == gridDim.x * gridDim.y - 1u;
+                    named_bar(2, kG0);
+                    if (s_last) {
+                        // the last CTA: every row's token, and the keys and the
+                        // ticket cleared for the next call
                         __threadfence();
-                        named_bar(2, kG0);
-                        if (j0 == 0) s_last = atomicAdd(p.ticket, 1u) == unsigned(p.tiles) - 1u;
-                        named_bar(2, kG0);
-                        if (s_last) {
-                            // the last tile: every row's token, and the keys
-                            // and the ticket cleared for the next call
-                            __threadfence();
-                            for (int64_t t = j0; t < p.T; t += kG0) {
-                                const unsigned long long key = atomicExch(p.keys + t, 0ull);
-                                int32_t tk;
-                                double val;
-                                argmax_unkey(key, tk, val);
-                                p.tok[t] = tk;
-                                if (p.maxval) p.maxval[t] = val;
-                            }
-                            if (j0 == 0) *p.ticket = 0u;
+                        for (int64_t t = j; t < p.T; t += kG0) {
+                            const unsigned long long key = atomicExch(p.keys + t, 0ull);
+                            int32_t tk;
+                            double val;
+                            argmax_unkey(key, tk, val);
+                            p.tok[t] = tk;
+                            if (p.maxval) p.maxval[t] = val;
                         }
-                        // the candidates and s_last are read before the next
-                        // tile writes them
-                        named_bar(2, kG0);
+                        if (j == 0) *p.ticket = 0u;
                     }
                 }
-            }
-            tx += p.dtx;
-            ty += p.dty;
-            if (tx >= p.t_tiles) {
-                tx -= p.t_tiles;
-                ++ty;
             }
         }
     }
 
-    if (walk_split && !(warp >= C::kEpiWarp0 && ((warp - C::kEpiWarp0) >> 2) / C::kEC == 0)) cluster_wait();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    if (KIND == kCkPlain && ks > 1 && ntl > 0) {
-        // the last tile's split-K sum: each CTA adds a slice of it over the
-        // cluster, in rank order
+    if (!DEBUG && gridDim.z > 1) {
         cluster_sync();
-        const int64_t t0 = tile_t0(ntl - 1), m0 = tile_m0(ntl - 1);
+        const uint32_t ks = gridDim.z, rank = blockIdx.z;
         const int n4 = TT * kCkM / 4;
-        const int per = (n4 + ks - 1) / ks;
-        const int i_end = min(n4, (rank + 1) * per);
+        const int per = (n4 + int(ks) - 1) / int(ks);
+        const int i_end = min(n4, int(rank + 1) * per);
         const uint32_t base = stages_a;
-        for (int i = rank * per + tid; i < i_end; i += C::kThreads) {
+        for (int i = int(rank) * per + tid; i < i_end; i += C::kThreads) {
             float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int r = 0; r < ks; ++r) {
-                const float4 v = ld_cluster_v4(cluster_map(base + uint32_t(i) * 16u, uint32_t(r)));
+            for (uint32_t r = 0; r < ks; ++r) {
+                const float4 v = ld_cluster_v4(cluster_map(base + uint32_t(i) * 16u, r));
                 s.x += v.x;
                 s.y += v.y;
                 s.z += v.z;
@@ -1067,18 +823,10 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, u
               sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Whether a configuration has the walking layout: plain projections with a
-// small tile (where the start-up and the end of a tile weigh most against its
-// blocks), and the multi-row LM head.
-template <int MODE, int TT, int KIND>
-constexpr bool ck_walks() {
-    return (KIND == kCkPlain && CkCfg<MODE, TT, true>::kN <= 64) || (KIND == kCkArgmax && TT == 16);
-}
-
 // Clusters of `ks` CTAs of this kernel that fit on the device at once.
-template <int MODE, int TT, int KIND, bool WALK>
+template <int MODE, int TT, int KIND>
 static int active_clusters(int ks, const LaunchCtx& ctx) {
-    using C = CkCfg<MODE, TT, WALK>;
+    using C = CkCfg<MODE, TT>;
     // per device and split; threads that race here store the same value
     static std::atomic<int> cache[kMaxDevices][kCkMaxSplit + 1];
     std::atomic<int>& slot = cache[ctx.dev][ks];
@@ -1097,7 +845,7 @@ static int active_clusters(int ks, const LaunchCtx& ctx) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, chunk_kernel<MODE, TT, KIND, WALK>, &cfg) == cudaSuccess &&
+        if (cudaOccupancyMaxActiveClusters(&c, chunk_kernel<MODE, TT, KIND>, &cfg) == cudaSuccess &&
             c > 0)
             n = c;
         else
@@ -1108,51 +856,22 @@ static int active_clusters(int ks, const LaunchCtx& ctx) {
     return n;
 }
 
-struct CkPlan {
-    int ks = 1;          // CTAs of a cluster, each over its range of K
-    bool walk = false;   // the walking layout
-    int64_t ncl = 1;     // clusters
-};
-
-// The split of K and the layout, by an estimate of the launch's time in ns
-// on the busiest SM (calibrated on gate+up 28672 x 4096 and Wqkv 6144 x 4096
-// runs): an 8-block group of a tile takes G(N) (N = the MMA's N); one tile per
-// cluster, in waves of the clusters that fit, costs ~6.5 us a wave for the
-// start-up and the end of its tiles; walking (where the configuration has it
-// and its receive area takes the split) pays ~3 us once and 3-5 us at the end
-// of each tile, and only wins where there would be more than one wave.
-// Splits are powers of two: clusters of 3 (48 of them, where the occupancy
-// query allows 50) ran a 6144 x 4096 projection at 1.6x the time of clusters
-// of 2 in back-to-back launches, though the estimate favours them.
-constexpr int64_t ck_group_ns(int n) { return n <= 16 ? 1340 : n <= 32 ? 1700 : n <= 64 ? 2460 : 3750; }
-
+// Split of K over a cluster: the count with the fewest 8-block groups on
+// the busiest SM, counting whole waves of clusters.  Powers of two only:
+// clusters of 3 (48 of them, where the occupancy query allows 50) ran a
+// 6144 x 4096 projection at 1.6x the time of clusters of 2 in back-to-back
+// launches, although this count favours them.
 template <int MODE, int TT, int KIND>
-static CkPlan choose_plan(int64_t tiles, int groups, const LaunchCtx& ctx) {
-    constexpr int64_t G = ck_group_ns(CkCfg<MODE, TT>::kN);
-    constexpr int64_t kWave = 6500, kWalkOnce = 3000, kWalkTile = CkCfg<MODE, TT>::kN <= 32 ? 3000 : 5000;
-    CkPlan best;
+static int choose_split(int64_t tiles, int groups, const LaunchCtx& ctx) {
+    int best = 1;
     int64_t best_cost = -1;
-    auto consider = [&](int64_t cost, int ks, bool walk, int64_t ncl) {
+    for (int ks = 1; ks <= kCkMaxSplit && ks <= groups; ks *= 2) {
+        const int ac = active_clusters<MODE, TT, KIND>(ks, ctx);
+        const int64_t waves = (tiles + ac - 1) / ac;
+        const int64_t cost = waves * ((groups + ks - 1) / ks);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
-            best.ks = ks;
-            best.walk = walk;
-            best.ncl = ncl;
-        }
-    };
-    const int kmax = KIND == kCkPlain ? kCkMaxSplit : 1;   // only plain projections split K
-    for (int k = 1; k <= kmax && k <= groups; k *= 2) {
-        const int per = (groups + k - 1) / k, ks = (groups + per - 1) / per;
-        if (ks != k) continue;   // the same split as a smaller k
-        const int64_t ac = active_clusters<MODE, TT, KIND, false>(ks, ctx);
-        const int64_t waves = (tiles + ac - 1) / ac;
-        consider(waves * (per * G + kWave), ks, false, tiles);
-        if constexpr (ck_walks<MODE, TT, KIND>()) {
-            if (ks <= CkCfg<MODE, TT, true>::kRecvKs) {
-                const int64_t acw = active_clusters<MODE, TT, KIND, true>(ks, ctx);
-                const int64_t wv = (tiles + acw - 1) / acw;
-                if (wv > 1) consider(wv * (per * G + kWalkTile) + kWalkOnce, ks, true, acw);
-            }
+            best = ks;
         }
     }
     return best;
@@ -1167,76 +886,41 @@ struct ChunkOut {
     double* maxval = nullptr;
 };
 
-struct CkMaps {
-    alignas(64) CUtensorMap w, xh, xl, s, xd;
-};
-
-template <int MODE, int TT, int KIND, bool WALK>
-static cudaError_t launch_chunk_k(const CkMaps& m, const CkParams& p, int64_t ncl, int ks,
-                                  const LaunchCtx& ctx) {
-    using C = CkCfg<MODE, TT, WALK>;
-    auto kern = chunk_kernel<MODE, TT, KIND, WALK>;
-    static std::atomic<bool> configured[kMaxDevices];
-    if (const cudaError_t e = set_smem_once(kern, size_t(C::kSmem), ctx.dev, configured); e != cudaSuccess)
-        return e;
-    cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attrs[2];
-    // walking: clusters along x; else one CTA (cluster) per tile, (T tiles, N tiles)
-    cfg.gridDim = WALK ? dim3(unsigned(ncl), 1u, unsigned(ks))
-                       : dim3(unsigned(p.t_tiles), unsigned(p.tiles / p.t_tiles), unsigned(ks));
-    cfg.blockDim = dim3(C::kThreads);
-    cfg.dynamicSmemBytes = C::kSmem;
-    cfg.stream = ctx.stream;
-    int na = pdl_attrs(ctx, attrs);
-    if (ks > 1) {
-        attrs[na].id = cudaLaunchAttributeClusterDimension;
-        attrs[na].val.clusterDim.x = 1;
-        attrs[na].val.clusterDim.y = 1;
-        attrs[na].val.clusterDim.z = unsigned(ks);
-        ++na;
-    }
-    cfg.numAttrs = na;
-    cfg.attrs = attrs;
-    return cudaLaunchKernelEx(&cfg, kern, m.w, m.xh, m.xl, m.s, m.xd, p);
-}
-
 template <int MODE, int TT, int KIND>
 static cudaError_t launch_chunk_t(const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                                   const void* xq, const float* xd, int64_t T, const ChunkOut& out,
                                   const LaunchCtx& ctx) {
+    using C = CkCfg<MODE, TT>;
     constexpr bool DEBUG = KIND == kCkDebug;
-    CkMaps m;
+    auto kern = chunk_kernel<MODE, TT, KIND>;
+    static std::atomic<bool> configured[kMaxDevices];
+    if (const cudaError_t e = set_smem_once(kern, size_t(C::kSmem), ctx.dev, configured); e != cudaSuccess)
+        return e;
+    alignas(64) CUtensorMap tw, txh, txl, ts, txd;
     const int64_t nb = K / Q8_QK;
     const int8_t* xh = reinterpret_cast<const int8_t*>(xq);
-    bool ok = make_map(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, K, N, K, kCkStageK, kCkM,
+    bool ok = make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, K, N, K, kCkStageK, kCkM,
                        CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map(&m.xh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, K, T, K, kCkStageK, TT,
+              make_map(&txh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, K, T, K, kCkStageK, TT,
                        CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map(&m.xl, CU_TENSOR_MAP_DATA_TYPE_UINT8, MODE == 2 ? xh + T * K : xh, K, T, K,
+              make_map(&txl, CU_TENSOR_MAP_DATA_TYPE_UINT8, MODE == 2 ? xh + T * K : xh, K, T, K,
                        kCkStageK, TT, CU_TENSOR_MAP_SWIZZLE_128B) &&
               // (the debug variant reads neither scale array: any valid base will do)
-              make_map(&m.s, CU_TENSOR_MAP_DATA_TYPE_UINT16, DEBUG ? static_cast<const void*>(q) : s,
+              make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, DEBUG ? static_cast<const void*>(q) : s,
                        nb, N, nb * 2, kCkGroup, kCkM, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&m.xd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, DEBUG ? static_cast<const void*>(q) : xd,
+              make_map(&txd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, DEBUG ? static_cast<const void*>(q) : xd,
                        DEBUG ? nb / 2 : nb, DEBUG ? N : T, nb * 4, 4, TT, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return cudaErrorInvalidValue;
     const int64_t t_tiles = (T + TT - 1) / TT, n_tiles = (N + kCkM - 1) / kCkM;
-    const int64_t tiles = t_tiles * n_tiles;
-    if (t_tiles > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;   // grid y
+    if (t_tiles > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
     const int groups = int(K / (Q8_QK * kCkGroup));
-    const CkPlan plan = choose_plan<MODE, TT, KIND>(tiles, groups, ctx);
-    const int ks = plan.ks, per = (groups + ks - 1) / ks;
+    const int ks = KIND != kCkPlain ? 1 : choose_split<MODE, TT, KIND>(t_tiles * n_tiles, groups, ctx);
+    const int per = (groups + ks - 1) / ks;
     CkParams p{};
     p.N = N;
     p.K = K;
     p.T = T;
-    p.tiles = int(tiles);
-    p.t_tiles = int(t_tiles);
     p.groups_per_split = per;
-    p.dtx = int(plan.ncl % t_tiles);
-    p.dty = int(plan.ncl / t_tiles);
-    p.maxr = (kCkM + ks - 1) / ks;
-    for (int q = 0; q <= ks; ++q) p.r0[q] = q * kCkM / ks;
     p.y = out.y;
     p.isum = out.isum;
     p.err = ctx.dev_err;
@@ -1246,22 +930,38 @@ static cudaError_t launch_chunk_t(const int8_t* q, const uint16_t* s, int64_t N,
         p.tok = out.tok;
         p.maxval = out.maxval;
     }
-    if constexpr (ck_walks<MODE, TT, KIND>()) {
-        if (plan.walk) return launch_chunk_k<MODE, TT, KIND, true>(m, p, plan.ncl, ks, ctx);
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attrs[2];
+    cfg.gridDim = dim3(unsigned(t_tiles), unsigned(n_tiles), unsigned((groups + per - 1) / per));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = ctx.stream;
+    int na = pdl_attrs(ctx, attrs);
+    if (cfg.gridDim.z > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 1;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = cfg.gridDim.z;
+        ++na;
     }
-    return launch_chunk_k<MODE, TT, KIND, false>(m, p, plan.ncl, ks, ctx);
+    cfg.numAttrs = na;
+    cfg.attrs = attrs;
+    return cudaLaunchKernelEx(&cfg, kern, tw, txh, txl, ts, txd, p);
 }
 
 template <int MODE, int TT, int KIND>
-static void plan_of(int64_t N, int64_t K, int64_t T, const LaunchCtx& ctx, int64_t* out) {
+static void plan_of(int64_t N, int64_t K, const int64_t T, const LaunchCtx& ctx, int64_t* out) {
     const int64_t tiles = ((T + TT - 1) / TT) * ((N + kCkM - 1) / kCkM);
-    const CkPlan pl = choose_plan<MODE, TT, KIND>(tiles, int(K / (Q8_QK * kCkGroup)), ctx);
+    const int groups = int(K / (Q8_QK * kCkGroup));
+    const int kc = KIND != kCkPlain ? 1 : choose_split<MODE, TT, KIND>(tiles, groups, ctx);
+    const int per = (groups + kc - 1) / kc, ks = (groups + per - 1) / per;
+    const int64_t ac = active_clusters<MODE, TT, KIND>(ks, ctx);
     out[0] = TT;
-    out[1] = pl.ks;
-    out[2] = pl.walk ? 1 : 0;
-    out[3] = pl.ncl;
-    out[4] = tiles;
-    out[5] = pl.walk ? CkCfg<MODE, TT, true>::kStages : CkCfg<MODE, TT, false>::kStages;
+    out[1] = ks;
+    out[2] = tiles;
+    out[3] = ac;
+    out[4] = (tiles + ac - 1) / ac;
+    out[5] = CkCfg<MODE, TT>::kStages;
 }
 
 template <int KIND>

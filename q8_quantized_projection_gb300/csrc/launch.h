@@ -98,9 +98,8 @@ cudaError_t launch_chunk_argmax(int mode, const int8_t* q, const uint16_t* s, in
                                 const void* xq, const float* xd, int64_t T, float* logits,
                                 int32_t* tok, double* maxval, void* ws, const LaunchCtx& ctx);
 // The launch plan the chunk path would use (host side; occupancy queries
-// only): out[6] = TT, ks (CTAs splitting K), walk (1: clusters walk several
-// tiles), clusters, tiles, pipeline stages.  False where the path does not
-// apply (mode, K).
+// only): out[6] = TT, ks (CTAs splitting K), tiles, clusters that fit at once,
+// waves, pipeline stages.  False where the path does not apply (mode, K).
 bool chunk_plan(int mode, int64_t N, int64_t K, int64_t T, bool argmax, const LaunchCtx& ctx,
                 int64_t* out);
 // Activation rows from which projections run on the tensor cores: where one

@@ -250,7 +250,7 @@ def q8_debug_row_geometry(mode, rows, n, k, grid, cta):
     return dict(zip(ROW_GEOMETRY_FIELDS, list(out)))
 
 
-CHUNK_PLAN_FIELDS = ("TT", "ks", "walk", "clusters", "tiles", "stages")
+CHUNK_PLAN_FIELDS = ("TT", "ks", "tiles", "clusters", "waves", "stages")
 
 
 def q8_debug_chunk_plan(mode, n, k, t, argmax=False):

@@ -592,21 +592,20 @@ def test_chunk_tensor_core_parity(mode, n, k, t):
     assert np.array_equal(host(y).view(np.uint32), host(y2).view(np.uint32))
 
 
-# Shapes with more 128 x TT tiles than clusters that fit, so that each cluster
-# walks several tiles: K unsplit (256), and split over 2 or 4 CTAs whose
-# partials of every tile but the last meet in the owning CTA (K = 2304: 9
-# groups of 8 blocks split 5 + 4; a ragged last tile at N = 20000).
-WALK_SHAPES = [("i8", 16, 40000, 256), ("i8", 16, 20000, 2048), ("i8", 5, 20000, 6144),
+# Shapes with more 128 x TT tiles than clusters that fit, so that the clusters
+# run in several waves: K unsplit (256), and split over a cluster of CTAs whose
+# partials meet in distributed shared memory (K = 2304: 9 groups of 8 blocks
+# split 5 + 4; a ragged last tile at N = 20000).
+WAVE_SHAPES = [("i8", 16, 40000, 256), ("i8", 16, 20000, 2048), ("i8", 5, 20000, 6144),
                ("i8", 16, 20000, 8192), ("i8", 32, 20000, 12288), ("i8", 40, 20000, 8192),
                ("i8x2", 16, 25600, 2304), ("i8x2", 32, 20000, 2048)]
 
 
-@pytest.mark.parametrize("mode,t,n,k", WALK_SHAPES)
-def test_chunk_walking_tiles_sampled(mode, t, n, k):
+@pytest.mark.parametrize("mode,t,n,k", WAVE_SHAPES)
+def test_chunk_many_tiles_sampled(mode, t, n, k):
     plan = native.q8_debug_chunk_plan(mode, n, k, t)
-    assert plan["walk"] == 1 and plan["tiles"] > plan["clusters"], plan
-    if k > 256:
-        assert plan["ks"] > 1, plan
+    assert plan["waves"] > 1 and plan["tiles"] > plan["clusters"], plan
+    assert plan["ks"] & (plan["ks"] - 1) == 0, plan   # splits are powers of two
     rng = np.random.default_rng(6000 + t + n + k)
     q, s = synth.q8_weights(rng, n, k)
     act = orc.quantize(mode, synth.activations(rng, t, k))
@@ -621,17 +620,20 @@ def test_chunk_walking_tiles_sampled(mode, t, n, k):
     idx = np.unique(np.concatenate([np.arange(128), np.arange((n - 1) // 128 * 128, n),
                                     np.arange(mid - 3, mid + 3), rng.integers(0, n, 300)]))
     y_o, norm = orc.project(mode, q[idx], s[idx], act)
-    check_close(mode, host(y)[:, idx], y_o, norm, what=f"walking chunk {mode} {n}x{k} T={t} {plan}")
+    check_close(mode, host(y)[:, idx], y_o, norm, what=f"chunk {mode} {n}x{k} T={t} {plan}")
     # the split-K sums are added in rank order: the same bits every time
     y2 = tt.empty_like(y)
     native.q8_proj_chunk(mode, qd, sd, xq, xd, t, y2)
     assert np.array_equal(host(y).view(np.uint32), host(y2).view(np.uint32))
 
 
-def test_head_plan_walks_tiles():
-    """The 16-row LM head on the tensor cores walks its 1002 tiles."""
+def test_head_plan():
+    """The 16-row LM head on the tensor cores: 1002 tiles of 128 x 16, K
+    unsplit (the arg-max needs whole dots), one CTA per SM at a time."""
     plan = native.q8_debug_chunk_plan("i8", *synth.HEAD_SHAPE, 16, argmax=True)
-    assert plan["walk"] == 1 and plan["ks"] == 1 and plan["tiles"] == 1002, plan
+    assert plan["ks"] == 1 and plan["tiles"] == 1002 and plan["TT"] == 16, plan
+    sms = torch().cuda.get_device_properties(0).multi_processor_count
+    assert plan["clusters"] == sms and plan["waves"] == -(-1002 // sms), plan
 
 
 @pytest.mark.parametrize("mode", ["i8", "i8x2"])
