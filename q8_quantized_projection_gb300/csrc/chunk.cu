@@ -220,6 +220,12 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The arriving half of named barrier `id`: counts this warp's threads towards
+// `count` without waiting (the other side waits with named_bar).
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
@@ -638,17 +644,22 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
         }
         if constexpr (!DEBUG) {
             constexpr int kEpiThreads = 32 * C::kEpiWarps;
-            // every block is consumed once all epilogue warps get here, so the
-            // stage area is free for the end-of-tile scratch
-            named_bar(1, kEpiThreads);
+            // The stage area is free for the end-of-tile scratch once a warp
+            // has its last block: that block's MMAs have completed, so the
+            // converters have read every stage.  Group 1 (its last block is
+            // the tile's last) writes its partial sums there and group 0 waits
+            // only for that.
             if constexpr (C::kEG > 1) {
+                static_assert(C::kEG == 2, "one partial-sum exchange");
                 if (eg > 0) {
 #pragma unroll
                     for (int i = 0; i < CW; ++i)
                         sts32(stages_a + uint32_t(((eg - 1) * C::kPartial) + ((c0 + i) * kCkM + n) * 4),
                               (i & 1) ? uint32_t(acc[i >> 1] >> 32) : uint32_t(acc[i >> 1]));
+                    named_bar_arrive(1, kEpiThreads);
+                } else {
+                    named_bar(1, kEpiThreads);
                 }
-                named_bar(1, kEpiThreads);
                 if (eg == 0) {
                     // the groups' partial sums in group order
                     for (int g2 = 1; g2 < C::kEG; ++g2) {
