@@ -382,17 +382,23 @@ def run_ours(args, world, rank, local):
             if rank == 0:
                 print(json.dumps({"case": args.case, "launches": args.warmup + args.steps}))
             return
-        # MODE:PROJ[:fused], PROJ one of the layer's matrices or "all" (the four
-        # in layer order each iteration)
+        # MODE:PROJ[:fused | :rowsR], PROJ one of the layer's matrices or "all"
+        # (the four in layer order each iteration); rowsR: a batch of R rows
+        # through q8_proj (R seeded RMSNorm(N(0,1)) rows)
         mode, proj = parts[0], parts[1]
         fused = len(parts) > 2 and parts[2] == "fused"
+        nrows = int(parts[2][4:]) if len(parts) > 2 and parts[2].startswith("rows") else 1
         names = [nm for nm, _, _ in synth.LAYER_D4096]
         projs = list(range(len(names))) if proj == "all" else [names.index(proj)]
-        acts = {}
+        acts, Yb = {}, {}
         for p in projs:
             k = synth.LAYER_D4096[p][2]
-            acts[p] = native.activation_buffers(mode, 1, k, device=dev)
-            native.act_quant(mode, H[p], acts[p][0], acts[p][1], norm=True)
+            acts[p] = native.activation_buffers(mode, nrows, k, device=dev)
+            hb = H[p] if nrows == 1 else torch.from_numpy(
+                synth.activations(np.random.default_rng(20 + p), nrows, k)).to(dev)
+            native.act_quant(mode, hb, acts[p][0], acts[p][1], norm=True)
+            Yb[p] = Y[mode][p] if nrows == 1 else torch.empty(
+                (nrows, synth.LAYER_D4096[p][1]), dtype=torch.float32, device=dev)
         for i in range(args.warmup + args.steps):
             for p in projs:
                 if fused:
@@ -400,7 +406,7 @@ def run_ours(args, world, rank, local):
                                          Y[mode][p], WS[mode][p])
                 else:
                     native.q8_proj(mode, Q[i % COPIES][p], S[i % COPIES][p], acts[p][0],
-                                   acts[p][1], 1, Y[mode][p])
+                                   acts[p][1], nrows, Yb[p])
         torch.cuda.synchronize(dev)
         if rank == 0:
             print(json.dumps({"case": args.case,
