@@ -307,6 +307,20 @@ q8_status q8_debug_row_geometry(int mode, int64_t rows, int64_t N, int64_t K, in
                                 int64_t* out);
 
 /*
+ * Debug, host only: the same 21 fields for the decode launch of a fused call
+ * at rows = 1 and K <= 16384 values, by its producer: prod 0 q8_proj_fused
+ * (and its KV-row form), 1 q8_proj_fused_residual, 2 q8_proj_fused_swiglu.
+ * The int8 modes and the plain producer run the rows = 1 geometry above.  In
+ * f32 mode the residual and SwiGLU producers above 4096 values shorten the
+ * ring (field 16): the converted activation (128 bytes a 32-value block, 4K
+ * bytes rounded up to 1 KB) stays in shared memory after it for the whole
+ * launch.  Errors as q8_debug_row_geometry (prod outside 0..2: Q8_ERR_ARG);
+ * Q8_ERR_UNSUPPORTED above 16384 values.
+ */
+q8_status q8_debug_row_geometry_fused(int mode, int prod, int64_t N, int64_t K, int grid,
+                                      int cta, int64_t* out);
+
+/*
  * Debug, host side (the current device's occupancy is queried; nothing is
  * launched): the plan of the tensor-core path for a projection of T rows
  * (argmax = 0: q8_proj_chunk and q8_proj from 9 one-word / 5 two-word rows;

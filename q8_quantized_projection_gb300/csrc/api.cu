@@ -171,7 +171,7 @@ const char* q8_status_str(int status) {
     }
 }
 
-int q8_version(void) { return 105; }
+int q8_version(void) { return 106; }
 
 int q8_last_cuda_error(void) { return t_last_cuda; }
 

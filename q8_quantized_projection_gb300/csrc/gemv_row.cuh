@@ -56,7 +56,30 @@ __host__ __device__ constexpr int row_ring() {
     return MODE == 0 ? kRowRingF32 : kRowRing;
 }
 constexpr int kRowPsumBytes = 16384;   // part sums of one super-block of rows
-constexpr int kRowEpBytes = 1024;      // f32 mode: the parts' binades, beside the part sums
+// f32 mode, beside the part sums: the (slice, part) binades in the first half,
+// the 32-value blocks' binades of a shared block conversion (up to 16384
+// values) in the second
+constexpr int kRowEpBytes = 2048;
+constexpr int kRowEpPartBytes = 1024;
+
+// Weight-ring bytes of a launch.  f32 mode with a residual or SwiGLU producer
+// fused and more than 4096 values a row: the converted activation (128 bytes
+// of planes a 32-value block, 4K bytes; the residual producer stages its
+// input s there first) stays in shared memory for the whole launch, in the
+// ring's last 4K bytes (rounded up to 1 KB), which the stages give up.  K <=
+// 16384 there, so at least 128 KB of stages remain.  (The plain RMSNorm
+// producer keeps the full ring: its per-warp conversion is cheap, and in a
+// chained layer the deeper ring measured faster than converting once.)
+template <int MODE, bool FUSE, int PROD>
+__host__ __device__ inline bool row_planes_after_ring(int64_t K) {
+    return MODE == 0 && FUSE && PROD != kProdPlain && K > 4096;
+}
+template <int MODE, bool FUSE, int PROD>
+__host__ __device__ inline int row_ring_of(int64_t K) {
+    if (row_planes_after_ring<MODE, FUSE, PROD>(K))
+        return row_ring<MODE>() - int((4 * K + 1023) & ~int64_t(1023));
+    return row_ring<MODE>();
+}
 
 // 16-byte chunks a lane owns per part: the activation registers (R rows, one
 // or two planes, or 17 words of fixed point in f32 mode) stay within ~32.
@@ -143,7 +166,7 @@ __host__ __device__ inline RowGeo row_geo(int64_t N, int64_t K, int G, int c, in
     const int64_t per_row = int64_t(g.nks) * g.nprr * psum_row_unit;
     const int64_t ep_bytes = (int64_t(g.nks) * g.nprr * part_extra + 15) & ~int64_t(15);
     g.ep_off = kRowPsumBytes;   // in an area of kRowEpBytes after the part sums
-    g.sbrows = ep_bytes > kRowEpBytes ? 0 : ((kRowPsumBytes / per_row) / g.RS) * g.RS;
+    g.sbrows = ep_bytes > kRowEpPartBytes ? 0 : ((kRowPsumBytes / per_row) / g.RS) * g.RS;
     return g;
 }
 
@@ -222,6 +245,22 @@ __device__ __forceinline__ DF warp_sum_rows(const DF (&v)[R], int lane) {
     return s;
 }
 
+// A lane's 32-value block of f32-mode planes from shared memory (block b's
+// 16-byte word group i in slot i ^ (b & 7) of its 128 bytes) and its binade.
+__device__ __forceinline__ void load_planes_block(uint32_t planes_a, const short* pe, int blk,
+                                                  FixChunk32& f) {
+    const uint32_t base = planes_a + uint32_t(blk) * 128u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int4 v = lds128(base + uint32_t(((i ^ (blk & 7)) << 4)));
+        f.p[i >> 1][4 * (i & 1) + 0] = v.x;
+        f.p[i >> 1][4 * (i & 1) + 1] = v.y;
+        f.p[i >> 1][4 * (i & 1) + 2] = v.z;
+        f.p[i >> 1][4 * (i & 1) + 3] = v.w;
+    }
+    f.e = pe[blk];
+}
+
 // v * 2^d for d <= 0 by two multiplies by normal powers of two (exact but in
 // the subnormal range); a part more than 2^252 below the row's largest is
 // dropped.
@@ -297,7 +336,7 @@ __device__ __forceinline__ void kv_store(const GemvParams& p, const int* s_pos, 
 // cut into slices whose count divides the warp groups, which divide the ring:
 // row_slices_inner).
 template <int MODE, int R, bool ARGMAX, bool FUSE, int PROD = kProdPlain, bool KV = false,
-          bool SLI = false>
+          bool SLI = false, bool PLN = false>
 __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvParams p) {
     static_assert(!FUSE || R == 1, "fused producer: one row");
     static_assert(MODE != 0 || R == 1, "f32 mode: one row per launch");
@@ -330,7 +369,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
-    const RowGeo g = row_geo(p.N, p.K, G, c, CPL, int(R * sizeof(A)), row_rpw<MODE, R>(), kRing,
+    // PLN: the f32 planes' area after a shortened ring (row_planes_after_ring)
+    static_assert(!PLN || (MODE == 0 && FUSE && PROD != kProdPlain),
+                  "the planes after the ring serve the fused f32 residual and SwiGLU kernels");
+    const int ring = PLN ? row_ring_of<MODE, FUSE, PROD>(p.K) : kRing;
+    const RowGeo g = row_geo(p.N, p.K, G, c, CPL, int(R * sizeof(A)), row_rpw<MODE, R>(), ring,
                              row_part_extra<MODE, R>());
     // f32 mode, one row: a lane owns a whole 32-value block of its part (one
     // binade, one weight scale, one exact dot and one f32-pair scaling), and
@@ -431,11 +474,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     int64_t plane = p.plane;
     float rf = 1.0f;   // f32 mode, fused: x = (h*rf)*g is formed where it is used
     if constexpr (FUSE && MODE == 0) {
-        // f32: the consumers form x themselves (no shared-memory activation:
-        // the f32 kernel allocates none); with the norm only rf is computed here
-        // rows of one slice and K <= 4096 keep the input in the part-sum area
-        // (not in use yet) for the block conversion below
-        float* const stage = (g.nks == 1 && K <= 4096) ? reinterpret_cast<float*>(psum) : nullptr;
+        // f32: the consumers convert x into fixed-point planes themselves (no
+        // code plane); with the norm only rf is computed here, and the RMS pass
+        // keeps the input for the block conversion below: in the part-sum area
+        // (not in use yet) up to 4096 values, else in the area after the ring
+        float* const stage = PLN ? reinterpret_cast<float*>(wring + ring)
+                                 : (g.nks == 1 && K <= 4096) ? reinterpret_cast<float*>(psum) : nullptr;
         if constexpr (NORM) rf = row_rms_scale(p.h, res, s_out, K, p.eps, tid, 1, s_pair, &s_rf, stage);
     } else if constexpr (FUSE) {
         static_assert(MODE != 0, "the shared-memory activation exists for the int8 modes only");
@@ -474,31 +518,40 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
     bool validb = false;
     int cur_sl = -1;
     int ncc = 0, rag = 0;   // full 512-byte chunk columns of this part, lanes of the ragged one
+    // f32 one-row kernel, the shared block conversion: each 32-value block is
+    // converted once, by one thread, and every warp reads its blocks from
+    // shared memory (a quarter of the conversions and of the activation's L2
+    // traffic).  Block b's 32 words sit at b*128 bytes, 16-byte word group i in
+    // slot i ^ (b & 7) (no bank conflicts); the blocks' binades follow the
+    // parts' binades.  Rows of one slice up to 4096 values: warp w converts
+    // part w into the part-sum area (not in use yet), and each warp keeps its
+    // one block in registers for the launch.  PLN (a residual or SwiGLU
+    // producer fused, more than 4096 values): warp w converts the w-th 1024 values (part w % nprr
+    // of slice w / nprr: slices of whole parts) into the area after the ring,
+    // where they stay, and a warp reloads its block at each change of slice.
     if constexpr (kBL) {
-        if (g.nks == 1 && K <= 4096) {
-            // Rows of one slice and up to 4096 values: each 32-value block is
-            // converted once, by the first warp of its part (one warp a part),
-            // into the part-sum area (not in use yet), and every warp reads its
-            // block from there: a quarter of the conversions and of the
-            // activation's L2 traffic.  Block b's 32 words sit at b*128 bytes,
-            // 16-byte word group i in slot i ^ (b & 7) (no bank conflicts).
-            unsigned char* planes = reinterpret_cast<unsigned char*>(psum);
-            short* pe = reinterpret_cast<short*>(reinterpret_cast<unsigned char*>(psum) + kRowPsumBytes +
-                                                 kRowEpBytes / 2);   // block binades [K/32]
-            const int bpp = g.PB >> 5;                              // blocks a part
-            if (warp < g.npr) {
-                // warp w < npr is the first warp of part w (item w: row 0, part w)
-                const int pbytes = int(min64(max64(K - int64_t(warp) * g.PB, 0), g.PB));
+        if (PLN || (g.nks == 1 && K <= 4096)) {
+            const uint32_t planes_a = smem_u32(PLN ? wring + ring : reinterpret_cast<unsigned char*>(psum));
+            short* const pe = reinterpret_cast<short*>(reinterpret_cast<unsigned char*>(psum) + g.ep_off +
+                                                       kRowEpPartBytes);   // block binades [K/32]
+            // PLN: one warp a (slice, part), <= 16 (K <= 16384); the empty
+            // parts of a ragged last slice record the binade of zero, which
+            // the combine reads with the others
+            if (warp < (PLN ? g.nks * g.nprr : g.npr)) {
+                const int64_t k0 = int64_t(warp) * g.PB;
+                const int pbytes = int(min64(max64(K - k0, 0), g.PB));
                 const bool valid = lane < (pbytes >> 5);
                 FixChunk32 f = FixChunk32{};
                 f.e = -126;
                 if (valid) {
-                    const int64_t k = int64_t(warp) * g.PB + int64_t(lane) * 32;
+                    const int64_t k = k0 + int64_t(lane) * 32;
                     float xs[32];
                     if constexpr (FUSE && NORM) {
                         // the RMS pass kept the input (h, or h + r) in this very
                         // block of the area: x = (s*rf)*g, then the planes in place
-                        const float* sp = reinterpret_cast<const float*>(planes) + k;
+                        const float* sp = reinterpret_cast<const float*>(
+                                              PLN ? wring + ring : reinterpret_cast<unsigned char*>(psum)) +
+                                          k;
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             const float4 s4 = *reinterpret_cast<const float4*>(sp + 4 * u);
@@ -534,10 +587,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     f = fix_chunk32(xs);
                 }
                 const int ep = __reduce_max_sync(0xffffffffu, f.e);
-                if (lane == 0 && warp < g.nprr) s_ep[warp] = short(ep);
+                if constexpr (PLN) {
+                    // the (slice, part) these values form
+                    const int sl_w = int(k0 / g.KS);
+                    const int pw_w = int((k0 - int64_t(sl_w) * g.KS) / g.PB);
+                    if (lane == 0) s_ep[sl_w * g.nprr + pw_w] = short(ep);
+                } else {
+                    if (lane == 0 && warp < g.nprr) s_ep[warp] = short(ep);
+                }
                 if (valid) {
-                    const int blk = warp * bpp + lane;
-                    const uint32_t base = smem_u32(planes) + uint32_t(blk) * 128u;
+                    const int blk = warp * (g.PB >> 5) + lane;
+                    const uint32_t base = planes_a + uint32_t(blk) * 128u;
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         sts128(base + uint32_t(((i ^ (blk & 7)) << 4)), uint32_t(f.p[i >> 1][4 * (i & 1) + 0]),
@@ -547,26 +607,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                 }
             }
             consumer_bar<NT>();
-            cur_sl = 0;
-            const int pbytes = int(min64(max64(K - int64_t(pw) * g.PB, 0), g.PB));
-            validb = lane < (pbytes >> 5);
-            fxb = FixChunk32{};
-            fxb.e = -126;
-            if (validb) {
-                const int blk = pw * bpp + lane;
-                const uint32_t base = smem_u32(planes) + uint32_t(blk) * 128u;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int4 v = lds128(base + uint32_t(((i ^ (blk & 7)) << 4)));
-                    fxb.p[i >> 1][4 * (i & 1) + 0] = v.x;
-                    fxb.p[i >> 1][4 * (i & 1) + 1] = v.y;
-                    fxb.p[i >> 1][4 * (i & 1) + 2] = v.z;
-                    fxb.p[i >> 1][4 * (i & 1) + 3] = v.w;
-                }
-                fxb.e = pe[blk];
+            if constexpr (!PLN) {
+                // one slice: this warp's block into registers for the launch
+                cur_sl = 0;
+                const int pbytes = int(min64(max64(K - int64_t(pw) * g.PB, 0), g.PB));
+                validb = lane < (pbytes >> 5);
+                fxb = FixChunk32{};
+                fxb.e = -126;
+                if (validb) load_planes_block(planes_a, pe, pw * (g.PB >> 5) + lane, fxb);
+                p2sb = validb ? ldexpf(1.0f, fxb.e - s_ep[pw]) : 0.0f;
+                consumer_bar<NT>();   // the area holds part sums from here on
             }
-            p2sb = validb ? ldexpf(1.0f, fxb.e - s_ep[pw]) : 0.0f;
-            consumer_bar<NT>();   // the area holds part sums from here on
         }
     }
 
@@ -612,7 +663,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                     validb = lane < (pbytes >> 5);
                     fxb = FixChunk32{};
                     fxb.e = -126;   // the binade of zero: below every other
-                    if (validb) {
+                    if constexpr (PLN) {
+                        // the slice's block, converted in the prologue
+                        const uint32_t planes_a = smem_u32(wring + ring);
+                        const short* pe = reinterpret_cast<const short*>(reinterpret_cast<unsigned char*>(psum) +
+                                                                         g.ep_off + kRowEpPartBytes);
+                        if (validb) load_planes_block(planes_a, pe, int(ks >> 5) + pw * (g.PB >> 5) + lane, fxb);
+                        p2sb = validb ? ldexpf(1.0f, fxb.e - s_ep[sl * g.nprr + pw]) : 0.0f;
+                    } else if (validb) {
                         const int64_t k = ks + pw * g.PB + int64_t(lane) * 32;
                         float xs[32];
 #pragma unroll
@@ -628,10 +686,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
                         }
                         fxb = fix_chunk32(xs);
                     }
-                    // the part's largest binade; its sums are in units of 2^(ep-30)
-                    const int ep = __reduce_max_sync(0xffffffffu, fxb.e);
-                    p2sb = validb ? ldexpf(1.0f, fxb.e - ep) : 0.0f;
-                    if (lane == 0 && pw < g.nprr) s_ep[sl * g.nprr + pw] = short(ep);
+                    if constexpr (!PLN) {
+                        // the part's largest binade; its sums are in units of 2^(ep-30)
+                        const int ep = __reduce_max_sync(0xffffffffu, fxb.e);
+                        p2sb = validb ? ldexpf(1.0f, fxb.e - ep) : 0.0f;
+                        if (lane == 0 && pw < g.nprr) s_ep[sl * g.nprr + pw] = short(ep);
+                    }
                 }
 #pragma unroll
                 for (int cc = 0; cc < (kBL ? 0 : CPL); ++cc) {
@@ -971,13 +1031,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) gemv_row_kernel(const GemvPara
 
 template <int MODE, int R, bool ARGMAX, bool FUSE = false, int PROD = kProdPlain, bool KV = false>
 cudaError_t launch_gemv_row_t(const GemvArgs& a, const LaunchCtx& ctx) {
-    auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD, KV, false>;
-    bool sli = false;
+    auto kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD, KV, false, false>;
+    bool sli = false;   // the kernel's variant: slice-inner order, or planes after the ring
     if constexpr (MODE == 0 && R == 1 && !FUSE) {
         // (measured: the fused launches run slower in this order, so they keep
         // the slice-outer one)
         sli = row_slices_inner(a.K);
-        if (sli) kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD, KV, true>;
+        if (sli) kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD, KV, true, false>;
+    }
+    if constexpr (MODE == 0 && R == 1 && FUSE && PROD != kProdPlain) {
+        sli = row_planes_after_ring<MODE, FUSE, PROD>(a.K);
+        if (sli) kern = gemv_row_kernel<MODE, R, ARGMAX, FUSE, PROD, KV, false, true>;
     }
     constexpr size_t smem = row_smem_bytes<MODE, R, FUSE>();
     static std::atomic<bool> configured[2][kMaxDevices];   // per kernel (order), per device
@@ -985,6 +1049,7 @@ cudaError_t launch_gemv_row_t(const GemvArgs& a, const LaunchCtx& ctx) {
         e != cudaSuccess)
         return e;
     if (!row_kernel_fits<MODE, R>(a.K)) return cudaErrorInvalidValue;   // callers check first
+    if (FUSE && a.K > kFusedMaxK) return cudaErrorInvalidValue;         // the producer's row
     GemvParams p{};
     p.q = a.q;
     p.s = a.s;

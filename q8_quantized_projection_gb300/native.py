@@ -49,6 +49,7 @@ SIGNATURES = {
     "head_argmax_workspace": (_sz, [_i64]),
     "q8_debug_block_dots": (_int, [_int, _vp, _vp, _i64, _i64, _i64, _vp, _int, _vp]),
     "q8_debug_row_geometry": (_int, [_int, _i64, _i64, _i64, _int, _int, _vp]),
+    "q8_debug_row_geometry_fused": (_int, [_int, _int, _i64, _i64, _int, _int, _vp]),
     "q8_debug_chunk_plan": (_int, [_int, _i64, _i64, _i64, _int, _vp]),
     "head_argmax_noalloc": (_int, [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp,
                                    _vp]),
@@ -247,6 +248,21 @@ def q8_debug_row_geometry(mode, rows, n, k, grid, cta):
     if st == 6:   # Q8_ERR_UNSUPPORTED
         return None
     _check(st, "q8_debug_row_geometry")
+    return dict(zip(ROW_GEOMETRY_FIELDS, list(out)))
+
+
+FUSED_PRODUCERS = {"plain": 0, "residual": 1, "swiglu": 2}
+
+
+def q8_debug_row_geometry_fused(mode, prod, n, k, grid, cta):
+    """The same fields for a fused call's decode launch (rows = 1), prod one of
+    FUSED_PRODUCERS; None when the fused producer does not take K."""
+    out = (C.c_int64 * len(ROW_GEOMETRY_FIELDS))()
+    st = load().q8_debug_row_geometry_fused(_mode(mode), FUSED_PRODUCERS[prod], int(n), int(k),
+                                            int(grid), int(cta), C.cast(out, C.c_void_p))
+    if st == 6:   # Q8_ERR_UNSUPPORTED
+        return None
+    _check(st, "q8_debug_row_geometry_fused")
     return dict(zip(ROW_GEOMETRY_FIELDS, list(out)))
 
 

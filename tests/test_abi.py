@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
 
 
 def test_status_names_and_version(lib):
-    assert lib.q8_version() == 105
+    assert lib.q8_version() == 106
     for i, name in enumerate(native._STATUS):
         assert lib.q8_status_str(i).decode() == name
     assert lib.q8_status_str(99).decode() == "Q8_ERR_UNKNOWN"

@@ -197,7 +197,11 @@ def test_proj_deterministic_and_zero(mode):
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("n,k,rows", [(300, 4096, 1), (100, 14336, 2), (64, 1024, 16),
-                                      (50, 16384, 1), (40, 16416, 1), (37, 96, 1), (7, 14336, 1)])
+                                      (50, 16384, 1), (40, 16416, 1), (37, 96, 1), (7, 14336, 1),
+                                      # rows of one slice above 4096 values, a ragged part, and
+                                      # two slices with a ragged last one (the f32 kernel keeps
+                                      # the converted activation after its weight ring there)
+                                      (77, 4128, 1), (61, 5120, 1), (45, 8224, 1), (33, 11008, 1)])
 def test_fused_matches_oracle_and_composition(mode, n, k, rows):
     rng = np.random.default_rng(5 + n + k + rows)
     q, s = synth.q8_weights(rng, n, k)
@@ -245,7 +249,8 @@ def test_act_quant_residual_bit_exact(mode, rows, k, with_gain):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("n,k,rows", [(300, 4096, 1), (7, 14336, 1), (37, 96, 1), (100, 4096, 3)])
+@pytest.mark.parametrize("n,k,rows", [(300, 4096, 1), (7, 14336, 1), (37, 96, 1), (100, 4096, 3),
+                                      (50, 5120, 1), (29, 11008, 1)])
 def test_fused_residual_matches_oracle_and_composition(mode, n, k, rows):
     rng = np.random.default_rng(60 + n + k + rows)
     q, s = synth.q8_weights(rng, n, k)
@@ -297,7 +302,8 @@ def test_act_quant_swiglu_bit_exact(mode, rows, k):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("n,k,rows", [(300, 14336, 1), (64, 4096, 1), (37, 96, 1), (100, 1024, 3)])
+@pytest.mark.parametrize("n,k,rows", [(300, 14336, 1), (64, 4096, 1), (37, 96, 1), (100, 1024, 3),
+                                      (31, 4128, 1), (40, 8224, 1), (20, 16384, 1)])
 def test_fused_swiglu_matches_oracle_and_composition(mode, n, k, rows):
     rng = np.random.default_rng(90 + n + k + rows)
     q, s = synth.q8_weights(rng, n, k)

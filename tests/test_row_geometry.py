@@ -66,8 +66,13 @@ def check_invariants(mode, rows, n, k, grid, cta, g):
             # the shared block conversion: 128 bytes a block in the part-sum
             # area, the blocks' binades after the parts' binades
             assert (k // 32) * 128 <= g["psum_bytes"], where
-            assert nprr * 2 <= 512 and 512 + (k // 32) * 2 <= 1024, where
             assert 4 * k <= g["psum_bytes"], where   # the fused RMS pass's staged input
+        if k <= 16384:
+            # the blocks' binades of a shared block conversion (up to the fused
+            # producer's 16384 values) follow the parts' 1024 bytes
+            assert nprr * nks * 2 <= 1024 and 1024 + (k // 32) * 2 <= 2048, where
+            # warp w converts the w-th 1024 values: slices of whole parts
+            assert nks == 1 or KS % PB == 0, where
     else:
         assert rpw in (1, 2) and rpw <= RS, where
 
@@ -124,3 +129,41 @@ def test_f32_two_slice_rows_take_the_slice_inner_order(lib):
         g = geometry("f32", 1, 4096, k, 152, 0)
         assert g["nks"] == 2 and g["stride"] % g["nks"] == 0, g
         assert g["nstages"] % g["stride"] == 0, g
+
+
+@pytest.mark.parametrize("mode", ["f32", "i8", "i8x2"])
+@pytest.mark.parametrize("prod", ["plain", "residual", "swiglu"])
+def test_fused_decode_geometry(lib, mode, prod):
+    # a fused call's decode launch (rows = 1, up to the producer's 16384
+    # values): the same invariants; in f32 mode the residual and SwiGLU
+    # producers above 4096 values give up the ring's last 4K bytes (rounded up
+    # to 1 KB) to the converted activation, and the stages fit what is left
+    full = 196608 if mode == "f32" else 163840
+    for k in [kk for kk in KS if kk <= 16384]:
+        for n in (7, 4096, 28672):
+            grid = min(152, n)
+            for cta in sorted({0, grid - 1}):
+                g = native.q8_debug_row_geometry_fused(mode, prod, n, k, grid, cta)
+                assert g is not None, (mode, n, k)
+                check_invariants(mode, 1, n, k, grid, cta, g)
+                shorter = mode == "f32" and prod != "plain" and k > 4096
+                planes = (4 * k + 1023) // 1024 * 1024 if shorter else 0
+                assert g["ring_bytes"] == full - planes, (mode, k, g)
+                if planes:
+                    # the converting warps: one a (slice, part), all 16 at most
+                    assert g["nks"] * g["nprr"] <= g["warps"], (k, g)
+                    assert g["nstages"] >= 3, (k, g)
+                else:
+                    assert g == native.q8_debug_row_geometry(mode, 1, n, k, grid, cta)
+    assert native.q8_debug_row_geometry_fused(mode, prod, 4096, 16416, 152, 0) is None
+
+
+def test_fused_geometry_argument_errors(lib):
+    out = (native.C.c_int64 * 21)()
+    f = lib.q8_debug_row_geometry_fused
+    assert f(0, 0, 100, 4096, 10, 0, None) == 1          # no output buffer
+    assert f(0, 3, 100, 4096, 10, 0, out) == 1           # producer kind
+    assert f(9, 0, 100, 4096, 10, 0, out) == 4           # mode
+    assert f(0, 1, 100, 4100, 10, 0, out) == 2           # K % 32
+    assert f(0, 2, 100, 4096, 10, 10, out) == 1          # cta outside the grid
+    assert f(0, 1, 100, 16416, 10, 0, out) == 6          # beyond the fused producer's row
