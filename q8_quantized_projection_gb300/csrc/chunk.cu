@@ -213,6 +213,22 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 __device__ __forceinline__ float f2_lo(uint64_t a) { return __uint_as_float(uint32_t(a)); }
 __device__ __forceinline__ float f2_hi(uint64_t a) { return __uint_as_float(uint32_t(a >> 32)); }
 
+// The block rescale of four accumulator columns: (a01, a23) += (v01, v23) *
+// (sw * x0..x3), two packed products and two packed FMAs (the scale pairs
+// formed from the consecutive registers of one shared-memory load).
+__device__ __forceinline__ void rescale4(uint64_t& a01, uint64_t& a23, uint64_t v01, uint64_t v23,
+                                         const int4& x, uint64_t sw2) {
+    asm("{\n\t.reg .b64 x01, x23;\n\t"
+        "mov.b64 x01, {%4, %5};\n\t"
+        "mov.b64 x23, {%6, %7};\n\t"
+        "mul.rn.f32x2 x01, x01, %8;\n\t"
+        "mul.rn.f32x2 x23, x23, %8;\n\t"
+        "fma.rn.f32x2 %0, %2, x01, %0;\n\t"
+        "fma.rn.f32x2 %1, %3, x23, %1;\n\t}"
+        : "+l"(a01), "+l"(a23)
+        : "l"(v01), "l"(v23), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "l"(sw2));
+}
+
 // ------------------------------------------------------ thread-block clusters
 
 __device__ __forceinline__ void cluster_sync() {
@@ -253,6 +269,82 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
         : "r"(taddr));
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// TMEM -> registers as f32 pairs, waited for inside the same PTX (the pairs
+// are the load's own consecutive destination registers, so forming them
+// costs no moves): 16 or 32 consecutive columns of the warp's 32 lanes, or 16
+// columns at each of two addresses (the two-word mode's planes).
+__device__ __forceinline__ void tmem_ld16_pairs(uint32_t taddr, uint64_t (&p)[8]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<16>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld32_pairs(uint32_t taddr, uint64_t (&p)[16]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<32>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld16x2_pairs(uint32_t taddr, uint32_t taddr2, uint64_t (&p)[16]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<32>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
+        : "r"(taddr), "r"(taddr2)
+        : "memory");
 }
 
 // ------------------------------------------------------------- arg-max keys
@@ -589,22 +681,19 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t(qd * 32) << 16) + uint32_t(ts * C::kN + c0);
-            float v[CW];
-            float vl[MODE == 2 ? CW : 1];
-#pragma unroll
-            for (int c = 0; c < CW / 16; ++c) {
-                tmem_ld16(d + uint32_t(16 * c), v + 16 * c);
-                if constexpr (MODE == 2) tmem_ld16(d + uint32_t(TT + 16 * c), vl + 16 * c);
-            }
-            // the block's weight scale while the accumulator is on its way
-            const uint32_t e = scl_a + uint32_t(se * C::kScl);
-            const float sw = DEBUG ? 0.0f : half_bits_to_float(lds16(e + uint32_t(2 * n)));
-            tmem_wait_ld();
-            // the data is in registers: the slot goes back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tm_empty[(b / C::kGS) % C::kSG]);
             if constexpr (DEBUG) {
+                float v[CW];
+                float vl[MODE == 2 ? CW : 1];
+#pragma unroll
+                for (int c = 0; c < CW / 16; ++c) {
+                    tmem_ld16(d + uint32_t(16 * c), v + 16 * c);
+                    if constexpr (MODE == 2) tmem_ld16(d + uint32_t(TT + 16 * c), vl + 16 * c);
+                }
+                tmem_wait_ld();
+                // the data is in registers: the slot goes back
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tm_empty[(b / C::kGS) % C::kSG]);
                 // the plane sums are exact integers below 2^24
                 const int64_t row = m0 + n;
 #pragma unroll
@@ -617,25 +706,34 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
                     }
                 }
             } else {
+                // the block's weight scale, then its accumulator columns as
+                // f32 pairs (the load waited for inside the same PTX)
+                const uint32_t e = scl_a + uint32_t(se * C::kScl);
+                const float sw = half_bits_to_float(lds16(e + uint32_t(2 * n)));
+                uint64_t vp[CW / 2];
                 if constexpr (MODE == 2) {
+                    static_assert(CW == 16, "two-word tiles: 16 columns a thread");
+                    uint64_t hl[16];
+                    tmem_ld16x2_pairs(d, d + uint32_t(TT), hl);
                     // 128*hi + lo rounds once: exactly float(isum)
                     const uint64_t k128 = f2_pack(128.0f, 128.0f);
 #pragma unroll
-                    for (int i = 0; i < CW / 2; ++i) {
-                        const uint64_t r = f2_fma(k128, f2_pack(v[2 * i], v[2 * i + 1]),
-                                                  f2_pack(vl[2 * i], vl[2 * i + 1]));
-                        v[2 * i] = f2_lo(r);
-                        v[2 * i + 1] = f2_hi(r);
-                    }
+                    for (int i = 0; i < 8; ++i) vp[i] = f2_fma(hl[i], k128, hl[8 + i]);
+                } else if constexpr (CW == 32) {
+                    tmem_ld32_pairs(d, vp);
+                } else {
+                    static_assert(CW == 16, "16 or 32 columns a thread");
+                    tmem_ld16_pairs(d, vp);
                 }
+                // the data is in registers: the slot goes back
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tm_empty[(b / C::kGS) % C::kSG]);
                 const uint64_t sw2 = f2_pack(sw, sw);
 #pragma unroll
                 for (int i4 = 0; i4 < CW / 4; ++i4) {
                     const int4 x4 = lds128(e + uint32_t(kCkM * 2 + c0 * 4 + 16 * i4));
-                    const uint64_t c01 = f2_mul(sw2, uint64_t(uint32_t(x4.x)) | (uint64_t(uint32_t(x4.y)) << 32));
-                    const uint64_t c23 = f2_mul(sw2, uint64_t(uint32_t(x4.z)) | (uint64_t(uint32_t(x4.w)) << 32));
-                    acc[2 * i4] = f2_fma(f2_pack(v[4 * i4], v[4 * i4 + 1]), c01, acc[2 * i4]);
-                    acc[2 * i4 + 1] = f2_fma(f2_pack(v[4 * i4 + 2], v[4 * i4 + 3]), c23, acc[2 * i4 + 1]);
+                    rescale4(acc[2 * i4], acc[2 * i4 + 1], vp[2 * i4], vp[2 * i4 + 1], x4, sw2);
                 }
                 // the block's scales are read: its scale entry goes back
                 __syncwarp();
