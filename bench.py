@@ -493,7 +493,7 @@ def run_ours(args, world, rank, local):
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": committed_traffic(f"fused_{dom}"),
-                "kernel": f"gemv_row_kernel<{inst},1,0,1,0,0,0> ({dom} mode, producer fused)",
+                "kernel": f"gemv_row_kernel<{inst},1,0,1,0,0,0,0> ({dom} mode, producer fused)",
                 "peak_source": peak_kind, "launches": 4,
                 "per_launch_us": round(per_mode[dom]["ms_per_step"] * 1e3 / 4, 3),
                 "alg_bytes_per_launch": round(mode_alg / 4),
