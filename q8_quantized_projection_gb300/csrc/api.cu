@@ -128,14 +128,13 @@ q8_status run_projection(int mode, const int8_t* q, const uint16_t* s, int64_t N
     return Q8_OK;
 }
 
-// Plain projection of a quantised activation: the tensor-core chunk kernel from
-// chunk_min_rows(mode) rows on (int8 modes, K % 256 == 0), the CUDA-core
-// kernels else.
+// Plain projection of an activation: the tensor-core chunk kernel from
+// chunk_min_rows(mode) rows on (K % 256 == 0), the CUDA-core kernels else.
 q8_status project_dispatch(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                            const void* xq, const float* xd, int64_t rows, void* y, int out_f64,
                            const LaunchCtx& ctx) {
-    if (!out_f64 && rows >= chunk_min_rows(mode) && chunk_supported(mode, N, K, rows))
-        return launched(launch_chunk(mode, q, s, N, K, xq, xd, rows, static_cast<float*>(y), ctx));
+    if ((!out_f64 || mode == Q8_ACT_F32) && rows >= chunk_min_rows(mode) && chunk_supported(mode, N, K, rows))
+        return launched(launch_chunk(mode, q, s, N, K, xq, xd, rows, y, out_f64 != 0, ctx));
     return run_projection(mode, q, s, N, K, xq, xd, rows, y, out_f64, nullptr, nullptr, nullptr,
                           ctx);
 }
@@ -430,9 +429,13 @@ q8_status head_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, i
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
     static_assert(kArgmaxKeyBytes >= 8 * Q8_MAX_ROWS, "one arg-max key per row");
-    if (mode != Q8_ACT_F32 && rows >= chunk_min_rows(mode) && chunk_supported(mode, N, K, rows))
-        return launched(launch_chunk_argmax(mode, q, s, N, K, xq, xd, rows, static_cast<float*>(logits), tok,
-                                            maxval, workspace, ctx));
+    // the tensor-core path from chunk_min_rows(mode) rows; in f32 mode up to
+    // kArgmaxGroupRows rows and kMaxGrid tiles (its candidates use the
+    // CUDA-core layout of the workspace)
+    const bool f32_fits = mode != Q8_ACT_F32 || (rows <= kArgmaxGroupRows && (N + 127) / 128 <= kMaxGrid);
+    if (f32_fits && rows >= chunk_min_rows(mode) && chunk_supported(mode, N, K, rows))
+        return launched(launch_chunk_argmax(mode, q, s, N, K, xq, xd, rows, logits, tok, maxval, workspace,
+                                            ctx));
     return run_projection(mode, q, s, N, K, xq, xd, rows, logits, mode == Q8_ACT_F32 ? 1 : 0, tok,
                           maxval, static_cast<unsigned char*>(workspace) + kArgmaxGemvOff, ctx);
 }

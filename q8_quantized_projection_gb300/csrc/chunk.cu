@@ -59,6 +59,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "gemv.cuh"
 #include "launch.h"
 #include "tc.cuh"
 
@@ -80,7 +81,9 @@ constexpr int kCkArgmax = 2;   // the arg-max of every row (and y when given)
 
 template <int MODE, int TT>
 struct CkCfg {
-    static constexpr int kPlanes = (MODE == 2) ? 2 : 1;
+    // activation planes along the MMA's N: one-word 1, two-word 2 (hi, lo),
+    // f32 4 (the byte planes of each block's 31-bit fixed point)
+    static constexpr int kPlanes = (MODE == 2) ? 2 : (MODE == 0 ? 4 : 1);
     static constexpr int kN = TT * kPlanes;                            // MMA N
     // converted stages in flight (A in TMEM, B in shared memory): three where
     // the accumulator slots leave room, so the converters run two stages ahead
@@ -96,7 +99,8 @@ struct CkCfg {
     static constexpr int kWConv = kN <= 32 ? 8 : 4;
     static constexpr int kConv = kWConv + kCkAConvWarps;
     static constexpr int kEpiWarps = kN <= 32 ? 8 : 16;
-    static constexpr int kEC = kN >= 128 ? 4 : (kN >= 64 ? 2 : 1);
+    // (f32: 8 columns a thread, each four plane sums and an f32-pair sum)
+    static constexpr int kEC = MODE == 0 ? TT / 8 : (kN >= 128 ? 4 : (kN >= 64 ? 2 : 1));
     static constexpr int kEG = kEpiWarps / (4 * kEC);
     static constexpr int kSlots = kSlotsRaw / kEG * kEG;               // a multiple of the groups
     // accumulator slots are released in groups of kGS blocks (one barrier a
@@ -106,8 +110,9 @@ struct CkCfg {
     static constexpr int kCW = TT / kEC;                               // columns per thread
     static constexpr int kW = kCkM * kCkStageK;                        // 16 KB
     static constexpr int kXPlane = TT * kCkStageK;
-    static constexpr int kX = kXPlane * kPlanes;
-    static constexpr int kXD = TT * 4 * 4;                             // [TT][4 blocks] f32
+    // f32: the stage's f32 activation rows, converted in shared memory
+    static constexpr int kX = MODE == 0 ? TT * kCkStageK * 4 : kXPlane * kPlanes;
+    static constexpr int kXD = MODE == 0 ? 0 : TT * 4 * 4;             // [TT][4 blocks] f32
     static constexpr int kStage = (kW + kX + kXD + 1023) / 1024 * 1024;
     static constexpr int kSGroup = kCkM * kCkGroup * 2;                // [128][8 blocks] f16
     static constexpr int kBBlock = kN * 64;                            // [kN][32] f16
@@ -125,13 +130,14 @@ struct CkCfg {
     static constexpr size_t kSmem = size_t(kStages) * kStage + kFixed;
     // the end-of-tile scratch in the stage area: the groups' partial sums
     // (or the CTA's split-K partial), then the arg-max candidates
-    static constexpr int kPartial = kCkM * TT * 4;
-    static constexpr int kCandOff = (kEG > 1 ? kEG - 1 : 1) * kPartial;
+    static constexpr int kPartial = kCkM * TT * (MODE == 0 ? 8 : 4);   // f32 mode: f32 pairs
+    static constexpr int kBinOff = (kEG > 1 ? kEG - 1 : 1) * kPartial;   // f32: the groups' binades
+    static constexpr int kCandOff = kBinOff + (MODE == 0 ? 4 * TT * 4 : 0);
     static_assert(kStages >= 3, "TMA pipeline depth");
     static_assert(kStage % 1024 == 0, "swizzled TMA tiles need 1024-byte alignment");
-    static_assert(kCandOff + 4 * TT * 8 <= kStages * kStage, "end-of-tile scratch must fit the stages");
+    static_assert(kCandOff + 4 * TT * 16 <= kStages * kStage, "end-of-tile scratch must fit the stages");
     static_assert(kSmem <= size_t(kCkSmemBudget), "shared memory");
-    static_assert(kCW % 16 == 0 && kCW <= 32, "epilogue columns");
+    static_assert(MODE == 0 ? kCW == 8 : (kCW % 16 == 0 && kCW <= 32), "epilogue columns");
     static_assert(kSlots >= 3 && kSlots % kEG == 0, "accumulator slots: each served by one group");
     static_assert(kSE == 8 && kSE % kEG == 0, "scale entries: two stages, each served by one group");
     static_assert(kSlots % kGS == 0 && kSG >= 2 && kGS % kEG == 0 || kGS == 1, "slot groups");
@@ -147,6 +153,10 @@ struct CkParams {
     int* err;
     unsigned int* ticket;   // arg-max: CTAs done
     unsigned long long* keys;   // arg-max: one key per activation row
+    // f32 mode: y as f64 (instead of y), and the arg-max's (value, row) per
+    // tile and activation row [tiles][T]
+    double* y64;
+    ArgmaxCand* cands;
     int32_t* tok;
     double* maxval;
 };
@@ -165,16 +175,36 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return uint32_t(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// The 32 int8 values of one block row (two 16-byte chunks) as f16, stored as
-// row r of a K-major no-swizzle operand tile at `dst`.
+// Four unsigned bytes of w -> two f16x2 words, exact: each byte b maps to the
+// f16 1024 + b, then 1024 is subtracted.
+__device__ __forceinline__ void u8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x7170;" : "=r"(a) : "r"(w), "r"(0x64646464u));   // bytes 0,1
+    asm("prmt.b32 %0, %1, %2, 0x7372;" : "=r"(b) : "r"(w), "r"(0x64646464u));   // bytes 2,3
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&ha);
+    hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+// The 32 8-bit values of one block row (two 16-byte chunks; signed, or
+// unsigned bytes with SIGNED false) as f16, stored as row r of a K-major
+// no-swizzle operand tile at `dst`.
+template <bool SIGNED = true>
 __device__ __forceinline__ void store_row_f16(uint32_t dst, int r, const int4 a, const int4 b) {
     const uint32_t w[8] = {uint32_t(a.x), uint32_t(a.y), uint32_t(a.z), uint32_t(a.w),
                            uint32_t(b.x), uint32_t(b.y), uint32_t(b.z), uint32_t(b.w)};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {   // 8 values (one core-matrix row) per c
         uint32_t h[4];
-        i8x4_to_f16x4(w[2 * c], h[0], h[1]);
-        i8x4_to_f16x4(w[2 * c + 1], h[2], h[3]);
+        if constexpr (SIGNED) {
+            i8x4_to_f16x4(w[2 * c], h[0], h[1]);
+            i8x4_to_f16x4(w[2 * c + 1], h[2], h[3]);
+        } else {
+            u8x4_to_f16x4(w[2 * c], h[0], h[1]);
+            u8x4_to_f16x4(w[2 * c + 1], h[2], h[3]);
+        }
         sts128(dst + tile_offset(r, 8 * c), h[0], h[1], h[2], h[3]);
     }
 }
@@ -229,6 +259,15 @@ __device__ __forceinline__ void rescale4(uint64_t& a01, uint64_t& a23, uint64_t 
         : "l"(v01), "l"(v23), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "l"(sw2));
 }
 
+__device__ __forceinline__ void sts64(uint32_t a, uint64_t v) {
+    asm volatile("st.shared.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t lds64(uint32_t a) {
+    uint64_t v;
+    asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------ thread-block clusters
 
 __device__ __forceinline__ void cluster_sync() {
@@ -246,6 +285,12 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
@@ -347,6 +392,25 @@ __device__ __forceinline__ void tmem_ld16x2_pairs(uint32_t taddr, uint32_t taddr
         : "memory");
 }
 
+// The f32 mode's four plane sums of 8 columns: 8 consecutive TMEM columns at
+// taddr + pl * stride for pl = 0..3, waited for.
+__device__ __forceinline__ void tmem_ld8x4(uint32_t taddr, uint32_t stride, float (&P)[4][8]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%33];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16, %17, %18, %19, %20, %21, %22, %23}, [%34];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24, %25, %26, %27, %28, %29, %30, %31}, [%35];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr), "r"(taddr + stride), "r"(taddr + 2 * stride), "r"(taddr + 3 * stride)
+        : "memory");
+#pragma unroll
+    for (int pl = 0; pl < 4; ++pl)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) P[pl][i] = __uint_as_float(r[8 * pl + i]);
+}
+
 // ------------------------------------------------------------- arg-max keys
 
 // The 64-bit arg-max key of logit v at row n: the value's bits in an order
@@ -369,6 +433,221 @@ __device__ __forceinline__ void argmax_unkey(unsigned long long key, int32_t& to
     const unsigned b = (ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord;
     tok = int32_t(0xffffffffu - unsigned(key & 0xffffffffull));
     val = double(__uint_as_float(b));
+}
+
+// The f32 mode's epilogue warps.  Each block's four plane sums per (weight
+// row, activation row) are exact integers below 2^20; they combine as in the
+// CUDA-core f32 path into the block dot V = P3*2^24 + P2*2^16 + P1*2^8 + P0,
+// scaled by the weight scale and the block's binade E as an exact f32 pair and
+// added to the column's f32-pair sum.  A column's sum is kept in units of 2^(ecur
+// - 30), ecur the largest binade seen so far, and rescaled when a larger one
+// comes (exact powers of two; a part more than 2^252 below is dropped).
+template <int TT, int KIND, class C>
+__device__ __forceinline__ void chunk_epilogue_f32(const CkParams& p, uint32_t tmem, uint32_t scl_a,
+                                                   uint32_t stages_a, uint64_t* sc_full, uint64_t* sc_empty,
+                                                   uint64_t* tm_full, uint64_t* tm_empty, int warp, int lane,
+                                                   int nblk, int64_t m0, int64_t t0, int* s_last) {
+    constexpr bool ARGMAX = KIND == kCkArgmax;
+    static_assert(KIND != kCkDebug, "the f32 mode has no block-dot debug path");
+    constexpr int CW = C::kCW;   // 8
+    const int ew = warp - C::kEpiWarp0;
+    const int qd = warp & 3;                      // TMEM lane quadrant of this warp
+    const int ec = (ew >> 2) % C::kEC;            // column slice
+    const int eg = (ew >> 2) / C::kEC;            // block group
+    const int n = qd * 32 + lane;                 // weight row within the tile
+    const int c0 = ec * CW;
+    DF acc[CW];
+    int ecur[CW];
+#pragma unroll
+    for (int i = 0; i < CW; ++i) {
+        acc[i] = DF{0.0f, 0.0f};
+        ecur[i] = -1000;   // below every binade (the first block sets it)
+    }
+    bool ok = true;
+    for (int b = eg; b < nblk; b += C::kEG) {
+        const int ts = b % C::kSlots, se = b % C::kSE;
+        const uint32_t par = uint32_t(b / C::kSlots) & 1u;
+        if (ok) ok = mbar_wait_fast(&sc_full[(b >> 2) & 1], uint32_t(b >> 3) & 1u, p.err);
+        if (ok) ok = mbar_wait_fast(&tm_full[(b / C::kGS) % C::kSG], par, p.err);
+        ok = __all_sync(0xffffffffu, ok);   // the TMEM loads below are warp-wide
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t e = scl_a + uint32_t(se * C::kScl);
+        const float sw = half_bits_to_float(lds16(e + uint32_t(2 * n)));
+        const int4 e0 = lds128(e + uint32_t(kCkM * 2 + c0 * 4));
+        const int4 e1 = lds128(e + uint32_t(kCkM * 2 + c0 * 4 + 16));
+        const int eb[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        float P[4][8];
+        tmem_ld8x4(tmem + (uint32_t(qd * 32) << 16) + uint32_t(ts * C::kN + c0), uint32_t(TT), P);
+        // the data is in registers: the slot and the scale entry go back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&tm_empty[(b / C::kGS) % C::kSG]);
+            mbar_arrive(&sc_empty[(b >> 2) & 1]);
+        }
+        // columns past the last activation row are left out (warp-uniform)
+        const int live = int(min64(int64_t(CW), p.T - (t0 + c0)));
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+            if (i >= live) break;
+            if (eb[i] > ecur[i]) {
+                const int dd = ecur[i] - eb[i];
+                acc[i] = DF{mul_pow2_neg(acc[i].hi, dd), mul_pow2_neg(acc[i].lo, dd)};
+                ecur[i] = eb[i];
+            }
+            // the column's factor 2^(E - ecur) <= 1: f = sw * g is exact while
+            // normal; a block more than 2^100 below the column's largest
+            // (below 2^-70 of it after the weight scale) is dropped
+            const int dg = eb[i] - ecur[i];
+            const float g = dg < -100 ? 0.0f : pow2i(dg < -126 ? -126 : dg);
+            const float f = __fmul_rn(sw, g);
+            // the plane sums as integers: exact floats below 2^20 read through
+            // 1.5 * 2^23 (the offsets cancel below, modulo 2^32)
+            const uint32_t b0 = __float_as_uint(__fadd_rn(P[0][i], 12582912.0f));
+            const uint32_t b1 = __float_as_uint(__fadd_rn(P[1][i], 12582912.0f));
+            const uint32_t b2 = __float_as_uint(__fadd_rn(P[2][i], 12582912.0f));
+            const uint32_t b3 = __float_as_uint(__fadd_rn(P[3][i], 12582912.0f));
+            const int L = int(b1 * 256u + b0 - 257u * 0x4B400000u);   // P1*2^8 + P0
+            const int H = int(b3 * 256u + b2 - 257u * 0x4B400000u);   // P3*2^8 + P2
+            const int2 v = make_int2((H >> 5) + (L >> 21) + 1, (H & 31) * 65536 + (L & 0x1fffff) - 2097152);
+            acc[i] = df_add(acc[i], scaled_pair_split(f, v));
+        }
+    }
+    constexpr int kEpiThreads = 32 * C::kEpiWarps;
+    if constexpr (C::kEG > 1) {
+        // group 1 hands its sums and binades to group 0 (the stage area is free:
+        // a group's last block lies in the last stage, and its MMAs are done)
+        static_assert(C::kEG == 2, "one partial-sum exchange");
+        if (eg > 0) {
+#pragma unroll
+            for (int i = 0; i < CW; ++i) {
+                const uint32_t a = stages_a + uint32_t(((c0 + i) * kCkM + n) * 8);
+                sts32(a, __float_as_uint(acc[i].hi));
+                sts32(a + 4u, __float_as_uint(acc[i].lo));
+            }
+            if (n == 0) {
+#pragma unroll
+                for (int i = 0; i < CW; ++i) sts32(stages_a + uint32_t(C::kBinOff + (c0 + i) * 4), uint32_t(ecur[i]));
+            }
+            named_bar_arrive(1, kEpiThreads);
+        } else {
+            named_bar(1, kEpiThreads);
+#pragma unroll
+            for (int i = 0; i < CW; ++i) {
+                const uint32_t a = stages_a + uint32_t(((c0 + i) * kCkM + n) * 8);
+                const DF o{__uint_as_float(lds32(a)), __uint_as_float(lds32(a + 4u))};
+                const int eo = int(lds32(stages_a + uint32_t(C::kBinOff + (c0 + i) * 4)));
+                const int em = max(ecur[i], eo);
+                const DF x{mul_pow2_neg(acc[i].hi, ecur[i] - em), mul_pow2_neg(acc[i].lo, ecur[i] - em)};
+                const DF y{mul_pow2_neg(o.hi, eo - em), mul_pow2_neg(o.lo, eo - em)};
+                acc[i] = df_add(x, y);
+                ecur[i] = em;
+            }
+        }
+    }
+    if (eg != 0) return;
+    const int64_t row = m0 + n;
+    if (gridDim.z > 1) {
+        // split K: the CTA's partial sums and binades for the cluster's sum
+        // (after the groups' exchange, in their own words)
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+            const uint32_t a = stages_a + uint32_t(((c0 + i) * kCkM + n) * 8);
+            sts32(a, __float_as_uint(acc[i].hi));
+            sts32(a + 4u, __float_as_uint(acc[i].lo));
+        }
+        if (n == 0) {
+#pragma unroll
+            for (int i = 0; i < CW; ++i)
+                sts32(stages_a + uint32_t(C::kBinOff + TT * 4 + (c0 + i) * 4), uint32_t(ecur[i]));
+        }
+        return;
+    }
+    // outputs: f32 (the pair rounded once, then scaled by 2^(ecur - 30)) or f64
+#pragma unroll
+    for (int i = 0; i < CW; ++i) {
+        const int64_t t = t0 + c0 + i;
+        if (t < p.T && row < p.N) {
+            const int sc = ecur[i] - 30;   // in [-156, 97]
+            if (p.y64)
+                p.y64[t * p.N + row] = ldexp(double(acc[i].hi) + double(acc[i].lo), sc);
+            else if (p.y)
+                p.y[t * p.N + row] = __fmul_rn(__fmul_rn(__fadd_rn(acc[i].hi, acc[i].lo), pow2i(sc >> 1)),
+                                               pow2i(sc - (sc >> 1)));
+        }
+    }
+    if constexpr (ARGMAX) {
+        // per activation row: the best (value, lowest row) of each quadrant's 32
+        // rows, then of the tile, then (the last CTA) of every tile
+        constexpr int kG0 = 32 * 4 * C::kEC;   // threads of group 0
+        const uint32_t cand = stages_a + uint32_t(C::kCandOff);   // [4][TT] {f64 value, row}
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+            double bv = -INFINITY;
+            long long bi = 0x7fffffffffffffffll;
+            if (row < p.N) argmax_keep(bv, bi, ldexp(double(acc[i].hi) + double(acc[i].lo), ecur[i] - 30), row);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const long long oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                argmax_keep(bv, bi, ov, oi);
+            }
+            if (lane == 0) {
+                const uint32_t a = cand + uint32_t((qd * TT + c0 + i) * 16);
+                sts64(a, uint64_t(__double_as_longlong(bv)));
+                sts64(a + 8u, uint64_t(bi));
+            }
+        }
+        named_bar(2, kG0);
+        const int j = (ec * 4 + qd) * 32 + lane;   // 0..kG0-1
+        for (int col = j; col < TT; col += kG0) {
+            double bv = -INFINITY;
+            long long bi = 0x7fffffffffffffffll;
+            for (int q2 = 0; q2 < 4; ++q2) {
+                const uint32_t a = cand + uint32_t((q2 * TT + col) * 16);
+                argmax_keep(bv, bi, __longlong_as_double((long long)lds64(a)), (long long)lds64(a + 8u));
+            }
+            const int64_t t = t0 + col;
+            if (t < p.T) p.cands[int64_t(blockIdx.y) * p.T + t] = ArgmaxCand{bv, bi};
+        }
+        __threadfence();
+        named_bar(2, kG0);
+        if (j == 0) *s_last = atomicAdd(p.ticket, 1u) == gridDim.x * gridDim.y - 1u;
+        named_bar(2, kG0);
+        if (*s_last) {
+            __threadfence();
+            const uint32_t rs = cand + uint32_t(4 * TT * 16);      // [kG0 / 32] candidates
+            const int G = int(gridDim.y);
+            for (int64_t t = 0; t < p.T; ++t) {
+                double bv = -INFINITY;
+                long long bi = 0x7fffffffffffffffll;
+                for (int c2 = j; c2 < G; c2 += kG0) {
+                    const ArgmaxCand* src = p.cands + int64_t(c2) * p.T + t;
+                    argmax_keep(bv, bi, __ldcg(&src->v), __ldcg(&src->i));
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const long long oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                    argmax_keep(bv, bi, ov, oi);
+                }
+                if (lane == 0) {
+                    sts64(rs + uint32_t((j >> 5) * 16), uint64_t(__double_as_longlong(bv)));
+                    sts64(rs + uint32_t((j >> 5) * 16 + 8), uint64_t(bi));
+                }
+                named_bar(2, kG0);
+                if (j == 0) {
+                    for (int w = 1; w < kG0 / 32; ++w)
+                        argmax_keep(bv, bi, __longlong_as_double((long long)lds64(rs + uint32_t(w * 16))),
+                                    (long long)lds64(rs + uint32_t(w * 16 + 8)));
+                    argmax_store(ArgmaxCand{bv, bi}, p.tok, p.maxval, int(t));
+                }
+                named_bar(2, kG0);
+            }
+            if (j == 0) *p.ticket = 0u;
+        }
+    }
 }
 
 template <int MODE, int TT, int KIND>
@@ -462,9 +741,9 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
                 unsigned char* st = stages + size_t(s % C::kStages) * C::kStage;
                 const int kx = (st0 + s) * kCkStageK;   // byte (= element) of K
                 uint64_t* bar = &st_full[s % C::kStages];
-                tma2d(st + C::kW, &tm_xh, kx, int(t0), bar);
+                tma2d(st + C::kW, &tm_xh, kx, int(t0), bar);   // f32 mode: the f32 rows
                 if constexpr (MODE == 2) tma2d(st + C::kW + C::kXPlane, &tm_xl, kx, int(t0), bar);
-                if constexpr (!DEBUG) tma2d(st + C::kW + C::kX, &tm_xd, kx / Q8_QK, int(t0), bar);
+                if constexpr (!DEBUG && MODE != 0) tma2d(st + C::kW + C::kX, &tm_xd, kx / Q8_QK, int(t0), bar);
             };
             auto scales = [&](int g) {
                 const int gs = g % kCkSGroups;
@@ -597,7 +876,43 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
             } else {
-                if constexpr (TT <= 32) {
+                if constexpr (MODE == 0) {
+                    // f32 rows: each (row, block) pair of the stage gives its
+                    // binade E and the four byte planes of X = rint(x *
+                    // 2^(30-E)) (planes 0-2 unsigned, plane 3 signed), stored
+                    // as the block's B rows pl * TT + row; E goes to the
+                    // block's scale entry in place of a scale
+                    static_assert(TT * 4 == kAPasses * 64, "activation pairs");
+#pragma unroll 1
+                    for (int pass = 0; pass < kAPasses; ++pass) {
+                        const int item = (2 * pass + aw) * 32 + lane;   // j * TT + ra
+                        const int ra = item % TT, j = item / TT;
+                        const uint32_t xs = st + uint32_t(C::kW + ra * (kCkStageK * 4) + j * (Q8_QK * 4));
+                        float v[32];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int4 x4 = lds128(xs + uint32_t(16 * u));
+                            v[4 * u + 0] = __int_as_float(x4.x);
+                            v[4 * u + 1] = __int_as_float(x4.y);
+                            v[4 * u + 2] = __int_as_float(x4.z);
+                            v[4 * u + 3] = __int_as_float(x4.w);
+                        }
+                        const FixChunk32 f = fix_chunk32(v);
+                        const uint32_t bq = bquads_a + uint32_t(qs * C::kBQuad + j * C::kBBlock);
+#pragma unroll
+                        for (int pl = 0; pl < 4; ++pl) {
+                            const int4 lo4 = make_int4(f.p[pl][0], f.p[pl][1], f.p[pl][2], f.p[pl][3]);
+                            const int4 hi4 = make_int4(f.p[pl][4], f.p[pl][5], f.p[pl][6], f.p[pl][7]);
+                            if (pl == 3)
+                                store_row_f16<true>(bq, pl * TT + ra, lo4, hi4);
+                            else
+                                store_row_f16<false>(bq, pl * TT + ra, lo4, hi4);
+                        }
+                        if constexpr (!DEBUG)
+                            sts32(scl_a + uint32_t(((4 * s + j) % C::kSE) * C::kScl + kCkM * 2 + 4 * ra),
+                                  uint32_t(f.e));
+                    }
+                } else if constexpr (TT <= 32) {
                     // exactly 4 * TT (row, block) pairs: two warps of 32 lanes,
                     // kAPasses passes, rows first within a block
                     static_assert(TT * 4 == kAPasses * 64, "activation pairs");
@@ -661,6 +976,10 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         pdl_wait();   // outputs and arg-max keys belong to the previous kernel until here
+        if constexpr (MODE == 0) {
+            chunk_epilogue_f32<TT, KIND, C>(p, tmem, scl_a, stages_a, sc_full, sc_empty, tm_full, tm_empty,
+                                           warp, lane, nblk, m0, t0, &s_last);
+        } else {
         constexpr int CW = C::kCW;
         const int ew = warp - C::kEpiWarp0;           // 0..15
         const int qd = warp & 3;                      // TMEM lane quadrant of this warp
@@ -858,6 +1177,7 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
                 }
             }
         }
+        }
     }
 
     tc_fence_before();
@@ -866,7 +1186,42 @@ __global__ void __launch_bounds__(CkCfg<MODE, TT>::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    if (!DEBUG && gridDim.z > 1) {
+    if (MODE == 0 && gridDim.z > 1) {
+        // f32 mode, split K: each CTA adds up a slice of the tile over the
+        // cluster in rank order, each partial first brought to the column's
+        // largest binade (exact powers of two)
+        cluster_sync();
+        const uint32_t ks = gridDim.z, rank = blockIdx.z;
+        const int ne = TT * kCkM;
+        const int per = (ne + int(ks) - 1) / int(ks);
+        const int i_end = min(ne, int(rank + 1) * per);
+        for (int i = int(rank) * per + tid; i < i_end; i += C::kThreads) {
+            const int t = i / kCkM, nn = i % kCkM;
+            const uint32_t pa = stages_a + uint32_t(i) * 8u;
+            const uint32_t ba = stages_a + uint32_t(C::kBinOff + TT * 4 + t * 4);
+            int em = -1000;
+            for (uint32_t r = 0; r < ks; ++r) em = max(em, int(ld_cluster_u32(cluster_map(ba, r))));
+            DF sum{0.0f, 0.0f};
+            for (uint32_t r = 0; r < ks; ++r) {
+                const uint32_t pr = cluster_map(pa, r);
+                const int d = int(ld_cluster_u32(cluster_map(ba, r))) - em;
+                const DF v{mul_pow2_neg(__uint_as_float(ld_cluster_u32(pr)), d),
+                           mul_pow2_neg(__uint_as_float(ld_cluster_u32(pr + 4u)), d)};
+                sum = df_add(sum, v);
+            }
+            const int64_t tg = t0 + t, row = m0 + nn;
+            if (tg < p.T && row < p.N) {
+                const int sc = em - 30;
+                if (p.y64)
+                    p.y64[tg * p.N + row] = ldexp(double(sum.hi) + double(sum.lo), sc);
+                else if (p.y)
+                    p.y[tg * p.N + row] = __fmul_rn(__fmul_rn(__fadd_rn(sum.hi, sum.lo), pow2i(sc >> 1)),
+                                                    pow2i(sc - (sc >> 1)));
+            }
+        }
+        // no CTA may leave while another still reads its shared memory
+        cluster_sync();
+    } else if (!DEBUG && gridDim.z > 1) {
         cluster_sync();
         const uint32_t ks = gridDim.z, rank = blockIdx.z;
         const int n4 = TT * kCkM / 4;
@@ -988,6 +1343,7 @@ static int choose_split(int64_t tiles, int groups, const LaunchCtx& ctx) {
 
 struct ChunkOut {
     float* y = nullptr;
+    double* y64 = nullptr;   // f32 mode: f64 outputs instead of y
     int32_t* isum = nullptr;
     // arg-max
     unsigned char* ws = nullptr;
@@ -1010,15 +1366,21 @@ static cudaError_t launch_chunk_t(const int8_t* q, const uint16_t* s, int64_t N,
     const int8_t* xh = reinterpret_cast<const int8_t*>(xq);
     bool ok = make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, K, N, K, kCkStageK, kCkM,
                        CU_TENSOR_MAP_SWIZZLE_128B) &&
-              make_map(&txh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, K, T, K, kCkStageK, TT,
-                       CU_TENSOR_MAP_SWIZZLE_128B) &&
+              // f32 mode: the f32 rows, a stage's 128 values of TT rows, unswizzled
+              (MODE == 0 ? make_map(&txh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xq, K, T, K * 4, kCkStageK, TT,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE)
+                         : make_map(&txh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, K, T, K, kCkStageK, TT,
+                                    CU_TENSOR_MAP_SWIZZLE_128B)) &&
               make_map(&txl, CU_TENSOR_MAP_DATA_TYPE_UINT8, MODE == 2 ? xh + T * K : xh, K, T, K,
                        kCkStageK, TT, CU_TENSOR_MAP_SWIZZLE_128B) &&
               // (the debug variant reads neither scale array: any valid base will do)
               make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, DEBUG ? static_cast<const void*>(q) : s,
                        nb, N, nb * 2, kCkGroup, kCkM, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&txd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, DEBUG ? static_cast<const void*>(q) : xd,
-                       DEBUG ? nb / 2 : nb, DEBUG ? N : T, nb * 4, 4, TT, CU_TENSOR_MAP_SWIZZLE_NONE);
+              // (the f32 mode reads no activation scales: any valid map will do)
+              make_map(&txd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                       (DEBUG || MODE == 0) ? static_cast<const void*>(q) : xd,
+                       (DEBUG || MODE == 0) ? nb / 2 : nb, (DEBUG || MODE == 0) ? N : T, nb * 4, 4, TT,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return cudaErrorInvalidValue;
     const int64_t t_tiles = (T + TT - 1) / TT, n_tiles = (N + kCkM - 1) / kCkM;
     if (t_tiles > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
@@ -1031,11 +1393,20 @@ static cudaError_t launch_chunk_t(const int8_t* q, const uint16_t* s, int64_t N,
     p.T = T;
     p.groups_per_split = per;
     p.y = out.y;
+    p.y64 = out.y64;
     p.isum = out.isum;
     p.err = ctx.dev_err;
     if (KIND == kCkArgmax) {
-        p.ticket = reinterpret_cast<unsigned int*>(out.ws);
-        p.keys = reinterpret_cast<unsigned long long*>(out.ws + kArgmaxHeader);
+        if (MODE == 0) {
+            // the CUDA-core arg-max's layout: its ticket, then one (value,
+            // row) per n tile and activation row
+            if (n_tiles > kMaxGrid || T > kArgmaxGroupRows) return cudaErrorInvalidValue;
+            p.ticket = reinterpret_cast<unsigned int*>(out.ws + kArgmaxGemvOff);
+            p.cands = reinterpret_cast<ArgmaxCand*>(out.ws + kArgmaxGemvOff + kArgmaxHeader);
+        } else {
+            p.ticket = reinterpret_cast<unsigned int*>(out.ws);
+            p.keys = reinterpret_cast<unsigned long long*>(out.ws + kArgmaxHeader);
+        }
         p.tok = out.tok;
         p.maxval = out.maxval;
     }
@@ -1075,6 +1446,10 @@ static void plan_of(int64_t N, int64_t K, const int64_t T, const LaunchCtx& ctx,
 
 template <int KIND>
 static void plan_any(int mode, int64_t N, int64_t K, int64_t T, const LaunchCtx& ctx, int64_t* out) {
+    if (mode == 0) {
+        if (T <= 16) return plan_of<0, 16, KIND>(N, K, T, ctx, out);
+        return plan_of<0, 32, KIND>(N, K, T, ctx, out);
+    }
     if (mode == 1) {
         if (T <= 16) return plan_of<1, 16, KIND>(N, K, T, ctx, out);
         if (T <= 32) return plan_of<1, 32, KIND>(N, K, T, ctx, out);
@@ -1097,7 +1472,7 @@ bool chunk_plan(int mode, int64_t N, int64_t K, int64_t T, bool argmax, const La
 }
 
 bool chunk_supported(int mode, int64_t N, int64_t K, int64_t T) {
-    return (mode == 1 || mode == 2) && K % (Q8_QK * kCkGroup) == 0 && T >= 1 && N >= 1 &&
+    return (mode == 0 || mode == 1 || mode == 2) && K % (Q8_QK * kCkGroup) == 0 && T >= 1 && N >= 1 &&
            encode_fn() != nullptr;
 }
 
@@ -1105,6 +1480,13 @@ template <int KIND>
 static cudaError_t launch_chunk_any(int mode, const int8_t* q, const uint16_t* s, int64_t N,
                                     int64_t K, const void* xq, const float* xd, int64_t T,
                                     const ChunkOut& out, const LaunchCtx& ctx) {
+    if (mode == 0) {
+        if constexpr (KIND == kCkDebug) return cudaErrorInvalidValue;   // no f32 block dots
+        else {
+            if (T <= 16) return launch_chunk_t<0, 16, KIND>(q, s, N, K, xq, xd, T, out, ctx);
+            return launch_chunk_t<0, 32, KIND>(q, s, N, K, xq, xd, T, out, ctx);
+        }
+    }
     if (mode == 1) {
         if (T <= 16) return launch_chunk_t<1, 16, KIND>(q, s, N, K, xq, xd, T, out, ctx);
         if (T <= 32) return launch_chunk_t<1, 32, KIND>(q, s, N, K, xq, xd, T, out, ctx);
@@ -1117,10 +1499,13 @@ static cudaError_t launch_chunk_any(int mode, const int8_t* q, const uint16_t* s
 }
 
 cudaError_t launch_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
-                         const void* xq, const float* xd, int64_t T, float* y,
+                         const void* xq, const float* xd, int64_t T, void* y, bool out_f64,
                          const LaunchCtx& ctx) {
     ChunkOut out;
-    out.y = y;
+    if (out_f64)
+        out.y64 = static_cast<double*>(y);
+    else
+        out.y = static_cast<float*>(y);
     return launch_chunk_any<kCkPlain>(mode, q, s, N, K, xq, xd, T, out, ctx);
 }
 
@@ -1132,10 +1517,13 @@ cudaError_t launch_chunk_debug(int mode, const int8_t* q, int64_t N, int64_t K, 
 }
 
 cudaError_t launch_chunk_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
-                                const void* xq, const float* xd, int64_t T, float* logits,
+                                const void* xq, const float* xd, int64_t T, void* logits,
                                 int32_t* tok, double* maxval, void* ws, const LaunchCtx& ctx) {
     ChunkOut out;
-    out.y = logits;
+    if (mode == 0)
+        out.y64 = static_cast<double*>(logits);   // f32 mode: f64 logits
+    else
+        out.y = static_cast<float*>(logits);
     out.ws = static_cast<unsigned char*>(ws);
     out.tok = tok;
     out.maxval = maxval;

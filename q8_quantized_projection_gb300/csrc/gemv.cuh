@@ -232,6 +232,14 @@ struct FixChunk32 {
     int e;
 };
 
+// v * 2^d for d <= 0 by two multiplies by normal powers of two (exact but in
+// the subnormal range); a part more than 2^252 below the row's largest is
+// dropped.
+__device__ __forceinline__ float mul_pow2_neg(float v, int d) {
+    if (d < -252) return 0.0f;
+    return __fmul_rn(__fmul_rn(v, pow2i(d >> 1)), pow2i(d - (d >> 1)));
+}
+
 // 32 values -> X = rint(x * 2^(30-E)) in four byte planes, E the block's
 // binade.  The scaling by 2^(30-E) (30-E in [-98, 156]) is two multiplies by
 // normal powers of two: exact, except that an intermediate below 2^-126 can

@@ -261,14 +261,6 @@ __device__ __forceinline__ void load_planes_block(uint32_t planes_a, const short
     f.e = pe[blk];
 }
 
-// v * 2^d for d <= 0 by two multiplies by normal powers of two (exact but in
-// the subnormal range); a part more than 2^252 below the row's largest is
-// dropped.
-__device__ __forceinline__ float mul_pow2_neg(float v, int d) {
-    if (d < -252) return 0.0f;
-    return __fmul_rn(__fmul_rn(v, pow2i(d >> 1)), pow2i(d - (d >> 1)));
-}
-
 // Four f32 activation values: read as they are, or (f32 mode with the
 // producer fused) formed as x = (s*rf)*g with the producer's two roundings,
 // s = h or, with a residual r, h + r rounded once.

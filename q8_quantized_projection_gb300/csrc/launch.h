@@ -87,15 +87,20 @@ constexpr int gemv_max_rows(int mode) { return mode == 0 ? 1 : mode == 1 ? 8 : 4
 
 // tensor-core chunk path (chunk.cu): modes 1 and 2, K % 256 == 0
 bool chunk_supported(int mode, int64_t N, int64_t K, int64_t T);
+// (f32 mode: xq is the f32 activation, xd unused; y is double [T][N] with
+// out_f64, float else)
 cudaError_t launch_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
-                         const void* xq, const float* xd, int64_t T, float* y, const LaunchCtx& ctx);
+                         const void* xq, const float* xd, int64_t T, void* y, bool out_f64,
+                         const LaunchCtx& ctx);
 cudaError_t launch_chunk_debug(int mode, const int8_t* q, int64_t N, int64_t K, const void* xq,
                                int64_t T, int32_t* isum, const LaunchCtx& ctx);
 // The chunk projection fused with the arg-max of every activation row (the LM
-// head): ws is the arg-max workspace (ticket and keys, see below); logits
-// (float [T][N]) may be NULL.
+// head): ws is the arg-max workspace (int8 modes: ticket and keys; f32 mode:
+// the CUDA-core layout from kArgmaxGemvOff, at most kMaxGrid tiles of 128
+// rows and kArgmaxGroupRows activation rows); logits (float [T][N], f32 mode
+// double) may be NULL.
 cudaError_t launch_chunk_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
-                                const void* xq, const float* xd, int64_t T, float* logits,
+                                const void* xq, const float* xd, int64_t T, void* logits,
                                 int32_t* tok, double* maxval, void* ws, const LaunchCtx& ctx);
 // The launch plan the chunk path would use (host side; occupancy queries
 // only): out[6] = TT, ks (CTAs splitting K), tiles, clusters that fit at once,
@@ -104,8 +109,9 @@ bool chunk_plan(int mode, int64_t N, int64_t K, int64_t T, bool argmax, const La
                 int64_t* out);
 // Activation rows from which projections run on the tensor cores: where one
 // chunk launch beats the decode kernel's groups of rows (one-word: groups of
-// 8, so 9 rows and more; two-word: groups of 4, so 5 and more).
-inline int64_t chunk_min_rows(int mode) { return mode == 2 ? 5 : 9; }
+// 8, so 9 rows and more; two-word: groups of 4, so 5 and more; f32: a row a
+// pass, measured break-even near 5 rows of the d = 4096 layer).
+inline int64_t chunk_min_rows(int mode) { return mode == 2 ? 5 : mode == 0 ? 6 : 9; }
 
 // K/V slices of y [rows][N] into cache row pos[m] of each row's cache
 cudaError_t launch_kv_scatter(const float* y, int64_t rows, int64_t N, const int32_t* pos, int64_t kv_col,

@@ -153,6 +153,34 @@ def test_proj_parity(mode, n, k, rows):
     check_close(mode, host(y2), y_o, norm, what=f"chunk {mode} {n}x{k} rows={rows}")
 
 
+@pytest.mark.parametrize("n,k,rows", [(300, 4096, 8), (64, 14336, 13), (200, 2048, 40)])
+def test_f32_batch_binade_spread(n, k, rows):
+    """f32 activations whose 32-value blocks lie up to 2^130 apart within a
+    row (and one all-zero row), through the batched path (tensor cores from 6
+    rows: each column's sum is kept relative to the largest block binade seen
+    so far and rescaled when a larger one comes; blocks far below are
+    negligible): within 1e-9 of the norm, f32 and f64 outputs."""
+    rng = np.random.default_rng(77 + n + k + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, rows, k).astype(np.float64)
+    scale = 2.0 ** rng.integers(-100, 30, size=(rows, k // 32))
+    x = (x.reshape(rows, k // 32, 32) * scale[:, :, None]).reshape(rows, k).astype(np.float32)
+    x[rows // 2] = 0.0
+    act = orc.quantize("f32", x)
+    y_o, norm = orc.project("f32", q, s, act)
+    qd, sd = upload_weights(q, s)
+    xq, xd = upload_act("f32", act, rows, k)
+    t = torch()
+    y = t.empty((rows, n), dtype=t.float32, device="cuda")
+    native.q8_proj("f32", qd, sd, xq, xd, rows, y)
+    check_close("f32", host(y), y_o, norm, what=f"f32 spread {n}x{k} rows={rows}")
+    y64 = t.empty((rows, n), dtype=t.float64, device="cuda")
+    native.q8_proj("f32", qd, sd, xq, xd, rows, y64, out_f64=True)
+    check_close("f32", host(y64), y_o, norm, out_f64=True, what=f"f64 spread {n}x{k} rows={rows}")
+    assert np.all(host(y64)[rows // 2] == 0.0)
+    no_device_error()
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("n,k", [(300, 4096), (64, 14336), (129, 4128)])
 @pytest.mark.parametrize("rows", [32, 64])
