@@ -718,7 +718,7 @@ def run_sweeps(native, torch, dev, capture, timed, Q, S, mats, oracle_slices=Tru
     batch = {}
     for m in ("i8", "i8x2", "f32"):
         batch[m] = {}
-        for B in ((1, 2, 4, 8, 12, 16, 32, 64) if m != "f32" else (1, 2, 4)):
+        for B in ((1, 2, 4, 8, 12, 16, 32, 64) if m != "f32" else (1, 2, 4, 8, 16)):
             acts = []
             for p, (_, n, k) in enumerate(synth.LAYER_D4096):
                 h = torch.from_numpy(synth.activations(rng, B, k)).to(dev)

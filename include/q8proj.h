@@ -166,8 +166,9 @@ q8_status act_quant_swiglu(int mode, const float* gu, int64_t rows, int64_t K, v
  * Quantized projection of a stacked activation (codegen_cuda::lane: the
  * decode step, rows = 1, and a batch's step, rows = B, with each weight read
  * once for a group of rows: up to 8 rows (one-word) or 4 (two-word) a pass;
- * from 9 (one-word) or 5 (two-word) rows with K % 256 == 0 one pass on the
- * tensor cores; f32 runs one row a pass, its arithmetic being the bound).
+ * from 9 (one-word), 5 (two-word) or 6 (f32) rows with K % 256 == 0 one pass
+ * on the tensor cores; f32 below 6 rows runs one row a pass, its arithmetic
+ * being the bound).
  *   y[m][n] for m < rows, n < N; y is float, or double when mode is
  *   Q8_ACT_F32 and out_f64 != 0.  1 <= rows <= Q8_MAX_ROWS.
  */
@@ -241,9 +242,9 @@ q8_status q8_proj_fused_swiglu(int mode, const int8_t* q, const uint16_t* s, int
  * LM head fused with its arg-max (model::author, decode_head: "the final
  * norm, the LM head and the arg-max"; decode_batch_head: one token per
  * sequence).  Modes Q8_ACT_F32 (logits to f64 accuracy) and Q8_ACT_I8 /
- * Q8_ACT_I8X2 (f32 logits).  The int8 modes from 9 (one-word) or 5
- * (two-word) rows on, with K % 256 == 0, read the head once for all rows on
- * the tensor cores.
+ * Q8_ACT_I8X2 (f32 logits).  From 9 (one-word), 5 (two-word) or 6 (f32, up
+ * to 16 rows and N <= 131072) rows on, with K % 256 == 0, the head is read
+ * once for all rows on the tensor cores.
  *   tok     int32 [rows]: the smallest n holding the row's maximum logit; NaN
  *           logits are never the maximum, and a row of NaN gives 0
  *   maxval  double [rows] or NULL: that maximum (NaN for a row of NaN)
