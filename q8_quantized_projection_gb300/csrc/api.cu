@@ -429,11 +429,11 @@ q8_status head_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, i
     LaunchCtx ctx;
     if ((st = make_ctx(stream, ctx)) != Q8_OK) return st;
     static_assert(kArgmaxKeyBytes >= 8 * Q8_MAX_ROWS, "one arg-max key per row");
-    // the tensor-core path from chunk_min_rows(mode) rows; in f32 mode up to
+    // the tensor-core path from chunk_min_head_rows(mode) rows; in f32 mode up to
     // kArgmaxGroupRows rows and kMaxGrid tiles (its candidates use the
     // CUDA-core layout of the workspace)
     const bool f32_fits = mode != Q8_ACT_F32 || (rows <= kArgmaxGroupRows && (N + 127) / 128 <= kMaxGrid);
-    if (f32_fits && rows >= chunk_min_rows(mode) && chunk_supported(mode, N, K, rows))
+    if (f32_fits && rows >= chunk_min_head_rows(mode) && chunk_supported(mode, N, K, rows))
         return launched(launch_chunk_argmax(mode, q, s, N, K, xq, xd, rows, logits, tok, maxval, workspace,
                                             ctx));
     return run_projection(mode, q, s, N, K, xq, xd, rows, logits, mode == Q8_ACT_F32 ? 1 : 0, tok,

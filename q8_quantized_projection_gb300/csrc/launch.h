@@ -110,8 +110,10 @@ bool chunk_plan(int mode, int64_t N, int64_t K, int64_t T, bool argmax, const La
 // Activation rows from which projections run on the tensor cores: where one
 // chunk launch beats the decode kernel's groups of rows (one-word: groups of
 // 8, so 9 rows and more; two-word: groups of 4, so 5 and more; f32: a row a
-// pass, measured break-even near 5 rows of the d = 4096 layer).
-inline int64_t chunk_min_rows(int mode) { return mode == 2 ? 5 : mode == 0 ? 6 : 9; }
+// pass, measured on the d = 4096 layer: even at 3 rows, 199 against 239 us
+// at 4).  The f32 LM head (a launch per row) breaks even at 6 rows.
+inline int64_t chunk_min_rows(int mode) { return mode == 2 ? 5 : mode == 0 ? 4 : 9; }
+inline int64_t chunk_min_head_rows(int mode) { return mode == 0 ? 6 : chunk_min_rows(mode); }
 
 // K/V slices of y [rows][N] into cache row pos[m] of each row's cache
 cudaError_t launch_kv_scatter(const float* y, int64_t rows, int64_t N, const int32_t* pos, int64_t kv_col,
