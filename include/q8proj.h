@@ -324,12 +324,12 @@ q8_status q8_debug_row_geometry_fused(int mode, int prod, int64_t N, int64_t K, 
 /*
  * Debug, host side (the current device's occupancy is queried; nothing is
  * launched): the plan of the tensor-core path for a projection of T rows
- * (argmax = 0: q8_proj_chunk and q8_proj from 9 one-word / 5 two-word rows;
- * argmax = 1: head_argmax).  out (host, 6 int64) receives: TT (activation rows
- * a tile), ks (CTAs of a cluster, each over 1/ks of K), tiles (128 x TT, one
- * cluster each), clusters that fit on the device at once, waves, pipeline
- * stages.  Modes Q8_ACT_I8 / Q8_ACT_I8X2,
- * K % 256 == 0, 1 <= T <= Q8_MAX_ROWS; otherwise Q8_ERR_MODE / Q8_ERR_SHAPE.
+ * (argmax = 0: q8_proj_chunk and q8_proj from 9 one-word / 5 two-word / 4
+ * f32 rows; argmax = 1: head_argmax).  out (host, 6 int64) receives: TT
+ * (activation rows a tile), ks (CTAs of a cluster, each over 1/ks of K),
+ * tiles (128 x TT, one cluster each), clusters that fit on the device at
+ * once, waves, pipeline stages.  Any activation mode, K % 256 == 0,
+ * 1 <= T <= Q8_MAX_ROWS; otherwise Q8_ERR_MODE / Q8_ERR_SHAPE.
  */
 q8_status q8_debug_chunk_plan(int mode, int64_t N, int64_t K, int64_t T, int argmax, int64_t* out);
 

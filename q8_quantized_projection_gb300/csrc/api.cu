@@ -279,7 +279,7 @@ q8_status q8_proj_chunk(int mode, const int8_t* q, const uint16_t* s, int64_t N,
 
 q8_status q8_debug_chunk_plan(int mode, int64_t N, int64_t K, int64_t T, int argmax, int64_t* out) {
     if (!out) return Q8_ERR_ARG;
-    if (mode != Q8_ACT_I8 && mode != Q8_ACT_I8X2) return Q8_ERR_MODE;
+    if (!valid_mode(mode)) return Q8_ERR_MODE;
     if (N < 1 || N > (int64_t(1) << 31) || T < 1 || T > Q8_MAX_ROWS || K < 256 || K % 256 != 0 ||
         K > (int64_t(1) << 24))
         return Q8_ERR_SHAPE;

@@ -136,7 +136,7 @@ def test_chunk_plan_host_errors(lib):
     """q8_debug_chunk_plan checks its arguments before touching a device."""
     import ctypes as C
     out = (C.c_int64 * 6)()
-    assert lib.q8_debug_chunk_plan(0, 128, 4096, 16, 0, C.cast(out, C.c_void_p)) == 4     # f32: MODE
+    assert lib.q8_debug_chunk_plan(3, 128, 4096, 16, 0, C.cast(out, C.c_void_p)) == 4     # mode
     assert lib.q8_debug_chunk_plan(1, 128, 4100, 16, 0, C.cast(out, C.c_void_p)) == 2     # K % 256
     assert lib.q8_debug_chunk_plan(1, 128, 4096, 0, 0, C.cast(out, C.c_void_p)) == 2      # T
     assert lib.q8_debug_chunk_plan(1, 128, 4096, 257, 0, C.cast(out, C.c_void_p)) == 2    # T > max

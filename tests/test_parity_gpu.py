@@ -670,6 +670,18 @@ def test_head_plan():
     assert plan["clusters"] == sms and plan["waves"] == -(-1002 // sms), plan
 
 
+def test_f32_chunk_plan():
+    """The f32 mode's tensor-core plan: tiles of 16 or 32 activation rows (four
+    byte planes make the MMA's N), the head's K unsplit, and K split over a
+    cluster where a projection has few tiles."""
+    head = native.q8_debug_chunk_plan("f32", *synth.HEAD_SHAPE, 16, argmax=True)
+    assert head["TT"] == 16 and head["ks"] == 1 and head["tiles"] == 1002, head
+    wo = native.q8_debug_chunk_plan("f32", 4096, 4096, 8)
+    assert wo["TT"] == 16 and wo["tiles"] == 32 and wo["ks"] > 1, wo
+    big = native.q8_debug_chunk_plan("f32", 4096, 4096, 40)
+    assert big["TT"] == 32 and big["tiles"] == 64, big
+
+
 @pytest.mark.parametrize("mode", ["i8", "i8x2"])
 @pytest.mark.parametrize("n,k,t", [(129, 1024, 16), (64, 4096, 130), (40, 512, 3), (130, 768, 64)])
 def test_chunk_block_dots_exact(mode, n, k, t):

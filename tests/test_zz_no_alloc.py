@@ -17,7 +17,7 @@ from q8_quantized_projection_gb300 import build, native, synth
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode,rows", [("i8", 16), ("f32", 3), ("i8x2", 1)])
+@pytest.mark.parametrize("mode,rows", [("i8", 16), ("f32", 3), ("f32", 8), ("i8x2", 1)])
 def test_noalloc_head_matches_workspace_head(mode, rows):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
