@@ -1274,9 +1274,10 @@ static EncodeTiledFn encode_fn() {
     return f;
 }
 
-static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                     uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                     CUtensorMapSwizzle sw) {
+// A 2-D tiled tensor map (also used by the batched kernel of gemv_rpl.cuh).
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle sw) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {inner, outer};

@@ -1,0 +1,266 @@
+// gemv_rpl.cuh -- batched projection of a few activation rows (2-8 one-word,
+// 2-4 two-word) with a weight row a lane.
+//
+// The decode kernel gives each lane 16-byte chunks of a row's part and sums a
+// row over the warp with a butterfly per item; with several activation rows
+// that butterfly and the per-chunk scale products dominate its instruction
+// count.  Here lane l of a warp owns weight row l of a group of 32 rows: it
+// reads its row's 32-value blocks from shared memory, each activation row's
+// block (the same address for every lane: one broadcast load) and its scale,
+// and keeps R running sums in registers.  No lane-to-lane reduction is left
+// in the stream, only one combine of the warps' partial sums per row group.
+//
+// Stages: 32 weight rows x 1024 bytes of K as eight 2-D TMA tiles of 32 rows x
+// 128 bytes (128-byte swizzle, so the 16-byte loads of 8 consecutive lanes hit
+// distinct bank groups), and the activation rows' codes (tiles of R rows x 256
+// bytes) and scales (R rows x 32) over the same 1024 values: weights before the
+// wait on the previous kernel, activations after it.  A ring of four slots;
+// the 16 consumer warps are four per slot, and warp (slot, quarter) reduces a
+// quarter of each of its slot's stages (8 blocks) for every row of the group.
+// A lane reads its row's 8 weight scales of the quarter straight from global
+// memory.  At the end of a row group the warps' sums meet in shared memory
+// and are added in warp order (fixed: results do not depend on timing).
+//
+// Requires K % 1024 == 0 (whole stages).  Every wait is bounded (device error
+// word on time-out).
+#pragma once
+
+#include <cuda.h>
+
+#include "gemv.cuh"
+
+namespace q8 {
+
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle sw);
+
+constexpr int kRplWarps = 16;                      // consumer warps
+constexpr int kRplThreads = 32 * (kRplWarps + 1);
+constexpr int kRplRows = 32;                       // weight rows a group: a lane each
+constexpr int kRplKS = 1024;                       // bytes of K a stage
+constexpr int kRplSlots = 4;                       // ring slots, four consumer warps each
+
+template <int MODE, int R>
+struct RplCfg {
+    static constexpr int kPlanes = MODE == 2 ? 2 : 1;
+    static constexpr int kW = kRplRows * kRplKS;                // 8 tiles of [32][128]
+    static constexpr int kX = kPlanes * R * kRplKS;             // [plane][4 tiles][R][256]
+    static constexpr int kXD = R * (kRplKS / Q8_QK) * 4;        // [R][32] f32
+    static constexpr int kStage = (kW + kX + kXD + 1023) / 1024 * 1024;
+    static constexpr int kPsum = kRplWarps * kRplRows * R * 4;  // [warp][lane][R]
+    static constexpr size_t kSmem = size_t(kRplSlots) * kStage + kPsum + 2 * kRplSlots * 8 + 1024;
+    static_assert(kSmem <= 227 * 1024, "shared memory");
+};
+
+// A plain projection of 2 or more rows in whole stages, with the 16-byte
+// alignment the tensor maps need; anything else takes the decode kernel.
+inline bool rpl_fits(const GemvArgs& a) {
+    const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    return a.rows >= 2 && a.K >= kRplKS && a.K % kRplKS == 0 && a.N <= (int64_t(1) << 31) && a.y &&
+           !a.out_f64 && !a.tok && !a.h && !a.k_cache && al16(a.q) && al16(a.s) && al16(a.act) && al16(a.xd) &&
+           a.plane % 16 == 0;
+}
+
+__device__ __forceinline__ void rpl_tma2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+template <int MODE, int R>
+__global__ void __launch_bounds__(kRplThreads, 1)
+    gemv_rpl_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
+                    const __grid_constant__ CUtensorMap tm_xl, const __grid_constant__ CUtensorMap tm_xd,
+                    const GemvParams p) {
+    static_assert(MODE == 1 || MODE == 2, "int8 activation codes");
+    using C = RplCfg<MODE, R>;
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte alignment for the swizzled weight tiles
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* psum = reinterpret_cast<float*>(smem + size_t(kRplSlots) * C::kStage);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kRplSlots) * C::kStage + C::kPsum);
+    uint64_t* empty = full + kRplSlots;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int64_t N = p.N, K = p.K;
+    const int64_t r0 = N * c / G, r1 = N * (c + 1) / G;
+    const int ngroups = int((r1 - r0 + kRplRows - 1) / kRplRows);
+    const int nsl = int(K / kRplKS);
+    const int64_t nst = int64_t(ngroups) * nsl;
+    const int rows = p.rows;
+
+    if (tid == 0) {
+        for (int i = 0; i < kRplSlots; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 4);   // the slot's four warps
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == kRplWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            constexpr uint32_t kTx = uint32_t(C::kW + C::kX + C::kXD);   // whole tiles, rows past the end zero
+            auto acts = [&](int64_t t) {
+                const int j = int(t % nsl), slot = int(t % kRplSlots);
+                unsigned char* st = smem + size_t(slot) * C::kStage;
+                for (int k = 0; k < 4; ++k) {
+                    rpl_tma2d(st + C::kW + k * R * 256, &tm_xh, j * kRplKS + k * 256, 0, &full[slot]);
+                    if constexpr (MODE == 2)
+                        rpl_tma2d(st + C::kW + (4 + k) * R * 256, &tm_xl, j * kRplKS + k * 256, 0, &full[slot]);
+                }
+                rpl_tma2d(st + C::kW + C::kX, &tm_xd, j * (kRplKS / Q8_QK), 0, &full[slot]);
+            };
+            const int64_t npre = nst < kRplSlots ? nst : kRplSlots;
+            int64_t issued = 0;
+            for (int64_t t = 0; t < nst; ++t) {
+                const int g = int(t / nsl), j = int(t % nsl), slot = int(t % kRplSlots);
+                if (t >= kRplSlots &&
+                    !mbar_wait(&empty[slot], uint32_t((t / kRplSlots) - 1) & 1u, p.err))
+                    break;
+                const int rg0 = int(r0 + int64_t(g) * kRplRows);
+                mbar_arrive_expect_tx(&full[slot], kTx);
+                unsigned char* st = smem + size_t(slot) * C::kStage;
+                for (int k = 0; k < 8; ++k)
+                    rpl_tma2d(st + k * (kRplRows * 128), &tm_w, j * kRplKS + k * 128, rg0, &full[slot]);
+                if (t == npre - 1) {
+                    // the first stages' weights are on their way: the
+                    // activations belong to the previous kernel until here
+                    pdl_wait();
+                    for (int64_t u = 0; u <= t; ++u) acts(u);
+                } else if (t >= npre) {
+                    acts(t);
+                }
+                ++issued;
+            }
+            // never leave with copies in flight into this CTA's shared memory
+            for (int64_t t = issued > kRplSlots ? issued - kRplSlots : 0; t < issued; ++t)
+                mbar_wait(&full[t % kRplSlots], uint32_t((t / kRplSlots) & 1), p.err);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    pdl_wait();   // y belongs to the previous kernel until here
+    const int slot = warp >> 2, qw = warp & 3;   // this warp's slot and quarter of a stage
+    bool ok = true;
+    for (int g = 0; g < ngroups; ++g) {
+        const int64_t rg0 = r0 + int64_t(g) * kRplRows;
+        const int nr = int(min64(kRplRows, r1 - rg0));
+        float acc[R];
+#pragma unroll
+        for (int m = 0; m < R; ++m) acc[m] = 0.0f;
+        for (int j = 0; j < nsl; ++j) {
+            const int64_t t = int64_t(g) * nsl + j;
+            if (int(t % kRplSlots) != slot) continue;
+            int4 s8 = make_int4(0, 0, 0, 0);
+            if (lane < nr)   // the lane's row's 8 block scales of this quarter
+                s8 = ldg_nc_v4(reinterpret_cast<const unsigned char*>(p.s) + (rg0 + lane) * (K / 16) +
+                               int64_t(j) * (kRplKS / 16) + qw * 16);
+            if (ok) ok = mbar_wait(&full[slot], uint32_t((t / kRplSlots) & 1), p.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok && lane < nr) {
+                const uint32_t st = smem_u32(smem + size_t(slot) * C::kStage);
+                const uint32_t xa = st + uint32_t(C::kW);
+                const uint32_t da = st + uint32_t(C::kW + C::kX + qw * 32);
+                const uint32_t sh[4] = {uint32_t(s8.x), uint32_t(s8.y), uint32_t(s8.z), uint32_t(s8.w)};
+#pragma unroll 2
+                for (int b = 0; b < 8; ++b) {
+                    const int B = qw * 8 + b;   // block within the stage
+                    // weight tile B / 4, row lane, 16-byte chunks (B % 4) * 2 and + 1, swizzled
+                    const uint32_t wr = st + uint32_t((B >> 2) * (kRplRows * 128) + lane * 128);
+                    const int c0 = (B & 3) * 2;
+                    const int4 w0 = lds128(wr + uint32_t(((c0 ^ (lane & 7)) << 4)));
+                    const int4 w1 = lds128(wr + uint32_t((((c0 + 1) ^ (lane & 7)) << 4)));
+                    const float sw = half_bits_to_float(uint16_t((b & 1) ? (sh[b >> 1] >> 16) : (sh[b >> 1] & 0xFFFFu)));
+                    // activation tile B / 8 (rows of 256 bytes), block B % 8
+                    const uint32_t xb = xa + uint32_t((B >> 3) * R * 256 + (B & 7) * 32);
+#pragma unroll
+                    for (int m = 0; m < R; ++m) {
+                        const uint32_t xm = xb + uint32_t(m * 256);
+                        const float xd = __uint_as_float(lds32(da + uint32_t(m * (kRplKS / Q8_QK) * 4 + 4 * b)));
+                        float fi;
+                        if constexpr (MODE == 1) {
+                            const int isum = dot16_i8(w0, lds128(xm)) + dot16_i8(w1, lds128(xm + 16u));
+                            fi = small_int_to_float(isum);   // |isum| < 2^19
+                        } else {
+                            const uint32_t xl = xm + uint32_t(4 * R * 256);   // the lo plane
+                            const int isum = dot16_i8x2(w0, lds128(xm), lds128(xl)) +
+                                             dot16_i8x2(w1, lds128(xm + 16u), lds128(xl + 16u));
+                            fi = float(isum);
+                        }
+                        acc[m] = fmaf(fi, sw * xd, acc[m]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && ok) mbar_arrive(&empty[slot]);
+        }
+        // the row group's sums: each warp's into shared memory, then per (row,
+        // activation row) the 16 warps' in warp order
+#pragma unroll
+        for (int m = 0; m < R; ++m) psum[(warp * kRplRows + lane) * R + m] = acc[m];
+        consumer_bar<kRplWarps * 32>();
+        if (ok && tid < kRplRows * R) {
+            const int l = tid % kRplRows, m = tid / kRplRows;
+            if (l < nr && m < rows) {
+                float sum = psum[l * R + m];
+                for (int w = 1; w < kRplWarps; ++w) sum += psum[(w * kRplRows + l) * R + m];
+                reinterpret_cast<float*>(p.y)[m * N + rg0 + l] = sum;
+            }
+        }
+        consumer_bar<kRplWarps * 32>();
+    }
+}
+
+template <int MODE, int R>
+cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
+    using C = RplCfg<MODE, R>;
+    auto kern = gemv_rpl_kernel<MODE, R>;
+    static std::atomic<bool> configured[kMaxDevices];
+    if (const cudaError_t e = set_smem_once(kern, C::kSmem, ctx.dev, configured); e != cudaSuccess) return e;
+    if (!rpl_fits(a) || a.rows > R) return cudaErrorInvalidValue;
+    alignas(64) CUtensorMap tw, txh, txl, txd;
+    const int8_t* xh = static_cast<const int8_t*>(a.act);
+    const bool ok =
+        make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q, a.K, a.N, a.K, 128, kRplRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) &&
+        make_map(&txh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, a.K, a.rows, a.K, 256, R, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        make_map(&txl, CU_TENSOR_MAP_DATA_TYPE_UINT8, MODE == 2 ? xh + a.plane : xh, a.K, a.rows, a.K, 256, R,
+                 CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        make_map(&txd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.xd, a.K / Q8_QK, a.rows, (a.K / Q8_QK) * 4,
+                 kRplKS / Q8_QK, R, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) return cudaErrorInvalidValue;
+    GemvParams p{};
+    p.q = a.q;
+    p.s = a.s;
+    p.N = a.N;
+    p.K = a.K;
+    p.act = a.act;
+    p.xd = a.xd;
+    p.plane = a.plane;
+    p.rows = a.rows;
+    p.y = a.y;
+    p.err = ctx.dev_err;
+    int grid = ctx.num_sms;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+    if (int64_t(grid) > a.N) grid = int(a.N);
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attrs[2];
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kRplThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = ctx.stream;
+    cfg.numAttrs = pdl_attrs(ctx, attrs);
+    cfg.attrs = attrs;
+    return cudaLaunchKernelEx(&cfg, kern, tw, txh, txl, txd, p);
+}
+
+}  // namespace q8

@@ -201,6 +201,29 @@ def test_proj_parity_large_batches(mode, n, k, rows):
     check_close(mode, host(y), y_o, norm, what=f"{mode} {n}x{k} rows={rows}")
 
 
+@pytest.mark.parametrize("mode,rows", [("i8", 3), ("i8", 4), ("i8", 5), ("i8", 8),
+                                       ("i8x2", 2), ("i8x2", 3), ("i8x2", 4)])
+@pytest.mark.parametrize("n,k", [(6100, 2048), (5000, 5120), (9731, 1024), (4900, 14336)])
+def test_batched_row_groups(mode, rows, n, k):
+    """Batched int8 projections where each CTA owns several 32-row groups
+    (N well above 32 x the SM count), ragged in N, with 1, 2, 5 and 14 stages
+    of 1024 values per group; two calls give identical bits."""
+    rng = np.random.default_rng(3000 + n + k + rows)
+    q, s = synth.q8_weights(rng, n, k)
+    x = synth.activations(rng, rows, k)
+    act = orc.quantize(mode, x)
+    y_o, norm = orc.project(mode, q, s, act)
+    qd, sd = upload_weights(q, s)
+    xq, xd = upload_act(mode, act, rows, k)
+    t = torch()
+    y = t.empty((rows, n), dtype=t.float32, device="cuda")
+    native.q8_proj(mode, qd, sd, xq, xd, rows, y)
+    check_close(mode, host(y), y_o, norm, what=f"{mode} {n}x{k} rows={rows}")
+    y2 = t.full((rows, n), float("nan"), dtype=t.float32, device="cuda")
+    native.q8_proj(mode, qd, sd, xq, xd, rows, y2)
+    assert t.equal(y, y2)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_proj_deterministic_and_zero(mode):
     rng = np.random.default_rng(77)
