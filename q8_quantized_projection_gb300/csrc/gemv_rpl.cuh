@@ -12,13 +12,13 @@
 //
 // Stages: 32 weight rows x 1024 bytes of K as eight 2-D TMA tiles of 32 rows x
 // 128 bytes (128-byte swizzle, so the 16-byte loads of 8 consecutive lanes hit
-// distinct bank groups), and the activation rows' codes (tiles of R rows x 256
-// bytes) and scales (R rows x 32) over the same 1024 values: weights before the
-// wait on the previous kernel, activations after it.  A ring of four slots;
+// distinct bank groups) and their block scales, and the activation rows' codes
+// (tiles of R rows x 256 bytes) and scales (R rows x 32) over the same 1024
+// values: weights before the wait on the previous kernel, activations after it.  A ring of four slots;
 // the 16 consumer warps are four per slot, and warp (slot, quarter) reduces a
 // quarter of each of its slot's stages (8 blocks) for every row of the group.
-// A lane reads its row's 8 weight scales of the quarter straight from global
-// memory.  At the end of a row group the warps' sums meet in shared memory
+// The weight rows' block scales come in the same stage (32 rows x 64 bytes,
+// 64-byte swizzle: the lanes' 16-byte reads hit distinct bank groups).  At the end of a row group the warps' sums meet in shared memory
 // and are added in warp order (fixed: results do not depend on timing).
 //
 // Requires K % 1024 == 0 (whole stages).  Every wait is bounded (device error
@@ -45,9 +45,10 @@ template <int MODE, int R>
 struct RplCfg {
     static constexpr int kPlanes = MODE == 2 ? 2 : 1;
     static constexpr int kW = kRplRows * kRplKS;                // 8 tiles of [32][128]
+    static constexpr int kS = kRplRows * (kRplKS / Q8_QK) * 2;  // [32][64] bytes of f16 scales
     static constexpr int kX = kPlanes * R * kRplKS;             // [plane][4 tiles][R][256]
     static constexpr int kXD = R * (kRplKS / Q8_QK) * 4;        // [R][32] f32
-    static constexpr int kStage = (kW + kX + kXD + 1023) / 1024 * 1024;
+    static constexpr int kStage = (kW + kS + kX + kXD + 1023) / 1024 * 1024;
     static constexpr int kPsum = kRplWarps * kRplRows * R * 4;  // [warp][lane][R]
     static constexpr size_t kSmem = size_t(kRplSlots) * kStage + kPsum + 2 * kRplSlots * 8 + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory");
@@ -72,7 +73,8 @@ __device__ __forceinline__ void rpl_tma2d(void* dst, const CUtensorMap* map, int
 
 template <int MODE, int R>
 __global__ void __launch_bounds__(kRplThreads, 1)
-    gemv_rpl_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
+    gemv_rpl_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
+                    const __grid_constant__ CUtensorMap tm_xh,
                     const __grid_constant__ CUtensorMap tm_xl, const __grid_constant__ CUtensorMap tm_xd,
                     const GemvParams p) {
     static_assert(MODE == 1 || MODE == 2, "int8 activation codes");
@@ -107,16 +109,17 @@ __global__ void __launch_bounds__(kRplThreads, 1)
     if (warp == kRplWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            constexpr uint32_t kTx = uint32_t(C::kW + C::kX + C::kXD);   // whole tiles, rows past the end zero
+            constexpr uint32_t kTx = uint32_t(C::kW + C::kS + C::kX + C::kXD);   // whole tiles, rows past the end zero
             auto acts = [&](int64_t t) {
                 const int j = int(t % nsl), slot = int(t % kRplSlots);
                 unsigned char* st = smem + size_t(slot) * C::kStage;
                 for (int k = 0; k < 4; ++k) {
-                    rpl_tma2d(st + C::kW + k * R * 256, &tm_xh, j * kRplKS + k * 256, 0, &full[slot]);
+                    rpl_tma2d(st + C::kW + C::kS + k * R * 256, &tm_xh, j * kRplKS + k * 256, 0, &full[slot]);
                     if constexpr (MODE == 2)
-                        rpl_tma2d(st + C::kW + (4 + k) * R * 256, &tm_xl, j * kRplKS + k * 256, 0, &full[slot]);
+                        rpl_tma2d(st + C::kW + C::kS + (4 + k) * R * 256, &tm_xl, j * kRplKS + k * 256, 0,
+                                  &full[slot]);
                 }
-                rpl_tma2d(st + C::kW + C::kX, &tm_xd, j * (kRplKS / Q8_QK), 0, &full[slot]);
+                rpl_tma2d(st + C::kW + C::kS + C::kX, &tm_xd, j * (kRplKS / Q8_QK), 0, &full[slot]);
             };
             const int64_t npre = nst < kRplSlots ? nst : kRplSlots;
             int64_t issued = 0;
@@ -130,6 +133,7 @@ __global__ void __launch_bounds__(kRplThreads, 1)
                 unsigned char* st = smem + size_t(slot) * C::kStage;
                 for (int k = 0; k < 8; ++k)
                     rpl_tma2d(st + k * (kRplRows * 128), &tm_w, j * kRplKS + k * 128, rg0, &full[slot]);
+                rpl_tma2d(st + C::kW, &tm_s, j * (kRplKS / 16), rg0, &full[slot]);
                 if (t == npre - 1) {
                     // the first stages' weights are on their way: the
                     // activations belong to the previous kernel until here
@@ -160,16 +164,15 @@ __global__ void __launch_bounds__(kRplThreads, 1)
         for (int j = 0; j < nsl; ++j) {
             const int64_t t = int64_t(g) * nsl + j;
             if (int(t % kRplSlots) != slot) continue;
-            int4 s8 = make_int4(0, 0, 0, 0);
-            if (lane < nr)   // the lane's row's 8 block scales of this quarter
-                s8 = ldg_nc_v4(reinterpret_cast<const unsigned char*>(p.s) + (rg0 + lane) * (K / 16) +
-                               int64_t(j) * (kRplKS / 16) + qw * 16);
             if (ok) ok = mbar_wait(&full[slot], uint32_t((t / kRplSlots) & 1), p.err);
             ok = __all_sync(0xffffffffu, ok);
             if (ok && lane < nr) {
                 const uint32_t st = smem_u32(smem + size_t(slot) * C::kStage);
-                const uint32_t xa = st + uint32_t(C::kW);
-                const uint32_t da = st + uint32_t(C::kW + C::kX + qw * 32);
+                const uint32_t xa = st + uint32_t(C::kW + C::kS);
+                const uint32_t da = st + uint32_t(C::kW + C::kS + C::kX + qw * 32);
+                // the lane's row's 8 block scales of this quarter: 16-byte chunk
+                // qw of its 64-byte row, 64-byte swizzle
+                const int4 s8 = lds128(st + uint32_t(C::kW + lane * 64 + ((qw ^ ((lane >> 1) & 3)) << 4)));
                 const uint32_t sh[4] = {uint32_t(s8.x), uint32_t(s8.y), uint32_t(s8.z), uint32_t(s8.w)};
 #pragma unroll 2
                 for (int b = 0; b < 8; ++b) {
@@ -227,11 +230,13 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     static std::atomic<bool> configured[kMaxDevices];
     if (const cudaError_t e = set_smem_once(kern, C::kSmem, ctx.dev, configured); e != cudaSuccess) return e;
     if (!rpl_fits(a) || a.rows > R) return cudaErrorInvalidValue;
-    alignas(64) CUtensorMap tw, txh, txl, txd;
+    alignas(64) CUtensorMap tw, ts, txh, txl, txd;
     const int8_t* xh = static_cast<const int8_t*>(a.act);
     const bool ok =
         make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q, a.K, a.N, a.K, 128, kRplRows,
                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+        make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.s, a.K / 16, a.N, a.K / 16, kRplKS / 16, kRplRows,
+                 CU_TENSOR_MAP_SWIZZLE_64B) &&
         make_map(&txh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, a.K, a.rows, a.K, 256, R, CU_TENSOR_MAP_SWIZZLE_NONE) &&
         make_map(&txl, CU_TENSOR_MAP_DATA_TYPE_UINT8, MODE == 2 ? xh + a.plane : xh, a.K, a.rows, a.K, 256, R,
                  CU_TENSOR_MAP_SWIZZLE_NONE) &&
@@ -260,7 +265,7 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     cfg.stream = ctx.stream;
     cfg.numAttrs = pdl_attrs(ctx, attrs);
     cfg.attrs = attrs;
-    return cudaLaunchKernelEx(&cfg, kern, tw, txh, txl, txd, p);
+    return cudaLaunchKernelEx(&cfg, kern, tw, ts, txh, txl, txd, p);
 }
 
 }  // namespace q8
