@@ -21,6 +21,9 @@
 // 64-byte swizzle: the lanes' 16-byte reads hit distinct bank groups).  At the end of a row group the warps' sums meet in shared memory
 // and are added in warp order (fixed: results do not depend on timing).
 //
+// CTAs own whole 32-row groups (the ceil(N/32) groups split evenly over the
+// grid): a tile never carries rows that another CTA reads as well.
+//
 // Requires K % 1024 == 0 (whole stages).  Every wait is bounded (device error
 // word on time-out).
 #pragma once
@@ -90,8 +93,11 @@ __global__ void __launch_bounds__(kRplThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
     const int64_t N = p.N, K = p.K;
-    const int64_t r0 = N * c / G, r1 = N * (c + 1) / G;
-    const int ngroups = int((r1 - r0 + kRplRows - 1) / kRplRows);
+    // whole 32-row groups a CTA: a tile never holds another CTA's rows
+    const int64_t ng_all = (N + kRplRows - 1) / kRplRows;
+    const int64_t g0 = ng_all * c / G, g1 = ng_all * (c + 1) / G;
+    const int64_t r0 = g0 * kRplRows, r1 = min64(N, g1 * kRplRows);
+    const int ngroups = int(g1 - g0);
     const int nsl = int(K / kRplKS);
     const int64_t nst = int64_t(ngroups) * nsl;
     const int rows = p.rows;
@@ -256,7 +262,7 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     p.err = ctx.dev_err;
     int grid = ctx.num_sms;
     if (grid > kMaxGrid) grid = kMaxGrid;
-    if (int64_t(grid) > a.N) grid = int(a.N);
+    if (int64_t(grid) > (a.N + kRplRows - 1) / kRplRows) grid = int((a.N + kRplRows - 1) / kRplRows);
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attrs[2];
     cfg.gridDim = dim3(grid);
