@@ -14,7 +14,8 @@
 // 128 bytes (128-byte swizzle, so the 16-byte loads of 8 consecutive lanes hit
 // distinct bank groups) and their block scales, and the activation rows' codes
 // (tiles of R rows x 256 bytes) and scales (R rows x 32) over the same 1024
-// values: weights before the wait on the previous kernel, activations after it.  A ring of four slots;
+// values: weights before the wait on the previous kernel, activations after it.
+// Weight and scale tiles carry an evict-first L2 hint (read once per launch).  A ring of four slots;
 // the 16 consumer warps are four per slot, and warp (slot, quarter) reduces a
 // quarter of each of its slot's stages (8 blocks) for every row of the group.
 // The weight rows' block scales come in the same stage (32 rows x 64 bytes,
@@ -74,6 +75,15 @@ __device__ __forceinline__ void rpl_tma2d(void* dst, const CUtensorMap* map, int
         : "memory");
 }
 
+__device__ __forceinline__ void rpl_tma2d_ef(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                             uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
 template <int MODE, int R>
 __global__ void __launch_bounds__(kRplThreads, 1)
     gemv_rpl_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
@@ -128,6 +138,7 @@ __global__ void __launch_bounds__(kRplThreads, 1)
                 rpl_tma2d(st + C::kW + C::kS + C::kX, &tm_xd, j * (kRplKS / Q8_QK), 0, &full[slot]);
             };
             const int64_t npre = nst < kRplSlots ? nst : kRplSlots;
+            const uint64_t pol = policy_evict_first();
             int64_t issued = 0;
             for (int64_t t = 0; t < nst; ++t) {
                 const int g = int(t / nsl), j = int(t % nsl), slot = int(t % kRplSlots);
@@ -138,8 +149,8 @@ __global__ void __launch_bounds__(kRplThreads, 1)
                 mbar_arrive_expect_tx(&full[slot], kTx);
                 unsigned char* st = smem + size_t(slot) * C::kStage;
                 for (int k = 0; k < 8; ++k)
-                    rpl_tma2d(st + k * (kRplRows * 128), &tm_w, j * kRplKS + k * 128, rg0, &full[slot]);
-                rpl_tma2d(st + C::kW, &tm_s, j * (kRplKS / 16), rg0, &full[slot]);
+                    rpl_tma2d_ef(st + k * (kRplRows * 128), &tm_w, j * kRplKS + k * 128, rg0, &full[slot], pol);
+                rpl_tma2d_ef(st + C::kW, &tm_s, j * (kRplKS / 16), rg0, &full[slot], pol);
                 if (t == npre - 1) {
                     // the first stages' weights are on their way: the
                     // activations belong to the previous kernel until here
