@@ -1,26 +1,31 @@
-// gemv_rpl.cuh -- batched projection of a few activation rows (2-8 one-word,
+// gemv_rpl.cuh -- batched projection of a few activation rows (3-8 one-word,
 // 2-4 two-word) with a weight row a lane.
 //
 // The decode kernel gives each lane 16-byte chunks of a row's part and sums a
 // row over the warp with a butterfly per item; with several activation rows
 // that butterfly and the per-chunk scale products dominate its instruction
 // count.  Here lane l of a warp owns weight row l of a group of 32 rows: it
-// reads its row's 32-value blocks from shared memory, each activation row's
-// block (the same address for every lane: one broadcast load) and its scale,
-// and keeps R running sums in registers.  No lane-to-lane reduction is left
-// in the stream, only one combine of the warps' partial sums per row group.
+// reads its row's 32-value blocks and block scales from shared memory, each
+// activation row's block (the same address for every lane: one broadcast
+// load) and its scale, and keeps R running sums in registers.  No lane-to-lane
+// reduction is left in the stream.
 //
-// Stages: 32 weight rows x 1024 bytes of K as eight 2-D TMA tiles of 32 rows x
-// 128 bytes (128-byte swizzle, so the 16-byte loads of 8 consecutive lanes hit
-// distinct bank groups) and their block scales, and the activation rows' codes
-// (tiles of R rows x 256 bytes) and scales (R rows x 32) over the same 1024
-// values: weights before the wait on the previous kernel, activations after it.
-// Weight and scale tiles carry an evict-first L2 hint (read once per launch).  A ring of four slots;
-// the 16 consumer warps are four per slot, and warp (slot, quarter) reduces a
-// quarter of each of its slot's stages (8 blocks) for every row of the group.
-// The weight rows' block scales come in the same stage (32 rows x 64 bytes,
-// 64-byte swizzle: the lanes' 16-byte reads hit distinct bank groups).  At the end of a row group the warps' sums meet in shared memory
-// and are added in warp order (fixed: results do not depend on timing).
+// A stage covers 32 weight rows x 1024 values of K:
+//   - the weights as eight 2-D TMA tiles of 32 rows x 128 bytes (128-byte
+//     swizzle, so the 16-byte loads of 8 consecutive lanes hit distinct bank
+//     groups);
+//   - the rows' block scales, 32 rows x 64 bytes (64-byte swizzle, same
+//     reason);
+//   - the activation rows' codes (tiles of R rows x 256 bytes a plane) and
+//     block scales (R rows x 32).
+// Weights and scales are issued before the wait on the previous kernel, with
+// an evict-first L2 hint (read once per launch); activations after it.  A ring
+// of four stages; the 16 consumer warps are four per slot, and warp (slot,
+// quarter) reduces a quarter of each of its slot's stages (8 blocks) for every
+// row of the group.  At the end of a row group the warps' sums go to shared
+// memory and are added in warp order (fixed: results do not depend on timing):
+// by a combining warp through two buffers (no consumer warp waits for
+// another), or by the consumer warps themselves between two barriers.
 //
 // CTAs own whole 32-row groups (the ceil(N/32) groups split evenly over the
 // grid): a tile never carries rows that another CTA reads as well.
@@ -40,7 +45,6 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
               CUtensorMapSwizzle sw);
 
 constexpr int kRplWarps = 16;                      // consumer warps
-constexpr int kRplThreads = 32 * (kRplWarps + 1);
 constexpr int kRplRows = 32;                       // weight rows a group: a lane each
 constexpr int kRplKS = 1024;                       // bytes of K a stage
 constexpr int kRplSlots = 4;                       // ring slots, four consumer warps each
@@ -53,8 +57,15 @@ struct RplCfg {
     static constexpr int kX = kPlanes * R * kRplKS;             // [plane][4 tiles][R][256]
     static constexpr int kXD = R * (kRplKS / Q8_QK) * 4;        // [R][32] f32
     static constexpr int kStage = (kW + kS + kX + kXD + 1023) / 1024 * 1024;
-    static constexpr int kPsum = kRplWarps * kRplRows * R * 4;  // [warp][lane][R]
-    static constexpr size_t kSmem = size_t(kRplSlots) * kStage + kPsum + 2 * kRplSlots * 8 + 1024;
+    // The row group's partial sums are added by a combining warp through two
+    // buffers where that pays (one-word 8 rows: 69.8 against 71.9 us a layer
+    // of the four d = 4096 projections), else by the consumer warps between
+    // two named barriers (4 rows: 56.5 against 57.6 us).
+    static constexpr bool kComb = MODE == 1 && R >= 8;
+    static constexpr int kThreads = 32 * (kRplWarps + 1 + (kComb ? 1 : 0));
+    static constexpr int kPsum = kRplWarps * R * kRplRows * 4;  // one buffer: [warp][R][lane]
+    static constexpr int kBufs = kComb ? 2 : 1;
+    static constexpr size_t kSmem = size_t(kRplSlots) * kStage + kBufs * kPsum + (2 * kRplSlots + 4) * 8 + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
@@ -85,7 +96,7 @@ __device__ __forceinline__ void rpl_tma2d_ef(void* dst, const CUtensorMap* map, 
 }
 
 template <int MODE, int R>
-__global__ void __launch_bounds__(kRplThreads, 1)
+__global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
     gemv_rpl_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                     const __grid_constant__ CUtensorMap tm_xh,
                     const __grid_constant__ CUtensorMap tm_xl, const __grid_constant__ CUtensorMap tm_xd,
@@ -97,8 +108,10 @@ __global__ void __launch_bounds__(kRplThreads, 1)
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* psum = reinterpret_cast<float*>(smem + size_t(kRplSlots) * C::kStage);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kRplSlots) * C::kStage + C::kPsum);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kRplSlots) * C::kStage + C::kBufs * C::kPsum);
     uint64_t* empty = full + kRplSlots;
+    uint64_t* pfull = empty + kRplSlots;   // [2] a row group's partial sums written (kComb)
+    uint64_t* pempty = pfull + 2;          // [2] and added up (kComb)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
@@ -116,6 +129,10 @@ __global__ void __launch_bounds__(kRplThreads, 1)
         for (int i = 0; i < kRplSlots; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 4);   // the slot's four warps
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&pfull[i], kRplWarps);   // lane 0 of each consumer warp
+            mbar_init(&pempty[i], 1);          // lane 0 of the combining warp
         }
         fence_barrier_init();
     }
@@ -168,8 +185,38 @@ __global__ void __launch_bounds__(kRplThreads, 1)
         return;
     }
 
+    if (C::kComb && warp == kRplWarps + 1) {
+        // ------------------------------------------------- combining warp
+        // lane l adds row l's partial sums of the 16 warps in warp order
+        pdl_wait();   // y belongs to the previous kernel until here
+        bool okc = true;
+        for (int g = 0; g < ngroups; ++g) {
+            const int b = g & 1;
+            const int64_t rg0 = r0 + int64_t(g) * kRplRows;
+            const int nr = int(min64(kRplRows, r1 - rg0));
+            if (okc) okc = mbar_wait(&pfull[b], uint32_t((g >> 1) & 1), p.err);
+            if (okc && lane < nr) {
+                // all R sums at once: every load is issued before the adds
+                const float* ps = psum + b * (C::kPsum / 4);
+                float sum[R];
+#pragma unroll
+                for (int m = 0; m < R; ++m) sum[m] = ps[m * kRplRows + lane];
+#pragma unroll
+                for (int w = 1; w < kRplWarps; ++w)
+#pragma unroll
+                    for (int m = 0; m < R; ++m) sum[m] += ps[(w * R + m) * kRplRows + lane];
+#pragma unroll
+                for (int m = 0; m < R; ++m)
+                    if (m < rows) reinterpret_cast<float*>(p.y)[m * N + rg0 + lane] = sum[m];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pempty[b]);
+        }
+        return;
+    }
+
     // ---------------------------------------------------------------- consumers
-    pdl_wait();   // y belongs to the previous kernel until here
+    if constexpr (!C::kComb) pdl_wait();   // y belongs to the previous kernel until here
     const int slot = warp >> 2, qw = warp & 3;   // this warp's slot and quarter of a stage
     bool ok = true;
     for (int g = 0; g < ngroups; ++g) {
@@ -223,20 +270,32 @@ __global__ void __launch_bounds__(kRplThreads, 1)
             __syncwarp();
             if (lane == 0 && ok) mbar_arrive(&empty[slot]);
         }
-        // the row group's sums: each warp's into shared memory, then per (row,
-        // activation row) the 16 warps' in warp order
+        if constexpr (C::kComb) {
+            // the row group's sums to the combining warp, through one of two
+            // buffers (free again once it has added the group before last)
+            const int b = g & 1;
+            if (ok && g >= 2) ok = mbar_wait(&pempty[b], uint32_t(((g >> 1) - 1) & 1), p.err);
+            float* ps = psum + b * (C::kPsum / 4);
 #pragma unroll
-        for (int m = 0; m < R; ++m) psum[(warp * kRplRows + lane) * R + m] = acc[m];
-        consumer_bar<kRplWarps * 32>();
-        if (ok && tid < kRplRows * R) {
-            const int l = tid % kRplRows, m = tid / kRplRows;
-            if (l < nr && m < rows) {
-                float sum = psum[l * R + m];
-                for (int w = 1; w < kRplWarps; ++w) sum += psum[(w * kRplRows + l) * R + m];
-                reinterpret_cast<float*>(p.y)[m * N + rg0 + l] = sum;
+            for (int m = 0; m < R; ++m) ps[(warp * R + m) * kRplRows + lane] = acc[m];
+            __syncwarp();   // the warp's writes before lane 0's release
+            if (lane == 0) mbar_arrive(&pfull[b]);
+        } else {
+            // the row group's sums into shared memory; then thread (m, l) adds
+            // row l's sums of activation row m over the 16 warps in warp order
+#pragma unroll
+            for (int m = 0; m < R; ++m) psum[(warp * R + m) * kRplRows + lane] = acc[m];
+            consumer_bar<kRplWarps * 32>();
+            if (ok && tid < kRplRows * R) {
+                const int l = tid % kRplRows, m = tid / kRplRows;
+                if (l < nr && m < rows) {
+                    float sum = psum[m * kRplRows + l];
+                    for (int w = 1; w < kRplWarps; ++w) sum += psum[(w * R + m) * kRplRows + l];
+                    reinterpret_cast<float*>(p.y)[m * N + rg0 + l] = sum;
+                }
             }
+            consumer_bar<kRplWarps * 32>();
         }
-        consumer_bar<kRplWarps * 32>();
     }
 }
 
@@ -277,7 +336,7 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attrs[2];
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kRplThreads);
+    cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = ctx.stream;
     cfg.numAttrs = pdl_attrs(ctx, attrs);
