@@ -1288,6 +1288,21 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
               sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 3-D tiled tensor map for the batched kernel of gemv_rpl.cuh: dims[0] is
+// contiguous, strides[] are the byte strides of dims 1 and 2 (in any order in
+// memory, so one box can gather the 128-byte chunks of a tile of rows).
+bool make_map3(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t dims[3],
+               const uint64_t strides[2], const uint32_t box[3], CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t st[2] = {strides[0], strides[1]};
+    const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void*>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Clusters of `ks` CTAs of this kernel that fit on the device at once.
 template <int MODE, int TT, int KIND>
 static int active_clusters(int ks, const LaunchCtx& ctx) {

@@ -11,13 +11,16 @@
 // reduction is left in the stream.
 //
 // A stage covers 32 weight rows x 1024 values of K:
-//   - the weights as eight 2-D TMA tiles of 32 rows x 128 bytes (128-byte
-//     swizzle, so the 16-byte loads of 8 consecutive lanes hit distinct bank
-//     groups);
+//   - the weights as eight tiles of 32 rows x 128 bytes, gathered by one 3-D
+//     TMA box (128-byte swizzle, so the 16-byte loads of 8 consecutive lanes
+//     hit distinct bank groups);
 //   - the rows' block scales, 32 rows x 64 bytes (64-byte swizzle, same
 //     reason);
-//   - the activation rows' codes (tiles of R rows x 256 bytes a plane) and
-//     block scales (R rows x 32).
+//   - the activation rows' codes (four tiles of R rows x 256 bytes a plane, one
+//     3-D box) and block scales (R rows x 32).
+// So a stage takes 4 TMA instructions (5 two-word): the producer's issue rate,
+// which shares the memory-instruction queue with the consumers' shared-memory
+// loads, kept up with HBM only once the eight weight tiles were one box.
 // Weights and scales are issued before the wait on the previous kernel, with
 // an evict-first L2 hint (read once per launch); activations after it.  A ring
 // of four stages; the 16 consumer warps are four per slot, and warp (slot,
@@ -43,6 +46,8 @@ namespace q8 {
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
               CUtensorMapSwizzle sw);
+bool make_map3(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t dims[3],
+               const uint64_t strides[2], const uint32_t box[3], CUtensorMapSwizzle sw);
 
 constexpr int kRplWarps = 16;                      // consumer warps
 constexpr int kRplRows = 32;                       // weight rows a group: a lane each
@@ -83,6 +88,23 @@ __device__ __forceinline__ void rpl_tma2d(void* dst, const CUtensorMap* map, int
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void rpl_tma3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void rpl_tma3d_ef(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                             uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
 
@@ -146,12 +168,9 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
             auto acts = [&](int64_t t) {
                 const int j = int(t % nsl), slot = int(t % kRplSlots);
                 unsigned char* st = smem + size_t(slot) * C::kStage;
-                for (int k = 0; k < 4; ++k) {
-                    rpl_tma2d(st + C::kW + C::kS + k * R * 256, &tm_xh, j * kRplKS + k * 256, 0, &full[slot]);
-                    if constexpr (MODE == 2)
-                        rpl_tma2d(st + C::kW + C::kS + (4 + k) * R * 256, &tm_xl, j * kRplKS + k * 256, 0,
-                                  &full[slot]);
-                }
+                // [4 chunks][R rows][256 bytes] a plane, one box each
+                rpl_tma3d(st + C::kW + C::kS, &tm_xh, 0, 0, j * 4, &full[slot]);
+                if constexpr (MODE == 2) rpl_tma3d(st + C::kW + C::kS + 4 * R * 256, &tm_xl, 0, 0, j * 4, &full[slot]);
                 rpl_tma2d(st + C::kW + C::kS + C::kX, &tm_xd, j * (kRplKS / Q8_QK), 0, &full[slot]);
             };
             const int64_t npre = nst < kRplSlots ? nst : kRplSlots;
@@ -165,8 +184,8 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
                 const int rg0 = int(r0 + int64_t(g) * kRplRows);
                 mbar_arrive_expect_tx(&full[slot], kTx);
                 unsigned char* st = smem + size_t(slot) * C::kStage;
-                for (int k = 0; k < 8; ++k)
-                    rpl_tma2d_ef(st + k * (kRplRows * 128), &tm_w, j * kRplKS + k * 128, rg0, &full[slot], pol);
+                // [8 chunks][32 rows][128 bytes] in one box
+                rpl_tma3d_ef(st, &tm_w, 0, rg0, j * 8, &full[slot], pol);
                 rpl_tma2d_ef(st + C::kW, &tm_s, j * (kRplKS / 16), rg0, &full[slot], pol);
                 if (t == npre - 1) {
                     // the first stages' weights are on their way: the
@@ -308,14 +327,20 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     if (!rpl_fits(a) || a.rows > R) return cudaErrorInvalidValue;
     alignas(64) CUtensorMap tw, ts, txh, txl, txd;
     const int8_t* xh = static_cast<const int8_t*>(a.act);
+    // weights as (byte in a 128-byte chunk, row, chunk): a box of 8 chunks of
+    // 32 rows lands as eight [32][128] tiles
+    const uint64_t wd[3] = {128, uint64_t(a.N), uint64_t(a.K / 128)}, ws[2] = {uint64_t(a.K), 128};
+    const uint32_t wb[3] = {128, kRplRows, kRplKS / 128};
+    // activation codes as (byte in a 256-byte chunk, row, chunk)
+    const uint64_t xdims[3] = {256, uint64_t(a.rows), uint64_t(a.K / 256)}, xs[2] = {uint64_t(a.K), 256};
+    const uint32_t xb[3] = {256, uint32_t(R), kRplKS / 256};
     const bool ok =
-        make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q, a.K, a.N, a.K, 128, kRplRows,
-                 CU_TENSOR_MAP_SWIZZLE_128B) &&
+        make_map3(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q, wd, ws, wb, CU_TENSOR_MAP_SWIZZLE_128B) &&
         make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.s, a.K / 16, a.N, a.K / 16, kRplKS / 16, kRplRows,
                  CU_TENSOR_MAP_SWIZZLE_64B) &&
-        make_map(&txh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, a.K, a.rows, a.K, 256, R, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-        make_map(&txl, CU_TENSOR_MAP_DATA_TYPE_UINT8, MODE == 2 ? xh + a.plane : xh, a.K, a.rows, a.K, 256, R,
-                 CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        make_map3(&txh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, xdims, xs, xb, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        make_map3(&txl, CU_TENSOR_MAP_DATA_TYPE_UINT8, MODE == 2 ? xh + a.plane : xh, xdims, xs, xb,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) &&
         make_map(&txd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.xd, a.K / Q8_QK, a.rows, (a.K / Q8_QK) * 4,
                  kRplKS / Q8_QK, R, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return cudaErrorInvalidValue;
