@@ -339,6 +339,20 @@ __device__ __forceinline__ DF scaled_pair(float f, long long V) {
 // --------------------------------------------------------------- geometry
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// The KV-row epilogue (decode and row-per-lane kernels): output column n of
+// row m, when it falls in the K or V slice, also goes to cache row s_pos[m]
+// of that row's sequence (-1: none).
+__device__ __forceinline__ void kv_store(const GemvParams& p, const int* s_pos, int m, int64_t n,
+                                         float v) {
+    const int ps = s_pos[m];
+    if (ps < 0) return;
+    const int64_t d = n - p.kv_col;
+    if (d < 0 || d >= 2 * p.kv_dim) return;
+    float* cache = d < p.kv_dim ? p.k_cache : p.v_cache;
+    const int64_t dd = d < p.kv_dim ? d : d - p.kv_dim;
+    cache[(int64_t(m) * p.n_pos + ps) * p.kv_dim + dd] = v;
+}
 __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
 struct Geo {

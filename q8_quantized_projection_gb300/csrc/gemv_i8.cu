@@ -1,7 +1,8 @@
 // gemv_i8.cu -- instantiations of the CUDA-core projection for activation
-// mode 1: the decode kernel (gemv_row.cuh) for 1-2 rows, the row-per-lane
-// kernel (gemv_rpl.cuh) for 3-8 rows of a plain projection with K % 1024 == 0
-// (else the decode kernel), the slice-major kernel (gemv.cuh) for more.  One
+// mode 1: the row-per-lane kernel (gemv_rpl.cuh) for 1-8 rows with K % 1024 ==
+// 0 (plain projections and fused decode steps without the KV-row epilogue),
+// else the decode kernel (gemv_row.cuh: the LM head's arg-max, the KV-row
+// epilogue, other K); the slice-major kernel (gemv.cuh) for more rows.  One
 // file per mode so the build runs in parallel.
 #include "gemv_row.cuh"
 #include "gemv_rpl.cuh"
@@ -10,13 +11,15 @@ namespace q8 {
 
 template <bool ARGMAX>
 static cudaError_t dispatch_rows(const GemvArgs& a, const LaunchCtx& ctx) {
-    if (a.rows <= 1 && row_kernel_fits<1, 1>(a.K)) return launch_gemv_row_t<1, 1, ARGMAX>(a, ctx);
-    if (a.rows <= 2 && row_kernel_fits<1, 2>(a.K)) return launch_gemv_row_t<1, 2, ARGMAX>(a, ctx);
     if constexpr (!ARGMAX) {
         // a weight row a lane (plain projections, K % 1024 == 0)
+        if (a.rows <= 1 && rpl_fits(a)) return launch_gemv_rpl_t<1, 1>(a, ctx);
+        if (a.rows <= 2 && rpl_fits(a)) return launch_gemv_rpl_t<1, 2>(a, ctx);
         if (a.rows <= 4 && rpl_fits(a)) return launch_gemv_rpl_t<1, 4>(a, ctx);
         if (a.rows <= 8 && rpl_fits(a)) return launch_gemv_rpl_t<1, 8>(a, ctx);
     }
+    if (a.rows <= 1 && row_kernel_fits<1, 1>(a.K)) return launch_gemv_row_t<1, 1, ARGMAX>(a, ctx);
+    if (a.rows <= 2 && row_kernel_fits<1, 2>(a.K)) return launch_gemv_row_t<1, 2, ARGMAX>(a, ctx);
     if (a.rows <= 4 && row_kernel_fits<1, 4>(a.K)) return launch_gemv_row_t<1, 4, ARGMAX>(a, ctx);
     if (a.rows <= 8 && row_kernel_fits<1, 8>(a.K)) return launch_gemv_row_t<1, 8, ARGMAX>(a, ctx);
     if (a.rows <= 4) return launch_gemv_t<1, 4, ARGMAX>(a, ctx);
@@ -29,6 +32,13 @@ cudaError_t launch_gemv_mode1(const GemvArgs& a, const LaunchCtx& ctx) {
 }
 
 cudaError_t launch_gemv_fused_mode1(const GemvArgs& a, const LaunchCtx& ctx) {
+    if (rpl_fits_fused(a)) {
+        // a weight row a lane, the produced row in shared memory
+        if (a.k_cache) return launch_gemv_rpl_t<1, 1, true, kProdPlain, true>(a, ctx);
+        if (a.prod == kProdResidual) return launch_gemv_rpl_t<1, 1, true, kProdResidual>(a, ctx);
+        if (a.prod == kProdSwiglu) return launch_gemv_rpl_t<1, 1, true, kProdSwiglu>(a, ctx);
+        return launch_gemv_rpl_t<1, 1, true>(a, ctx);
+    }
     if (a.k_cache) return launch_gemv_row_t<1, 1, false, true, kProdPlain, true>(a, ctx);
     if (a.prod == kProdResidual) return launch_gemv_row_t<1, 1, false, true, kProdResidual>(a, ctx);
     if (a.prod == kProdSwiglu) return launch_gemv_row_t<1, 1, false, true, kProdSwiglu>(a, ctx);

@@ -1,8 +1,9 @@
 // gemv_i8x2.cu -- instantiations of the CUDA-core projection for activation
-// mode 2: the decode kernel (gemv_row.cuh) for 1 row, the row-per-lane kernel
-// (gemv_rpl.cuh) for 2-4 rows of a plain projection with K % 1024 == 0 (else
-// the decode kernel), the slice-major kernel (gemv.cuh) for more.  One file
-// per mode so the build runs in parallel.
+// mode 2: the row-per-lane kernel (gemv_rpl.cuh) for 1-4 rows with K % 1024 ==
+// 0 (plain projections and fused decode steps without the KV-row epilogue),
+// else the decode kernel (gemv_row.cuh: the LM head's arg-max, the KV-row
+// epilogue, other K); the slice-major kernel (gemv.cuh) for more rows.  One
+// file per mode so the build runs in parallel.
 #include "gemv_row.cuh"
 #include "gemv_rpl.cuh"
 
@@ -10,12 +11,13 @@ namespace q8 {
 
 template <bool ARGMAX>
 static cudaError_t dispatch_rows(const GemvArgs& a, const LaunchCtx& ctx) {
-    if (a.rows <= 1 && row_kernel_fits<2, 1>(a.K)) return launch_gemv_row_t<2, 1, ARGMAX>(a, ctx);
     if constexpr (!ARGMAX) {
         // a weight row a lane (plain projections, K % 1024 == 0)
+        if (a.rows <= 1 && rpl_fits(a)) return launch_gemv_rpl_t<2, 1>(a, ctx);
         if (a.rows <= 2 && rpl_fits(a)) return launch_gemv_rpl_t<2, 2>(a, ctx);
         if (a.rows <= 4 && rpl_fits(a)) return launch_gemv_rpl_t<2, 4>(a, ctx);
     }
+    if (a.rows <= 1 && row_kernel_fits<2, 1>(a.K)) return launch_gemv_row_t<2, 1, ARGMAX>(a, ctx);
     if (a.rows <= 2 && row_kernel_fits<2, 2>(a.K)) return launch_gemv_row_t<2, 2, ARGMAX>(a, ctx);
     if (a.rows <= 4 && row_kernel_fits<2, 4>(a.K)) return launch_gemv_row_t<2, 4, ARGMAX>(a, ctx);
     if (a.rows <= 4) return launch_gemv_t<2, 4, ARGMAX>(a, ctx);
@@ -28,6 +30,13 @@ cudaError_t launch_gemv_mode2(const GemvArgs& a, const LaunchCtx& ctx) {
 }
 
 cudaError_t launch_gemv_fused_mode2(const GemvArgs& a, const LaunchCtx& ctx) {
+    if (rpl_fits_fused(a)) {
+        // a weight row a lane, the produced row in shared memory
+        if (a.k_cache) return launch_gemv_rpl_t<2, 1, true, kProdPlain, true>(a, ctx);
+        if (a.prod == kProdResidual) return launch_gemv_rpl_t<2, 1, true, kProdResidual>(a, ctx);
+        if (a.prod == kProdSwiglu) return launch_gemv_rpl_t<2, 1, true, kProdSwiglu>(a, ctx);
+        return launch_gemv_rpl_t<2, 1, true>(a, ctx);
+    }
     if (a.k_cache) return launch_gemv_row_t<2, 1, false, true, kProdPlain, true>(a, ctx);
     if (a.prod == kProdResidual) return launch_gemv_row_t<2, 1, false, true, kProdResidual>(a, ctx);
     if (a.prod == kProdSwiglu) return launch_gemv_row_t<2, 1, false, true, kProdSwiglu>(a, ctx);

@@ -306,19 +306,6 @@ __device__ __forceinline__ void load_x4(const float* x, const float* h, const fl
     }
 }
 
-// The KV-row epilogue: output column n of row m, when it falls in the K or V
-// slice, also goes to cache row s_pos[m] of that row's sequence (-1: none).
-__device__ __forceinline__ void kv_store(const GemvParams& p, const int* s_pos, int m, int64_t n,
-                                         float v) {
-    const int ps = s_pos[m];
-    if (ps < 0) return;
-    const int64_t d = n - p.kv_col;
-    if (d < 0 || d >= 2 * p.kv_dim) return;
-    float* cache = d < p.kv_dim ? p.k_cache : p.v_cache;
-    const int64_t dd = d < p.kv_dim ? d : d - p.kv_dim;
-    cache[(int64_t(m) * p.n_pos + ps) * p.kv_dim + dd] = v;
-}
-
 // PROD (fused producer only): kProdPlain (RMSNorm of h), kProdResidual (the
 // residual added before the norm) or kProdSwiglu (the SwiGLU of the fused
 // gate+up row h); each a separate instantiation, so the plain fused kernel

@@ -40,6 +40,7 @@
 #include <cuda.h>
 
 #include "gemv.cuh"
+#include "rmsnorm.cuh"
 
 namespace q8 {
 
@@ -54,13 +55,19 @@ constexpr int kRplRows = 32;                       // weight rows a group: a lan
 constexpr int kRplKS = 1024;                       // bytes of K a stage
 constexpr int kRplSlots = 4;                       // ring slots, four consumer warps each
 
-template <int MODE, int R>
+// FUSE: one activation row, produced (RMSNorm -> quant, or by PROD the
+// residual added before the norm, or the SwiGLU of a gate+up row) by the
+// consumer warps into shared memory for the whole launch; the stages then
+// carry weights and scales only.
+template <int MODE, int R, bool FUSE = false>
 struct RplCfg {
     static constexpr int kPlanes = MODE == 2 ? 2 : 1;
     static constexpr int kW = kRplRows * kRplKS;                // 8 tiles of [32][128]
     static constexpr int kS = kRplRows * (kRplKS / Q8_QK) * 2;  // [32][64] bytes of f16 scales
-    static constexpr int kX = kPlanes * R * kRplKS;             // [plane][4 tiles][R][256]
-    static constexpr int kXD = R * (kRplKS / Q8_QK) * 4;        // [R][32] f32
+    static constexpr int kX = FUSE ? 0 : kPlanes * R * kRplKS;  // [plane][4 tiles][R][256]
+    static constexpr int kXD = FUSE ? 0 : R * (kRplKS / Q8_QK) * 4;   // [R][32] f32
+    // the produced row: [plane][kFusedMaxK] codes, then kFusedMaxK / 32 scales
+    static constexpr int kAct = FUSE ? int(2 * kFusedMaxK + (kFusedMaxK / Q8_QK) * 4) : 0;
     static constexpr int kStage = (kW + kS + kX + kXD + 1023) / 1024 * 1024;
     // The row group's partial sums are added by a combining warp through two
     // buffers where that pays (one-word 8 rows: 69.8 against 71.9 us a layer
@@ -70,17 +77,29 @@ struct RplCfg {
     static constexpr int kThreads = 32 * (kRplWarps + 1 + (kComb ? 1 : 0));
     static constexpr int kPsum = kRplWarps * R * kRplRows * 4;  // one buffer: [warp][R][lane]
     static constexpr int kBufs = kComb ? 2 : 1;
-    static constexpr size_t kSmem = size_t(kRplSlots) * kStage + kBufs * kPsum + (2 * kRplSlots + 4) * 8 + 1024;
+    static constexpr size_t kSmem =
+        size_t(kRplSlots) * kStage + kBufs * kPsum + (2 * kRplSlots + 4) * 8 + kAct + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory");
+    static_assert(!FUSE || (R == 1 && !kComb), "fused producer: one row");
 };
 
-// A plain projection of 2 or more rows in whole stages, with the 16-byte
-// alignment the tensor maps need; anything else takes the decode kernel.
+inline bool rpl_al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A plain projection in whole stages, with the 16-byte alignment the tensor
+// maps need; anything else takes the decode kernel.
 inline bool rpl_fits(const GemvArgs& a) {
-    const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    return a.rows >= 2 && a.K >= kRplKS && a.K % kRplKS == 0 && a.N <= (int64_t(1) << 31) && a.y &&
+    const auto al16 = rpl_al16;
+    return a.rows >= 1 && a.K >= kRplKS && a.K % kRplKS == 0 && a.N <= (int64_t(1) << 31) && a.y &&
            !a.out_f64 && !a.tok && !a.h && !a.k_cache && al16(a.q) && al16(a.s) && al16(a.act) && al16(a.xd) &&
            a.plane % 16 == 0;
+}
+
+// A fused decode step (one row, the producer in the kernel; with or without
+// the KV-row epilogue) in whole stages, with its row in shared memory.
+inline bool rpl_fits_fused(const GemvArgs& a) {
+    return a.rows == 1 && a.h && a.K >= kRplKS && a.K % kRplKS == 0 && a.K <= kFusedMaxK &&
+           a.N <= (int64_t(1) << 31) && a.y && !a.out_f64 && !a.tok && rpl_al16(a.q) && rpl_al16(a.s) &&
+           rpl_al16(a.h);
 }
 
 __device__ __forceinline__ void rpl_tma2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -117,14 +136,22 @@ __device__ __forceinline__ void rpl_tma2d_ef(void* dst, const CUtensorMap* map, 
         : "memory");
 }
 
-template <int MODE, int R>
-__global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
+template <int MODE, int R, bool FUSE = false, int PROD = kProdPlain, bool KV = false>
+__global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
     gemv_rpl_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                     const __grid_constant__ CUtensorMap tm_xh,
                     const __grid_constant__ CUtensorMap tm_xl, const __grid_constant__ CUtensorMap tm_xd,
                     const GemvParams p) {
     static_assert(MODE == 1 || MODE == 2, "int8 activation codes");
-    using C = RplCfg<MODE, R>;
+    static_assert(PROD == kProdPlain || FUSE, "producer kinds belong to the fused producer");
+    static_assert(!KV || (FUSE && PROD == kProdPlain), "the KV-row epilogue: fused plain decode step");
+    static_assert(!FUSE || kRplWarps * 32 == kProdThreads, "fused producer needs kProdThreads consumers");
+    using C = RplCfg<MODE, R, FUSE>;
+    constexpr bool RES = PROD == kProdResidual;
+    constexpr bool NORM = PROD != kProdSwiglu;
+    __shared__ float2 s_pair[kProdWarps];
+    __shared__ float s_rf;
+    __shared__ int s_pos[1];   // KV-row epilogue: the row's cache position
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled weight tiles
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -134,6 +161,8 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
     uint64_t* empty = full + kRplSlots;
     uint64_t* pfull = empty + kRplSlots;   // [2] a row group's partial sums written (kComb)
     uint64_t* pempty = pfull + 2;          // [2] and added up (kComb)
+    unsigned char* sact = reinterpret_cast<unsigned char*>(pempty + 2);   // FUSE: the produced row
+    float* sxd = reinterpret_cast<float*>(sact + 2 * kFusedMaxK);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
@@ -165,6 +194,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             constexpr uint32_t kTx = uint32_t(C::kW + C::kS + C::kX + C::kXD);   // whole tiles, rows past the end zero
+            // (fused: no activation copies; the weights never wait on the previous kernel)
             auto acts = [&](int64_t t) {
                 const int j = int(t % nsl), slot = int(t % kRplSlots);
                 unsigned char* st = smem + size_t(slot) * C::kStage;
@@ -187,13 +217,15 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
                 // [8 chunks][32 rows][128 bytes] in one box
                 rpl_tma3d_ef(st, &tm_w, 0, rg0, j * 8, &full[slot], pol);
                 rpl_tma2d_ef(st + C::kW, &tm_s, j * (kRplKS / 16), rg0, &full[slot], pol);
-                if (t == npre - 1) {
-                    // the first stages' weights are on their way: the
-                    // activations belong to the previous kernel until here
-                    pdl_wait();
-                    for (int64_t u = 0; u <= t; ++u) acts(u);
-                } else if (t >= npre) {
-                    acts(t);
+                if constexpr (!FUSE) {
+                    if (t == npre - 1) {
+                        // the first stages' weights are on their way: the
+                        // activations belong to the previous kernel until here
+                        pdl_wait();
+                        for (int64_t u = 0; u <= t; ++u) acts(u);
+                    } else if (t >= npre) {
+                        acts(t);
+                    }
                 }
                 ++issued;
             }
@@ -235,7 +267,31 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
     }
 
     // ---------------------------------------------------------------- consumers
-    if constexpr (!C::kComb) pdl_wait();   // y belongs to the previous kernel until here
+    if constexpr (!C::kComb) pdl_wait();   // h, y belong to the previous kernel until here
+    if constexpr (KV) {
+        if (tid == 0) {
+            // the position belongs to the previous kernel until
+            // griddepcontrol.wait; one outside the cache writes nothing and
+            // is reported
+            int ps = p.pos[0];
+            if (ps < 0 || ps >= p.n_pos) {
+                atomicExch(p.err, Q8_DEVERR_POSITION);
+                ps = -1;
+            }
+            s_pos[0] = ps;
+        }
+    }
+    if constexpr (FUSE) {
+        // the producer, fused: RMSNorm -> quant of the one activation row into
+        // shared memory, by the same code and thread layout as act_quant, while
+        // the producer warp already streams weights; CTA 0 writes the updated
+        // residual stream, when asked
+        const float* const res = RES ? p.res : nullptr;
+        float* const s_out = RES && blockIdx.x == 0 ? p.s_out : nullptr;
+        row_produce<MODE, NORM, PROD>(p.h, res, s_out, p.gain, p.eps, K, tid, 1, s_pair, &s_rf, sact, K, sxd);
+        consumer_bar<kRplWarps * 32>();
+    }
+    const uint32_t sact_a = smem_u32(sact), sxd_a = smem_u32(sxd);
     const int slot = warp >> 2, qw = warp & 3;   // this warp's slot and quarter of a stage
     bool ok = true;
     for (int g = 0; g < ngroups; ++g) {
@@ -251,8 +307,12 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok && lane < nr) {
                 const uint32_t st = smem_u32(smem + size_t(slot) * C::kStage);
-                const uint32_t xa = st + uint32_t(C::kW + C::kS);
-                const uint32_t da = st + uint32_t(C::kW + C::kS + C::kX + qw * 32);
+                // the stage's activation codes and block scales: in the stage,
+                // or (fused) at K offset j * 1024 of the produced row
+                const uint32_t xa = FUSE ? sact_a + uint32_t(j * kRplKS) : st + uint32_t(C::kW + C::kS);
+                const uint32_t da = FUSE ? sxd_a + uint32_t((j * (kRplKS / Q8_QK) + qw * 8) * 4)
+                                         : st + uint32_t(C::kW + C::kS + C::kX + qw * 32);
+                const uint32_t lo = FUSE ? uint32_t(K) : uint32_t(4 * R * 256);   // the lo plane
                 // the lane's row's 8 block scales of this quarter: 16-byte chunk
                 // qw of its 64-byte row, 64-byte swizzle
                 const int4 s8 = lds128(st + uint32_t(C::kW + lane * 64 + ((qw ^ ((lane >> 1) & 3)) << 4)));
@@ -266,8 +326,8 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
                     const int4 w0 = lds128(wr + uint32_t(((c0 ^ (lane & 7)) << 4)));
                     const int4 w1 = lds128(wr + uint32_t((((c0 + 1) ^ (lane & 7)) << 4)));
                     const float sw = half_bits_to_float(uint16_t((b & 1) ? (sh[b >> 1] >> 16) : (sh[b >> 1] & 0xFFFFu)));
-                    // activation tile B / 8 (rows of 256 bytes), block B % 8
-                    const uint32_t xb = xa + uint32_t((B >> 3) * R * 256 + (B & 7) * 32);
+                    // activation tile B / 8 (rows of 256 bytes), block B % 8; fused: block B
+                    const uint32_t xb = FUSE ? xa + uint32_t(B * 32) : xa + uint32_t((B >> 3) * R * 256 + (B & 7) * 32);
 #pragma unroll
                     for (int m = 0; m < R; ++m) {
                         const uint32_t xm = xb + uint32_t(m * 256);
@@ -277,7 +337,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
                             const int isum = dot16_i8(w0, lds128(xm)) + dot16_i8(w1, lds128(xm + 16u));
                             fi = small_int_to_float(isum);   // |isum| < 2^19
                         } else {
-                            const uint32_t xl = xm + uint32_t(4 * R * 256);   // the lo plane
+                            const uint32_t xl = xm + lo;
                             const int isum = dot16_i8x2(w0, lds128(xm), lds128(xl)) +
                                              dot16_i8x2(w1, lds128(xm + 16u), lds128(xl + 16u));
                             fi = float(isum);
@@ -311,6 +371,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
                     float sum = psum[m * kRplRows + l];
                     for (int w = 1; w < kRplWarps; ++w) sum += psum[(w * R + m) * kRplRows + l];
                     reinterpret_cast<float*>(p.y)[m * N + rg0 + l] = sum;
+                    if constexpr (KV) kv_store(p, s_pos, m, rg0 + l, sum);
                 }
             }
             consumer_bar<kRplWarps * 32>();
@@ -318,13 +379,14 @@ __global__ void __launch_bounds__(RplCfg<MODE, R>::kThreads, 1)
     }
 }
 
-template <int MODE, int R>
+template <int MODE, int R, bool FUSE = false, int PROD = kProdPlain, bool KV = false>
 cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
-    using C = RplCfg<MODE, R>;
-    auto kern = gemv_rpl_kernel<MODE, R>;
+    using C = RplCfg<MODE, R, FUSE>;
+    auto kern = gemv_rpl_kernel<MODE, R, FUSE, PROD, KV>;
     static std::atomic<bool> configured[kMaxDevices];
     if (const cudaError_t e = set_smem_once(kern, C::kSmem, ctx.dev, configured); e != cudaSuccess) return e;
-    if (!rpl_fits(a) || a.rows > R) return cudaErrorInvalidValue;
+    if (FUSE ? !rpl_fits_fused(a) : (!rpl_fits(a) || a.rows > R)) return cudaErrorInvalidValue;
+    if (KV != (a.k_cache != nullptr)) return cudaErrorInvalidValue;
     alignas(64) CUtensorMap tw, ts, txh, txl, txd;
     const int8_t* xh = static_cast<const int8_t*>(a.act);
     // weights as (byte in a 128-byte chunk, row, chunk): a box of 8 chunks of
@@ -334,15 +396,18 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     // activation codes as (byte in a 256-byte chunk, row, chunk)
     const uint64_t xdims[3] = {256, uint64_t(a.rows), uint64_t(a.K / 256)}, xs[2] = {uint64_t(a.K), 256};
     const uint32_t xb[3] = {256, uint32_t(R), kRplKS / 256};
-    const bool ok =
+    const bool okw =
         make_map3(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q, wd, ws, wb, CU_TENSOR_MAP_SWIZZLE_128B) &&
         make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.s, a.K / 16, a.N, a.K / 16, kRplKS / 16, kRplRows,
-                 CU_TENSOR_MAP_SWIZZLE_64B) &&
-        make_map3(&txh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, xdims, xs, xb, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                 CU_TENSOR_MAP_SWIZZLE_64B);
+    // fused: no activation copies (the unused maps repeat the weights')
+    if (FUSE) txh = txl = txd = tw;
+    const bool ok = okw && (FUSE ||
+        (make_map3(&txh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, xdims, xs, xb, CU_TENSOR_MAP_SWIZZLE_NONE) &&
         make_map3(&txl, CU_TENSOR_MAP_DATA_TYPE_UINT8, MODE == 2 ? xh + a.plane : xh, xdims, xs, xb,
                   CU_TENSOR_MAP_SWIZZLE_NONE) &&
         make_map(&txd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.xd, a.K / Q8_QK, a.rows, (a.K / Q8_QK) * 4,
-                 kRplKS / Q8_QK, R, CU_TENSOR_MAP_SWIZZLE_NONE);
+                 kRplKS / Q8_QK, R, CU_TENSOR_MAP_SWIZZLE_NONE)));
     if (!ok) return cudaErrorInvalidValue;
     GemvParams p{};
     p.q = a.q;
@@ -355,6 +420,17 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     p.rows = a.rows;
     p.y = a.y;
     p.err = ctx.dev_err;
+    p.h = a.h;
+    p.res = a.res;
+    p.s_out = a.s_out;
+    p.gain = a.gain;
+    p.eps = a.eps;
+    p.pos = a.pos;
+    p.kv_col = a.kv_col;
+    p.kv_dim = a.kv_dim;
+    p.n_pos = a.n_pos;
+    p.k_cache = a.k_cache;
+    p.v_cache = a.v_cache;
     int grid = ctx.num_sms;
     if (grid > kMaxGrid) grid = kMaxGrid;
     if (int64_t(grid) > (a.N + kRplRows - 1) / kRplRows) grid = int((a.N + kRplRows - 1) / kRplRows);
