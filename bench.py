@@ -247,10 +247,16 @@ def run_reference(args, world, rank):
 
 # --------------------------------------------------------------- our arm
 
-# The sources the decode projection kernel is compiled from (its headers and
-# its three instantiation units); the C-ABI layer and the other kernels are not.
-DECODE_KERNEL_SOURCES = ("common.cuh", "launch.h", "gemv.cuh", "gemv_row.cuh", "rmsnorm.cuh", "gemv_f32.cu",
-                         "gemv_i8.cu", "gemv_i8x2.cu")
+# The sources the fused decode kernels are compiled from (the decode kernel
+# of the f32 mode and the row-per-lane kernel of the int8 modes, their headers
+# and three instantiation units); the C-ABI layer and the other kernels are not.
+DECODE_KERNEL_SOURCES = ("common.cuh", "launch.h", "gemv.cuh", "gemv_row.cuh", "gemv_rpl.cuh", "rmsnorm.cuh",
+                         "gemv_f32.cu", "gemv_i8.cu", "gemv_i8x2.cu")
+
+# The kernel each mode's fused decode launch runs (the layer's K are all
+# multiples of 1024, which the int8 row-per-lane kernel takes)
+FUSED_KERNEL = {"f32": "gemv_row_kernel<0,1,0,1,0,0,0,0>", "i8": "gemv_rpl_kernel<1,1,1,0,0>",
+                "i8x2": "gemv_rpl_kernel<2,1,1,0,0>"}
 
 
 def kernel_source_hash():
@@ -464,7 +470,6 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = load_peaks()
     dom = max(MODES, key=lambda m: per_mode[m]["ms_per_step"])
     achieved = mode_alg / (per_mode[dom]["ms_per_step"] * 1e-3) / 1e9
-    inst = {"f32": 0, "i8": 1, "i8x2": 2}[dom]
 
     # sub-record: each fused projection replayed alone from graphs of REPS
     # launches, rotating over enough weight copies that each projection's
@@ -493,7 +498,7 @@ def run_ours(args, world, rank, local):
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": committed_traffic(f"fused_{dom}"),
-                "kernel": f"gemv_row_kernel<{inst},1,0,1,0,0,0,0> ({dom} mode, producer fused)",
+                "kernel": f"{FUSED_KERNEL[dom]} ({dom} mode, producer fused)",
                 "peak_source": peak_kind, "launches": 4,
                 "per_launch_us": round(per_mode[dom]["ms_per_step"] * 1e3 / 4, 3),
                 "alg_bytes_per_launch": round(mode_alg / 4),

@@ -40,6 +40,7 @@
 #include <cuda.h>
 
 #include "gemv.cuh"
+#include "gemv_row.cuh"
 #include "rmsnorm.cuh"
 
 namespace q8 {
@@ -59,15 +60,23 @@ constexpr int kRplSlots = 4;                       // ring slots, four consumer 
 // residual added before the norm, or the SwiGLU of a gate+up row) by the
 // consumer warps into shared memory for the whole launch; the stages then
 // carry weights and scales only.
+// MODE 0 (f32 activations, one row): the row is converted once per CTA into
+// shared memory, as 31-bit fixed-point byte planes of each 32-value block
+// relative to the block's binade, with each block's factor 2^(E_b - E) to the
+// row's largest binade E (fused or not).
 template <int MODE, int R, bool FUSE = false>
 struct RplCfg {
+    static constexpr bool kResAct = FUSE || MODE == 0;          // the row resident in shared memory
     static constexpr int kPlanes = MODE == 2 ? 2 : 1;
     static constexpr int kW = kRplRows * kRplKS;                // 8 tiles of [32][128]
     static constexpr int kS = kRplRows * (kRplKS / Q8_QK) * 2;  // [32][64] bytes of f16 scales
-    static constexpr int kX = FUSE ? 0 : kPlanes * R * kRplKS;  // [plane][4 tiles][R][256]
-    static constexpr int kXD = FUSE ? 0 : R * (kRplKS / Q8_QK) * 4;   // [R][32] f32
-    // the produced row: [plane][kFusedMaxK] codes, then kFusedMaxK / 32 scales
-    static constexpr int kAct = FUSE ? int(2 * kFusedMaxK + (kFusedMaxK / Q8_QK) * 4) : 0;
+    static constexpr int kX = kResAct ? 0 : kPlanes * R * kRplKS;        // [plane][4 tiles][R][256]
+    static constexpr int kXD = kResAct ? 0 : R * (kRplKS / Q8_QK) * 4;   // [R][32] f32
+    // the resident row: [plane][kFusedMaxK] codes (int8 modes) or
+    // [kFusedMaxK / 32][128] fixed-point planes (f32), then kFusedMaxK / 32
+    // block scales (int8) or block factors (f32)
+    static constexpr int kActBytes = MODE == 0 ? int(4 * kFusedMaxK) : int(2 * kFusedMaxK);
+    static constexpr int kAct = kResAct ? kActBytes + int(kFusedMaxK / Q8_QK) * 4 : 0;
     static constexpr int kStage = (kW + kS + kX + kXD + 1023) / 1024 * 1024;
     // The row group's partial sums are added by a combining warp through two
     // buffers where that pays (one-word 8 rows: 69.8 against 71.9 us a layer
@@ -75,12 +84,14 @@ struct RplCfg {
     // two named barriers (4 rows: 56.5 against 57.6 us).
     static constexpr bool kComb = MODE == 1 && R >= 8;
     static constexpr int kThreads = 32 * (kRplWarps + 1 + (kComb ? 1 : 0));
-    static constexpr int kPsum = kRplWarps * R * kRplRows * 4;  // one buffer: [warp][R][lane]
+    // one buffer: [warp][R][lane], f32 (int8 modes) or f32 pairs (f32 mode)
+    static constexpr int kPsum = kRplWarps * R * kRplRows * (MODE == 0 ? 8 : 4);
     static constexpr int kBufs = kComb ? 2 : 1;
     static constexpr size_t kSmem =
         size_t(kRplSlots) * kStage + kBufs * kPsum + (2 * kRplSlots + 4) * 8 + kAct + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory");
     static_assert(!FUSE || (R == 1 && !kComb), "fused producer: one row");
+    static_assert(MODE != 0 || R == 1, "f32 mode: one row");
 };
 
 inline bool rpl_al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -89,17 +100,19 @@ inline bool rpl_al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1
 // maps need; anything else takes the decode kernel.
 inline bool rpl_fits(const GemvArgs& a) {
     const auto al16 = rpl_al16;
-    return a.rows >= 1 && a.K >= kRplKS && a.K % kRplKS == 0 && a.N <= (int64_t(1) << 31) && a.y &&
-           !a.out_f64 && !a.tok && !a.h && !a.k_cache && al16(a.q) && al16(a.s) && al16(a.act) && al16(a.xd) &&
-           a.plane % 16 == 0;
+    // f32 mode: one row, resident in shared memory (f64 output allowed)
+    const bool f32ok = a.mode != 0 || (a.rows == 1 && a.K <= kFusedMaxK);
+    return f32ok && a.rows >= 1 && a.K >= kRplKS && a.K % kRplKS == 0 && a.N <= (int64_t(1) << 31) && a.y &&
+           (!a.out_f64 || a.mode == 0) && !a.tok && !a.h && !a.k_cache && al16(a.q) && al16(a.s) &&
+           al16(a.act) && (a.mode == 0 || al16(a.xd)) && a.plane % 16 == 0;
 }
 
 // A fused decode step (one row, the producer in the kernel; with or without
 // the KV-row epilogue) in whole stages, with its row in shared memory.
 inline bool rpl_fits_fused(const GemvArgs& a) {
     return a.rows == 1 && a.h && a.K >= kRplKS && a.K % kRplKS == 0 && a.K <= kFusedMaxK &&
-           a.N <= (int64_t(1) << 31) && a.y && !a.out_f64 && !a.tok && rpl_al16(a.q) && rpl_al16(a.s) &&
-           rpl_al16(a.h);
+           a.N <= (int64_t(1) << 31) && a.y && (!a.out_f64 || a.mode == 0) && !a.tok && rpl_al16(a.q) &&
+           rpl_al16(a.s) && rpl_al16(a.h);
 }
 
 __device__ __forceinline__ void rpl_tma2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -108,6 +121,10 @@ __device__ __forceinline__ void rpl_tma2d(void* dst, const CUtensorMap* map, int
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+__device__ __forceinline__ void rpl_sts64(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
 __device__ __forceinline__ void rpl_tma3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
@@ -142,7 +159,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_xh,
                     const __grid_constant__ CUtensorMap tm_xl, const __grid_constant__ CUtensorMap tm_xd,
                     const GemvParams p) {
-    static_assert(MODE == 1 || MODE == 2, "int8 activation codes");
+    static_assert(MODE >= 0 && MODE <= 2, "activation mode");
     static_assert(PROD == kProdPlain || FUSE, "producer kinds belong to the fused producer");
     static_assert(!KV || (FUSE && PROD == kProdPlain), "the KV-row epilogue: fused plain decode step");
     static_assert(!FUSE || kRplWarps * 32 == kProdThreads, "fused producer needs kProdThreads consumers");
@@ -152,6 +169,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
     __shared__ float2 s_pair[kProdWarps];
     __shared__ float s_rf;
     __shared__ int s_pos[1];   // KV-row epilogue: the row's cache position
+    __shared__ int s_emax[kRplWarps + 1];   // f32 mode: the warps' largest block binades, then the row's
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled weight tiles
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -161,8 +179,8 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
     uint64_t* empty = full + kRplSlots;
     uint64_t* pfull = empty + kRplSlots;   // [2] a row group's partial sums written (kComb)
     uint64_t* pempty = pfull + 2;          // [2] and added up (kComb)
-    unsigned char* sact = reinterpret_cast<unsigned char*>(pempty + 2);   // FUSE: the produced row
-    float* sxd = reinterpret_cast<float*>(sact + 2 * kFusedMaxK);
+    unsigned char* sact = reinterpret_cast<unsigned char*>(pempty + 2);   // the resident row
+    float* sxd = reinterpret_cast<float*>(sact + C::kActBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
@@ -194,7 +212,8 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             constexpr uint32_t kTx = uint32_t(C::kW + C::kS + C::kX + C::kXD);   // whole tiles, rows past the end zero
-            // (fused: no activation copies; the weights never wait on the previous kernel)
+            // (a resident row: no activation copies; the weights never wait on
+            // the previous kernel)
             auto acts = [&](int64_t t) {
                 const int j = int(t % nsl), slot = int(t % kRplSlots);
                 unsigned char* st = smem + size_t(slot) * C::kStage;
@@ -217,7 +236,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
                 // [8 chunks][32 rows][128 bytes] in one box
                 rpl_tma3d_ef(st, &tm_w, 0, rg0, j * 8, &full[slot], pol);
                 rpl_tma2d_ef(st + C::kW, &tm_s, j * (kRplKS / 16), rg0, &full[slot], pol);
-                if constexpr (!FUSE) {
+                if constexpr (!C::kResAct) {
                     if (t == npre - 1) {
                         // the first stages' weights are on their way: the
                         // activations belong to the previous kernel until here
@@ -281,7 +300,93 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
             s_pos[0] = ps;
         }
     }
-    if constexpr (FUSE) {
+    if constexpr (MODE == 0) {
+        // f32: x (read, or with the producer fused formed as the producer
+        // forms it: x = (s*rf)*g, s = h or h + r, or the SwiGLU of a gate+up
+        // row) converted into fixed-point planes, four lanes a block (8 values
+        // each, 4 float4 groups of a block per lane pair); CTA 0 writes the
+        // updated residual stream, when asked.  With the norm, the RMS pass
+        // keeps s in the plane area (K floats: the planes' size), and each
+        // block's planes are built in place.
+        const float* const res = RES ? p.res : nullptr;
+        float* const s_out = RES && blockIdx.x == 0 ? p.s_out : nullptr;
+        constexpr bool STASH = FUSE && NORM;
+        float* const stash = reinterpret_cast<float*>(sact);
+        float rf = 1.0f;
+        if constexpr (STASH) rf = row_rms_scale(p.h, res, s_out, K, p.eps, tid, 1, s_pair, &s_rf, stash);
+        const float* actf = static_cast<const float*>(p.act);
+        int* const se = reinterpret_cast<int*>(sxd);   // block binades until E is known
+        int emax = -126;                                // the binade of zero
+        // every lane of a warp runs the same iterations (K / 8 is a multiple
+        // of 128), so the shuffles over a block's four lanes stay full
+        for (int64_t t8 = tid; t8 < K / 8; t8 += kRplWarps * 32) {
+            const int64_t k = t8 * 8;
+            const int b = int(t8 >> 2), q = int(t8 & 3);   // block, eighth-of-32 within it
+            float xs[8];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                float xv[4];
+                if constexpr (STASH) {
+                    const float4 s4 = *reinterpret_cast<const float4*>(stash + k + 4 * u);
+                    float gg[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+                    if (p.gain) {
+                        const int4 g4 = ldg_nc_v4(p.gain + k + 4 * u);
+                        gg[0] = __int_as_float(g4.x);
+                        gg[1] = __int_as_float(g4.y);
+                        gg[2] = __int_as_float(g4.z);
+                        gg[3] = __int_as_float(g4.w);
+                    }
+                    const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float v = __fmul_rn(sv[e], rf);
+                        if (p.gain) v = __fmul_rn(v, gg[e]);
+                        xv[e] = v;
+                    }
+                } else {
+                    load_x4<FUSE, PROD>(actf + k + 4 * u, p.h + k + 4 * u, RES ? res + k + 4 * u : nullptr,
+                                        p.gain ? p.gain + k + 4 * u : nullptr, rf, xv, K);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) xs[4 * u + e] = xv[e];
+            }
+            // the block's binade from its 32 values over the four lanes
+            float amax = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(xs[e]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const int eb = binade(amax);
+            // X = rint(x * 2^(30 - eb)) as in fix_chunk32, two words a plane
+            const int sh = 30 - eb;
+            const float s1 = pow2i(sh >> 1), s2 = pow2i(sh - (sh >> 1));
+            int X[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) X[e] = rint_scaled30(__fmul_rn(xs[e], s1), s2);
+            int pl[2][4];
+            byte_planes4(X[0], X[1], X[2], X[3], pl[0][0], pl[0][1], pl[0][2], pl[0][3]);
+            byte_planes4(X[4], X[5], X[6], X[7], pl[1][0], pl[1][1], pl[1][2], pl[1][3]);
+            if constexpr (STASH) __syncwarp();   // the block's s read by its four lanes before the planes overwrite it
+            // plane j words 2q, 2q+1: 16-byte group 2j + q / 2 (slot
+            // (2j + q / 2) ^ (b & 7) of the block's 128 bytes), bytes 8 * (q % 2)
+            const uint32_t base = smem_u32(sact) + uint32_t(b) * 128u + uint32_t(8 * (q & 1));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                rpl_sts64(base + uint32_t((((2 * j + (q >> 1)) ^ (b & 7)) << 4)), uint32_t(pl[0][j]),
+                          uint32_t(pl[1][j]));
+            if (q == 0) se[b] = eb;
+            emax = max(emax, eb);
+        }
+        emax = __reduce_max_sync(0xffffffffu, emax);
+        if (lane == 0) s_emax[warp] = emax;
+        consumer_bar<kRplWarps * 32>();
+        int E = s_emax[0];
+        for (int w = 1; w < kRplWarps; ++w) E = max(E, s_emax[w]);
+        // each block's factor 2^(E_b - E): exact, or 0 far below the row's largest
+        for (int b = tid; b < int(K / Q8_QK); b += kRplWarps * 32) sxd[b] = mul_pow2_neg(1.0f, se[b] - E);
+        consumer_bar<kRplWarps * 32>();   // everyone has read s_emax
+        if (tid == 0) s_emax[kRplWarps] = E;
+    } else if constexpr (FUSE) {
         // the producer, fused: RMSNorm -> quant of the one activation row into
         // shared memory, by the same code and thread layout as act_quant, while
         // the producer warp already streams weights; CTA 0 writes the updated
@@ -300,6 +405,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
         float acc[R];
 #pragma unroll
         for (int m = 0; m < R; ++m) acc[m] = 0.0f;
+        DF accd = DF{0.0f, 0.0f};   // f32 mode: the row's sum in units of 2^(E - 30), an f32 pair
         for (int j = 0; j < nsl; ++j) {
             const int64_t t = int64_t(g) * nsl + j;
             if (int(t % kRplSlots) != slot) continue;
@@ -317,6 +423,33 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
                 // qw of its 64-byte row, 64-byte swizzle
                 const int4 s8 = lds128(st + uint32_t(C::kW + lane * 64 + ((qw ^ ((lane >> 1) & 3)) << 4)));
                 const uint32_t sh[4] = {uint32_t(s8.x), uint32_t(s8.y), uint32_t(s8.z), uint32_t(s8.w)};
+                if constexpr (MODE == 0) {
+#pragma unroll 1
+                    for (int b = 0; b < 8; ++b) {
+                        const int B = qw * 8 + b;
+                        const uint32_t wr = st + uint32_t((B >> 2) * (kRplRows * 128) + lane * 128);
+                        const int c0 = (B & 3) * 2;
+                        const int4 w0 = lds128(wr + uint32_t(((c0 ^ (lane & 7)) << 4)));
+                        const int4 w1 = lds128(wr + uint32_t((((c0 + 1) ^ (lane & 7)) << 4)));
+                        const float sw =
+                            half_bits_to_float(uint16_t((b & 1) ? (sh[b >> 1] >> 16) : (sh[b >> 1] & 0xFFFFu)));
+                        // the block's planes (the same address for every lane)
+                        // and its factor to the row's binade
+                        const int blk = j * (kRplKS / Q8_QK) + B;
+                        FixChunk32 fx;
+                        const uint32_t pb = sact_a + uint32_t(blk) * 128u;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int4 v = lds128(pb + uint32_t(((i ^ (blk & 7)) << 4)));
+                            fx.p[i >> 1][4 * (i & 1) + 0] = v.x;
+                            fx.p[i >> 1][4 * (i & 1) + 1] = v.y;
+                            fx.p[i >> 1][4 * (i & 1) + 2] = v.z;
+                            fx.p[i >> 1][4 * (i & 1) + 3] = v.w;
+                        }
+                        const float f = __fmul_rn(sw, __uint_as_float(lds32(sxd_a + uint32_t(blk) * 4u)));
+                        accd = df_add(accd, scaled_pair_split(f, fix_dot32_split(w0, w1, fx)));
+                    }
+                } else {
 #pragma unroll 2
                 for (int b = 0; b < 8; ++b) {
                     const int B = qw * 8 + b;   // block within the stage
@@ -345,6 +478,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
                         acc[m] = fmaf(fi, sw * xd, acc[m]);
                     }
                 }
+                }
             }
             __syncwarp();
             if (lane == 0 && ok) mbar_arrive(&empty[slot]);
@@ -359,6 +493,27 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
             for (int m = 0; m < R; ++m) ps[(warp * R + m) * kRplRows + lane] = acc[m];
             __syncwarp();   // the warp's writes before lane 0's release
             if (lane == 0) mbar_arrive(&pfull[b]);
+        } else if constexpr (MODE == 0) {
+            // the row group's f32-pair sums into shared memory; then thread l
+            // adds row l's over the 16 warps in warp order and scales the pair,
+            // rounded once, by 2^(E - 30) (f32), or the exact pair (f64)
+            DF* const psd = reinterpret_cast<DF*>(psum);
+            psd[warp * kRplRows + lane] = accd;
+            consumer_bar<kRplWarps * 32>();
+            if (ok && tid < kRplRows && tid < nr) {
+                DF sum = psd[tid];
+                for (int w = 1; w < kRplWarps; ++w) sum = df_add(sum, psd[w * kRplRows + tid]);
+                const int sc = s_emax[kRplWarps] - 30;   // in [-156, 98]
+                if (p.out_f64) {
+                    reinterpret_cast<double*>(p.y)[rg0 + tid] = ldexp(double(sum.hi) + double(sum.lo), sc);
+                } else {
+                    const float yv =
+                        __fmul_rn(__fmul_rn(__fadd_rn(sum.hi, sum.lo), pow2i(sc >> 1)), pow2i(sc - (sc >> 1)));
+                    reinterpret_cast<float*>(p.y)[rg0 + tid] = yv;
+                    if constexpr (KV) kv_store(p, s_pos, 0, rg0 + tid, yv);
+                }
+            }
+            consumer_bar<kRplWarps * 32>();
         } else {
             // the row group's sums into shared memory; then thread (m, l) adds
             // row l's sums of activation row m over the 16 warps in warp order
@@ -400,9 +555,9 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
         make_map3(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q, wd, ws, wb, CU_TENSOR_MAP_SWIZZLE_128B) &&
         make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.s, a.K / 16, a.N, a.K / 16, kRplKS / 16, kRplRows,
                  CU_TENSOR_MAP_SWIZZLE_64B);
-    // fused: no activation copies (the unused maps repeat the weights')
-    if (FUSE) txh = txl = txd = tw;
-    const bool ok = okw && (FUSE ||
+    // a resident row: no activation copies (the unused maps repeat the weights')
+    if (C::kResAct) txh = txl = txd = tw;
+    const bool ok = okw && (C::kResAct ||
         (make_map3(&txh, CU_TENSOR_MAP_DATA_TYPE_UINT8, xh, xdims, xs, xb, CU_TENSOR_MAP_SWIZZLE_NONE) &&
         make_map3(&txl, CU_TENSOR_MAP_DATA_TYPE_UINT8, MODE == 2 ? xh + a.plane : xh, xdims, xs, xb,
                   CU_TENSOR_MAP_SWIZZLE_NONE) &&
@@ -419,6 +574,7 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     p.plane = a.plane;
     p.rows = a.rows;
     p.y = a.y;
+    p.out_f64 = a.out_f64;
     p.err = ctx.dev_err;
     p.h = a.h;
     p.res = a.res;
