@@ -166,10 +166,10 @@ q8_status act_quant_swiglu(int mode, const float* gu, int64_t rows, int64_t K, v
  * Quantized projection of a stacked activation (codegen_cuda::lane: the
  * decode step, rows = 1, and a batch's step, rows = B, with each weight read
  * once for a group of rows: up to 8 rows (one-word) or 4 (two-word) a pass,
- * from 3 (one-word) or 2 (two-word) rows with K % 1024 == 0 with a weight row
- * per lane; from 9 (one-word), 5 (two-word) or 4 (f32) rows with K % 256 == 0
- * one pass on the tensor cores; f32 below 4 rows runs one row a pass, its
- * arithmetic being the bound).
+ * with a weight row per lane when K % 1024 == 0 (f32: one row, K <= 16384);
+ * from 9 (one-word), 5 (two-word) or 4 (f32) rows with K % 256 == 0 one pass
+ * on the tensor cores; f32 below 4 rows runs one row a pass, its arithmetic
+ * being the bound).
  *   y[m][n] for m < rows, n < N; y is float, or double when mode is
  *   Q8_ACT_F32 and out_f64 != 0.  1 <= rows <= Q8_MAX_ROWS.
  */
@@ -296,6 +296,10 @@ q8_status q8_debug_block_dots(int mode, const int8_t* q, const void* xq, int64_t
  * Debug, host only (no device work, no CUDA call): the stage geometry the
  * decode kernel (rows <= 8 one-word, <= 4 two-word, 1 f32) uses for CTA `cta`
  * of a grid of `grid` CTAs (the library launches min(SM count, N) of them).
+ * That kernel serves the LM head's arg-max and the projections whose K is not
+ * a multiple of 1024 (f32: or above 16384); the others of those row counts
+ * run the row-per-lane kernel, whose geometry is fixed (a lane per weight
+ * row, 32-row groups, whole groups per CTA, stages of 1024 values).
  * out (host, 21 int64) receives: R (activation rows the kernel is built for),
  * KS (bytes of K a slice), nks (slices a row), PB (bytes a part), npr (parts a
  * slice, a power of two), nprr (parts holding data), RS (rows a stage), rpw
@@ -312,6 +316,8 @@ q8_status q8_debug_row_geometry(int mode, int64_t rows, int64_t N, int64_t K, in
  * Debug, host only: the same 21 fields for the decode launch of a fused call
  * at rows = 1 and K <= 16384 values, by its producer: prod 0 q8_proj_fused
  * (and its KV-row form), 1 q8_proj_fused_residual, 2 q8_proj_fused_swiglu.
+ * (Fused calls whose K is a multiple of 1024 run the row-per-lane kernel
+ * instead, as the plain projections do.)
  * The int8 modes and the plain producer run the rows = 1 geometry above.  In
  * f32 mode the residual and SwiGLU producers above 4096 values shorten the
  * ring (field 16): the converted activation (128 bytes a 32-value block, 4K
