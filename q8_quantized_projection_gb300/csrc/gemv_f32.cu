@@ -13,6 +13,7 @@ namespace q8 {
 
 template <bool ARGMAX>
 static cudaError_t dispatch_rows(const GemvArgs& a, const LaunchCtx& ctx) {
+    // a weight row a lane (K % 1024 == 0; the arg-max keeps the decode kernel)
     if constexpr (!ARGMAX) {
         if (a.rows <= 1 && rpl_fits(a)) return launch_gemv_rpl_t<0, 1>(a, ctx);
     }

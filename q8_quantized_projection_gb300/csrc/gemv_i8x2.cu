@@ -1,9 +1,8 @@
 // gemv_i8x2.cu -- instantiations of the CUDA-core projection for activation
 // mode 2: the row-per-lane kernel (gemv_rpl.cuh) for 1-4 rows with K % 1024 ==
-// 0 (plain projections and fused decode steps without the KV-row epilogue),
-// else the decode kernel (gemv_row.cuh: the LM head's arg-max, the KV-row
-// epilogue, other K); the slice-major kernel (gemv.cuh) for more rows.  One
-// file per mode so the build runs in parallel.
+// 0 (plain projections, the LM head's arg-max and fused decode steps), else
+// the decode kernel (gemv_row.cuh: other K); the slice-major kernel (gemv.cuh)
+// for more rows.  One file per mode so the build runs in parallel.
 #include "gemv_row.cuh"
 #include "gemv_rpl.cuh"
 
@@ -11,12 +10,10 @@ namespace q8 {
 
 template <bool ARGMAX>
 static cudaError_t dispatch_rows(const GemvArgs& a, const LaunchCtx& ctx) {
-    if constexpr (!ARGMAX) {
-        // a weight row a lane (plain projections, K % 1024 == 0)
-        if (a.rows <= 1 && rpl_fits(a)) return launch_gemv_rpl_t<2, 1>(a, ctx);
-        if (a.rows <= 2 && rpl_fits(a)) return launch_gemv_rpl_t<2, 2>(a, ctx);
-        if (a.rows <= 4 && rpl_fits(a)) return launch_gemv_rpl_t<2, 4>(a, ctx);
-    }
+    // a weight row a lane (K % 1024 == 0), plain or with the arg-max
+    if (a.rows <= 1 && rpl_fits(a)) return launch_gemv_rpl_t<2, 1, false, kProdPlain, false, ARGMAX>(a, ctx);
+    if (a.rows <= 2 && rpl_fits(a)) return launch_gemv_rpl_t<2, 2, false, kProdPlain, false, ARGMAX>(a, ctx);
+    if (a.rows <= 4 && rpl_fits(a)) return launch_gemv_rpl_t<2, 4, false, kProdPlain, false, ARGMAX>(a, ctx);
     if (a.rows <= 1 && row_kernel_fits<2, 1>(a.K)) return launch_gemv_row_t<2, 1, ARGMAX>(a, ctx);
     if (a.rows <= 2 && row_kernel_fits<2, 2>(a.K)) return launch_gemv_row_t<2, 2, ARGMAX>(a, ctx);
     if (a.rows <= 4 && row_kernel_fits<2, 4>(a.K)) return launch_gemv_row_t<2, 4, ARGMAX>(a, ctx);

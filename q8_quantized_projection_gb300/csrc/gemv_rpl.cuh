@@ -64,7 +64,7 @@ constexpr int kRplSlots = 4;                       // ring slots, four consumer 
 // shared memory, as 31-bit fixed-point byte planes of each 32-value block
 // relative to the block's binade, with each block's factor 2^(E_b - E) to the
 // row's largest binade E (fused or not).
-template <int MODE, int R, bool FUSE = false>
+template <int MODE, int R, bool FUSE = false, bool ARGMAX = false>
 struct RplCfg {
     static constexpr bool kResAct = FUSE || MODE == 0;          // the row resident in shared memory
     static constexpr int kPlanes = MODE == 2 ? 2 : 1;
@@ -82,7 +82,7 @@ struct RplCfg {
     // buffers where that pays (one-word 8 rows: 69.8 against 71.9 us a layer
     // of the four d = 4096 projections), else by the consumer warps between
     // two named barriers (4 rows: 56.5 against 57.6 us).
-    static constexpr bool kComb = MODE == 1 && R >= 8;
+    static constexpr bool kComb = MODE == 1 && R >= 8 && !ARGMAX;
     static constexpr int kThreads = 32 * (kRplWarps + 1 + (kComb ? 1 : 0));
     // one buffer: [warp][R][lane], f32 (int8 modes) or f32 pairs (f32 mode)
     static constexpr int kPsum = kRplWarps * R * kRplRows * (MODE == 0 ? 8 : 4);
@@ -102,9 +102,10 @@ inline bool rpl_fits(const GemvArgs& a) {
     const auto al16 = rpl_al16;
     // f32 mode: one row, resident in shared memory (f64 output allowed)
     const bool f32ok = a.mode != 0 || (a.rows == 1 && a.K <= kFusedMaxK);
-    return f32ok && a.rows >= 1 && a.K >= kRplKS && a.K % kRplKS == 0 && a.N <= (int64_t(1) << 31) && a.y &&
-           (!a.out_f64 || a.mode == 0) && !a.tok && !a.h && !a.k_cache && al16(a.q) && al16(a.s) &&
-           al16(a.act) && (a.mode == 0 || al16(a.xd)) && a.plane % 16 == 0;
+    // y may be NULL for the arg-max (the LM head without logits)
+    return f32ok && a.rows >= 1 && a.K >= kRplKS && a.K % kRplKS == 0 && a.N <= (int64_t(1) << 31) &&
+           (a.y || a.tok) && (!a.out_f64 || a.mode == 0) && !a.h && !a.k_cache && al16(a.q) && al16(a.s) &&
+           al16(a.act) && (a.mode == 0 || al16(a.xd)) && a.plane % 16 == 0 && (!a.tok || al16(a.ws));
 }
 
 // A fused decode step (one row, the producer in the kernel; with or without
@@ -153,8 +154,8 @@ __device__ __forceinline__ void rpl_tma2d_ef(void* dst, const CUtensorMap* map, 
         : "memory");
 }
 
-template <int MODE, int R, bool FUSE = false, int PROD = kProdPlain, bool KV = false>
-__global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
+template <int MODE, int R, bool FUSE = false, int PROD = kProdPlain, bool KV = false, bool ARGMAX = false>
+__global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
     gemv_rpl_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                     const __grid_constant__ CUtensorMap tm_xh,
                     const __grid_constant__ CUtensorMap tm_xl, const __grid_constant__ CUtensorMap tm_xd,
@@ -163,13 +164,20 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
     static_assert(PROD == kProdPlain || FUSE, "producer kinds belong to the fused producer");
     static_assert(!KV || (FUSE && PROD == kProdPlain), "the KV-row epilogue: fused plain decode step");
     static_assert(!FUSE || kRplWarps * 32 == kProdThreads, "fused producer needs kProdThreads consumers");
-    using C = RplCfg<MODE, R, FUSE>;
+    // (the f32 head keeps the decode kernel: at K = 4096 its warps hold their
+    // activation block in registers for the launch, where this kernel reloads
+    // a block's planes at every row group; measured 98.5 against 101.0 us)
+    static_assert(!ARGMAX || (!FUSE && MODE != 0), "the arg-max epilogue: int8 plain projections");
+    using C = RplCfg<MODE, R, FUSE, ARGMAX>;
     constexpr bool RES = PROD == kProdResidual;
     constexpr bool NORM = PROD != kProdSwiglu;
     __shared__ float2 s_pair[kProdWarps];
     __shared__ float s_rf;
     __shared__ int s_pos[1];   // KV-row epilogue: the row's cache position
     __shared__ int s_emax[kRplWarps + 1];   // f32 mode: the warps' largest block binades, then the row's
+    __shared__ ArgmaxCand s_cand[R > 0 ? R : 1];   // arg-max: the CTA's best per activation row
+    __shared__ ArgmaxCand s_red[kRplWarps];         // and the last CTA's reduction scratch
+    __shared__ unsigned int s_ticket;
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled weight tiles
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -399,6 +407,9 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
     const uint32_t sact_a = smem_u32(sact), sxd_a = smem_u32(sxd);
     const int slot = warp >> 2, qw = warp & 3;   // this warp's slot and quarter of a stage
     bool ok = true;
+    // arg-max: combine thread (m, l)'s best (value, lowest index) over the launch
+    double bv = -INFINITY;
+    long long bi = 0x7fffffffffffffffll;
     for (int g = 0; g < ngroups; ++g) {
         const int64_t rg0 = r0 + int64_t(g) * kRplRows;
         const int nr = int(min64(kRplRows, r1 - rg0));
@@ -505,7 +516,9 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
                 for (int w = 1; w < kRplWarps; ++w) sum = df_add(sum, psd[w * kRplRows + tid]);
                 const int sc = s_emax[kRplWarps] - 30;   // in [-156, 98]
                 if (p.out_f64) {
-                    reinterpret_cast<double*>(p.y)[rg0 + tid] = ldexp(double(sum.hi) + double(sum.lo), sc);
+                    // exact: a power of two well inside the f64 range
+                    reinterpret_cast<double*>(p.y)[rg0 + tid] =
+                        (double(sum.hi) + double(sum.lo)) * __longlong_as_double((long long)(sc + 1023) << 52);
                 } else {
                     const float yv =
                         __fmul_rn(__fmul_rn(__fadd_rn(sum.hi, sum.lo), pow2i(sc >> 1)), pow2i(sc - (sc >> 1)));
@@ -525,23 +538,55 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE>::kThreads, 1)
                 if (l < nr && m < rows) {
                     float sum = psum[m * kRplRows + l];
                     for (int w = 1; w < kRplWarps; ++w) sum += psum[(w * R + m) * kRplRows + l];
-                    reinterpret_cast<float*>(p.y)[m * N + rg0 + l] = sum;
+                    if (p.y) reinterpret_cast<float*>(p.y)[m * N + rg0 + l] = sum;
                     if constexpr (KV) kv_store(p, s_pos, m, rg0 + l, sum);
+                    if constexpr (ARGMAX) argmax_keep(bv, bi, double(sum), rg0 + l);
                 }
             }
             consumer_bar<kRplWarps * 32>();
         }
     }
+
+    if constexpr (ARGMAX) {
+        // warp m's lanes hold activation row m's candidates: the warp's best,
+        // then per CTA into the workspace, and the last CTA to take a ticket
+        // reduces every CTA's candidate (lowest index on ties)
+        if (warp < R) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const long long oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                argmax_keep(bv, bi, ov, oi);
+            }
+            if (lane == 0) s_cand[warp] = {bv, bi};
+        }
+        consumer_bar<kRplWarps * 32>();
+        ArgmaxCand* gc = reinterpret_cast<ArgmaxCand*>(p.ws + kArgmaxHeader);
+        unsigned int* counter = reinterpret_cast<unsigned int*>(p.ws);
+        if (tid < rows) {
+            gc[size_t(c) * rows + tid] = s_cand[tid];
+            __threadfence();
+        }
+        consumer_bar<kRplWarps * 32>();
+        if (tid == 0) s_ticket = atomicAdd(counter, 1u);
+        consumer_bar<kRplWarps * 32>();
+        if (s_ticket == unsigned(G - 1)) {
+            __threadfence();
+            argmax_final<kRplWarps * 32>(gc, G, rows, tid, s_red, p.tok, p.maxval);
+            if (tid == 0) *counter = 0u;
+        }
+    }
 }
 
-template <int MODE, int R, bool FUSE = false, int PROD = kProdPlain, bool KV = false>
+template <int MODE, int R, bool FUSE = false, int PROD = kProdPlain, bool KV = false, bool ARGMAX = false>
 cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
-    using C = RplCfg<MODE, R, FUSE>;
-    auto kern = gemv_rpl_kernel<MODE, R, FUSE, PROD, KV>;
+    using C = RplCfg<MODE, R, FUSE, ARGMAX>;
+    auto kern = gemv_rpl_kernel<MODE, R, FUSE, PROD, KV, ARGMAX>;
     static std::atomic<bool> configured[kMaxDevices];
     if (const cudaError_t e = set_smem_once(kern, C::kSmem, ctx.dev, configured); e != cudaSuccess) return e;
     if (FUSE ? !rpl_fits_fused(a) : (!rpl_fits(a) || a.rows > R)) return cudaErrorInvalidValue;
     if (KV != (a.k_cache != nullptr)) return cudaErrorInvalidValue;
+    if (ARGMAX != (a.tok != nullptr) || (ARGMAX && !a.ws)) return cudaErrorInvalidValue;
     alignas(64) CUtensorMap tw, ts, txh, txl, txd;
     const int8_t* xh = static_cast<const int8_t*>(a.act);
     // weights as (byte in a 128-byte chunk, row, chunk): a box of 8 chunks of
@@ -575,6 +620,9 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     p.rows = a.rows;
     p.y = a.y;
     p.out_f64 = a.out_f64;
+    p.tok = a.tok;
+    p.maxval = a.maxval;
+    p.ws = reinterpret_cast<unsigned char*>(a.ws);
     p.err = ctx.dev_err;
     p.h = a.h;
     p.res = a.res;
