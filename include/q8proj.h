@@ -245,7 +245,9 @@ q8_status q8_proj_fused_swiglu(int mode, const int8_t* q, const uint16_t* s, int
  * sequence).  Modes Q8_ACT_F32 (logits to f64 accuracy) and Q8_ACT_I8 /
  * Q8_ACT_I8X2 (f32 logits).  From 9 (one-word), 5 (two-word) or 6 (f32, up
  * to 16 rows and N <= 131072) rows on, with K % 256 == 0, the head is read
- * once for all rows on the tensor cores.
+ * once for all rows on the tensor cores; below that, once per group of up to
+ * 8 (one-word) or 4 (two-word) rows (with a weight row per lane when
+ * K % 1024 == 0), and f32 once per row.
  *   tok     int32 [rows]: the smallest n holding the row's maximum logit; NaN
  *           logits are never the maximum, and a row of NaN gives 0
  *   maxval  double [rows] or NULL: that maximum (NaN for a row of NaN)
