@@ -97,13 +97,13 @@ struct KvArgs {
     float* v_cache = nullptr;
 };
 
-// Runs the CUDA-core projection over groups of gemv_max_rows(mode) activation
-// rows (each group one launch reading the weights once).
+// Runs the CUDA-core projection over groups of gemv_group_rows(mode, K, ...)
+// activation rows (each group one launch reading the weights once).
 q8_status run_projection(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                          const void* xq, const float* xd, int64_t rows, void* y, int out_f64,
                          int32_t* tok, double* maxval, void* ws, const LaunchCtx& ctx) {
     const int64_t nb = K / Q8_QK;
-    const int group = gemv_max_rows(mode);
+    const int group = gemv_group_rows(mode, K, tok != nullptr);
     const size_t elem = (mode == Q8_ACT_F32) ? 4 : 1;
     const size_t ysz = (mode == Q8_ACT_F32 && out_f64) ? 8 : 4;
     for (int64_t g0 = 0; g0 < rows; g0 += group) {

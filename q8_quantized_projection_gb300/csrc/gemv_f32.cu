@@ -1,11 +1,10 @@
 // gemv_f32.cu -- instantiations of the CUDA-core projection for activation
-// mode 0, one activation row per launch (the mode is bound by instruction
-// issue, not HBM, so a row per pass over the weights is faster than sharing a
-// pass): the row-per-lane kernel (gemv_rpl.cuh) for K % 1024 == 0 up to
-// 16384 (plain projections and fused decode steps), else the decode kernel
-// (gemv_row.cuh: the LM head's arg-max, other K), and the slice-major kernel
-// (gemv.cuh) for K beyond the decode kernel's part sums.  One file per mode so
-// the build runs in parallel.
+// mode 0: the row-per-lane kernel (gemv_rpl.cuh) for K % 1024 == 0, one row
+// up to 16384 values or a pair of rows up to 8192 (plain projections and fused
+// decode steps), else the decode kernel (gemv_row.cuh: the LM head's arg-max,
+// other K; one row a launch, the mode being bound by instruction issue), and
+// the slice-major kernel (gemv.cuh) for K beyond the decode kernel's part
+// sums.  One file per mode so the build runs in parallel.
 #include "gemv_row.cuh"
 #include "gemv_rpl.cuh"
 
@@ -16,6 +15,7 @@ static cudaError_t dispatch_rows(const GemvArgs& a, const LaunchCtx& ctx) {
     // a weight row a lane (K % 1024 == 0; the arg-max keeps the decode kernel)
     if constexpr (!ARGMAX) {
         if (a.rows <= 1 && rpl_fits(a)) return launch_gemv_rpl_t<0, 1>(a, ctx);
+        if (a.rows == 2 && rpl_fits(a)) return launch_gemv_rpl_t<0, 2>(a, ctx);
     }
     if (a.rows <= 1 && row_kernel_fits<0, 1>(a.K)) return launch_gemv_row_t<0, 1, ARGMAX>(a, ctx);
     return launch_gemv_t<0, 4, ARGMAX>(a, ctx);

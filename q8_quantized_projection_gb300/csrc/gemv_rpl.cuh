@@ -60,10 +60,10 @@ constexpr int kRplSlots = 4;                       // ring slots, four consumer 
 // residual added before the norm, or the SwiGLU of a gate+up row) by the
 // consumer warps into shared memory for the whole launch; the stages then
 // carry weights and scales only.
-// MODE 0 (f32 activations, one row): the row is converted once per CTA into
-// shared memory, as 31-bit fixed-point byte planes of each 32-value block
-// relative to the block's binade, with each block's factor 2^(E_b - E) to the
-// row's largest binade E (fused or not).
+// MODE 0 (f32 activations, one or two rows): the rows are converted once per
+// CTA into shared memory, as 31-bit fixed-point byte planes of each 32-value
+// block relative to the block's binade, with each block's factor 2^(E_b - E)
+// to the row's largest binade E (fused or not).
 template <int MODE, int R, bool FUSE = false, bool ARGMAX = false>
 struct RplCfg {
     static constexpr bool kResAct = FUSE || MODE == 0;          // the row resident in shared memory
@@ -72,11 +72,14 @@ struct RplCfg {
     static constexpr int kS = kRplRows * (kRplKS / Q8_QK) * 2;  // [32][64] bytes of f16 scales
     static constexpr int kX = kResAct ? 0 : kPlanes * R * kRplKS;        // [plane][4 tiles][R][256]
     static constexpr int kXD = kResAct ? 0 : R * (kRplKS / Q8_QK) * 4;   // [R][32] f32
-    // the resident row: [plane][kFusedMaxK] codes (int8 modes) or
-    // [kFusedMaxK / 32][128] fixed-point planes (f32), then kFusedMaxK / 32
+    // the resident rows: [plane][kMaxK] codes (int8 modes, one row) or
+    // [R][kMaxK / 32][128] fixed-point planes (f32), then [R][kMaxK / 32]
     // block scales (int8) or block factors (f32)
-    static constexpr int kActBytes = MODE == 0 ? int(4 * kFusedMaxK) : int(2 * kFusedMaxK);
-    static constexpr int kAct = kResAct ? kActBytes + int(kFusedMaxK / Q8_QK) * 4 : 0;
+    // the longest resident row: f32 pairs of rows up to 8192 values (both rows'
+    // planes beside the ring), else kFusedMaxK
+    static constexpr int kMaxK = (MODE == 0 && R == 2) ? 8192 : int(kFusedMaxK);
+    static constexpr int kActBytes = MODE == 0 ? R * 4 * kMaxK : 2 * kMaxK;
+    static constexpr int kAct = kResAct ? kActBytes + R * (kMaxK / Q8_QK) * 4 : 0;
     static constexpr int kStage = (kW + kS + kX + kXD + 1023) / 1024 * 1024;
     // The row group's partial sums are added by a combining warp through two
     // buffers where that pays (one-word 8 rows: 69.8 against 71.9 us a layer
@@ -91,7 +94,8 @@ struct RplCfg {
         size_t(kRplSlots) * kStage + kBufs * kPsum + (2 * kRplSlots + 4) * 8 + kAct + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory");
     static_assert(!FUSE || (R == 1 && !kComb), "fused producer: one row");
-    static_assert(MODE != 0 || R == 1, "f32 mode: one row");
+    static_assert(MODE != 0 || R <= 2, "f32 mode: one or two rows");
+    static_assert(MODE != 0 || R == 1 || !FUSE, "f32 pairs: plain projections");
 };
 
 inline bool rpl_al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -100,8 +104,9 @@ inline bool rpl_al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1
 // maps need; anything else takes the decode kernel.
 inline bool rpl_fits(const GemvArgs& a) {
     const auto al16 = rpl_al16;
-    // f32 mode: one row, resident in shared memory (f64 output allowed)
-    const bool f32ok = a.mode != 0 || (a.rows == 1 && a.K <= kFusedMaxK);
+    // f32 mode: one row up to kFusedMaxK values or a pair up to 8192, resident
+    // in shared memory (f64 output allowed)
+    const bool f32ok = a.mode != 0 || (a.rows == 1 && a.K <= kFusedMaxK) || (a.rows == 2 && a.K <= 8192);
     // y may be NULL for the arg-max (the LM head without logits)
     return f32ok && a.rows >= 1 && a.K >= kRplKS && a.K % kRplKS == 0 && a.N <= (int64_t(1) << 31) &&
            (a.y || a.tok) && (!a.out_f64 || a.mode == 0) && !a.h && !a.k_cache && al16(a.q) && al16(a.s) &&
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
     __shared__ float2 s_pair[kProdWarps];
     __shared__ float s_rf;
     __shared__ int s_pos[1];   // KV-row epilogue: the row's cache position
-    __shared__ int s_emax[kRplWarps + 1];   // f32 mode: the warps' largest block binades, then the row's
+    __shared__ int s_emax[R][kRplWarps + 1];   // f32 mode: the warps' largest block binades, then the row's
     __shared__ ArgmaxCand s_cand[R > 0 ? R : 1];   // arg-max: the CTA's best per activation row
     __shared__ ArgmaxCand s_red[kRplWarps];         // and the last CTA's reduction scratch
     __shared__ unsigned int s_ticket;
@@ -322,8 +327,12 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
         float* const stash = reinterpret_cast<float*>(sact);
         float rf = 1.0f;
         if constexpr (STASH) rf = row_rms_scale(p.h, res, s_out, K, p.eps, tid, 1, s_pair, &s_rf, stash);
-        const float* actf = static_cast<const float*>(p.act);
-        int* const se = reinterpret_cast<int*>(sxd);   // block binades until E is known
+        for (int m = 0; m < R; ++m) {
+        // row m: planes at m * 4 * kMaxK, block factors at m * kMaxK / 32
+        unsigned char* const plm = sact + size_t(m) * 4 * C::kMaxK;
+        float* const sxm = sxd + m * (C::kMaxK / Q8_QK);
+        const float* actf = static_cast<const float*>(p.act) + m * K;
+        int* const se = reinterpret_cast<int*>(sxm);   // block binades until E is known
         int emax = -126;                                // the binade of zero
         // every lane of a warp runs the same iterations (K / 8 is a multiple
         // of 128), so the shuffles over a block's four lanes stay full
@@ -377,7 +386,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
             if constexpr (STASH) __syncwarp();   // the block's s read by its four lanes before the planes overwrite it
             // plane j words 2q, 2q+1: 16-byte group 2j + q / 2 (slot
             // (2j + q / 2) ^ (b & 7) of the block's 128 bytes), bytes 8 * (q % 2)
-            const uint32_t base = smem_u32(sact) + uint32_t(b) * 128u + uint32_t(8 * (q & 1));
+            const uint32_t base = smem_u32(plm) + uint32_t(b) * 128u + uint32_t(8 * (q & 1));
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 rpl_sts64(base + uint32_t((((2 * j + (q >> 1)) ^ (b & 7)) << 4)), uint32_t(pl[0][j]),
@@ -386,14 +395,15 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
             emax = max(emax, eb);
         }
         emax = __reduce_max_sync(0xffffffffu, emax);
-        if (lane == 0) s_emax[warp] = emax;
+        if (lane == 0) s_emax[m][warp] = emax;
         consumer_bar<kRplWarps * 32>();
-        int E = s_emax[0];
-        for (int w = 1; w < kRplWarps; ++w) E = max(E, s_emax[w]);
+        int E = s_emax[m][0];
+        for (int w = 1; w < kRplWarps; ++w) E = max(E, s_emax[m][w]);
         // each block's factor 2^(E_b - E): exact, or 0 far below the row's largest
-        for (int b = tid; b < int(K / Q8_QK); b += kRplWarps * 32) sxd[b] = mul_pow2_neg(1.0f, se[b] - E);
+        for (int b = tid; b < int(K / Q8_QK); b += kRplWarps * 32) sxm[b] = mul_pow2_neg(1.0f, se[b] - E);
         consumer_bar<kRplWarps * 32>();   // everyone has read s_emax
-        if (tid == 0) s_emax[kRplWarps] = E;
+        if (tid == 0) s_emax[m][kRplWarps] = E;
+        }
     } else if constexpr (FUSE) {
         // the producer, fused: RMSNorm -> quant of the one activation row into
         // shared memory, by the same code and thread layout as act_quant, while
@@ -416,7 +426,9 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
         float acc[R];
 #pragma unroll
         for (int m = 0; m < R; ++m) acc[m] = 0.0f;
-        DF accd = DF{0.0f, 0.0f};   // f32 mode: the row's sum in units of 2^(E - 30), an f32 pair
+        DF accd[R];   // f32 mode: each row's sum in units of 2^(E - 30), an f32 pair
+#pragma unroll
+        for (int m = 0; m < R; ++m) accd[m] = DF{0.0f, 0.0f};
         for (int j = 0; j < nsl; ++j) {
             const int64_t t = int64_t(g) * nsl + j;
             if (int(t % kRplSlots) != slot) continue;
@@ -444,21 +456,25 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                         const int4 w1 = lds128(wr + uint32_t((((c0 + 1) ^ (lane & 7)) << 4)));
                         const float sw =
                             half_bits_to_float(uint16_t((b & 1) ? (sh[b >> 1] >> 16) : (sh[b >> 1] & 0xFFFFu)));
-                        // the block's planes (the same address for every lane)
-                        // and its factor to the row's binade
+                        // each row's planes of the block (the same address for
+                        // every lane) and its factor to that row's binade
                         const int blk = j * (kRplKS / Q8_QK) + B;
-                        FixChunk32 fx;
-                        const uint32_t pb = sact_a + uint32_t(blk) * 128u;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int4 v = lds128(pb + uint32_t(((i ^ (blk & 7)) << 4)));
-                            fx.p[i >> 1][4 * (i & 1) + 0] = v.x;
-                            fx.p[i >> 1][4 * (i & 1) + 1] = v.y;
-                            fx.p[i >> 1][4 * (i & 1) + 2] = v.z;
-                            fx.p[i >> 1][4 * (i & 1) + 3] = v.w;
+                        for (int m = 0; m < R; ++m) {
+                            FixChunk32 fx;
+                            const uint32_t pb = sact_a + uint32_t(m * 4 * C::kMaxK) + uint32_t(blk) * 128u;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int4 v = lds128(pb + uint32_t(((i ^ (blk & 7)) << 4)));
+                                fx.p[i >> 1][4 * (i & 1) + 0] = v.x;
+                                fx.p[i >> 1][4 * (i & 1) + 1] = v.y;
+                                fx.p[i >> 1][4 * (i & 1) + 2] = v.z;
+                                fx.p[i >> 1][4 * (i & 1) + 3] = v.w;
+                            }
+                            const float f = __fmul_rn(
+                                sw, __uint_as_float(lds32(sxd_a + uint32_t((m * (C::kMaxK / Q8_QK) + blk) * 4))));
+                            accd[m] = df_add(accd[m], scaled_pair_split(f, fix_dot32_split(w0, w1, fx)));
                         }
-                        const float f = __fmul_rn(sw, __uint_as_float(lds32(sxd_a + uint32_t(blk) * 4u)));
-                        accd = df_add(accd, scaled_pair_split(f, fix_dot32_split(w0, w1, fx)));
                     }
                 } else {
 #pragma unroll 2
@@ -505,25 +521,30 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
             __syncwarp();   // the warp's writes before lane 0's release
             if (lane == 0) mbar_arrive(&pfull[b]);
         } else if constexpr (MODE == 0) {
-            // the row group's f32-pair sums into shared memory; then thread l
-            // adds row l's over the 16 warps in warp order and scales the pair,
-            // rounded once, by 2^(E - 30) (f32), or the exact pair (f64)
+            // the row group's f32-pair sums into shared memory; then thread
+            // (m, l) adds row l's of activation row m over the 16 warps in warp
+            // order and scales the pair, rounded once, by 2^(E_m - 30) (f32),
+            // or the exact pair (f64)
             DF* const psd = reinterpret_cast<DF*>(psum);
-            psd[warp * kRplRows + lane] = accd;
+#pragma unroll
+            for (int m = 0; m < R; ++m) psd[(warp * R + m) * kRplRows + lane] = accd[m];
             consumer_bar<kRplWarps * 32>();
-            if (ok && tid < kRplRows && tid < nr) {
-                DF sum = psd[tid];
-                for (int w = 1; w < kRplWarps; ++w) sum = df_add(sum, psd[w * kRplRows + tid]);
-                const int sc = s_emax[kRplWarps] - 30;   // in [-156, 98]
-                if (p.out_f64) {
-                    // exact: a power of two well inside the f64 range
-                    reinterpret_cast<double*>(p.y)[rg0 + tid] =
-                        (double(sum.hi) + double(sum.lo)) * __longlong_as_double((long long)(sc + 1023) << 52);
-                } else {
-                    const float yv =
-                        __fmul_rn(__fmul_rn(__fadd_rn(sum.hi, sum.lo), pow2i(sc >> 1)), pow2i(sc - (sc >> 1)));
-                    reinterpret_cast<float*>(p.y)[rg0 + tid] = yv;
-                    if constexpr (KV) kv_store(p, s_pos, 0, rg0 + tid, yv);
+            if (ok && tid < kRplRows * R) {
+                const int l = tid % kRplRows, m = tid / kRplRows;
+                if (l < nr) {
+                    DF sum = psd[m * kRplRows + l];
+                    for (int w = 1; w < kRplWarps; ++w) sum = df_add(sum, psd[(w * R + m) * kRplRows + l]);
+                    const int sc = s_emax[m][kRplWarps] - 30;   // in [-156, 98]
+                    if (p.out_f64) {
+                        // exact: a power of two well inside the f64 range
+                        reinterpret_cast<double*>(p.y)[m * N + rg0 + l] =
+                            (double(sum.hi) + double(sum.lo)) * __longlong_as_double((long long)(sc + 1023) << 52);
+                    } else {
+                        const float yv = __fmul_rn(__fmul_rn(__fadd_rn(sum.hi, sum.lo), pow2i(sc >> 1)),
+                                                   pow2i(sc - (sc >> 1)));
+                        reinterpret_cast<float*>(p.y)[m * N + rg0 + l] = yv;
+                        if constexpr (KV) kv_store(p, s_pos, 0, rg0 + l, yv);
+                    }
                 }
             }
             consumer_bar<kRplWarps * 32>();
@@ -585,6 +606,7 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     static std::atomic<bool> configured[kMaxDevices];
     if (const cudaError_t e = set_smem_once(kern, C::kSmem, ctx.dev, configured); e != cudaSuccess) return e;
     if (FUSE ? !rpl_fits_fused(a) : (!rpl_fits(a) || a.rows > R)) return cudaErrorInvalidValue;
+    if (MODE == 0 && a.rows != R) return cudaErrorInvalidValue;   // f32: every resident row is used
     if (KV != (a.k_cache != nullptr)) return cudaErrorInvalidValue;
     if (ARGMAX != (a.tok != nullptr) || (ARGMAX && !a.ws)) return cudaErrorInvalidValue;
     alignas(64) CUtensorMap tw, ts, txh, txl, txd;

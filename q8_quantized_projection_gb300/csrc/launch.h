@@ -84,6 +84,12 @@ constexpr int64_t kFusedMaxK = 16384;
 // per launch: it is issue-bound, and a two-row pass cost 1.5x two one-row
 // passes (LM head, 16 rows: 3.19 ms in pairs, 2.07 ms row by row).
 constexpr int gemv_max_rows(int mode) { return mode == 0 ? 1 : mode == 1 ? 8 : 4; }
+// The rows one such launch takes for a projection with K values: f32 pairs
+// where the row-per-lane kernel holds both rows in shared memory (K % 1024 ==
+// 0, K <= 8192, no arg-max), else gemv_max_rows(mode).
+constexpr int gemv_group_rows(int mode, int64_t K, bool argmax) {
+    return (mode == 0 && !argmax && K % 1024 == 0 && K <= 8192) ? 2 : gemv_max_rows(mode);
+}
 
 // tensor-core chunk path (chunk.cu): modes 1 and 2, K % 256 == 0
 bool chunk_supported(int mode, int64_t N, int64_t K, int64_t T);
