@@ -409,8 +409,10 @@ def test_fused_kv_rows(mode, rows, pos):
 
 
 @pytest.mark.parametrize("rows", [1, 3])
-def test_fused_kv_position_out_of_range(rows):
-    n, k, kv_col, d, n_pos = 256, 512, 128, 32, 4
+@pytest.mark.parametrize("k", [512, 1024])
+def test_fused_kv_position_out_of_range(rows, k):
+    # K = 1024: the row-per-lane kernel's KV epilogue at rows = 1
+    n, kv_col, d, n_pos = 256, 128, 32, 4
     rng = np.random.default_rng(7 + rows)
     q, s = synth.q8_weights(rng, n, k)
     h = synth.activations(rng, rows, k)
@@ -452,8 +454,8 @@ def _planted_head(n, k, rows, seed):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("n,k,rows", [(20000, 1024, 1), (20000, 1024, 16), (5000, 4096, 20),
-                                      (8, 256, 1)])
+@pytest.mark.parametrize("n,k,rows", [(20000, 1024, 1), (20000, 1024, 3), (20000, 2048, 8),
+                                      (20000, 1024, 16), (5000, 4096, 20), (8, 256, 1)])
 def test_head_argmax_planted(mode, n, k, rows):
     q, s, h, pos = _planted_head(n, k, rows, seed=n + k + rows)
     x, _ = orc.rmsnorm(h)
@@ -541,13 +543,15 @@ def test_head_argmax_exact_ties(mode, rows, noalloc):
 
 
 @pytest.mark.parametrize("mode", ["i8", "i8x2"])
-@pytest.mark.parametrize("rows", [1, 16])
-def test_head_argmax_nan_and_infinite_logits(mode, rows):
+@pytest.mark.parametrize("rows", [1, 3, 16])
+@pytest.mark.parametrize("k", [256, 1024])
+def test_head_argmax_nan_and_infinite_logits(mode, rows, k):
     """NaN logits are never the maximum; a row of -inf gives index 0; a row of
     NaN gives index 0 and the value NaN (infinite binary16 scales: 0 * inf is
-    NaN, a negative block dot times inf is -inf)."""
-    n, k = 3000, 256
-    rng = np.random.default_rng(77 + rows)
+    NaN, a negative block dot times inf is -inf).  K = 1024: the row-per-lane
+    kernel's arg-max; K = 256: the decode kernel's."""
+    n = 3000
+    rng = np.random.default_rng(77 + rows + k)
     q, s = synth.q8_weights(rng, n, k)
     h, base = synth.head_activations(rng, rows, k)
     pos = np.array([5, 2999, 1, 700, 1500, 2000, 2500, 2998])
