@@ -404,15 +404,18 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
         consumer_bar<kRplWarps * 32>();   // everyone has read s_emax
         if (tid == 0) s_emax[m][kRplWarps] = E;
         }
-    } else if constexpr (FUSE) {
-        // the producer, fused: RMSNorm -> quant of the one activation row into
-        // shared memory, by the same code and thread layout as act_quant, while
-        // the producer warp already streams weights; CTA 0 writes the updated
-        // residual stream, when asked
-        const float* const res = RES ? p.res : nullptr;
+    }
+    // the producer, fused (int8 modes): the RMS scale here, by act_quant's
+    // reduction (CTA 0 writes the updated residual stream, when asked); the
+    // quantisation, by act_quant's per-group code, a stage's 1024 values at a
+    // time by the warp group that consumes that stage in the first row group,
+    // just before it does (a row-group barrier later makes every stage's codes
+    // visible to all groups)
+    const float* const res_in = RES ? p.res : nullptr;
+    float rf_in = 1.0f;
+    if constexpr (FUSE && MODE != 0 && NORM) {
         float* const s_out = RES && blockIdx.x == 0 ? p.s_out : nullptr;
-        row_produce<MODE, NORM, PROD>(p.h, res, s_out, p.gain, p.eps, K, tid, 1, s_pair, &s_rf, sact, K, sxd);
-        consumer_bar<kRplWarps * 32>();
+        rf_in = row_rms_scale(p.h, res_in, s_out, K, p.eps, tid, 1, s_pair, &s_rf);
     }
     const uint32_t sact_a = smem_u32(sact), sxd_a = smem_u32(sxd);
     const int slot = warp >> 2, qw = warp & 3;   // this warp's slot and quarter of a stage
@@ -432,6 +435,31 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
         for (int j = 0; j < nsl; ++j) {
             const int64_t t = int64_t(g) * nsl + j;
             if (int(t % kRplSlots) != slot) continue;
+            if constexpr (FUSE && MODE != 0) {
+                if (g == 0) {
+                    // this stage's 1024 values: 256 float4 groups, two a thread
+                    // of the warp group (8 lanes a block, as in act_quant)
+                    const int tg = qw * 32 + lane;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int64_t gi = int64_t(j) * (kRplKS / 4) + tg + 128 * i;
+                        const float4 v = PROD == kProdSwiglu ? load_swiglu4(p.h, K, gi)
+                                                             : load_input4(p.h, res_in, nullptr, gi);
+                        float x[4] = {v.x, v.y, v.z, v.w};
+                        float gg[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+                        if (NORM && p.gain) {
+                            const int4 g4 = ldg_nc_v4(p.gain + 4 * gi);
+                            gg[0] = __int_as_float(g4.x);
+                            gg[1] = __int_as_float(g4.y);
+                            gg[2] = __int_as_float(g4.z);
+                            gg[3] = __int_as_float(g4.w);
+                        }
+                        produce_group<MODE, NORM>(x, gg, p.gain != nullptr, rf_in, gi, true, sact, K, sxd);
+                    }
+                    // the group's four warps (named barrier 2 + slot)
+                    asm volatile("bar.sync %0, 128;" ::"r"(2 + slot) : "memory");
+                }
+            }
             if (ok) ok = mbar_wait(&full[slot], uint32_t((t / kRplSlots) & 1), p.err);
             ok = __all_sync(0xffffffffu, ok);
             if (ok && lane < nr) {
