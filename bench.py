@@ -255,8 +255,8 @@ DECODE_KERNEL_SOURCES = ("common.cuh", "launch.h", "gemv.cuh", "gemv_row.cuh", "
 
 # The kernel each mode's fused decode launch runs (the layer's K are all
 # multiples of 1024 and at most 16384, which the row-per-lane kernel takes)
-FUSED_KERNEL = {"f32": "gemv_rpl_kernel<0,1,1,0,0>", "i8": "gemv_rpl_kernel<1,1,1,0,0>",
-                "i8x2": "gemv_rpl_kernel<2,1,1,0,0>"}
+FUSED_KERNEL = {"f32": "gemv_rpl_kernel<0,1,1,0,0,0>", "i8": "gemv_rpl_kernel<1,1,1,0,0,0>",
+                "i8x2": "gemv_rpl_kernel<2,1,1,0,0,0>"}
 
 
 def kernel_source_hash():
