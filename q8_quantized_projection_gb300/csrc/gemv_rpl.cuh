@@ -429,9 +429,11 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
         float acc[R];
 #pragma unroll
         for (int m = 0; m < R; ++m) acc[m] = 0.0f;
-        DF accd[R];   // f32 mode: each row's sum in units of 2^(E - 30), an f32 pair
+        // f32 mode: each row's sum in units of 2^(E - 30), an f32 pair, as two
+        // chains (even and odd blocks, added at the row group's end)
+        DF accd[R][2];
 #pragma unroll
-        for (int m = 0; m < R; ++m) accd[m] = DF{0.0f, 0.0f};
+        for (int m = 0; m < R; ++m) accd[m][0] = accd[m][1] = DF{0.0f, 0.0f};
         for (int j = 0; j < nsl; ++j) {
             const int64_t t = int64_t(g) * nsl + j;
             if (int(t % kRplSlots) != slot) continue;
@@ -475,7 +477,8 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                 const int4 s8 = lds128(st + uint32_t(C::kW + lane * 64 + ((qw ^ ((lane >> 1) & 3)) << 4)));
                 const uint32_t sh[4] = {uint32_t(s8.x), uint32_t(s8.y), uint32_t(s8.z), uint32_t(s8.w)};
                 if constexpr (MODE == 0) {
-#pragma unroll 1
+                    // (two blocks in flight at one row; at two rows that spills)
+#pragma unroll(R == 1 ? 2 : 1)
                     for (int b = 0; b < 8; ++b) {
                         const int B = qw * 8 + b;
                         const uint32_t wr = st + uint32_t((B >> 2) * (kRplRows * 128) + lane * 128);
@@ -501,7 +504,10 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                             }
                             const float f = __fmul_rn(
                                 sw, __uint_as_float(lds32(sxd_a + uint32_t((m * (C::kMaxK / Q8_QK) + blk) * 4))));
-                            accd[m] = df_add(accd[m], scaled_pair_split(f, fix_dot32_split(w0, w1, fx)));
+                            // (one chain at two rows: the loop is not unrolled there)
+                            constexpr int kMask = R == 1 ? 1 : 0;
+                            accd[m][b & kMask] =
+                                df_add(accd[m][b & kMask], scaled_pair_split(f, fix_dot32_split(w0, w1, fx)));
                         }
                     }
                 } else {
@@ -555,7 +561,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
             // or the exact pair (f64)
             DF* const psd = reinterpret_cast<DF*>(psum);
 #pragma unroll
-            for (int m = 0; m < R; ++m) psd[(warp * R + m) * kRplRows + lane] = accd[m];
+            for (int m = 0; m < R; ++m) psd[(warp * R + m) * kRplRows + lane] = df_add(accd[m][0], accd[m][1]);
             consumer_bar<kRplWarps * 32>();
             if (ok && tid < kRplRows * R) {
                 const int l = tid % kRplRows, m = tid / kRplRows;
