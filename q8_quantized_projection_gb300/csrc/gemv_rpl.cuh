@@ -169,10 +169,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
     static_assert(PROD == kProdPlain || FUSE, "producer kinds belong to the fused producer");
     static_assert(!KV || (FUSE && PROD == kProdPlain), "the KV-row epilogue: fused plain decode step");
     static_assert(!FUSE || kRplWarps * 32 == kProdThreads, "fused producer needs kProdThreads consumers");
-    // (the f32 head keeps the decode kernel: at K = 4096 its warps hold their
-    // activation block in registers for the launch, where this kernel reloads
-    // a block's planes at every row group; measured 98.5 against 101.0 us)
-    static_assert(!ARGMAX || (!FUSE && MODE != 0), "the arg-max epilogue: int8 plain projections");
+    static_assert(!ARGMAX || (!FUSE && (MODE != 0 || R == 1)), "the arg-max epilogue: plain projections");
     using C = RplCfg<MODE, R, FUSE, ARGMAX>;
     constexpr bool RES = PROD == kProdResidual;
     constexpr bool NORM = PROD != kProdSwiglu;
@@ -569,10 +566,17 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                     DF sum = psd[m * kRplRows + l];
                     for (int w = 1; w < kRplWarps; ++w) sum = df_add(sum, psd[(w * R + m) * kRplRows + l]);
                     const int sc = s_emax[m][kRplWarps] - 30;   // in [-156, 98]
-                    if (p.out_f64) {
+                    if (ARGMAX || p.out_f64) {
                         // exact: a power of two well inside the f64 range
-                        reinterpret_cast<double*>(p.y)[m * N + rg0 + l] =
+                        const double val =
                             (double(sum.hi) + double(sum.lo)) * __longlong_as_double((long long)(sc + 1023) << 52);
+                        if (p.y) {
+                            if (p.out_f64)
+                                reinterpret_cast<double*>(p.y)[m * N + rg0 + l] = val;
+                            else
+                                reinterpret_cast<float*>(p.y)[m * N + rg0 + l] = float(val);
+                        }
+                        if constexpr (ARGMAX) argmax_keep(bv, bi, val, rg0 + l);
                     } else {
                         const float yv = __fmul_rn(__fmul_rn(__fadd_rn(sum.hi, sum.lo), pow2i(sc >> 1)),
                                                    pow2i(sc - (sc >> 1)));
