@@ -168,8 +168,9 @@ q8_status act_quant_swiglu(int mode, const float* gu, int64_t rows, int64_t K, v
  * once for a group of rows: up to 8 rows (one-word) or 4 (two-word) a pass,
  * with a weight row per lane when K % 1024 == 0 (f32: one row up to 16384
  * values, or two up to 8192); from 9 (one-word), 5 (two-word) or 4 (f32) rows
- * with K % 256 == 0 one pass on the tensor cores; f32 below 4 rows otherwise
- * runs one row a pass, its arithmetic being the bound).
+ * with K % 256 == 0 one pass on the tensor cores, except f32 at 4 rows where
+ * two row pairs fit; f32 below 4 rows otherwise runs one row a pass, its
+ * arithmetic being the bound).
  *   y[m][n] for m < rows, n < N; y is float, or double when mode is
  *   Q8_ACT_F32 and out_f64 != 0.  1 <= rows <= Q8_MAX_ROWS.
  */
