@@ -248,7 +248,7 @@ q8_status q8_proj_fused_swiglu(int mode, const int8_t* q, const uint16_t* s, int
  * to 16 rows and N <= 131072) rows on, with K % 256 == 0, the head is read
  * once for all rows on the tensor cores; below that, once per group of up to
  * 8 (one-word) or 4 (two-word) rows (with a weight row per lane when
- * K % 1024 == 0), and f32 once per row.
+ * K % 1024 == 0), and f32 once per row pair (K % 1024 == 0, K <= 8192) or row.
  *   tok     int32 [rows]: the smallest n holding the row's maximum logit; NaN
  *           logits are never the maximum, and a row of NaN gives 0
  *   maxval  double [rows] or NULL: that maximum (NaN for a row of NaN)

@@ -97,13 +97,13 @@ struct KvArgs {
     float* v_cache = nullptr;
 };
 
-// Runs the CUDA-core projection over groups of gemv_group_rows(mode, K, ...)
+// Runs the CUDA-core projection over groups of gemv_group_rows(mode, K)
 // activation rows (each group one launch reading the weights once).
 q8_status run_projection(int mode, const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                          const void* xq, const float* xd, int64_t rows, void* y, int out_f64,
                          int32_t* tok, double* maxval, void* ws, const LaunchCtx& ctx) {
     const int64_t nb = K / Q8_QK;
-    const int group = gemv_group_rows(mode, K, tok != nullptr);
+    const int group = gemv_group_rows(mode, K);
     const size_t elem = (mode == Q8_ACT_F32) ? 4 : 1;
     const size_t ysz = (mode == Q8_ACT_F32 && out_f64) ? 8 : 4;
     for (int64_t g0 = 0; g0 < rows; g0 += group) {
@@ -135,7 +135,7 @@ q8_status project_dispatch(int mode, const int8_t* q, const uint16_t* s, int64_t
                            const LaunchCtx& ctx) {
     // (f32 at 4 rows runs as two row pairs where the row-per-lane kernel holds
     // a pair: 2 x 87 against 197 us for the d = 4096 layer)
-    const bool f32_pairs = mode == Q8_ACT_F32 && rows == 4 && gemv_group_rows(mode, K, false) == 2;
+    const bool f32_pairs = mode == Q8_ACT_F32 && rows == 4 && gemv_group_rows(mode, K) == 2;
     if (!f32_pairs && (!out_f64 || mode == Q8_ACT_F32) && rows >= chunk_min_rows(mode) &&
         chunk_supported(mode, N, K, rows))
         return launched(launch_chunk(mode, q, s, N, K, xq, xd, rows, y, out_f64 != 0, ctx));

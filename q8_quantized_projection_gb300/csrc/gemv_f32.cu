@@ -1,7 +1,7 @@
 // gemv_f32.cu -- instantiations of the CUDA-core projection for activation
 // mode 0: the row-per-lane kernel (gemv_rpl.cuh) for K % 1024 == 0, one row
-// up to 16384 values (plain projections, the LM head's arg-max and fused
-// decode steps) or a pair of rows up to 8192, else the decode kernel
+// up to 16384 values or a pair of rows up to 8192 (plain projections, the LM
+// head's arg-max and fused decode steps), else the decode kernel
 // (gemv_row.cuh: other K; one row a launch, the mode being bound by
 // instruction issue), and the slice-major kernel (gemv.cuh) for K beyond the
 // decode kernel's part sums.  One file per mode so the build runs in parallel.
@@ -12,11 +12,9 @@ namespace q8 {
 
 template <bool ARGMAX>
 static cudaError_t dispatch_rows(const GemvArgs& a, const LaunchCtx& ctx) {
-    // a weight row a lane (K % 1024 == 0), plain or with the arg-max (one row)
+    // a weight row a lane (K % 1024 == 0), plain or with the arg-max
     if (a.rows <= 1 && rpl_fits(a)) return launch_gemv_rpl_t<0, 1, false, kProdPlain, false, ARGMAX>(a, ctx);
-    if constexpr (!ARGMAX) {
-        if (a.rows == 2 && rpl_fits(a)) return launch_gemv_rpl_t<0, 2>(a, ctx);
-    }
+    if (a.rows == 2 && rpl_fits(a)) return launch_gemv_rpl_t<0, 2, false, kProdPlain, false, ARGMAX>(a, ctx);
     if (a.rows <= 1 && row_kernel_fits<0, 1>(a.K)) return launch_gemv_row_t<0, 1, ARGMAX>(a, ctx);
     return launch_gemv_t<0, 4, ARGMAX>(a, ctx);
 }

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
     static_assert(PROD == kProdPlain || FUSE, "producer kinds belong to the fused producer");
     static_assert(!KV || (FUSE && PROD == kProdPlain), "the KV-row epilogue: fused plain decode step");
     static_assert(!FUSE || kRplWarps * 32 == kProdThreads, "fused producer needs kProdThreads consumers");
-    static_assert(!ARGMAX || (!FUSE && (MODE != 0 || R == 1)), "the arg-max epilogue: plain projections");
+    static_assert(!ARGMAX || !FUSE, "the arg-max epilogue: plain projections");
     using C = RplCfg<MODE, R, FUSE, ARGMAX>;
     constexpr bool RES = PROD == kProdResidual;
     constexpr bool NORM = PROD != kProdSwiglu;

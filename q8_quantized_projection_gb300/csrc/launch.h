@@ -86,9 +86,9 @@ constexpr int64_t kFusedMaxK = 16384;
 constexpr int gemv_max_rows(int mode) { return mode == 0 ? 1 : mode == 1 ? 8 : 4; }
 // The rows one such launch takes for a projection with K values: f32 pairs
 // where the row-per-lane kernel holds both rows in shared memory (K % 1024 ==
-// 0, K <= 8192, no arg-max), else gemv_max_rows(mode).
-constexpr int gemv_group_rows(int mode, int64_t K, bool argmax) {
-    return (mode == 0 && !argmax && K % 1024 == 0 && K <= 8192) ? 2 : gemv_max_rows(mode);
+// 0, K <= 8192; plain or with the arg-max), else gemv_max_rows(mode).
+constexpr int gemv_group_rows(int mode, int64_t K) {
+    return (mode == 0 && K % 1024 == 0 && K <= 8192) ? 2 : gemv_max_rows(mode);
 }
 
 // tensor-core chunk path (chunk.cu): modes 1 and 2, K % 256 == 0
