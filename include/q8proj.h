@@ -245,7 +245,8 @@ q8_status q8_proj_fused_swiglu(int mode, const int8_t* q, const uint16_t* s, int
  * norm, the LM head and the arg-max"; decode_batch_head: one token per
  * sequence).  Modes Q8_ACT_F32 (logits to f64 accuracy) and Q8_ACT_I8 /
  * Q8_ACT_I8X2 (f32 logits).  From 9 (one-word), 5 (two-word) or 6 (f32, up
- * to 16 rows and N <= 131072) rows on, with K % 256 == 0, the head is read
+ * to 16 rows and N <= 131072; 8 where f32 row pairs fit, K % 1024 == 0 and
+ * K <= 8192) rows on, with K % 256 == 0, the head is read
  * once for all rows on the tensor cores; below that, once per group of up to
  * 8 (one-word) or 4 (two-word) rows (with a weight row per lane when
  * K % 1024 == 0), and f32 once per row pair (K % 1024 == 0, K <= 8192) or row.

@@ -437,7 +437,10 @@ q8_status head_argmax(int mode, const int8_t* q, const uint16_t* s, int64_t N, i
     // kArgmaxGroupRows rows and kMaxGrid tiles (its candidates use the
     // CUDA-core layout of the workspace)
     const bool f32_fits = mode != Q8_ACT_F32 || (rows <= kArgmaxGroupRows && (N + 127) / 128 <= kMaxGrid);
-    if (f32_fits && rows >= chunk_min_head_rows(mode) && chunk_supported(mode, N, K, rows))
+    // (f32 row pairs, where they fit, beat the tensor cores up to 7 rows)
+    const int64_t min_rows =
+        (mode == Q8_ACT_F32 && gemv_group_rows(mode, K) == 2) ? 8 : chunk_min_head_rows(mode);
+    if (f32_fits && rows >= min_rows && chunk_supported(mode, N, K, rows))
         return launched(launch_chunk_argmax(mode, q, s, N, K, xq, xd, rows, logits, tok, maxval, workspace,
                                             ctx));
     return run_projection(mode, q, s, N, K, xq, xd, rows, logits, mode == Q8_ACT_F32 ? 1 : 0, tok,
