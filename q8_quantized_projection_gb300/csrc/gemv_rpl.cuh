@@ -525,8 +525,21 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                         const float xd = __uint_as_float(lds32(da + uint32_t(m * (kRplKS / Q8_QK) * 4 + 4 * b)));
                         float fi;
                         if constexpr (MODE == 1) {
-                            const int isum = dot16_i8(w0, lds128(xm)) + dot16_i8(w1, lds128(xm + 16u));
-                            fi = small_int_to_float(isum);   // |isum| < 2^19
+                            // one dp4a chain started at the bits of 1.5 * 2^23:
+                            // read as a float it is 1.5 * 2^23 + isum exactly
+                            // (|isum| < 2^19), so one subtraction gives
+                            // float(isum)
+                            const int4 a0 = lds128(xm), a1 = lds128(xm + 16u);
+                            int acc_i = 0x4B400000;
+                            acc_i = __dp4a(w0.x, a0.x, acc_i);
+                            acc_i = __dp4a(w0.y, a0.y, acc_i);
+                            acc_i = __dp4a(w0.z, a0.z, acc_i);
+                            acc_i = __dp4a(w0.w, a0.w, acc_i);
+                            acc_i = __dp4a(w1.x, a1.x, acc_i);
+                            acc_i = __dp4a(w1.y, a1.y, acc_i);
+                            acc_i = __dp4a(w1.z, a1.z, acc_i);
+                            acc_i = __dp4a(w1.w, a1.w, acc_i);
+                            fi = __fsub_rn(__int_as_float(acc_i), 12582912.0f);
                         } else {
                             const uint32_t xl = xm + lo;
                             const int isum = dot16_i8x2(w0, lds128(xm), lds128(xl)) +
