@@ -454,8 +454,9 @@ def _planted_head(n, k, rows, seed):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("n,k,rows", [(20000, 1024, 1), (20000, 1024, 3), (20000, 2048, 8),
-                                      (20000, 1024, 16), (5000, 4096, 20), (8, 256, 1)])
+@pytest.mark.parametrize("n,k,rows", [(20000, 1024, 1), (20000, 1024, 3), (20000, 1024, 6),
+                                      (20000, 2048, 8), (20000, 1024, 16), (5000, 4096, 20),
+                                      (8, 256, 1)])
 def test_head_argmax_planted(mode, n, k, rows):
     q, s, h, pos = _planted_head(n, k, rows, seed=n + k + rows)
     x, _ = orc.rmsnorm(h)
