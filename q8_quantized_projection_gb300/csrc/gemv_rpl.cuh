@@ -1,10 +1,13 @@
-// gemv_rpl.cuh -- batched projection of a few activation rows (3-8 one-word,
-// 2-4 two-word) with a weight row a lane.
+// gemv_rpl.cuh -- the projection with a weight row a lane: the decode step
+// (one row, with the RMSNorm -> quant producer and the KV-row epilogue fused or
+// not), batches of up to 8 one-word or 4 two-word rows, f32 rows one or two at
+// a time, and the LM head's arg-max; K % 1024 == 0.
 //
-// The decode kernel gives each lane 16-byte chunks of a row's part and sums a
-// row over the warp with a butterfly per item; with several activation rows
-// that butterfly and the per-chunk scale products dominate its instruction
-// count.  Here lane l of a warp owns weight row l of a group of 32 rows: it
+// The decode kernel (gemv_row.cuh) gives each lane 16-byte chunks of a row's
+// part and sums a row over the warp with a butterfly per item; with several
+// activation rows that butterfly and the per-chunk scale products dominate its
+// instruction count.  Here lane l of a warp owns weight row l of a group of 32
+// rows: it
 // reads its row's 32-value blocks and block scales from shared memory, each
 // activation row's block (the same address for every lane: one broadcast
 // load) and its scale, and keeps R running sums in registers.  No lane-to-lane
@@ -17,7 +20,9 @@
 //   - the rows' block scales, 32 rows x 64 bytes (64-byte swizzle, same
 //     reason);
 //   - the activation rows' codes (four tiles of R rows x 256 bytes a plane, one
-//     3-D box) and block scales (R rows x 32).
+//     3-D box) and block scales (R rows x 32), unless the rows are resident in
+//     shared memory for the launch: the fused producer's row, and every f32
+//     launch (fixed-point planes, see RplCfg).
 // So a stage takes 4 TMA instructions (5 two-word): the producer's issue rate,
 // which shares the memory-instruction queue with the consumers' shared-memory
 // loads, kept up with HBM only once the eight weight tiles were one box.
