@@ -225,6 +225,32 @@ def test_batched_row_groups(mode, rows, n, k):
 
 
 @pytest.mark.parametrize("mode", MODES)
+def test_largest_resident_row(mode):
+    """K = 16384, the longest row a fused launch (and a one-row f32 launch)
+    keeps in shared memory: q8_proj and q8_proj_fused at one row against the
+    oracle, and the fused result bitwise equal to act_quant + q8_proj."""
+    n, k = 300, 16384
+    rng = np.random.default_rng(4242)
+    q, s = synth.q8_weights(rng, n, k)
+    h = synth.activations(rng, 1, k)
+    g = synth.gain(rng, k)
+    x, _ = orc.rmsnorm(h, g, 1e-5)
+    y_o, norm = orc.project(mode, q, s, orc.quantize(mode, x))
+    qd, sd = upload_weights(q, s)
+    t = torch()
+    ws = t.empty(native.q8_proj_fused_workspace(mode, 1, k), dtype=t.uint8, device="cuda")
+    y = t.empty((1, n), dtype=t.float32, device="cuda")
+    native.q8_proj_fused(mode, qd, sd, dev(h), y, ws, gain=dev(g), eps=1e-5)
+    check_close(mode, host(y), y_o, norm, what=f"fused {mode} K={k}")
+    xq, xd = native.activation_buffers(mode, 1, k, device="cuda")
+    native.act_quant(mode, dev(h), xq, xd, norm=True, gain=dev(g), eps=1e-5)
+    y2 = t.empty((1, n), dtype=t.float32, device="cuda")
+    native.q8_proj(mode, qd, sd, xq, xd, 1, y2)
+    assert np.array_equal(host(y).view(np.uint32), host(y2).view(np.uint32))
+    no_device_error()
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_proj_deterministic_and_zero(mode):
     rng = np.random.default_rng(77)
     n, k, rows = 500, 4096, 4
