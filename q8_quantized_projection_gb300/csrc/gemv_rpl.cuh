@@ -79,12 +79,13 @@ struct RplCfg {
     static constexpr int kXD = kResAct ? 0 : R * (kRplKS / Q8_QK) * 4;   // [R][32] f32
     // the resident rows: [plane][kMaxK] codes (int8 modes, one row) or
     // [R][kMaxK / 32][128] fixed-point planes (f32), then [R][kMaxK / 32]
-    // block scales (int8) or block factors (f32)
+    // block scales (int8) or block factors (f32), then (f32) [R][kMaxK / 32]
+    // int16 block binades
     // the longest resident row: f32 pairs of rows up to 8192 values (both rows'
     // planes beside the ring), else kFusedMaxK
     static constexpr int kMaxK = (MODE == 0 && R == 2) ? 8192 : int(kFusedMaxK);
     static constexpr int kActBytes = MODE == 0 ? R * 4 * kMaxK : 2 * kMaxK;
-    static constexpr int kAct = kResAct ? kActBytes + R * (kMaxK / Q8_QK) * 4 : 0;
+    static constexpr int kAct = kResAct ? kActBytes + R * (kMaxK / Q8_QK) * (MODE == 0 ? 6 : 4) : 0;
     static constexpr int kStage = (kW + kS + kX + kXD + 1023) / 1024 * 1024;
     // The row group's partial sums are added by a combining warp through two
     // buffers where that pays (one-word 8 rows: 69.8 against 71.9 us a layer
@@ -196,6 +197,12 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
     uint64_t* pempty = pfull + 2;          // [2] and added up (kComb)
     unsigned char* sact = reinterpret_cast<unsigned char*>(pempty + 2);   // the resident row
     float* sxd = reinterpret_cast<float*>(sact + C::kActBytes);
+    short* const seb = reinterpret_cast<short*>(sxd + R * (C::kMaxK / Q8_QK));   // f32: block binades
+    // f32 rows longer than 4096 values (one row): the prologue forms x and the
+    // block binades only, and the warp group that consumes a stage in the first
+    // row group builds that stage's planes in place just before (`down`:
+    // 18.4 -> 17.7 us; shorter rows convert faster in the prologue)
+    const bool lazy = MODE == 0 && R == 1 && p.K > 4096;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, c = blockIdx.x;
@@ -376,6 +383,13 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             const int eb = binade(amax);
+            if (lazy) {
+                // x in place of s (or written there), and the block's binade
+                float* const xw = reinterpret_cast<float*>(plm) + k;
+                *reinterpret_cast<float4*>(xw) = make_float4(xs[0], xs[1], xs[2], xs[3]);
+                *reinterpret_cast<float4*>(xw + 4) = make_float4(xs[4], xs[5], xs[6], xs[7]);
+                if (q == 0) seb[b] = short(eb);
+            } else {
             // X = rint(x * 2^(30 - eb)) as in fix_chunk32, two words a plane
             const int sh = 30 - eb;
             const float s1 = pow2i(sh >> 1), s2 = pow2i(sh - (sh >> 1));
@@ -393,6 +407,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
             for (int j = 0; j < 4; ++j)
                 rpl_sts64(base + uint32_t((((2 * j + (q >> 1)) ^ (b & 7)) << 4)), uint32_t(pl[0][j]),
                           uint32_t(pl[1][j]));
+            }
             if (q == 0) se[b] = eb;
             emax = max(emax, eb);
         }
@@ -439,6 +454,34 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
         for (int j = 0; j < nsl; ++j) {
             const int64_t t = int64_t(g) * nsl + j;
             if (int(t % kRplSlots) != slot) continue;
+            if constexpr (MODE == 0) {
+                if (lazy && g == 0) {
+                    // this stage's 32 blocks: X = rint(x * 2^(30 - E_b)) as in
+                    // fix_chunk32, four lanes a block, in place of x (the
+                    // block's lanes share a warp), then the group's barrier
+                    const int tg = qw * 32 + lane;
+                    const int b = j * (kRplKS / Q8_QK) + (tg >> 2), q = tg & 3;
+                    const float* const xr = reinterpret_cast<const float*>(sact) + int64_t(b) * Q8_QK + 8 * q;
+                    const float4 x0 = *reinterpret_cast<const float4*>(xr);
+                    const float4 x1 = *reinterpret_cast<const float4*>(xr + 4);
+                    const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    const int sh = 30 - int(seb[b]);
+                    const float s1 = pow2i(sh >> 1), s2 = pow2i(sh - (sh >> 1));
+                    int X[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) X[e] = rint_scaled30(__fmul_rn(xs[e], s1), s2);
+                    int pl[2][4];
+                    byte_planes4(X[0], X[1], X[2], X[3], pl[0][0], pl[0][1], pl[0][2], pl[0][3]);
+                    byte_planes4(X[4], X[5], X[6], X[7], pl[1][0], pl[1][1], pl[1][2], pl[1][3]);
+                    __syncwarp();   // the block's x read by its four lanes before the planes overwrite it
+                    const uint32_t base = smem_u32(sact) + uint32_t(b) * 128u + uint32_t(8 * (q & 1));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        rpl_sts64(base + uint32_t((((2 * i + (q >> 1)) ^ (b & 7)) << 4)), uint32_t(pl[0][i]),
+                                  uint32_t(pl[1][i]));
+                    asm volatile("bar.sync %0, 128;" ::"r"(2 + slot) : "memory");   // the group's four warps
+                }
+            }
             if constexpr (FUSE && MODE != 0) {
                 if (g == 0) {
                     // this stage's 1024 values: 256 float4 groups, two a thread
