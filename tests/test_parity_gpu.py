@@ -153,12 +153,15 @@ def test_proj_parity(mode, n, k, rows):
     check_close(mode, host(y2), y_o, norm, what=f"chunk {mode} {n}x{k} rows={rows}")
 
 
-@pytest.mark.parametrize("n,k,rows", [(300, 4096, 8), (64, 14336, 13), (200, 2048, 40)])
+@pytest.mark.parametrize("n,k,rows", [(300, 4096, 2), (64, 14336, 2), (300, 4096, 8), (64, 14336, 13),
+                                      (200, 2048, 40)])
 def test_f32_batch_binade_spread(n, k, rows):
     """f32 activations whose 32-value blocks lie up to 2^130 apart within a
-    row (and one all-zero row), through the batched path (tensor cores from 6
-    rows: each column's sum is kept relative to the largest block binade seen
-    so far and rescaled when a larger one comes; blocks far below are
+    row (and one all-zero row): at 2 rows the row-per-lane kernel (a row pair
+    at K = 4096; one row a launch, planes built stage by stage, at K =
+    14336), each block scaled to its row's largest binade; from 8 rows the
+    tensor cores, each column's sum kept relative to the largest block binade
+    seen so far and rescaled when a larger one comes (blocks far below are
     negligible): within 1e-9 of the norm, f32 and f64 outputs."""
     rng = np.random.default_rng(77 + n + k + rows)
     q, s = synth.q8_weights(rng, n, k)
