@@ -58,8 +58,7 @@ bool make_map3(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const u
 
 constexpr int kRplWarps = 16;                      // consumer warps
 constexpr int kRplRows = 32;                       // weight rows a group: a lane each
-constexpr int kRplKS = 1024;                       // bytes of K a stage
-constexpr int kRplSlots = 4;                       // ring slots, four consumer warps each
+constexpr int kRplGroups = 4;                      // consumer warp groups of four warps
 
 // FUSE: one activation row, produced (RMSNorm -> quant, or by PROD the
 // residual added before the norm, or the SwiGLU of a gate+up row) by the
@@ -71,12 +70,27 @@ constexpr int kRplSlots = 4;                       // ring slots, four consumer 
 // to the row's largest binade E (fused or not).
 template <int MODE, int R, bool FUSE = false, bool ARGMAX = false>
 struct RplCfg {
-    static constexpr bool kResAct = FUSE || MODE == 0;          // the row resident in shared memory
+    // A stage: 1024 values of K in a ring of four slots, one per warp group;
+    // the one-row int8 launches (fused or not: the row is resident, so two TMA
+    // instructions a stage) take 512 values in eight slots, warp group g
+    // owning slots g and g + 4, so that a group's next stage loads while it
+    // works on the current one (fused layer one-word 50.5 -> 47.5 us, two-word
+    // 53.2 -> 49.8 us; launches that copy activations every stage lose at that
+    // size: twice the TMA instructions a byte).  Fused and plain one-row
+    // launches share the schedule, so their results stay bitwise equal.
+    static constexpr bool kHalf = MODE != 0 && R == 1 && !ARGMAX;
+    static constexpr int kKS = kHalf ? 512 : 1024;           // values of K a stage
+    static constexpr int kSlots = kHalf ? 8 : 4;             // ring slots
+    static constexpr int kBPW = kKS / Q8_QK / kRplGroups;    // blocks a warp takes of a stage
+    // the row resident in shared memory: fused, f32, and one-row int8 (not the
+    // LM head's arg-max, which keeps the 1024-value stages: 83.2 against
+    // 84.3 us with half stages)
+    static constexpr bool kResAct = FUSE || MODE == 0 || kHalf;
     static constexpr int kPlanes = MODE == 2 ? 2 : 1;
-    static constexpr int kW = kRplRows * kRplKS;                // 8 tiles of [32][128]
-    static constexpr int kS = kRplRows * (kRplKS / Q8_QK) * 2;  // [32][64] bytes of f16 scales
-    static constexpr int kX = kResAct ? 0 : kPlanes * R * kRplKS;        // [plane][4 tiles][R][256]
-    static constexpr int kXD = kResAct ? 0 : R * (kRplKS / Q8_QK) * 4;   // [R][32] f32
+    static constexpr int kW = kRplRows * kKS;                // 8 tiles of [32][128]
+    static constexpr int kS = kRplRows * (kKS / Q8_QK) * 2;  // [32][64] bytes of f16 scales
+    static constexpr int kX = kResAct ? 0 : kPlanes * R * kKS;        // [plane][4 tiles][R][256]
+    static constexpr int kXD = kResAct ? 0 : R * (kKS / Q8_QK) * 4;   // [R][32] f32
     // the resident rows: [plane][kMaxK] codes (int8 modes, one row) or
     // [R][kMaxK / 32][128] fixed-point planes (f32), then [R][kMaxK / 32]
     // block scales (int8) or block factors (f32), then (f32) [R][kMaxK / 32]
@@ -97,7 +111,7 @@ struct RplCfg {
     static constexpr int kPsum = kRplWarps * R * kRplRows * (MODE == 0 ? 8 : 4);
     static constexpr int kBufs = kComb ? 2 : 1;
     static constexpr size_t kSmem =
-        size_t(kRplSlots) * kStage + kBufs * kPsum + (2 * kRplSlots + 4) * 8 + kAct + 1024;
+        size_t(kSlots) * kStage + kBufs * kPsum + (2 * kSlots + 4) * 8 + kAct + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory");
     static_assert(!FUSE || (R == 1 && !kComb), "fused producer: one row");
     static_assert(MODE != 0 || R <= 2, "f32 mode: one or two rows");
@@ -111,10 +125,12 @@ inline bool rpl_al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1
 inline bool rpl_fits(const GemvArgs& a) {
     const auto al16 = rpl_al16;
     // f32 mode: one row up to kFusedMaxK values or a pair up to 8192, resident
-    // in shared memory (f64 output allowed)
-    const bool f32ok = a.mode != 0 || (a.rows == 1 && a.K <= kFusedMaxK) || (a.rows == 2 && a.K <= 8192);
+    // in shared memory (f64 output allowed); int8: one row up to kFusedMaxK
+    // values, resident
+    const bool f32ok = a.mode != 0 ? (a.rows > 1 || a.K <= kFusedMaxK)
+                                   : (a.rows == 1 && a.K <= kFusedMaxK) || (a.rows == 2 && a.K <= 8192);
     // y may be NULL for the arg-max (the LM head without logits)
-    return f32ok && a.rows >= 1 && a.K >= kRplKS && a.K % kRplKS == 0 && a.N <= (int64_t(1) << 31) &&
+    return f32ok && a.rows >= 1 && a.K >= 1024 && a.K % 1024 == 0 && a.N <= (int64_t(1) << 31) &&
            (a.y || a.tok) && (!a.out_f64 || a.mode == 0) && !a.h && !a.k_cache && al16(a.q) && al16(a.s) &&
            al16(a.act) && (a.mode == 0 || al16(a.xd)) && a.plane % 16 == 0 && (!a.tok || al16(a.ws));
 }
@@ -122,7 +138,7 @@ inline bool rpl_fits(const GemvArgs& a) {
 // A fused decode step (one row, the producer in the kernel; with or without
 // the KV-row epilogue) in whole stages, with its row in shared memory.
 inline bool rpl_fits_fused(const GemvArgs& a) {
-    return a.rows == 1 && a.h && a.K >= kRplKS && a.K % kRplKS == 0 && a.K <= kFusedMaxK &&
+    return a.rows == 1 && a.h && a.K >= 1024 && a.K % 1024 == 0 && a.K <= kFusedMaxK &&
            a.N <= (int64_t(1) << 31) && a.y && (!a.out_f64 || a.mode == 0) && !a.tok && rpl_al16(a.q) &&
            rpl_al16(a.s) && rpl_al16(a.h);
 }
@@ -190,10 +206,10 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
     // 1024-byte alignment for the swizzled weight tiles
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* psum = reinterpret_cast<float*>(smem + size_t(kRplSlots) * C::kStage);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kRplSlots) * C::kStage + C::kBufs * C::kPsum);
-    uint64_t* empty = full + kRplSlots;
-    uint64_t* pfull = empty + kRplSlots;   // [2] a row group's partial sums written (kComb)
+    float* psum = reinterpret_cast<float*>(smem + size_t(C::kSlots) * C::kStage);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(C::kSlots) * C::kStage + C::kBufs * C::kPsum);
+    uint64_t* empty = full + C::kSlots;
+    uint64_t* pfull = empty + C::kSlots;   // [2] a row group's partial sums written (kComb)
     uint64_t* pempty = pfull + 2;          // [2] and added up (kComb)
     unsigned char* sact = reinterpret_cast<unsigned char*>(pempty + 2);   // the resident row
     float* sxd = reinterpret_cast<float*>(sact + C::kActBytes);
@@ -212,12 +228,12 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
     const int64_t g0 = ng_all * c / G, g1 = ng_all * (c + 1) / G;
     const int64_t r0 = g0 * kRplRows, r1 = min64(N, g1 * kRplRows);
     const int ngroups = int(g1 - g0);
-    const int nsl = int(K / kRplKS);
+    const int nsl = int(K / C::kKS);
     const int64_t nst = int64_t(ngroups) * nsl;
     const int rows = p.rows;
 
     if (tid == 0) {
-        for (int i = 0; i < kRplSlots; ++i) {
+        for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 4);   // the slot's four warps
         }
@@ -237,27 +253,29 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
             // (a resident row: no activation copies; the weights never wait on
             // the previous kernel)
             auto acts = [&](int64_t t) {
-                const int j = int(t % nsl), slot = int(t % kRplSlots);
+                const int j = int(t % nsl), slot = int(t % C::kSlots);
                 unsigned char* st = smem + size_t(slot) * C::kStage;
                 // [4 chunks][R rows][256 bytes] a plane, one box each
-                rpl_tma3d(st + C::kW + C::kS, &tm_xh, 0, 0, j * 4, &full[slot]);
-                if constexpr (MODE == 2) rpl_tma3d(st + C::kW + C::kS + 4 * R * 256, &tm_xl, 0, 0, j * 4, &full[slot]);
-                rpl_tma2d(st + C::kW + C::kS + C::kX, &tm_xd, j * (kRplKS / Q8_QK), 0, &full[slot]);
+                rpl_tma3d(st + C::kW + C::kS, &tm_xh, 0, 0, j * (C::kKS / 256), &full[slot]);
+                if constexpr (MODE == 2)
+                    rpl_tma3d(st + C::kW + C::kS + (C::kKS / 256) * R * 256, &tm_xl, 0, 0, j * (C::kKS / 256),
+                              &full[slot]);
+                rpl_tma2d(st + C::kW + C::kS + C::kX, &tm_xd, j * (C::kKS / Q8_QK), 0, &full[slot]);
             };
-            const int64_t npre = nst < kRplSlots ? nst : kRplSlots;
+            const int64_t npre = nst < C::kSlots ? nst : C::kSlots;
             const uint64_t pol = policy_evict_first();
             int64_t issued = 0;
             for (int64_t t = 0; t < nst; ++t) {
-                const int g = int(t / nsl), j = int(t % nsl), slot = int(t % kRplSlots);
-                if (t >= kRplSlots &&
-                    !mbar_wait(&empty[slot], uint32_t((t / kRplSlots) - 1) & 1u, p.err))
+                const int g = int(t / nsl), j = int(t % nsl), slot = int(t % C::kSlots);
+                if (t >= C::kSlots &&
+                    !mbar_wait(&empty[slot], uint32_t((t / C::kSlots) - 1) & 1u, p.err))
                     break;
                 const int rg0 = int(r0 + int64_t(g) * kRplRows);
                 mbar_arrive_expect_tx(&full[slot], kTx);
                 unsigned char* st = smem + size_t(slot) * C::kStage;
                 // [8 chunks][32 rows][128 bytes] in one box
-                rpl_tma3d_ef(st, &tm_w, 0, rg0, j * 8, &full[slot], pol);
-                rpl_tma2d_ef(st + C::kW, &tm_s, j * (kRplKS / 16), rg0, &full[slot], pol);
+                rpl_tma3d_ef(st, &tm_w, 0, rg0, j * (C::kKS / 128), &full[slot], pol);
+                rpl_tma2d_ef(st + C::kW, &tm_s, j * (C::kKS / 16), rg0, &full[slot], pol);
                 if constexpr (!C::kResAct) {
                     if (t == npre - 1) {
                         // the first stages' weights are on their way: the
@@ -271,8 +289,8 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                 ++issued;
             }
             // never leave with copies in flight into this CTA's shared memory
-            for (int64_t t = issued > kRplSlots ? issued - kRplSlots : 0; t < issued; ++t)
-                mbar_wait(&full[t % kRplSlots], uint32_t((t / kRplSlots) & 1), p.err);
+            for (int64_t t = issued > C::kSlots ? issued - C::kSlots : 0; t < issued; ++t)
+                mbar_wait(&full[t % C::kSlots], uint32_t((t / C::kSlots) & 1), p.err);
         }
         return;
     }
@@ -428,6 +446,18 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
     // time by the warp group that consumes that stage in the first row group,
     // just before it does (a row-group barrier later makes every stage's codes
     // visible to all groups)
+    if constexpr (MODE != 0 && !FUSE && C::kResAct) {
+        // one int8 row, plain: its codes (and lo plane) and block scales into
+        // shared memory, where the fused launch keeps its produced row
+        const unsigned char* src = static_cast<const unsigned char*>(p.act);
+        for (int64_t i = tid; i < K / 16; i += kRplWarps * 32) {
+            *reinterpret_cast<int4*>(sact + 16 * i) = ldg_nc_v4(src + 16 * i);
+            if constexpr (MODE == 2) *reinterpret_cast<int4*>(sact + K + 16 * i) = ldg_nc_v4(src + p.plane + 16 * i);
+        }
+        for (int64_t i = tid; i < K / Q8_QK / 4; i += kRplWarps * 32)
+            *reinterpret_cast<int4*>(sxd + 4 * i) = ldg_nc_v4(p.xd + 4 * i);
+        consumer_bar<kRplWarps * 32>();
+    }
     const float* const res_in = RES ? p.res : nullptr;
     float rf_in = 1.0f;
     if constexpr (FUSE && MODE != 0 && NORM) {
@@ -435,7 +465,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
         rf_in = row_rms_scale(p.h, res_in, s_out, K, p.eps, tid, 1, s_pair, &s_rf);
     }
     const uint32_t sact_a = smem_u32(sact), sxd_a = smem_u32(sxd);
-    const int slot = warp >> 2, qw = warp & 3;   // this warp's slot and quarter of a stage
+    const int wg = warp >> 2, qw = warp & 3;   // this warp's group and quarter of a stage
     bool ok = true;
     // arg-max: combine thread (m, l)'s best (value, lowest index) over the launch
     double bv = -INFINITY;
@@ -453,14 +483,17 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
         for (int m = 0; m < R; ++m) accd[m][0] = accd[m][1] = DF{0.0f, 0.0f};
         for (int j = 0; j < nsl; ++j) {
             const int64_t t = int64_t(g) * nsl + j;
-            if (int(t % kRplSlots) != slot) continue;
+            if (int(t % kRplGroups) != wg) continue;
+            // (with one slot a group, the slot is the group: a constant)
+            const int slot = C::kSlots == kRplGroups ? wg : int(t % C::kSlots);
             if constexpr (MODE == 0) {
                 if (lazy && g == 0) {
                     // this stage's 32 blocks: X = rint(x * 2^(30 - E_b)) as in
                     // fix_chunk32, four lanes a block, in place of x (the
                     // block's lanes share a warp), then the group's barrier
                     const int tg = qw * 32 + lane;
-                    const int b = j * (kRplKS / Q8_QK) + (tg >> 2), q = tg & 3;
+                    if (tg < C::kKS / 8) {
+                    const int b = j * (C::kKS / Q8_QK) + (tg >> 2), q = tg & 3;
                     const float* const xr = reinterpret_cast<const float*>(sact) + int64_t(b) * Q8_QK + 8 * q;
                     const float4 x0 = *reinterpret_cast<const float4*>(xr);
                     const float4 x1 = *reinterpret_cast<const float4*>(xr + 4);
@@ -479,7 +512,8 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                     for (int i = 0; i < 4; ++i)
                         rpl_sts64(base + uint32_t((((2 * i + (q >> 1)) ^ (b & 7)) << 4)), uint32_t(pl[0][i]),
                                   uint32_t(pl[1][i]));
-                    asm volatile("bar.sync %0, 128;" ::"r"(2 + slot) : "memory");   // the group's four warps
+                    }
+                    asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");   // the group's four warps
                 }
             }
             if constexpr (FUSE && MODE != 0) {
@@ -488,8 +522,8 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                     // of the warp group (8 lanes a block, as in act_quant)
                     const int tg = qw * 32 + lane;
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int64_t gi = int64_t(j) * (kRplKS / 4) + tg + 128 * i;
+                    for (int i = 0; i < C::kKS / 512; ++i) {
+                        const int64_t gi = int64_t(j) * (C::kKS / 4) + tg + 128 * i;
                         const float4 v = PROD == kProdSwiglu ? load_swiglu4(p.h, K, gi)
                                                              : load_input4(p.h, res_in, nullptr, gi);
                         float x[4] = {v.x, v.y, v.z, v.w};
@@ -504,28 +538,39 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                         produce_group<MODE, NORM>(x, gg, p.gain != nullptr, rf_in, gi, true, sact, K, sxd);
                     }
                     // the group's four warps (named barrier 2 + slot)
-                    asm volatile("bar.sync %0, 128;" ::"r"(2 + slot) : "memory");
+                    asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
                 }
             }
-            if (ok) ok = mbar_wait(&full[slot], uint32_t((t / kRplSlots) & 1), p.err);
+            if (ok) ok = mbar_wait(&full[slot], uint32_t((t / C::kSlots) & 1), p.err);
             ok = __all_sync(0xffffffffu, ok);
             if (ok && lane < nr) {
                 const uint32_t st = smem_u32(smem + size_t(slot) * C::kStage);
                 // the stage's activation codes and block scales: in the stage,
-                // or (fused) at K offset j * 1024 of the produced row
-                const uint32_t xa = FUSE ? sact_a + uint32_t(j * kRplKS) : st + uint32_t(C::kW + C::kS);
-                const uint32_t da = FUSE ? sxd_a + uint32_t((j * (kRplKS / Q8_QK) + qw * 8) * 4)
-                                         : st + uint32_t(C::kW + C::kS + C::kX + qw * 32);
-                const uint32_t lo = FUSE ? uint32_t(K) : uint32_t(4 * R * 256);   // the lo plane
-                // the lane's row's 8 block scales of this quarter: 16-byte chunk
-                // qw of its 64-byte row, 64-byte swizzle
-                const int4 s8 = lds128(st + uint32_t(C::kW + lane * 64 + ((qw ^ ((lane >> 1) & 3)) << 4)));
-                const uint32_t sh[4] = {uint32_t(s8.x), uint32_t(s8.y), uint32_t(s8.z), uint32_t(s8.w)};
+                // or (fused) at K offset j * kKS of the produced row
+                const uint32_t xa = C::kResAct ? sact_a + uint32_t(j * C::kKS) : st + uint32_t(C::kW + C::kS);
+                const uint32_t da = C::kResAct ? sxd_a + uint32_t((j * (C::kKS / Q8_QK) + qw * C::kBPW) * 4)
+                                               : st + uint32_t(C::kW + C::kS + C::kX + qw * C::kBPW * 4);
+                const uint32_t lo = C::kResAct ? uint32_t(K) : uint32_t((C::kKS / 256) * R * 256);   // the lo plane
+                // the lane's row's block scales of this quarter: 16 bytes of a
+                // 64-byte row, 64-byte swizzle (1024-value stages), or 8 bytes of
+                // a 32-byte row, unswizzled (512-value stages)
+                uint32_t sh[C::kBPW / 2];
+                if constexpr (C::kKS == 1024) {
+                    const int4 s8 = lds128(st + uint32_t(C::kW + lane * 64 + ((qw ^ ((lane >> 1) & 3)) << 4)));
+                    sh[0] = uint32_t(s8.x);
+                    sh[1] = uint32_t(s8.y);
+                    sh[2] = uint32_t(s8.z);
+                    sh[3] = uint32_t(s8.w);
+                } else {
+                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                                 : "=r"(sh[0]), "=r"(sh[1])
+                                 : "r"(st + uint32_t(C::kW + lane * (C::kKS / 16) + qw * 8)));
+                }
                 if constexpr (MODE == 0) {
                     // (two blocks in flight at one row; at two rows that spills)
 #pragma unroll(R == 1 ? 2 : 1)
-                    for (int b = 0; b < 8; ++b) {
-                        const int B = qw * 8 + b;
+                    for (int b = 0; b < C::kBPW; ++b) {
+                        const int B = qw * C::kBPW + b;
                         const uint32_t wr = st + uint32_t((B >> 2) * (kRplRows * 128) + lane * 128);
                         const int c0 = (B & 3) * 2;
                         const int4 w0 = lds128(wr + uint32_t(((c0 ^ (lane & 7)) << 4)));
@@ -534,7 +579,7 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                             half_bits_to_float(uint16_t((b & 1) ? (sh[b >> 1] >> 16) : (sh[b >> 1] & 0xFFFFu)));
                         // each row's planes of the block (the same address for
                         // every lane) and its factor to that row's binade
-                        const int blk = j * (kRplKS / Q8_QK) + B;
+                        const int blk = j * (C::kKS / Q8_QK) + B;
 #pragma unroll
                         for (int m = 0; m < R; ++m) {
                             FixChunk32 fx;
@@ -557,20 +602,21 @@ __global__ void __launch_bounds__(RplCfg<MODE, R, FUSE, ARGMAX>::kThreads, 1)
                     }
                 } else {
 #pragma unroll 2
-                for (int b = 0; b < 8; ++b) {
-                    const int B = qw * 8 + b;   // block within the stage
+                for (int b = 0; b < C::kBPW; ++b) {
+                    const int B = qw * C::kBPW + b;   // block within the stage
                     // weight tile B / 4, row lane, 16-byte chunks (B % 4) * 2 and + 1, swizzled
                     const uint32_t wr = st + uint32_t((B >> 2) * (kRplRows * 128) + lane * 128);
                     const int c0 = (B & 3) * 2;
                     const int4 w0 = lds128(wr + uint32_t(((c0 ^ (lane & 7)) << 4)));
                     const int4 w1 = lds128(wr + uint32_t((((c0 + 1) ^ (lane & 7)) << 4)));
                     const float sw = half_bits_to_float(uint16_t((b & 1) ? (sh[b >> 1] >> 16) : (sh[b >> 1] & 0xFFFFu)));
-                    // activation tile B / 8 (rows of 256 bytes), block B % 8; fused: block B
-                    const uint32_t xb = FUSE ? xa + uint32_t(B * 32) : xa + uint32_t((B >> 3) * R * 256 + (B & 7) * 32);
+                    // activation tile B / 8 (rows of 256 bytes), block B % 8; resident row: block B
+                    const uint32_t xb =
+                        C::kResAct ? xa + uint32_t(B * 32) : xa + uint32_t((B >> 3) * R * 256 + (B & 7) * 32);
 #pragma unroll
                     for (int m = 0; m < R; ++m) {
                         const uint32_t xm = xb + uint32_t(m * 256);
-                        const float xd = __uint_as_float(lds32(da + uint32_t(m * (kRplKS / Q8_QK) * 4 + 4 * b)));
+                        const float xd = __uint_as_float(lds32(da + uint32_t(m * (C::kKS / Q8_QK) * 4 + 4 * b)));
                         float fi;
                         if constexpr (MODE == 1) {
                             // one dp4a chain started at the bits of 1.5 * 2^23:
@@ -713,14 +759,14 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
     // weights as (byte in a 128-byte chunk, row, chunk): a box of 8 chunks of
     // 32 rows lands as eight [32][128] tiles
     const uint64_t wd[3] = {128, uint64_t(a.N), uint64_t(a.K / 128)}, ws[2] = {uint64_t(a.K), 128};
-    const uint32_t wb[3] = {128, kRplRows, kRplKS / 128};
+    const uint32_t wb[3] = {128, kRplRows, C::kKS / 128};
     // activation codes as (byte in a 256-byte chunk, row, chunk)
     const uint64_t xdims[3] = {256, uint64_t(a.rows), uint64_t(a.K / 256)}, xs[2] = {uint64_t(a.K), 256};
-    const uint32_t xb[3] = {256, uint32_t(R), kRplKS / 256};
+    const uint32_t xb[3] = {256, uint32_t(R), C::kKS / 256};
     const bool okw =
         make_map3(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q, wd, ws, wb, CU_TENSOR_MAP_SWIZZLE_128B) &&
-        make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.s, a.K / 16, a.N, a.K / 16, kRplKS / 16, kRplRows,
-                 CU_TENSOR_MAP_SWIZZLE_64B);
+        make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.s, a.K / 16, a.N, a.K / 16, C::kKS / 16, kRplRows,
+                 C::kKS == 1024 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE);
     // a resident row: no activation copies (the unused maps repeat the weights')
     if (C::kResAct) txh = txl = txd = tw;
     const bool ok = okw && (C::kResAct ||
@@ -728,7 +774,7 @@ cudaError_t launch_gemv_rpl_t(const GemvArgs& a, const LaunchCtx& ctx) {
         make_map3(&txl, CU_TENSOR_MAP_DATA_TYPE_UINT8, MODE == 2 ? xh + a.plane : xh, xdims, xs, xb,
                   CU_TENSOR_MAP_SWIZZLE_NONE) &&
         make_map(&txd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.xd, a.K / Q8_QK, a.rows, (a.K / Q8_QK) * 4,
-                 kRplKS / Q8_QK, R, CU_TENSOR_MAP_SWIZZLE_NONE)));
+                 C::kKS / Q8_QK, R, CU_TENSOR_MAP_SWIZZLE_NONE)));
     if (!ok) return cudaErrorInvalidValue;
     GemvParams p{};
     p.q = a.q;
