@@ -13,10 +13,11 @@
 // load) and its scale, and keeps R running sums in registers.  No lane-to-lane
 // reduction is left in the stream.
 //
-// A stage covers 32 weight rows x 1024 values of K:
-//   - the weights as eight tiles of 32 rows x 128 bytes, gathered by one 3-D
-//     TMA box (128-byte swizzle, so the 16-byte loads of 8 consecutive lanes
-//     hit distinct bank groups);
+// A stage covers 32 weight rows x 1024 values of K (512 for one-row int8
+// launches, see RplCfg):
+//   - the weights as eight (four) tiles of 32 rows x 128 bytes, gathered by one
+//     3-D TMA box (128-byte swizzle, so the 16-byte loads of 8 consecutive
+//     lanes hit distinct bank groups);
 //   - the rows' block scales, 32 rows x 64 bytes (64-byte swizzle, same
 //     reason);
 //   - the activation rows' codes (four tiles of R rows x 256 bytes a plane, one
@@ -28,9 +29,10 @@
 // loads, kept up with HBM only once the eight weight tiles were one box.
 // Weights and scales are issued before the wait on the previous kernel, with
 // an evict-first L2 hint (read once per launch); activations after it.  A ring
-// of four stages; the 16 consumer warps are four per slot, and warp (slot,
-// quarter) reduces a quarter of each of its slot's stages (8 blocks) for every
-// row of the group.  At the end of a row group the warps' sums go to shared
+// of four stages (eight half stages), the 16 consumer warps in four groups:
+// group g takes stages t with t % 4 == g (from slots g, or g and g + 4, so
+// each slot's phases are waited on by one group in order), and its warp q
+// reduces quarter q of each (8 or 4 blocks) for every row of the group.  At the end of a row group the warps' sums go to shared
 // memory and are added in warp order (fixed: results do not depend on timing):
 // by a combining warp through two buffers (no consumer warp waits for
 // another), or by the consumer warps themselves between two barriers.
